@@ -1,0 +1,424 @@
+/*
+ * spmv_oracle.c -- plain, slow, single-threaded CPU oracle for sparse
+ * matrix-vector multiply-and-accumulate y = A*x + y and for the storage
+ * formats COO, CSR, ELL, hybrid ELL+COO and JDS.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing in the product library calls, links or
+ * includes this file; only the tests, the smoke check and the bench's CPU
+ * baseline do. It shares no code, header, table or helper with the CUDA path.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [P1] PMPP notes, "Sparse Matrices and Basic Formats (COO and CSR)":
+ *        "Background & SpMV", Fig. 14.1, "COO format and SpMV",
+ *        "CSR format and SpMV".
+ *   [P2] PMPP notes, "Regularized Formats (ELL, Hybrid ELL-COO and JDS)":
+ *        "ELL format: padding + transposition", "Hybrid ELL-COO format",
+ *        "JDS format", "Summary: data-dependent performance and OP/B".
+ *   [P3] "[CUDA performance tuning] SpMV storage format selection and
+ *        performance comparison": section 4.1 (matrix feature analysis),
+ *        section 4.3 (automatic format selection).
+ *   [P5] "Sparse matrix multiplication acceleration techniques", section 5.3
+ *        (common problems: input sanity checks).
+ *
+ * Readings where the pages are open (each is also listed in the design notes):
+ *   - SpMV accumulates: y_i <- y_i + sum_k a_k x_col(k)   ([P1] Background).
+ *   - ELL padding slot: value +0.0f ([P2] ELL step 1 says the padding value
+ *     is 0) and column index -1 (the page prints '*' and leaves it open).
+ *   - ELL width K = the longest row; an all-empty matrix has K = 0.
+ *   - JDS: rows sorted by length, longest first, ties kept in original row
+ *     order (the worked example puts r0 before r2); zero-length rows last.
+ *   - HYB: the first min(len, K) entries of a row (in CSR order) stay in the
+ *     ELL part, the rest go to the COO part in row order.
+ *   - Accumulation in the oracle is fp64, summed in CSR order.
+ *
+ * Parity status: every function here is pinned by tests (worked example of
+ * Fig. 14.1 and the ELL/JDS figures, dense brute force, closed forms, round
+ * trips, invariants), except or_select, whose comparison operators are
+ * stripped in the source page: "parity unpinned" for its thresholds (its
+ * outcome on the page's own described cases is still tested).
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <math.h>
+
+/* Status values of the oracle (its own names; tests map them). */
+#define OR_OK 0
+#define OR_BAD_ARG 1
+#define OR_BAD_ROWPTRS 2
+#define OR_COL_RANGE 3
+#define OR_NO_MEMORY 4
+
+/* Input sanity rules of [P5] section 5.3: row_ptr monotone non-decreasing,
+ * every column index below the column count, value length = nnz (here:
+ * rowPtrs[0] = 0 and rowPtrs[numRows] = nnz). Row-pointer errors are
+ * reported before column errors. */
+int or_validate_csr(int64_t R, int64_t C, int64_t Z, const int32_t *rowPtrs,
+                    const int32_t *colIdx) {
+    if (R < 0 || C < 0 || Z < 0) return OR_BAD_ARG;
+    if (rowPtrs[0] != 0) return OR_BAD_ROWPTRS;
+    for (int64_t r = 0; r < R; ++r)
+        if (rowPtrs[r + 1] < rowPtrs[r]) return OR_BAD_ROWPTRS;
+    if ((int64_t)rowPtrs[R] != Z) return OR_BAD_ROWPTRS;
+    for (int64_t k = 0; k < Z; ++k)
+        if (colIdx[k] < 0 || (int64_t)colIdx[k] >= C) return OR_COL_RANGE;
+    return OR_OK;
+}
+
+/* Row-length statistics of [P3] section 4.1 (distribution histogram and
+ * row-length variance): longest row, mean, population variance (two-pass,
+ * fp64) and a log2 histogram with bin 0 = empty rows and bin b >= 1 holding
+ * lengths in [2^(b-1), 2^b). */
+void or_row_stats(int64_t R, const int32_t *rowPtrs, int64_t *maxLen,
+                  double *mean, double *var, int64_t hist33[33]) {
+    int64_t mx = 0;
+    double sum = 0.0;
+    for (int b = 0; b < 33; ++b) hist33[b] = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t len = (int64_t)rowPtrs[r + 1] - rowPtrs[r];
+        if (len > mx) mx = len;
+        sum += (double)len;
+        int b = 0;
+        while (b < 32 && ((int64_t)1 << b) <= len) ++b;
+        hist33[b] += 1;
+    }
+    double m = R > 0 ? sum / (double)R : 0.0;
+    double ss = 0.0;
+    for (int64_t r = 0; r < R; ++r) {
+        double d = (double)((int64_t)rowPtrs[r + 1] - rowPtrs[r]) - m;
+        ss += d * d;
+    }
+    *maxLen = mx;
+    *mean = m;
+    *var = R > 0 ? ss / (double)R : 0.0;
+}
+
+/* SpMV over CSR, [P1] "CSR format and SpMV": for each row, walk
+ * value/colIdx from rowPtrs[row] to rowPtrs[row+1] and add the dot product
+ * to y[row]. fp64 accumulation; also returns the per-row magnitude
+ * sum_k |a_k x_col(k)| + |y0_row| used by the tolerance. */
+void or_spmv_csr(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
+                 const float *value, const float *x, const float *y0,
+                 double *y, double *mag) {
+    for (int64_t r = 0; r < R; ++r) {
+        double s = 0.0, a = 0.0;
+        for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k) {
+            double p = (double)value[k] * (double)x[colIdx[k]];
+            s += p;
+            a += fabs(p);
+        }
+        y[r] = (double)y0[r] + s;
+        if (mag) mag[r] = a + fabs((double)y0[r]);
+    }
+}
+
+/* The same definition for a subset of rows (sampled checks at full size). */
+void or_spmv_csr_rows(int64_t nrows, const int64_t *rows, const int32_t *rowPtrs,
+                      const int32_t *colIdx, const float *value, const float *x,
+                      const float *y0, double *y, double *mag) {
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t r = rows[i];
+        double s = 0.0, a = 0.0;
+        for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k) {
+            double p = (double)value[k] * (double)x[colIdx[k]];
+            s += p;
+            a += fabs(p);
+        }
+        y[i] = (double)y0[r] + s;
+        mag[i] = a + fabs((double)y0[r]);
+    }
+}
+
+/* Dense row-major matrix to CSR, [P1] "CSR format and SpMV": nonzeros grouped
+ * by row, ascending column inside a row, rowPtrs[numRows] = nnz. Returns nnz;
+ * pass NULL outputs to count only. */
+int64_t or_dense_to_csr(int64_t R, int64_t C, const float *A, int32_t *rowPtrs,
+                        int32_t *colIdx, float *value) {
+    int64_t z = 0;
+    if (rowPtrs) rowPtrs[0] = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t c = 0; c < C; ++c) {
+            float a = A[r * C + c];
+            if (a != 0.0f) {
+                if (colIdx) { colIdx[z] = (int32_t)c; value[z] = a; }
+                ++z;
+            }
+        }
+        if (rowPtrs) rowPtrs[r + 1] = (int32_t)z;
+    }
+    return z;
+}
+
+/* CSR -> COO, [P1] "COO format and SpMV": every nonzero keeps its value and
+ * column and gains its row index; order is unchanged (grouped by row). */
+void or_csr_to_coo(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
+                   const float *value, int32_t *rowIdx, int32_t *cooCol,
+                   float *cooVal) {
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k) {
+            rowIdx[k] = (int32_t)r;
+            cooCol[k] = colIdx[k];
+            cooVal[k] = value[k];
+        }
+}
+
+/* COO (grouped by row) -> CSR: count entries per row, prefix them. */
+void or_coo_to_csr(int64_t R, int64_t Z, const int32_t *rowIdx, int32_t *rowPtrs) {
+    for (int64_t r = 0; r <= R; ++r) rowPtrs[r] = 0;
+    for (int64_t k = 0; k < Z; ++k) rowPtrs[rowIdx[k] + 1] += 1;
+    for (int64_t r = 0; r < R; ++r) rowPtrs[r + 1] += rowPtrs[r];
+}
+
+/* CSR -> ELL, [P2] "ELL format": (1) pad every row to the longest row's
+ * length, (2) lay the padded rectangle out column-major, so the t-th slot of
+ * row r sits at i = t*numRows + r. nnzPerRow[r] keeps the true length.
+ * ellCol/ellVal must hold R*K entries, K = longest row. */
+void or_csr_to_ell(int64_t R, int64_t K, const int32_t *rowPtrs,
+                   const int32_t *colIdx, const float *value, int32_t *nnzPerRow,
+                   int32_t *ellCol, float *ellVal) {
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t len = (int64_t)rowPtrs[r + 1] - rowPtrs[r];
+        nnzPerRow[r] = (int32_t)len;
+        for (int64_t t = 0; t < K; ++t) {
+            int64_t i = t * R + r;
+            if (t < len) {
+                ellCol[i] = colIdx[rowPtrs[r] + t];
+                ellVal[i] = value[rowPtrs[r] + t];
+            } else {
+                ellCol[i] = -1;
+                ellVal[i] = 0.0f;
+            }
+        }
+    }
+}
+
+/* ELL -> CSR: row r's entries are its first nnzPerRow[r] slots. */
+void or_ell_to_csr(int64_t R, int64_t K, const int32_t *nnzPerRow,
+                   const int32_t *ellCol, const float *ellVal, int32_t *rowPtrs,
+                   int32_t *colIdx, float *value) {
+    int64_t z = 0;
+    rowPtrs[0] = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t t = 0; t < nnzPerRow[r]; ++t) {
+            colIdx[z] = ellCol[t * R + r];
+            value[z] = ellVal[t * R + r];
+            ++z;
+        }
+        rowPtrs[r + 1] = (int32_t)z;
+    }
+    (void)K;
+}
+
+/* CSR -> hybrid ELL+COO, [P2] "Hybrid ELL-COO format": before the ELL step
+ * the surplus entries of each row beyond width K are moved to a separate COO
+ * part; the rest is an ELL of width K. Returns the number of COO entries;
+ * pass NULL COO outputs to count only. */
+int64_t or_csr_to_hyb(int64_t R, int64_t K, const int32_t *rowPtrs,
+                      const int32_t *colIdx, const float *value,
+                      int32_t *nnzPerRow, int32_t *ellCol, float *ellVal,
+                      int32_t *cooRow, int32_t *cooCol, float *cooVal) {
+    int64_t nc = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t len = (int64_t)rowPtrs[r + 1] - rowPtrs[r];
+        int64_t inEll = len < K ? len : K;
+        if (nnzPerRow) {
+            nnzPerRow[r] = (int32_t)inEll;
+            for (int64_t t = 0; t < K; ++t) {
+                int64_t i = t * R + r;
+                if (t < inEll) {
+                    ellCol[i] = colIdx[rowPtrs[r] + t];
+                    ellVal[i] = value[rowPtrs[r] + t];
+                } else {
+                    ellCol[i] = -1;
+                    ellVal[i] = 0.0f;
+                }
+            }
+        }
+        for (int64_t t = inEll; t < len; ++t) {
+            if (cooRow) {
+                cooRow[nc] = (int32_t)r;
+                cooCol[nc] = colIdx[rowPtrs[r] + t];
+                cooVal[nc] = value[rowPtrs[r] + t];
+            }
+            ++nc;
+        }
+    }
+    return nc;
+}
+
+/* Hybrid -> CSR: row r = its ELL slots followed by its COO entries. */
+void or_hyb_to_csr(int64_t R, int64_t K, const int32_t *nnzPerRow,
+                   const int32_t *ellCol, const float *ellVal, int64_t nc,
+                   const int32_t *cooRow, const int32_t *cooCol,
+                   const float *cooVal, int32_t *rowPtrs, int32_t *colIdx,
+                   float *value) {
+    int64_t z = 0, c = 0;
+    rowPtrs[0] = 0;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t t = 0; t < nnzPerRow[r]; ++t) {
+            colIdx[z] = ellCol[t * R + r];
+            value[z] = ellVal[t * R + r];
+            ++z;
+        }
+        while (c < nc && cooRow[c] == r) {
+            colIdx[z] = cooCol[c];
+            value[z] = cooVal[c];
+            ++z;
+            ++c;
+        }
+        rowPtrs[r + 1] = (int32_t)z;
+    }
+    (void)K;
+}
+
+/* CSR -> JDS, [P2] "JDS format", steps (1)-(4): (1) group by row as in CSR;
+ * (2) sort the rows by their nonzero count, longest first, recording the
+ * original row index of sorted row s in perm[s] (stable: equal lengths keep
+ * original order); (3) store column-major: the t-th nonzero of every sorted
+ * row that has one forms jagged diagonal t, sorted rows in order; (4)
+ * iterPtr[t] = where diagonal t starts, iterPtr[maxLen] = nnz.
+ * perm has R entries, iterPtr maxLen+1, jdsCol/jdsVal nnz. */
+int or_csr_to_jds(int64_t R, int64_t maxLen, const int32_t *rowPtrs,
+                  const int32_t *colIdx, const float *value, int32_t *perm,
+                  int32_t *iterPtr, int32_t *jdsCol, float *jdsVal) {
+    /* Stable counting sort by length, longest first. */
+    int64_t *count = (int64_t *)calloc((size_t)maxLen + 2, sizeof(int64_t));
+    if (!count) return OR_NO_MEMORY;
+    for (int64_t r = 0; r < R; ++r) count[rowPtrs[r + 1] - rowPtrs[r]] += 1;
+    /* first[len] = number of rows strictly longer than len */
+    int64_t *first = (int64_t *)calloc((size_t)maxLen + 2, sizeof(int64_t));
+    if (!first) { free(count); return OR_NO_MEMORY; }
+    int64_t acc = 0;
+    for (int64_t len = maxLen; len >= 0; --len) {
+        first[len] = acc;
+        acc += count[len];
+    }
+    for (int64_t r = 0; r < R; ++r) {
+        int64_t len = rowPtrs[r + 1] - rowPtrs[r];
+        perm[first[len]] = (int32_t)r;
+        first[len] += 1;
+    }
+    /* iterPtr: diagonal t holds one entry per sorted row longer than t. */
+    iterPtr[0] = 0;
+    int64_t longer = R - count[0];
+    for (int64_t t = 0; t < maxLen; ++t) {
+        iterPtr[t + 1] = (int32_t)(iterPtr[t] + longer);
+        longer -= count[t + 1];
+    }
+    for (int64_t s = 0; s < R; ++s) {
+        int64_t r = perm[s];
+        int64_t len = rowPtrs[r + 1] - rowPtrs[r];
+        for (int64_t t = 0; t < len; ++t) {
+            int64_t i = (int64_t)iterPtr[t] + s;
+            jdsCol[i] = colIdx[rowPtrs[r] + t];
+            jdsVal[i] = value[rowPtrs[r] + t];
+        }
+    }
+    free(count);
+    free(first);
+    return OR_OK;
+}
+
+/* JDS -> CSR: sorted row s owns entry iterPtr[t] + s of every diagonal t
+ * that is wider than s; put them back under row perm[s]. */
+void or_jds_to_csr(int64_t R, int64_t maxLen, const int32_t *perm,
+                   const int32_t *iterPtr, const int32_t *jdsCol,
+                   const float *jdsVal, int32_t *rowPtrs, int32_t *colIdx,
+                   float *value) {
+    int32_t *lens = (int32_t *)calloc((size_t)R + 1, sizeof(int32_t));
+    for (int64_t s = 0; s < R; ++s) {
+        int64_t len = 0;
+        while (len < maxLen && iterPtr[len] + s < iterPtr[len + 1]) ++len;
+        lens[perm[s]] = (int32_t)len;
+    }
+    rowPtrs[0] = 0;
+    for (int64_t r = 0; r < R; ++r) rowPtrs[r + 1] = rowPtrs[r] + lens[r];
+    for (int64_t s = 0; s < R; ++s) {
+        int64_t r = perm[s];
+        for (int64_t t = 0; t < lens[r]; ++t) {
+            colIdx[rowPtrs[r] + t] = jdsCol[iterPtr[t] + s];
+            value[rowPtrs[r] + t] = jdsVal[iterPtr[t] + s];
+        }
+    }
+    free(lens);
+}
+
+/* SpMV walking each format's own layout, fp64. */
+
+/* [P1] "COO format and SpMV": one contribution per stored nonzero. */
+void or_spmv_coo(int64_t R, int64_t Z, const int32_t *rowIdx, const int32_t *colIdx,
+                 const float *value, const float *x, const float *y0, double *y) {
+    for (int64_t r = 0; r < R; ++r) y[r] = (double)y0[r];
+    for (int64_t k = 0; k < Z; ++k)
+        y[rowIdx[k]] += (double)value[k] * (double)x[colIdx[k]];
+}
+
+/* [P2] "ELL format": row r reads slot t*numRows + r for t < nnzPerRow[r]. */
+void or_spmv_ell(int64_t R, int64_t K, const int32_t *nnzPerRow,
+                 const int32_t *ellCol, const float *ellVal, const float *x,
+                 const float *y0, double *y) {
+    for (int64_t r = 0; r < R; ++r) {
+        double s = 0.0;
+        for (int64_t t = 0; t < nnzPerRow[r]; ++t) {
+            int64_t i = t * R + r;
+            s += (double)ellVal[i] * (double)x[ellCol[i]];
+        }
+        y[r] = (double)y0[r] + s;
+    }
+    (void)K;
+}
+
+/* [P2] "Hybrid ELL-COO format": ELL part plus COO part, added into y. */
+void or_spmv_hyb(int64_t R, int64_t K, const int32_t *nnzPerRow,
+                 const int32_t *ellCol, const float *ellVal, int64_t nc,
+                 const int32_t *cooRow, const int32_t *cooCol,
+                 const float *cooVal, const float *x, const float *y0, double *y) {
+    or_spmv_ell(R, K, nnzPerRow, ellCol, ellVal, x, y0, y);
+    for (int64_t k = 0; k < nc; ++k)
+        y[cooRow[k]] += (double)cooVal[k] * (double)x[cooCol[k]];
+}
+
+/* [P2] "JDS format": sorted row s walks diagonal t at iterPtr[t] + s while
+ * that diagonal is wider than s; the sum goes back to row perm[s]. */
+void or_spmv_jds(int64_t R, int64_t maxLen, const int32_t *perm,
+                 const int32_t *iterPtr, const int32_t *jdsCol,
+                 const float *jdsVal, const float *x, const float *y0, double *y) {
+    for (int64_t r = 0; r < R; ++r) y[r] = (double)y0[r];
+    for (int64_t s = 0; s < R; ++s) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < maxLen && iterPtr[t] + s < iterPtr[t + 1]; ++t) {
+            int64_t i = (int64_t)iterPtr[t] + s;
+            acc += (double)jdsVal[i] * (double)x[jdsCol[i]];
+        }
+        y[perm[s]] += acc;
+    }
+}
+
+/* Format selection, [P3] section 4.3. The page's comparison operators are
+ * lost in extraction; the reading used here is: longest row <= 2 x mean ->
+ * ELL; else mean < 10 -> COO; else HYB when longest > 5 x mean, otherwise
+ * CSR. (parity unpinned: the thresholds' directions are a reading.)
+ * Format codes: 0 COO, 1 CSR, 2 ELL, 3 HYB. */
+int or_select(int64_t R, int64_t Z, int64_t maxLen) {
+    double mean = R > 0 ? (double)Z / (double)R : 0.0;
+    if ((double)maxLen <= 2.0 * mean) return 2;
+    if (mean < 10.0) return 0;
+    return (double)maxLen > 5.0 * mean ? 3 : 1;
+}
+
+/* Automatic HYB width: the smallest L such that at least 99% of the rows
+ * have length <= L, i.e. 100 * #{len <= L} >= 99 * R ([P3] section 4.1's
+ * example keeps the 99% of rows of length 10-20 whole in an ELL part of
+ * width 20 and sends the few very long rows' surplus to COO). */
+int64_t or_hyb_auto_width(int64_t R, const int32_t *rowPtrs, int64_t maxLen) {
+    if (R == 0) return 0;
+    int64_t *count = (int64_t *)calloc((size_t)maxLen + 1, sizeof(int64_t));
+    for (int64_t r = 0; r < R; ++r) count[rowPtrs[r + 1] - rowPtrs[r]] += 1;
+    int64_t cum = 0, L = 0;
+    for (L = 0; L <= maxLen; ++L) {
+        cum += count[L];
+        if (100 * cum >= 99 * R) break;
+    }
+    free(count);
+    return L;
+}

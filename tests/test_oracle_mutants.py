@@ -1,0 +1,114 @@
+"""The pins are strong enough: plant a plausible mistake in a copy of the
+oracle's C source (a dropped term, a wrong index, a reversed order, a
+transposed layout), build it on the CPU, and check that at least one pin
+test fails against the mutant. The real oracle is never modified."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import build as obuild
+import test_oracle_pins as pins
+
+SRC = open(obuild.SRC).read()
+
+MUTANTS = {
+    "csr_drops_y0": ("y[r] = (double)y0[r] + s;\n        if (mag)", "y[r] = s;\n        if (mag)"),
+    "csr_skips_first_entry": ("for (int64_t r = 0; r < R; ++r) {\n        double s = 0.0, a = 0.0;\n"
+                              "        for (int64_t k = rowPtrs[r]; k",
+                              "for (int64_t r = 0; r < R; ++r) {\n        double s = 0.0, a = 0.0;\n"
+                              "        for (int64_t k = rowPtrs[r] + 1; k"),
+    "csr_wrong_sign": ("            s += p;\n            a += fabs(p);\n        }\n        y[r] = (double)y0[r] + s;\n        if (mag)",
+                       "            s -= p;\n            a += fabs(p);\n        }\n        y[r] = (double)y0[r] + s;\n        if (mag)"),
+    "ell_row_major": ("                   int32_t *ellCol, float *ellVal) {\n"
+                      "    for (int64_t r = 0; r < R; ++r) {\n"
+                      "        int64_t len = (int64_t)rowPtrs[r + 1] - rowPtrs[r];\n"
+                      "        nnzPerRow[r] = (int32_t)len;\n"
+                      "        for (int64_t t = 0; t < K; ++t) {\n"
+                      "            int64_t i = t * R + r;",
+                      "                   int32_t *ellCol, float *ellVal) {\n"
+                      "    for (int64_t r = 0; r < R; ++r) {\n"
+                      "        int64_t len = (int64_t)rowPtrs[r + 1] - rowPtrs[r];\n"
+                      "        nnzPerRow[r] = (int32_t)len;\n"
+                      "        for (int64_t t = 0; t < K; ++t) {\n"
+                      "            int64_t i = r * K + t;"),
+    "ell_pad_col_zero": ("                ellCol[i] = -1;\n                ellVal[i] = 0.0f;\n            }\n        }\n    }\n}",
+                         "                ellCol[i] = 0;\n                ellVal[i] = 0.0f;\n            }\n        }\n    }\n}"),
+    "jds_ascending": ("for (int64_t len = maxLen; len >= 0; --len) {",
+                      "for (int64_t len = 0; len <= maxLen; ++len) {"),
+    "jds_iterptr_off_by_one": ("longer -= count[t + 1];", "longer -= count[t];"),
+    "jds_unstable": ("    for (int64_t r = 0; r < R; ++r) {\n        int64_t len = rowPtrs[r + 1] - rowPtrs[r];\n        perm[first[len]] = (int32_t)r;",
+                     "    for (int64_t r = R - 1; r >= 0; --r) {\n        int64_t len = rowPtrs[r + 1] - rowPtrs[r];\n        perm[first[len]] = (int32_t)r;"),
+    "jds_spmv_no_unpermute": ("y[perm[s]] += acc;", "y[s] += acc;"),
+    "hyb_width_off_by_one": ("int64_t inEll = len < K ? len : K;",
+                             "int64_t inEll = len < K ? len : (K > 0 ? K - 1 : 0);"),
+    "coo_row_shift": ("rowIdx[k] = (int32_t)r;", "rowIdx[k] = (int32_t)(r > 0 ? r - 1 : 0);"),
+    "validate_rejects_empty_rows": ("if (rowPtrs[r + 1] < rowPtrs[r]) return OR_BAD_ROWPTRS;",
+                                    "if (rowPtrs[r + 1] <= rowPtrs[r]) return OR_BAD_ROWPTRS;"),
+    "validate_col_off_by_one": ("(int64_t)colIdx[k] >= C", "(int64_t)colIdx[k] > C"),
+    "stats_sample_variance": ("*var = R > 0 ? ss / (double)R : 0.0;",
+                              "*var = R > 1 ? ss / (double)(R - 1) : 0.0;"),
+    "auto_width_strict": ("if (100 * cum >= 99 * R) break;", "if (100 * cum > 99 * R) break;"),
+}
+
+
+def _pin_calls():
+    calls = [(pins.test_fig14_1_csr, {}), (pins.test_fig14_1_coo, {}),
+             (pins.test_fig14_1_ell, {}), (pins.test_fig14_1_ell_index_formula, {}),
+             (pins.test_fig14_1_jds, {}), (pins.test_fig14_1_spmv_every_format, {}),
+             (pins.test_fig14_1_hyb_width2, {}), (pins.test_hyb_schematic_counts, {}),
+             (pins.test_validate, {}), (pins.test_hyb_auto_width_quantile, {}),
+             (pins.test_select_outcomes_described_by_page, {})]
+    calls += [(pins.test_spmv_matches_dense_brute_force, {"seed": 0, "case": c})
+              for c in range(len(pins.CASES))]
+    calls += [(pins.test_laplace2d_closed_form, {"side": 5})]
+    for i in range(7):
+        calls += [(pins.test_round_trips_bit_exact, {"idx": i}),
+                  (pins.test_layout_invariants, {"idx": i}),
+                  (pins.test_row_stats, {"idx": i}),
+                  (pins.test_format_spmvs_agree, {"idx": i})]
+    return calls
+
+
+def test_validate_accepts_empty_rows(orc):
+    rp = np.array([0, 0, 2, 2, 3], np.int32)
+    ci = np.array([0, 1, 2], np.int32)
+    assert orc.validate(4, 3, rp, ci) == oracle.OK
+
+
+def run_pins_against(lib_path):
+    """Run every pin against the library at ``lib_path``; return the names of
+    the pins that failed."""
+    mut = oracle.Oracle(oracle.load(lib_path))
+    failures = []
+    for fn, kw in _pin_calls() + [(test_validate_accepts_empty_rows, {})]:
+        try:
+            fn(mut, **kw)
+        except (AssertionError, MemoryError, ValueError, IndexError):
+            failures.append(fn.__name__)
+    return failures
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, tmp_path):
+    """A mutant that writes out of bounds may crash: it runs in a child
+    process, and a crash counts as caught."""
+    import subprocess
+    import sys
+    old, new = MUTANTS[name]
+    assert SRC.count(old) == 1, f"mutation site for {name} not unique"
+    src = tmp_path / "mutant.c"
+    src.write_text(SRC.replace(old, new))
+    out = str(tmp_path / "libmutant.so")
+    subprocess.run(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", out, str(src), "-lm"], check=True)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = ("import sys; sys.path[:0] = [%r, %r]\n"
+            "import test_oracle_mutants as m\n"
+            "f = m.run_pins_against(%r)\n"
+            "print('FAILED_PINS', len(f), f)\n"
+            "sys.exit(3 if f else 0)\n") % (here, os.path.dirname(here), out)
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True,
+                         timeout=300)
+    assert res.returncode != 0, f"no pin caught mutant {name}: {res.stdout[-500:]}"
