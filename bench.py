@@ -1,0 +1,459 @@
+#!/usr/bin/env python3
+"""Benchmark of the whole SpMV path on one GB300 (or N replicas).
+
+One step = one pass of every stage of the path over one matrix already
+resident in HBM:
+  create (validation + row statistics + nnz-balanced CSR partition),
+  convert to COO, ELL, HYB (automatic width) and JDS, select,
+  and y <- A x + y once in each of CSR, COO, ELL, HYB and JDS, then destroy.
+The metric counts the compulsory SpMV bytes of the five products:
+  effective GB/s = 5 * (8*nnz + 12*rows + 4*cols) / step time,
+  GFLOP/s        = 5 * 2*nnz / step time.
+Per-call CUDA-event times inside the timed steps give each stage's own
+GB/s; `roofline` reports the call that takes the largest share of the step.
+The e2e figure repeats the step through the same C ABI with the inputs in
+pinned host memory: the host-to-device copy of the CSR arrays, x and y0 and
+the device-to-host read of the five results are inside its timed region.
+
+--impl reference times the CPU oracle (plain single-threaded C, fp64) on the
+same workload and metric, on a bounded row sample per step.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload laplace2d] [--no-e2e] [--no-cpu-baseline]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("SpMV fp32 GFLOP/s & effective HBM GB/s (fraction of ~8 TB/s) per format, 1 GB300")
+FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS")
+DEFAULT_WORKLOAD = "laplace2d"
+WORKLOAD_DESC = {
+    "tiny_uniform": "uniform 4096x4096, 8 nnz/row (32,768 nnz)",
+    "laplace2d": "2D 5-point Laplacian on 2048x2048, Dirichlet (4,194,304 rows, 20,963,328 nnz)",
+    "uniform_random": "uniform random 1M x 1M, 5 nnz/row (5M nnz)",
+    "skewed": "skewed 2M x 2M: rows of 10-20 nnz + 200 rows of 1000-5000 nnz",
+    "stencil27": "3D 27-point stencil on 160^3, Dirichlet (4,096,000 rows, 109,215,352 nnz)",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def compulsory_bytes(R, C, Z):
+    return 8 * Z + 12 * R + 4 * C
+
+
+def call_bytes(name, R, C, Z, K_ell, K_hyb, hyb_tail):
+    """Algorithmic bytes of each library call (what it must read and write)."""
+    spmv = compulsory_bytes(R, C, Z)
+    return {
+        "create": 4 * (R + 1) + 4 * Z,
+        "convert_coo": 4 * (R + 1) + 4 * Z,
+        "convert_ell": 4 * (R + 1) + 8 * Z + 8 * R * K_ell + 4 * R,
+        "convert_hyb": 4 * (R + 1) + 8 * Z + 8 * R * K_hyb + 4 * R + 12 * hyb_tail,
+        "convert_jds": 4 * (R + 1) + 4 * R + 16 * Z,
+        "spmv_CSR": spmv, "spmv_COO": spmv, "spmv_ELL": spmv, "spmv_HYB": spmv,
+        "spmv_JDS": spmv,
+    }[name]
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 100 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, device):
+    import torch
+    import spmv_sparse_storage_gb300 as sp
+
+    inp = synth.make_workload(args.workload, seed=0)
+    R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
+    stream = torch.cuda.current_stream(device)
+    rp = torch.from_numpy(inp.row_ptrs).to(device)
+    ci = torch.from_numpy(inp.col_idx).to(device)
+    va = torch.from_numpy(inp.value).to(device)
+    x = torch.from_numpy(inp.x).to(device)
+    ys = {f: torch.from_numpy(inp.y0).to(device) for f in FORMATS}
+    torch.cuda.synchronize(device)
+
+    names = ["create", "convert_coo", "convert_ell", "convert_hyb", "convert_jds"] + \
+            [f"spmv_{f}" for f in FORMATS]
+    info = {}
+
+    def step(events=None, inputs=None):
+        ev = events
+        i = 0
+
+        def mark():
+            nonlocal i
+            if ev is not None:
+                ev[i].record(stream)
+                i += 1
+
+        if inputs is not None:  # e2e: inputs come from pinned host memory
+            hrp, hci, hva, hx, hy0, outs = inputs
+            rp.copy_(hrp, non_blocking=True)
+            ci.copy_(hci, non_blocking=True)
+            va.copy_(hva, non_blocking=True)
+            x.copy_(hx, non_blocking=True)
+            for f in FORMATS:
+                ys[f].copy_(hy0, non_blocking=True)
+        mark()
+        h = sp.spmv_create_csr(R, C, Z, rp, ci, va, stream)
+        mark()
+        sp.spmv_convert_coo(h, stream)
+        mark()
+        sp.spmv_convert_ell(h, stream)
+        mark()
+        sp.spmv_convert_hyb(h, 0, stream)
+        mark()
+        sp.spmv_convert_jds(h, stream)
+        mark()
+        fmt, width = sp.spmv_select(h)
+        for f in FORMATS:
+            sp.spmv_run(h, f, x, ys[f], stream)
+            mark()
+        if "auto" not in info:
+            a = sp.spmv_export(h, "HYB")
+            info.update(auto=fmt, hyb_width=width, hyb_tail=a["coo_nnz"],
+                        ell_width=sp.spmv_export(h, "ELL")["width"])
+        sp.spmv_destroy(h)
+        if inputs is not None:
+            for f, o in zip(FORMATS, outs):
+                o.copy_(ys[f], non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+           for _ in range(K)]
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = sp.spmv_launch_count()
+    t0.record(stream)
+    for k in range(K):
+        step(evs[k])
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    launches = sp.spmv_launch_count() - launches0
+    barrier(world)
+    clk = clocks.stop() if rank == 0 else None
+    elapsed_ms = t0.elapsed_time(t1)
+    elapsed_ms = allreduce_max(elapsed_ms, world, device)
+
+    per_call = {}
+    for j, nm in enumerate(names):
+        ts = [evs[k][j].elapsed_time(evs[k][j + 1]) for k in range(K)]
+        per_call[nm] = float(np.mean(ts))
+
+    # e2e: the same step with host inputs
+    e2e = None
+    if not args.no_e2e:
+        hrp = torch.from_numpy(inp.row_ptrs).pin_memory()
+        hci = torch.from_numpy(inp.col_idx).pin_memory()
+        hva = torch.from_numpy(inp.value).pin_memory()
+        hx = torch.from_numpy(inp.x).pin_memory()
+        hy0 = torch.from_numpy(inp.y0).pin_memory()
+        outs = [torch.empty(R, dtype=torch.float32).pin_memory() for _ in FORMATS]
+        inputs = (hrp, hci, hva, hx, hy0, outs)
+        for _ in range(max(2, args.warmup // 2)):
+            step(inputs=inputs)
+        torch.cuda.synchronize(device)
+        Ke = max(3, K // 4)
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            step(inputs=inputs)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e_ms = allreduce_max(e0.elapsed_time(e1), world, device)
+        h2d = 4 * (R + 1) + 8 * Z + 4 * C + 4 * R * len(FORMATS)
+        d2h = 4 * R * len(FORMATS)
+        e2e = {"value": round(world * len(FORMATS) * compulsory_bytes(R, C, Z) * Ke
+                              / (e_ms * 1e-3) / 1e9, 2),
+               "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms / Ke, 4), "steps": Ke}
+
+    if rank != 0:
+        return None
+
+    peak, peak_kind = load_peaks()
+    step_ms = elapsed_ms / K
+    spmv_bytes = len(FORMATS) * compulsory_bytes(R, C, Z)
+    value = world * spmv_bytes / (step_ms * 1e-3) / 1e9
+    gflops = world * len(FORMATS) * 2 * Z / (step_ms * 1e-3) / 1e9
+    calls = {}
+    for nm in names:
+        b = call_bytes(nm, R, C, Z, info["ell_width"], info["hyb_width"], info["hyb_tail"])
+        ms = per_call[nm]
+        gbs = b / (ms * 1e-3) / 1e9 if ms > 0 else None
+        calls[nm] = {"ms": round(ms, 5), "alg_bytes": b, "GB/s": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "share": round(ms / step_ms, 4)}
+        if nm.startswith("spmv_"):
+            calls[nm]["GFLOP/s"] = round(2 * Z / (ms * 1e-3) / 1e9, 1)
+    top = max(calls, key=lambda n: calls[n]["ms"])
+    best_spmv = min((n for n in calls if n.startswith("spmv_")), key=lambda n: calls[n]["ms"])
+    roof = {"bound": "hbm", "kernel_call": top, "achieved": calls[top]["GB/s"],
+            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": calls[top]["frac"], "traffic": args.traffic.get(top),
+            "best_spmv": {"call": best_spmv, "GB/s": calls[best_spmv]["GB/s"],
+                          "frac": calls[best_spmv]["frac"],
+                          "GFLOP/s": calls[best_spmv]["GFLOP/s"]}}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded generator, seed 0)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
+                   "num_rows": R, "num_cols": C, "nnz": Z,
+                   "step": "create+validate+stats, convert COO/ELL/HYB/JDS, select, "
+                           "SpMV in CSR/COO/ELL/HYB/JDS",
+                   "auto_format": info["auto"], "hyb_width": info["hyb_width"],
+                   "l2": "no flush: each step moves > 1 GB, far beyond the 129 MB L2",
+                   "parallelism": f"replicas x{world}"},
+        "gflops": round(gflops, 1),
+        "calls": calls,
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    return line
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(v, world, device):
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline object and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step(orc, inp):
+    """The whole path on the CPU oracle: validate, statistics, conversions,
+    selection and the SpMV of every format (fp64 sums)."""
+    rp, ci, va, x, y0 = inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0
+    R = inp.num_rows
+    orc.validate(R, inp.num_cols, rp, ci)
+    st = orc.row_stats(rp)
+    coo = orc.csr_to_coo(rp, ci, va)
+    ell = orc.csr_to_ell(rp, ci, va)
+    K = orc.hyb_auto_width(rp)
+    hyb = orc.csr_to_hyb(rp, ci, va, K)
+    jds = orc.csr_to_jds(rp, ci, va)
+    orc.select(R, inp.nnz, st["max_len"])
+    orc.spmv_csr(rp, ci, va, x, y0)
+    orc.spmv_coo(R, coo["row_idx"], coo["col_idx"], coo["value"], x, y0)
+    orc.spmv_ell(ell, x, y0)
+    orc.spmv_hyb(hyb, x, y0)
+    orc.spmv_jds(jds, x, y0)
+
+
+def row_sample(inp, rows):
+    """The first `rows` rows of the workload (all their entries); x unchanged."""
+    rows = min(rows, inp.num_rows)
+    end = int(inp.row_ptrs[rows])
+    return synth.CSRInput(inp.name + f"[:{rows}]", rows, inp.num_cols,
+                          inp.row_ptrs[:rows + 1].copy(), inp.col_idx[:end].copy(),
+                          inp.value[:end].copy(), inp.x, inp.y0[:rows].copy())
+
+
+def time_oracle(inp, budget_s, max_steps=None):
+    import oracle
+    orc = oracle.get()
+    # calibrate: size the row sample so one step takes about budget_s / 5
+    probe = row_sample(inp, max(1, inp.num_rows // 64))
+    t = time.perf_counter()
+    oracle_step(orc, probe)
+    per_row = (time.perf_counter() - t) / probe.num_rows
+    rows = int(min(inp.num_rows, max(1, (budget_s / 5) / max(per_row, 1e-12))))
+    sample = row_sample(inp, rows)
+    times = []
+    t_end = time.perf_counter() + budget_s
+    while time.perf_counter() < t_end and (max_steps is None or len(times) < max_steps):
+        t = time.perf_counter()
+        oracle_step(orc, sample)
+        times.append(time.perf_counter() - t)
+    step_s = float(np.median(times))
+    b = len(FORMATS) * compulsory_bytes(sample.num_rows, sample.num_rows if
+                                        sample.num_rows < inp.num_cols else inp.num_cols,
+                                        sample.nnz)
+    return {"value": round(b / step_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"rows [0, {sample.num_rows}) of {inp.name} ({sample.nnz} nnz), "
+                      f"whole path per step, median of {len(times)} steps",
+            "ms_per_step": round(step_s * 1e3, 3), "steps": len(times)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    inp = synth.make_workload(args.workload, seed=0)
+    budget = max(5.0, min(120.0, 0.5 * (args.steps + args.warmup)))
+    cb = time_oracle(inp, budget_s=budget, max_steps=args.steps + args.warmup)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
+        "n_gpus": world, "steps": cb["steps"], "warmup": 0, "ms_per_step": cb["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded generator, seed 0)",
+        "config": {"workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
+                   "step": "the same path on the CPU oracle (plain C, fp64, 1 thread)",
+                   "parallelism": "1 CPU core"},
+        "cpu_baseline": {"value": cb["value"], "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": cb["sample"]},
+        "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--traffic-json", default=None,
+                    help="per-call DRAM bytes from an ncu capture (json: call -> bytes)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    args.traffic = {}
+    if args.traffic_json and os.path.exists(args.traffic_json):
+        with open(args.traffic_json) as f:
+            args.traffic = json.load(f)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from spmv_sparse_storage_gb300 import _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    line = run_ours(args, rank, world, device)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            inp = synth.make_workload(args.workload, seed=0)
+            line["cpu_baseline"] = time_oracle(inp, budget_s=args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * spmv.h -- C ABI of the GB300 (sm_103a) sparse matrix-vector library.
+ *
+ * Operation (PMPP notes, "Sparse Matrices and Basic Formats (COO and CSR)",
+ * section "Background & SpMV"): sparse matrix-vector multiplication AND
+ * ACCUMULATION, y <- A*x + y, with A sparse and x, y dense fp32 vectors.
+ *
+ * The matrix enters in CSR form (same page, section "CSR format and SpMV":
+ * rowPtrs[numRows+1] with rowPtrs[0] = 0 and rowPtrs[numRows] = nnz, colIdx
+ * and value grouped by row; columns inside a row need not be sorted). The
+ * library converts it ON THE DEVICE into the pages' other storage formats
+ * and runs a hand-written kernel per format:
+ *   COO  -- "Sparse Matrices and Basic Formats (COO and CSR)", section
+ *           "COO format and SpMV": value/colIdx/rowIdx per nonzero.
+ *   ELL  -- "Regularized Formats (ELL, Hybrid ELL-COO and JDS)", section
+ *           "ELL format: padding + transposition": rows padded to the longest
+ *           row, stored column-major, slot i = t*numRows + row.
+ *   HYB  -- same page, section "Hybrid ELL-COO format": an ELL part of width
+ *           K plus a COO part holding each row's entries beyond K.
+ *   JDS  -- same page, section "JDS format": rows sorted by length (longest
+ *           first, stable), a row permutation, and jagged diagonals starting
+ *           at iterPtr[t].
+ *
+ * Conventions for every function:
+ *   - Every function returns an int status (spmv_status); nothing throws or
+ *     aborts across this ABI. spmv_status_string() names a status.
+ *   - "device pointer" means memory of the CURRENT CUDA device, allocated by
+ *     the caller (cudaMalloc, a torch tensor, ...). Handles are bound to the
+ *     device current at spmv_create_csr and must be used with it current.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream). Work is enqueued on it asynchronously unless stated.
+ *   - Index type is int32 (signed; negatives are rejected), values are fp32.
+ *   - Ownership: the caller owns the CSR arrays, x and y. The handle BORROWS
+ *     the CSR arrays (it reads them again in spmv_run(SPMV_CSR) and the
+ *     COO format reuses colIdx/value), so they must stay alive and unchanged
+ *     until spmv_destroy. The handle OWNS every converted array; they are
+ *     allocated from a library-private stream-ordered pool on the stream of
+ *     the call that creates them and released by spmv_destroy.
+ *   - Thread safety: distinct handles may be used from distinct threads; one
+ *     handle must not be used by two threads at once.
+ */
+#ifndef SPMV_GB300_H
+#define SPMV_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct spmv_handle_s *spmv_handle; /* opaque */
+
+typedef enum {
+  SPMV_COO = 0,
+  SPMV_CSR = 1,
+  SPMV_ELL = 2,
+  SPMV_HYB = 3,
+  SPMV_JDS = 4,
+  SPMV_AUTO = 5 /* spmv_run: the format spmv_select would choose */
+} spmv_format;
+
+typedef enum {
+  SPMV_OK = 0,
+  SPMV_ERR_INVALID_ARG = -1,      /* null/negative/inconsistent argument */
+  SPMV_ERR_BAD_ROWPTRS = -2,      /* rowPtrs[0] != 0, decreasing, or rowPtrs[numRows] != nnz */
+  SPMV_ERR_COL_OUT_OF_RANGE = -3, /* some colIdx < 0 or >= numCols */
+  SPMV_ERR_TOO_LARGE = -4,        /* ELL/HYB slot count beyond int32 or the padding budget */
+  SPMV_ERR_NOT_CONVERTED = -5,    /* spmv_run/export of a format not converted yet */
+  SPMV_ERR_CUDA = -6,             /* a CUDA runtime call failed (see spmv_last_cuda_error) */
+  SPMV_ERR_ALLOC = -7,            /* device allocation failed or exceeded the set limit */
+  SPMV_ERR_TIMEOUT = -8           /* reserved: a bounded device wait gave up */
+} spmv_status;
+
+/* Row-length statistics computed on the device by spmv_create_csr
+ * ("[CUDA performance tuning] SpMV storage format selection and performance
+ * comparison", section 4.1: nonzero distribution histogram and row-length
+ * variance; "Introduction to sparse computing and performance bottleneck
+ * location", section "Building the problem framework": max/mean load ratio). */
+typedef struct {
+  int64_t num_rows, num_cols, nnz;
+  int64_t max_len;          /* longest row */
+  int64_t min_len;          /* shortest row (0 if numRows == 0) */
+  int64_t empty_rows;       /* rows with no entry */
+  int64_t sum_sq_len;       /* sum over rows of len^2 (exact) */
+  double mean_len;          /* nnz / numRows */
+  double var_len;           /* population variance of the row lengths */
+  int64_t hist_log2[33];    /* bin 0: len 0; bin b >= 1: len in [2^(b-1), 2^b) */
+  double imbalance_thread;  /* max_len / mean_len: one row per thread */
+  double imbalance_warp;    /* max over groups of 32 consecutive rows of their nnz,
+                               divided by the mean group nnz: one group per warp */
+  int32_t auto_format;      /* spmv_format chosen by spmv_select */
+  int32_t auto_hyb_width;   /* HYB width used when spmv_convert_hyb gets 0 */
+} spmv_stats;
+
+/* Read-only view of one converted format (device pointers owned by the
+ * handle, valid until spmv_destroy or until the format is converted again).
+ * Unused fields are NULL / 0. */
+typedef struct {
+  int32_t format;           /* spmv_format */
+  int64_t num_rows, num_cols, nnz;
+  int32_t width;            /* ELL and HYB: K (slots per row); JDS: longest row */
+  int64_t ell_slots;        /* ELL/HYB: num_rows * width */
+  int64_t coo_nnz;          /* COO: nnz; HYB: entries of the COO part */
+  const int32_t *row_ptrs;  /* CSR: numRows + 1 (the caller's array) */
+  const int32_t *row_idx;   /* COO: nnz;  HYB: coo_nnz */
+  const int32_t *col_idx;   /* CSR/COO: nnz; ELL/HYB: ell_slots (padding = -1); JDS: nnz */
+  const float *value;       /* as col_idx (padding = +0.0f) */
+  const int32_t *nnz_per_row;  /* ELL/HYB: entries of each row held in the ELL slots */
+  const int32_t *coo_col_idx;  /* HYB: coo_nnz */
+  const float *coo_value;      /* HYB: coo_nnz */
+  const int32_t *perm;      /* JDS: perm[s] = original row of sorted row s (numRows) */
+  const int32_t *iter_ptr;  /* JDS: width + 1 entries, iter_ptr[width] = nnz */
+} spmv_arrays;
+
+/* Create a handle over a CSR matrix that lives on the current device.
+ *   numRows, numCols >= 0; nnz >= 0; d_rowPtrs: numRows+1 ints; d_colIdx and
+ *   d_value: nnz entries (may be NULL when nnz == 0).
+ * Validates the input on the device by the sanity rules of "Sparse matrix
+ * multiplication acceleration techniques", section 5.3 (rowPtrs monotone,
+ * every column below numCols, nnz consistent with rowPtrs[numRows]),
+ * computes the row statistics and the nnz-balanced CSR partition, then
+ * SYNCHRONISES `stream` once to read the result. On any error *out is set to
+ * NULL and nothing stays allocated. Returns SPMV_ERR_BAD_ROWPTRS before
+ * SPMV_ERR_COL_OUT_OF_RANGE when both apply. */
+int spmv_create_csr(spmv_handle *out, int32_t numRows, int32_t numCols, int32_t nnz,
+                    const int32_t *d_rowPtrs, const int32_t *d_colIdx,
+                    const float *d_value, void *stream);
+
+/* CSR -> COO ("COO format and SpMV"): expands rowPtrs into rowIdx[nnz]
+ * (rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]). colIdx and value are
+ * unchanged, so the COO view shares the caller's two arrays. Asynchronous. */
+int spmv_convert_coo(spmv_handle h, void *stream);
+
+/* CSR -> ELL ("ELL format: padding + transposition"): K = longest row;
+ * slot t*numRows + r holds the t-th entry of row r, or value +0.0f and
+ * column -1 when row r has fewer than t+1 entries; nnzPerRow[r] = len(r).
+ * Returns SPMV_ERR_TOO_LARGE (nothing allocated) when numRows*K exceeds
+ * INT32_MAX or the padding budget numRows*K <= 4*nnz + numRows. Async. */
+int spmv_convert_ell(spmv_handle h, void *stream);
+
+/* CSR -> HYB ("Hybrid ELL-COO format"): an ELL part of width K with the first
+ * min(len, K) entries of each row, and a COO part with every row's remaining
+ * entries in row order, then in-row order. ellWidth = 0 picks K as the
+ * smallest L such that 99% of the rows have length <= L; ellWidth > 0 is used
+ * as given (capped at the longest row). Same size limits as ELL. Async
+ * except for one small device-to-host read of the COO part's size. */
+int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void *stream);
+
+/* CSR -> JDS ("JDS format", steps 1-4): perm sorts the rows by length,
+ * longest first, equal lengths in original order; iterPtr[t] is where
+ * jagged diagonal t starts (iterPtr[maxLen] = nnz); entry iterPtr[t] + s is
+ * the t-th entry of sorted row s. Asynchronous. */
+int spmv_convert_jds(spmv_handle h, void *stream);
+
+/* y <- A*x + y with the given format (SPMV_AUTO = spmv_select's choice).
+ * d_x: numCols floats, d_y: numRows floats, both on the handle's device;
+ * x and y must not overlap (SPMV_ERR_INVALID_ARG). The format must have been
+ * converted (SPMV_CSR always is), else SPMV_ERR_NOT_CONVERTED; nothing is
+ * converted implicitly. Asynchronous on `stream`; launches 1 kernel
+ * (CSR, COO, ELL, JDS) or 2 (HYB: ELL part, then the COO part with a
+ * programmatic dependent launch). Floating-point rounding differs from a
+ * sequential sum (tree and atomic reductions); per row the result is within
+ * 1e-5 * (sum_j |a_ij x_j| + |y_i|) of the exact value for rows up to
+ * several thousand entries. */
+int spmv_run(spmv_handle h, spmv_format format, const float *d_x, float *d_y, void *stream);
+
+/* Format choice from the row-length statistics ("[CUDA performance tuning]
+ * SpMV storage format selection and performance comparison", section 4.3;
+ * its comparison operators are lost in the page, the reading is):
+ * longest <= 2*mean -> ELL; else mean < 10 -> COO; else HYB when
+ * longest > 5*mean, otherwise CSR. *ellWidth gets the automatic HYB width.
+ * Host-only; either output pointer may be NULL. */
+int spmv_select(spmv_handle h, spmv_format *format, int32_t *ellWidth);
+
+/* Copy the statistics computed at creation into *out (host). */
+int spmv_get_stats(spmv_handle h, spmv_stats *out);
+
+/* Describe the device arrays of a converted format (SPMV_NOT_CONVERTED if
+ * absent). The pointers are read-only views owned by the handle. */
+int spmv_export(spmv_handle h, spmv_format format, spmv_arrays *out);
+
+/* Release every array the handle owns, in stream order on the stream of the
+ * handle's most recent call, and free the handle. Work on other streams that
+ * uses the handle must be complete. NULL is accepted. */
+int spmv_destroy(spmv_handle h);
+
+/* Static English text for a status code. */
+const char *spmv_status_string(int status);
+
+/* The last cudaError_t the library saw on this thread (0 if none). */
+int spmv_last_cuda_error(void);
+
+/* Number of kernels this process has launched through the library. */
+uint64_t spmv_launch_count(void);
+
+/* Cap (bytes) on device memory the library may hold in total; a request
+ * beyond it fails with SPMV_ERR_ALLOC. A negative value removes the cap. */
+int spmv_set_memory_limit(int64_t bytes);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int spmv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPMV_GB300_H */

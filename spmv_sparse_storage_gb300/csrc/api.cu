@@ -1,0 +1,663 @@
+// api.cu -- the C ABI declared in include/spmv.h: handle life cycle,
+// device-memory pool, validation read-back, format selection, conversion and
+// SpMV dispatch. All arithmetic on the matrix runs in the CUDA kernels of
+// stats.cu, convert.cu and spmv_kernels.cu.
+#include <atomic>
+#include <climits>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+namespace {
+
+using spmv::DevStats;
+
+// ---------------------------------------------------------------------------
+// Process-wide state
+// ---------------------------------------------------------------------------
+std::atomic<unsigned long long> g_launches{0};
+std::atomic<long long> g_memLimit{-1};
+std::atomic<long long> g_memInUse{0};
+thread_local int g_lastCudaError = 0;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_poolMu;
+cudaMemPool_t g_pools[kMaxDevices] = {};
+int g_smCount[kMaxDevices] = {};
+
+int record(cudaError_t e) {
+  if (e != cudaSuccess) {
+    g_lastCudaError = (int)e;
+    return e == cudaErrorMemoryAllocation ? SPMV_ERR_ALLOC : SPMV_ERR_CUDA;
+  }
+  return SPMV_OK;
+}
+
+#define SPMV_TRY(expr)            \
+  do {                            \
+    int st_ = (expr);             \
+    if (st_ != SPMV_OK) return st_; \
+  } while (0)
+
+// A library-private stream-ordered pool per device, kept at full size
+// between uses (release threshold = max), so repeated create/convert/destroy
+// cycles do not return memory to the driver.
+int get_pool(int dev, cudaMemPool_t* out) {
+  if (dev < 0 || dev >= kMaxDevices) return SPMV_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_poolMu);
+  if (!g_pools[dev]) {
+    cudaMemPoolProps props;
+    std::memset(&props, 0, sizeof(props));
+    props.allocType = cudaMemAllocationTypePinned;
+    props.handleTypes = cudaMemHandleTypeNone;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    cudaMemPool_t pool;
+    SPMV_TRY(record(cudaMemPoolCreate(&pool, &props)));
+    unsigned long long threshold = ~0ull;
+    cudaError_t e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+    if (e != cudaSuccess) {
+      cudaMemPoolDestroy(pool);
+      return record(e);
+    }
+    g_pools[dev] = pool;
+  }
+  *out = g_pools[dev];
+  return SPMV_OK;
+}
+
+struct Buf {
+  void* p;
+  size_t bytes;
+};
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  int set(int dev) {
+    SPMV_TRY(record(cudaGetDevice(&prev)));
+    if (prev != dev) {
+      SPMV_TRY(record(cudaSetDevice(dev)));
+      changed = true;
+    }
+    return SPMV_OK;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+// Device memory (or managed memory) on device `dev`; anything else (host,
+// pageable, another device) is rejected before a kernel could touch it.
+int check_device_ptr(const void* p, int dev) {
+  cudaPointerAttributes a;
+  cudaError_t e = cudaPointerGetAttributes(&a, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error state of this query
+    return SPMV_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeManaged) return SPMV_OK;
+  if (a.type == cudaMemoryTypeDevice && a.device == dev) return SPMV_OK;
+  return SPMV_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+namespace spmv {
+void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+int num_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= kMaxDevices) return 152;
+  if (!g_smCount[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+    g_smCount[dev] = n;
+  }
+  return g_smCount[dev];
+}
+}  // namespace spmv
+
+// ---------------------------------------------------------------------------
+// Handle
+// ---------------------------------------------------------------------------
+struct spmv_handle_s {
+  int device = 0;
+  cudaMemPool_t pool = nullptr;
+  cudaStream_t lastStream = nullptr;
+  int R = 0, C = 0, Z = 0;
+  const int* rowPtrs = nullptr;
+  const int* colIdx = nullptr;
+  const float* value = nullptr;
+  spmv_stats stats;
+  std::vector<unsigned> histExact;  // exact row-length counts for len < kExactLenBins
+
+  // CSR: nnz-balanced partition (merge path), computed at creation
+  int nTiles = 0;
+  int* tileRow = nullptr;
+  std::vector<Buf> csrBufs;
+
+  // COO (shares colIdx/value with the caller's CSR arrays)
+  bool hasCoo = false;
+  int* cooRow = nullptr;
+  std::vector<Buf> cooBufs;
+
+  // ELL
+  bool hasEll = false;
+  int ellK = 0;
+  int* ellCol = nullptr;
+  float* ellVal = nullptr;
+  int* ellNnz = nullptr;
+  std::vector<Buf> ellBufs;
+
+  // HYB
+  bool hasHyb = false;
+  int hybK = 0;
+  int hybCooN = 0;
+  int* hybCol = nullptr;
+  float* hybVal = nullptr;
+  int* hybNnz = nullptr;
+  int* hybCooRow = nullptr;
+  int* hybCooCol = nullptr;
+  float* hybCooVal = nullptr;
+  std::vector<Buf> hybBufs;
+
+  // JDS
+  bool hasJds = false;
+  int jdsMaxLen = 0;
+  int jdsTSplit = 0;
+  int jdsWTail = 0;
+  int* jdsPerm = nullptr;
+  int* jdsIterPtr = nullptr;
+  int* jdsCol = nullptr;
+  float* jdsVal = nullptr;
+  std::vector<Buf> jdsBufs;
+
+  int alloc(size_t bytes, cudaStream_t s, void** out, std::vector<Buf>& list) {
+    *out = nullptr;
+    if (bytes == 0) return SPMV_OK;
+    const long long lim = g_memLimit.load();
+    const long long now = g_memInUse.fetch_add((long long)bytes) + (long long)bytes;
+    if (lim >= 0 && now > lim) {
+      g_memInUse.fetch_sub((long long)bytes);
+      return SPMV_ERR_ALLOC;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&p, bytes, pool, s);
+    if (e != cudaSuccess) {
+      g_memInUse.fetch_sub((long long)bytes);
+      return record(e);
+    }
+    list.push_back({p, bytes});
+    *out = p;
+    return SPMV_OK;
+  }
+
+  void release(std::vector<Buf>& list, cudaStream_t s) {
+    for (const Buf& b : list) {
+      cudaFreeAsync(b.p, s);
+      g_memInUse.fetch_sub((long long)b.bytes);
+    }
+    list.clear();
+  }
+
+  // width(t) = number of rows longer than t, exact for t < kExactLenBins
+  long long width_at(int t) const {
+    long long le = 0;
+    for (int L = 0; L <= t && L < spmv::kExactLenBins; ++L) le += histExact[L];
+    return (long long)R - le;
+  }
+};
+
+namespace {
+
+template <class T>
+int alloc_typed(spmv_handle h, long long n, cudaStream_t s, T** out, std::vector<Buf>& list) {
+  void* p = nullptr;
+  int st = h->alloc((size_t)n * sizeof(T), s, &p, list);
+  *out = static_cast<T*>(p);
+  return st;
+}
+
+// Format choice ("[CUDA performance tuning] SpMV storage format selection and
+// performance comparison", section 4.3). The page's comparison operators are
+// lost; the reading: longest <= 2*mean -> ELL, else mean < 10 -> COO, else
+// HYB when longest > 5*mean, otherwise CSR.
+int select_format(long long R, long long Z, long long maxLen) {
+  const double mean = R > 0 ? (double)Z / (double)R : 0.0;
+  if ((double)maxLen <= 2.0 * mean) return SPMV_ELL;
+  if (mean < 10.0) return SPMV_COO;
+  return (double)maxLen > 5.0 * mean ? SPMV_HYB : SPMV_CSR;
+}
+
+// Automatic HYB width: smallest L with 100 * #{len <= L} >= 99 * R (section
+// 4.1 of the same page keeps the 99% of rows of length 10-20 whole in an ELL
+// part of width 20). Beyond the exact histogram the log2 bins give an upper
+// bound, capped at the longest row.
+int auto_hyb_width(const spmv_handle_s* h) {
+  const long long R = h->R;
+  if (R == 0) return 0;
+  long long cum = 0;
+  for (int L = 0; L < spmv::kExactLenBins && L <= h->stats.max_len; ++L) {
+    cum += h->histExact[L];
+    if (100 * cum >= 99 * R) return L;
+  }
+  // remaining rows are at least kExactLenBins long; walk the log2 bins
+  long long cumLog = 0;
+  for (int b = 0; b < 33; ++b) {
+    cumLog += h->stats.hist_log2[b];
+    if (100 * cumLog >= 99 * R) {
+      long long upper = b == 0 ? 0 : (1LL << b) - 1;
+      if (upper > h->stats.max_len) upper = h->stats.max_len;
+      return (int)upper;
+    }
+  }
+  return (int)h->stats.max_len;
+}
+
+// ELL/HYB slot budget: numRows*K within int32 and at most 4*nnz + numRows.
+bool ell_fits(long long R, long long K, long long Z) {
+  const long long slots = R * K;
+  return slots <= (long long)INT_MAX && slots <= 4 * Z + R;
+}
+
+int check_handle(spmv_handle h) { return h ? SPMV_OK : SPMV_ERR_INVALID_ARG; }
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Exported functions
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
+                    const int32_t* d_rowPtrs, const int32_t* d_colIdx, const float* d_value,
+                    void* stream) {
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (numRows < 0 || numCols < 0 || nnz < 0 || !d_rowPtrs) return SPMV_ERR_INVALID_ARG;
+  if (nnz > 0 && (!d_colIdx || !d_value)) return SPMV_ERR_INVALID_ARG;
+  if (nnz > 0 && numCols == 0) return SPMV_ERR_COL_OUT_OF_RANGE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int dev = 0;
+  SPMV_TRY(record(cudaGetDevice(&dev)));
+  SPMV_TRY(check_device_ptr(d_rowPtrs, dev));
+  if (nnz > 0) {
+    SPMV_TRY(check_device_ptr(d_colIdx, dev));
+    SPMV_TRY(check_device_ptr(d_value, dev));
+  }
+  spmv_handle h = new (std::nothrow) spmv_handle_s();
+  if (!h) return SPMV_ERR_ALLOC;
+  h->device = dev;
+  h->R = numRows;
+  h->C = numCols;
+  h->Z = nnz;
+  h->rowPtrs = d_rowPtrs;
+  h->colIdx = d_colIdx;
+  h->value = d_value;
+  h->lastStream = s;
+  int st = get_pool(dev, &h->pool);
+  std::vector<Buf> tmp;
+  DevStats* dst = nullptr;
+  DevStats* hst = nullptr;
+  auto fail = [&](int code) {
+    h->release(tmp, s);
+    h->release(h->csrBufs, s);
+    delete hst;
+    delete h;
+    return code;
+  };
+  if (st != SPMV_OK) return fail(st);
+  st = alloc_typed(h, 1, s, &dst, tmp);
+  if (st != SPMV_OK) return fail(st);
+  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, s));
+  if (st != SPMV_OK) return fail(st);
+  // nnz-balanced partition for the CSR kernel (binary searches stay bounded
+  // even if validation fails below)
+  const long long items = (long long)numRows + nnz;
+  h->nTiles = (int)((items + spmv::kCsrTileItems - 1) / spmv::kCsrTileItems);
+  st = alloc_typed(h, (long long)h->nTiles + 1, s, &h->tileRow, h->csrBufs);
+  if (st != SPMV_OK) return fail(st);
+  st = record(spmv::launch_csr_partition(numRows, nnz, d_rowPtrs, h->nTiles, h->tileRow, s));
+  if (st != SPMV_OK) return fail(st);
+  hst = new (std::nothrow) DevStats;
+  if (!hst) return fail(SPMV_ERR_ALLOC);
+  st = record(cudaMemcpyAsync(hst, dst, sizeof(DevStats), cudaMemcpyDeviceToHost, s));
+  if (st != SPMV_OK) return fail(st);
+  st = record(cudaStreamSynchronize(s));
+  if (st != SPMV_OK) return fail(st);
+  if (hst->err & (spmv::kErrRowPtrStart | spmv::kErrRowPtrDecrease | spmv::kErrRowPtrEnd))
+    return fail(SPMV_ERR_BAD_ROWPTRS);
+  if (hst->err & spmv::kErrColRange) return fail(SPMV_ERR_COL_OUT_OF_RANGE);
+
+  spmv_stats& S = h->stats;
+  std::memset(&S, 0, sizeof(S));
+  S.num_rows = numRows;
+  S.num_cols = numCols;
+  S.nnz = nnz;
+  S.max_len = hst->maxLen;
+  S.min_len = numRows > 0 ? hst->minLen : 0;
+  S.empty_rows = hst->emptyRows;
+  S.sum_sq_len = (int64_t)hst->sumSq;
+  S.mean_len = numRows > 0 ? (double)nnz / (double)numRows : 0.0;
+  if (numRows > 0) {
+    const long double Rl = numRows, Zl = nnz;
+    const long double num = Rl * (long double)hst->sumSq - Zl * Zl;
+    S.var_len = (double)(num / Rl / Rl);
+  }
+  for (int b = 0; b < 33; ++b) S.hist_log2[b] = (int64_t)hst->histLog2[b];
+  S.imbalance_thread = S.mean_len > 0 ? (double)S.max_len / S.mean_len : 0.0;
+  if (numRows > 0 && nnz > 0) {
+    const double groups = (double)((numRows + 31) / 32);
+    S.imbalance_warp = (double)hst->maxWarpNnz / ((double)nnz / groups);
+  }
+  h->histExact.assign(hst->histExact, hst->histExact + spmv::kExactLenBins);
+  S.auto_format = select_format(numRows, nnz, S.max_len);
+  S.auto_hyb_width = auto_hyb_width(h);
+  h->release(tmp, s);
+  delete hst;
+  *out = h;
+  return SPMV_OK;
+}
+
+int spmv_convert_coo(spmv_handle h, void* stream) {
+  SPMV_TRY(check_handle(h));
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  h->release(h->cooBufs, s);
+  h->hasCoo = false;
+  SPMV_TRY(alloc_typed(h, h->Z, s, &h->cooRow, h->cooBufs));
+  SPMV_TRY(record(spmv::launch_expand_rows(h->R, h->rowPtrs, h->cooRow, s)));
+  h->hasCoo = true;
+  return SPMV_OK;
+}
+
+int spmv_convert_ell(spmv_handle h, void* stream) {
+  SPMV_TRY(check_handle(h));
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  const long long K = h->stats.max_len;
+  if (!ell_fits(h->R, K, h->Z)) return SPMV_ERR_TOO_LARGE;
+  h->release(h->ellBufs, s);
+  h->hasEll = false;
+  const long long slots = (long long)h->R * K;
+  SPMV_TRY(alloc_typed(h, slots, s, &h->ellCol, h->ellBufs));
+  SPMV_TRY(alloc_typed(h, slots, s, &h->ellVal, h->ellBufs));
+  SPMV_TRY(alloc_typed(h, h->R, s, &h->ellNnz, h->ellBufs));
+  SPMV_TRY(record(spmv::launch_csr_to_ell(h->R, (int)K, h->rowPtrs, h->colIdx, h->value,
+                                          h->ellCol, h->ellVal, h->ellNnz, s)));
+  h->ellK = (int)K;
+  h->hasEll = true;
+  return SPMV_OK;
+}
+
+int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (ellWidth < 0) return SPMV_ERR_INVALID_ARG;
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  long long K = ellWidth > 0 ? ellWidth : h->stats.auto_hyb_width;
+  if (K > h->stats.max_len) K = h->stats.max_len;
+  if (!ell_fits(h->R, K, h->Z)) return SPMV_ERR_TOO_LARGE;
+  h->release(h->hybBufs, s);
+  h->hasHyb = false;
+  const long long R = h->R;
+  const long long slots = R * K;
+  SPMV_TRY(alloc_typed(h, slots, s, &h->hybCol, h->hybBufs));
+  SPMV_TRY(alloc_typed(h, slots, s, &h->hybVal, h->hybBufs));
+  SPMV_TRY(alloc_typed(h, R, s, &h->hybNnz, h->hybBufs));
+  SPMV_TRY(record(spmv::launch_csr_to_ell(h->R, (int)K, h->rowPtrs, h->colIdx, h->value,
+                                          h->hybCol, h->hybVal, h->hybNnz, s)));
+  // COO part size: nnz - sum_r min(len_r, K), exact from the histogram when
+  // K is below the exact range (longer rows then all keep K entries).
+  long long tail = -1;
+  if (K < spmv::kExactLenBins) {
+    long long kept = 0, counted = 0;
+    for (int L = 0; L < spmv::kExactLenBins; ++L) {
+      kept += (long long)h->histExact[L] * (L < K ? L : K);
+      counted += h->histExact[L];
+    }
+    kept += (R - counted) * K;
+    tail = (long long)h->Z - kept;
+  }
+  std::vector<Buf> tmp;
+  int* tailPtr = nullptr;
+  int* scratch = nullptr;
+  auto done = [&](int code) {
+    h->release(tmp, s);
+    return code;
+  };
+  int st = alloc_typed(h, R + 1, s, &tailPtr, tmp);
+  if (st == SPMV_OK) st = alloc_typed(h, (long long)spmv::scan_scratch_ints(R), s, &scratch, tmp);
+  if (st == SPMV_OK) st = record(spmv::launch_tail_scan(h->R, (int)K, h->rowPtrs, tailPtr, scratch, s));
+  if (st != SPMV_OK) return done(st);
+  if (tail < 0) {
+    int t = 0;
+    st = record(cudaMemcpyAsync(&t, tailPtr + R, sizeof(int), cudaMemcpyDeviceToHost, s));
+    if (st == SPMV_OK) st = record(cudaStreamSynchronize(s));
+    if (st != SPMV_OK) return done(st);
+    tail = t;
+  }
+  st = alloc_typed(h, tail, s, &h->hybCooRow, h->hybBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, tail, s, &h->hybCooCol, h->hybBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, tail, s, &h->hybCooVal, h->hybBufs);
+  if (st == SPMV_OK && tail > 0)
+    st = record(spmv::launch_hyb_tail_copy(h->R, (int)K, h->rowPtrs, h->colIdx, h->value, tailPtr,
+                                           h->hybCooRow, h->hybCooCol, h->hybCooVal, s));
+  if (st != SPMV_OK) return done(st);
+  h->hybK = (int)K;
+  h->hybCooN = (int)tail;
+  h->hasHyb = true;
+  return done(SPMV_OK);
+}
+
+int spmv_convert_jds(spmv_handle h, void* stream) {
+  SPMV_TRY(check_handle(h));
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  h->release(h->jdsBufs, s);
+  h->hasJds = false;
+  const int L = (int)h->stats.max_len;
+  SPMV_TRY(alloc_typed(h, h->R, s, &h->jdsPerm, h->jdsBufs));
+  SPMV_TRY(alloc_typed(h, (long long)L + 1, s, &h->jdsIterPtr, h->jdsBufs));
+  SPMV_TRY(alloc_typed(h, h->Z, s, &h->jdsCol, h->jdsBufs));
+  SPMV_TRY(alloc_typed(h, h->Z, s, &h->jdsVal, h->jdsBufs));
+  std::vector<Buf> tmp;
+  void* scratch = nullptr;
+  int st = h->alloc(spmv::jds_sort_scratch_bytes(h->R, L), s, &scratch, tmp);
+  if (st == SPMV_OK)
+    st = record(spmv::launch_jds_build(h->R, L, h->rowPtrs, h->colIdx, h->value, h->jdsPerm,
+                                       h->jdsIterPtr, h->jdsCol, h->jdsVal, scratch, s));
+  h->release(tmp, s);
+  if (st != SPMV_OK) return st;
+  // Row-parallel part: the leading diagonals at least min(kJdsSplitMinWidth,
+  // width(0)) wide, at most kJdsSplitMaxDiag of them (widths are exact from
+  // the histogram there).
+  const long long w0 = h->width_at(0);
+  const long long thr = w0 < spmv::kJdsSplitMinWidth ? w0 : spmv::kJdsSplitMinWidth;
+  int tSplit = 0;
+  const int cap = L < spmv::kJdsSplitMaxDiag ? L : spmv::kJdsSplitMaxDiag;
+  while (tSplit < cap && thr > 0 && h->width_at(tSplit) >= thr) ++tSplit;
+  h->jdsTSplit = tSplit;
+  h->jdsWTail = tSplit < L ? (int)h->width_at(tSplit) : 0;
+  h->jdsMaxLen = L;
+  h->hasJds = true;
+  return SPMV_OK;
+}
+
+int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
+  SPMV_TRY(check_handle(h));
+  if (format) *format = (spmv_format)h->stats.auto_format;
+  if (ellWidth) *ellWidth = h->stats.auto_hyb_width;
+  return SPMV_OK;
+}
+
+int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
+  if (format < SPMV_COO || format > SPMV_JDS) return SPMV_ERR_INVALID_ARG;
+  if (h->R > 0 && !d_y) return SPMV_ERR_INVALID_ARG;
+  if (h->C > 0 && !d_x) return SPMV_ERR_INVALID_ARG;
+  if (h->R > 0 && h->C > 0) {
+    const char* xb = reinterpret_cast<const char*>(d_x);
+    const char* yb = reinterpret_cast<const char*>(d_y);
+    if (xb < yb + (size_t)h->R * 4 && yb < xb + (size_t)h->C * 4) return SPMV_ERR_INVALID_ARG;
+  }
+  switch (format) {
+    case SPMV_COO: if (!h->hasCoo) return SPMV_ERR_NOT_CONVERTED; break;
+    case SPMV_ELL: if (!h->hasEll) return SPMV_ERR_NOT_CONVERTED; break;
+    case SPMV_HYB: if (!h->hasHyb) return SPMV_ERR_NOT_CONVERTED; break;
+    case SPMV_JDS: if (!h->hasJds) return SPMV_ERR_NOT_CONVERTED; break;
+    default: break;
+  }
+  if (h->R == 0) return SPMV_OK;
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  SPMV_TRY(check_device_ptr(d_y, h->device));
+  if (h->C > 0) SPMV_TRY(check_device_ptr(d_x, h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  switch (format) {
+    case SPMV_CSR:
+      return record(spmv::launch_spmv_csr(h->R, h->Z, h->rowPtrs, h->colIdx, h->value,
+                                          h->tileRow, h->nTiles, d_x, d_y, s));
+    case SPMV_COO:
+      return record(spmv::launch_spmv_coo(h->Z, h->cooRow, h->colIdx, h->value, d_x, d_y,
+                                          false, s));
+    case SPMV_ELL:
+      return record(spmv::launch_spmv_ell(h->R, h->ellK, h->ellCol, h->ellVal, d_x, d_y, s));
+    case SPMV_HYB: {
+      bool ellRan = false;
+      if (h->hybK > 0) {
+        SPMV_TRY(record(spmv::launch_spmv_ell(h->R, h->hybK, h->hybCol, h->hybVal, d_x, d_y, s)));
+        ellRan = true;
+      }
+      if (h->hybCooN > 0)
+        SPMV_TRY(record(spmv::launch_spmv_coo(h->hybCooN, h->hybCooRow, h->hybCooCol,
+                                              h->hybCooVal, d_x, d_y, ellRan, s)));
+      return SPMV_OK;
+    }
+    case SPMV_JDS:
+      return record(spmv::launch_spmv_jds(h->R, h->jdsMaxLen, h->jdsTSplit, h->jdsWTail,
+                                          h->jdsIterPtr, h->jdsPerm, h->jdsCol, h->jdsVal, d_x,
+                                          d_y, s));
+    default:
+      return SPMV_ERR_INVALID_ARG;
+  }
+}
+
+int spmv_get_stats(spmv_handle h, spmv_stats* out) {
+  SPMV_TRY(check_handle(h));
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  *out = h->stats;
+  return SPMV_OK;
+}
+
+int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
+  SPMV_TRY(check_handle(h));
+  if (!out) return SPMV_ERR_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->format = format;
+  out->num_rows = h->R;
+  out->num_cols = h->C;
+  out->nnz = h->Z;
+  switch (format) {
+    case SPMV_CSR:
+      out->row_ptrs = h->rowPtrs;
+      out->col_idx = h->colIdx;
+      out->value = h->value;
+      return SPMV_OK;
+    case SPMV_COO:
+      if (!h->hasCoo) return SPMV_ERR_NOT_CONVERTED;
+      out->row_idx = h->cooRow;
+      out->col_idx = h->colIdx;
+      out->value = h->value;
+      out->coo_nnz = h->Z;
+      return SPMV_OK;
+    case SPMV_ELL:
+      if (!h->hasEll) return SPMV_ERR_NOT_CONVERTED;
+      out->width = h->ellK;
+      out->ell_slots = (int64_t)h->R * h->ellK;
+      out->col_idx = h->ellCol;
+      out->value = h->ellVal;
+      out->nnz_per_row = h->ellNnz;
+      return SPMV_OK;
+    case SPMV_HYB:
+      if (!h->hasHyb) return SPMV_ERR_NOT_CONVERTED;
+      out->width = h->hybK;
+      out->ell_slots = (int64_t)h->R * h->hybK;
+      out->col_idx = h->hybCol;
+      out->value = h->hybVal;
+      out->nnz_per_row = h->hybNnz;
+      out->coo_nnz = h->hybCooN;
+      out->row_idx = h->hybCooRow;
+      out->coo_col_idx = h->hybCooCol;
+      out->coo_value = h->hybCooVal;
+      return SPMV_OK;
+    case SPMV_JDS:
+      if (!h->hasJds) return SPMV_ERR_NOT_CONVERTED;
+      out->width = h->jdsMaxLen;
+      out->col_idx = h->jdsCol;
+      out->value = h->jdsVal;
+      out->perm = h->jdsPerm;
+      out->iter_ptr = h->jdsIterPtr;
+      return SPMV_OK;
+    default:
+      return SPMV_ERR_INVALID_ARG;
+  }
+}
+
+int spmv_destroy(spmv_handle h) {
+  if (!h) return SPMV_OK;
+  DeviceGuard g;
+  int st = g.set(h->device);
+  cudaStream_t s = h->lastStream;
+  h->release(h->csrBufs, s);
+  h->release(h->cooBufs, s);
+  h->release(h->ellBufs, s);
+  h->release(h->hybBufs, s);
+  h->release(h->jdsBufs, s);
+  delete h;
+  return st;
+}
+
+const char* spmv_status_string(int status) {
+  switch (status) {
+    case SPMV_OK: return "ok";
+    case SPMV_ERR_INVALID_ARG: return "invalid argument";
+    case SPMV_ERR_BAD_ROWPTRS: return "rowPtrs must start at 0, never decrease and end at nnz";
+    case SPMV_ERR_COL_OUT_OF_RANGE: return "a column index is negative or not below numCols";
+    case SPMV_ERR_TOO_LARGE: return "ELL slot count exceeds int32 or the padding budget";
+    case SPMV_ERR_NOT_CONVERTED: return "format not converted";
+    case SPMV_ERR_CUDA: return "CUDA runtime error";
+    case SPMV_ERR_ALLOC: return "device allocation failed or exceeded the memory limit";
+    case SPMV_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int spmv_last_cuda_error(void) { return g_lastCudaError; }
+
+uint64_t spmv_launch_count(void) { return g_launches.load(); }
+
+int spmv_set_memory_limit(int64_t bytes) {
+  g_memLimit.store(bytes < 0 ? -1 : bytes);
+  return SPMV_OK;
+}
+
+int spmv_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+}  // extern "C"

@@ -1,0 +1,503 @@
+// convert.cu -- on-device conversion of a CSR matrix into the other storage
+// formats, plus the device scans and the stable row sort they use.
+//
+// Formats (PMPP notes):
+//   COO -- "Sparse Matrices and Basic Formats (COO and CSR)", section "COO
+//          format and SpMV": every nonzero carries its row index.
+//   ELL -- "Regularized Formats (ELL, Hybrid ELL-COO and JDS)", section "ELL
+//          format: padding + transposition": rows padded to a common width,
+//          stored column-major (slot t*numRows + row).
+//   HYB -- same page, section "Hybrid ELL-COO format": surplus entries of
+//          long rows move to a COO part in row order.
+//   JDS -- same page, section "JDS format": rows sorted by length (longest
+//          first), a row permutation, jagged diagonals starting at iterPtr[t].
+#include <climits>
+
+#include "device_util.cuh"
+#include "internal.h"
+
+namespace spmv {
+namespace {
+
+// ---------------------------------------------------------------------------
+// Warp-cooperative segmented expansion. A warp owns 32 consecutive segments
+// (rows) whose outputs are contiguous: segment j covers output positions
+// [start_j, start_{j+1}). The warp walks its output range 32 positions at a
+// time (coalesced writes); each lane finds its segment by a 5-step binary
+// search over the 32 starts held one per lane.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int find_segment(int start, int k) {
+  // largest lane j with start_j <= k (starts non-decreasing over lanes)
+  int j = 0;
+#pragma unroll
+  for (int step = 16; step >= 1; step >>= 1) {
+    const int sc = __shfl_sync(kFullMask, start, j + step);
+    if (sc <= k) j += step;
+  }
+  return j;
+}
+
+// CSR -> COO: rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1].
+__global__ void __launch_bounds__(256) k_expand_rows(int R, const int* __restrict__ rowPtrs,
+                                                     int* __restrict__ rowIdx) {
+  const int lane = threadIdx.x & 31;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long r0 = warp * 32;
+  if (r0 >= R) return;
+  const long long r = r0 + lane;
+  const int start = r < R ? rowPtrs[r] : INT_MAX;
+  const int A = __shfl_sync(kFullMask, start, 0);
+  const int B = rowPtrs[min(r0 + 32, (long long)R)];
+  for (int base = A; base < B; base += 32) {
+    const int k = base + lane;
+    const int j = find_segment(start, k);
+    if (k < B) rowIdx[k] = (int)(r0 + j);
+  }
+}
+
+// CSR -> ELL of width K (also the ELL part of HYB): thread per row, writes
+// coalesced across rows. Padding slots get column -1 and value +0.0f.
+__global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __restrict__ rowPtrs,
+                                                    const int* __restrict__ colIdx,
+                                                    const float* __restrict__ value,
+                                                    int* __restrict__ ellCol,
+                                                    float* __restrict__ ellVal,
+                                                    int* __restrict__ nnzPerRow) {
+  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  const int a = rowPtrs[r];
+  const int len = rowPtrs[r + 1] - a;
+  const int kept = len < K ? len : K;
+  nnzPerRow[r] = kept;
+  for (int t = 0; t < K; ++t) {
+    const size_t i = (size_t)t * (size_t)R + (size_t)r;
+    int c = -1;
+    float v = 0.0f;
+    if (t < kept) {
+      c = colIdx[a + t];
+      v = value[a + t];
+    }
+    __stcs(ellCol + i, c);
+    __stcs(ellVal + i, v);
+  }
+}
+
+// HYB COO part: row r's entries at in-row positions >= K, written at
+// tailPtr[r] ... in row order (warp-cooperative expansion as above).
+__global__ void __launch_bounds__(256) k_hyb_tail_copy(int R, int K, const int* __restrict__ rowPtrs,
+                                                       const int* __restrict__ colIdx,
+                                                       const float* __restrict__ value,
+                                                       const int* __restrict__ tailPtr,
+                                                       int* __restrict__ cooRow,
+                                                       int* __restrict__ cooCol,
+                                                       float* __restrict__ cooVal) {
+  const int lane = threadIdx.x & 31;
+  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long r0 = warp * 32;
+  if (r0 >= R) return;
+  const long long r = r0 + lane;
+  const int start = r < R ? tailPtr[r] : INT_MAX;
+  const int src = r < R ? rowPtrs[r] + K : 0;
+  const int A = __shfl_sync(kFullMask, start, 0);
+  const int B = tailPtr[min(r0 + 32, (long long)R)];
+  for (int base = A; base < B; base += 32) {
+    const int o = base + lane;
+    const int j = find_segment(start, o);
+    const int sj = __shfl_sync(kFullMask, start, j);
+    const int srcj = __shfl_sync(kFullMask, src, j);
+    if (o < B) {
+      const int k = srcj + (o - sj);
+      cooRow[o] = (int)(r0 + j);
+      cooCol[o] = colIdx[k];
+      cooVal[o] = value[k];
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Exclusive scan (reduce, scan of block sums, apply), no inter-block waits.
+// Input is produced by a functor so that lengths need not be materialised.
+// ---------------------------------------------------------------------------
+constexpr int kScanThreads = 256;
+constexpr int kScanItems = 8;
+constexpr int kScanTile = kScanThreads * kScanItems;
+
+struct ArrayIn {
+  const int* p;
+  __device__ int operator()(long long i) const { return p[i]; }
+};
+
+struct TailLenIn {  // max(0, len(r) - K)
+  const int* rowPtrs;
+  int K;
+  __device__ int operator()(long long i) const {
+    const int len = rowPtrs[i + 1] - rowPtrs[i];
+    return len > K ? len - K : 0;
+  }
+};
+
+__device__ __forceinline__ int block_exclusive_scan(int v, int* total, int* sWarp) {
+  // exclusive scan of one value per thread across a 256-thread block
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(kFullMask, inc, off);
+    if (lane >= off) inc += o;
+  }
+  if (lane == 31) sWarp[w] = inc;
+  __syncthreads();
+  if (w == 0) {
+    int s = lane < kScanThreads / 32 ? sWarp[lane] : 0;
+    int si = s;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFullMask, si, off);
+      if (lane >= off) si += o;
+    }
+    if (lane < kScanThreads / 32) sWarp[lane] = si - s;
+    if (lane == kScanThreads / 32 - 1) sWarp[kScanThreads / 32] = si;
+  }
+  __syncthreads();
+  const int res = inc - v + sWarp[w];
+  *total = sWarp[kScanThreads / 32];
+  __syncthreads();
+  return res;
+}
+
+template <class In>
+__global__ void __launch_bounds__(kScanThreads) k_scan_reduce(In in, long long n, int* blockSums) {
+  __shared__ int sWarp[kScanThreads / 32 + 1];
+  const long long base = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kScanItems;
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i)
+    if (base + i < n) s += in(base + i);
+  int total;
+  block_exclusive_scan(s, &total, sWarp);
+  if (threadIdx.x == 0) blockSums[blockIdx.x] = total;
+}
+
+// Single block: exclusive scan of nb block sums in chunks with a carry.
+__global__ void __launch_bounds__(kScanThreads) k_scan_block_sums(int* sums, long long nb) {
+  __shared__ int sWarp[kScanThreads / 32 + 1];
+  int carry = 0;
+  for (long long c = 0; c < nb; c += kScanTile) {
+    const long long base = c + (long long)threadIdx.x * kScanItems;
+    int v[kScanItems];
+    int s = 0;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      v[i] = base + i < nb ? sums[base + i] : 0;
+      s += v[i];
+    }
+    int total;
+    int ex = block_exclusive_scan(s, &total, sWarp) + carry;
+#pragma unroll
+    for (int i = 0; i < kScanItems; ++i) {
+      if (base + i < nb) sums[base + i] = ex;
+      ex += v[i];
+    }
+    carry += total;
+  }
+}
+
+template <class In>
+__global__ void __launch_bounds__(kScanThreads) k_scan_apply(In in, long long n, const int* blockOffs,
+                                                             int* out) {
+  __shared__ int sWarp[kScanThreads / 32 + 1];
+  const long long base = (long long)blockIdx.x * kScanTile + (long long)threadIdx.x * kScanItems;
+  int v[kScanItems];
+  int s = 0;
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    v[i] = base + i < n ? in(base + i) : 0;
+    s += v[i];
+  }
+  int total;
+  int ex = block_exclusive_scan(s, &total, sWarp) + blockOffs[blockIdx.x];
+#pragma unroll
+  for (int i = 0; i < kScanItems; ++i) {
+    if (base + i < n) out[base + i] = ex;
+    ex += v[i];
+  }
+  if (blockIdx.x == gridDim.x - 1 && threadIdx.x == kScanThreads - 1) out[n] = ex;
+}
+
+// out[0..n] = exclusive scan of in(0..n-1), out[n] = total. scratch holds
+// scan_scratch_ints(n) ints.
+template <class In>
+cudaError_t exclusive_scan(In in, long long n, int* out, int* scratch, cudaStream_t s) {
+  const long long nb = n > 0 ? (n + kScanTile - 1) / kScanTile : 1;
+  k_scan_reduce<In><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, scratch);
+  k_scan_block_sums<<<1, kScanThreads, 0, s>>>(scratch, nb);
+  k_scan_apply<In><<<(unsigned)nb, kScanThreads, 0, s>>>(in, n, scratch, out);
+  note_launches(3);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// JDS: stable least-significant-digit radix sort of the rows on the key
+// maxLen - len (ascending key = longest row first; equal lengths keep their
+// original order because every pass is stable).
+// ---------------------------------------------------------------------------
+constexpr int kSortThreads = 256;
+constexpr int kSortRounds = 8;
+constexpr int kSortTile = kSortThreads * kSortRounds;  // rows per tile
+constexpr int kRadixBits = 8;
+constexpr int kRadix = 1 << kRadixBits;
+
+struct SortIn {
+  // pass 0 reads keys from rowPtrs (items are the rows themselves)
+  const int* rowPtrs;
+  int maxLen;
+  const int* keysIn;  // later passes
+  const int* valsIn;
+  __device__ void get(long long i, int& key, int& val) const {
+    if (keysIn) {
+      key = keysIn[i];
+      val = valsIn[i];
+    } else {
+      key = maxLen - (rowPtrs[i + 1] - rowPtrs[i]);
+      val = (int)i;
+    }
+  }
+};
+
+// Per tile, count keys per digit; hist is digit-major: hist[d * nTiles + tile].
+__global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, int shift, int nTiles,
+                                                             int* __restrict__ hist) {
+  __shared__ int sCount[kRadix];
+  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) sCount[d] = 0;
+  __syncthreads();
+  const long long base = (long long)blockIdx.x * kSortTile;
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    if (i < R) {
+      int key, val;
+      in.get(i, key, val);
+      atomicAdd(&sCount[(key >> shift) & (kRadix - 1)], 1);
+    }
+  }
+  __syncthreads();
+  for (int d = threadIdx.x; d < kRadix; d += kSortThreads)
+    hist[(long long)d * nTiles + blockIdx.x] = sCount[d];
+}
+
+// Stable scatter: rank of each item among equal digits = tile offset (from the
+// scanned histogram) + items of earlier rounds + earlier warps of this round +
+// earlier lanes of this warp (found with a warp match).
+__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R, int shift, int nTiles,
+                                                                const int* __restrict__ offs,
+                                                                int* __restrict__ keysOut,
+                                                                int* __restrict__ valsOut) {
+  constexpr int kWarps = kSortThreads / 32;
+  __shared__ int sRun[kRadix];             // running count per digit in this tile
+  __shared__ int sWarpCnt[kWarps][kRadix];  // per-warp counts of the current round
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
+    sRun[d] = offs[(long long)d * nTiles + blockIdx.x];
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) sWarpCnt[q][d] = 0;
+  }
+  __syncthreads();
+  const long long base = (long long)blockIdx.x * kSortTile;
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    const bool valid = i < R;
+    int key = 0, val = 0, digit = kRadix;  // invalid items get a digit no one shares
+    if (valid) {
+      in.get(i, key, val);
+      digit = (key >> shift) & (kRadix - 1);
+    }
+    const unsigned peers = __match_any_sync(kFullMask, digit);
+    const int rankInWarp = __popc(peers & lanemask_lt());
+    const int leader = __ffs(peers) - 1;
+    if (valid && lane == leader) sWarpCnt[w][digit] = __popc(peers);
+    __syncthreads();
+    if (valid) {
+      int before = sRun[digit];
+      for (int q = 0; q < w; ++q) before += sWarpCnt[q][digit];
+      const int pos = before + rankInWarp;
+      keysOut[pos] = key;
+      valsOut[pos] = val;
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
+      int add = 0;
+#pragma unroll
+      for (int q = 0; q < kWarps; ++q) {
+        add += sWarpCnt[q][d];
+        sWarpCnt[q][d] = 0;
+      }
+      sRun[d] += add;
+    }
+    __syncthreads();
+  }
+}
+
+// Diagonal widths from the sorted lengths: width(t) = #{s : len(s) > t}. With
+// lengths non-increasing over s, width(t) = s+1 for t in [len(s+1), len(s)).
+__global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKeys,
+                             int* __restrict__ width) {
+  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= R) return;
+  const int len = maxLen - sortedKeys[s];
+  const int next = s + 1 < R ? maxLen - sortedKeys[s + 1] : 0;
+  for (int t = next; t < len; ++t) width[t] = (int)(s + 1);
+}
+
+// Jagged scatter: entry t of sorted row s goes to iterPtr[t] + s. A thread per
+// sorted row handles its first kCoop entries (coalesced over s); the warp then
+// walks each longer row's remaining entries together, one entry per lane.
+constexpr int kCoop = 64;
+__global__ void __launch_bounds__(256) k_jds_scatter(int R, const int* __restrict__ rowPtrs,
+                                                     const int* __restrict__ colIdx,
+                                                     const float* __restrict__ value,
+                                                     const int* __restrict__ perm,
+                                                     const int* __restrict__ iterPtr,
+                                                     int* __restrict__ jdsCol,
+                                                     float* __restrict__ jdsVal) {
+  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  int a = 0, len = 0;
+  if (s < R) {
+    const int r = perm[s];
+    a = rowPtrs[r];
+    len = rowPtrs[r + 1] - a;
+    const int lim = len < kCoop ? len : kCoop;
+    for (int t = 0; t < lim; ++t) {
+      const long long o = (long long)iterPtr[t] + s;
+      jdsCol[o] = colIdx[a + t];
+      jdsVal[o] = value[a + t];
+    }
+  }
+  unsigned longRows = __ballot_sync(kFullMask, len > kCoop);
+  while (longRows) {
+    const int src = __ffs(longRows) - 1;
+    longRows &= longRows - 1;
+    const int la = __shfl_sync(kFullMask, a, src);
+    const int ll = __shfl_sync(kFullMask, len, src);
+    const long long ss = s - lane + src;
+    for (int t = kCoop + lane; t < ll; t += 32) {
+      const long long o = (long long)iterPtr[t] + ss;
+      jdsCol[o] = colIdx[la + t];
+      jdsVal[o] = value[la + t];
+    }
+  }
+}
+
+}  // namespace
+
+size_t scan_scratch_ints(long long n) { return (size_t)((n + kScanTile - 1) / kScanTile + 1); }
+
+cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const long long warps = ((long long)R + 31) / 32;
+  const long long blocks = (warps * 32 + 255) / 256;
+  k_expand_rows<<<(unsigned)blocks, 256, 0, s>>>(R, rowPtrs, rowIdx);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
+                              const float* value, int* ellCol, float* ellVal, int* nnzPerRow,
+                              cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const long long blocks = ((long long)R + 255) / 256;
+  k_csr_to_ell<<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, ellCol, ellVal,
+                                                nnzPerRow);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tail_scan(int R, int K, const int* rowPtrs, int* tailPtr, int* scratch,
+                             cudaStream_t s) {
+  return exclusive_scan(TailLenIn{rowPtrs, K}, (long long)R, tailPtr, scratch, s);
+}
+
+cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* colIdx,
+                                 const float* value, const int* tailPtr, int* cooRow,
+                                 int* cooCol, float* cooVal, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const long long warps = ((long long)R + 31) / 32;
+  const long long blocks = (warps * 32 + 255) / 256;
+  k_hyb_tail_copy<<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, tailPtr, cooRow,
+                                                   cooCol, cooVal);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// Scratch layout for the JDS build (all int32):
+//   keysA[R] valsA[R] keysB[R] hist[kRadix*nTiles + 1] scanScratch[...] width[maxLen]
+size_t jds_sort_scratch_bytes(int R, int maxLen) {
+  const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
+  const long long nh = (long long)kRadix * (nTiles > 0 ? nTiles : 1);
+  const long long scanN = nh > maxLen ? nh : maxLen;
+  const long long ints = 3LL * R + (nh + 1) + (long long)scan_scratch_ints(scanN) + maxLen + 16;
+  return (size_t)ints * sizeof(int);
+}
+
+cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
+                             const float* value, int* perm, int* iterPtr, int* jdsCol,
+                             float* jdsVal, void* scratch, cudaStream_t s) {
+  if (R <= 0) {
+    // iterPtr has maxLen + 1 = 1 entry
+    return cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
+  }
+  const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
+  const long long nh = (long long)kRadix * nTiles;
+  int* keysA = static_cast<int*>(scratch);
+  int* valsA = keysA + R;
+  int* keysB = valsA + R;
+  int* hist = keysB + R;
+  int* scanScratch = hist + nh + 1;
+  const long long scanN = nh > maxLen ? nh : maxLen;
+  int* width = scanScratch + scan_scratch_ints(scanN);
+
+  int bits = 0;
+  while (bits < 31 && (1LL << bits) <= maxLen) ++bits;
+  const int passes = bits == 0 ? 1 : (bits + kRadixBits - 1) / kRadixBits;
+  // Ping-pong so that the last pass writes perm (values) and keysA (keys).
+  // pass p reads (kIn, vIn), writes (kOut, vOut).
+  int* kBuf[2] = {keysA, keysB};
+  int* vBuf[2] = {valsA, perm};
+  // choose the first output slot so that the final pass lands in slot 1
+  int outSlot = (passes % 2 == 1) ? 1 : 0;
+  const int* kIn = nullptr;
+  const int* vIn = nullptr;
+  cudaError_t err = cudaSuccess;
+  for (int p = 0; p < passes; ++p) {
+    SortIn in{rowPtrs, maxLen, kIn, vIn};
+    const int shift = p * kRadixBits;
+    k_radix_hist<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, (int)nTiles, hist);
+    note_launches(1);
+    err = exclusive_scan(ArrayIn{hist}, nh, hist, scanScratch, s);
+    if (err != cudaSuccess) return err;
+    k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, (int)nTiles, hist,
+                                                             kBuf[outSlot], vBuf[outSlot]);
+    note_launches(1);
+    kIn = kBuf[outSlot];
+    vIn = vBuf[outSlot];
+    outSlot ^= 1;
+  }
+  const int* sortedKeys = kIn;  // == keysB when the final pass used slot 1
+  // widths and iterPtr
+  if (maxLen > 0) {
+    k_jds_widths<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(R, maxLen, sortedKeys,
+                                                                       width);
+    note_launches(1);
+    err = exclusive_scan(ArrayIn{width}, (long long)maxLen, iterPtr, scanScratch, s);
+    if (err != cudaSuccess) return err;
+    k_jds_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
+        R, rowPtrs, colIdx, value, perm, iterPtr, jdsCol, jdsVal);
+    note_launches(1);
+  } else {
+    err = cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
+    if (err != cudaSuccess) return err;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace spmv

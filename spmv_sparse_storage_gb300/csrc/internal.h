@@ -1,0 +1,96 @@
+// internal.h -- declarations shared by the library's translation units.
+// Not installed; the public ABI is include/spmv.h.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/spmv.h"
+
+namespace spmv {
+
+// ---------------------------------------------------------------------------
+// Row statistics and validation results, written by the stats kernels.
+// ---------------------------------------------------------------------------
+constexpr int kExactLenBins = 4096;  // exact row-length histogram for len < 4096
+
+enum : unsigned {
+  kErrRowPtrStart = 1u,     // rowPtrs[0] != 0
+  kErrRowPtrDecrease = 2u,  // rowPtrs[r+1] < rowPtrs[r]
+  kErrRowPtrEnd = 4u,       // rowPtrs[numRows] != nnz
+  kErrColRange = 8u,        // colIdx outside [0, numCols)
+};
+
+struct DevStats {
+  unsigned int err;
+  int firstBadRow;
+  int firstBadNnz;
+  int maxLen;
+  int minLen;
+  int emptyRows;
+  int maxWarpNnz;
+  int pad0;
+  unsigned long long sumSq;
+  unsigned long long histLog2[33];
+  unsigned int histExact[kExactLenBins];
+};
+
+// ---------------------------------------------------------------------------
+// Tiling constants (shared between the partition kernel and the CSR kernel).
+// ---------------------------------------------------------------------------
+constexpr int kCsrThreads = 256;
+constexpr int kCsrItemsPerThread = 8;
+constexpr int kCsrTileItems = kCsrThreads * kCsrItemsPerThread;  // rows + nonzeros per tile
+
+constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
+constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
+constexpr int kJdsTailRows = 256;        // tail blocks: sorted rows per block
+constexpr int kJdsTailDiags = 64;        // tail blocks: diagonals per block
+
+// ---------------------------------------------------------------------------
+// Launch accounting (every launcher reports its kernels).
+// ---------------------------------------------------------------------------
+void note_launches(int n);
+int num_sms();
+
+// ---------------------------------------------------------------------------
+// Launchers. Each returns the cudaError_t of its launches.
+// ---------------------------------------------------------------------------
+// stats.cu
+cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
+                         DevStats* st, cudaStream_t s);
+cudaError_t launch_csr_partition(int R, int Z, const int* rowPtrs, int nTiles, int* tileRow,
+                                 cudaStream_t s);
+
+// convert.cu
+cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s);
+cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
+                              const float* value, int* ellCol, float* ellVal, int* nnzPerRow,
+                              cudaStream_t s);
+// Exclusive scan of max(0, len(r) - K) over rows into tailPtr[0..R].
+cudaError_t launch_tail_scan(int R, int K, const int* rowPtrs, int* tailPtr, int* scratch,
+                             cudaStream_t s);
+size_t scan_scratch_ints(long long n);
+cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* colIdx,
+                                 const float* value, const int* tailPtr, int* cooRow,
+                                 int* cooCol, float* cooVal, cudaStream_t s);
+// JDS: stable sort of rows by length (longest first), iterPtr, jagged scatter.
+size_t jds_sort_scratch_bytes(int R, int maxLen);
+cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
+                             const float* value, int* perm, int* iterPtr, int* jdsCol,
+                             float* jdsVal, void* scratch, cudaStream_t s);
+
+// spmv_kernels.cu
+cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
+                            const float* value, const int* tileRow, int nTiles, const float* x,
+                            float* y, cudaStream_t s);
+cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
+                            const float* x, float* y, bool dependent, cudaStream_t s);
+cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
+                            const float* x, float* y, cudaStream_t s);
+cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
+                            const int* perm, const int* jdsCol, const float* jdsVal,
+                            const float* x, float* y, cudaStream_t s);
+
+}  // namespace spmv

@@ -1,0 +1,406 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+Converters are compared bit for bit (exported device arrays vs the oracle's
+conversion of the same CSR input). SpMV results must satisfy, per row,
+|y_gpu - y_ref| <= 1e-5 * (sum_j |a_ij x_j| + |y0_i|) + 1e-30 with y_ref in
+fp64: fp32 products summed in a different order (shuffle trees, shared and
+global atomics) differ from a sequential sum by a few ulps of the magnitude
+sum, far inside that bound for rows of up to several thousand entries.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS")
+
+
+@pytest.fixture(scope="module")
+def sp():
+    from spmv_sparse_storage_gb300 import _build
+    _build.build()
+    import spmv_sparse_storage_gb300 as sp
+    assert torch.cuda.is_available()
+    torch.cuda.set_device(0)
+    return sp
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def same_bits(a, b):
+    a = np.asarray(a)
+    b = np.asarray(b)
+    if a.dtype == np.float32:
+        a, b = a.view(np.int32), np.asarray(b, np.float32).view(np.int32)
+    return a.shape == b.shape and np.array_equal(a, b)
+
+
+def check_tol(y, yref, mag, what):
+    ok, worst = oracle.within_tolerance(y, yref, mag)
+    assert ok, f"{what}: worst |err|/bound = {worst:.3g}"
+    return worst
+
+
+def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, ell_ok=True,
+                 offset=0):
+    """Convert `inp` to every format on the GPU, compare the arrays with the
+    oracle's conversions and the SpMV results with the oracle's y."""
+    rp_t = dev(inp.row_ptrs)
+    if offset:
+        # misaligned views of colIdx/value/y to exercise the scalar paths
+        ci_buf = dev(np.concatenate([np.zeros(offset, np.int32), inp.col_idx]))
+        va_buf = dev(np.concatenate([np.zeros(offset, np.float32), inp.value]))
+        ci_t, va_t = ci_buf[offset:], va_buf[offset:]
+    else:
+        ci_t, va_t = dev(inp.col_idx), dev(inp.value)
+    x_t = dev(inp.x)
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    R, Z = inp.num_rows, inp.nnz
+    results = {}
+    with sp.SparseMatrix(R, inp.num_cols, rp_t, ci_t, va_t) as m:
+        st = m.stats()
+        ost = orc.row_stats(inp.row_ptrs)
+        assert st["max_len"] == ost["max_len"]
+        assert st["hist_log2"] == ost["hist_log2"].tolist()
+        assert st["mean_len"] == pytest.approx(ost["mean"], rel=1e-12, abs=1e-12)
+        assert st["var_len"] == pytest.approx(ost["var"], rel=1e-9, abs=1e-9)
+        assert st["auto_format"] == orc.select(R, Z, ost["max_len"])
+        if R and ost["max_len"] < 4096:
+            assert st["auto_hyb_width"] == orc.hyb_auto_width(inp.row_ptrs)
+        for f in formats:
+            widths = hyb_widths if f == "HYB" else (None,)
+            for w in widths:
+                if f == "ELL" and not ell_ok:
+                    with pytest.raises(sp.SpmvError) as ei:
+                        m.convert("ELL")
+                    assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
+                    continue
+                if f == "HYB":
+                    m.convert(f, ell_width=w)
+                else:
+                    m.convert(f)
+                if arrays:
+                    got = m.export(f)
+                    compare_arrays(orc, inp, f, got, w, st)
+                y_t = dev(inp.y0)
+                m.run(f, x_t, y_t)
+                torch.cuda.synchronize()
+                key = f if f != "HYB" else f"HYB{w}"
+                results[key] = check_tol(y_t.cpu().numpy(), yref, mag, f"{inp.name}/{key}")
+        if st["auto_format"] in formats and (st["auto_format"] != "ELL" or ell_ok):
+            y_t = dev(inp.y0)
+            m.run("AUTO", x_t, y_t)
+            torch.cuda.synchronize()
+            check_tol(y_t.cpu().numpy(), yref, mag, f"{inp.name}/AUTO")
+    return results
+
+
+def compare_arrays(orc, inp, f, got, w, st):
+    rp, ci, va = inp.row_ptrs, inp.col_idx, inp.value
+    if f == "CSR":
+        assert same_bits(got["row_ptrs"], rp) and same_bits(got["col_idx"], ci)
+    elif f == "COO":
+        want = orc.csr_to_coo(rp, ci, va)
+        assert same_bits(got["row_idx"], want["row_idx"])
+        assert same_bits(got["col_idx"], want["col_idx"])
+        assert same_bits(got["value"], want["value"])
+    elif f == "ELL":
+        want = orc.csr_to_ell(rp, ci, va)
+        assert got["width"] == want["width"]
+        assert same_bits(got["col_idx"], want["col_idx"])
+        assert same_bits(got["value"], want["value"])
+        assert same_bits(got["nnz_per_row"], want["nnz_per_row"])
+    elif f == "HYB":
+        K = w if w else st["auto_hyb_width"]
+        K = min(K, st["max_len"])
+        want = orc.csr_to_hyb(rp, ci, va, K)
+        assert got["width"] == K
+        assert same_bits(got["col_idx"], want["col_idx"])
+        assert same_bits(got["value"], want["value"])
+        assert same_bits(got["nnz_per_row"], want["nnz_per_row"])
+        assert same_bits(got["coo_row_idx"], want["coo_row_idx"])
+        assert same_bits(got["coo_col_idx"], want["coo_col_idx"])
+        assert same_bits(got["coo_value"], want["coo_value"])
+    elif f == "JDS":
+        want = orc.csr_to_jds(rp, ci, va)
+        assert got["width"] == want["max_len"]
+        assert same_bits(got["perm"], want["perm"])
+        assert same_bits(got["iter_ptr"], want["iter_ptr"])
+        assert same_bits(got["col_idx"], want["col_idx"])
+        assert same_bits(got["value"], want["value"])
+
+
+# --- the worked example -------------------------------------------------------
+
+def test_fig14_1_every_format(sp, orc):
+    rp, ci, va = orc.dense_to_csr(synth.fig14_1_dense())
+    inp = synth.CSRInput("fig14_1", 4, 4, rp, ci, va, np.array([1, 2, 3, 4], np.float32),
+                         np.zeros(4, np.float32))
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 2, 3))
+    with sp.SparseMatrix(4, 4, dev(rp), dev(ci), dev(va)) as m:
+        for f in ("COO", "ELL", "HYB", "JDS"):
+            m.convert(f, ell_width=2) if f == "HYB" else m.convert(f)
+        for f in FORMATS:
+            y = torch.zeros(4, device="cuda")
+            m.run(f, dev(inp.x), y)
+            assert y.cpu().tolist() == [15.0, 50.0, 28.0, 24.0], f
+        ell = m.export("ELL")
+        assert ell["value"].tolist() == [1, 5, 2, 6, 7, 3, 8, 0, 0, 9, 0, 0]
+        assert ell["col_idx"].tolist() == [0, 0, 1, 3, 1, 2, 2, -1, -1, 3, -1, -1]
+        jds = m.export("JDS")
+        assert jds["perm"].tolist() == [1, 0, 2, 3]
+        assert jds["iter_ptr"].tolist() == [0, 4, 7, 8]
+
+
+# --- irregular and degenerate matrices -------------------------------------------
+
+EDGE = {
+    "one_by_one": dict(num_rows=1, num_cols=1, mean_len=1),
+    "empty_rows": dict(num_rows=3001, num_cols=2000, mean_len=5, empty_frac=0.3),
+    "all_empty": dict(num_rows=777, num_cols=50, mean_len=0, empty_frac=1.0),
+    "one_long_row": dict(num_rows=100, num_cols=200_000, mean_len=3, long_rows=1,
+                         long_len=150_000),
+    "few_long_rows": dict(num_rows=5003, num_cols=60_000, mean_len=7, long_rows=5,
+                          long_len=50_000),
+    "unsorted": dict(num_rows=2048, num_cols=4096, mean_len=9, unsorted=True),
+    "duplicates": dict(num_rows=1500, num_cols=300, mean_len=12, duplicates=True),
+    "explicit_zeros": dict(num_rows=1024, num_cols=1024, mean_len=6, zeros_frac=0.3),
+    "rows_not_mult4": dict(num_rows=1003, num_cols=1003, mean_len=4),
+    "tall_skinny": dict(num_rows=100_000, num_cols=3, mean_len=2),
+    "wide_short": dict(num_rows=3, num_cols=100_000, mean_len=4000),
+    "len_beyond_exact_hist": dict(num_rows=60, num_cols=20_000, mean_len=5000),
+    "many_empty_then_long": dict(num_rows=20_000, num_cols=9000, mean_len=1, empty_frac=0.97,
+                                 long_rows=3, long_len=9000),
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE))
+def test_edge_cases(sp, orc, name):
+    inp = synth.random_csr(11, name=name, **EDGE[name])
+    lens = np.diff(inp.row_ptrs)
+    mx = int(lens.max()) if lens.size else 0
+    R, Z = inp.num_rows, inp.nnz
+    ell_ok = R * mx <= min(2**31 - 1, 4 * Z + R)
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 5), ell_ok=ell_ok)
+
+
+@pytest.mark.parametrize("offset", [1, 2, 3])
+def test_misaligned_arrays(sp, orc, offset):
+    inp = synth.random_csr(3, 4001, 3000, mean_len=8, empty_frac=0.05, long_rows=3,
+                           long_len=2500, name=f"misaligned{offset}")
+    check_matrix(sp, orc, inp, hyb_widths=(0,), offset=offset)
+
+
+def test_empty_matrix(sp):
+    rp = torch.zeros(1, dtype=torch.int32, device="cuda")
+    with sp.SparseMatrix(0, 0, rp, torch.empty(0, dtype=torch.int32, device="cuda"),
+                         torch.empty(0, device="cuda")) as m:
+        for f in ("COO", "ELL", "HYB", "JDS"):
+            m.convert(f)
+        for f in FORMATS:
+            m.run(f, None, None)
+        assert m.stats()["max_len"] == 0
+
+
+def test_zero_columns_with_entries_rejected(sp):
+    rp = dev(np.array([0, 1], np.int32))
+    with pytest.raises(sp.SpmvError) as ei:
+        sp.spmv_create_csr(1, 0, 1, rp, dev(np.array([0], np.int32)),
+                           dev(np.array([1.0], np.float32)))
+    assert ei.value.code == sp.SPMV_ERR_COL_OUT_OF_RANGE
+
+
+# --- full-size workloads (the bench's configurations) ---------------------------
+
+_CACHE = {}
+
+
+def workload(name):
+    if name not in _CACHE:
+        _CACHE.clear()
+        _CACHE[name] = synth.make_workload(name)
+    return _CACHE[name]
+
+
+@pytest.mark.parametrize("name", ["tiny_uniform", "laplace2d", "uniform_random", "skewed",
+                                  "stencil27"])
+def test_workload_full_size(sp, orc, name):
+    inp = workload(name)
+    res = check_matrix(sp, orc, inp, hyb_widths=(0,), ell_ok=(name != "skewed"))
+    print(name, {k: round(v, 4) for k, v in res.items()})
+
+
+def test_skewed_selects_hyb_width_20(sp):
+    inp = workload("skewed")
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        assert m.select() == ("HYB", 20)
+
+
+# --- validation errors (input sanity rules) --------------------------------------
+
+def _create_status(sp, R, C, rp, ci, va):
+    import ctypes
+    h = ctypes.c_void_p()
+    rp_t, ci_t, va_t = dev(rp), dev(ci), dev(va)
+    st = sp._lib.spmv_create_csr(ctypes.byref(h), R, C, len(ci), rp_t.data_ptr(),
+                                 ci_t.data_ptr() if len(ci) else None,
+                                 va_t.data_ptr() if len(va) else None,
+                                 torch.cuda.current_stream().cuda_stream)
+    if st == sp.SPMV_OK:
+        sp._lib.spmv_destroy(h)
+    else:
+        assert h.value is None
+    return st
+
+
+def test_validation_errors(sp, orc):
+    rp, ci, va = orc.dense_to_csr(synth.fig14_1_dense())
+    assert _create_status(sp, 4, 4, rp, ci, va) == sp.SPMV_OK
+    for bad_rp in ([1, 2, 5, 7, 8], [0, 3, 2, 7, 8], [0, 2, 5, 7, 7], [0, 2, 5, 9, 8]):
+        assert _create_status(sp, 4, 4, np.array(bad_rp, np.int32), ci, va) == \
+            sp.SPMV_ERR_BAD_ROWPTRS, bad_rp
+    for pos, val in ((5, 4), (0, -1), (7, 1 << 30)):
+        bad = ci.copy()
+        bad[pos] = val
+        assert _create_status(sp, 4, 4, rp, bad, va) == sp.SPMV_ERR_COL_OUT_OF_RANGE
+    assert _create_status(sp, 4, 3, rp, ci, va) == sp.SPMV_ERR_COL_OUT_OF_RANGE
+    bad = ci.copy()
+    bad[0] = 9
+    assert _create_status(sp, 4, 4, np.array([0, 3, 2, 7, 8], np.int32), bad, va) == \
+        sp.SPMV_ERR_BAD_ROWPTRS  # row pointers are reported first
+    # the same checks the oracle makes
+    assert orc.validate(4, 4, np.array([0, 3, 2, 7, 8], np.int32), ci) == oracle.BAD_ROWPTRS
+
+
+def test_large_validation_error_position(sp):
+    inp = synth.random_csr(5, 200_000, 1000, mean_len=6)
+    ci = inp.col_idx.copy()
+    ci[len(ci) // 2 + 1] = 1000
+    assert _create_status(sp, inp.num_rows, 1000, inp.row_ptrs, ci, inp.value) == \
+        sp.SPMV_ERR_COL_OUT_OF_RANGE
+    rp = inp.row_ptrs.copy()
+    rp[150_000] = rp[150_001] + 1
+    assert _create_status(sp, inp.num_rows, 1000, rp, inp.col_idx, inp.value) == \
+        sp.SPMV_ERR_BAD_ROWPTRS
+
+
+# --- API behaviour ------------------------------------------------------------------
+
+def _fig(sp, orc):
+    rp, ci, va = orc.dense_to_csr(synth.fig14_1_dense())
+    return sp.SparseMatrix(4, 4, dev(rp), dev(ci), dev(va))
+
+
+def test_not_converted_and_argument_errors(sp, orc):
+    with _fig(sp, orc) as m:
+        x = dev(np.array([1, 2, 3, 4], np.float32))
+        y = torch.zeros(4, device="cuda")
+        for f in ("COO", "ELL", "HYB", "JDS"):
+            with pytest.raises(sp.SpmvError) as ei:
+                m.run(f, x, y)
+            assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
+        with pytest.raises(sp.SpmvError) as ei:
+            m.export("ELL")
+        assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
+        buf = torch.zeros(8, device="cuda")
+        with pytest.raises(sp.SpmvError) as ei:
+            m.run("CSR", buf[:4], buf[2:6])  # x and y overlap
+        assert ei.value.code == sp.SPMV_ERR_INVALID_ARG
+        host = torch.zeros(4).pin_memory()
+        st = sp._lib.spmv_run(m.handle, sp.SPMV_CSR, x.data_ptr(), host.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+        assert st == sp.SPMV_ERR_INVALID_ARG  # host memory is refused, never touched
+        assert host.tolist() == [0, 0, 0, 0]
+        with pytest.raises(sp.SpmvError):
+            m.run(7, x, y)
+        with pytest.raises(sp.SpmvError):
+            sp.spmv_convert_hyb(m.handle, -1)
+
+
+def test_accumulates_and_streams(sp, orc):
+    inp = synth.random_csr(21, 5000, 4000, mean_len=9, empty_frac=0.1)
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    ax = yref - inp.y0.astype(np.float64)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        m = sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                            dev(inp.value))
+        for f in ("COO", "ELL", "HYB", "JDS"):
+            m.convert(f)
+        for f in FORMATS:
+            y = dev(inp.y0)
+            m.run(f, dev(inp.x), y)
+            m.run(f, dev(inp.x), y)  # y = y0 + 2 A x
+            s.synchronize()
+            ok, worst = oracle.within_tolerance(y.cpu().numpy(), inp.y0 + 2 * ax,
+                                                2 * mag, rel=1e-5)
+            assert ok, (f, worst)
+        m.close()
+
+
+def test_guard_bands_untouched(sp, orc):
+    inp = synth.random_csr(8, 3001, 2999, mean_len=6, long_rows=2, long_len=2000)
+    G = 64
+    sentinel = np.float32(-7.25e33)
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        for f in ("COO", "ELL", "HYB", "JDS"):
+            m.convert(f)
+        for f in FORMATS:
+            buf = torch.full((inp.num_rows + 2 * G,), float(sentinel), device="cuda")
+            y = buf[G:G + inp.num_rows]
+            y.copy_(dev(inp.y0))
+            xb = torch.full((inp.num_cols + 2 * G,), float(sentinel), device="cuda")
+            x = xb[G:G + inp.num_cols]
+            x.copy_(dev(inp.x))
+            m.run(f, x, y)
+            torch.cuda.synchronize()
+            b = buf.cpu().numpy()
+            assert np.all(b[:G] == sentinel) and np.all(b[-G:] == sentinel), f
+            xb2 = xb.cpu().numpy()
+            assert np.all(xb2[:G] == sentinel) and np.all(xb2[-G:] == sentinel), f
+
+
+def test_memory_limit(sp, orc):
+    inp = synth.random_csr(4, 20_000, 20_000, mean_len=10)
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        sp.spmv_set_memory_limit(1024)
+        try:
+            with pytest.raises(sp.SpmvError) as ei:
+                m.convert("ELL")
+            assert ei.value.code == sp.SPMV_ERR_ALLOC
+        finally:
+            sp.spmv_set_memory_limit(None)
+        m.convert("ELL")
+
+
+def test_hyb_reconvert_widths(sp, orc):
+    inp = synth.random_csr(9, 4000, 3000, mean_len=8, long_rows=4, long_len=1500)
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        for w in (3, 0, 1, 10_000, 7):
+            m.convert("HYB", ell_width=w)
+            y = dev(inp.y0)
+            m.run("HYB", dev(inp.x), y)
+            torch.cuda.synchronize()
+            check_tol(y.cpu().numpy(), yref, mag, f"hyb width {w}")
+
+
+def test_launch_counter_counts_kernels(sp, orc):
+    with _fig(sp, orc) as m:
+        m.convert("HYB", ell_width=2)
+        n0 = sp.spmv_launch_count()
+        x = dev(np.array([1, 2, 3, 4], np.float32))
+        y = torch.zeros(4, device="cuda")
+        m.run("CSR", x, y)
+        m.run("HYB", x, y)
+        assert sp.spmv_launch_count() - n0 == 3
