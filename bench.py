@@ -440,9 +440,13 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    from spmv_sparse_storage_gb300 import _build
     if rank == 0:
-        _build.build()
+        import importlib.util
+        path = os.path.join(ROOT, "spmv_sparse_storage_gb300", "_build.py")
+        spec = importlib.util.spec_from_file_location("_spmv_build", path)
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
     barrier(world)
     line = run_ours(args, rank, world, device)
     if rank == 0:

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libspmv_gb300.so")
 if not os.path.exists(LIB_PATH):
     raise ImportError(
         f"{LIB_PATH} is missing; build it with "
-        "`python -m spmv_sparse_storage_gb300._build`")
+        "`python spmv_sparse_storage_gb300/_build.py`")
 
 _lib = C.CDLL(LIB_PATH)
 

@@ -2,7 +2,7 @@
 
 Each translation unit is compiled in parallel, then linked into one shared
 library with the CUDA runtime linked statically. Run as
-``python -m spmv_sparse_storage_gb300._build [--force] [--verbose]``.
+``python spmv_sparse_storage_gb300/_build.py [--force] [--verbose]``.
 """
 from __future__ import annotations
 

@@ -23,3 +23,14 @@ def load_golden(name):
 def orc():
     import oracle
     return oracle.get()
+
+
+def build_library():
+    """Compile the CUDA library (loading the build script by path, so that the
+    package itself is imported only once the library exists)."""
+    import importlib.util
+    path = os.path.join(ROOT, "spmv_sparse_storage_gb300", "_build.py")
+    spec = importlib.util.spec_from_file_location("_spmv_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.build()

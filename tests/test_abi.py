@@ -17,8 +17,8 @@ def header_functions():
 
 @pytest.fixture(scope="module")
 def sp():
-    from spmv_sparse_storage_gb300 import _build
-    _build.build()
+    from conftest import build_library
+    build_library()
     import spmv_sparse_storage_gb300 as sp
     return sp
 

@@ -21,8 +21,8 @@ FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS")
 
 @pytest.fixture(scope="module")
 def sp():
-    from spmv_sparse_storage_gb300 import _build
-    _build.build()
+    from conftest import build_library
+    build_library()
     import spmv_sparse_storage_gb300 as sp
     assert torch.cuda.is_available()
     torch.cuda.set_device(0)
