@@ -207,7 +207,7 @@ class _DeviceView:
 
     def __init__(self, ptr, n, typestr):
         self.__cuda_array_interface__ = {"shape": (int(n),), "typestr": typestr,
-                                         "data": (int(ptr or 0), True), "version": 3}
+                                         "data": (int(ptr or 0), False), "version": 3}
 
 
 def device_view(ptr, n, dtype):
