@@ -194,7 +194,9 @@ def test_edge_cases(sp, orc, name):
 def test_misaligned_arrays(sp, orc, offset):
     inp = synth.random_csr(3, 4001, 3000, mean_len=8, empty_frac=0.05, long_rows=3,
                            long_len=2500, name=f"misaligned{offset}")
-    check_matrix(sp, orc, inp, hyb_widths=(0,), offset=offset)
+    check_matrix(sp, orc, inp, hyb_widths=(0,), offset=offset, ell_ok=False)
+    short = synth.random_csr(4, 4001, 3000, mean_len=8, name=f"misaligned{offset}_short")
+    check_matrix(sp, orc, short, hyb_widths=(0, 3), offset=offset)
 
 
 def test_empty_matrix(sp):
@@ -346,7 +348,7 @@ def test_accumulates_and_streams(sp, orc):
 
 
 def test_guard_bands_untouched(sp, orc):
-    inp = synth.random_csr(8, 3001, 2999, mean_len=6, long_rows=2, long_len=2000)
+    inp = synth.random_csr(8, 3001, 2999, mean_len=6, long_rows=2, long_len=20)
     G = 64
     sentinel = np.float32(-7.25e33)
     with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
@@ -387,7 +389,10 @@ def test_hyb_reconvert_widths(sp, orc):
     yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
     with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                          dev(inp.value)) as m:
-        for w in (3, 0, 1, 10_000, 7):
+        with pytest.raises(sp.SpmvError) as ei:
+            m.convert("HYB", ell_width=10_000)  # capped at the longest row: over budget
+        assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
+        for w in (3, 0, 1, 7, 40):
             m.convert("HYB", ell_width=w)
             y = dev(inp.y0)
             m.run("HYB", dev(inp.x), y)
