@@ -137,9 +137,9 @@ struct spmv_handle_s {
   spmv_stats stats;
   std::vector<unsigned> histExact;  // exact row-length counts for len < kExactLenBins
 
-  // CSR: nnz-balanced partition (merge path), computed at creation
-  int nTiles = 0;
-  int* tileRow = nullptr;
+  // CSR: nnz-balanced split, one warp per kCsrChunk nonzeros (computed at creation)
+  int nChunks = 0;
+  int* chunkRow = nullptr;
   std::vector<Buf> csrBufs;
 
   // COO (shares colIdx/value with the caller's CSR arrays)
@@ -317,13 +317,12 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   if (st != SPMV_OK) return fail(st);
   st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, s));
   if (st != SPMV_OK) return fail(st);
-  // nnz-balanced partition for the CSR kernel (binary searches stay bounded
-  // even if validation fails below)
-  const long long items = (long long)numRows + nnz;
-  h->nTiles = (int)((items + spmv::kCsrTileItems - 1) / spmv::kCsrTileItems);
-  st = alloc_typed(h, (long long)h->nTiles + 1, s, &h->tileRow, h->csrBufs);
+  // nnz-balanced split for the CSR kernel (the kernel checks bounds, so it
+  // stays in bounds even if validation fails below)
+  h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
+  st = alloc_typed(h, (long long)h->nChunks + 1, s, &h->chunkRow, h->csrBufs);
   if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_csr_partition(numRows, nnz, d_rowPtrs, h->nTiles, h->tileRow, s));
+  st = record(spmv::launch_csr_chunk_rows(numRows, nnz, d_rowPtrs, h->nChunks, h->chunkRow, s));
   if (st != SPMV_OK) return fail(st);
   hst = new (std::nothrow) DevStats;
   if (!hst) return fail(SPMV_ERR_ALLOC);
@@ -533,7 +532,7 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   switch (format) {
     case SPMV_CSR:
       return record(spmv::launch_spmv_csr(h->R, h->Z, h->rowPtrs, h->colIdx, h->value,
-                                          h->tileRow, h->nTiles, d_x, d_y, s));
+                                          h->chunkRow, d_x, d_y, s));
     case SPMV_COO:
       return record(spmv::launch_spmv_coo(h->Z, h->cooRow, h->colIdx, h->value, d_x, d_y,
                                           false, s));

@@ -37,11 +37,9 @@ struct DevStats {
 };
 
 // ---------------------------------------------------------------------------
-// Tiling constants (shared between the partition kernel and the CSR kernel).
+// CSR work split: one warp per kCsrChunk consecutive nonzeros.
 // ---------------------------------------------------------------------------
-constexpr int kCsrThreads = 256;
-constexpr int kCsrItemsPerThread = 8;
-constexpr int kCsrTileItems = kCsrThreads * kCsrItemsPerThread;  // rows + nonzeros per tile
+constexpr int kCsrChunk = 128;
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
@@ -60,8 +58,6 @@ int num_sms();
 // stats.cu
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
                          DevStats* st, cudaStream_t s);
-cudaError_t launch_csr_partition(int R, int Z, const int* rowPtrs, int nTiles, int* tileRow,
-                                 cudaStream_t s);
 
 // convert.cu
 cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s);
@@ -82,9 +78,12 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
                              float* jdsVal, void* scratch, cudaStream_t s);
 
 // spmv_kernels.cu
+// chunkRow[c] = row holding nonzero c*kCsrChunk, chunkRow[nChunks] = numRows-1
+cudaError_t launch_csr_chunk_rows(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
+                                  cudaStream_t s);
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* tileRow, int nTiles, const float* x,
-                            float* y, cudaStream_t s);
+                            const float* value, const int* chunkRow, const float* x, float* y,
+                            cudaStream_t s);
 cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,

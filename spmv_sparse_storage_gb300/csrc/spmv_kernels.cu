@@ -7,6 +7,8 @@
 // Formats (ELL, Hybrid ELL-COO and JDS)", section "Summary": 0.25 op/byte),
 // so the designs below are about streaming those bytes at HBM speed, keeping
 // the gathered x resident in L2, and balancing the work.
+#include <climits>
+
 #include "device_util.cuh"
 #include "internal.h"
 
@@ -14,147 +16,147 @@ namespace spmv {
 namespace {
 
 // ===========================================================================
-// CSR, nnz-balanced (merge path).
-//
-// The pages' kernels give a row to a thread ("CSR format and SpMV") or a warp
-// ("[CUDA performance tuning] ...", section 2.2); both leave threads idle when
-// row lengths differ ("Introduction to sparse computing ...", section
-// "Building the problem framework": split work by nonzero count and split
-// very long rows). Here each CTA owns an equal share of the merged sequence
-// of row ends and nonzeros (kCsrTileItems items), located by a merge-path
-// search done once at handle creation (tileRow). A CTA:
-//   1. stages its slice of rowPtrs and the products value[k]*x[colIdx[k]] of
-//      its nonzeros in shared memory (value/colIdx streamed with 16-byte
-//      loads when aligned);
-//   2. splits its items again, IPT per thread, by a merge-path search in
-//      shared memory, and each thread sums its run of products, closing rows
-//      as it meets their ends;
-//   3. adds each row's sum into y: rows wholly inside the tile with a plain
-//      read-modify-write (coalesced over consecutive rows), the first and last
-//      row of the tile (possibly shared with a neighbour tile) atomically.
+// Warp-level segmented add. Each lane holds 4 consecutive entries of a
+// 128-entry chunk (entry 4*lane + e): their row `row[e]` (-1 = no entry) and
+// product `p[e]`. Runs of equal row are summed inside the lane, then across
+// lanes with a segmented shuffle scan, and each run is added into y with ONE
+// atomicAdd (a fire-and-forget reduction in L2). Only adjacent equal rows
+// merge, so any entry order is correct; rows grouped together give one
+// atomic per row per chunk. `waitFirst`: wait for the preceding kernel of the
+// stream (programmatic dependent launch) before the first write to y.
 // ===========================================================================
-template <int THREADS, int IPT, bool VEC>
-__global__ void __launch_bounds__(THREADS, 4) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
-                                                      const int* __restrict__ colIdx,
-                                                      const float* __restrict__ value,
-                                                      const int* __restrict__ tileRow,
-                                                      const float* __restrict__ x,
-                                                      float* __restrict__ y) {
-  constexpr int NT = THREADS * IPT;
-  __shared__ float sProd[NT];
-  __shared__ int sRp[NT + 1];
-  __shared__ float sAcc[NT + 1];
-
-  const int tile = blockIdx.x;
-  const long long total = (long long)R + Z;
-  const long long d0 = (long long)tile * NT;
-  const long long d1 = d0 + NT < total ? d0 + NT : total;
-  const int i0 = tileRow[tile];
-  const int i1 = tileRow[tile + 1];
-  const int j0 = (int)(d0 - i0);
-  const int j1 = (int)(d1 - i1);
-  const int nr = i1 - i0;  // rows whose end lies in this tile
-  const int nn = j1 - j0;  // nonzeros of this tile
-
-  // 1a. rowPtrs[i0 .. i1] (i1 <= R, so every entry exists)
-  for (int q = threadIdx.x; q <= nr; q += THREADS) {
-    sRp[q] = rowPtrs[i0 + q];
-    sAcc[q] = 0.0f;
-  }
-  // 1b. products of nonzeros j0 .. j1-1
-  if (VEC) {
-    const int v0 = (j0 + 3) & ~3;          // first 16-byte aligned index
-    const int v1 = j1 & ~3;                // end of the aligned body
-    if (v0 < v1) {
-      const int nvec = (v1 - v0) >> 2;
-      const int4* c4 = reinterpret_cast<const int4*>(colIdx + v0);
-      const float4* a4 = reinterpret_cast<const float4*>(value + v0);
-      float* dst = sProd + (v0 - j0);
-      for (int q = threadIdx.x; q < nvec; q += THREADS) {
-        const int4 c = ld_stream(c4 + q);
-        const float4 a = ld_stream(a4 + q);
-        float4 p;
-        p.x = a.x * ld_x(x + c.x);
-        p.y = a.y * ld_x(x + c.y);
-        p.z = a.z * ld_x(x + c.z);
-        p.w = a.w * ld_x(x + c.w);
-        dst[4 * q + 0] = p.x;
-        dst[4 * q + 1] = p.y;
-        dst[4 * q + 2] = p.z;
-        dst[4 * q + 3] = p.w;
-      }
-      // unaligned head [j0, v0) and tail [v1, j1): at most 3 each
-      const int t = threadIdx.x;
-      if (t < v0 - j0) {
-        const int k = j0 + t;
-        sProd[k - j0] = ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k));
-      } else if (t >= 4 && t < 4 + (j1 - v1)) {
-        const int k = v1 + (t - 4);
-        sProd[k - j0] = ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k));
-      }
-    } else {
-      for (int k = j0 + threadIdx.x; k < j1; k += THREADS)
-        sProd[k - j0] = ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k));
-    }
-  } else {
-    for (int k = j0 + threadIdx.x; k < j1; k += THREADS)
-      sProd[k - j0] = ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k));
-  }
-  __syncthreads();
-
-  // 2. per-thread merge path over (row ends sRp[1..nr], nonzeros j0..j1-1)
-  const int items = nr + nn;
-  const int dt = threadIdx.x * IPT < items ? threadIdx.x * IPT : items;
-  int lo = dt - nn > 0 ? dt - nn : 0;
-  int hi = dt < nr ? dt : nr;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (sRp[mid + 1] <= j0 + dt - 1 - mid)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  int li = lo;         // local row
-  int k = j0 + dt - lo;  // global nonzero index
-  float acc = 0.0f;
-  bool firstEnd = true;
-  const int dEnd = dt + IPT < items ? dt + IPT : items;
+__device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const float (&p)[4],
+                                                   float* __restrict__ y, bool waitFirst) {
+  const int lane = threadIdx.x & 31;
+  // in-lane run sums: s[e] = sum of the run that ends at e
+  float s[4];
+  s[0] = p[0];
 #pragma unroll
-  for (int it = 0; it < IPT; ++it) {
-    if (dt + it < dEnd) {
-      if (li < nr && sRp[li + 1] <= k) {
-        // row i0 + li ends here
-        if (firstEnd)
-          atomicAdd(&sAcc[li], acc);  // may have started in an earlier thread
-        else
-          sAcc[li] = acc;  // started and ended inside this thread
-        firstEnd = false;
-        acc = 0.0f;
-        ++li;
-      } else {
-        acc += sProd[k - j0];
-        ++k;
-      }
-    }
-  }
-  if (acc != 0.0f) atomicAdd(&sAcc[li], acc);  // row continues in the next thread
-  __syncthreads();
+  for (int e = 1; e < 4; ++e) s[e] = (row[e] == row[e - 1]) ? s[e - 1] + p[e] : p[e];
+  const int hEnd = row[1] != row[0] ? 0 : row[2] != row[1] ? 1 : row[3] != row[2] ? 2 : 3;
+  const bool single = (hEnd == 3);
+  const int rh = row[0], rt = row[3];
+  const float sh = s[hEnd], st = s[3];
 
-  // 3. write-out, coalesced over rows i0 .. i1
-  for (int q = threadIdx.x; q <= nr; q += THREADS) {
-    const int row = i0 + q;
-    if (row >= R) break;
-    const float v = sAcc[q];
-    if (q == nr) {
-      // row i1: its end is in a later tile; contribute only if it has
-      // nonzeros here
-      if (sRp[nr] < j1) atomicAdd(y + row, v);
-    } else if (q == 0 && sRp[0] < j0) {
-      atomicAdd(y + row, v);  // started in an earlier tile
-    } else {
-      y[row] += v;
+  // across lanes: w = tail-run sum carried to the right while lanes continue one run
+  const int prevRt = __shfl_up_sync(kFullMask, rt, 1);
+  const bool connected = lane > 0 && prevRt == rh;
+  const unsigned heads = __ballot_sync(kFullMask, !(single && connected));
+  const int segStart = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
+  float w = st;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float o = __shfl_up_sync(kFullMask, w, off);
+    if (lane - off >= segStart) w += o;
+  }
+  const float wPrev = __shfl_up_sync(kFullMask, w, 1);
+  const float carryIn = connected ? wPrev : 0.0f;
+  const int nextRh = __shfl_down_sync(kFullMask, rh, 1);
+  const bool tailEnds = (lane == 31) || nextRh != rt;
+
+  if (waitFirst) grid_dependency_wait();
+  if (single) {
+    if (tailEnds && rt >= 0) atomicAdd(y + rt, st + carryIn);
+  } else {
+    if (rh >= 0) atomicAdd(y + rh, sh + carryIn);
+#pragma unroll
+    for (int e = 1; e < 3; ++e)  // runs strictly inside the lane
+      if (e > hEnd && row[e] != row[e + 1] && row[e] >= 0) atomicAdd(y + row[e], s[e]);
+    if (tailEnds && rt >= 0) atomicAdd(y + rt, st);
+  }
+}
+
+// ===========================================================================
+// CSR, nnz-balanced.
+//
+// The pages' CSR kernels give a row to a thread ("CSR format and SpMV") or a
+// warp ("[CUDA performance tuning] ...", section 2.2); both idle threads when
+// row lengths differ, and the remedy named in "Introduction to sparse
+// computing ...", section "Building the problem framework", is to split the
+// work by nonzero count and to split very long rows. Here every warp takes
+// exactly kCsrChunk = 128 consecutive nonzeros (4 per lane, 16-byte loads of
+// value and colIdx when aligned), whatever rows they belong to: a 5000-entry
+// row spreads over 40 warps, an empty row costs nothing. The rows of a
+// chunk lie between chunkRow[c] and chunkRow[c+1] (computed once at handle
+// creation); each lane finds the row of its first entry by a binary search on
+// rowPtrs in that range (L1-resident after the first lane) and walks forward.
+// The warp then sums runs of equal row with shuffles and adds each run with
+// one atomicAdd, so no warp waits on a read of y.
+// ===========================================================================
+template <bool VEC>
+__global__ void __launch_bounds__(256) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
+                                                  const int* __restrict__ colIdx,
+                                                  const float* __restrict__ value,
+                                                  const int* __restrict__ chunkRow,
+                                                  const float* __restrict__ x,
+                                                  float* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long cbase = c * kCsrChunk;
+  if (cbase >= Z) return;  // warp-uniform
+  const int base = (int)cbase + 4 * lane;
+
+  int col[4];
+  float v[4];
+  if (VEC && base + 4 <= Z) {
+    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
+    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+    col[0] = c4.x; col[1] = c4.y; col[2] = c4.z; col[3] = c4.w;
+    v[0] = v4.x; v[1] = v4.y; v[2] = v4.z; v[3] = v4.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = base + e;
+      col[e] = k < Z ? ld_stream(colIdx + k) : 0;
+      v[e] = k < Z ? ld_stream(value + k) : 0.0f;
     }
   }
+  const int lo = __ldg(chunkRow + c);
+  const int hi = __ldg(chunkRow + c + 1);
+  // largest r in [lo, hi] with rowPtrs[r] <= base (rowPtrs[lo] <= chunk start)
+  int r = lo;
+  if (lo < hi && base < Z) {
+    int b = hi;
+    while (r < b) {
+      const int m = (r + b + 1) >> 1;
+      if (__ldg(rowPtrs + m) <= base)
+        r = m;
+      else
+        b = m - 1;
+    }
+  }
+  int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+  int row[4];
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int k = base + e;
+    while (k >= nextStart) {  // skips empty rows; bounded by hi
+      ++r;
+      nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+    }
+    row[e] = k < Z ? r : -1;
+    p[e] = k < Z ? v[e] * ld_x(x + col[e]) : 0.0f;
+  }
+  warp_segmented_add(row, p, y, false);
+}
+
+// chunkRow[c] = the row holding nonzero c*kCsrChunk (c < nChunks) and
+// chunkRow[nChunks] = numRows - 1. A row writes the entries of the chunks
+// that start inside it. Bounds are checked so that this kernel, which runs
+// before the validation result is read, stays in bounds on invalid input.
+__global__ void k_csr_chunk_rows(int R, int Z, const int* __restrict__ rowPtrs, int nChunks,
+                                 int* __restrict__ chunkRow) {
+  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r == 0) chunkRow[nChunks] = R > 0 ? R - 1 : 0;
+  if (r >= R) return;
+  const int a = rowPtrs[r];
+  const int b = rowPtrs[r + 1];
+  if (a < 0 || b > Z || b <= a) return;
+  const int c0 = (a + kCsrChunk - 1) / kCsrChunk;
+  int c1 = (b - 1) / kCsrChunk;
+  if (c1 > nChunks - 1) c1 = nChunks - 1;
+  for (int cc = c0; cc <= c1; ++cc) chunkRow[cc] = (int)r;
 }
 
 // ===========================================================================
@@ -167,9 +169,9 @@ __global__ void __launch_bounds__(THREADS, 4) k_spmv_csr(int R, int Z, const int
 // ===========================================================================
 template <bool VEC4>
 __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __restrict__ ellCol,
-                                                  const float* __restrict__ ellVal,
-                                                  const float* __restrict__ x,
-                                                  float* __restrict__ y) {
+                                                     const float* __restrict__ ellVal,
+                                                     const float* __restrict__ x,
+                                                     float* __restrict__ y) {
   // let a programmatically dependent kernel (the COO part of HYB) start its
   // loads; it waits for this grid to finish before it writes y
   grid_dependency_trigger();
@@ -238,20 +240,17 @@ __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __
 // COO ("Sparse Matrices and Basic Formats ...", section "COO format and
 // SpMV" uses one atomicAdd per nonzero, and same-row nonzeros contend). Here
 // a warp takes 128 consecutive entries, 4 per lane (16-byte loads when
-// aligned), reduces runs of equal row index first inside each lane and then
-// across lanes with a segmented shuffle scan, and issues ONE atomicAdd per
-// run. Correct for any entry order (only adjacent equal rows merge); fastest
-// when entries are grouped by row, as the converter produces them.
-// `dependent`: the kernel was launched as a programmatic dependent of the
-// ELL part of HYB; it computes everything before waiting for that kernel and
-// only then touches y.
+// aligned) and adds each run of equal row index with one atomicAdd (see
+// warp_segmented_add). `dependent`: launched as a programmatic dependent of
+// the ELL part of HYB, the kernel loads and reduces before waiting for that
+// kernel, and only then touches y.
 // ===========================================================================
 template <bool VEC>
 __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__ rowIdx,
                                                   const int* __restrict__ colIdx,
                                                   const float* __restrict__ value,
                                                   const float* __restrict__ x,
-                                                  float* __restrict__ y) {
+                                                  float* __restrict__ y, int dependent) {
   const int lane = threadIdx.x & 31;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long base = warp * 128 + 4 * lane;
@@ -280,42 +279,7 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
       }
     }
   }
-  // in-lane run sums: s[e] = sum of the run ending at e
-  float s[4];
-  s[0] = p[0];
-#pragma unroll
-  for (int e = 1; e < 4; ++e) s[e] = (row[e] == row[e - 1]) ? s[e - 1] + p[e] : p[e];
-  const int hEnd = row[1] != row[0] ? 0 : row[2] != row[1] ? 1 : row[3] != row[2] ? 2 : 3;
-  const bool single = (hEnd == 3);
-  const int rh = row[0], rt = row[3];
-  const float sh = s[hEnd], st = s[3];
-
-  // across lanes: w = tail-run sum carried right while lanes are one run
-  const int prevRt = __shfl_up_sync(kFullMask, rt, 1);
-  const bool connected = lane > 0 && prevRt == rh;
-  const unsigned heads = __ballot_sync(kFullMask, !(single && connected));
-  const int segStart = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
-  float w = st;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const float o = __shfl_up_sync(kFullMask, w, off);
-    if (lane - off >= segStart) w += o;
-  }
-  const float wPrev = __shfl_up_sync(kFullMask, w, 1);
-  const float carryIn = connected ? wPrev : 0.0f;
-  const int nextRh = __shfl_down_sync(kFullMask, rh, 1);
-  const bool tailEnds = (lane == 31) || nextRh != rt;
-
-  grid_dependency_wait();
-  if (single) {
-    if (tailEnds && rt >= 0) atomicAdd(y + rt, st + carryIn);
-  } else {
-    if (rh >= 0) atomicAdd(y + rh, sh + carryIn);
-#pragma unroll
-    for (int e = 1; e < 3; ++e)  // runs strictly inside the lane
-      if (e > hEnd && row[e] != row[e + 1] && row[e] >= 0) atomicAdd(y + row[e], s[e]);
-    if (tailEnds && rt >= 0) atomicAdd(y + rt, st);
-  }
+  warp_segmented_add(row, p, y, dependent != 0);
 }
 
 // ===========================================================================
@@ -325,27 +289,29 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // s < width(t), contiguous in s, so a warp's loads are coalesced. Widths only
 // shrink with t; the first tSplit diagonals (those at least
 // kJdsSplitMinWidth wide, at most kJdsSplitMaxDiag of them) run one thread
-// per sorted row. The remaining diagonals belong to the few longest rows
-// (s < wTail) and would serialise one thread over thousands of entries, so
-// they are split into blocks of kJdsTailRows rows x kJdsTailDiags diagonals
-// that run in parallel and add their partial sums atomically. The result of
-// sorted row s goes straight to y[perm[s]] (the page permutes the result back
-// with the row array).
+// per sorted row, which issues the loads of up to 8 diagonals and of perm[s]
+// before it waits for any of them. The remaining diagonals belong to the few
+// longest rows (s < wTail) and would serialise one thread over thousands of
+// entries, so they are split into blocks of kJdsTailRows rows x
+// kJdsTailDiags diagonals that run in parallel and add their partial sums
+// atomically. The result of sorted row s goes straight to y[perm[s]] (the
+// page permutes the result back with the row array).
 // ===========================================================================
-__global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
-                                                  int nMainBlocks, int tailRowBlocks,
-                                                  const int* __restrict__ iterPtr,
-                                                  const int* __restrict__ perm,
-                                                  const int* __restrict__ jdsCol,
-                                                  const float* __restrict__ jdsVal,
-                                                  const float* __restrict__ x,
-                                                  float* __restrict__ y) {
+__global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
+                                                     int nMainBlocks, int tailRowBlocks,
+                                                     const int* __restrict__ iterPtr,
+                                                     const int* __restrict__ perm,
+                                                     const int* __restrict__ jdsCol,
+                                                     const float* __restrict__ jdsVal,
+                                                     const float* __restrict__ x,
+                                                     float* __restrict__ y) {
   __shared__ int sIp[kJdsSplitMaxDiag + 1];
   if ((int)blockIdx.x < nMainBlocks) {
     for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
     __syncthreads();
     const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (s >= R) return;
+    const int r = ld_stream(perm + s);
     // number of leading diagonals wider than s (binary search; widths shrink)
     int lo = 0, hi = tSplit;
     while (lo < hi) {
@@ -357,24 +323,21 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
     }
     const int n = lo;
     float acc = 0.0f;
-    int t = 0;
-    for (; t + 4 <= n; t += 4) {
-      int c[4];
-      float v[4];
+    for (int t = 0; t < n; t += 8) {
+      int c[8];
+      float v[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const long long i = (long long)sIp[t + u] + s;
-        c[u] = ld_stream(jdsCol + i);
-        v[u] = ld_stream(jdsVal + i);
+      for (int u = 0; u < 8; ++u) {
+        if (t + u < n) {
+          const long long i = (long long)sIp[t + u] + s;
+          c[u] = ld_stream(jdsCol + i);
+          v[u] = ld_stream(jdsVal + i);
+        }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc = fmaf(v[u], ld_x(x + c[u]), acc);
+      for (int u = 0; u < 8; ++u)
+        if (t + u < n) acc = fmaf(v[u], ld_x(x + c[u]), acc);
     }
-    for (; t < n; ++t) {
-      const long long i = (long long)sIp[t] + s;
-      acc = fmaf(ld_stream(jdsVal + i), ld_x(x + ld_stream(jdsCol + i)), acc);
-    }
-    const int r = perm[s];
     if (s < wTail)
       atomicAdd(y + r, acc);  // the tail blocks add to this row too
     else
@@ -403,17 +366,25 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
 
 }  // namespace
 
+cudaError_t launch_csr_chunk_rows(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
+                                  cudaStream_t s) {
+  const long long n = R > 0 ? R : 1;
+  k_csr_chunk_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(R, Z, rowPtrs, nChunks, chunkRow);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* tileRow, int nTiles, const float* x,
-                            float* y, cudaStream_t s) {
-  if (nTiles <= 0) return cudaSuccess;
+                            const float* value, const int* chunkRow, const float* x, float* y,
+                            cudaStream_t s) {
+  if (Z <= 0 || R <= 0) return cudaSuccess;
+  const long long chunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
+  const long long blocks = (chunks * 32 + 255) / 256;
   const bool vec = aligned16(colIdx) && aligned16(value);
   if (vec)
-    k_spmv_csr<kCsrThreads, kCsrItemsPerThread, true>
-        <<<nTiles, kCsrThreads, 0, s>>>(R, Z, rowPtrs, colIdx, value, tileRow, x, y);
+    k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow, x, y);
   else
-    k_spmv_csr<kCsrThreads, kCsrItemsPerThread, false>
-        <<<nTiles, kCsrThreads, 0, s>>>(R, Z, rowPtrs, colIdx, value, tileRow, x, y);
+    k_spmv_csr<false><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -434,11 +405,12 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = dependent ? 1 : 0;
+  const int dep = dependent ? 1 : 0;
   cudaError_t err;
   if (vec)
-    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<true>, Z, rowIdx, colIdx, value, x, y);
+    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<true>, Z, rowIdx, colIdx, value, x, y, dep);
   else
-    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<false>, Z, rowIdx, colIdx, value, x, y);
+    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<false>, Z, rowIdx, colIdx, value, x, y, dep);
   note_launches(1);
   return err;
 }

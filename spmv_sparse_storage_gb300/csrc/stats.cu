@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
   for (long long r0 = (long long)blockIdx.x * blockDim.x; r0 < R; r0 += stride) {
     const long long r = r0 + threadIdx.x;
     int len = 0;
+    int exactKey = -1, logKey = -1;  // histogram bins, -1 = none
     if (r < R) {
       const int a = rowPtrs[r];
       const int b = rowPtrs[r + 1];
@@ -76,8 +77,8 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       lmin = min(lmin, len);
       empties += (len == 0);
       sq += (unsigned long long)len * (unsigned long long)len;
-      if (len < kExactLenBins) atomicAdd(&sExact[len], 1u);
-      atomicAdd(&sLog2[log2_bin(len)], 1u);
+      exactKey = len < kExactLenBins ? len : -1;
+      logKey = log2_bin(len);
       if (lane == 0) {
         // 32 consecutive rows handled by one warp of a row-per-thread kernel
         const long long e = min(r + 32, (long long)R);
@@ -85,6 +86,12 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
         gmax = max(gmax, g);
       }
     }
+    // warp-aggregated histogram updates: rows of equal length in a warp are
+    // counted by one shared-memory atomic (stencil rows share few lengths)
+    const unsigned pe = __match_any_sync(kFullMask, exactKey);
+    if (exactKey >= 0 && lane == __ffs(pe) - 1) atomicAdd(&sExact[exactKey], (unsigned)__popc(pe));
+    const unsigned pl = __match_any_sync(kFullMask, logKey);
+    if (logKey >= 0 && lane == __ffs(pl) - 1) atomicAdd(&sLog2[logKey], (unsigned)__popc(pl));
   }
   lmax = warp_max(lmax);
   lmin = warp_min(lmin);
@@ -141,34 +148,6 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
   }
 }
 
-// Merge-path split of diagonal d over the merge of the row ends
-// (rowPtrs[1..R]) with the nonzero indices 0..Z-1: returns the number of rows
-// completed before diagonal d (the rest of d are nonzeros). A row end is
-// taken before nonzero j when rowPtrs[i+1] <= j.
-__device__ __forceinline__ int merge_path_rows(long long d, const int* __restrict__ rowPtrs,
-                                               int R, int Z) {
-  long long lo = d - Z > 0 ? d - Z : 0;
-  long long hi = d < R ? d : R;
-  while (lo < hi) {
-    const long long mid = (lo + hi) >> 1;
-    if ((long long)rowPtrs[mid + 1] <= d - 1 - mid)
-      lo = mid + 1;
-    else
-      hi = mid;
-  }
-  return (int)lo;
-}
-
-__global__ void k_csr_partition(int R, int Z, const int* __restrict__ rowPtrs, int nTiles,
-                                int* __restrict__ tileRow) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t > nTiles) return;
-  long long d = (long long)t * kCsrTileItems;
-  const long long total = (long long)R + Z;
-  if (d > total) d = total;
-  tileRow[t] = merge_path_rows(d, rowPtrs, R, Z);
-}
-
 }  // namespace
 
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
@@ -191,15 +170,6 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
     ++n;
   }
   note_launches(n);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_csr_partition(int R, int Z, const int* rowPtrs, int nTiles, int* tileRow,
-                                 cudaStream_t s) {
-  const int threads = 256;
-  const int blocks = (nTiles + 1 + threads - 1) / threads;
-  k_csr_partition<<<blocks, threads, 0, s>>>(R, Z, rowPtrs, nTiles, tileRow);
-  note_launches(1);
   return cudaGetLastError();
 }
 
