@@ -307,6 +307,56 @@ def run_ours(args, rank, world, device):
     return line
 
 
+def run_kernels(args, device):
+    """Per-format SpMV timing on one workload: each rep flushes L2 (writes a
+    buffer of twice its size) outside the timed events, then times one
+    spmv_run with CUDA events on the launching stream; median over reps."""
+    import torch
+    import spmv_sparse_storage_gb300 as sp
+    inp = synth.make_workload(args.workload, seed=0)
+    R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
+    stream = torch.cuda.current_stream(device)
+    rp = torch.from_numpy(inp.row_ptrs).to(device)
+    ci = torch.from_numpy(inp.col_idx).to(device)
+    va = torch.from_numpy(inp.value).to(device)
+    x = torch.from_numpy(inp.x).to(device)
+    y = torch.from_numpy(inp.y0).to(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+    peak, peak_kind = load_peaks()
+    out = {}
+    with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
+        fmts = [f for f in args.formats.split(",") if f]
+        for f in fmts:
+            try:
+                m.convert(f, stream=stream)
+            except sp.SpmvError as e:
+                out[f] = {"error": str(e)}
+        torch.cuda.synchronize(device)
+        for f in fmts:
+            if f in out:
+                continue
+            times = []
+            for rep in range(args.warmup + args.reps):
+                flush.fill_(float(rep))
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                m.run(f, x, y, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                if rep >= args.warmup:
+                    times.append(e0.elapsed_time(e1))
+            ms = float(np.median(times))
+            gbs = compulsory_bytes(R, C, Z) / (ms * 1e-3) / 1e9
+            out[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                      "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1)}
+        sel = m.select()
+    return {"mode": "kernels", "workload": args.workload, "rows": R, "nnz": Z,
+            "l2_flush_bytes": int(flush.numel() * 4), "reps": args.reps, "peak": peak,
+            "peak_kind": peak_kind, "auto": sel, "kernels": out}
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -413,6 +463,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--mode", choices=["step", "kernels"], default="step",
+                    help="step: the whole path (default); kernels: per-format SpMV, cold L2")
+    ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS")
+    ap.add_argument("--reps", type=int, default=50)
     ap.add_argument("--traffic-json", default=None,
                     help="per-call DRAM bytes from an ncu capture (json: call -> bytes)")
     args = ap.parse_args()
@@ -448,6 +502,10 @@ def main():
         spec.loader.exec_module(mod)
         mod.build()
     barrier(world)
+    if args.mode == "kernels":
+        if rank == 0:
+            print(json.dumps(run_kernels(args, device)), flush=True)
+        return
     line = run_ours(args, rank, world, device)
     if rank == 0:
         if not args.no_cpu_baseline:

@@ -315,14 +315,13 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   if (st != SPMV_OK) return fail(st);
   st = alloc_typed(h, 1, s, &dst, tmp);
   if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, s));
-  if (st != SPMV_OK) return fail(st);
-  // nnz-balanced split for the CSR kernel (the kernel checks bounds, so it
-  // stays in bounds even if validation fails below)
+  // nnz-balanced split for the CSR kernel, written by the statistics pass
+  // (which checks bounds, so it stays in bounds even if validation fails)
   h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
   st = alloc_typed(h, (long long)h->nChunks + 1, s, &h->chunkRow, h->csrBufs);
   if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_csr_chunk_rows(numRows, nnz, d_rowPtrs, h->nChunks, h->chunkRow, s));
+  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, h->nChunks,
+                                 h->chunkRow, s));
   if (st != SPMV_OK) return fail(st);
   hst = new (std::nothrow) DevStats;
   if (!hst) return fail(SPMV_ERR_ALLOC);
@@ -350,6 +349,11 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
     S.var_len = (double)(num / Rl / Rl);
   }
   for (int b = 0; b < 33; ++b) S.hist_log2[b] = (int64_t)hst->histLog2[b];
+  for (int L = 0; L < spmv::kExactLenBins; ++L) {
+    int b = 0;
+    while (b < 32 && (1LL << b) <= L) ++b;  // bin 0: len 0; bin b: [2^(b-1), 2^b)
+    S.hist_log2[b] += hst->histExact[L];
+  }
   S.imbalance_thread = S.mean_len > 0 ? (double)S.max_len / S.mean_len : 0.0;
   if (numRows > 0 && nnz > 0) {
     const double groups = (double)((numRows + 31) / 32);
@@ -429,6 +433,12 @@ int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void* stream) {
     }
     kept += (R - counted) * K;
     tail = (long long)h->Z - kept;
+  }
+  if (tail == 0) {  // every row fits in the ELL part: no COO part
+    h->hybK = (int)K;
+    h->hybCooN = 0;
+    h->hasHyb = true;
+    return SPMV_OK;
   }
   std::vector<Buf> tmp;
   int* tailPtr = nullptr;

@@ -13,7 +13,7 @@ namespace spmv {
 // ---------------------------------------------------------------------------
 // Row statistics and validation results, written by the stats kernels.
 // ---------------------------------------------------------------------------
-constexpr int kExactLenBins = 4096;  // exact row-length histogram for len < 4096
+constexpr int kExactLenBins = 1024;  // exact row-length histogram for len < 1024
 
 enum : unsigned {
   kErrRowPtrStart = 1u,     // rowPtrs[0] != 0
@@ -32,7 +32,7 @@ struct DevStats {
   int maxWarpNnz;
   int pad0;
   unsigned long long sumSq;
-  unsigned long long histLog2[33];
+  unsigned long long histLog2[33];  // rows with len >= kExactLenBins only
   unsigned int histExact[kExactLenBins];
 };
 
@@ -40,11 +40,13 @@ struct DevStats {
 // CSR work split: one warp per kCsrChunk consecutive nonzeros.
 // ---------------------------------------------------------------------------
 constexpr int kCsrChunk = 128;
+constexpr int kCsrChunksPerWarp = 4;
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
 constexpr int kJdsTailRows = 256;        // tail blocks: sorted rows per block
 constexpr int kJdsTailDiags = 64;        // tail blocks: diagonals per block
+constexpr int kJdsRowsPerThread = 4;     // row-parallel part: sorted rows per thread
 
 // ---------------------------------------------------------------------------
 // Launch accounting (every launcher reports its kernels).
@@ -55,9 +57,10 @@ int num_sms();
 // ---------------------------------------------------------------------------
 // Launchers. Each returns the cudaError_t of its launches.
 // ---------------------------------------------------------------------------
-// stats.cu
+// stats.cu (also writes chunkRow[0..nChunks] for the CSR kernel:
+// chunkRow[c] = row holding nonzero c*kCsrChunk, chunkRow[nChunks] = numRows-1)
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, cudaStream_t s);
+                         DevStats* st, int nChunks, int* chunkRow, cudaStream_t s);
 
 // convert.cu
 cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s);
@@ -78,9 +81,6 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
                              float* jdsVal, void* scratch, cudaStream_t s);
 
 // spmv_kernels.cu
-// chunkRow[c] = row holding nonzero c*kCsrChunk, chunkRow[nChunks] = numRows-1
-cudaError_t launch_csr_chunk_rows(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
-                                  cudaStream_t s);
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const float* value, const int* chunkRow, const float* x, float* y,
                             cudaStream_t s);

@@ -73,91 +73,120 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // warp ("[CUDA performance tuning] ...", section 2.2); both idle threads when
 // row lengths differ, and the remedy named in "Introduction to sparse
 // computing ...", section "Building the problem framework", is to split the
-// work by nonzero count and to split very long rows. Here every warp takes
-// exactly kCsrChunk = 128 consecutive nonzeros (4 per lane, 16-byte loads of
-// value and colIdx when aligned), whatever rows they belong to: a 5000-entry
-// row spreads over 40 warps, an empty row costs nothing. The rows of a
-// chunk lie between chunkRow[c] and chunkRow[c+1] (computed once at handle
-// creation); each lane finds the row of its first entry by a binary search on
-// rowPtrs in that range (L1-resident after the first lane) and walks forward.
-// The warp then sums runs of equal row with shuffles and adds each run with
-// one atomicAdd, so no warp waits on a read of y.
+// work by nonzero count and to split very long rows. Here the nonzeros are
+// cut into chunks of kCsrChunk = 128 (4 per lane, 16-byte loads of value and
+// colIdx when aligned) whatever rows they belong to: a 5000-entry row spreads
+// over 40 chunks, an empty row costs nothing. A warp takes kCsrChunksPerWarp
+// consecutive chunks and issues all their loads before it waits for any.
+// The rows of chunk c lie in [chunkRow[c], chunkRow[c+1]] (computed once at
+// handle creation); when that range holds at most 32 rows the warp loads
+// their rowPtrs with one coalesced load and each lane finds the row of each
+// of its entries by a 5-step shuffle search, otherwise (very short or empty
+// rows) each lane binary-searches rowPtrs in L1. The warp then sums runs of
+// equal row with shuffles and adds each run with one atomicAdd, so no warp
+// waits on a read of y.
 // ===========================================================================
 template <bool VEC>
-__global__ void __launch_bounds__(256) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
-                                                  const int* __restrict__ colIdx,
-                                                  const float* __restrict__ value,
-                                                  const int* __restrict__ chunkRow,
-                                                  const float* __restrict__ x,
-                                                  float* __restrict__ y) {
+__global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
+                                                     const int* __restrict__ colIdx,
+                                                     const float* __restrict__ value,
+                                                     const int* __restrict__ chunkRow,
+                                                     int nChunks, const float* __restrict__ x,
+                                                     float* __restrict__ y) {
+  constexpr int U = kCsrChunksPerWarp;
   const int lane = threadIdx.x & 31;
-  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long cbase = c * kCsrChunk;
-  if (cbase >= Z) return;  // warp-uniform
-  const int base = (int)cbase + 4 * lane;
+  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long c0 = w * U;
+  if (c0 >= nChunks) return;  // warp-uniform
 
-  int col[4];
-  float v[4];
-  if (VEC && base + 4 <= Z) {
-    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
-    col[0] = c4.x; col[1] = c4.y; col[2] = c4.z; col[3] = c4.w;
-    v[0] = v4.x; v[1] = v4.y; v[2] = v4.z; v[3] = v4.w;
-  } else {
+  // chunk row bounds: lane j holds chunkRow[c0 + j] for j <= U
+  const int crv = lane <= U ? __ldg(chunkRow + min(c0 + lane, (long long)nChunks)) : 0;
+  int col[U][4];
+  float val[U][4];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
+    if (VEC && base + 4 <= Z) {
+      const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
+      const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+      col[u][0] = c4.x; col[u][1] = c4.y; col[u][2] = c4.z; col[u][3] = c4.w;
+      val[u][0] = v4.x; val[u][1] = v4.y; val[u][2] = v4.z; val[u][3] = v4.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const long long k = base + e;
+        col[u][e] = k < Z ? ld_stream(colIdx + k) : 0;
+        val[u][e] = k < Z ? ld_stream(value + k) : 0.0f;
+      }
+    }
+  }
+  // rowPtrs windows (row starts of rows lo .. lo+31) for every chunk
+  int lo[U], span[U], win[U];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    lo[u] = __shfl_sync(kFullMask, crv, u);
+    span[u] = __shfl_sync(kFullMask, crv, u + 1) - lo[u];
+    win[u] = (span[u] < 32 && lane <= span[u]) ? __ldg(rowPtrs + lo[u] + lane) : INT_MAX;
+  }
+  // gathers (products overwrite the values) and row of every entry
+  int row[U][4];
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
+    const bool live = c0 + u < nChunks;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int k = base + e;
-      col[e] = k < Z ? ld_stream(colIdx + k) : 0;
-      v[e] = k < Z ? ld_stream(value + k) : 0.0f;
+      const bool in = live && base + e < Z;
+      val[u][e] = in ? val[u][e] * ld_x(x + col[u][e]) : 0.0f;
     }
-  }
-  const int lo = __ldg(chunkRow + c);
-  const int hi = __ldg(chunkRow + c + 1);
-  // largest r in [lo, hi] with rowPtrs[r] <= base (rowPtrs[lo] <= chunk start)
-  int r = lo;
-  if (lo < hi && base < Z) {
-    int b = hi;
-    while (r < b) {
-      const int m = (r + b + 1) >> 1;
-      if (__ldg(rowPtrs + m) <= base)
-        r = m;
-      else
-        b = m - 1;
-    }
-  }
-  int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-  int row[4];
-  float p[4];
+    if (span[u] < 32) {
+      // shuffle search: rows lo..lo+span have their starts in lanes 0..span
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int k = base + e;
-    while (k >= nextStart) {  // skips empty rows; bounded by hi
-      ++r;
-      nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+      for (int e = 0; e < 4; ++e) {
+        const int k = (int)(base + e);
+        int idx = 0;
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const int cand = idx + step;
+          const int sc = __shfl_sync(kFullMask, win[u], cand & 31);
+          if (cand <= span[u] && sc <= k) idx = cand;
+        }
+        row[u][e] = (live && base + e < Z) ? lo[u] + idx : -1;
+      }
+    } else {
+      // many short or empty rows: binary search on rowPtrs, then walk
+      const int hi = lo[u] + span[u];
+      int r = lo[u];
+      if (live && base < Z) {
+        int b = hi;
+        while (r < b) {
+          const int m = (r + b + 1) >> 1;
+          if (__ldg(rowPtrs + m) <= (int)base)
+            r = m;
+          else
+            b = m - 1;
+        }
+      }
+      int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const long long k = base + e;
+        while (k >= nextStart) {  // skips empty rows; bounded by hi
+          ++r;
+          nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+        }
+        row[u][e] = (live && k < Z) ? r : -1;
+      }
     }
-    row[e] = k < Z ? r : -1;
-    p[e] = k < Z ? v[e] * ld_x(x + col[e]) : 0.0f;
   }
-  warp_segmented_add(row, p, y, false);
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    if (c0 + u < nChunks) warp_segmented_add(row[u], val[u], y, false);
+  }
 }
 
-// chunkRow[c] = the row holding nonzero c*kCsrChunk (c < nChunks) and
-// chunkRow[nChunks] = numRows - 1. A row writes the entries of the chunks
-// that start inside it. Bounds are checked so that this kernel, which runs
-// before the validation result is read, stays in bounds on invalid input.
-__global__ void k_csr_chunk_rows(int R, int Z, const int* __restrict__ rowPtrs, int nChunks,
-                                 int* __restrict__ chunkRow) {
-  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r == 0) chunkRow[nChunks] = R > 0 ? R - 1 : 0;
-  if (r >= R) return;
-  const int a = rowPtrs[r];
-  const int b = rowPtrs[r + 1];
-  if (a < 0 || b > Z || b <= a) return;
-  const int c0 = (a + kCsrChunk - 1) / kCsrChunk;
-  int c1 = (b - 1) / kCsrChunk;
-  if (c1 > nChunks - 1) c1 = nChunks - 1;
-  for (int cc = c0; cc <= c1; ++cc) chunkRow[cc] = (int)r;
-}
+// chunkRow[c] = the row holding nonzero c*kCsrChunk (c < nChunks) is written
+// by the row statistics pass (stats.cu); chunkRow[nChunks] = numRows - 1.
 
 // ===========================================================================
 // ELL ("Regularized Formats ...", section "ELL format: padding +
@@ -289,15 +318,16 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // s < width(t), contiguous in s, so a warp's loads are coalesced. Widths only
 // shrink with t; the first tSplit diagonals (those at least
 // kJdsSplitMinWidth wide, at most kJdsSplitMaxDiag of them) run one thread
-// per sorted row, which issues the loads of up to 8 diagonals and of perm[s]
-// before it waits for any of them. The remaining diagonals belong to the few
+// per sorted row (kJdsRowsPerThread rows per thread, 256 rows apart so that
+// every load instruction stays coalesced), with the loads of 4 diagonals of
+// all its rows in flight at once. The remaining diagonals belong to the few
 // longest rows (s < wTail) and would serialise one thread over thousands of
 // entries, so they are split into blocks of kJdsTailRows rows x
 // kJdsTailDiags diagonals that run in parallel and add their partial sums
 // atomically. The result of sorted row s goes straight to y[perm[s]] (the
 // page permutes the result back with the row array).
 // ===========================================================================
-__global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
+__global__ void __launch_bounds__(256, 3) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
                                                      const int* __restrict__ perm,
@@ -309,39 +339,63 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
   if ((int)blockIdx.x < nMainBlocks) {
     for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
     __syncthreads();
-    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (s >= R) return;
-    const int r = ld_stream(perm + s);
-    // number of leading diagonals wider than s (binary search; widths shrink)
-    int lo = 0, hi = tSplit;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (sIp[mid + 1] - sIp[mid] > s)
-        lo = mid + 1;
-      else
-        hi = mid;
-    }
-    const int n = lo;
-    float acc = 0.0f;
-    for (int t = 0; t < n; t += 8) {
-      int c[8];
-      float v[8];
+    constexpr int U = kJdsRowsPerThread;
+    const long long s0 = (long long)blockIdx.x * blockDim.x * U + threadIdx.x;
+    int r[U], n[U];
+    float acc[U], y0[U];
+    int nmax = 0;
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        if (t + u < n) {
-          const long long i = (long long)sIp[t + u] + s;
-          c[u] = ld_stream(jdsCol + i);
-          v[u] = ld_stream(jdsVal + i);
+    for (int u = 0; u < U; ++u) {
+      const long long s = s0 + (long long)u * blockDim.x;
+      r[u] = s < R ? ld_stream(perm + s) : -1;
+      // number of leading diagonals wider than s (binary search; widths shrink)
+      int lo = 0, hi = s < R ? tSplit : 0;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sIp[mid + 1] - sIp[mid] > s)
+          lo = mid + 1;
+        else
+          hi = mid;
+      }
+      n[u] = lo;
+      nmax = max(nmax, lo);
+      acc[u] = 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long s = s0 + (long long)u * blockDim.x;
+      y0[u] = (r[u] >= 0 && s >= wTail) ? y[r[u]] : 0.0f;
+    }
+    for (int t = 0; t < nmax; t += 4) {
+      int c[U][4];
+      float v[U][4];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const long long s = s0 + (long long)u * blockDim.x;
+#pragma unroll
+        for (int d = 0; d < 4; ++d) {
+          if (t + d < n[u]) {
+            const long long i = (long long)sIp[t + d] + s;
+            c[u][d] = ld_stream(jdsCol + i);
+            v[u][d] = ld_stream(jdsVal + i);
+          }
         }
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (t + u < n) acc = fmaf(v[u], ld_x(x + c[u]), acc);
+      for (int u = 0; u < U; ++u)
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+          if (t + d < n[u]) acc[u] = fmaf(v[u][d], ld_x(x + c[u][d]), acc[u]);
     }
-    if (s < wTail)
-      atomicAdd(y + r, acc);  // the tail blocks add to this row too
-    else
-      y[r] += acc;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long s = s0 + (long long)u * blockDim.x;
+      if (r[u] < 0) continue;
+      if (s < wTail)
+        atomicAdd(y + r[u], acc[u]);  // the tail blocks add to this row too
+      else
+        y[r[u]] = y0[u] + acc[u];
+    }
   } else {
     const int b = blockIdx.x - nMainBlocks;
     const int rb = b % tailRowBlocks;
@@ -366,25 +420,20 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
 
 }  // namespace
 
-cudaError_t launch_csr_chunk_rows(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
-                                  cudaStream_t s) {
-  const long long n = R > 0 ? R : 1;
-  k_csr_chunk_rows<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(R, Z, rowPtrs, nChunks, chunkRow);
-  note_launches(1);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const float* value, const int* chunkRow, const float* x, float* y,
                             cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long chunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long blocks = (chunks * 32 + 255) / 256;
+  const long long warps = (chunks + kCsrChunksPerWarp - 1) / kCsrChunksPerWarp;
+  const long long blocks = (warps * 32 + 255) / 256;
   const bool vec = aligned16(colIdx) && aligned16(value);
   if (vec)
-    k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow, x, y);
+    k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
+                                                      (int)chunks, x, y);
   else
-    k_spmv_csr<false><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow, x, y);
+    k_spmv_csr<false><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
+                                                       (int)chunks, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -433,7 +482,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
                             const int* perm, const int* jdsCol, const float* jdsVal,
                             const float* x, float* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
-  const long long mainBlocks = ((long long)R + 255) / 256;
+  const long long mainBlocks = ((long long)R + 256 * kJdsRowsPerThread - 1) / (256 * kJdsRowsPerThread);
   long long tailBlocks = 0;
   int tailRowBlocks = 1;
   if (tSplit < maxLen && wTail > 0) {

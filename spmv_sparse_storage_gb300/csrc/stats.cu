@@ -1,5 +1,5 @@
 // stats.cu -- input validation, row-length statistics and the nnz-balanced
-// CSR partition, all on the device.
+// CSR chunk map, all on the device.
 //
 // Validation follows the sanity rules of "Sparse matrix multiplication
 // acceleration techniques", section 5.3: row_ptr must be monotone, every
@@ -33,16 +33,19 @@ __global__ void k_stats_init(DevStats* st) {
   }
 }
 
-__device__ __forceinline__ int log2_bin(int len) {
-  // bin 0: len 0; bin b >= 1: len in [2^(b-1), 2^b)
-  return len <= 0 ? 0 : 32 - __clz(len);
-}
+// One pass over rowPtrs: monotonicity, endpoints, lengths, histograms, and
+// the CSR chunk map (chunkRow[c] = row holding nonzero c*kCsrChunk). A block
+// takes kStatsRows consecutive rows, kStatsRowsPerThread per thread, 256
+// apart so that each load instruction is coalesced, and issues all its loads
+// before it uses any. Lengths below kExactLenBins go to an exact histogram
+// (their log2 bins are derived from it on the host); longer rows are counted
+// in the log2 bins directly.
+constexpr int kStatsRowsPerThread = 8;
+constexpr int kStatsRows = 256 * kStatsRowsPerThread;
 
-// One pass over rowPtrs: monotonicity, endpoints, lengths, histograms.
-// Grid-stride over rows; block size 256 (a multiple of 32, so that each warp
-// sees 32 consecutive rows and its lane 0 owns one 32-row group).
 __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __restrict__ rowPtrs,
-                                                   DevStats* __restrict__ st) {
+                                                   DevStats* __restrict__ st, int nChunks,
+                                                   int* __restrict__ chunkRow) {
   __shared__ unsigned int sExact[kExactLenBins];
   __shared__ unsigned int sLog2[33];
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) sExact[i] = 0u;
@@ -52,46 +55,50 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (rowPtrs[0] != 0) atomicOr(&st->err, kErrRowPtrStart);
     if (rowPtrs[R] != Z) atomicOr(&st->err, kErrRowPtrEnd);
+    chunkRow[nChunks] = R > 0 ? R - 1 : 0;
   }
-
+  const int lane = threadIdx.x & 31;
+  const long long base = (long long)blockIdx.x * kStatsRows + threadIdx.x;
+  int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
+#pragma unroll
+  for (int i = 0; i < kStatsRowsPerThread; ++i) {
+    const long long r = base + i * 256;
+    a[i] = r < R ? rowPtrs[r] : 0;
+    b[i] = r < R ? rowPtrs[r + 1] : 0;
+    // 32 consecutive rows handled by one warp of a row-per-thread kernel
+    g[i] = (r < R && lane == 0) ? rowPtrs[min(r + 32, (long long)R)] : 0;
+  }
   int lmax = 0, lmin = INT_MAX, empties = 0, gmax = 0;
   unsigned long long sq = 0ull;
-  bool bad = false;
   int firstBad = INT_MAX;
-  const int lane = threadIdx.x & 31;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long r0 = (long long)blockIdx.x * blockDim.x; r0 < R; r0 += stride) {
-    const long long r = r0 + threadIdx.x;
+#pragma unroll
+  for (int i = 0; i < kStatsRowsPerThread; ++i) {
+    const long long r = base + i * 256;
+    const bool live = r < R;
     int len = 0;
-    int exactKey = -1, logKey = -1;  // histogram bins, -1 = none
-    if (r < R) {
-      const int a = rowPtrs[r];
-      const int b = rowPtrs[r + 1];
-      if (b < a) {
-        bad = true;
+    if (live) {
+      if (b[i] < a[i])
         firstBad = min(firstBad, (int)r);
-      } else {
-        len = b - a;
-      }
+      else
+        len = b[i] - a[i];
       lmax = max(lmax, len);
       lmin = min(lmin, len);
       empties += (len == 0);
       sq += (unsigned long long)len * (unsigned long long)len;
-      exactKey = len < kExactLenBins ? len : -1;
-      logKey = log2_bin(len);
-      if (lane == 0) {
-        // 32 consecutive rows handled by one warp of a row-per-thread kernel
-        const long long e = min(r + 32, (long long)R);
-        const int g = rowPtrs[e] - a;
-        gmax = max(gmax, g);
+      if (lane == 0) gmax = max(gmax, g[i] - a[i]);
+      if (len >= kExactLenBins) atomicAdd(&sLog2[32 - __clz(len)], 1u);
+      // chunks whose first nonzero lies in this row (bounds-checked: runs
+      // before the validation result is known)
+      if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
+        const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
+        const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
+        for (int c = c0; c <= c1; ++c) chunkRow[c] = (int)r;
       }
     }
-    // warp-aggregated histogram updates: rows of equal length in a warp are
-    // counted by one shared-memory atomic (stencil rows share few lengths)
-    const unsigned pe = __match_any_sync(kFullMask, exactKey);
-    if (exactKey >= 0 && lane == __ffs(pe) - 1) atomicAdd(&sExact[exactKey], (unsigned)__popc(pe));
-    const unsigned pl = __match_any_sync(kFullMask, logKey);
-    if (logKey >= 0 && lane == __ffs(pl) - 1) atomicAdd(&sLog2[logKey], (unsigned)__popc(pl));
+    // warp-aggregated exact histogram: one shared atomic per distinct length
+    const int key = (live && len < kExactLenBins) ? len : -1;
+    const unsigned peers = __match_any_sync(kFullMask, key);
+    if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
   }
   lmax = warp_max(lmax);
   lmin = warp_min(lmin);
@@ -104,7 +111,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
     if (sq) atomicAdd(&st->sumSq, sq);
     if (gmax > 0) atomicMax(&st->maxWarpNnz, gmax);
   }
-  if (bad) {
+  if (firstBad != INT_MAX) {
     atomicOr(&st->err, kErrRowPtrDecrease);
     atomicMin(&st->firstBadRow, firstBad);
   }
@@ -151,12 +158,11 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
 }  // namespace
 
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, cudaStream_t s) {
+                         DevStats* st, int nChunks, int* chunkRow, cudaStream_t s) {
   k_stats_init<<<1, 256, 0, s>>>(st);
   const int sms = num_sms();
-  long long rb = ((long long)R + 255) / 256;
-  int gridR = (int)(rb < 1 ? 1 : (rb > 8LL * sms ? 8LL * sms : rb));
-  k_row_stats<<<gridR, 256, 0, s>>>(R, Z, rowPtrs, st);
+  const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
+  k_row_stats<<<(unsigned)(rb < 1 ? 1 : rb), 256, 0, s>>>(R, Z, rowPtrs, st, nChunks, chunkRow);
   int n = 2;
   if (Z > 0) {
     const bool vec = aligned16(colIdx);
