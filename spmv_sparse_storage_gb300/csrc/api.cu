@@ -315,13 +315,16 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   if (st != SPMV_OK) return fail(st);
   st = alloc_typed(h, 1, s, &dst, tmp);
   if (st != SPMV_OK) return fail(st);
+  void* statsScratch = nullptr;
+  st = h->alloc(spmv::stats_scratch_bytes(numRows), s, &statsScratch, tmp);
+  if (st != SPMV_OK) return fail(st);
   // nnz-balanced split for the CSR kernel, written by the statistics pass
   // (which checks bounds, so it stays in bounds even if validation fails)
   h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
   st = alloc_typed(h, (long long)h->nChunks + 1, s, &h->chunkRow, h->csrBufs);
   if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, h->nChunks,
-                                 h->chunkRow, s));
+  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, statsScratch,
+                                 h->nChunks, h->chunkRow, s));
   if (st != SPMV_OK) return fail(st);
   hst = new (std::nothrow) DevStats;
   if (!hst) return fail(SPMV_ERR_ALLOC);

@@ -36,6 +36,17 @@ struct DevStats {
   unsigned int histExact[kExactLenBins];
 };
 
+// Work space of the statistics pass (device): per-block partial results and
+// kStatsReplicas copies of the exact histogram, so that no two blocks of a
+// large matrix update one address; a final one-block kernel folds them into
+// DevStats.
+constexpr int kStatsReplicas = 32;
+struct StatsPartial {
+  int maxLen, minLen, emptyRows, maxWarpNnz, firstBadRow, pad0;
+  unsigned long long sumSq;
+};
+size_t stats_scratch_bytes(int R);
+
 // ---------------------------------------------------------------------------
 // CSR work split: one warp per kCsrChunk consecutive nonzeros.
 // ---------------------------------------------------------------------------
@@ -60,7 +71,8 @@ int num_sms();
 // stats.cu (also writes chunkRow[0..nChunks] for the CSR kernel:
 // chunkRow[c] = row holding nonzero c*kCsrChunk, chunkRow[nChunks] = numRows-1)
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, int nChunks, int* chunkRow, cudaStream_t s);
+                         DevStats* st, void* scratch, int nChunks, int* chunkRow,
+                         cudaStream_t s);
 
 // convert.cu
 cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s);

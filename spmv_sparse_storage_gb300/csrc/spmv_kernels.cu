@@ -79,10 +79,11 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // over 40 chunks, an empty row costs nothing. A warp takes kCsrChunksPerWarp
 // consecutive chunks and issues all their loads before it waits for any.
 // The rows of chunk c lie in [chunkRow[c], chunkRow[c+1]] (computed once at
-// handle creation); when that range holds at most 32 rows the warp loads
-// their rowPtrs with one coalesced load and each lane finds the row of each
-// of its entries by a 5-step shuffle search, otherwise (very short or empty
-// rows) each lane binary-searches rowPtrs in L1. The warp then sums runs of
+// handle creation); when that range holds at most 32 rows, none empty, the
+// warp loads their rowPtrs with one coalesced load, builds a 128-bit mask of
+// the positions where rows start (four warp OR-reductions) and each lane
+// counts the set bits before each of its entries (popcount) to get its row;
+// otherwise (very short or empty rows) each lane binary-searches rowPtrs in L1. The warp then sums runs of
 // equal row with shuffles and adds each run with one atomicAdd, so no warp
 // waits on a read of y.
 // ===========================================================================
@@ -132,26 +133,38 @@ __global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __
   int row[U][4];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
+    const long long cb = (c0 + u) * kCsrChunk;
+    const long long base = cb + 4 * lane;
     const bool live = c0 + u < nChunks;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const bool in = live && base + e < Z;
       val[u][e] = in ? val[u][e] * ld_x(x + col[u][e]) : 0.0f;
     }
-    if (span[u] < 32) {
-      // shuffle search: rows lo..lo+span have their starts in lanes 0..span
+    // fast path: the chunk's rows fit one window and none of them is empty,
+    // so every row after lo starts at a distinct position of the chunk
+    const int prevStart = __shfl_up_sync(kFullMask, win[u], 1);
+    const bool emptyRow = lane >= 1 && lane <= span[u] && win[u] == prevStart;
+    if (span[u] < 32 && !__any_sync(kFullMask, emptyRow)) {
+      // head mask: bit p set when a row lo+j (j >= 1) starts at chunk position p
+      const long long pos = (long long)win[u] - cb;
+      const bool head = lane >= 1 && lane <= span[u] && pos >= 0 && pos < kCsrChunk;
+      const int pw = head ? (int)(pos >> 5) : -1;
+      const unsigned bit = head ? 1u << (pos & 31) : 0u;
+      const unsigned m0 = __reduce_or_sync(kFullMask, pw == 0 ? bit : 0u);
+      const unsigned m1 = __reduce_or_sync(kFullMask, pw == 1 ? bit : 0u);
+      const unsigned m2 = __reduce_or_sync(kFullMask, pw == 2 ? bit : 0u);
+      const unsigned m3 = __reduce_or_sync(kFullMask, pw == 3 ? bit : 0u);
+      // lane's entries 4*lane .. 4*lane+3 sit in word lane/8, bits 4*(lane%8)+e
+      const int wd = lane >> 3;
+      const unsigned mw = wd == 0 ? m0 : wd == 1 ? m1 : wd == 2 ? m2 : m3;
+      const int before = (wd > 0 ? __popc(m0) : 0) + (wd > 1 ? __popc(m1) : 0) +
+                         (wd > 2 ? __popc(m2) : 0);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int k = (int)(base + e);
-        int idx = 0;
-#pragma unroll
-        for (int step = 16; step >= 1; step >>= 1) {
-          const int cand = idx + step;
-          const int sc = __shfl_sync(kFullMask, win[u], cand & 31);
-          if (cand <= span[u] && sc <= k) idx = cand;
-        }
-        row[u][e] = (live && base + e < Z) ? lo[u] + idx : -1;
+        const int b = 4 * (lane & 7) + e;
+        const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
+        row[u][e] = (live && base + e < Z) ? lo[u] + before + __popc(mw & upto) : -1;
       }
     } else {
       // many short or empty rows: binary search on rowPtrs, then walk

@@ -17,19 +17,26 @@
 namespace spmv {
 namespace {
 
-__global__ void k_stats_init(DevStats* st) {
-  for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) st->histExact[i] = 0u;
-  if (threadIdx.x < 33) st->histLog2[threadIdx.x] = 0ull;
-  if (threadIdx.x == 0) {
-    st->err = 0u;
-    st->firstBadRow = INT_MAX;
-    st->firstBadNnz = INT_MAX;
-    st->maxLen = 0;
-    st->minLen = INT_MAX;
-    st->emptyRows = 0;
-    st->maxWarpNnz = 0;
-    st->pad0 = 0;
-    st->sumSq = 0ull;
+constexpr int kStatsRowsPerThread = 8;
+constexpr int kStatsRows = 256 * kStatsRowsPerThread;
+
+__global__ void k_stats_init(DevStats* st, unsigned* histRep) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  for (int i = t; i < kStatsReplicas * kExactLenBins; i += gridDim.x * blockDim.x) histRep[i] = 0u;
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) st->histExact[i] = 0u;
+    if (threadIdx.x < 33) st->histLog2[threadIdx.x] = 0ull;
+    if (threadIdx.x == 0) {
+      st->err = 0u;
+      st->firstBadRow = INT_MAX;
+      st->firstBadNnz = INT_MAX;
+      st->maxLen = 0;
+      st->minLen = INT_MAX;
+      st->emptyRows = 0;
+      st->maxWarpNnz = 0;
+      st->pad0 = 0;
+      st->sumSq = 0ull;
+    }
   }
 }
 
@@ -37,19 +44,20 @@ __global__ void k_stats_init(DevStats* st) {
 // the CSR chunk map (chunkRow[c] = row holding nonzero c*kCsrChunk). A block
 // takes kStatsRows consecutive rows, kStatsRowsPerThread per thread, 256
 // apart so that each load instruction is coalesced, and issues all its loads
-// before it uses any. Lengths below kExactLenBins go to an exact histogram
-// (their log2 bins are derived from it on the host); longer rows are counted
-// in the log2 bins directly.
-constexpr int kStatsRowsPerThread = 8;
-constexpr int kStatsRows = 256 * kStatsRowsPerThread;
-
+// before it uses any. The block's maxima, minima and sums go to its own
+// partial record (no atomics); lengths below kExactLenBins are counted in a
+// shared histogram that is added to one of kStatsReplicas global copies;
+// longer rows are counted in the log2 bins directly (their log2 bins for
+// shorter rows are derived on the host from the exact histogram).
 __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __restrict__ rowPtrs,
-                                                   DevStats* __restrict__ st, int nChunks,
+                                                   DevStats* __restrict__ st,
+                                                   StatsPartial* __restrict__ partials,
+                                                   unsigned* __restrict__ histRep, int nChunks,
                                                    int* __restrict__ chunkRow) {
   __shared__ unsigned int sExact[kExactLenBins];
-  __shared__ unsigned int sLog2[33];
+  __shared__ int sRed[5][8];
+  __shared__ unsigned long long sSq[8];
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) sExact[i] = 0u;
-  if (threadIdx.x < 33) sLog2[threadIdx.x] = 0u;
   __syncthreads();
 
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -57,7 +65,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
     if (rowPtrs[R] != Z) atomicOr(&st->err, kErrRowPtrEnd);
     chunkRow[nChunks] = R > 0 ? R - 1 : 0;
   }
-  const int lane = threadIdx.x & 31;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long long base = (long long)blockIdx.x * kStatsRows + threadIdx.x;
   int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
 #pragma unroll
@@ -86,7 +94,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       empties += (len == 0);
       sq += (unsigned long long)len * (unsigned long long)len;
       if (lane == 0) gmax = max(gmax, g[i] - a[i]);
-      if (len >= kExactLenBins) atomicAdd(&sLog2[32 - __clz(len)], 1u);
+      if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
       // chunks whose first nonzero lies in this row (bounds-checked: runs
       // before the validation result is known)
       if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
@@ -104,22 +112,95 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
   lmin = warp_min(lmin);
   empties = warp_sum(empties);
   sq = warp_sum(sq);
+  gmax = warp_max(gmax);
+  firstBad = warp_min(firstBad);
   if (lane == 0) {
-    if (lmax > 0) atomicMax(&st->maxLen, lmax);
-    if (lmin != INT_MAX) atomicMin(&st->minLen, lmin);
-    if (empties) atomicAdd(&st->emptyRows, empties);
-    if (sq) atomicAdd(&st->sumSq, sq);
-    if (gmax > 0) atomicMax(&st->maxWarpNnz, gmax);
-  }
-  if (firstBad != INT_MAX) {
-    atomicOr(&st->err, kErrRowPtrDecrease);
-    atomicMin(&st->firstBadRow, firstBad);
+    sRed[0][wid] = lmax;
+    sRed[1][wid] = lmin;
+    sRed[2][wid] = empties;
+    sRed[3][wid] = gmax;
+    sRed[4][wid] = firstBad;
+    sSq[wid] = sq;
   }
   __syncthreads();
+  if (threadIdx.x == 0) {
+    StatsPartial p;
+    p.maxLen = 0; p.minLen = INT_MAX; p.emptyRows = 0; p.maxWarpNnz = 0;
+    p.firstBadRow = INT_MAX; p.pad0 = 0; p.sumSq = 0ull;
+    for (int w = 0; w < 8; ++w) {
+      p.maxLen = max(p.maxLen, sRed[0][w]);
+      p.minLen = min(p.minLen, sRed[1][w]);
+      p.emptyRows += sRed[2][w];
+      p.maxWarpNnz = max(p.maxWarpNnz, sRed[3][w]);
+      p.firstBadRow = min(p.firstBadRow, sRed[4][w]);
+      p.sumSq += sSq[w];
+    }
+    partials[blockIdx.x] = p;
+  }
+  unsigned* rep = histRep + (size_t)(blockIdx.x % kStatsReplicas) * kExactLenBins;
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x)
-    if (sExact[i]) atomicAdd(&st->histExact[i], sExact[i]);
-  if (threadIdx.x < 33 && sLog2[threadIdx.x])
-    atomicAdd(&st->histLog2[threadIdx.x], (unsigned long long)sLog2[threadIdx.x]);
+    if (sExact[i]) atomicAdd(rep + i, sExact[i]);
+}
+
+// Fold the per-block partials and the histogram replicas into DevStats.
+__global__ void __launch_bounds__(1024) k_stats_reduce(int nBlocks,
+                                                       const StatsPartial* __restrict__ partials,
+                                                       const unsigned* __restrict__ histRep,
+                                                       DevStats* __restrict__ st) {
+  __shared__ int sRed[5][32];
+  __shared__ unsigned long long sSq[32];
+  for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) {
+    unsigned v = 0u;
+    for (int r = 0; r < kStatsReplicas; ++r) v += histRep[(size_t)r * kExactLenBins + i];
+    st->histExact[i] = v;
+  }
+  int mx = 0, mn = INT_MAX, emp = 0, gm = 0, fb = INT_MAX;
+  unsigned long long sq = 0ull;
+  for (int i = threadIdx.x; i < nBlocks; i += blockDim.x) {
+    const StatsPartial p = partials[i];
+    mx = max(mx, p.maxLen);
+    mn = min(mn, p.minLen);
+    emp += p.emptyRows;
+    gm = max(gm, p.maxWarpNnz);
+    fb = min(fb, p.firstBadRow);
+    sq += p.sumSq;
+  }
+  mx = warp_max(mx);
+  mn = warp_min(mn);
+  emp = warp_sum(emp);
+  gm = warp_max(gm);
+  fb = warp_min(fb);
+  sq = warp_sum(sq);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) {
+    sRed[0][wid] = mx; sRed[1][wid] = mn; sRed[2][wid] = emp; sRed[3][wid] = gm; sRed[4][wid] = fb;
+    sSq[wid] = sq;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int nw = blockDim.x / 32;
+    for (int w = 0; w < nw; ++w) {
+      mx = max(mx, sRed[0][w]);
+      mn = min(mn, sRed[1][w]);
+      gm = max(gm, sRed[3][w]);
+      fb = min(fb, sRed[4][w]);
+    }
+    emp = 0;
+    sq = 0ull;
+    for (int w = 0; w < nw; ++w) {
+      emp += sRed[2][w];
+      sq += sSq[w];
+    }
+    st->maxLen = mx;
+    st->minLen = mn;
+    st->emptyRows = emp;
+    st->maxWarpNnz = gm;
+    st->sumSq = sq;
+    if (fb != INT_MAX) {
+      st->err |= kErrRowPtrDecrease;
+      st->firstBadRow = fb;
+    }
+  }
 }
 
 // Every column index must satisfy 0 <= c < numCols (unsigned compare catches
@@ -157,13 +238,24 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
 
 }  // namespace
 
+size_t stats_scratch_bytes(int R) {
+  const long long nb = ((long long)R + kStatsRows - 1) / kStatsRows;
+  return (size_t)(nb < 1 ? 1 : nb) * sizeof(StatsPartial) +
+         (size_t)kStatsReplicas * kExactLenBins * sizeof(unsigned);
+}
+
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, int nChunks, int* chunkRow, cudaStream_t s) {
-  k_stats_init<<<1, 256, 0, s>>>(st);
-  const int sms = num_sms();
+                         DevStats* st, void* scratch, int nChunks, int* chunkRow,
+                         cudaStream_t s) {
   const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
-  k_row_stats<<<(unsigned)(rb < 1 ? 1 : rb), 256, 0, s>>>(R, Z, rowPtrs, st, nChunks, chunkRow);
-  int n = 2;
+  const int nb = (int)(rb < 1 ? 1 : rb);
+  unsigned* histRep = static_cast<unsigned*>(scratch);
+  StatsPartial* partials =
+      reinterpret_cast<StatsPartial*>(histRep + (size_t)kStatsReplicas * kExactLenBins);
+  k_stats_init<<<32, 256, 0, s>>>(st, histRep);
+  k_row_stats<<<nb, 256, 0, s>>>(R, Z, rowPtrs, st, partials, histRep, nChunks, chunkRow);
+  int n = 3;
+  const int sms = num_sms();
   if (Z > 0) {
     const bool vec = aligned16(colIdx);
     long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
@@ -175,6 +267,7 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
       k_col_check<false><<<gridC, 256, 0, s>>>(Z, C, colIdx, st);
     ++n;
   }
+  k_stats_reduce<<<1, 1024, 0, s>>>(nb, partials, histRep, st);
   note_launches(n);
   return cudaGetLastError();
 }
