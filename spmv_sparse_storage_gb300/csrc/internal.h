@@ -51,7 +51,7 @@ size_t stats_scratch_bytes(int R);
 // CSR work split: one warp per kCsrChunk consecutive nonzeros.
 // ---------------------------------------------------------------------------
 constexpr int kCsrChunk = 128;
-constexpr int kCsrChunksPerWarp = 4;
+constexpr int kCsrChunksPerWarp = 2;
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
@@ -93,9 +93,13 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
                              float* jdsVal, void* scratch, cudaStream_t s);
 
 // spmv_kernels.cu
+// chunkMask[c] (bit p: a row starts at position p of chunk c) and the
+// empty-row flag in the sign bit of chunkRow[c]; runs after the stats pass
+cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
+                                   uint4* chunkMask, cudaStream_t s);
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* chunkRow, const float* x, float* y,
-                            cudaStream_t s);
+                            const float* value, const int* chunkRow, const uint4* chunkMask,
+                            const float* x, float* y, cudaStream_t s);
 cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,

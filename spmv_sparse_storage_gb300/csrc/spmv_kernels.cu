@@ -78,20 +78,25 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // colIdx when aligned) whatever rows they belong to: a 5000-entry row spreads
 // over 40 chunks, an empty row costs nothing. A warp takes kCsrChunksPerWarp
 // consecutive chunks and issues all their loads before it waits for any.
-// The rows of chunk c lie in [chunkRow[c], chunkRow[c+1]] (computed once at
-// handle creation); when that range holds at most 32 rows, none empty, the
-// warp loads their rowPtrs with one coalesced load, builds a 128-bit mask of
-// the positions where rows start (four warp OR-reductions) and each lane
-// counts the set bits before each of its entries (popcount) to get its row;
-// otherwise (very short or empty rows) each lane binary-searches rowPtrs in L1. The warp then sums runs of
-// equal row with shuffles and adds each run with one atomicAdd, so no warp
-// waits on a read of y.
+//
+// Row ids come from an index built once at handle creation (the row
+// statistics pass and k_csr_chunk_masks): chunkRow[c] = the row holding the
+// chunk's first nonzero, and chunkMask[c] = a 128-bit mask of the chunk
+// positions where a later row starts. The row of entry p is chunkRow[c] plus
+// the number of mask bits at positions <= p (popcounts), so the kernel reads
+// 0.125 byte of index per nonzero and never waits on rowPtrs. A chunk in
+// which an empty row sits (the sign bit of chunkRow[c] marks it) takes the
+// general path instead: each lane binary-searches rowPtrs for its first
+// entry's row and walks forward. The warp then sums runs of equal row with
+// shuffles and adds each run with one atomicAdd, so no warp waits on a read
+// of y either.
 // ===========================================================================
 template <bool VEC>
 __global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
                                                      const float* __restrict__ value,
                                                      const int* __restrict__ chunkRow,
+                                                     const uint4* __restrict__ chunkMask,
                                                      int nChunks, const float* __restrict__ x,
                                                      float* __restrict__ y) {
   constexpr int U = kCsrChunksPerWarp;
@@ -100,12 +105,15 @@ __global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __
   const long long c0 = w * U;
   if (c0 >= nChunks) return;  // warp-uniform
 
-  // chunk row bounds: lane j holds chunkRow[c0 + j] for j <= U
-  const int crv = lane <= U ? __ldg(chunkRow + min(c0 + lane, (long long)nChunks)) : 0;
   int col[U][4];
   float val[U][4];
+  int loF[U];
+  uint4 mask[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
+    const long long c = c0 + u < nChunks ? c0 + u : nChunks - 1;
+    loF[u] = __ldg(chunkRow + c);  // same address in every lane: one request
+    mask[u] = __ldg(chunkMask + c);
     const long long base = (c0 + u) * kCsrChunk + 4 * lane;
     if (VEC && base + 4 <= Z) {
       const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
@@ -121,56 +129,33 @@ __global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __
       }
     }
   }
-  // rowPtrs windows (row starts of rows lo .. lo+31) for every chunk
-  int lo[U], span[U], win[U];
 #pragma unroll
   for (int u = 0; u < U; ++u) {
-    lo[u] = __shfl_sync(kFullMask, crv, u);
-    span[u] = __shfl_sync(kFullMask, crv, u + 1) - lo[u];
-    win[u] = (span[u] < 32 && lane <= span[u]) ? __ldg(rowPtrs + lo[u] + lane) : INT_MAX;
-  }
-  // gathers (products overwrite the values) and row of every entry
-  int row[U][4];
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const long long cb = (c0 + u) * kCsrChunk;
-    const long long base = cb + 4 * lane;
     const bool live = c0 + u < nChunks;
+    if (!live) break;  // warp-uniform
+    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const bool in = live && base + e < Z;
-      val[u][e] = in ? val[u][e] * ld_x(x + col[u][e]) : 0.0f;
-    }
-    // fast path: the chunk's rows fit one window and none of them is empty,
-    // so every row after lo starts at a distinct position of the chunk
-    const int prevStart = __shfl_up_sync(kFullMask, win[u], 1);
-    const bool emptyRow = lane >= 1 && lane <= span[u] && win[u] == prevStart;
-    if (span[u] < 32 && !__any_sync(kFullMask, emptyRow)) {
-      // head mask: bit p set when a row lo+j (j >= 1) starts at chunk position p
-      const long long pos = (long long)win[u] - cb;
-      const bool head = lane >= 1 && lane <= span[u] && pos >= 0 && pos < kCsrChunk;
-      const int pw = head ? (int)(pos >> 5) : -1;
-      const unsigned bit = head ? 1u << (pos & 31) : 0u;
-      const unsigned m0 = __reduce_or_sync(kFullMask, pw == 0 ? bit : 0u);
-      const unsigned m1 = __reduce_or_sync(kFullMask, pw == 1 ? bit : 0u);
-      const unsigned m2 = __reduce_or_sync(kFullMask, pw == 2 ? bit : 0u);
-      const unsigned m3 = __reduce_or_sync(kFullMask, pw == 3 ? bit : 0u);
-      // lane's entries 4*lane .. 4*lane+3 sit in word lane/8, bits 4*(lane%8)+e
+    for (int e = 0; e < 4; ++e)
+      val[u][e] = base + e < Z ? val[u][e] * ld_x(x + col[u][e]) : 0.0f;
+    int row[4];
+    const int lo = loF[u] & 0x7fffffff;
+    if (loF[u] >= 0) {
+      // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e
       const int wd = lane >> 3;
-      const unsigned mw = wd == 0 ? m0 : wd == 1 ? m1 : wd == 2 ? m2 : m3;
-      const int before = (wd > 0 ? __popc(m0) : 0) + (wd > 1 ? __popc(m1) : 0) +
-                         (wd > 2 ? __popc(m2) : 0);
+      const unsigned mw = wd == 0 ? mask[u].x : wd == 1 ? mask[u].y : wd == 2 ? mask[u].z : mask[u].w;
+      const int before = (wd > 0 ? __popc(mask[u].x) : 0) + (wd > 1 ? __popc(mask[u].y) : 0) +
+                         (wd > 2 ? __popc(mask[u].z) : 0);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int b = 4 * (lane & 7) + e;
         const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
-        row[u][e] = (live && base + e < Z) ? lo[u] + before + __popc(mw & upto) : -1;
+        row[e] = base + e < Z ? lo + before + __popc(mw & upto) : -1;
       }
     } else {
-      // many short or empty rows: binary search on rowPtrs, then walk
-      const int hi = lo[u] + span[u];
-      int r = lo[u];
-      if (live && base < Z) {
+      // a chunk holding empty rows: binary search on rowPtrs, then walk
+      const int hi = __ldg(chunkRow + c0 + u + 1) & 0x7fffffff;
+      int r = lo;
+      if (base < Z) {
         int b = hi;
         while (r < b) {
           const int m = (r + b + 1) >> 1;
@@ -188,14 +173,41 @@ __global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __
           ++r;
           nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
         }
-        row[u][e] = (live && k < Z) ? r : -1;
+        row[e] = k < Z ? r : -1;
       }
     }
+    warp_segmented_add(row, val[u], y, false);
   }
-#pragma unroll
-  for (int u = 0; u < U; ++u) {
-    if (c0 + u < nChunks) warp_segmented_add(row[u], val[u], y, false);
+}
+
+// chunkMask[c]: bit p set when a row other than chunkRow[c] starts at
+// position p of chunk c; the sign bit of chunkRow[c] is set when an empty row
+// lies inside the chunk. Thread per chunk, walking the rows that start in it
+// (at most kCsrChunk + 1 steps).
+__global__ void k_csr_chunk_masks(int R, int Z, const int* __restrict__ rowPtrs, int nChunks,
+                                  int* __restrict__ chunkRow, uint4* __restrict__ chunkMask) {
+  const long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= nChunks) return;
+  const int lo = chunkRow[c];
+  const long long cb = c * kCsrChunk;
+  unsigned m[4] = {0u, 0u, 0u, 0u};
+  bool hasEmpty = false;
+  if (lo >= 0 && lo < R) {
+    int next = rowPtrs[lo + 1];
+    for (int r = lo + 1; r < R; ++r) {
+      const int st = next;
+      if (st >= cb + kCsrChunk || st >= Z) break;
+      next = rowPtrs[r + 1];
+      if (next == st) {  // row r is empty and sits inside the chunk
+        hasEmpty = true;
+        break;
+      }
+      const long long pos = st - cb;
+      if (pos > 0 && pos < kCsrChunk) m[pos >> 5] |= 1u << (pos & 31);
+    }
   }
+  chunkMask[c] = make_uint4(m[0], m[1], m[2], m[3]);
+  if (hasEmpty) chunkRow[c] = lo | (int)0x80000000;
 }
 
 // chunkRow[c] = the row holding nonzero c*kCsrChunk (c < nChunks) is written
@@ -433,9 +445,18 @@ __global__ void __launch_bounds__(256, 3) k_spmv_jds(int R, int maxLen, int tSpl
 
 }  // namespace
 
+cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
+                                   uint4* chunkMask, cudaStream_t s) {
+  if (nChunks <= 0) return cudaSuccess;
+  k_csr_chunk_masks<<<(unsigned)(((long long)nChunks + 255) / 256), 256, 0, s>>>(
+      R, Z, rowPtrs, nChunks, chunkRow, chunkMask);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* chunkRow, const float* x, float* y,
-                            cudaStream_t s) {
+                            const float* value, const int* chunkRow, const uint4* chunkMask,
+                            const float* x, float* y, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long chunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
   const long long warps = (chunks + kCsrChunksPerWarp - 1) / kCsrChunksPerWarp;
@@ -443,10 +464,10 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
   const bool vec = aligned16(colIdx) && aligned16(value);
   if (vec)
     k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
-                                                      (int)chunks, x, y);
+                                                      chunkMask, (int)chunks, x, y);
   else
     k_spmv_csr<false><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
-                                                       (int)chunks, x, y);
+                                                       chunkMask, (int)chunks, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
