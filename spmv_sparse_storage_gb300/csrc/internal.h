@@ -51,7 +51,7 @@ size_t stats_scratch_bytes(int R);
 // CSR work split: one warp per kCsrChunk consecutive nonzeros.
 // ---------------------------------------------------------------------------
 constexpr int kCsrChunk = 128;
-constexpr int kCsrChunksPerWarp = 2;
+constexpr int kCsrRowOwnerMinRows = 8;  // chunks with >= 8 rows: lane-per-row sums
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part

@@ -76,108 +76,144 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // work by nonzero count and to split very long rows. Here the nonzeros are
 // cut into chunks of kCsrChunk = 128 (4 per lane, 16-byte loads of value and
 // colIdx when aligned) whatever rows they belong to: a 5000-entry row spreads
-// over 40 chunks, an empty row costs nothing. A warp takes kCsrChunksPerWarp
-// consecutive chunks and issues all their loads before it waits for any.
+// over 40 chunks, an empty row costs nothing. One warp per chunk.
 //
 // Row ids come from an index built once at handle creation (the row
 // statistics pass and k_csr_chunk_masks): chunkRow[c] = the row holding the
 // chunk's first nonzero, and chunkMask[c] = a 128-bit mask of the chunk
 // positions where a later row starts. The row of entry p is chunkRow[c] plus
 // the number of mask bits at positions <= p (popcounts), so the kernel reads
-// 0.125 byte of index per nonzero and never waits on rowPtrs. A chunk in
-// which an empty row sits (the sign bit of chunkRow[c] marks it) takes the
-// general path instead: each lane binary-searches rowPtrs for its first
-// entry's row and walks forward. The warp then sums runs of equal row with
-// shuffles and adds each run with one atomicAdd, so no warp waits on a read
-// of y either.
+// 0.125 byte of index per nonzero and never waits on rowPtrs. Two ways to
+// sum: when the chunk holds at least kCsrRowOwnerMinRows rows (short rows),
+// the products go to shared memory and lane j sums row chunkRow[c] + j
+// itself (its span is between the j-th and (j+1)-th mask bits) and adds it
+// with one atomicAdd, consecutive lanes on consecutive rows; otherwise (few,
+// long rows) the warp sums runs of equal row with a segmented shuffle scan
+// (warp_segmented_add). A chunk in which an empty row sits (the sign bit of
+// chunkRow[c] marks it) finds its rows by a binary search on rowPtrs. Either
+// way each row gets one atomicAdd per chunk, so no warp waits on a read of y.
 // ===========================================================================
+// Position of the k-th (0-based) set bit of m (k < popc(m)).
+__device__ __forceinline__ int select_bit(unsigned m, int k) {
+  int pos = 0;
+  int c = __popc(m & 0xffffu);
+  if (k >= c) { k -= c; pos += 16; m >>= 16; }
+  c = __popc(m & 0xffu);
+  if (k >= c) { k -= c; pos += 8; m >>= 8; }
+  c = __popc(m & 0xfu);
+  if (k >= c) { k -= c; pos += 4; m >>= 4; }
+  c = __popc(m & 0x3u);
+  if (k >= c) { k -= c; pos += 2; m >>= 2; }
+  c = (int)(m & 1u);
+  if (k >= c) pos += 1;
+  return pos;
+}
+
+// Position in the chunk where segment j starts (segment 0 at 0, segment
+// j >= 1 at the j-th set bit of the 128-bit mask).
+__device__ __forceinline__ int segment_start(const uint4& m, int j, int c0, int c1, int c2) {
+  if (j == 0) return 0;
+  int k = j - 1;
+  if (k < c0) return select_bit(m.x, k);
+  k -= c0;
+  if (k < c1) return 32 + select_bit(m.y, k);
+  k -= c1;
+  if (k < c2) return 64 + select_bit(m.z, k);
+  return 96 + select_bit(m.w, k - c2);
+}
+
 template <bool VEC>
-__global__ void __launch_bounds__(256, 4) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
+__global__ void __launch_bounds__(256, 6) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
                                                      const float* __restrict__ value,
                                                      const int* __restrict__ chunkRow,
                                                      const uint4* __restrict__ chunkMask,
                                                      int nChunks, const float* __restrict__ x,
                                                      float* __restrict__ y) {
-  constexpr int U = kCsrChunksPerWarp;
-  const int lane = threadIdx.x & 31;
-  const long long w = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long c0 = w * U;
-  if (c0 >= nChunks) return;  // warp-uniform
+  __shared__ float4 sProd[8][kCsrChunk / 4];  // one chunk of products per warp
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (c >= nChunks) return;  // warp-uniform
+  const long long cb = c * kCsrChunk;
+  const long long base = cb + 4 * lane;
 
-  int col[U][4];
-  float val[U][4];
-  int loF[U];
-  uint4 mask[U];
+  const int loF = __ldg(chunkRow + c);  // same address in every lane: one request
+  const uint4 mask = __ldg(chunkMask + c);
+  int col[4];
+  float p[4];
+  if (VEC && base + 4 <= Z) {
+    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
+    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+    col[0] = c4.x; col[1] = c4.y; col[2] = c4.z; col[3] = c4.w;
+    p[0] = v4.x; p[1] = v4.y; p[2] = v4.z; p[3] = v4.w;
+  } else {
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const long long c = c0 + u < nChunks ? c0 + u : nChunks - 1;
-    loF[u] = __ldg(chunkRow + c);  // same address in every lane: one request
-    mask[u] = __ldg(chunkMask + c);
-    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
-    if (VEC && base + 4 <= Z) {
-      const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-      const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
-      col[u][0] = c4.x; col[u][1] = c4.y; col[u][2] = c4.z; col[u][3] = c4.w;
-      val[u][0] = v4.x; val[u][1] = v4.y; val[u][2] = v4.z; val[u][3] = v4.w;
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const long long k = base + e;
-        col[u][e] = k < Z ? ld_stream(colIdx + k) : 0;
-        val[u][e] = k < Z ? ld_stream(value + k) : 0.0f;
-      }
+    for (int e = 0; e < 4; ++e) {
+      const long long k = base + e;
+      col[e] = k < Z ? ld_stream(colIdx + k) : 0;
+      p[e] = k < Z ? ld_stream(value + k) : 0.0f;
     }
   }
 #pragma unroll
-  for (int u = 0; u < U; ++u) {
-    const bool live = c0 + u < nChunks;
-    if (!live) break;  // warp-uniform
-    const long long base = (c0 + u) * kCsrChunk + 4 * lane;
+  for (int e = 0; e < 4; ++e) p[e] = base + e < Z ? p[e] * ld_x(x + col[e]) : 0.0f;
+
+  const int lo = loF & 0x7fffffff;
+  const int c0 = __popc(mask.x), c1 = __popc(mask.y), c2 = __popc(mask.z), c3 = __popc(mask.w);
+  const int nseg = 1 + c0 + c1 + c2 + c3;  // rows with entries in this chunk
+  if (loF >= 0 && nseg >= kCsrRowOwnerMinRows) {
+    // many short rows: lane j sums row lo+j from shared memory and adds it
+    // with one atomic; consecutive lanes hit consecutive rows (coalesced)
+    sProd[wib][lane] = make_float4(p[0], p[1], p[2], p[3]);
+    __syncwarp();
+    const float* sp = reinterpret_cast<const float*>(sProd[wib]);
+    const int end = Z - cb < kCsrChunk ? (int)(Z - cb) : kCsrChunk;
+    for (int j = lane; j < nseg; j += 32) {
+      const int h0 = segment_start(mask, j, c0, c1, c2);
+      const int h1 = j + 1 < nseg ? segment_start(mask, j + 1, c0, c1, c2) : end;
+      float sum = 0.0f;
+      for (int q = h0; q < h1; ++q) sum += sp[q];
+      atomicAdd(y + lo + j, sum);
+    }
+    return;
+  }
+  int row[4];
+  if (loF >= 0) {
+    // few long rows: row of each entry by popcount, then a warp segmented add
+    const int wd = lane >> 3;
+    const unsigned mw = wd == 0 ? mask.x : wd == 1 ? mask.y : wd == 2 ? mask.z : mask.w;
+    const int before = (wd > 0 ? c0 : 0) + (wd > 1 ? c1 : 0) + (wd > 2 ? c2 : 0);
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      val[u][e] = base + e < Z ? val[u][e] * ld_x(x + col[u][e]) : 0.0f;
-    int row[4];
-    const int lo = loF[u] & 0x7fffffff;
-    if (loF[u] >= 0) {
-      // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e
-      const int wd = lane >> 3;
-      const unsigned mw = wd == 0 ? mask[u].x : wd == 1 ? mask[u].y : wd == 2 ? mask[u].z : mask[u].w;
-      const int before = (wd > 0 ? __popc(mask[u].x) : 0) + (wd > 1 ? __popc(mask[u].y) : 0) +
-                         (wd > 2 ? __popc(mask[u].z) : 0);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int b = 4 * (lane & 7) + e;
-        const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
-        row[e] = base + e < Z ? lo + before + __popc(mw & upto) : -1;
-      }
-    } else {
-      // a chunk holding empty rows: binary search on rowPtrs, then walk
-      const int hi = __ldg(chunkRow + c0 + u + 1) & 0x7fffffff;
-      int r = lo;
-      if (base < Z) {
-        int b = hi;
-        while (r < b) {
-          const int m = (r + b + 1) >> 1;
-          if (__ldg(rowPtrs + m) <= (int)base)
-            r = m;
-          else
-            b = m - 1;
-        }
-      }
-      int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const long long k = base + e;
-        while (k >= nextStart) {  // skips empty rows; bounded by hi
-          ++r;
-          nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-        }
-        row[e] = k < Z ? r : -1;
+    for (int e = 0; e < 4; ++e) {
+      const int b = 4 * (lane & 7) + e;
+      const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
+      row[e] = base + e < Z ? lo + before + __popc(mw & upto) : -1;
+    }
+  } else {
+    // a chunk holding empty rows: binary search on rowPtrs, then walk
+    const int hi = __ldg(chunkRow + c + 1) & 0x7fffffff;
+    int r = lo;
+    if (base < Z) {
+      int b = hi;
+      while (r < b) {
+        const int m = (r + b + 1) >> 1;
+        if (__ldg(rowPtrs + m) <= (int)base)
+          r = m;
+        else
+          b = m - 1;
       }
     }
-    warp_segmented_add(row, val[u], y, false);
+    int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const long long k = base + e;
+      while (k >= nextStart) {  // skips empty rows; bounded by hi
+        ++r;
+        nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+      }
+      row[e] = k < Z ? r : -1;
+    }
   }
+  warp_segmented_add(row, p, y, false);
 }
 
 // chunkMask[c]: bit p set when a row other than chunkRow[c] starts at
@@ -459,8 +495,7 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const float* x, float* y, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long chunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long warps = (chunks + kCsrChunksPerWarp - 1) / kCsrChunksPerWarp;
-  const long long blocks = (warps * 32 + 255) / 256;
+  const long long blocks = (chunks * 32 + 255) / 256;
   const bool vec = aligned16(colIdx) && aligned16(value);
   if (vec)
     k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
