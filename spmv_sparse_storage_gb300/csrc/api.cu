@@ -139,8 +139,8 @@ struct spmv_handle_s {
 
   // CSR: nnz-balanced split, one warp per kCsrChunk nonzeros (computed at creation)
   int nChunks = 0;
-  int* chunkRow = nullptr;     // row of each chunk's first nonzero (+ empty-row flag)
-  uint4* chunkMask = nullptr;  // row-start positions inside each chunk
+  spmv::CsrChunkDesc* chunkDesc = nullptr;  // one record per kCsrChunk nonzeros
+  int* devStatus = nullptr;                  // set by kernels whose bounded waits time out
   std::vector<Buf> csrBufs;
 
   // COO (shares colIdx/value with the caller's CSR arrays)
@@ -322,15 +322,16 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   // nnz-balanced split for the CSR kernel, written by the statistics pass
   // (which checks bounds, so it stays in bounds even if validation fails)
   h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
-  st = alloc_typed(h, (long long)h->nChunks + 1, s, &h->chunkRow, h->csrBufs);
+  st = alloc_typed(h, (long long)h->nChunks, s, &h->chunkDesc, h->csrBufs);
+  if (st != SPMV_OK) return fail(st);
+  st = alloc_typed(h, 1, s, &h->devStatus, h->csrBufs);
+  if (st != SPMV_OK) return fail(st);
+  st = record(cudaMemsetAsync(h->devStatus, 0, sizeof(int), s));
   if (st != SPMV_OK) return fail(st);
   st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, statsScratch,
-                                 h->nChunks, h->chunkRow, s));
+                                 h->nChunks, h->chunkDesc, s));
   if (st != SPMV_OK) return fail(st);
-  st = alloc_typed(h, (long long)h->nChunks, s, &h->chunkMask, h->csrBufs);
-  if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_csr_chunk_masks(numRows, nnz, d_rowPtrs, h->nChunks, h->chunkRow,
-                                           h->chunkMask, s));
+  st = record(spmv::launch_csr_chunk_masks(numRows, nnz, d_rowPtrs, h->nChunks, h->chunkDesc, s));
   if (st != SPMV_OK) return fail(st);
   hst = new (std::nothrow) DevStats;
   if (!hst) return fail(SPMV_ERR_ALLOC);
@@ -551,7 +552,7 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   switch (format) {
     case SPMV_CSR:
       return record(spmv::launch_spmv_csr(h->R, h->Z, h->rowPtrs, h->colIdx, h->value,
-                                          h->chunkRow, h->chunkMask, d_x, d_y, s));
+                                          h->chunkDesc, d_x, d_y, h->devStatus, s));
     case SPMV_COO:
       return record(spmv::launch_spmv_coo(h->Z, h->cooRow, h->colIdx, h->value, d_x, d_y,
                                           false, s));

@@ -48,10 +48,20 @@ struct StatsPartial {
 size_t stats_scratch_bytes(int R);
 
 // ---------------------------------------------------------------------------
-// CSR work split: one warp per kCsrChunk consecutive nonzeros.
+// CSR work split: the nonzeros in chunks of kCsrChunk, each described by a
+// 32-byte record built at handle creation.
 // ---------------------------------------------------------------------------
 constexpr int kCsrChunk = 128;
-constexpr int kCsrRowOwnerMinRows = 8;  // chunks with >= 8 rows: lane-per-row sums
+struct __align__(16) CsrChunkDesc {
+  int lo;      // row holding the chunk's first nonzero
+  int hi;      // row holding the next chunk's first nonzero (numRows-1 for the last)
+  int flags;   // kCsrChunkHasEmptyRow: an empty row lies inside the chunk
+  int pad0;
+  uint4 mask;  // bit p: a row other than lo starts at position p of the chunk
+};
+constexpr int kCsrChunkHasEmptyRow = 1;
+constexpr int kCsrStages = 4;         // bulk-copy stages per warp
+constexpr int kCsrWarpsPerBlock = 8;
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
@@ -68,10 +78,9 @@ int num_sms();
 // ---------------------------------------------------------------------------
 // Launchers. Each returns the cudaError_t of its launches.
 // ---------------------------------------------------------------------------
-// stats.cu (also writes chunkRow[0..nChunks] for the CSR kernel:
-// chunkRow[c] = row holding nonzero c*kCsrChunk, chunkRow[nChunks] = numRows-1)
+// stats.cu (also writes desc[c].lo = row holding nonzero c*kCsrChunk)
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, void* scratch, int nChunks, int* chunkRow,
+                         DevStats* st, void* scratch, int nChunks, CsrChunkDesc* desc,
                          cudaStream_t s);
 
 // convert.cu
@@ -93,13 +102,12 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
                              float* jdsVal, void* scratch, cudaStream_t s);
 
 // spmv_kernels.cu
-// chunkMask[c] (bit p: a row starts at position p of chunk c) and the
-// empty-row flag in the sign bit of chunkRow[c]; runs after the stats pass
-cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
-                                   uint4* chunkMask, cudaStream_t s);
+// fills hi, flags and mask of every chunk record; runs after the stats pass
+cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks,
+                                   CsrChunkDesc* desc, cudaStream_t s);
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* chunkRow, const uint4* chunkMask,
-                            const float* x, float* y, cudaStream_t s);
+                            const float* value, const CsrChunkDesc* desc, const float* x,
+                            float* y, int* devStatus, cudaStream_t s);
 cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,

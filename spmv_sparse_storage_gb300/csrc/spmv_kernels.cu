@@ -74,124 +74,48 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // row lengths differ, and the remedy named in "Introduction to sparse
 // computing ...", section "Building the problem framework", is to split the
 // work by nonzero count and to split very long rows. Here the nonzeros are
-// cut into chunks of kCsrChunk = 128 (4 per lane, 16-byte loads of value and
-// colIdx when aligned) whatever rows they belong to: a 5000-entry row spreads
-// over 40 chunks, an empty row costs nothing. One warp per chunk.
+// cut into chunks of kCsrChunk = 128 whatever rows they belong to: a
+// 5000-entry row spreads over 40 chunks, an empty row costs nothing.
 //
-// Row ids come from an index built once at handle creation (the row
-// statistics pass and k_csr_chunk_masks): chunkRow[c] = the row holding the
-// chunk's first nonzero, and chunkMask[c] = a 128-bit mask of the chunk
-// positions where a later row starts. The row of entry p is chunkRow[c] plus
+// Row ids come from a 32-byte record per chunk built once at handle
+// creation: lo = the row holding the chunk's first nonzero and mask = the
+// chunk positions where a later row starts. The row of entry p is lo plus
 // the number of mask bits at positions <= p (popcounts), so the kernel reads
-// 0.125 byte of index per nonzero and never waits on rowPtrs. Two ways to
-// sum: when the chunk holds at least kCsrRowOwnerMinRows rows (short rows),
-// the products go to shared memory and lane j sums row chunkRow[c] + j
-// itself (its span is between the j-th and (j+1)-th mask bits) and adds it
-// with one atomicAdd, consecutive lanes on consecutive rows; otherwise (few,
-// long rows) the warp sums runs of equal row with a segmented shuffle scan
-// (warp_segmented_add). A chunk in which an empty row sits (the sign bit of
-// chunkRow[c] marks it) finds its rows by a binary search on rowPtrs. Either
-// way each row gets one atomicAdd per chunk, so no warp waits on a read of y.
+// 0.25 byte of index per nonzero and never waits on rowPtrs; a chunk in
+// which an empty row sits (flagged) binary-searches rowPtrs instead.
+//
+// Streaming: each warp owns kCsrStages shared-memory stages and keeps that
+// many chunks in flight with bulk (TMA) copies of the chunk's colIdx, value
+// and record (1056 bytes), completed on an mbarrier per stage. The bytes in
+// flight per SM are then set by shared memory, not by registers. A warp
+// takes chunks w, w + W, w + 2W, ... (W = warps in the grid, a persistent
+// grid of full SMs), so the warps of the GPU sweep the arrays in order.
+// Each chunk: lane l takes entries 4l..4l+3, gathers x, and the warp sums
+// runs of equal row with a segmented shuffle scan, one atomicAdd per row
+// per chunk (warp_segmented_add): no warp waits on a read of y.
 // ===========================================================================
-// Position of the k-th (0-based) set bit of m (k < popc(m)).
-__device__ __forceinline__ int select_bit(unsigned m, int k) {
-  int pos = 0;
-  int c = __popc(m & 0xffffu);
-  if (k >= c) { k -= c; pos += 16; m >>= 16; }
-  c = __popc(m & 0xffu);
-  if (k >= c) { k -= c; pos += 8; m >>= 8; }
-  c = __popc(m & 0xfu);
-  if (k >= c) { k -= c; pos += 4; m >>= 4; }
-  c = __popc(m & 0x3u);
-  if (k >= c) { k -= c; pos += 2; m >>= 2; }
-  c = (int)(m & 1u);
-  if (k >= c) pos += 1;
-  return pos;
-}
 
-// Position in the chunk where segment j starts (segment 0 at 0, segment
-// j >= 1 at the j-th set bit of the 128-bit mask).
-__device__ __forceinline__ int segment_start(const uint4& m, int j, int c0, int c1, int c2) {
-  if (j == 0) return 0;
-  int k = j - 1;
-  if (k < c0) return select_bit(m.x, k);
-  k -= c0;
-  if (k < c1) return 32 + select_bit(m.y, k);
-  k -= c1;
-  if (k < c2) return 64 + select_bit(m.z, k);
-  return 96 + select_bit(m.w, k - c2);
-}
-
-template <bool VEC>
-__global__ void __launch_bounds__(256, 6) k_spmv_csr(int R, int Z, const int* __restrict__ rowPtrs,
-                                                     const int* __restrict__ colIdx,
-                                                     const float* __restrict__ value,
-                                                     const int* __restrict__ chunkRow,
-                                                     const uint4* __restrict__ chunkMask,
-                                                     int nChunks, const float* __restrict__ x,
-                                                     float* __restrict__ y) {
-  __shared__ float4 sProd[8][kCsrChunk / 4];  // one chunk of products per warp
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (c >= nChunks) return;  // warp-uniform
-  const long long cb = c * kCsrChunk;
+// Row of each of the lane's 4 entries (entries at or beyond Z get -1).
+__device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long cb, int lane,
+                                               int Z, const int* __restrict__ rowPtrs,
+                                               int (&row)[4]) {
   const long long base = cb + 4 * lane;
-
-  const int loF = __ldg(chunkRow + c);  // same address in every lane: one request
-  const uint4 mask = __ldg(chunkMask + c);
-  int col[4];
-  float p[4];
-  if (VEC && base + 4 <= Z) {
-    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
-    col[0] = c4.x; col[1] = c4.y; col[2] = c4.z; col[3] = c4.w;
-    p[0] = v4.x; p[1] = v4.y; p[2] = v4.z; p[3] = v4.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const long long k = base + e;
-      col[e] = k < Z ? ld_stream(colIdx + k) : 0;
-      p[e] = k < Z ? ld_stream(value + k) : 0.0f;
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) p[e] = base + e < Z ? p[e] * ld_x(x + col[e]) : 0.0f;
-
-  const int lo = loF & 0x7fffffff;
-  const int c0 = __popc(mask.x), c1 = __popc(mask.y), c2 = __popc(mask.z), c3 = __popc(mask.w);
-  const int nseg = 1 + c0 + c1 + c2 + c3;  // rows with entries in this chunk
-  if (loF >= 0 && nseg >= kCsrRowOwnerMinRows) {
-    // many short rows: lane j sums row lo+j from shared memory and adds it
-    // with one atomic; consecutive lanes hit consecutive rows (coalesced)
-    sProd[wib][lane] = make_float4(p[0], p[1], p[2], p[3]);
-    __syncwarp();
-    const float* sp = reinterpret_cast<const float*>(sProd[wib]);
-    const int end = Z - cb < kCsrChunk ? (int)(Z - cb) : kCsrChunk;
-    for (int j = lane; j < nseg; j += 32) {
-      const int h0 = segment_start(mask, j, c0, c1, c2);
-      const int h1 = j + 1 < nseg ? segment_start(mask, j + 1, c0, c1, c2) : end;
-      float sum = 0.0f;
-      for (int q = h0; q < h1; ++q) sum += sp[q];
-      atomicAdd(y + lo + j, sum);
-    }
-    return;
-  }
-  int row[4];
-  if (loF >= 0) {
-    // few long rows: row of each entry by popcount, then a warp segmented add
+  if (!(d.flags & kCsrChunkHasEmptyRow)) {
+    // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e
     const int wd = lane >> 3;
-    const unsigned mw = wd == 0 ? mask.x : wd == 1 ? mask.y : wd == 2 ? mask.z : mask.w;
-    const int before = (wd > 0 ? c0 : 0) + (wd > 1 ? c1 : 0) + (wd > 2 ? c2 : 0);
+    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
+    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
+                       (wd > 2 ? __popc(d.mask.z) : 0);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int b = 4 * (lane & 7) + e;
       const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
-      row[e] = base + e < Z ? lo + before + __popc(mw & upto) : -1;
+      row[e] = base + e < Z ? d.lo + before + __popc(mw & upto) : -1;
     }
   } else {
     // a chunk holding empty rows: binary search on rowPtrs, then walk
-    const int hi = __ldg(chunkRow + c + 1) & 0x7fffffff;
-    int r = lo;
+    const int hi = d.hi;
+    int r = d.lo;
     if (base < Z) {
       int b = hi;
       while (r < b) {
@@ -213,21 +137,113 @@ __global__ void __launch_bounds__(256, 6) k_spmv_csr(int R, int Z, const int* __
       row[e] = k < Z ? r : -1;
     }
   }
+}
+
+struct __align__(16) CsrStage {
+  int4 col[kCsrChunk / 4];
+  float4 val[kCsrChunk / 4];
+  CsrChunkDesc desc;
+};
+constexpr unsigned kCsrStageBytes = sizeof(CsrStage);
+
+// TMA-fed kernel: full chunks only (c < nFull); needs 16-byte aligned
+// colIdx and value. The last, partial chunk is left to k_spmv_csr_tail.
+__global__ void __launch_bounds__(kCsrWarpsPerBlock * 32) k_spmv_csr_tma(
+    int Z, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
+    const float* __restrict__ value, const CsrChunkDesc* __restrict__ desc, int nFull,
+    const float* __restrict__ x, float* __restrict__ y, int* __restrict__ devStatus) {
+  __shared__ CsrStage sStage[kCsrWarpsPerBlock][kCsrStages];
+  __shared__ uint64_t sBar[kCsrWarpsPerBlock][kCsrStages];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const long long W = (long long)gridDim.x * kCsrWarpsPerBlock;
+  const long long w = (long long)blockIdx.x * kCsrWarpsPerBlock + wib;
+  const long long nk = nFull > w ? (nFull - w + W - 1) / W : 0;
+  if (nk == 0) return;  // warp-uniform
+  CsrStage* st = sStage[wib];
+  uint64_t* bar = sBar[wib];
+  const uint64_t pol = policy_evict_first();
+  if (lane == 0) {
+    for (int s = 0; s < kCsrStages; ++s) mbar_init(&bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int s, long long c) {
+    mbar_arrive_expect_tx(&bar[s], kCsrStageBytes);
+    bulk_g2s(st[s].col, colIdx + c * kCsrChunk, kCsrChunk * 4, &bar[s], pol);
+    bulk_g2s(st[s].val, value + c * kCsrChunk, kCsrChunk * 4, &bar[s], pol);
+    bulk_g2s(&st[s].desc, desc + c, sizeof(CsrChunkDesc), &bar[s], pol);
+  };
+  if (lane == 0)
+    for (int s = 0; s < kCsrStages && s < nk; ++s) issue(s, w + s * W);
+  for (long long k = 0; k < nk; ++k) {
+    const int s = (int)(k % kCsrStages);
+    const unsigned parity = (unsigned)((k / kCsrStages) & 1);
+    if (!mbar_wait_bounded(&bar[s], parity)) {
+      // a copy never completed: record it and drain the other stages
+      if (lane == 0) atomicOr(devStatus, 1);
+      for (long long q = k + 1; q < nk && q < k + kCsrStages; ++q)
+        mbar_wait_bounded(&bar[q % kCsrStages], (unsigned)((q / kCsrStages) & 1));
+      return;
+    }
+    const long long c = w + k * W;
+    const long long cb = c * kCsrChunk;
+    const int4 c4 = st[s].col[lane];
+    const float4 v4 = st[s].val[lane];
+    const CsrChunkDesc d = st[s].desc;
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && k + kCsrStages < nk) issue(s, w + (k + kCsrStages) * W);
+    float p[4];
+    p[0] = v4.x * ld_x(x + c4.x);
+    p[1] = v4.y * ld_x(x + c4.y);
+    p[2] = v4.z * ld_x(x + c4.z);
+    p[3] = v4.w * ld_x(x + c4.w);
+    int row[4];
+    csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
+    warp_segmented_add(row, p, y, false);
+  }
+}
+
+// Chunks [c0, c1) with plain loads: the partial last chunk, and every chunk
+// when colIdx/value are not 16-byte aligned. One warp per chunk.
+__global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, long long c1,
+                                                        const int* __restrict__ rowPtrs,
+                                                        const int* __restrict__ colIdx,
+                                                        const float* __restrict__ value,
+                                                        const CsrChunkDesc* __restrict__ desc,
+                                                        const float* __restrict__ x,
+                                                        float* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const long long c = c0 + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (c >= c1) return;  // warp-uniform
+  const long long cb = c * kCsrChunk;
+  const long long base = cb + 4 * lane;
+  const CsrChunkDesc d = desc[c];
+  float p[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const long long k = base + e;
+    p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : 0.0f;
+  }
+  int row[4];
+  csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
   warp_segmented_add(row, p, y, false);
 }
 
-// chunkMask[c]: bit p set when a row other than chunkRow[c] starts at
-// position p of chunk c; the sign bit of chunkRow[c] is set when an empty row
-// lies inside the chunk. Thread per chunk, walking the rows that start in it
-// (at most kCsrChunk + 1 steps).
+// Chunk records: hi from the next chunk's lo, and the positions where rows
+// start inside the chunk (or the empty-row flag). Thread per chunk, walking
+// the rows that start in it (at most kCsrChunk + 1 steps). Bounds are checked
+// so that this kernel, which runs before validation is known, stays in
+// bounds on invalid input.
 __global__ void k_csr_chunk_masks(int R, int Z, const int* __restrict__ rowPtrs, int nChunks,
-                                  int* __restrict__ chunkRow, uint4* __restrict__ chunkMask) {
+                                  CsrChunkDesc* __restrict__ desc) {
   const long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= nChunks) return;
-  const int lo = chunkRow[c];
+  const int lo = desc[c].lo;
+  const int hi = c + 1 < nChunks ? desc[c + 1].lo : (R > 0 ? R - 1 : 0);
   const long long cb = c * kCsrChunk;
   unsigned m[4] = {0u, 0u, 0u, 0u};
-  bool hasEmpty = false;
+  int flags = 0;
   if (lo >= 0 && lo < R) {
     int next = rowPtrs[lo + 1];
     for (int r = lo + 1; r < R; ++r) {
@@ -235,19 +251,23 @@ __global__ void k_csr_chunk_masks(int R, int Z, const int* __restrict__ rowPtrs,
       if (st >= cb + kCsrChunk || st >= Z) break;
       next = rowPtrs[r + 1];
       if (next == st) {  // row r is empty and sits inside the chunk
-        hasEmpty = true;
+        flags |= kCsrChunkHasEmptyRow;
         break;
       }
       const long long pos = st - cb;
       if (pos > 0 && pos < kCsrChunk) m[pos >> 5] |= 1u << (pos & 31);
     }
+  } else {
+    flags |= kCsrChunkHasEmptyRow;  // invalid input: take the searching path
   }
-  chunkMask[c] = make_uint4(m[0], m[1], m[2], m[3]);
-  if (hasEmpty) chunkRow[c] = lo | (int)0x80000000;
+  CsrChunkDesc d;
+  d.lo = lo;
+  d.hi = hi;
+  d.flags = flags;
+  d.pad0 = 0;
+  d.mask = make_uint4(m[0], m[1], m[2], m[3]);
+  desc[c] = d;
 }
-
-// chunkRow[c] = the row holding nonzero c*kCsrChunk (c < nChunks) is written
-// by the row statistics pass (stats.cu); chunkRow[nChunks] = numRows - 1.
 
 // ===========================================================================
 // ELL ("Regularized Formats ...", section "ELL format: padding +
@@ -481,29 +501,48 @@ __global__ void __launch_bounds__(256, 3) k_spmv_jds(int R, int maxLen, int tSpl
 
 }  // namespace
 
-cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks, int* chunkRow,
-                                   uint4* chunkMask, cudaStream_t s) {
+cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks,
+                                   CsrChunkDesc* desc, cudaStream_t s) {
   if (nChunks <= 0) return cudaSuccess;
-  k_csr_chunk_masks<<<(unsigned)(((long long)nChunks + 255) / 256), 256, 0, s>>>(
-      R, Z, rowPtrs, nChunks, chunkRow, chunkMask);
+  k_csr_chunk_masks<<<(unsigned)(((long long)nChunks + 255) / 256), 256, 0, s>>>(R, Z, rowPtrs,
+                                                                                nChunks, desc);
   note_launches(1);
   return cudaGetLastError();
 }
 
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const int* chunkRow, const uint4* chunkMask,
-                            const float* x, float* y, cudaStream_t s) {
+                            const float* value, const CsrChunkDesc* desc, const float* x,
+                            float* y, int* devStatus, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
-  const long long chunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long blocks = (chunks * 32 + 255) / 256;
-  const bool vec = aligned16(colIdx) && aligned16(value);
-  if (vec)
-    k_spmv_csr<true><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
-                                                      chunkMask, (int)chunks, x, y);
-  else
-    k_spmv_csr<false><<<(unsigned)blocks, 256, 0, s>>>(R, Z, rowPtrs, colIdx, value, chunkRow,
-                                                       chunkMask, (int)chunks, x, y);
-  note_launches(1);
+  const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
+  const long long nFull = (long long)Z / kCsrChunk;
+  const bool tma = aligned16(colIdx) && aligned16(value) && nFull > 0;
+  int n = 0;
+  if (tma) {
+    // persistent grid: as many blocks as fit on every SM, at most one warp per chunk
+    static int perSm = 0;  // same on every device of one architecture
+    if (perSm == 0) {
+      int n = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_spmv_csr_tma,
+                                                        kCsrWarpsPerBlock * 32, 0) != cudaSuccess)
+        n = 1;
+      perSm = n < 1 ? 1 : n;
+    }
+    long long blocks = (long long)perSm * num_sms();
+    const long long need = (nFull + kCsrWarpsPerBlock - 1) / kCsrWarpsPerBlock;
+    if (blocks > need) blocks = need;
+    k_spmv_csr_tma<<<(unsigned)blocks, kCsrWarpsPerBlock * 32, 0, s>>>(
+        Z, rowPtrs, colIdx, value, desc, (int)nFull, x, y, devStatus);
+    ++n;
+  }
+  const long long p0 = tma ? nFull : 0;
+  if (p0 < nChunks) {
+    const long long warps = nChunks - p0;
+    k_spmv_csr_plain<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
+        Z, p0, nChunks, rowPtrs, colIdx, value, desc, x, y);
+    ++n;
+  }
+  note_launches(n);
   return cudaGetLastError();
 }
 

@@ -41,7 +41,7 @@ __global__ void k_stats_init(DevStats* st, unsigned* histRep) {
 }
 
 // One pass over rowPtrs: monotonicity, endpoints, lengths, histograms, and
-// the CSR chunk map (chunkRow[c] = row holding nonzero c*kCsrChunk). A block
+// the CSR chunk map (desc[c].lo = row holding nonzero c*kCsrChunk). A block
 // takes kStatsRows consecutive rows, kStatsRowsPerThread per thread, 256
 // apart so that each load instruction is coalesced, and issues all its loads
 // before it uses any. The block's maxima, minima and sums go to its own
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
                                                    DevStats* __restrict__ st,
                                                    StatsPartial* __restrict__ partials,
                                                    unsigned* __restrict__ histRep, int nChunks,
-                                                   int* __restrict__ chunkRow) {
+                                                   CsrChunkDesc* __restrict__ desc) {
   __shared__ unsigned int sExact[kExactLenBins];
   __shared__ int sRed[5][8];
   __shared__ unsigned long long sSq[8];
@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (rowPtrs[0] != 0) atomicOr(&st->err, kErrRowPtrStart);
     if (rowPtrs[R] != Z) atomicOr(&st->err, kErrRowPtrEnd);
-    chunkRow[nChunks] = R > 0 ? R - 1 : 0;
   }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long long base = (long long)blockIdx.x * kStatsRows + threadIdx.x;
@@ -100,7 +99,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
         const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
         const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
-        for (int c = c0; c <= c1; ++c) chunkRow[c] = (int)r;
+        for (int c = c0; c <= c1; ++c) desc[c].lo = (int)r;
       }
     }
     // warp-aggregated exact histogram: one shared atomic per distinct length
@@ -245,7 +244,7 @@ size_t stats_scratch_bytes(int R) {
 }
 
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, void* scratch, int nChunks, int* chunkRow,
+                         DevStats* st, void* scratch, int nChunks, CsrChunkDesc* desc,
                          cudaStream_t s) {
   const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
   const int nb = (int)(rb < 1 ? 1 : rb);
@@ -253,7 +252,7 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
   StatsPartial* partials =
       reinterpret_cast<StatsPartial*>(histRep + (size_t)kStatsReplicas * kExactLenBins);
   k_stats_init<<<32, 256, 0, s>>>(st, histRep);
-  k_row_stats<<<nb, 256, 0, s>>>(R, Z, rowPtrs, st, partials, histRep, nChunks, chunkRow);
+  k_row_stats<<<nb, 256, 0, s>>>(R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
   int n = 3;
   const int sms = num_sms();
   if (Z > 0) {
