@@ -91,6 +91,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // L2 policy for a stream read once: evict first, so the gathered x stays.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;

@@ -60,8 +60,9 @@ struct __align__(16) CsrChunkDesc {
   uint4 mask;  // bit p: a row other than lo starts at position p of the chunk
 };
 constexpr int kCsrChunkHasEmptyRow = 1;
-constexpr int kCsrStages = 4;         // bulk-copy stages per warp
-constexpr int kCsrWarpsPerBlock = 8;
+constexpr int kCsrConsumerWarps = 16;              // per block, one chunk each per stage
+constexpr int kCsrGroupChunks = kCsrConsumerWarps;  // chunks moved by one stage
+constexpr int kCsrStages = 4;                       // stages in flight per block
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part

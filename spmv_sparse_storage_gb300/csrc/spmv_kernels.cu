@@ -84,12 +84,10 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const fl
 // 0.25 byte of index per nonzero and never waits on rowPtrs; a chunk in
 // which an empty row sits (flagged) binary-searches rowPtrs instead.
 //
-// Streaming: each warp owns kCsrStages shared-memory stages and keeps that
-// many chunks in flight with bulk (TMA) copies of the chunk's colIdx, value
-// and record (1056 bytes), completed on an mbarrier per stage. The bytes in
-// flight per SM are then set by shared memory, not by registers. A warp
-// takes chunks w, w + W, w + 2W, ... (W = warps in the grid, a persistent
-// grid of full SMs), so the warps of the GPU sweep the arrays in order.
+// Streaming: a block keeps kCsrStages groups of kCsrGroupChunks chunks in
+// flight with bulk (TMA) copies into shared memory, so the bytes in flight
+// per SM are set by shared memory, not by registers, and each copy is large
+// (8 KiB) so that the copy engine's per-operation cost stays small.
 // Each chunk: lane l takes entries 4l..4l+3, gathers x, and the warp sums
 // runs of equal row with a segmented shuffle scan, one atomicAdd per row
 // per chunk (warp_segmented_add): no warp waits on a read of y.
@@ -139,67 +137,89 @@ __device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long 
   }
 }
 
-struct __align__(16) CsrStage {
-  int4 col[kCsrChunk / 4];
-  float4 val[kCsrChunk / 4];
-  CsrChunkDesc desc;
+// One stage: kCsrGroupChunks consecutive chunks (colIdx, value, records).
+struct __align__(128) CsrGroupStage {
+  int col[kCsrGroupChunks * kCsrChunk];
+  float val[kCsrGroupChunks * kCsrChunk];
+  CsrChunkDesc desc[kCsrGroupChunks];
 };
-constexpr unsigned kCsrStageBytes = sizeof(CsrStage);
+constexpr unsigned kCsrStageBytes = sizeof(CsrGroupStage);
+constexpr size_t kCsrTmaSmemBytes = kCsrStages * sizeof(CsrGroupStage) + 2 * kCsrStages * 8;
 
-// TMA-fed kernel: full chunks only (c < nFull); needs 16-byte aligned
-// colIdx and value. The last, partial chunk is left to k_spmv_csr_tail.
-__global__ void __launch_bounds__(kCsrWarpsPerBlock * 32) k_spmv_csr_tma(
+// TMA-fed kernel over groups of kCsrGroupChunks full chunks (g < nGroups);
+// needs 16-byte aligned colIdx and value. A producer warp fills kCsrStages
+// shared-memory stages with three bulk copies each (8 KiB + 8 KiB + 512 B)
+// and kCsrConsumerWarps consumer warps take one chunk each per stage; full
+// and empty mbarriers hand the stages back and forth. Blocks take groups
+// blockIdx.x, blockIdx.x + gridDim.x, ... (a persistent grid over all SMs).
+// Every wait is bounded: on timeout the block records it in devStatus and
+// stops.
+__global__ void __launch_bounds__((kCsrConsumerWarps + 1) * 32, 3) k_spmv_csr_tma(
     int Z, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
-    const float* __restrict__ value, const CsrChunkDesc* __restrict__ desc, int nFull,
+    const float* __restrict__ value, const CsrChunkDesc* __restrict__ desc, int nGroups,
     const float* __restrict__ x, float* __restrict__ y, int* __restrict__ devStatus) {
-  __shared__ CsrStage sStage[kCsrWarpsPerBlock][kCsrStages];
-  __shared__ uint64_t sBar[kCsrWarpsPerBlock][kCsrStages];
-  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
-  const long long W = (long long)gridDim.x * kCsrWarpsPerBlock;
-  const long long w = (long long)blockIdx.x * kCsrWarpsPerBlock + wib;
-  const long long nk = nFull > w ? (nFull - w + W - 1) / W : 0;
-  if (nk == 0) return;  // warp-uniform
-  CsrStage* st = sStage[wib];
-  uint64_t* bar = sBar[wib];
-  const uint64_t pol = policy_evict_first();
-  if (lane == 0) {
-    for (int s = 0; s < kCsrStages; ++s) mbar_init(&bar[s], 1);
+  extern __shared__ __align__(128) unsigned char smem[];
+  CsrGroupStage* stage = reinterpret_cast<CsrGroupStage*>(smem);
+  uint64_t* fullBar = reinterpret_cast<uint64_t*>(smem + kCsrStages * sizeof(CsrGroupStage));
+  uint64_t* emptyBar = fullBar + kCsrStages;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long long G = gridDim.x;
+  const long long nk = nGroups > blockIdx.x ? (nGroups - blockIdx.x + G - 1) / G : 0;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kCsrStages; ++s) {
+      mbar_init(&fullBar[s], 1);
+      mbar_init(&emptyBar[s], kCsrConsumerWarps);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
-  auto issue = [&](int s, long long c) {
-    mbar_arrive_expect_tx(&bar[s], kCsrStageBytes);
-    bulk_g2s(st[s].col, colIdx + c * kCsrChunk, kCsrChunk * 4, &bar[s], pol);
-    bulk_g2s(st[s].val, value + c * kCsrChunk, kCsrChunk * 4, &bar[s], pol);
-    bulk_g2s(&st[s].desc, desc + c, sizeof(CsrChunkDesc), &bar[s], pol);
-  };
-  if (lane == 0)
-    for (int s = 0; s < kCsrStages && s < nk; ++s) issue(s, w + s * W);
+  __syncthreads();
+  if (nk == 0) return;  // block-uniform
+
+  if (warp == kCsrConsumerWarps) {
+    // producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      for (long long k = 0; k < nk; ++k) {
+        const int s = (int)(k % kCsrStages);
+        if (k >= kCsrStages &&
+            !mbar_wait_bounded(&emptyBar[s], (unsigned)(((k / kCsrStages) - 1) & 1))) {
+          atomicOr(devStatus, 1);
+          break;
+        }
+        const long long g = blockIdx.x + k * G;
+        const long long c0 = g * kCsrGroupChunks;
+        mbar_arrive_expect_tx(&fullBar[s], kCsrStageBytes);
+        bulk_g2s(stage[s].col, colIdx + c0 * kCsrChunk, kCsrGroupChunks * kCsrChunk * 4,
+                 &fullBar[s], pol);
+        bulk_g2s(stage[s].val, value + c0 * kCsrChunk, kCsrGroupChunks * kCsrChunk * 4,
+                 &fullBar[s], pol);
+        bulk_g2s(stage[s].desc, desc + c0, kCsrGroupChunks * sizeof(CsrChunkDesc), &fullBar[s],
+                 pol);
+      }
+    }
+    return;
+  }
+  // consumers: warp `warp` takes chunk `warp` of every stage
   for (long long k = 0; k < nk; ++k) {
     const int s = (int)(k % kCsrStages);
-    const unsigned parity = (unsigned)((k / kCsrStages) & 1);
-    if (!mbar_wait_bounded(&bar[s], parity)) {
-      // a copy never completed: record it and drain the other stages
+    if (!mbar_wait_bounded(&fullBar[s], (unsigned)((k / kCsrStages) & 1))) {
       if (lane == 0) atomicOr(devStatus, 1);
-      for (long long q = k + 1; q < nk && q < k + kCsrStages; ++q)
-        mbar_wait_bounded(&bar[q % kCsrStages], (unsigned)((q / kCsrStages) & 1));
-      return;
+      break;
     }
-    const long long c = w + k * W;
-    const long long cb = c * kCsrChunk;
-    const int4 c4 = st[s].col[lane];
-    const float4 v4 = st[s].val[lane];
-    const CsrChunkDesc d = st[s].desc;
+    const int4 c4 = reinterpret_cast<const int4*>(stage[s].col + warp * kCsrChunk)[lane];
+    const float4 v4 = reinterpret_cast<const float4*>(stage[s].val + warp * kCsrChunk)[lane];
+    const CsrChunkDesc d = stage[s].desc[warp];
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && k + kCsrStages < nk) issue(s, w + (k + kCsrStages) * W);
+    if (lane == 0) mbar_arrive(&emptyBar[s]);  // the stage may be refilled
+    const long long c = (blockIdx.x + k * G) * kCsrGroupChunks + warp;
     float p[4];
     p[0] = v4.x * ld_x(x + c4.x);
     p[1] = v4.y * ld_x(x + c4.y);
     p[2] = v4.z * ld_x(x + c4.z);
     p[3] = v4.w * ld_x(x + c4.w);
     int row[4];
-    csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
+    csr_chunk_rows(d, c * kCsrChunk, lane, Z, rowPtrs, row);
     warp_segmented_add(row, p, y, false);
   }
 }
@@ -515,27 +535,28 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             float* y, int* devStatus, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long nFull = (long long)Z / kCsrChunk;
-  const bool tma = aligned16(colIdx) && aligned16(value) && nFull > 0;
+  const long long nGroups = (long long)Z / ((long long)kCsrGroupChunks * kCsrChunk);
+  const bool tma = aligned16(colIdx) && aligned16(value) && nGroups > 0;
   int n = 0;
   if (tma) {
-    // persistent grid: as many blocks as fit on every SM, at most one warp per chunk
-    static int perSm = 0;  // same on every device of one architecture
+    static int perSm = 0;  // blocks per SM (same on every device of one architecture)
     if (perSm == 0) {
-      int n = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_spmv_csr_tma,
-                                                        kCsrWarpsPerBlock * 32, 0) != cudaSuccess)
-        n = 1;
-      perSm = n < 1 ? 1 : n;
+      int v = 0;
+      if (cudaFuncSetAttribute(k_spmv_csr_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kCsrTmaSmemBytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_spmv_csr_tma,
+                                                        (kCsrConsumerWarps + 1) * 32,
+                                                        kCsrTmaSmemBytes) != cudaSuccess)
+        v = 1;
+      perSm = v < 1 ? 1 : v;
     }
     long long blocks = (long long)perSm * num_sms();
-    const long long need = (nFull + kCsrWarpsPerBlock - 1) / kCsrWarpsPerBlock;
-    if (blocks > need) blocks = need;
-    k_spmv_csr_tma<<<(unsigned)blocks, kCsrWarpsPerBlock * 32, 0, s>>>(
-        Z, rowPtrs, colIdx, value, desc, (int)nFull, x, y, devStatus);
+    if (blocks > nGroups) blocks = nGroups;
+    k_spmv_csr_tma<<<(unsigned)blocks, (kCsrConsumerWarps + 1) * 32, kCsrTmaSmemBytes, s>>>(
+        Z, rowPtrs, colIdx, value, desc, (int)nGroups, x, y, devStatus);
     ++n;
   }
-  const long long p0 = tma ? nFull : 0;
+  const long long p0 = tma ? nGroups * kCsrGroupChunks : 0;
   if (p0 < nChunks) {
     const long long warps = nChunks - p0;
     k_spmv_csr_plain<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
