@@ -90,6 +90,9 @@ typedef struct {
                                divided by the mean group nnz: one group per warp */
   int32_t auto_format;      /* spmv_format chosen by spmv_select */
   int32_t auto_hyb_width;   /* HYB width used when spmv_convert_hyb gets 0 */
+  double gather_lines;      /* x locality, sampled: distinct 128-byte lines of x touched
+                               by 32 gathers of consecutive nonzeros (1 = all in one line,
+                               32 = all in different lines); 0 when not sampled */
 } spmv_stats;
 
 /* Read-only view of one converted format (device pointers owned by the

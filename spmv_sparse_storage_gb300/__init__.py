@@ -46,7 +46,7 @@ class spmv_stats(C.Structure):
                 ("sum_sq_len", C.c_int64), ("mean_len", C.c_double), ("var_len", C.c_double),
                 ("hist_log2", C.c_int64 * 33), ("imbalance_thread", C.c_double),
                 ("imbalance_warp", C.c_double), ("auto_format", C.c_int32),
-                ("auto_hyb_width", C.c_int32)]
+                ("auto_hyb_width", C.c_int32), ("gather_lines", C.c_double)]
 
 
 class spmv_arrays(C.Structure):

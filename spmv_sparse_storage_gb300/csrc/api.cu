@@ -370,6 +370,7 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
     S.imbalance_warp = (double)hst->maxWarpNnz / ((double)nnz / groups);
   }
   h->histExact.assign(hst->histExact, hst->histExact + spmv::kExactLenBins);
+  S.gather_lines = hst->gatherSets ? (double)hst->gatherLines / (double)hst->gatherSets : 0.0;
   S.auto_format = select_format(numRows, nnz, S.max_len);
   S.auto_hyb_width = auto_hyb_width(h);
   h->release(tmp, s);
@@ -551,8 +552,9 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   h->lastStream = s;
   switch (format) {
     case SPMV_CSR:
-      return record(spmv::launch_spmv_csr(h->R, h->Z, h->rowPtrs, h->colIdx, h->value,
-                                          h->chunkDesc, d_x, d_y, h->devStatus, s));
+      return record(spmv::launch_spmv_csr(
+          h->R, h->Z, h->rowPtrs, h->colIdx, h->value, h->chunkDesc, d_x, d_y, h->devStatus,
+          h->stats.gather_lines > 0.0 && h->stats.gather_lines <= spmv::kCsrPipelineMaxLines, s));
     case SPMV_COO:
       return record(spmv::launch_spmv_coo(h->Z, h->cooRow, h->colIdx, h->value, d_x, d_y,
                                           false, s));

@@ -32,6 +32,8 @@ struct DevStats {
   int maxWarpNnz;
   int pad0;
   unsigned long long sumSq;
+  unsigned long long gatherLines;   // sampled: distinct 128-byte x lines per gather set
+  unsigned long long gatherSets;    // sampled: number of 32-lane gather sets
   unsigned long long histLog2[33];  // rows with len >= kExactLenBins only
   unsigned int histExact[kExactLenBins];
 };
@@ -63,6 +65,11 @@ constexpr int kCsrChunkHasEmptyRow = 1;
 constexpr int kCsrConsumerWarps = 16;              // per block, one chunk each per stage
 constexpr int kCsrGroupChunks = kCsrConsumerWarps;  // chunks moved by one stage
 constexpr int kCsrStages = 4;                       // stages in flight per block
+// Gathers of x touching at most this many distinct 128-byte lines per 32
+// lanes (banded matrices) use the shared-memory pipeline; more scattered
+// gathers are limited by the L1 and use one warp per chunk.
+constexpr double kCsrPipelineMaxLines = 12.0;
+constexpr int kGatherSampleBlocks = 64;  // blocks of the column check that sample gathers
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
@@ -108,7 +115,7 @@ cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks
                                    CsrChunkDesc* desc, cudaStream_t s);
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const float* value, const CsrChunkDesc* desc, const float* x,
-                            float* y, int* devStatus, cudaStream_t s);
+                            float* y, int* devStatus, bool pipelined, cudaStream_t s);
 cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__((kCsrConsumerWarps + 1) * 32, 3) k_spmv_csr_tm
 
 // Chunks [c0, c1) with plain loads: the partial last chunk, and every chunk
 // when colIdx/value are not 16-byte aligned. One warp per chunk.
+template <bool VEC>
 __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, long long c1,
                                                         const int* __restrict__ rowPtrs,
                                                         const int* __restrict__ colIdx,
@@ -240,10 +241,19 @@ __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, lon
   const long long base = cb + 4 * lane;
   const CsrChunkDesc d = desc[c];
   float p[4];
+  if (VEC && base + 4 <= Z) {
+    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
+    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+    p[0] = v4.x * ld_x(x + c4.x);
+    p[1] = v4.y * ld_x(x + c4.y);
+    p[2] = v4.z * ld_x(x + c4.z);
+    p[3] = v4.w * ld_x(x + c4.w);
+  } else {
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const long long k = base + e;
-    p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : 0.0f;
+    for (int e = 0; e < 4; ++e) {
+      const long long k = base + e;
+      p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : 0.0f;
+    }
   }
   int row[4];
   csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
@@ -532,11 +542,12 @@ cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks
 
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const float* value, const CsrChunkDesc* desc, const float* x,
-                            float* y, int* devStatus, cudaStream_t s) {
+                            float* y, int* devStatus, bool pipelined, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
   const long long nGroups = (long long)Z / ((long long)kCsrGroupChunks * kCsrChunk);
-  const bool tma = aligned16(colIdx) && aligned16(value) && nGroups > 0;
+  const bool vec = aligned16(colIdx) && aligned16(value);
+  const bool tma = pipelined && vec && nGroups > 0;
   int n = 0;
   if (tma) {
     static int perSm = 0;  // blocks per SM (same on every device of one architecture)
@@ -559,8 +570,13 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
   const long long p0 = tma ? nGroups * kCsrGroupChunks : 0;
   if (p0 < nChunks) {
     const long long warps = nChunks - p0;
-    k_spmv_csr_plain<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(
-        Z, p0, nChunks, rowPtrs, colIdx, value, desc, x, y);
+    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+    if (vec)
+      k_spmv_csr_plain<true><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value, desc,
+                                                    x, y);
+    else
+      k_spmv_csr_plain<false><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
+                                                     desc, x, y);
     ++n;
   }
   note_launches(n);

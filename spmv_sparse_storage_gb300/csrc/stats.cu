@@ -36,6 +36,8 @@ __global__ void k_stats_init(DevStats* st, unsigned* histRep) {
       st->maxWarpNnz = 0;
       st->pad0 = 0;
       st->sumSq = 0ull;
+      st->gatherLines = 0ull;
+      st->gatherSets = 0ull;
     }
   }
 }
@@ -211,16 +213,35 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
   int firstBad = INT_MAX;
   const long long stride = (long long)gridDim.x * blockDim.x;
   long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const bool sample = blockIdx.x < kGatherSampleBlocks;
+  unsigned long long lines = 0ull, sets = 0ull;
   if (VEC) {
     const long long nv = Z / 4;
     const int4* c4 = reinterpret_cast<const int4*>(colIdx);
-    for (; i < nv; i += stride) {
-      const int4 c = ld_stream(c4 + i);
+    // all lanes of a warp run the same number of iterations (the bound only
+    // depends on the warp's first index), so the warp match below is uniform
+    long long i0 = i - (threadIdx.x & 31);
+    for (; i0 < nv; i += stride) {
+      const bool in = i < nv;
+      const int4 c = in ? ld_stream(c4 + i) : make_int4(0, 0, 0, 0);
       const int k = (int)(4 * i);
-      if ((unsigned)c.x >= uc) firstBad = min(firstBad, k);
-      if ((unsigned)c.y >= uc) firstBad = min(firstBad, k + 1);
-      if ((unsigned)c.z >= uc) firstBad = min(firstBad, k + 2);
-      if ((unsigned)c.w >= uc) firstBad = min(firstBad, k + 3);
+      if (in) {
+        if ((unsigned)c.x >= uc) firstBad = min(firstBad, k);
+        if ((unsigned)c.y >= uc) firstBad = min(firstBad, k + 1);
+        if ((unsigned)c.z >= uc) firstBad = min(firstBad, k + 2);
+        if ((unsigned)c.w >= uc) firstBad = min(firstBad, k + 3);
+      }
+      if (sample) {
+        // distinct 128-byte lines of x among the 32 gathers of one warp load
+        const unsigned ln = in ? ((unsigned)c.x >> 5) : 0xffffffffu;
+        const unsigned peers = __match_any_sync(kFullMask, ln);
+        const bool leader = (threadIdx.x & 31) == __ffs(peers) - 1;
+        if (i0 + 32 <= nv) {  // full sets only
+          if (leader) ++lines;
+          if ((threadIdx.x & 31) == 0) ++sets;
+        }
+      }
+      i0 += stride;
     }
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long k = 4 * nv + t;
@@ -232,6 +253,27 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
   if (firstBad != INT_MAX) {
     atomicOr(&st->err, kErrColRange);
     atomicMin(&st->firstBadNnz, firstBad);
+  }
+  if (VEC && sample) {
+    __shared__ unsigned long long sL[8], sS[8];
+    lines = warp_sum(lines);
+    sets = warp_sum(sets);
+    if ((threadIdx.x & 31) == 0) {
+      sL[threadIdx.x >> 5] = lines;
+      sS[threadIdx.x >> 5] = sets;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long L = 0ull, S = 0ull;
+      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+        L += sL[w];
+        S += sS[w];
+      }
+      if (S) {
+        atomicAdd(&st->gatherLines, L);
+        atomicAdd(&st->gatherSets, S);
+      }
+    }
   }
 }
 

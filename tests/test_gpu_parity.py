@@ -409,3 +409,17 @@ def test_launch_counter_counts_kernels(sp, orc):
         m.run("CSR", x, y)
         m.run("HYB", x, y)
         assert sp.spmv_launch_count() - n0 == 3
+
+
+def test_gather_locality_statistic(sp):
+    """Banded matrices touch few 128-byte lines of x per 32 gathers; uniform
+    random columns touch nearly 32 (the statistic picks the CSR kernel)."""
+    band = synth.laplace2d(256)
+    rand = synth.uniform_rows("rand", 200_000, 8)
+    got = {}
+    for inp in (band, rand):
+        with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                             dev(inp.value)) as m:
+            got[inp.name] = m.stats()["gather_lines"]
+    assert 0 < got["laplace2d"] <= 8, got
+    assert got["rand"] >= 24, got
