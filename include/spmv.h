@@ -187,6 +187,30 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays *out);
  * uses the handle must be complete. NULL is accepted. */
 int spmv_destroy(spmv_handle h);
 
+/* y <- A*x + y straight from CSR arrays, with no handle and no allocation.
+ * (The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory -- code running while a stream is captured
+ * into a CUDA graph, processes whose device memory is fully reserved by
+ * another allocator or pool, real-time loops that forbid allocation.)
+ *   Arguments as spmv_create_csr plus d_x (numCols floats) and d_y (numRows
+ *   floats); all device pointers on the current device, x and y not
+ *   overlapping. The CSR input is NOT validated: pass arrays that
+ *   spmv_create_csr would accept.
+ *   Scratch: the per-chunk row index lives in a fixed array of device global
+ *   memory reserved by the library (1 MiB on every GPU that loads it, held
+ *   until the process exits), so nnz is limited to 4,194,304 (32768 chunks of
+ *   128); a larger nnz returns SPMV_ERR_TOO_LARGE and does nothing.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the array's device address; make that first call before any stream
+ *   capture. Calls neither allocate nor free memory.
+ *   Concurrency: every call reuses the same array, so calls that overlap on
+ *   the GPU (different streams, no ordering between them) race and give
+ *   wrong results; calls ordered on one stream are fine.
+ *   Asynchronous on `stream`; launches 3 kernels and 1 memset. */
+int spmv_run_csr_noalloc(int32_t numRows, int32_t numCols, int32_t nnz,
+                         const int32_t *d_rowPtrs, const int32_t *d_colIdx,
+                         const float *d_value, const float *d_x, float *d_y, void *stream);
+
 /* Static English text for a status code. */
 const char *spmv_status_string(int status);
 

@@ -71,6 +71,7 @@ _SIGS = {
     "spmv_get_stats": (C.c_int, [_H, C.POINTER(spmv_stats)]),
     "spmv_export": (C.c_int, [_H, C.c_int, C.POINTER(spmv_arrays)]),
     "spmv_destroy": (C.c_int, [_H]),
+    "spmv_run_csr_noalloc": (C.c_int, [C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P, _P, _P]),
     "spmv_status_string": (C.c_char_p, [C.c_int]),
     "spmv_last_cuda_error": (C.c_int, []),
     "spmv_launch_count": (C.c_uint64, []),
@@ -178,6 +179,16 @@ def spmv_export(h, fmt):
 
 def spmv_destroy(h):
     _check(_lib.spmv_destroy(h), "spmv_destroy")
+
+
+def spmv_run_csr_noalloc(num_rows, num_cols, nnz, row_ptrs, col_idx, value, x, y,
+                         stream=None):
+    """y <- A x + y from CSR arrays without a handle or any allocation (see
+    spmv.h: nnz <= 4,194,304; first call on a device before stream capture;
+    calls that overlap on the GPU race)."""
+    _check(_lib.spmv_run_csr_noalloc(num_rows, num_cols, nnz, _ptr(row_ptrs), _ptr(col_idx),
+                                     _ptr(value), _ptr(x), _ptr(y), _stream(stream)),
+           "spmv_run_csr_noalloc")
 
 
 def spmv_status_string(code):
