@@ -493,14 +493,28 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   const int L = (int)h->stats.max_len;
   SPMV_TRY(alloc_typed(h, h->R, s, &h->jdsPerm, h->jdsBufs));
   SPMV_TRY(alloc_typed(h, (long long)L + 1, s, &h->jdsIterPtr, h->jdsBufs));
-  SPMV_TRY(alloc_typed(h, h->Z, s, &h->jdsCol, h->jdsBufs));
-  SPMV_TRY(alloc_typed(h, h->Z, s, &h->jdsVal, h->jdsBufs));
+  // padded so that the SpMV kernel's aligned 16-byte reads stay inside
+  SPMV_TRY(alloc_typed(h, (long long)h->Z + spmv::kJdsPad, s, &h->jdsCol, h->jdsBufs));
+  SPMV_TRY(alloc_typed(h, (long long)h->Z + spmv::kJdsPad, s, &h->jdsVal, h->jdsBufs));
+  // iterPtr from the exact length histogram when every row is shorter than
+  // kExactLenBins: iterPtr[t+1] = iterPtr[t] + #{rows longer than t}
+  std::vector<int> hostIp;
+  if (L > 0 && L < spmv::kExactLenBins) {
+    hostIp.assign((size_t)L + 1, 0);
+    long long le = 0, acc = 0;
+    for (int t = 0; t < L; ++t) {
+      le += h->histExact[t];
+      acc += (long long)h->R - le;
+      hostIp[(size_t)t + 1] = (int)acc;
+    }
+  }
   std::vector<Buf> tmp;
   void* scratch = nullptr;
   int st = h->alloc(spmv::jds_sort_scratch_bytes(h->R, L), s, &scratch, tmp);
   if (st == SPMV_OK)
     st = record(spmv::launch_jds_build(h->R, L, h->rowPtrs, h->colIdx, h->value, h->jdsPerm,
-                                       h->jdsIterPtr, h->jdsCol, h->jdsVal, scratch, s));
+                                       h->jdsIterPtr, h->jdsCol, h->jdsVal, scratch,
+                                       hostIp.empty() ? nullptr : hostIp.data(), s));
   h->release(tmp, s);
   if (st != SPMV_OK) return st;
   // Row-parallel part: the leading diagonals at least min(kJdsSplitMinWidth,

@@ -265,20 +265,29 @@ struct SortIn {
 };
 
 // Per tile, count keys per digit; hist is digit-major: hist[d * nTiles + tile].
+// All of a thread's keys are loaded before any is counted; equal digits in a
+// warp are counted with one shared atomic (warp match).
 __global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, int shift, int nTiles,
                                                              int* __restrict__ hist) {
   __shared__ int sCount[kRadix];
   for (int d = threadIdx.x; d < kRadix; d += kSortThreads) sCount[d] = 0;
   __syncthreads();
+  const int lane = threadIdx.x & 31;
   const long long base = (long long)blockIdx.x * kSortTile;
+  int key[kSortRounds];
 #pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
     const long long i = base + rd * kSortThreads + threadIdx.x;
-    if (i < R) {
-      int key, val;
-      in.get(i, key, val);
-      atomicAdd(&sCount[(key >> shift) & (kRadix - 1)], 1);
-    }
+    int val;
+    key[rd] = 0;
+    if (i < R) in.get(i, key[rd], val);
+  }
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    const int digit = i < R ? (key[rd] >> shift) & (kRadix - 1) : kRadix;
+    const unsigned peers = __match_any_sync(kFullMask, digit);
+    if (digit < kRadix && lane == __ffs(peers) - 1) atomicAdd(&sCount[digit], __popc(peers));
   }
   __syncthreads();
   for (int d = threadIdx.x; d < kRadix; d += kSortThreads)
@@ -287,11 +296,14 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, i
 
 // Stable scatter: rank of each item among equal digits = tile offset (from the
 // scanned histogram) + items of earlier rounds + earlier warps of this round +
-// earlier lanes of this warp (found with a warp match).
+// earlier lanes of this warp (found with a warp match). All keys are loaded
+// before the first round. The last pass also writes the inverse permutation
+// (invOut[row] = sorted position) when invOut is given.
 __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R, int shift, int nTiles,
                                                                 const int* __restrict__ offs,
                                                                 int* __restrict__ keysOut,
-                                                                int* __restrict__ valsOut) {
+                                                                int* __restrict__ valsOut,
+                                                                int* __restrict__ invOut) {
   constexpr int kWarps = kSortThreads / 32;
   __shared__ int sRun[kRadix];             // running count per digit in this tile
   __shared__ int sWarpCnt[kWarps][kRadix];  // per-warp counts of the current round
@@ -301,16 +313,21 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R
 #pragma unroll
     for (int q = 0; q < kWarps; ++q) sWarpCnt[q][d] = 0;
   }
-  __syncthreads();
   const long long base = (long long)blockIdx.x * kSortTile;
+  int key[kSortRounds], val[kSortRounds];
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    key[rd] = 0;
+    val[rd] = 0;
+    if (i < R) in.get(i, key[rd], val[rd]);
+  }
+  __syncthreads();
+#pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
     const long long i = base + rd * kSortThreads + threadIdx.x;
     const bool valid = i < R;
-    int key = 0, val = 0, digit = kRadix;  // invalid items get a digit no one shares
-    if (valid) {
-      in.get(i, key, val);
-      digit = (key >> shift) & (kRadix - 1);
-    }
+    const int digit = valid ? (key[rd] >> shift) & (kRadix - 1) : kRadix;  // kRadix: no one shares
     const unsigned peers = __match_any_sync(kFullMask, digit);
     const int rankInWarp = __popc(peers & lanemask_lt());
     const int leader = __ffs(peers) - 1;
@@ -320,8 +337,9 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R
       int before = sRun[digit];
       for (int q = 0; q < w; ++q) before += sWarpCnt[q][digit];
       const int pos = before + rankInWarp;
-      keysOut[pos] = key;
-      valsOut[pos] = val;
+      keysOut[pos] = key[rd];
+      valsOut[pos] = val[rd];
+      if (invOut) invOut[val[rd]] = pos;
     }
     __syncthreads();
     for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
@@ -339,6 +357,8 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R
 
 // Diagonal widths from the sorted lengths: width(t) = #{s : len(s) > t}. With
 // lengths non-increasing over s, width(t) = s+1 for t in [len(s+1), len(s)).
+// (Used when some row is at least kExactLenBins long; otherwise iterPtr comes
+// from the exact length histogram.)
 __global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKeys,
                              int* __restrict__ width) {
   const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -348,27 +368,38 @@ __global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKe
   for (int t = next; t < len; ++t) width[t] = (int)(s + 1);
 }
 
-// Jagged scatter: entry t of sorted row s goes to iterPtr[t] + s. A thread per
-// sorted row handles its first kCoop entries (coalesced over s); the warp then
-// walks each longer row's remaining entries together, one entry per lane.
+// Jagged scatter, row side: entry t of original row r goes to
+// iterPtr[t] + inv[r] (inv = sorted position). Rows are read in CSR order
+// (coalesced row pointers, row-contiguous entries); consecutive rows of one
+// length have consecutive sorted positions, so the writes of a warp are
+// contiguous per diagonal. A thread copies the first kCoop entries of its
+// row; the warp then copies each longer row's remaining entries together,
+// one entry per lane. The first kJdsScatterSmem entries of iterPtr are
+// staged in shared memory.
 constexpr int kCoop = 64;
-__global__ void __launch_bounds__(256) k_jds_scatter(int R, const int* __restrict__ rowPtrs,
+constexpr int kJdsScatterSmem = 1024;
+__global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
+                                                     const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
                                                      const float* __restrict__ value,
-                                                     const int* __restrict__ perm,
+                                                     const int* __restrict__ inv,
                                                      const int* __restrict__ iterPtr,
                                                      int* __restrict__ jdsCol,
                                                      float* __restrict__ jdsVal) {
-  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  __shared__ int sIp[kJdsScatterSmem];
+  const int nIp = maxLen < kJdsScatterSmem ? maxLen : kJdsScatterSmem;
+  for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = iterPtr[t];
+  __syncthreads();
+  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
-  int a = 0, len = 0;
-  if (s < R) {
-    const int r = perm[s];
+  int a = 0, len = 0, srow = 0;
+  if (r < R) {
     a = rowPtrs[r];
     len = rowPtrs[r + 1] - a;
+    srow = inv[r];
     const int lim = len < kCoop ? len : kCoop;
     for (int t = 0; t < lim; ++t) {
-      const long long o = (long long)iterPtr[t] + s;
+      const long long o = (long long)sIp[t] + srow;
       jdsCol[o] = colIdx[a + t];
       jdsVal[o] = value[a + t];
     }
@@ -379,9 +410,10 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, const int* __restric
     longRows &= longRows - 1;
     const int la = __shfl_sync(kFullMask, a, src);
     const int ll = __shfl_sync(kFullMask, len, src);
-    const long long ss = s - lane + src;
+    const int ls = __shfl_sync(kFullMask, srow, src);
     for (int t = kCoop + lane; t < ll; t += 32) {
-      const long long o = (long long)iterPtr[t] + ss;
+      const int ip = t < kJdsScatterSmem ? sIp[t] : __ldg(iterPtr + t);
+      const long long o = (long long)ip + ls;
       jdsCol[o] = colIdx[la + t];
       jdsVal[o] = value[la + t];
     }
@@ -430,18 +462,19 @@ cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* co
 }
 
 // Scratch layout for the JDS build (all int32):
-//   keysA[R] valsA[R] keysB[R] hist[kRadix*nTiles + 1] scanScratch[...] width[maxLen]
+//   keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles + 1] scanScratch[...] width[maxLen]
 size_t jds_sort_scratch_bytes(int R, int maxLen) {
   const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
   const long long nh = (long long)kRadix * (nTiles > 0 ? nTiles : 1);
   const long long scanN = nh > maxLen ? nh : maxLen;
-  const long long ints = 3LL * R + (nh + 1) + (long long)scan_scratch_ints(scanN) + maxLen + 16;
+  const long long ints = 4LL * R + (nh + 1) + (long long)scan_scratch_ints(scanN) + maxLen + 16;
   return (size_t)ints * sizeof(int);
 }
 
 cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
                              const float* value, int* perm, int* iterPtr, int* jdsCol,
-                             float* jdsVal, void* scratch, cudaStream_t s) {
+                             float* jdsVal, void* scratch, const int* hostIterPtr,
+                             cudaStream_t s) {
   if (R <= 0) {
     // iterPtr has maxLen + 1 = 1 entry
     return cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
@@ -451,7 +484,8 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
   int* keysA = static_cast<int*>(scratch);
   int* valsA = keysA + R;
   int* keysB = valsA + R;
-  int* hist = keysB + R;
+  int* inv = keysB + R;
+  int* hist = inv + R;
   int* scanScratch = hist + nh + 1;
   const long long scanN = nh > maxLen ? nh : maxLen;
   int* width = scanScratch + scan_scratch_ints(scanN);
@@ -459,11 +493,9 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
   int bits = 0;
   while (bits < 31 && (1LL << bits) <= maxLen) ++bits;
   const int passes = bits == 0 ? 1 : (bits + kRadixBits - 1) / kRadixBits;
-  // Ping-pong so that the last pass writes perm (values) and keysA (keys).
-  // pass p reads (kIn, vIn), writes (kOut, vOut).
+  // Ping-pong so that the last pass writes perm (values) and keysB (keys).
   int* kBuf[2] = {keysA, keysB};
   int* vBuf[2] = {valsA, perm};
-  // choose the first output slot so that the final pass lands in slot 1
   int outSlot = (passes % 2 == 1) ? 1 : 0;
   const int* kIn = nullptr;
   const int* vIn = nullptr;
@@ -475,23 +507,30 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
     note_launches(1);
     err = exclusive_scan(ArrayIn{hist}, nh, hist, scanScratch, s);
     if (err != cudaSuccess) return err;
-    k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, (int)nTiles, hist,
-                                                             kBuf[outSlot], vBuf[outSlot]);
+    k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(
+        in, R, shift, (int)nTiles, hist, kBuf[outSlot], vBuf[outSlot],
+        p == passes - 1 ? inv : nullptr);
     note_launches(1);
     kIn = kBuf[outSlot];
     vIn = vBuf[outSlot];
     outSlot ^= 1;
   }
-  const int* sortedKeys = kIn;  // == keysB when the final pass used slot 1
-  // widths and iterPtr
+  const int* sortedKeys = kIn;
   if (maxLen > 0) {
-    k_jds_widths<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(R, maxLen, sortedKeys,
-                                                                       width);
-    note_launches(1);
-    err = exclusive_scan(ArrayIn{width}, (long long)maxLen, iterPtr, scanScratch, s);
-    if (err != cudaSuccess) return err;
+    if (hostIterPtr) {
+      // widths known exactly on the host from the length histogram
+      err = cudaMemcpyAsync(iterPtr, hostIterPtr, sizeof(int) * ((size_t)maxLen + 1),
+                            cudaMemcpyHostToDevice, s);
+      if (err != cudaSuccess) return err;
+    } else {
+      k_jds_widths<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(R, maxLen, sortedKeys,
+                                                                         width);
+      note_launches(1);
+      err = exclusive_scan(ArrayIn{width}, (long long)maxLen, iterPtr, scanScratch, s);
+      if (err != cudaSuccess) return err;
+    }
     k_jds_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
-        R, rowPtrs, colIdx, value, perm, iterPtr, jdsCol, jdsVal);
+        R, maxLen, rowPtrs, colIdx, value, inv, iterPtr, jdsCol, jdsVal);
     note_launches(1);
   } else {
     err = cudaMemsetAsync(iterPtr, 0, sizeof(int), s);

@@ -75,7 +75,6 @@ constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thr
 constexpr int kJdsSplitMaxDiag = 1024;   // at most this many diagonals in the row-parallel part
 constexpr int kJdsTailRows = 256;        // tail blocks: sorted rows per block
 constexpr int kJdsTailDiags = 64;        // tail blocks: diagonals per block
-constexpr int kJdsRowsPerThread = 4;     // row-parallel part: sorted rows per thread
 
 // ---------------------------------------------------------------------------
 // Launch accounting (every launcher reports its kernels).
@@ -105,9 +104,12 @@ cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* co
                                  int* cooCol, float* cooVal, cudaStream_t s);
 // JDS: stable sort of rows by length (longest first), iterPtr, jagged scatter.
 size_t jds_sort_scratch_bytes(int R, int maxLen);
+// hostIterPtr: iterPtr computed on the host (nullptr: computed on the device)
 cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
                              const float* value, int* perm, int* iterPtr, int* jdsCol,
-                             float* jdsVal, void* scratch, cudaStream_t s);
+                             float* jdsVal, void* scratch, const int* hostIterPtr,
+                             cudaStream_t s);
+constexpr int kJdsPad = 8;  // extra elements after the JDS arrays (aligned vector reads)
 
 // spmv_kernels.cu
 // fills hi, flags and mask of every chunk record; runs after the stats pass

@@ -429,16 +429,17 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // s < width(t), contiguous in s, so a warp's loads are coalesced. Widths only
 // shrink with t; the first tSplit diagonals (those at least
 // kJdsSplitMinWidth wide, at most kJdsSplitMaxDiag of them) run one thread
-// per sorted row (kJdsRowsPerThread rows per thread, 256 rows apart so that
-// every load instruction stays coalesced), with the loads of 4 diagonals of
-// all its rows in flight at once. The remaining diagonals belong to the few
+// per sorted row, 4 consecutive rows per thread read with one aligned
+// 16-byte load per diagonal and array (diagonals start anywhere, so lanes
+// realign with one shuffle from the next lane; the arrays are padded so the
+// last vector stays inside). The remaining diagonals belong to the few
 // longest rows (s < wTail) and would serialise one thread over thousands of
 // entries, so they are split into blocks of kJdsTailRows rows x
 // kJdsTailDiags diagonals that run in parallel and add their partial sums
 // atomically. The result of sorted row s goes straight to y[perm[s]] (the
 // page permutes the result back with the row array).
 // ===========================================================================
-__global__ void __launch_bounds__(256, 3) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
+__global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
                                                      const int* __restrict__ perm,
@@ -450,62 +451,81 @@ __global__ void __launch_bounds__(256, 3) k_spmv_jds(int R, int maxLen, int tSpl
   if ((int)blockIdx.x < nMainBlocks) {
     for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
     __syncthreads();
-    constexpr int U = kJdsRowsPerThread;
-    const long long s0 = (long long)blockIdx.x * blockDim.x * U + threadIdx.x;
-    int r[U], n[U];
-    float acc[U], y0[U];
-    int nmax = 0;
+    const int lane = threadIdx.x & 31;
+    const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long s0 = 4 * q;                                 // first of this thread's 4 rows
+    const long long warpFirst = 4 * (q - lane);                 // first row of the warp
+    const int4* col4 = reinterpret_cast<const int4*>(jdsCol);  // padded by kJdsPad entries
+    const float4* val4 = reinterpret_cast<const float4*>(jdsVal);
+    int r[4];
+    if (s0 + 4 <= R) {
+      const int4 p4 = __ldg(reinterpret_cast<const int4*>(perm) + q);
+      r[0] = p4.x; r[1] = p4.y; r[2] = p4.z; r[3] = p4.w;
+    } else {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long s = s0 + (long long)u * blockDim.x;
-      r[u] = s < R ? ld_stream(perm + s) : -1;
-      // number of leading diagonals wider than s (binary search; widths shrink)
-      int lo = 0, hi = s < R ? tSplit : 0;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (sIp[mid + 1] - sIp[mid] > s)
-          lo = mid + 1;
-        else
-          hi = mid;
+      for (int e = 0; e < 4; ++e) r[e] = s0 + e < R ? __ldg(perm + s0 + e) : -1;
+    }
+    float y0[4], acc[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      y0[e] = (r[e] >= 0 && s0 + e >= wTail) ? y[r[e]] : 0.0f;
+      acc[e] = 0.0f;
+    }
+    for (int t = 0; t < tSplit; ++t) {
+      const int a = sIp[t];
+      const int wt = sIp[t + 1] - a;
+      if (warpFirst >= wt) break;  // widths shrink: no later diagonal reaches this warp
+      // rows s0..s0+3 of diagonal t sit at a+s0 .. a+s0+3, m entries past a
+      // 16-byte boundary (m is the same in every lane): lane q reads the
+      // aligned vector holding rows s0-m .. s0-m+3 and takes the rest from
+      // lane q+1's vector (the last lane reads that one itself)
+      const int m = a & 3;
+      const long long vi = ((long long)(a - m) >> 2) + q;
+      int4 cv = make_int4(0, 0, 0, 0);
+      float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 - m < wt) {
+        cv = ld_stream(col4 + vi);
+        vv = ld_stream(val4 + vi);
       }
-      n[u] = lo;
-      nmax = max(nmax, lo);
-      acc[u] = 0.0f;
-    }
+      int cw[4];
+      float fw[4];
+      if (m == 0) {
+        cw[0] = cv.x; cw[1] = cv.y; cw[2] = cv.z; cw[3] = cv.w;
+        fw[0] = vv.x; fw[1] = vv.y; fw[2] = vv.z; fw[3] = vv.w;
+      } else {
+        int4 cn;
+        float4 vn;
+        cn.x = __shfl_down_sync(kFullMask, cv.x, 1);
+        cn.y = __shfl_down_sync(kFullMask, cv.y, 1);
+        cn.z = __shfl_down_sync(kFullMask, cv.z, 1);
+        cn.w = __shfl_down_sync(kFullMask, cv.w, 1);
+        vn.x = __shfl_down_sync(kFullMask, vv.x, 1);
+        vn.y = __shfl_down_sync(kFullMask, vv.y, 1);
+        vn.z = __shfl_down_sync(kFullMask, vv.z, 1);
+        vn.w = __shfl_down_sync(kFullMask, vv.w, 1);
+        if (lane == 31 && s0 + 4 - m < wt) {
+          cn = ld_stream(col4 + vi + 1);
+          vn = ld_stream(val4 + vi + 1);
+        }
+        const int ca[8] = {cv.x, cv.y, cv.z, cv.w, cn.x, cn.y, cn.z, cn.w};
+        const float fa[8] = {vv.x, vv.y, vv.z, vv.w, vn.x, vn.y, vn.z, vn.w};
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long s = s0 + (long long)u * blockDim.x;
-      y0[u] = (r[u] >= 0 && s >= wTail) ? y[r[u]] : 0.0f;
-    }
-    for (int t = 0; t < nmax; t += 4) {
-      int c[U][4];
-      float v[U][4];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const long long s = s0 + (long long)u * blockDim.x;
-#pragma unroll
-        for (int d = 0; d < 4; ++d) {
-          if (t + d < n[u]) {
-            const long long i = (long long)sIp[t + d] + s;
-            c[u][d] = ld_stream(jdsCol + i);
-            v[u][d] = ld_stream(jdsVal + i);
-          }
+        for (int e = 0; e < 4; ++e) {
+          cw[e] = m == 1 ? ca[e + 1] : m == 2 ? ca[e + 2] : ca[e + 3];
+          fw[e] = m == 1 ? fa[e + 1] : m == 2 ? fa[e + 2] : fa[e + 3];
         }
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u)
-#pragma unroll
-        for (int d = 0; d < 4; ++d)
-          if (t + d < n[u]) acc[u] = fmaf(v[u][d], ld_x(x + c[u][d]), acc[u]);
+      for (int e = 0; e < 4; ++e)
+        if (s0 + e < wt) acc[e] = fmaf(fw[e], ld_x(x + cw[e]), acc[e]);
     }
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const long long s = s0 + (long long)u * blockDim.x;
-      if (r[u] < 0) continue;
-      if (s < wTail)
-        atomicAdd(y + r[u], acc[u]);  // the tail blocks add to this row too
+    for (int e = 0; e < 4; ++e) {
+      if (r[e] < 0) continue;
+      if (s0 + e < wTail)
+        atomicAdd(y + r[e], acc[e]);  // the tail blocks add to this row too
       else
-        y[r[u]] = y0[u] + acc[u];
+        y[r[e]] = y0[e] + acc[e];
     }
   } else {
     const int b = blockIdx.x - nMainBlocks;
@@ -627,7 +647,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
                             const int* perm, const int* jdsCol, const float* jdsVal,
                             const float* x, float* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
-  const long long mainBlocks = ((long long)R + 256 * kJdsRowsPerThread - 1) / (256 * kJdsRowsPerThread);
+  const long long mainBlocks = ((long long)R + 1023) / 1024;  // 4 sorted rows per thread
   long long tailBlocks = 0;
   int tailRowBlocks = 1;
   if (tSplit < maxLen && wTail > 0) {
