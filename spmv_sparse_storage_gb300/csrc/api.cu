@@ -328,10 +328,12 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   if (st != SPMV_OK) return fail(st);
   st = record(cudaMemsetAsync(h->devStatus, 0, sizeof(int), s));
   if (st != SPMV_OK) return fail(st);
+  if (h->nChunks > 0) {  // masks and flags are OR-ed into zeroed records
+    st = record(cudaMemsetAsync(h->chunkDesc, 0, sizeof(spmv::CsrChunkDesc) * h->nChunks, s));
+    if (st != SPMV_OK) return fail(st);
+  }
   st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, statsScratch,
                                  h->nChunks, h->chunkDesc, s));
-  if (st != SPMV_OK) return fail(st);
-  st = record(spmv::launch_csr_chunk_masks(numRows, nnz, d_rowPtrs, h->nChunks, h->chunkDesc, s));
   if (st != SPMV_OK) return fail(st);
   hst = new (std::nothrow) DevStats;
   if (!hst) return fail(SPMV_ERR_ALLOC);
@@ -388,7 +390,7 @@ int spmv_convert_coo(spmv_handle h, void* stream) {
   h->release(h->cooBufs, s);
   h->hasCoo = false;
   SPMV_TRY(alloc_typed(h, h->Z, s, &h->cooRow, h->cooBufs));
-  SPMV_TRY(record(spmv::launch_expand_rows(h->R, h->rowPtrs, h->cooRow, s)));
+  SPMV_TRY(record(spmv::launch_expand_rows(h->R, h->Z, h->rowPtrs, h->chunkDesc, h->cooRow, s)));
   h->hasCoo = true;
   return SPMV_OK;
 }

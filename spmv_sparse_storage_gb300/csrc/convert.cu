@@ -20,11 +20,11 @@ namespace spmv {
 namespace {
 
 // ---------------------------------------------------------------------------
-// Warp-cooperative segmented expansion. A warp owns 32 consecutive segments
-// (rows) whose outputs are contiguous: segment j covers output positions
-// [start_j, start_{j+1}). The warp walks its output range 32 positions at a
-// time (coalesced writes); each lane finds its segment by a 5-step binary
-// search over the 32 starts held one per lane.
+// Warp-cooperative segmented expansion (the HYB tail). A warp owns 32
+// consecutive segments (rows) whose outputs are contiguous: segment j covers
+// output positions [start_j, start_{j+1}). The warp walks its output range 32
+// positions at a time (coalesced writes); each lane finds its segment by a
+// 5-step binary search over the 32 starts held one per lane.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int find_segment(int start, int k) {
   // largest lane j with start_j <= k (starts non-decreasing over lanes)
@@ -35,24 +35,6 @@ __device__ __forceinline__ int find_segment(int start, int k) {
     if (sc <= k) j += step;
   }
   return j;
-}
-
-// CSR -> COO: rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1].
-__global__ void __launch_bounds__(256) k_expand_rows(int R, const int* __restrict__ rowPtrs,
-                                                     int* __restrict__ rowIdx) {
-  const int lane = threadIdx.x & 31;
-  const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long r0 = warp * 32;
-  if (r0 >= R) return;
-  const long long r = r0 + lane;
-  const int start = r < R ? rowPtrs[r] : INT_MAX;
-  const int A = __shfl_sync(kFullMask, start, 0);
-  const int B = rowPtrs[min(r0 + 32, (long long)R)];
-  for (int base = A; base < B; base += 32) {
-    const int k = base + lane;
-    const int j = find_segment(start, k);
-    if (k < B) rowIdx[k] = (int)(r0 + j);
-  }
 }
 
 // CSR -> ELL of width K (also the ELL part of HYB): thread per row, writes
@@ -423,15 +405,6 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
 }  // namespace
 
 size_t scan_scratch_ints(long long n) { return (size_t)((n + kScanTile - 1) / kScanTile + 1); }
-
-cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s) {
-  if (R <= 0) return cudaSuccess;
-  const long long warps = ((long long)R + 31) / 32;
-  const long long blocks = (warps * 32 + 255) / 256;
-  k_expand_rows<<<(unsigned)blocks, 256, 0, s>>>(R, rowPtrs, rowIdx);
-  note_launches(1);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
                               const float* value, int* ellCol, float* ellVal, int* nnzPerRow,

@@ -91,7 +91,9 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
                          cudaStream_t s);
 
 // convert.cu
-cudaError_t launch_expand_rows(int R, const int* rowPtrs, int* rowIdx, cudaStream_t s);
+// CSR -> COO rowIdx from the CSR chunk records (spmv_kernels.cu)
+cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
+                               int* rowIdx, cudaStream_t s);
 cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
                               const float* value, int* ellCol, float* ellVal, int* nnzPerRow,
                               cudaStream_t s);

@@ -260,6 +260,31 @@ __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, lon
   warp_segmented_add(row, p, y, false);
 }
 
+// CSR -> COO ("Sparse Matrices and Basic Formats ...", section "COO format
+// and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. One warp per
+// 128-entry chunk: the rows come from the chunk record exactly as in the
+// CSR kernel, and each lane stores its 4 row ids with one 16-byte store.
+__global__ void __launch_bounds__(256) k_expand_rows(int Z, long long nChunks,
+                                                     const int* __restrict__ rowPtrs,
+                                                     const CsrChunkDesc* __restrict__ desc,
+                                                     int* __restrict__ rowIdx) {
+  const int lane = threadIdx.x & 31;
+  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (c >= nChunks) return;  // warp-uniform
+  const long long cb = c * kCsrChunk;
+  const long long base = cb + 4 * lane;
+  const CsrChunkDesc d = desc[c];
+  int row[4];
+  csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
+  if (base + 4 <= Z) {
+    __stcs(reinterpret_cast<int4*>(rowIdx + base), make_int4(row[0], row[1], row[2], row[3]));
+  } else {
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (base + e < Z) rowIdx[base + e] = row[e];
+  }
+}
+
 // Chunk records: hi from the next chunk's lo, and the positions where rows
 // start inside the chunk (or the empty-row flag). Thread per chunk, walking
 // the rows that start in it (at most kCsrChunk + 1 steps). Bounds are checked
@@ -550,6 +575,16 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
 }
 
 }  // namespace
+
+cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
+                               int* rowIdx, cudaStream_t s) {
+  if (R <= 0 || Z <= 0) return cudaSuccess;
+  const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
+  k_expand_rows<<<(unsigned)((nChunks * 32 + 255) / 256), 256, 0, s>>>(Z, nChunks, rowPtrs, desc,
+                                                                        rowIdx);
+  note_launches(1);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks,
                                    CsrChunkDesc* desc, cudaStream_t s) {

@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kStatsRowsPerThread = 8;
 constexpr int kStatsRows = 256 * kStatsRowsPerThread;
+constexpr int kColUnroll = 4;  // column check: vectors in flight per thread
 
 __global__ void k_stats_init(DevStats* st, unsigned* histRep) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     if (rowPtrs[0] != 0) atomicOr(&st->err, kErrRowPtrStart);
     if (rowPtrs[R] != Z) atomicOr(&st->err, kErrRowPtrEnd);
+    if (nChunks > 0) desc[nChunks - 1].hi = R > 0 ? R - 1 : 0;
   }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const long long base = (long long)blockIdx.x * kStatsRows + threadIdx.x;
@@ -96,12 +98,25 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       sq += (unsigned long long)len * (unsigned long long)len;
       if (lane == 0) gmax = max(gmax, g[i] - a[i]);
       if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
-      // chunks whose first nonzero lies in this row (bounds-checked: runs
-      // before the validation result is known)
+      // CSR chunk records (bounds-checked: this runs before the validation
+      // result is known). A nonempty row is `lo` of every chunk whose first
+      // nonzero it holds (and `hi` of the chunk before), and sets the bit of
+      // its start position in the chunk where it starts; an empty row inside
+      // a chunk flags that chunk.
       if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
         const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
         const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
-        for (int c = c0; c <= c1; ++c) desc[c].lo = (int)r;
+        for (int c = c0; c <= c1; ++c) {
+          desc[c].lo = (int)r;
+          if (c > 0) desc[c - 1].hi = (int)r;
+        }
+        const int pos = a[i] % kCsrChunk;
+        if (pos != 0) {
+          unsigned* m = reinterpret_cast<unsigned*>(&desc[a[i] / kCsrChunk].mask);
+          atomicOr(m + (pos >> 5), 1u << (pos & 31));
+        }
+      } else if (a[i] == b[i] && a[i] > 0 && a[i] < Z && a[i] % kCsrChunk != 0) {
+        atomicOr(&desc[a[i] / kCsrChunk].flags, kCsrChunkHasEmptyRow);
       }
     }
     // warp-aggregated exact histogram: one shared atomic per distinct length
@@ -218,22 +233,31 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
   if (VEC) {
     const long long nv = Z / 4;
     const int4* c4 = reinterpret_cast<const int4*>(colIdx);
-    // all lanes of a warp run the same number of iterations (the bound only
-    // depends on the warp's first index), so the warp match below is uniform
+    // kColUnroll vectors per thread per iteration, all loaded before any is
+    // checked; all lanes of a warp run the same number of iterations (the
+    // bound only depends on the warp's first index), so the warp match below
+    // is uniform
     long long i0 = i - (threadIdx.x & 31);
-    for (; i0 < nv; i += stride) {
-      const bool in = i < nv;
-      const int4 c = in ? ld_stream(c4 + i) : make_int4(0, 0, 0, 0);
-      const int k = (int)(4 * i);
-      if (in) {
-        if ((unsigned)c.x >= uc) firstBad = min(firstBad, k);
-        if ((unsigned)c.y >= uc) firstBad = min(firstBad, k + 1);
-        if ((unsigned)c.z >= uc) firstBad = min(firstBad, k + 2);
-        if ((unsigned)c.w >= uc) firstBad = min(firstBad, k + 3);
+    for (; i0 < nv; i += kColUnroll * stride, i0 += kColUnroll * stride) {
+      int4 c[kColUnroll];
+#pragma unroll
+      for (int u = 0; u < kColUnroll; ++u)
+        c[u] = i + u * stride < nv ? ld_stream(c4 + i + u * stride) : make_int4(0, 0, 0, 0);
+#pragma unroll
+      for (int u = 0; u < kColUnroll; ++u) {
+        const long long iu = i + u * stride;
+        if (iu < nv) {
+          const int k = (int)(4 * iu);
+          if ((unsigned)c[u].x >= uc) firstBad = min(firstBad, k);
+          if ((unsigned)c[u].y >= uc) firstBad = min(firstBad, k + 1);
+          if ((unsigned)c[u].z >= uc) firstBad = min(firstBad, k + 2);
+          if ((unsigned)c[u].w >= uc) firstBad = min(firstBad, k + 3);
+        }
       }
       if (sample) {
         // distinct 128-byte lines of x among the 32 gathers of one warp load
-        const unsigned ln = in ? ((unsigned)c.x >> 5) : 0xffffffffu;
+        const bool in = i < nv;
+        const unsigned ln = in ? ((unsigned)c[0].x >> 5) : 0xffffffffu;
         const unsigned peers = __match_any_sync(kFullMask, ln);
         const bool leader = (threadIdx.x & 31) == __ffs(peers) - 1;
         if (i0 + 32 <= nv) {  // full sets only
@@ -241,7 +265,6 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
           if ((threadIdx.x & 31) == 0) ++sets;
         }
       }
-      i0 += stride;
     }
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     const long long k = 4 * nv + t;
@@ -301,7 +324,7 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
     const bool vec = aligned16(colIdx);
     long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
     long long cb = (work + 255) / 256;
-    int gridC = (int)(cb < 1 ? 1 : (cb > 16LL * sms ? 16LL * sms : cb));
+    int gridC = (int)(cb < 1 ? 1 : (cb > 8LL * sms ? 8LL * sms : cb));
     if (vec)
       k_col_check<true><<<gridC, 256, 0, s>>>(Z, C, colIdx, st);
     else
