@@ -278,22 +278,29 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, i
 
 // Stable scatter: rank of each item among equal digits = tile offset (from the
 // scanned histogram) + items of earlier rounds + earlier warps of this round +
-// earlier lanes of this warp (found with a warp match). All keys are loaded
-// before the first round. The last pass also writes the inverse permutation
-// (invOut[row] = sorted position) when invOut is given.
+// earlier lanes of this warp (found with a warp match). Per round, the warp
+// leaders record their counts, then one thread per digit turns them into
+// per-warp starting positions (and advances the digit's running count), so
+// each item reads a single shared value. All keys are loaded before the first
+// round. The last pass also writes the inverse permutation (invOut[row] =
+// sorted position) when invOut is given; keysOut may be null when the sorted
+// keys are not needed.
 __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R, int shift, int nTiles,
                                                                 const int* __restrict__ offs,
                                                                 int* __restrict__ keysOut,
                                                                 int* __restrict__ valsOut,
                                                                 int* __restrict__ invOut) {
   constexpr int kWarps = kSortThreads / 32;
-  __shared__ int sRun[kRadix];             // running count per digit in this tile
-  __shared__ int sWarpCnt[kWarps][kRadix];  // per-warp counts of the current round
+  __shared__ int sRun[kRadix];              // running count per digit in this tile
+  __shared__ int sWarp[2][kWarps][kRadix];  // per round (alternating): counts, then starts
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
     sRun[d] = offs[(long long)d * nTiles + blockIdx.x];
 #pragma unroll
-    for (int q = 0; q < kWarps; ++q) sWarpCnt[q][d] = 0;
+    for (int q = 0; q < kWarps; ++q) {
+      sWarp[0][q][d] = 0;
+      sWarp[1][q][d] = 0;
+    }
   }
   const long long base = (long long)blockIdx.x * kSortTile;
   int key[kSortRounds], val[kSortRounds];
@@ -307,33 +314,35 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R
   __syncthreads();
 #pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
+    int(*cur)[kRadix] = sWarp[rd & 1];
+    int(*nxt)[kRadix] = sWarp[(rd + 1) & 1];
     const long long i = base + rd * kSortThreads + threadIdx.x;
     const bool valid = i < R;
     const int digit = valid ? (key[rd] >> shift) & (kRadix - 1) : kRadix;  // kRadix: no one shares
     const unsigned peers = __match_any_sync(kFullMask, digit);
     const int rankInWarp = __popc(peers & lanemask_lt());
-    const int leader = __ffs(peers) - 1;
-    if (valid && lane == leader) sWarpCnt[w][digit] = __popc(peers);
+    if (valid && lane == __ffs(peers) - 1) cur[w][digit] = __popc(peers);
+    __syncthreads();
+    // counts -> starting positions; clear the other buffer for the next round
+    // (its readers, the previous round, finished before the barrier above)
+    for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
+      int run = sRun[d];
+#pragma unroll
+      for (int q = 0; q < kWarps; ++q) {
+        const int cnt = cur[q][d];
+        cur[q][d] = run;  // where warp q's items of digit d start
+        run += cnt;
+        nxt[q][d] = 0;
+      }
+      sRun[d] = run;
+    }
     __syncthreads();
     if (valid) {
-      int before = sRun[digit];
-      for (int q = 0; q < w; ++q) before += sWarpCnt[q][digit];
-      const int pos = before + rankInWarp;
-      keysOut[pos] = key[rd];
+      const int pos = cur[w][digit] + rankInWarp;
+      if (keysOut) keysOut[pos] = key[rd];
       valsOut[pos] = val[rd];
       if (invOut) invOut[val[rd]] = pos;
     }
-    __syncthreads();
-    for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
-      int add = 0;
-#pragma unroll
-      for (int q = 0; q < kWarps; ++q) {
-        add += sWarpCnt[q][d];
-        sWarpCnt[q][d] = 0;
-      }
-      sRun[d] += add;
-    }
-    __syncthreads();
   }
 }
 
@@ -480,9 +489,10 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
     note_launches(1);
     err = exclusive_scan(ArrayIn{hist}, nh, hist, scanScratch, s);
     if (err != cudaSuccess) return err;
+    const bool last = p == passes - 1;
     k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(
-        in, R, shift, (int)nTiles, hist, kBuf[outSlot], vBuf[outSlot],
-        p == passes - 1 ? inv : nullptr);
+        in, R, shift, (int)nTiles, hist, (last && hostIterPtr) ? nullptr : kBuf[outSlot],
+        vBuf[outSlot], last ? inv : nullptr);
     note_launches(1);
     kIn = kBuf[outSlot];
     vIn = vBuf[outSlot];

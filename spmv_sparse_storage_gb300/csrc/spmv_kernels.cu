@@ -99,16 +99,20 @@ __device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long 
                                                int (&row)[4]) {
   const long long base = cb + 4 * lane;
   if (!(d.flags & kCsrChunkHasEmptyRow)) {
-    // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e
+    // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e:
+    // row of entry 0 = lo + set bits up to it, then +1 at every later set bit
     const int wd = lane >> 3;
     const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
     const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
                        (wd > 2 ? __popc(d.mask.z) : 0);
+    const int b0 = 4 * (lane & 7);
+    const unsigned nib = mw >> b0;  // this lane's 4 bits at the bottom
+    int r = d.lo + before + __popc(mw & ((2u << b0) - 1u));
+    row[0] = base < Z ? r : -1;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int b = 4 * (lane & 7) + e;
-      const unsigned upto = (b == 31) ? 0xffffffffu : ((2u << b) - 1u);
-      row[e] = base + e < Z ? d.lo + before + __popc(mw & upto) : -1;
+    for (int e = 1; e < 4; ++e) {
+      r += (nib >> e) & 1u;
+      row[e] = base + e < Z ? r : -1;
     }
   } else {
     // a chunk holding empty rows: binary search on rowPtrs, then walk

@@ -119,10 +119,18 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
         atomicOr(&desc[a[i] / kCsrChunk].flags, kCsrChunkHasEmptyRow);
       }
     }
-    // warp-aggregated exact histogram: one shared atomic per distinct length
+    // warp-aggregated exact histogram: when all 32 rows share one length
+    // (stencils, uniform rows) one shared atomic; otherwise one per distinct
+    // length found with a warp match
     const int key = (live && len < kExactLenBins) ? len : -1;
-    const unsigned peers = __match_any_sync(kFullMask, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
+    const int kmin = __reduce_min_sync(kFullMask, key);
+    const int kmax = __reduce_max_sync(kFullMask, key);
+    if (kmin == kmax) {
+      if (lane == 0 && key >= 0) atomicAdd(&sExact[key], 32u);
+    } else {
+      const unsigned peers = __match_any_sync(kFullMask, key);
+      if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
+    }
   }
   lmax = warp_max(lmax);
   lmin = warp_min(lmin);
