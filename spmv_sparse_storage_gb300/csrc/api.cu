@@ -92,6 +92,22 @@ struct DeviceGuard {
 
 // Device memory (or managed memory) on device `dev`; anything else (host,
 // pageable, another device) is rejected before a kernel could touch it.
+// Page-locked host buffer for the statistics read-back, one per host thread
+// (allocated on the thread's first create, kept until exit), so that the
+// copy is a plain DMA.
+DevStats* pinned_stats_buffer() {
+  thread_local DevStats* buf = nullptr;
+  if (!buf) {
+    void* p = nullptr;
+    if (cudaMallocHost(&p, sizeof(DevStats)) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    buf = static_cast<DevStats*>(p);
+  }
+  return buf;
+}
+
 int check_device_ptr(const void* p, int dev) {
   cudaPointerAttributes a;
   cudaError_t e = cudaPointerGetAttributes(&a, p);
@@ -304,20 +320,19 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   h->lastStream = s;
   int st = get_pool(dev, &h->pool);
   std::vector<Buf> tmp;
-  DevStats* dst = nullptr;
-  DevStats* hst = nullptr;
   auto fail = [&](int code) {
     h->release(tmp, s);
     h->release(h->csrBufs, s);
-    delete hst;
     delete h;
     return code;
   };
   if (st != SPMV_OK) return fail(st);
-  st = alloc_typed(h, 1, s, &dst, tmp);
+  DevStats* hst = pinned_stats_buffer();
+  if (!hst) return fail(SPMV_ERR_ALLOC);
+  void* work = nullptr;
+  st = h->alloc(spmv::stats_work_bytes(numRows, nnz, d_colIdx), s, &work, tmp);
   if (st != SPMV_OK) return fail(st);
-  void* statsScratch = nullptr;
-  st = h->alloc(spmv::stats_scratch_bytes(numRows), s, &statsScratch, tmp);
+  st = record(cudaMemsetAsync(work, 0, spmv::stats_zero_bytes(), s));
   if (st != SPMV_OK) return fail(st);
   // nnz-balanced split for the CSR kernel, written by the statistics pass
   // (which checks bounds, so it stays in bounds even if validation fails)
@@ -332,12 +347,10 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
     st = record(cudaMemsetAsync(h->chunkDesc, 0, sizeof(spmv::CsrChunkDesc) * h->nChunks, s));
     if (st != SPMV_OK) return fail(st);
   }
-  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, dst, statsScratch,
-                                 h->nChunks, h->chunkDesc, s));
+  st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, work, h->nChunks,
+                                 h->chunkDesc, s));
   if (st != SPMV_OK) return fail(st);
-  hst = new (std::nothrow) DevStats;
-  if (!hst) return fail(SPMV_ERR_ALLOC);
-  st = record(cudaMemcpyAsync(hst, dst, sizeof(DevStats), cudaMemcpyDeviceToHost, s));
+  st = record(cudaMemcpyAsync(hst, work, sizeof(DevStats), cudaMemcpyDeviceToHost, s));
   if (st != SPMV_OK) return fail(st);
   st = record(cudaStreamSynchronize(s));
   if (st != SPMV_OK) return fail(st);
@@ -362,8 +375,8 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   }
   for (int b = 0; b < 33; ++b) S.hist_log2[b] = (int64_t)hst->histLog2[b];
   for (int L = 0; L < spmv::kExactLenBins; ++L) {
-    int b = 0;
-    while (b < 32 && (1LL << b) <= L) ++b;  // bin 0: len 0; bin b: [2^(b-1), 2^b)
+    // bin 0: len 0; bin b >= 1: len in [2^(b-1), 2^b)
+    const int b = L == 0 ? 0 : 32 - __builtin_clz((unsigned)L);
     S.hist_log2[b] += hst->histExact[L];
   }
   S.imbalance_thread = S.mean_len > 0 ? (double)S.max_len / S.mean_len : 0.0;
@@ -376,7 +389,6 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   S.auto_format = select_format(numRows, nnz, S.max_len);
   S.auto_hyb_width = auto_hyb_width(h);
   h->release(tmp, s);
-  delete hst;
   *out = h;
   return SPMV_OK;
 }

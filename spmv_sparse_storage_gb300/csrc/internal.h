@@ -38,16 +38,16 @@ struct DevStats {
   unsigned int histExact[kExactLenBins];
 };
 
-// Work space of the statistics pass (device): per-block partial results and
-// kStatsReplicas copies of the exact histogram, so that no two blocks of a
-// large matrix update one address; a final one-block kernel folds them into
-// DevStats.
-constexpr int kStatsReplicas = 32;
+// Per-block partial record of the statistics pass (stats.cu).
 struct StatsPartial {
   int maxLen, minLen, emptyRows, maxWarpNnz, firstBadRow, pad0;
   unsigned long long sumSq;
 };
-size_t stats_scratch_bytes(int R);
+// Work area of the statistics pass: DevStats first (read back by the host),
+// then counters and per-block records; its first stats_zero_bytes() bytes
+// must be zeroed before launch_stats.
+size_t stats_work_bytes(int R, int Z, const int* colIdx);
+size_t stats_zero_bytes();
 
 // ---------------------------------------------------------------------------
 // CSR work split: the nonzeros in chunks of kCsrChunk, each described by a
@@ -85,10 +85,9 @@ int num_sms();
 // ---------------------------------------------------------------------------
 // Launchers. Each returns the cudaError_t of its launches.
 // ---------------------------------------------------------------------------
-// stats.cu (also writes desc[c].lo = row holding nonzero c*kCsrChunk)
-cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, void* scratch, int nChunks, CsrChunkDesc* desc,
-                         cudaStream_t s);
+// stats.cu: one launch; also writes the CSR chunk records into zeroed desc
+cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx, void* work,
+                         int nChunks, CsrChunkDesc* desc, cudaStream_t s);
 
 // convert.cu
 // CSR -> COO rowIdx from the CSR chunk records (spmv_kernels.cu)

@@ -265,27 +265,37 @@ __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, lon
 }
 
 // CSR -> COO ("Sparse Matrices and Basic Formats ...", section "COO format
-// and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. One warp per
-// 128-entry chunk: the rows come from the chunk record exactly as in the
-// CSR kernel, and each lane stores its 4 row ids with one 16-byte store.
+// and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. A warp takes
+// kExpandChunks consecutive 128-entry chunks and loads all their records
+// before using any; the rows come from each record exactly as in the CSR
+// kernel, and each lane stores its 4 row ids with one 16-byte store.
+constexpr int kExpandChunks = 4;
 __global__ void __launch_bounds__(256) k_expand_rows(int Z, long long nChunks,
                                                      const int* __restrict__ rowPtrs,
                                                      const CsrChunkDesc* __restrict__ desc,
                                                      int* __restrict__ rowIdx) {
   const int lane = threadIdx.x & 31;
-  const long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (c >= nChunks) return;  // warp-uniform
-  const long long cb = c * kCsrChunk;
-  const long long base = cb + 4 * lane;
-  const CsrChunkDesc d = desc[c];
-  int row[4];
-  csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
-  if (base + 4 <= Z) {
-    __stcs(reinterpret_cast<int4*>(rowIdx + base), make_int4(row[0], row[1], row[2], row[3]));
-  } else {
+  const long long c0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kExpandChunks;
+  if (c0 >= nChunks) return;  // warp-uniform
+  CsrChunkDesc d[kExpandChunks];
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (base + e < Z) rowIdx[base + e] = row[e];
+  for (int u = 0; u < kExpandChunks; ++u)
+    d[u] = desc[c0 + u < nChunks ? c0 + u : nChunks - 1];
+#pragma unroll
+  for (int u = 0; u < kExpandChunks; ++u) {
+    const long long c = c0 + u;
+    if (c >= nChunks) break;  // warp-uniform
+    const long long cb = c * kCsrChunk;
+    const long long base = cb + 4 * lane;
+    int row[4];
+    csr_chunk_rows(d[u], cb, lane, Z, rowPtrs, row);
+    if (base + 4 <= Z) {
+      __stcs(reinterpret_cast<int4*>(rowIdx + base), make_int4(row[0], row[1], row[2], row[3]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (base + e < Z) rowIdx[base + e] = row[e];
+    }
   }
 }
 
@@ -584,8 +594,9 @@ cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkD
                                int* rowIdx, cudaStream_t s) {
   if (R <= 0 || Z <= 0) return cudaSuccess;
   const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  k_expand_rows<<<(unsigned)((nChunks * 32 + 255) / 256), 256, 0, s>>>(Z, nChunks, rowPtrs, desc,
-                                                                        rowIdx);
+  const long long warps = (nChunks + kExpandChunks - 1) / kExpandChunks;
+  k_expand_rows<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(Z, nChunks, rowPtrs, desc,
+                                                                      rowIdx);
   note_launches(1);
   return cudaGetLastError();
 }

@@ -1,5 +1,5 @@
 // stats.cu -- input validation, row-length statistics and the nnz-balanced
-// CSR chunk map, all on the device.
+// CSR chunk records, all on the device, in one kernel launch.
 //
 // Validation follows the sanity rules of "Sparse matrix multiplication
 // acceleration techniques", section 5.3: row_ptr must be monotone, every
@@ -9,6 +9,11 @@
 // storage format selection and performance comparison", section 4.1, plus the
 // max/mean load ratio of "Introduction to sparse computing and performance
 // bottleneck location", section "Building the problem framework".
+//
+// One grid does everything: its first blocks walk rowPtrs, the others walk
+// colIdx (both streams at once), each block writes a partial record, and the
+// last block to finish folds the records into DevStats (no inter-block wait:
+// a block learns it is last from an atomic ticket).
 #include <climits>
 
 #include "device_util.cuh"
@@ -18,58 +23,72 @@ namespace spmv {
 namespace {
 
 constexpr int kStatsRowsPerThread = 8;
-constexpr int kStatsRows = 256 * kStatsRowsPerThread;
-constexpr int kColUnroll = 4;  // column check: vectors in flight per thread
+constexpr int kStatsRows = 256 * kStatsRowsPerThread;  // rows per row block
+constexpr int kColUnroll = 4;                           // column check: vectors in flight
+constexpr int kStatsReplicaCount = 8;                   // copies of the exact histogram
 
-__global__ void k_stats_init(DevStats* st, unsigned* histRep) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  for (int i = t; i < kStatsReplicas * kExactLenBins; i += gridDim.x * blockDim.x) histRep[i] = 0u;
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) st->histExact[i] = 0u;
-    if (threadIdx.x < 33) st->histLog2[threadIdx.x] = 0ull;
-    if (threadIdx.x == 0) {
-      st->err = 0u;
-      st->firstBadRow = INT_MAX;
-      st->firstBadNnz = INT_MAX;
-      st->maxLen = 0;
-      st->minLen = INT_MAX;
-      st->emptyRows = 0;
-      st->maxWarpNnz = 0;
-      st->pad0 = 0;
-      st->sumSq = 0ull;
-      st->gatherLines = 0ull;
-      st->gatherSets = 0ull;
-    }
-  }
+struct ColPartial {
+  int firstBad;
+  int pad0;
+  unsigned long long lines, sets;
+};
+
+// Work area layout (one allocation, zeroed up to `zero_bytes`):
+//   DevStats | ticket (16 B) | histogram replicas | row partials | column partials
+struct WorkLayout {
+  size_t ticket, rep, rowPart, colPart, zero, total;
+};
+
+__host__ __device__ inline WorkLayout work_layout(int nbRow, int nbCol) {
+  WorkLayout L;
+  L.ticket = (sizeof(DevStats) + 15) / 16 * 16;
+  L.rep = L.ticket + 16;
+  L.rowPart = L.rep + (size_t)kStatsReplicaCount * kExactLenBins * sizeof(unsigned);
+  L.zero = L.rowPart;
+  L.colPart = L.rowPart + (size_t)nbRow * sizeof(StatsPartial);
+  L.total = L.colPart + (size_t)(nbCol > 0 ? nbCol : 1) * sizeof(ColPartial);
+  return L;
 }
 
-// One pass over rowPtrs: monotonicity, endpoints, lengths, histograms, and
-// the CSR chunk map (desc[c].lo = row holding nonzero c*kCsrChunk). A block
-// takes kStatsRows consecutive rows, kStatsRowsPerThread per thread, 256
-// apart so that each load instruction is coalesced, and issues all its loads
-// before it uses any. The block's maxima, minima and sums go to its own
-// partial record (no atomics); lengths below kExactLenBins are counted in a
-// shared histogram that is added to one of kStatsReplicas global copies;
-// longer rows are counted in the log2 bins directly (their log2 bins for
-// shorter rows are derived on the host from the exact histogram).
-__global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __restrict__ rowPtrs,
-                                                   DevStats* __restrict__ st,
-                                                   StatsPartial* __restrict__ partials,
-                                                   unsigned* __restrict__ histRep, int nChunks,
-                                                   CsrChunkDesc* __restrict__ desc) {
+int row_blocks(int R) {
+  const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
+  return (int)(rb < 1 ? 1 : rb);
+}
+
+int col_blocks(int Z, bool vec) {
+  if (Z <= 0) return 0;
+  const long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
+  const long long cb = (work + 255) / 256;
+  const long long cap = 8LL * num_sms();
+  return (int)(cb < 1 ? 1 : (cb > cap ? cap : cb));
+}
+
+// Row part. A block takes kStatsRows consecutive rows, kStatsRowsPerThread
+// per thread, 256 apart so that each load is coalesced, and issues all its
+// loads before it uses any: monotonicity, lengths, min/max/sum of squares,
+// the max nonzeros of any 32 consecutive rows, an exact length histogram
+// (lengths < kExactLenBins; longer rows go to the log2 bins), and the CSR
+// chunk records (bounds-checked: they are written before validation is
+// known). A nonempty row is `lo` of every chunk whose first nonzero it holds
+// (and `hi` of the chunk before) and sets the bit of its start position in
+// the chunk where it starts; an empty row inside a chunk flags that chunk.
+__device__ void row_part(int blk, int R, int Z, const int* __restrict__ rowPtrs,
+                         DevStats* __restrict__ st, StatsPartial* __restrict__ partials,
+                         unsigned* __restrict__ histRep, int nChunks,
+                         CsrChunkDesc* __restrict__ desc) {
   __shared__ unsigned int sExact[kExactLenBins];
   __shared__ int sRed[5][8];
   __shared__ unsigned long long sSq[8];
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) sExact[i] = 0u;
   __syncthreads();
 
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
+  if (blk == 0 && threadIdx.x == 0) {
     if (rowPtrs[0] != 0) atomicOr(&st->err, kErrRowPtrStart);
     if (rowPtrs[R] != Z) atomicOr(&st->err, kErrRowPtrEnd);
     if (nChunks > 0) desc[nChunks - 1].hi = R > 0 ? R - 1 : 0;
   }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const long long base = (long long)blockIdx.x * kStatsRows + threadIdx.x;
+  const long long base = (long long)blk * kStatsRows + threadIdx.x;
   int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
 #pragma unroll
   for (int i = 0; i < kStatsRowsPerThread; ++i) {
@@ -98,11 +117,6 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       sq += (unsigned long long)len * (unsigned long long)len;
       if (lane == 0) gmax = max(gmax, g[i] - a[i]);
       if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
-      // CSR chunk records (bounds-checked: this runs before the validation
-      // result is known). A nonempty row is `lo` of every chunk whose first
-      // nonzero it holds (and `hi` of the chunk before), and sets the bit of
-      // its start position in the chunk where it starts; an empty row inside
-      // a chunk flags that chunk.
       if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
         const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
         const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
@@ -159,92 +173,32 @@ __global__ void __launch_bounds__(256) k_row_stats(int R, int Z, const int* __re
       p.firstBadRow = min(p.firstBadRow, sRed[4][w]);
       p.sumSq += sSq[w];
     }
-    partials[blockIdx.x] = p;
+    partials[blk] = p;
   }
-  unsigned* rep = histRep + (size_t)(blockIdx.x % kStatsReplicas) * kExactLenBins;
+  unsigned* rep = histRep + (size_t)(blk % kStatsReplicaCount) * kExactLenBins;
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x)
     if (sExact[i]) atomicAdd(rep + i, sExact[i]);
 }
 
-// Fold the per-block partials and the histogram replicas into DevStats.
-__global__ void __launch_bounds__(1024) k_stats_reduce(int nBlocks,
-                                                       const StatsPartial* __restrict__ partials,
-                                                       const unsigned* __restrict__ histRep,
-                                                       DevStats* __restrict__ st) {
-  __shared__ int sRed[5][32];
-  __shared__ unsigned long long sSq[32];
-  for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) {
-    unsigned v = 0u;
-    for (int r = 0; r < kStatsReplicas; ++r) v += histRep[(size_t)r * kExactLenBins + i];
-    st->histExact[i] = v;
-  }
-  int mx = 0, mn = INT_MAX, emp = 0, gm = 0, fb = INT_MAX;
-  unsigned long long sq = 0ull;
-  for (int i = threadIdx.x; i < nBlocks; i += blockDim.x) {
-    const StatsPartial p = partials[i];
-    mx = max(mx, p.maxLen);
-    mn = min(mn, p.minLen);
-    emp += p.emptyRows;
-    gm = max(gm, p.maxWarpNnz);
-    fb = min(fb, p.firstBadRow);
-    sq += p.sumSq;
-  }
-  mx = warp_max(mx);
-  mn = warp_min(mn);
-  emp = warp_sum(emp);
-  gm = warp_max(gm);
-  fb = warp_min(fb);
-  sq = warp_sum(sq);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) {
-    sRed[0][wid] = mx; sRed[1][wid] = mn; sRed[2][wid] = emp; sRed[3][wid] = gm; sRed[4][wid] = fb;
-    sSq[wid] = sq;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const int nw = blockDim.x / 32;
-    for (int w = 0; w < nw; ++w) {
-      mx = max(mx, sRed[0][w]);
-      mn = min(mn, sRed[1][w]);
-      gm = max(gm, sRed[3][w]);
-      fb = min(fb, sRed[4][w]);
-    }
-    emp = 0;
-    sq = 0ull;
-    for (int w = 0; w < nw; ++w) {
-      emp += sRed[2][w];
-      sq += sSq[w];
-    }
-    st->maxLen = mx;
-    st->minLen = mn;
-    st->emptyRows = emp;
-    st->maxWarpNnz = gm;
-    st->sumSq = sq;
-    if (fb != INT_MAX) {
-      st->err |= kErrRowPtrDecrease;
-      st->firstBadRow = fb;
-    }
-  }
-}
-
-// Every column index must satisfy 0 <= c < numCols (unsigned compare catches
-// negatives). VEC: colIdx is 16-byte aligned, read as int4.
+// Column part: every column index must satisfy 0 <= c < numCols (unsigned
+// compare catches negatives). VEC: colIdx is 16-byte aligned, read as int4,
+// kColUnroll vectors per thread in flight. The first kGatherSampleBlocks
+// column blocks also sample the x-gather spread: distinct 128-byte lines of x
+// among the 32 gathers of one warp load.
 template <bool VEC>
-__global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __restrict__ colIdx,
-                                                   DevStats* __restrict__ st) {
+__device__ void col_part(int cblk, int nbCol, int Z, int C, const int* __restrict__ colIdx,
+                         ColPartial* __restrict__ colPart) {
   const unsigned uc = (unsigned)C;
   int firstBad = INT_MAX;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const bool sample = blockIdx.x < kGatherSampleBlocks;
+  const long long stride = (long long)nbCol * blockDim.x;
+  long long i = (long long)cblk * blockDim.x + threadIdx.x;
+  const bool sample = cblk < kGatherSampleBlocks;
   unsigned long long lines = 0ull, sets = 0ull;
   if (VEC) {
     const long long nv = Z / 4;
     const int4* c4 = reinterpret_cast<const int4*>(colIdx);
-    // kColUnroll vectors per thread per iteration, all loaded before any is
-    // checked; all lanes of a warp run the same number of iterations (the
-    // bound only depends on the warp's first index), so the warp match below
-    // is uniform
+    // all lanes of a warp run the same number of iterations (the bound only
+    // depends on the warp's first index), so the warp match below is uniform
     long long i0 = i - (threadIdx.x & 31);
     for (; i0 < nv; i += kColUnroll * stride, i0 += kColUnroll * stride) {
       int4 c[kColUnroll];
@@ -263,7 +217,6 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
         }
       }
       if (sample) {
-        // distinct 128-byte lines of x among the 32 gathers of one warp load
         const bool in = i < nv;
         const unsigned ln = in ? ((unsigned)c[0].x >> 5) : 0xffffffffu;
         const unsigned peers = __match_any_sync(kFullMask, ln);
@@ -274,73 +227,165 @@ __global__ void __launch_bounds__(256) k_col_check(int Z, int C, const int* __re
         }
       }
     }
-    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long t = (long long)cblk * blockDim.x + threadIdx.x;
     const long long k = 4 * nv + t;
     if (k < Z && (unsigned)colIdx[k] >= uc) firstBad = min(firstBad, (int)k);
   } else {
     for (; i < Z; i += stride)
       if ((unsigned)ld_stream(colIdx + i) >= uc) firstBad = min(firstBad, (int)i);
   }
-  if (firstBad != INT_MAX) {
-    atomicOr(&st->err, kErrColRange);
-    atomicMin(&st->firstBadNnz, firstBad);
+  __shared__ unsigned long long sL[8], sS[8];
+  __shared__ int sB[8];
+  firstBad = warp_min(firstBad);
+  lines = warp_sum(lines);
+  sets = warp_sum(sets);
+  if ((threadIdx.x & 31) == 0) {
+    sL[threadIdx.x >> 5] = lines;
+    sS[threadIdx.x >> 5] = sets;
+    sB[threadIdx.x >> 5] = firstBad;
   }
-  if (VEC && sample) {
-    __shared__ unsigned long long sL[8], sS[8];
-    lines = warp_sum(lines);
-    sets = warp_sum(sets);
-    if ((threadIdx.x & 31) == 0) {
-      sL[threadIdx.x >> 5] = lines;
-      sS[threadIdx.x >> 5] = sets;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ColPartial p;
+    p.firstBad = INT_MAX;
+    p.pad0 = 0;
+    p.lines = 0ull;
+    p.sets = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      p.firstBad = min(p.firstBad, sB[w]);
+      p.lines += sL[w];
+      p.sets += sS[w];
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long L = 0ull, S = 0ull;
-      for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-        L += sL[w];
-        S += sS[w];
-      }
-      if (S) {
-        atomicAdd(&st->gatherLines, L);
-        atomicAdd(&st->gatherSets, S);
-      }
+    colPart[cblk] = p;
+  }
+}
+
+// The last block: fold row partials, column partials and histogram replicas.
+__device__ void finalize(int nbRow, int nbCol, DevStats* __restrict__ st,
+                         const StatsPartial* __restrict__ partials,
+                         const ColPartial* __restrict__ colPart,
+                         const unsigned* __restrict__ histRep) {
+  __shared__ int sRed[6][8];
+  __shared__ unsigned long long sU[3][8];
+  for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) {
+    unsigned v = 0u;
+#pragma unroll
+    for (int r = 0; r < kStatsReplicaCount; ++r) v += histRep[(size_t)r * kExactLenBins + i];
+    st->histExact[i] = v;
+  }
+  int mx = 0, mn = INT_MAX, emp = 0, gm = 0, fb = INT_MAX, fc = INT_MAX;
+  unsigned long long sq = 0ull, ln = 0ull, ss = 0ull;
+  for (int i = threadIdx.x; i < nbRow; i += blockDim.x) {
+    const StatsPartial p = partials[i];
+    mx = max(mx, p.maxLen);
+    mn = min(mn, p.minLen);
+    emp += p.emptyRows;
+    gm = max(gm, p.maxWarpNnz);
+    fb = min(fb, p.firstBadRow);
+    sq += p.sumSq;
+  }
+  for (int i = threadIdx.x; i < nbCol; i += blockDim.x) {
+    const ColPartial p = colPart[i];
+    fc = min(fc, p.firstBad);
+    ln += p.lines;
+    ss += p.sets;
+  }
+  mx = warp_max(mx);
+  mn = warp_min(mn);
+  emp = warp_sum(emp);
+  gm = warp_max(gm);
+  fb = warp_min(fb);
+  fc = warp_min(fc);
+  sq = warp_sum(sq);
+  ln = warp_sum(ln);
+  ss = warp_sum(ss);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  if (lane == 0) {
+    sRed[0][wid] = mx; sRed[1][wid] = mn; sRed[2][wid] = emp;
+    sRed[3][wid] = gm; sRed[4][wid] = fb; sRed[5][wid] = fc;
+    sU[0][wid] = sq; sU[1][wid] = ln; sU[2][wid] = ss;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mx = 0; mn = INT_MAX; emp = 0; gm = 0; fb = INT_MAX; fc = INT_MAX;
+    sq = ln = ss = 0ull;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
+      mx = max(mx, sRed[0][w]);
+      mn = min(mn, sRed[1][w]);
+      emp += sRed[2][w];
+      gm = max(gm, sRed[3][w]);
+      fb = min(fb, sRed[4][w]);
+      fc = min(fc, sRed[5][w]);
+      sq += sU[0][w];
+      ln += sU[1][w];
+      ss += sU[2][w];
     }
+    st->maxLen = mx;
+    st->minLen = mn;
+    st->emptyRows = emp;
+    st->maxWarpNnz = gm;
+    st->sumSq = sq;
+    st->gatherLines = ln;
+    st->gatherSets = ss;
+    st->firstBadRow = fb;
+    st->firstBadNnz = fc;
+    unsigned err = st->err;
+    if (fb != INT_MAX) err |= kErrRowPtrDecrease;
+    if (fc != INT_MAX) err |= kErrColRange;
+    st->err = err;
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
+                                                        const int* __restrict__ rowPtrs,
+                                                        const int* __restrict__ colIdx,
+                                                        unsigned char* __restrict__ work,
+                                                        int nbRow, int nbCol, int nChunks,
+                                                        CsrChunkDesc* __restrict__ desc) {
+  const WorkLayout L = work_layout(nbRow, nbCol);
+  DevStats* st = reinterpret_cast<DevStats*>(work);
+  unsigned* ticket = reinterpret_cast<unsigned*>(work + L.ticket);
+  unsigned* histRep = reinterpret_cast<unsigned*>(work + L.rep);
+  StatsPartial* partials = reinterpret_cast<StatsPartial*>(work + L.rowPart);
+  ColPartial* colPart = reinterpret_cast<ColPartial*>(work + L.colPart);
+  if ((int)blockIdx.x < nbRow)
+    row_part(blockIdx.x, R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
+  else
+    col_part<VEC>(blockIdx.x - nbRow, nbCol, Z, C, colIdx, colPart);
+  // publish this block's results, then take a ticket; the last block folds
+  __shared__ bool sLast;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) sLast = atomicAdd(ticket, 1u) == (unsigned)(nbRow + nbCol - 1);
+  __syncthreads();
+  if (sLast) {
+    __threadfence();
+    finalize(nbRow, nbCol, st, partials, colPart, histRep);
   }
 }
 
 }  // namespace
 
-size_t stats_scratch_bytes(int R) {
-  const long long nb = ((long long)R + kStatsRows - 1) / kStatsRows;
-  return (size_t)(nb < 1 ? 1 : nb) * sizeof(StatsPartial) +
-         (size_t)kStatsReplicas * kExactLenBins * sizeof(unsigned);
+size_t stats_work_bytes(int R, int Z, const int* colIdx) {
+  return work_layout(row_blocks(R), col_blocks(Z, aligned16(colIdx))).total;
 }
 
-cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx,
-                         DevStats* st, void* scratch, int nChunks, CsrChunkDesc* desc,
-                         cudaStream_t s) {
-  const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
-  const int nb = (int)(rb < 1 ? 1 : rb);
-  unsigned* histRep = static_cast<unsigned*>(scratch);
-  StatsPartial* partials =
-      reinterpret_cast<StatsPartial*>(histRep + (size_t)kStatsReplicas * kExactLenBins);
-  k_stats_init<<<32, 256, 0, s>>>(st, histRep);
-  k_row_stats<<<nb, 256, 0, s>>>(R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
-  int n = 3;
-  const int sms = num_sms();
-  if (Z > 0) {
-    const bool vec = aligned16(colIdx);
-    long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
-    long long cb = (work + 255) / 256;
-    int gridC = (int)(cb < 1 ? 1 : (cb > 8LL * sms ? 8LL * sms : cb));
-    if (vec)
-      k_col_check<true><<<gridC, 256, 0, s>>>(Z, C, colIdx, st);
-    else
-      k_col_check<false><<<gridC, 256, 0, s>>>(Z, C, colIdx, st);
-    ++n;
-  }
-  k_stats_reduce<<<1, 1024, 0, s>>>(nb, partials, histRep, st);
-  note_launches(n);
+size_t stats_zero_bytes() { return work_layout(1, 1).zero; }
+
+cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx, void* work,
+                         int nChunks, CsrChunkDesc* desc, cudaStream_t s) {
+  const bool vec = aligned16(colIdx);
+  const int nbRow = row_blocks(R);
+  const int nbCol = col_blocks(Z, vec);
+  unsigned char* w = static_cast<unsigned char*>(work);
+  if (vec)
+    k_validate_stats<true><<<nbRow + nbCol, 256, 0, s>>>(R, C, Z, rowPtrs, colIdx, w, nbRow,
+                                                         nbCol, nChunks, desc);
+  else
+    k_validate_stats<false><<<nbRow + nbCol, 256, 0, s>>>(R, C, Z, rowPtrs, colIdx, w, nbRow,
+                                                          nbCol, nChunks, desc);
+  note_launches(1);
   return cudaGetLastError();
 }
 
