@@ -43,6 +43,9 @@ _SIGS = {
     "or_spmv_ell": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p]),
     "or_spmv_hyb": (None, [_i64, _i64, _p, _p, _p, _i64, _p, _p, _p, _p, _p, _p]),
     "or_spmv_jds": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_csr_to_sell": (_i64, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_sell_to_csr": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_spmv_sell": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_select": (C.c_int, [_i64, _i64, _i64]),
     "or_hyb_auto_width": (_i64, [_i64, _p, _i64]),
 }
@@ -258,6 +261,40 @@ class Oracle:
                                _ptr(jds["col_idx"]), _ptr(jds["value"]), _ptr(rp), _ptr(ci),
                                _ptr(v))
         return rp, ci, v
+
+    def csr_to_sell(self, row_ptrs, col_idx, value, section_rows):
+        rp, ci, v = _i32(row_ptrs), _i32(col_idx), _f32(value)
+        R, S = rp.shape[0] - 1, int(section_rows)
+        n = self.lib.or_csr_to_sell(R, S, _ptr(rp), _ptr(ci), _ptr(v), None, None, None, None)
+        Se = max(S, 1)
+        nsec = (R + Se - 1) // Se
+        perm = np.zeros(R, np.int32)
+        sp = np.zeros(nsec + 1, np.int64)
+        sc = np.zeros(n, np.int32)
+        sv = np.zeros(n, np.float32)
+        self.lib.or_csr_to_sell(R, S, _ptr(rp), _ptr(ci), _ptr(v), _ptr(perm), _ptr(sp),
+                                _ptr(sc), _ptr(sv))
+        return {"num_rows": R, "section_rows": Se, "perm": perm, "sec_ptr": sp,
+                "col_idx": sc, "value": sv}
+
+    def sell_to_csr(self, sell):
+        R, S = sell["num_rows"], sell["section_rows"]
+        Z = int((sell["col_idx"] >= 0).sum())
+        rp = np.zeros(R + 1, np.int32)
+        ci = np.zeros(Z, np.int32)
+        v = np.zeros(Z, np.float32)
+        self.lib.or_sell_to_csr(R, S, _ptr(sell["perm"]), _ptr(sell["sec_ptr"]),
+                                _ptr(sell["col_idx"]), _ptr(sell["value"]), _ptr(rp), _ptr(ci),
+                                _ptr(v))
+        return rp, ci, v
+
+    def spmv_sell(self, sell, x, y0):
+        R = sell["num_rows"]
+        y = np.zeros(R, np.float64)
+        self.lib.or_spmv_sell(R, sell["section_rows"], _ptr(sell["perm"]), _ptr(sell["sec_ptr"]),
+                              _ptr(sell["col_idx"]), _ptr(sell["value"]), _ptr(_f32(x)),
+                              _ptr(_f32(y0)), _ptr(y))
+        return y
 
     # --- selection -----------------------------------------------------------
     def select(self, num_rows, nnz, max_len):

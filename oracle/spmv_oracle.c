@@ -29,6 +29,9 @@
  *     order (the worked example puts r0 before r2); zero-length rows last.
  *   - HYB: the first min(len, K) entries of a row (in CSR order) stay in the
  *     ELL part, the rest go to the COO part in row order.
+ *   - Sectioned ELL (the JDS variant): section height S is a parameter (the
+ *     page leaves it open); sections are column-major with their own height,
+ *     so the last section may be shorter; padding as in ELL.
  *   - Accumulation in the oracle is fp64, summed in CSR order.
  *
  * Parity status: every function here is pinned by tests (worked example of
@@ -421,4 +424,116 @@ int64_t or_hyb_auto_width(int64_t R, const int32_t *rowPtrs, int64_t maxLen) {
     }
     free(count);
     return L;
+}
+
+/* CSR -> sectioned ELL, [P2] "JDS format", the variant paragraph: after the
+ * rows are sorted by length (longest first, stable, as for JDS) they are cut
+ * into sections of S consecutive sorted rows (the last section may be
+ * shorter); each section is an ELL of its own, padded only to the length of
+ * its longest (first) row and laid out column-major: slot t of the j-th row of
+ * section k sits at secPtr[k] + t*h_k + j, h_k the section's row count.
+ * secPtr[k] marks where section k starts (it replaces iterPtr); padding slots
+ * hold column -1 and value +0.0f as in ELL. perm[s] = original row of sorted
+ * row s. Returns the total slot count; pass NULL outputs to count only.
+ * S < 1 is treated as 1. */
+int64_t or_csr_to_sell(int64_t R, int64_t S, const int32_t *rowPtrs,
+                       const int32_t *colIdx, const float *value, int32_t *perm,
+                       int64_t *secPtr, int32_t *sellCol, float *sellVal) {
+    if (S < 1) S = 1;
+    int64_t maxLen = 0;
+    for (int64_t r = 0; r < R; ++r)
+        if (rowPtrs[r + 1] - rowPtrs[r] > maxLen) maxLen = rowPtrs[r + 1] - rowPtrs[r];
+    /* stable counting sort by length, longest first */
+    int64_t *first = (int64_t *)calloc((size_t)maxLen + 2, sizeof(int64_t));
+    int32_t *order = (int32_t *)malloc(sizeof(int32_t) * (size_t)(R > 0 ? R : 1));
+    for (int64_t r = 0; r < R; ++r) first[rowPtrs[r + 1] - rowPtrs[r]] += 1;
+    int64_t acc = 0;
+    for (int64_t len = maxLen; len >= 0; --len) {
+        int64_t c = first[len];
+        first[len] = acc;
+        acc += c;
+    }
+    for (int64_t r = 0; r < R; ++r) order[first[rowPtrs[r + 1] - rowPtrs[r]]++] = (int32_t)r;
+    int64_t nsec = (R + S - 1) / S, slots = 0;
+    for (int64_t k = 0; k < nsec; ++k) {
+        int64_t s0 = k * S, h = R - s0 < S ? R - s0 : S;
+        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];
+        if (secPtr) secPtr[k] = slots;
+        if (sellCol) {
+            for (int64_t j = 0; j < h; ++j) {
+                int64_t r = order[s0 + j];
+                int64_t len = rowPtrs[r + 1] - rowPtrs[r];
+                for (int64_t t = 0; t < w; ++t) {
+                    int64_t i = slots + t * h + j;
+                    if (t < len) {
+                        sellCol[i] = colIdx[rowPtrs[r] + t];
+                        sellVal[i] = value[rowPtrs[r] + t];
+                    } else {
+                        sellCol[i] = -1;
+                        sellVal[i] = 0.0f;
+                    }
+                }
+            }
+        }
+        slots += h * w;
+    }
+    if (secPtr) secPtr[nsec] = slots;
+    if (perm)
+        for (int64_t s = 0; s < R; ++s) perm[s] = order[s];
+    free(first);
+    free(order);
+    return slots;
+}
+
+/* Sectioned ELL -> CSR: a row's entries are its leading non-padding slots. */
+void or_sell_to_csr(int64_t R, int64_t S, const int32_t *perm, const int64_t *secPtr,
+                    const int32_t *sellCol, const float *sellVal, int32_t *rowPtrs,
+                    int32_t *colIdx, float *value) {
+    if (S < 1) S = 1;
+    int64_t nsec = (R + S - 1) / S;
+    int32_t *lens = (int32_t *)calloc((size_t)R + 1, sizeof(int32_t));
+    for (int64_t k = 0; k < nsec; ++k) {
+        int64_t s0 = k * S, h = R - s0 < S ? R - s0 : S;
+        int64_t w = h > 0 ? (secPtr[k + 1] - secPtr[k]) / h : 0;
+        for (int64_t j = 0; j < h; ++j) {
+            int64_t len = 0;
+            while (len < w && sellCol[secPtr[k] + len * h + j] >= 0) ++len;
+            lens[perm[s0 + j]] = (int32_t)len;
+        }
+    }
+    rowPtrs[0] = 0;
+    for (int64_t r = 0; r < R; ++r) rowPtrs[r + 1] = rowPtrs[r] + lens[r];
+    for (int64_t k = 0; k < nsec; ++k) {
+        int64_t s0 = k * S, h = R - s0 < S ? R - s0 : S;
+        for (int64_t j = 0; j < h; ++j) {
+            int64_t r = perm[s0 + j];
+            for (int64_t t = 0; t < lens[r]; ++t) {
+                colIdx[rowPtrs[r] + t] = sellCol[secPtr[k] + t * h + j];
+                value[rowPtrs[r] + t] = sellVal[secPtr[k] + t * h + j];
+            }
+        }
+    }
+    free(lens);
+}
+
+/* SpMV over the sectioned ELL: sorted row s (section k, position j) sums
+ * its non-padding slots and adds the result to y[perm[s]]. fp64. */
+void or_spmv_sell(int64_t R, int64_t S, const int32_t *perm, const int64_t *secPtr,
+                  const int32_t *sellCol, const float *sellVal, const float *x,
+                  const float *y0, double *y) {
+    if (S < 1) S = 1;
+    for (int64_t r = 0; r < R; ++r) y[r] = (double)y0[r];
+    int64_t nsec = (R + S - 1) / S;
+    for (int64_t k = 0; k < nsec; ++k) {
+        int64_t s0 = k * S, h = R - s0 < S ? R - s0 : S;
+        int64_t w = h > 0 ? (secPtr[k + 1] - secPtr[k]) / h : 0;
+        for (int64_t j = 0; j < h; ++j) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < w; ++t) {
+                int64_t i = secPtr[k] + t * h + j;
+                if (sellCol[i] >= 0) acc += (double)sellVal[i] * (double)x[sellCol[i]];
+            }
+            y[perm[s0 + j]] += acc;
+        }
+    }
 }

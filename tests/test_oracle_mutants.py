@@ -35,8 +35,8 @@ MUTANTS = {
                       "            int64_t i = r * K + t;"),
     "ell_pad_col_zero": ("                ellCol[i] = -1;\n                ellVal[i] = 0.0f;\n            }\n        }\n    }\n}",
                          "                ellCol[i] = 0;\n                ellVal[i] = 0.0f;\n            }\n        }\n    }\n}"),
-    "jds_ascending": ("for (int64_t len = maxLen; len >= 0; --len) {",
-                      "for (int64_t len = 0; len <= maxLen; ++len) {"),
+    "jds_ascending": ("for (int64_t len = maxLen; len >= 0; --len) {\n        first[len] = acc;",
+                      "for (int64_t len = 0; len <= maxLen; ++len) {\n        first[len] = acc;"),
     "jds_iterptr_off_by_one": ("longer -= count[t + 1];", "longer -= count[t];"),
     "jds_unstable": ("    for (int64_t r = 0; r < R; ++r) {\n        int64_t len = rowPtrs[r + 1] - rowPtrs[r];\n        perm[first[len]] = (int32_t)r;",
                      "    for (int64_t r = R - 1; r >= 0; --r) {\n        int64_t len = rowPtrs[r + 1] - rowPtrs[r];\n        perm[first[len]] = (int32_t)r;"),
@@ -50,6 +50,10 @@ MUTANTS = {
     "stats_sample_variance": ("*var = R > 0 ? ss / (double)R : 0.0;",
                               "*var = R > 1 ? ss / (double)(R - 1) : 0.0;"),
     "auto_width_strict": ("if (100 * cum >= 99 * R) break;", "if (100 * cum > 99 * R) break;"),
+    "sell_row_major": ("                    int64_t i = slots + t * h + j;",
+                       "                    int64_t i = slots + j * w + t;"),
+    "sell_width_from_last_row": ("        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];",
+                                 "        int64_t w = rowPtrs[order[s0 + h - 1] + 1] - rowPtrs[order[s0 + h - 1]];"),
 }
 
 
@@ -63,6 +67,9 @@ def _pin_calls():
     calls += [(pins.test_spmv_matches_dense_brute_force, {"seed": 0, "case": c})
               for c in range(len(pins.CASES))]
     calls += [(pins.test_laplace2d_closed_form, {"side": 5})]
+    import test_oracle_sell as sell
+    calls += [(sell.test_fig14_1_sections_of_two, {}), (sell.test_fig14_1_spmv, {})]
+    calls += [(sell.test_round_trip_and_padding, {"idx": i, "S": 3}) for i in range(7)]
     for i in range(7):
         calls += [(pins.test_round_trips_bit_exact, {"idx": i}),
                   (pins.test_layout_invariants, {"idx": i}),
