@@ -359,9 +359,18 @@ def run_kernels(args, device):
     out = {}
     with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
         fmts = [f for f in args.formats.split(",") if f]
+        conv_us = {}
         for f in fmts:
             try:
+                m.convert(f, stream=stream)  # warm (pool growth, first launches)
+                flush.fill_(-1.0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
                 m.convert(f, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                conv_us[f] = round(e0.elapsed_time(e1) * 1e3, 2)
             except sp.SpmvError as e:
                 out[f] = {"error": str(e)}
         torch.cuda.synchronize(device)
@@ -382,7 +391,10 @@ def run_kernels(args, device):
             ms = float(np.median(times))
             gbs = compulsory_bytes(R, C, Z) / (ms * 1e-3) / 1e9
             out[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
-                      "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1)}
+                      "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1),
+                      "convert_us": conv_us.get(f)}
+            if f in ("ELL", "HYB", "SELL"):
+                out[f]["slots"] = m.export(f)["ell_slots"]
         sel = m.select()
     return {"mode": "kernels", "workload": args.workload, "rows": R, "nnz": Z,
             "l2_flush_bytes": int(flush.numel() * 4), "reps": args.reps, "peak": peak,
@@ -497,7 +509,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--mode", choices=["step", "kernels"], default="step",
                     help="step: the whole path (default); kernels: per-format SpMV, cold L2")
-    ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS")
+    ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL")
     ap.add_argument("--reps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

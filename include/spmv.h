@@ -20,6 +20,9 @@
  *   JDS  -- same page, section "JDS format": rows sorted by length (longest
  *           first, stable), a row permutation, and jagged diagonals starting
  *           at iterPtr[t].
+ *   SELL -- same page, same section, the variant it describes: the sorted
+ *           rows cut into sections of S rows, each section an ELL padded to
+ *           its own longest row (sectioned / sliced ELL).
  *
  * Conventions for every function:
  *   - Every function returns an int status (spmv_status); nothing throws or
@@ -56,7 +59,8 @@ typedef enum {
   SPMV_ELL = 2,
   SPMV_HYB = 3,
   SPMV_JDS = 4,
-  SPMV_AUTO = 5 /* spmv_run: the format spmv_select would choose */
+  SPMV_AUTO = 5, /* spmv_run: the format spmv_select would choose */
+  SPMV_SELL = 6  /* sectioned ELL over the JDS row order */
 } spmv_format;
 
 typedef enum {
@@ -64,7 +68,7 @@ typedef enum {
   SPMV_ERR_INVALID_ARG = -1,      /* null/negative/inconsistent argument */
   SPMV_ERR_BAD_ROWPTRS = -2,      /* rowPtrs[0] != 0, decreasing, or rowPtrs[numRows] != nnz */
   SPMV_ERR_COL_OUT_OF_RANGE = -3, /* some colIdx < 0 or >= numCols */
-  SPMV_ERR_TOO_LARGE = -4,        /* ELL/HYB slot count beyond int32 or the padding budget */
+  SPMV_ERR_TOO_LARGE = -4,        /* ELL/HYB/SELL slot count beyond int32 or the padding budget */
   SPMV_ERR_NOT_CONVERTED = -5,    /* spmv_run/export of a format not converted yet */
   SPMV_ERR_CUDA = -6,             /* a CUDA runtime call failed (see spmv_last_cuda_error) */
   SPMV_ERR_ALLOC = -7,            /* device allocation failed or exceeded the set limit */
@@ -101,18 +105,22 @@ typedef struct {
 typedef struct {
   int32_t format;           /* spmv_format */
   int64_t num_rows, num_cols, nnz;
-  int32_t width;            /* ELL and HYB: K (slots per row); JDS: longest row */
-  int64_t ell_slots;        /* ELL/HYB: num_rows * width */
+  int32_t width;            /* ELL and HYB: K (slots per row); JDS: longest row;
+                               SELL: width of the widest (first) section */
+  int64_t ell_slots;        /* ELL/HYB: num_rows * width; SELL: total slots */
   int64_t coo_nnz;          /* COO: nnz; HYB: entries of the COO part */
   const int32_t *row_ptrs;  /* CSR: numRows + 1 (the caller's array) */
   const int32_t *row_idx;   /* COO: nnz;  HYB: coo_nnz */
-  const int32_t *col_idx;   /* CSR/COO: nnz; ELL/HYB: ell_slots (padding = -1); JDS: nnz */
+  const int32_t *col_idx;   /* CSR/COO: nnz; ELL/HYB/SELL: ell_slots (padding = -1); JDS: nnz */
   const float *value;       /* as col_idx (padding = +0.0f) */
   const int32_t *nnz_per_row;  /* ELL/HYB: entries of each row held in the ELL slots */
   const int32_t *coo_col_idx;  /* HYB: coo_nnz */
   const float *coo_value;      /* HYB: coo_nnz */
-  const int32_t *perm;      /* JDS: perm[s] = original row of sorted row s (numRows) */
+  const int32_t *perm;      /* JDS/SELL: perm[s] = original row of sorted row s (numRows) */
   const int32_t *iter_ptr;  /* JDS: width + 1 entries, iter_ptr[width] = nnz */
+  const int32_t *sec_ptr;   /* SELL: ceil(numRows/S) + 1 entries, first slot of each
+                               section, sec_ptr[last] = ell_slots */
+  int32_t section_rows;     /* SELL: S, rows per section (the last may be shorter) */
 } spmv_arrays;
 
 /* Create a handle over a CSR matrix that lives on the current device.
@@ -155,12 +163,25 @@ int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void *stream);
  * the t-th entry of sorted row s. Asynchronous. */
 int spmv_convert_jds(spmv_handle h, void *stream);
 
+/* CSR -> SELL, the sectioned variant of JDS ("Regularized Formats (ELL,
+ * Hybrid ELL-COO and JDS)", section "JDS format", last paragraph): rows
+ * sorted as for JDS (perm), sorted row s in section k = s / S; a section
+ * holds h_k = min(S, numRows - k*S) rows and is padded to w_k, the length of
+ * its first (longest) row; slot t of the j-th row of section k is at
+ * sec_ptr[k] + t*h_k + j (column-major inside the section), padding as ELL
+ * (column -1, value +0.0f). sectionRows = 0 picks S = 128; sectionRows < 0 is
+ * SPMV_ERR_INVALID_ARG. Returns SPMV_ERR_TOO_LARGE (nothing kept) when the
+ * slot count exceeds INT32_MAX or 4*nnz + numRows. Asynchronous, except for
+ * one device-to-host read of the section widths when some row has 1024 or
+ * more entries. */
+int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void *stream);
+
 /* y <- A*x + y with the given format (SPMV_AUTO = spmv_select's choice).
  * d_x: numCols floats, d_y: numRows floats, both on the handle's device;
  * x and y must not overlap (SPMV_ERR_INVALID_ARG). The format must have been
  * converted (SPMV_CSR always is), else SPMV_ERR_NOT_CONVERTED; nothing is
  * converted implicitly. Asynchronous on `stream`; launches 1 kernel
- * (CSR, COO, ELL, JDS) or 2 (HYB: ELL part, then the COO part with a
+ * (CSR, COO, ELL, JDS, SELL) or 2 (HYB: ELL part, then the COO part with a
  * programmatic dependent launch). Floating-point rounding differs from a
  * sequential sum (tree and atomic reductions); per row the result is within
  * 1e-5 * (sum_j |a_ij x_j| + |y_i|) of the exact value for rows up to

@@ -24,9 +24,9 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 # --- enums -----------------------------------------------------------------
-SPMV_COO, SPMV_CSR, SPMV_ELL, SPMV_HYB, SPMV_JDS, SPMV_AUTO = range(6)
+SPMV_COO, SPMV_CSR, SPMV_ELL, SPMV_HYB, SPMV_JDS, SPMV_AUTO, SPMV_SELL = range(7)
 FORMATS = {"COO": SPMV_COO, "CSR": SPMV_CSR, "ELL": SPMV_ELL, "HYB": SPMV_HYB,
-           "JDS": SPMV_JDS, "AUTO": SPMV_AUTO}
+           "JDS": SPMV_JDS, "AUTO": SPMV_AUTO, "SELL": SPMV_SELL}
 FORMAT_NAMES = {v: k for k, v in FORMATS.items()}
 
 SPMV_OK = 0
@@ -55,7 +55,8 @@ class spmv_arrays(C.Structure):
                 ("coo_nnz", C.c_int64), ("row_ptrs", C.c_void_p), ("row_idx", C.c_void_p),
                 ("col_idx", C.c_void_p), ("value", C.c_void_p), ("nnz_per_row", C.c_void_p),
                 ("coo_col_idx", C.c_void_p), ("coo_value", C.c_void_p), ("perm", C.c_void_p),
-                ("iter_ptr", C.c_void_p)]
+                ("iter_ptr", C.c_void_p), ("sec_ptr", C.c_void_p),
+                ("section_rows", C.c_int32)]
 
 
 _H = C.c_void_p
@@ -66,6 +67,7 @@ _SIGS = {
     "spmv_convert_ell": (C.c_int, [_H, _P]),
     "spmv_convert_hyb": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_convert_jds": (C.c_int, [_H, _P]),
+    "spmv_convert_sell": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_run": (C.c_int, [_H, C.c_int, _P, _P, _P]),
     "spmv_select": (C.c_int, [_H, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
     "spmv_get_stats": (C.c_int, [_H, C.POINTER(spmv_stats)]),
@@ -147,6 +149,10 @@ def spmv_convert_hyb(h, ell_width=0, stream=None):
 
 def spmv_convert_jds(h, stream=None):
     _check(_lib.spmv_convert_jds(h, _stream(stream)), "spmv_convert_jds")
+
+
+def spmv_convert_sell(h, section_rows=0, stream=None):
+    _check(_lib.spmv_convert_sell(h, section_rows, _stream(stream)), "spmv_convert_sell")
 
 
 def spmv_run(h, fmt, x, y, stream=None):
@@ -259,6 +265,11 @@ def export_tensors(h, fmt):
     elif f == "JDS":
         out.update(perm=get(a["perm"], R, i32), iter_ptr=get(a["iter_ptr"], a["width"] + 1, i32),
                    col_idx=get(a["col_idx"], Z, i32), value=get(a["value"], Z, f32))
+    elif f == "SELL":
+        S, n = a["section_rows"], a["ell_slots"]
+        out.update(section_rows=S, perm=get(a["perm"], R, i32),
+                   sec_ptr=get(a["sec_ptr"], (R + S - 1) // S + 1, i32),
+                   col_idx=get(a["col_idx"], n, i32), value=get(a["value"], n, f32))
     return out
 
 
@@ -272,7 +283,7 @@ class SparseMatrix:
         self.handle = spmv_create_csr(self.num_rows, self.num_cols, self.nnz, row_ptrs, col_idx,
                                       value, stream)
 
-    def convert(self, fmt, ell_width=0, stream=None):
+    def convert(self, fmt, ell_width=0, stream=None, section_rows=0):
         f = FORMAT_NAMES[_fmt(fmt)]
         if f == "COO":
             spmv_convert_coo(self.handle, stream)
@@ -282,6 +293,8 @@ class SparseMatrix:
             spmv_convert_hyb(self.handle, ell_width, stream)
         elif f == "JDS":
             spmv_convert_jds(self.handle, stream)
+        elif f == "SELL":
+            spmv_convert_sell(self.handle, section_rows, stream)
         elif f != "CSR":
             raise ValueError(f"cannot convert to {f}")
 

@@ -195,6 +195,19 @@ struct spmv_handle_s {
   float* jdsVal = nullptr;
   std::vector<Buf> jdsBufs;
 
+  // SELL (sectioned ELL, the JDS variant)
+  bool hasSell = false;
+  int sellS = 0;
+  int sellW0 = 0;          // widest section
+  long long sellSlots = 0;
+  int sellNItems = 0;
+  int* sellPerm = nullptr;
+  int* sellSecPtr = nullptr;
+  int* sellCol = nullptr;
+  float* sellVal = nullptr;
+  spmv::SellItem* sellItems = nullptr;
+  std::vector<Buf> sellBufs;
+
   int alloc(size_t bytes, cudaStream_t s, void** out, std::vector<Buf>& list) {
     *out = nullptr;
     if (bytes == 0) return SPMV_OK;
@@ -546,6 +559,104 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   return SPMV_OK;
 }
 
+int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (sectionRows < 0) return SPMV_ERR_INVALID_ARG;
+  const int S = sectionRows > 0 ? sectionRows : spmv::kSellDefaultRows;
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  h->release(h->sellBufs, s);
+  h->hasSell = false;
+  const long long R = h->R;
+  const int L = (int)h->stats.max_len;
+  const long long nsec = (R + S - 1) / S;
+  std::vector<Buf> tmp;
+  auto fail = [&](int code) {
+    h->release(tmp, s);
+    h->release(h->sellBufs, s);
+    return code;
+  };
+  int st = alloc_typed(h, R, s, &h->sellPerm, h->sellBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, nsec + 1, s, &h->sellSecPtr, h->sellBufs);
+  void* scratch = nullptr;
+  if (st == SPMV_OK) st = h->alloc(spmv::sell_scratch_bytes(h->R, L), s, &scratch, tmp);
+  if (st == SPMV_OK)
+    st = record(spmv::launch_sell_sort(h->R, L, h->rowPtrs, h->sellPerm, scratch, s));
+  if (st != SPMV_OK) return fail(st);
+  // Section widths (length of each section's first sorted row): from the
+  // exact length histogram when every row is shorter than kExactLenBins,
+  // else computed on the device and read back (one synchronisation).
+  std::vector<int> width((size_t)nsec, 0);
+  if (L < spmv::kExactLenBins) {
+    long long pos = 0;  // sorted positions [pos, pos + count) have length len
+    for (int len = L; len >= 0 && pos < R; --len) {
+      const long long c = h->histExact[len];
+      for (long long k = (pos + S - 1) / S; k < nsec && k * S < pos + c; ++k)
+        width[(size_t)k] = len;
+      pos += c;
+    }
+  } else if (nsec > 0) {
+    int* dW = nullptr;
+    st = alloc_typed(h, nsec, s, &dW, tmp);
+    if (st == SPMV_OK)
+      st = record(spmv::launch_sell_widths(h->R, S, (int)nsec, h->rowPtrs, h->sellPerm, dW, s));
+    if (st == SPMV_OK)
+      st = record(cudaMemcpyAsync(width.data(), dW, sizeof(int) * (size_t)nsec,
+                                  cudaMemcpyDeviceToHost, s));
+    if (st == SPMV_OK) st = record(cudaStreamSynchronize(s));
+    if (st != SPMV_OK) return fail(st);
+  }
+  std::vector<int> secPtr((size_t)nsec + 1, 0);
+  long long slots = 0;
+  for (long long k = 0; k < nsec; ++k) {
+    const long long hk = R - k * S < S ? R - k * S : S;
+    secPtr[(size_t)k] = (int)slots;
+    slots += hk * width[(size_t)k];
+    // int32 offsets, and the same padding budget as ELL
+    if (slots > INT32_MAX || slots > 4LL * h->Z + R) return fail(SPMV_ERR_TOO_LARGE);
+  }
+  secPtr[(size_t)nsec] = (int)slots;
+  st = record(cudaMemcpyAsync(h->sellSecPtr, secPtr.data(), sizeof(int) * secPtr.size(),
+                              cudaMemcpyHostToDevice, s));
+  if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellCol, h->sellBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellVal, h->sellBufs);
+  if (st == SPMV_OK && slots > 0)
+    st = record(spmv::launch_sell_scatter(h->R, S, h->rowPtrs, h->colIdx, h->value, scratch,
+                                          h->sellSecPtr, h->sellCol, h->sellVal, s));
+  if (st != SPMV_OK) return fail(st);
+  // tail work items of the sections wider than kSellMainSlots
+  std::vector<spmv::SellItem> items;
+  const int rowsPerItem = (S & 3) == 0 ? 128 : 32;
+  for (long long k = 0; k < nsec && width[(size_t)k] > spmv::kSellMainSlots; ++k) {
+    const int hk = (int)(R - k * S < S ? R - k * S : S);
+    for (int t0 = spmv::kSellMainSlots; t0 < width[(size_t)k]; t0 += spmv::kSellTailSlots) {
+      const int t1 = t0 + spmv::kSellTailSlots < width[(size_t)k] ? t0 + spmv::kSellTailSlots
+                                                                  : width[(size_t)k];
+      for (int j0 = 0; j0 < hk; j0 += rowsPerItem) items.push_back({(int)k, t0, t1, j0});
+    }
+  }
+  if (items.size() > (size_t)INT32_MAX) return fail(SPMV_ERR_TOO_LARGE);
+  if (!items.empty()) {
+    st = alloc_typed(h, (long long)items.size(), s, &h->sellItems, h->sellBufs);
+    if (st == SPMV_OK)
+      st = record(cudaMemcpyAsync(h->sellItems, items.data(),
+                                  sizeof(spmv::SellItem) * items.size(),
+                                  cudaMemcpyHostToDevice, s));
+    if (st != SPMV_OK) return fail(st);
+  } else {
+    h->sellItems = nullptr;
+  }
+  h->release(tmp, s);
+  h->sellS = S;
+  h->sellW0 = nsec > 0 ? width[0] : 0;
+  h->sellSlots = slots;
+  h->sellNItems = (int)items.size();
+  h->hasSell = true;
+  return SPMV_OK;
+}
+
 int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
   SPMV_TRY(check_handle(h));
   if (format) *format = (spmv_format)h->stats.auto_format;
@@ -556,7 +667,8 @@ int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
 int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
   SPMV_TRY(check_handle(h));
   if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
-  if (format < SPMV_COO || format > SPMV_JDS) return SPMV_ERR_INVALID_ARG;
+  if (format < SPMV_COO || format > SPMV_SELL || format == SPMV_AUTO)
+    return SPMV_ERR_INVALID_ARG;
   if (h->R > 0 && !d_y) return SPMV_ERR_INVALID_ARG;
   if (h->C > 0 && !d_x) return SPMV_ERR_INVALID_ARG;
   if (h->R > 0 && h->C > 0) {
@@ -569,6 +681,7 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
     case SPMV_ELL: if (!h->hasEll) return SPMV_ERR_NOT_CONVERTED; break;
     case SPMV_HYB: if (!h->hasHyb) return SPMV_ERR_NOT_CONVERTED; break;
     case SPMV_JDS: if (!h->hasJds) return SPMV_ERR_NOT_CONVERTED; break;
+    case SPMV_SELL: if (!h->hasSell) return SPMV_ERR_NOT_CONVERTED; break;
     default: break;
   }
   if (h->R == 0) return SPMV_OK;
@@ -603,6 +716,11 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
       return record(spmv::launch_spmv_jds(h->R, h->jdsMaxLen, h->jdsTSplit, h->jdsWTail,
                                           h->jdsIterPtr, h->jdsPerm, h->jdsCol, h->jdsVal, d_x,
                                           d_y, s));
+    case SPMV_SELL:
+      if (h->sellSlots == 0) return SPMV_OK;
+      return record(spmv::launch_spmv_sell(h->R, h->sellS, h->sellSecPtr, h->sellPerm,
+                                           h->sellCol, h->sellVal, h->sellItems, h->sellNItems,
+                                           d_x, d_y, s));
     default:
       return SPMV_ERR_INVALID_ARG;
   }
@@ -664,6 +782,16 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       out->perm = h->jdsPerm;
       out->iter_ptr = h->jdsIterPtr;
       return SPMV_OK;
+    case SPMV_SELL:
+      if (!h->hasSell) return SPMV_ERR_NOT_CONVERTED;
+      out->width = h->sellW0;
+      out->ell_slots = h->sellSlots;
+      out->col_idx = h->sellCol;
+      out->value = h->sellVal;
+      out->perm = h->sellPerm;
+      out->sec_ptr = h->sellSecPtr;
+      out->section_rows = h->sellS;
+      return SPMV_OK;
     default:
       return SPMV_ERR_INVALID_ARG;
   }
@@ -679,6 +807,7 @@ int spmv_destroy(spmv_handle h) {
   h->release(h->ellBufs, s);
   h->release(h->hybBufs, s);
   h->release(h->jdsBufs, s);
+  h->release(h->sellBufs, s);
   delete h;
   return st;
 }

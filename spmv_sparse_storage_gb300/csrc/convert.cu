@@ -453,25 +453,23 @@ size_t jds_sort_scratch_bytes(int R, int maxLen) {
   return (size_t)ints * sizeof(int);
 }
 
-cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
-                             const float* value, int* perm, int* iterPtr, int* jdsCol,
-                             float* jdsVal, void* scratch, const int* hostIterPtr,
-                             cudaStream_t s) {
-  if (R <= 0) {
-    // iterPtr has maxLen + 1 = 1 entry
-    return cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
-  }
+// Stable sort of the rows by length, longest first (LSD radix on maxLen - len
+// with 8-bit digits): perm[s] = row at sorted position s, inv[row] = s. The
+// sorted keys are left in keysB when needKeys (else they are not written).
+// Scratch (int32): keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles+1] scan.
+static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, int* scratch,
+                            bool needKeys, const int** sortedKeys, int** invOut,
+                            int** scanScratchOut, cudaStream_t s) {
   const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
   const long long nh = (long long)kRadix * nTiles;
-  int* keysA = static_cast<int*>(scratch);
+  int* keysA = scratch;
   int* valsA = keysA + R;
   int* keysB = valsA + R;
   int* inv = keysB + R;
   int* hist = inv + R;
   int* scanScratch = hist + nh + 1;
-  const long long scanN = nh > maxLen ? nh : maxLen;
-  int* width = scanScratch + scan_scratch_ints(scanN);
-
+  *invOut = inv;
+  *scanScratchOut = scanScratch;
   int bits = 0;
   while (bits < 31 && (1LL << bits) <= maxLen) ++bits;
   const int passes = bits == 0 ? 1 : (bits + kRadixBits - 1) / kRadixBits;
@@ -491,14 +489,35 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
     if (err != cudaSuccess) return err;
     const bool last = p == passes - 1;
     k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(
-        in, R, shift, (int)nTiles, hist, (last && hostIterPtr) ? nullptr : kBuf[outSlot],
+        in, R, shift, (int)nTiles, hist, (last && !needKeys) ? nullptr : kBuf[outSlot],
         vBuf[outSlot], last ? inv : nullptr);
     note_launches(1);
     kIn = kBuf[outSlot];
     vIn = vBuf[outSlot];
     outSlot ^= 1;
   }
-  const int* sortedKeys = kIn;
+  *sortedKeys = kIn;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
+                             const float* value, int* perm, int* iterPtr, int* jdsCol,
+                             float* jdsVal, void* scratch, const int* hostIterPtr,
+                             cudaStream_t s) {
+  if (R <= 0) {
+    // iterPtr has maxLen + 1 = 1 entry
+    return cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
+  }
+  const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
+  const long long nh = (long long)kRadix * nTiles;
+  const long long scanN = nh > maxLen ? nh : maxLen;
+  const int* sortedKeys = nullptr;
+  int* inv = nullptr;
+  int* scanScratch = nullptr;
+  cudaError_t err = row_sort(R, maxLen, rowPtrs, perm, static_cast<int*>(scratch),
+                             hostIterPtr == nullptr, &sortedKeys, &inv, &scanScratch, s);
+  if (err != cudaSuccess) return err;
+  int* width = scanScratch + scan_scratch_ints(scanN);
   if (maxLen > 0) {
     if (hostIterPtr) {
       // widths known exactly on the host from the length histogram
@@ -519,6 +538,103 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
     err = cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
     if (err != cudaSuccess) return err;
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Sectioned ELL ("Regularized Formats ...", section "JDS format", variant
+// paragraph): the rows sorted as for JDS, cut into sections of S sorted rows,
+// each section an ELL padded to its own longest row, column-major inside the
+// section: slot t of the j-th row of section k at secPtr[k] + t*h_k + j.
+// ---------------------------------------------------------------------------
+size_t sell_scratch_bytes(int R, int maxLen) { return jds_sort_scratch_bytes(R, maxLen); }
+
+cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, void* scratch,
+                             cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const int* sortedKeys = nullptr;
+  int* inv = nullptr;
+  int* scanScratch = nullptr;
+  return row_sort(R, maxLen, rowPtrs, perm, static_cast<int*>(scratch), false, &sortedKeys,
+                  &inv, &scanScratch, s);
+}
+
+// width of section k = length of its first sorted row
+__global__ void k_sell_widths(int R, int S, int nsec, const int* __restrict__ rowPtrs,
+                              const int* __restrict__ perm, int* __restrict__ widths) {
+  const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= nsec) return;
+  const int r = perm[k * S];
+  widths[k] = rowPtrs[r + 1] - rowPtrs[r];
+}
+
+cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const int* perm,
+                               int* widths, cudaStream_t s) {
+  if (nsec <= 0) return cudaSuccess;
+  k_sell_widths<<<(unsigned)(((long long)nsec + 255) / 256), 256, 0, s>>>(R, S, nsec, rowPtrs,
+                                                                         perm, widths);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
+// Row-side scatter: original row r (sorted position inv[r], section k, row j
+// of the section) writes its w_k slots, real entries then padding (column -1,
+// value +0.0f). A thread writes the first kCoop slots; the warp then writes
+// each wider section's remaining slots of its rows together, one per lane.
+__global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* __restrict__ rowPtrs,
+                                                      const int* __restrict__ colIdx,
+                                                      const float* __restrict__ value,
+                                                      const int* __restrict__ inv,
+                                                      const int* __restrict__ secPtr,
+                                                      int* __restrict__ sellCol,
+                                                      float* __restrict__ sellVal) {
+  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const int lane = threadIdx.x & 31;
+  int a = 0, len = 0, w = 0, h = 1, j = 0, base = 0;
+  if (r < R) {
+    a = rowPtrs[r];
+    len = rowPtrs[r + 1] - a;
+    const int sidx = inv[r];
+    const int k = sidx / S;
+    j = sidx - k * S;
+    h = min(S, R - k * S);
+    base = secPtr[k];
+    w = (secPtr[k + 1] - base) / h;
+    const int lim = w < kCoop ? w : kCoop;
+    for (int t = 0; t < lim; ++t) {
+      const long long o = (long long)base + (long long)t * h + j;
+      const bool real = t < len;
+      sellCol[o] = real ? colIdx[a + t] : -1;
+      sellVal[o] = real ? value[a + t] : 0.0f;
+    }
+  }
+  unsigned wide = __ballot_sync(kFullMask, w > kCoop);
+  while (wide) {
+    const int src = __ffs(wide) - 1;
+    wide &= wide - 1;
+    const int la = __shfl_sync(kFullMask, a, src);
+    const int ll = __shfl_sync(kFullMask, len, src);
+    const int lw = __shfl_sync(kFullMask, w, src);
+    const int lh = __shfl_sync(kFullMask, h, src);
+    const int lj = __shfl_sync(kFullMask, j, src);
+    const int lb = __shfl_sync(kFullMask, base, src);
+    for (int t = kCoop + lane; t < lw; t += 32) {
+      const long long o = (long long)lb + (long long)t * lh + lj;
+      const bool real = t < ll;
+      sellCol[o] = real ? colIdx[la + t] : -1;
+      sellVal[o] = real ? value[la + t] : 0.0f;
+    }
+  }
+}
+
+cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
+                                const float* value, const void* scratch, const int* secPtr,
+                                int* sellCol, float* sellVal, cudaStream_t s) {
+  if (R <= 0) return cudaSuccess;
+  const int* inv = static_cast<const int*>(scratch) + 3LL * R;  // row_sort's layout
+  k_sell_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
+      R, S, rowPtrs, colIdx, value, inv, secPtr, sellCol, sellVal);
+  note_launches(1);
   return cudaGetLastError();
 }
 

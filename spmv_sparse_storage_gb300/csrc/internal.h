@@ -111,6 +111,24 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
                              float* jdsVal, void* scratch, const int* hostIterPtr,
                              cudaStream_t s);
 constexpr int kJdsPad = 8;  // extra elements after the JDS arrays (aligned vector reads)
+// Sectioned ELL (the JDS variant): sort, section widths (for a read-back when
+// the host cannot derive them), scatter; secPtr is int32 (slots < 2^31).
+constexpr int kSellDefaultRows = 128;  // default section height
+constexpr int kSellMainSlots = 64;     // slots per row done by the row-parallel part
+constexpr int kSellTailSlots = 64;     // slots per row of one tail work item
+// One tail work item of a section wider than kSellMainSlots: slots [t0, t1) of
+// rows j0 .. j0 + 127 (4 per lane; 32 rows, one per lane, when S % 4 != 0).
+struct SellItem {
+  int k, t0, t1, j0;
+};
+size_t sell_scratch_bytes(int R, int maxLen);
+cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, void* scratch,
+                             cudaStream_t s);
+cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const int* perm,
+                               int* widths, cudaStream_t s);
+cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
+                                const float* value, const void* scratch, const int* secPtr,
+                                int* sellCol, float* sellVal, cudaStream_t s);
 
 // spmv_kernels.cu
 // fills hi, flags and mask of every chunk record; runs after the stats pass
@@ -123,6 +141,10 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
                             const float* x, float* y, cudaStream_t s);
+// items: tail work of the sections wider than kSellMainSlots (nItems of them)
+cudaError_t launch_spmv_sell(int R, int S, const int* secPtr, const int* perm,
+                             const int* sellCol, const float* sellVal, const SellItem* items,
+                             int nItems, const float* x, float* y, cudaStream_t s);
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
                             const int* perm, const int* jdsCol, const float* jdsVal,
                             const float* x, float* y, cudaStream_t s);

@@ -712,4 +712,142 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Sectioned ELL ("Regularized Formats (ELL, Hybrid ELL-COO and JDS)", section
+// "JDS format", variant paragraph). Sorted rows in sections of S; slot t of
+// row j of section k at secPtr[k] + t*h_k + j. A thread owns 4 consecutive
+// sorted rows (one when S % 4 != 0): with S % 4 == 0 every section starts on
+// a multiple of 4 slots, so a full section's 4 rows are one aligned 16-byte
+// load of columns and one of values per slot, a warp reads 512 contiguous
+// bytes per slot. Slots past kSellMainSlots of the wide sections (a prefix,
+// the rows being sorted) are cut into SellItems handled by extra warps; the
+// rows of those sections add into y with atomics.
+// ---------------------------------------------------------------------------
+template <bool VEC>
+__device__ __forceinline__ void sell_rows(const int* __restrict__ col,
+                                          const float* __restrict__ val,
+                                          const float* __restrict__ x, long long base, int h,
+                                          int j, int n, int t0, int t1, float acc[4]) {
+  if (VEC && n == 4 && (h & 3) == 0) {
+    const long long hq = h >> 2;
+    const int4* c4 = reinterpret_cast<const int4*>(col + base + (long long)t0 * h + j);
+    const float4* v4 = reinterpret_cast<const float4*>(val + base + (long long)t0 * h + j);
+    int t = t0;
+    for (; t + 4 <= t1; t += 4, c4 += 4 * hq, v4 += 4 * hq) {
+      int4 c[4];
+      float4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        c[u] = ld_stream(c4 + u * hq);
+        v[u] = ld_stream(v4 + u * hq);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c[u].x >= 0) acc[0] = fmaf(v[u].x, ld_x(x + c[u].x), acc[0]);
+        if (c[u].y >= 0) acc[1] = fmaf(v[u].y, ld_x(x + c[u].y), acc[1]);
+        if (c[u].z >= 0) acc[2] = fmaf(v[u].z, ld_x(x + c[u].z), acc[2]);
+        if (c[u].w >= 0) acc[3] = fmaf(v[u].w, ld_x(x + c[u].w), acc[3]);
+      }
+    }
+    for (; t < t1; ++t, c4 += hq, v4 += hq) {
+      const int4 c = ld_stream(c4);
+      const float4 v = ld_stream(v4);
+      if (c.x >= 0) acc[0] = fmaf(v.x, ld_x(x + c.x), acc[0]);
+      if (c.y >= 0) acc[1] = fmaf(v.y, ld_x(x + c.y), acc[1]);
+      if (c.z >= 0) acc[2] = fmaf(v.z, ld_x(x + c.z), acc[2]);
+      if (c.w >= 0) acc[3] = fmaf(v.w, ld_x(x + c.w), acc[3]);
+    }
+  } else {
+    // the last, partial section (h % 4 != 0), or S % 4 != 0
+    for (int t = t0; t < t1; ++t) {
+      const long long o = base + (long long)t * h + j;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (u < n) {
+          const int c = ld_stream(col + o + u);
+          const float v = ld_stream(val + o + u);
+          if (c >= 0) acc[u] = fmaf(v, ld_x(x + c), acc[u]);
+        }
+      }
+    }
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int mainBlocks,
+                                                      const int* __restrict__ secPtr,
+                                                      const int* __restrict__ perm,
+                                                      const int* __restrict__ col,
+                                                      const float* __restrict__ val,
+                                                      const SellItem* __restrict__ items,
+                                                      int nItems, const float* __restrict__ x,
+                                                      float* __restrict__ y) {
+  constexpr int kRows = VEC ? 4 : 1;
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  int s0, n;
+  bool atomic;
+  if ((int)blockIdx.x < mainBlocks) {
+    const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (q * kRows >= R) return;
+    s0 = (int)(q * kRows);
+    const int k = s0 / S;
+    const int k0 = k * S;
+    const int h = min(S, R - k0);
+    const int base = secPtr[k];
+    const int w = (secPtr[k + 1] - base) / h;
+    n = min(kRows, R - s0);
+    sell_rows<VEC>(col, val, x, base, h, s0 - k0, n, 0, min(w, kSellMainSlots), acc);
+    atomic = w > kSellMainSlots;
+  } else {
+    const long long id = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
+                         (threadIdx.x >> 5);
+    if (id >= nItems) return;
+    const SellItem it = items[id];
+    const int k0 = it.k * S;
+    const int h = min(S, R - k0);
+    const int j = it.j0 + (threadIdx.x & 31) * kRows;
+    if (j >= h) return;
+    n = min(kRows, h - j);
+    sell_rows<VEC>(col, val, x, secPtr[it.k], h, j, n, it.t0, it.t1, acc);
+    s0 = k0 + j;
+    atomic = true;
+  }
+  int r[4];
+  if (VEC && n == 4) {
+    const int4 p = *reinterpret_cast<const int4*>(perm + s0);
+    r[0] = p.x; r[1] = p.y; r[2] = p.z; r[3] = p.w;
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) r[u] = u < n ? perm[s0 + u] : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    if (u < n) {
+      if (atomic)
+        atomicAdd(y + r[u], acc[u]);
+      else
+        y[r[u]] += acc[u];
+    }
+  }
+}
+
+cudaError_t launch_spmv_sell(int R, int S, const int* secPtr, const int* perm,
+                             const int* sellCol, const float* sellVal, const SellItem* items,
+                             int nItems, const float* x, float* y, cudaStream_t s) {
+  if (R <= 0 || S <= 0) return cudaSuccess;
+  const bool vec = (S & 3) == 0;
+  const long long threads = vec ? ((long long)R + 3) / 4 : R;
+  const long long mainBlocks = (threads + 255) / 256;
+  const long long tailBlocks = ((long long)nItems + 7) / 8;
+  const unsigned grid = (unsigned)(mainBlocks + tailBlocks);
+  if (vec)
+    k_spmv_sell<true><<<grid, 256, 0, s>>>(R, S, (int)mainBlocks, secPtr, perm, sellCol, sellVal,
+                                           items, nItems, x, y);
+  else
+    k_spmv_sell<false><<<grid, 256, 0, s>>>(R, S, (int)mainBlocks, secPtr, perm, sellCol,
+                                            sellVal, items, nItems, x, y);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace spmv

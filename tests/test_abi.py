@@ -26,7 +26,7 @@ def sp():
 def test_header_lists_the_boundary():
     fns = header_functions()
     for name in ["spmv_create_csr", "spmv_convert_coo", "spmv_convert_ell", "spmv_convert_hyb",
-                 "spmv_convert_jds", "spmv_run", "spmv_select", "spmv_get_stats",
+                 "spmv_convert_jds", "spmv_convert_sell", "spmv_run", "spmv_select", "spmv_get_stats",
                  "spmv_export", "spmv_destroy", "spmv_status_string"]:
         assert name in fns
 
@@ -63,6 +63,7 @@ def test_host_argument_checks_without_gpu(sp):
     for fn in ("spmv_convert_coo", "spmv_convert_ell", "spmv_convert_jds"):
         assert getattr(lib, fn)(None, None) == sp.SPMV_ERR_INVALID_ARG
     assert lib.spmv_convert_hyb(None, 0, None) == sp.SPMV_ERR_INVALID_ARG
+    assert lib.spmv_convert_sell(None, 0, None) == sp.SPMV_ERR_INVALID_ARG
     assert lib.spmv_run(None, 0, None, None, None) == sp.SPMV_ERR_INVALID_ARG
     assert lib.spmv_select(None, None, None) == sp.SPMV_ERR_INVALID_ARG
     assert lib.spmv_get_stats(None, None) == sp.SPMV_ERR_INVALID_ARG

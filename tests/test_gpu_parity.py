@@ -16,7 +16,16 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS")
+FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS", "SELL")
+
+
+def sell_fits(row_ptrs, S):
+    """The library's size rule for SELL: total slots (each section of S sorted
+    rows padded to its longest row) within int32 and 4*nnz + numRows."""
+    lens = np.sort(np.diff(np.asarray(row_ptrs, np.int64)))[::-1]
+    R, Z = lens.size, int(lens.sum())
+    slots = sum(min(S, R - k) * int(lens[k]) for k in range(0, R, S))
+    return slots <= min(2**31 - 1, 4 * Z + R)
 
 
 @pytest.fixture(scope="module")
@@ -48,7 +57,7 @@ def check_tol(y, yref, mag, what):
 
 
 def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, ell_ok=True,
-                 offset=0):
+                 offset=0, sell_rows=(0,)):
     """Convert `inp` to every format on the GPU, compare the arrays with the
     oracle's conversions and the SpMV results with the oracle's y."""
     rp_t = dev(inp.row_ptrs)
@@ -74,15 +83,25 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
         if R and ost["max_len"] < 4096:
             assert st["auto_hyb_width"] == orc.hyb_auto_width(inp.row_ptrs)
         for f in formats:
-            widths = hyb_widths if f == "HYB" else (None,)
+            widths = hyb_widths if f == "HYB" else sell_rows if f == "SELL" else (None,)
             for w in widths:
                 if f == "ELL" and not ell_ok:
                     with pytest.raises(sp.SpmvError) as ei:
                         m.convert("ELL")
                     assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
                     continue
+                if f == "SELL" and not sell_fits(inp.row_ptrs, w or 128):
+                    with pytest.raises(sp.SpmvError) as ei:
+                        m.convert("SELL", section_rows=w)
+                    assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
+                    with pytest.raises(sp.SpmvError) as ei:
+                        m.run("SELL", x_t, dev(inp.y0))
+                    assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
+                    continue
                 if f == "HYB":
                     m.convert(f, ell_width=w)
+                elif f == "SELL":
+                    m.convert(f, section_rows=w)
                 else:
                     m.convert(f)
                 if arrays:
@@ -91,7 +110,7 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
                 y_t = dev(inp.y0)
                 m.run(f, x_t, y_t)
                 torch.cuda.synchronize()
-                key = f if f != "HYB" else f"HYB{w}"
+                key = f"{f}{w}" if f in ("HYB", "SELL") else f
                 results[key] = check_tol(y_t.cpu().numpy(), yref, mag, f"{inp.name}/{key}")
         if st["auto_format"] in formats and (st["auto_format"] != "ELL" or ell_ok):
             y_t = dev(inp.y0)
@@ -134,6 +153,16 @@ def compare_arrays(orc, inp, f, got, w, st):
         assert same_bits(got["iter_ptr"], want["iter_ptr"])
         assert same_bits(got["col_idx"], want["col_idx"])
         assert same_bits(got["value"], want["value"])
+    elif f == "SELL":
+        S = w or 128
+        want = orc.csr_to_sell(rp, ci, va, S)
+        assert got["section_rows"] == S
+        assert same_bits(got["perm"], want["perm"])
+        assert np.array_equal(got["sec_ptr"].astype(np.int64), want["sec_ptr"])
+        assert same_bits(got["col_idx"], want["col_idx"])
+        assert same_bits(got["value"], want["value"])
+        lens = np.diff(rp)
+        assert got["width"] == (int(lens.max()) if lens.size else 0)
 
 
 # --- the worked example -------------------------------------------------------
@@ -142,10 +171,10 @@ def test_fig14_1_every_format(sp, orc):
     rp, ci, va = orc.dense_to_csr(synth.fig14_1_dense())
     inp = synth.CSRInput("fig14_1", 4, 4, rp, ci, va, np.array([1, 2, 3, 4], np.float32),
                          np.zeros(4, np.float32))
-    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 2, 3))
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 2, 3), sell_rows=(0, 1, 2, 3, 4, 100))
     with sp.SparseMatrix(4, 4, dev(rp), dev(ci), dev(va)) as m:
-        for f in ("COO", "ELL", "HYB", "JDS"):
-            m.convert(f, ell_width=2) if f == "HYB" else m.convert(f)
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
+            m.convert(f, ell_width=2, section_rows=2)
         for f in FORMATS:
             y = torch.zeros(4, device="cuda")
             m.run(f, dev(inp.x), y)
@@ -156,6 +185,11 @@ def test_fig14_1_every_format(sp, orc):
         jds = m.export("JDS")
         assert jds["perm"].tolist() == [1, 0, 2, 3]
         assert jds["iter_ptr"].tolist() == [0, 4, 7, 8]
+        sell = m.export("SELL")  # two sections of two rows, widths 3 and 2
+        assert sell["perm"].tolist() == [1, 0, 2, 3]
+        assert sell["sec_ptr"].tolist() == [0, 6, 10]
+        assert sell["value"].tolist() == [5, 1, 3, 7, 9, 0, 2, 6, 8, 0]
+        assert sell["col_idx"].tolist() == [0, 0, 2, 1, 3, -1, 1, 3, 2, -1]
 
 
 # --- irregular and degenerate matrices -------------------------------------------
@@ -187,7 +221,7 @@ def test_edge_cases(sp, orc, name):
     mx = int(lens.max()) if lens.size else 0
     R, Z = inp.num_rows, inp.nnz
     ell_ok = R * mx <= min(2**31 - 1, 4 * Z + R)
-    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 5), ell_ok=ell_ok)
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 5), ell_ok=ell_ok, sell_rows=(0, 1, 3, 32))
 
 
 @pytest.mark.parametrize("offset", [1, 2, 3])
@@ -203,7 +237,7 @@ def test_empty_matrix(sp):
     rp = torch.zeros(1, dtype=torch.int32, device="cuda")
     with sp.SparseMatrix(0, 0, rp, torch.empty(0, dtype=torch.int32, device="cuda"),
                          torch.empty(0, device="cuda")) as m:
-        for f in ("COO", "ELL", "HYB", "JDS"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
             m.convert(f)
         for f in FORMATS:
             m.run(f, None, None)
@@ -304,7 +338,7 @@ def test_not_converted_and_argument_errors(sp, orc):
     with _fig(sp, orc) as m:
         x = dev(np.array([1, 2, 3, 4], np.float32))
         y = torch.zeros(4, device="cuda")
-        for f in ("COO", "ELL", "HYB", "JDS"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
             with pytest.raises(sp.SpmvError) as ei:
                 m.run(f, x, y)
             assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
@@ -324,6 +358,47 @@ def test_not_converted_and_argument_errors(sp, orc):
             m.run(7, x, y)
         with pytest.raises(sp.SpmvError):
             sp.spmv_convert_hyb(m.handle, -1)
+        with pytest.raises(sp.SpmvError) as ei:
+            sp.spmv_convert_sell(m.handle, -1)
+        assert ei.value.code == sp.SPMV_ERR_INVALID_ARG
+
+
+def test_sell_section_heights_and_wide_sections(sp, orc):
+    """Section heights that are and are not multiples of 4, numRows not a
+    multiple of S, and sections wider than the row-parallel part (split into
+    tail items): arrays bit-exact, y within the tolerance."""
+    inp = synth.random_csr(31, 9001, 7000, mean_len=6, empty_frac=0.05, long_rows=300,
+                           long_len=700, name="sell_wide")
+    check_matrix(sp, orc, inp, formats=("SELL",), sell_rows=(0, 1, 2, 4, 5, 64, 100, 128,
+                                                              256, 1000, 9001, 20000))
+    # some rows beyond the exact histogram range: widths read back from the device
+    big = synth.random_csr(32, 3000, 40_000, mean_len=20, long_rows=130, long_len=1500,
+                           name="sell_readback")
+    check_matrix(sp, orc, big, formats=("SELL",), sell_rows=(0, 4, 7, 128))
+
+
+def test_sell_reconvert_and_too_large(sp, orc):
+    inp = synth.random_csr(33, 2000, 50_000, mean_len=2, long_rows=1, long_len=40_000)
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        # S = 128: the long row pads a section to 128 * 40000 slots, over budget;
+        # a failed conversion leaves no SELL behind, a later one replaces it
+        assert not sell_fits(inp.row_ptrs, 128) and sell_fits(inp.row_ptrs, 1)
+        for S in (1, 0, 3, 8, 2, 128):
+            if not sell_fits(inp.row_ptrs, S or 128):
+                with pytest.raises(sp.SpmvError) as ei:
+                    m.convert("SELL", section_rows=S)
+                assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
+                with pytest.raises(sp.SpmvError) as ei:
+                    m.run("SELL", dev(inp.x), dev(inp.y0))
+                assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
+                continue
+            m.convert("SELL", section_rows=S)
+            y = dev(inp.y0)
+            m.run("SELL", dev(inp.x), y)
+            torch.cuda.synchronize()
+            check_tol(y.cpu().numpy(), yref, mag, f"sell S={S}")
 
 
 def test_accumulates_and_streams(sp, orc):
@@ -334,7 +409,7 @@ def test_accumulates_and_streams(sp, orc):
     with torch.cuda.stream(s):
         m = sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                             dev(inp.value))
-        for f in ("COO", "ELL", "HYB", "JDS"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
             m.convert(f)
         for f in FORMATS:
             y = dev(inp.y0)
@@ -353,7 +428,7 @@ def test_guard_bands_untouched(sp, orc):
     sentinel = np.float32(-7.25e33)
     with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                          dev(inp.value)) as m:
-        for f in ("COO", "ELL", "HYB", "JDS"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
             m.convert(f)
         for f in FORMATS:
             buf = torch.full((inp.num_rows + 2 * G,), float(sentinel), device="cuda")
