@@ -394,7 +394,7 @@ def run_kernels(args, device):
                       "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1),
                       "convert_us": conv_us.get(f)}
             if f in ("ELL", "HYB", "SELL"):
-                out[f]["slots"] = m.export(f)["ell_slots"]
+                out[f]["slots"] = sp.spmv_export(m.handle, f)["ell_slots"]
         sel = m.select()
     return {"mode": "kernels", "workload": args.workload, "rows": R, "nnz": Z,
             "l2_flush_bytes": int(flush.numel() * 4), "reps": args.reps, "peak": peak,

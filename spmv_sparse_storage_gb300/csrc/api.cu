@@ -572,6 +572,27 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
   const long long R = h->R;
   const int L = (int)h->stats.max_len;
   const long long nsec = (R + S - 1) / S;
+  const long long budget = 4LL * h->Z + R < INT32_MAX ? 4LL * h->Z + R : INT32_MAX;
+  auto section_rows = [&](long long k) { return R - k * S < S ? R - k * S : (long long)S; };
+  // Section widths (length of each section's first sorted row). With every
+  // row shorter than kExactLenBins they follow from the exact length
+  // histogram, before any device work: the size check comes first and the
+  // section offsets are scanned on the device. Otherwise they are computed on
+  // the device after the sort and read back (one synchronisation).
+  const bool fromHist = L < spmv::kExactLenBins;
+  std::vector<int> width((size_t)nsec, 0);
+  long long slots = 0;
+  if (fromHist) {
+    long long pos = 0;  // sorted positions [pos, pos + count) have length len
+    for (int len = L; len >= 0 && pos < R; --len) {
+      const long long c = h->histExact[len];
+      for (long long k = (pos + S - 1) / S; k < nsec && k * S < pos + c; ++k)
+        width[(size_t)k] = len;
+      pos += c;
+    }
+    for (long long k = 0; k < nsec; ++k) slots += section_rows(k) * width[(size_t)k];
+    if (slots > budget) return SPMV_ERR_TOO_LARGE;
+  }
   std::vector<Buf> tmp;
   auto fail = [&](int code) {
     h->release(tmp, s);
@@ -581,23 +602,14 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
   int st = alloc_typed(h, R, s, &h->sellPerm, h->sellBufs);
   if (st == SPMV_OK) st = alloc_typed(h, nsec + 1, s, &h->sellSecPtr, h->sellBufs);
   void* scratch = nullptr;
-  if (st == SPMV_OK) st = h->alloc(spmv::sell_scratch_bytes(h->R, L), s, &scratch, tmp);
+  if (st == SPMV_OK) st = h->alloc(spmv::sell_scratch_bytes(h->R, L, nsec), s, &scratch, tmp);
   if (st == SPMV_OK)
     st = record(spmv::launch_sell_sort(h->R, L, h->rowPtrs, h->sellPerm, scratch, s));
   if (st != SPMV_OK) return fail(st);
-  // Section widths (length of each section's first sorted row): from the
-  // exact length histogram when every row is shorter than kExactLenBins,
-  // else computed on the device and read back (one synchronisation).
-  std::vector<int> width((size_t)nsec, 0);
-  if (L < spmv::kExactLenBins) {
-    long long pos = 0;  // sorted positions [pos, pos + count) have length len
-    for (int len = L; len >= 0 && pos < R; --len) {
-      const long long c = h->histExact[len];
-      for (long long k = (pos + S - 1) / S; k < nsec && k * S < pos + c; ++k)
-        width[(size_t)k] = len;
-      pos += c;
-    }
-  } else if (nsec > 0) {
+  if (fromHist) {
+    st = record(spmv::launch_sell_offsets(h->R, S, L, nsec, h->rowPtrs, h->sellPerm,
+                                          h->sellSecPtr, scratch, s));
+  } else {
     int* dW = nullptr;
     st = alloc_typed(h, nsec, s, &dW, tmp);
     if (st == SPMV_OK)
@@ -607,37 +619,36 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
                                   cudaMemcpyDeviceToHost, s));
     if (st == SPMV_OK) st = record(cudaStreamSynchronize(s));
     if (st != SPMV_OK) return fail(st);
+    std::vector<int> secPtr((size_t)nsec + 1, 0);
+    for (long long k = 0; k < nsec; ++k) {
+      secPtr[(size_t)k] = (int)slots;
+      slots += section_rows(k) * width[(size_t)k];
+      if (slots > budget) return fail(SPMV_ERR_TOO_LARGE);  // int32 offsets, ELL's budget
+    }
+    secPtr[(size_t)nsec] = (int)slots;
+    st = record(cudaMemcpyAsync(h->sellSecPtr, secPtr.data(), sizeof(int) * secPtr.size(),
+                                cudaMemcpyHostToDevice, s));
   }
-  std::vector<int> secPtr((size_t)nsec + 1, 0);
-  long long slots = 0;
-  for (long long k = 0; k < nsec; ++k) {
-    const long long hk = R - k * S < S ? R - k * S : S;
-    secPtr[(size_t)k] = (int)slots;
-    slots += hk * width[(size_t)k];
-    // int32 offsets, and the same padding budget as ELL
-    if (slots > INT32_MAX || slots > 4LL * h->Z + R) return fail(SPMV_ERR_TOO_LARGE);
-  }
-  secPtr[(size_t)nsec] = (int)slots;
-  st = record(cudaMemcpyAsync(h->sellSecPtr, secPtr.data(), sizeof(int) * secPtr.size(),
-                              cudaMemcpyHostToDevice, s));
   if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellCol, h->sellBufs);
   if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellVal, h->sellBufs);
   if (st == SPMV_OK && slots > 0)
     st = record(spmv::launch_sell_scatter(h->R, S, h->rowPtrs, h->colIdx, h->value, scratch,
-                                          h->sellSecPtr, h->sellCol, h->sellVal, s));
+                                          h->sellSecPtr, (int)slots, h->sellCol, h->sellVal,
+                                          s));
   if (st != SPMV_OK) return fail(st);
-  // tail work items of the sections wider than kSellMainSlots
+  // tail work items of the sections wider than kSellMainSlots (a prefix)
   std::vector<spmv::SellItem> items;
   const int rowsPerItem = (S & 3) == 0 ? 128 : 32;
   for (long long k = 0; k < nsec && width[(size_t)k] > spmv::kSellMainSlots; ++k) {
-    const int hk = (int)(R - k * S < S ? R - k * S : S);
-    for (int t0 = spmv::kSellMainSlots; t0 < width[(size_t)k]; t0 += spmv::kSellTailSlots) {
-      const int t1 = t0 + spmv::kSellTailSlots < width[(size_t)k] ? t0 + spmv::kSellTailSlots
-                                                                  : width[(size_t)k];
-      for (int j0 = 0; j0 < hk; j0 += rowsPerItem) items.push_back({(int)k, t0, t1, j0});
+    const int wk = width[(size_t)k];
+    for (int t0 = spmv::kSellMainSlots; t0 < wk; t0 += spmv::kSellTailSlots) {
+      const int t1 = wk - t0 > spmv::kSellTailSlots ? t0 + spmv::kSellTailSlots : wk;
+      for (long long j0 = 0; j0 < section_rows(k); j0 += rowsPerItem)
+        items.push_back({(int)k, t0, t1, (int)j0});
     }
   }
   if (items.size() > (size_t)INT32_MAX) return fail(SPMV_ERR_TOO_LARGE);
+  h->sellItems = nullptr;
   if (!items.empty()) {
     st = alloc_typed(h, (long long)items.size(), s, &h->sellItems, h->sellBufs);
     if (st == SPMV_OK)
@@ -645,8 +656,6 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
                                   sizeof(spmv::SellItem) * items.size(),
                                   cudaMemcpyHostToDevice, s));
     if (st != SPMV_OK) return fail(st);
-  } else {
-    h->sellItems = nullptr;
   }
   h->release(tmp, s);
   h->sellS = S;
@@ -718,9 +727,9 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
                                           d_y, s));
     case SPMV_SELL:
       if (h->sellSlots == 0) return SPMV_OK;
-      return record(spmv::launch_spmv_sell(h->R, h->sellS, h->sellSecPtr, h->sellPerm,
-                                           h->sellCol, h->sellVal, h->sellItems, h->sellNItems,
-                                           d_x, d_y, s));
+      return record(spmv::launch_spmv_sell(h->R, h->sellS, (int)h->sellSlots, h->sellSecPtr,
+                                           h->sellPerm, h->sellCol, h->sellVal, h->sellItems,
+                                           h->sellNItems, d_x, d_y, s));
     default:
       return SPMV_ERR_INVALID_ARG;
   }

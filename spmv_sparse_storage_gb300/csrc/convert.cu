@@ -547,7 +547,30 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
 // each section an ELL padded to its own longest row, column-major inside the
 // section: slot t of the j-th row of section k at secPtr[k] + t*h_k + j.
 // ---------------------------------------------------------------------------
-size_t sell_scratch_bytes(int R, int maxLen) { return jds_sort_scratch_bytes(R, maxLen); }
+// the row sort's scratch, then the scratch of the scan of section sizes
+size_t sell_scratch_bytes(int R, int maxLen, long long nsec) {
+  return jds_sort_scratch_bytes(R, maxLen) + sizeof(int) * (size_t)scan_scratch_ints(nsec);
+}
+
+struct SellSlotsIn {  // slots of section k: h_k * length of its first sorted row
+  const int* rowPtrs;
+  const int* perm;
+  int R, S;
+  __device__ int operator()(long long k) const {
+    const long long s0 = k * S;
+    const int h = R - s0 < S ? (int)(R - s0) : S;
+    const int r = perm[s0];
+    return h * (rowPtrs[r + 1] - rowPtrs[r]);
+  }
+};
+
+cudaError_t launch_sell_offsets(int R, int S, int maxLen, long long nsec, const int* rowPtrs,
+                                const int* perm, int* secPtr, void* scratch, cudaStream_t s) {
+  if (nsec <= 0) return cudaMemsetAsync(secPtr, 0, sizeof(int), s);
+  int* scanScratch = reinterpret_cast<int*>(static_cast<char*>(scratch) +
+                                            jds_sort_scratch_bytes(R, maxLen));
+  return exclusive_scan(SellSlotsIn{rowPtrs, perm, R, S}, nsec, secPtr, scanScratch, s);
+}
 
 cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, void* scratch,
                              cudaStream_t s) {
@@ -586,7 +609,7 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
                                                       const float* __restrict__ value,
                                                       const int* __restrict__ inv,
                                                       const int* __restrict__ secPtr,
-                                                      int* __restrict__ sellCol,
+                                                      int cap, int* __restrict__ sellCol,
                                                       float* __restrict__ sellVal) {
   const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
@@ -599,7 +622,8 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
     j = sidx - k * S;
     h = min(S, R - k * S);
     base = secPtr[k];
-    w = (secPtr[k + 1] - base) / h;
+    const int end = secPtr[k + 1];
+    w = end <= cap ? (end - base) / h : 0;  // offsets past the arrays: write nothing
     const int lim = w < kCoop ? w : kCoop;
     for (int t = 0; t < lim; ++t) {
       const long long o = (long long)base + (long long)t * h + j;
@@ -629,11 +653,11 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
 
 cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
                                 const float* value, const void* scratch, const int* secPtr,
-                                int* sellCol, float* sellVal, cudaStream_t s) {
+                                int slots, int* sellCol, float* sellVal, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const int* inv = static_cast<const int*>(scratch) + 3LL * R;  // row_sort's layout
   k_sell_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
-      R, S, rowPtrs, colIdx, value, inv, secPtr, sellCol, sellVal);
+      R, S, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
   note_launches(1);
   return cudaGetLastError();
 }

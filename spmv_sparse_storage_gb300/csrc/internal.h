@@ -121,14 +121,18 @@ constexpr int kSellTailSlots = 64;     // slots per row of one tail work item
 struct SellItem {
   int k, t0, t1, j0;
 };
-size_t sell_scratch_bytes(int R, int maxLen);
+size_t sell_scratch_bytes(int R, int maxLen, long long nsec);
+// secPtr (nsec + 1 entries) by a device scan of the section sizes; the caller
+// guarantees that the total fits in int32
+cudaError_t launch_sell_offsets(int R, int S, int maxLen, long long nsec, const int* rowPtrs,
+                                const int* perm, int* secPtr, void* scratch, cudaStream_t s);
 cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, void* scratch,
                              cudaStream_t s);
 cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const int* perm,
                                int* widths, cudaStream_t s);
 cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
                                 const float* value, const void* scratch, const int* secPtr,
-                                int* sellCol, float* sellVal, cudaStream_t s);
+                                int slots, int* sellCol, float* sellVal, cudaStream_t s);
 
 // spmv_kernels.cu
 // fills hi, flags and mask of every chunk record; runs after the stats pass
@@ -142,7 +146,7 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
                             const float* x, float* y, cudaStream_t s);
 // items: tail work of the sections wider than kSellMainSlots (nItems of them)
-cudaError_t launch_spmv_sell(int R, int S, const int* secPtr, const int* perm,
+cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
                              const int* sellCol, const float* sellVal, const SellItem* items,
                              int nItems, const float* x, float* y, cudaStream_t s);
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,

@@ -773,8 +773,20 @@ __device__ __forceinline__ void sell_rows(const int* __restrict__ col,
   }
 }
 
+// perm[s0 .. s0+n-1] (one 16-byte load when n == 4: s0 is then a multiple of 4)
 template <bool VEC>
-__global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int mainBlocks,
+__device__ __forceinline__ void sell_perm(const int* __restrict__ perm, int s0, int n, int r[4]) {
+  if (VEC && n == 4) {
+    const int4 p = __ldg(reinterpret_cast<const int4*>(perm + s0));
+    r[0] = p.x; r[1] = p.y; r[2] = p.z; r[3] = p.w;
+  } else {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) r[u] = u < n ? __ldg(perm + s0 + u) : 0;
+  }
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, int mainBlocks,
                                                       const int* __restrict__ secPtr,
                                                       const int* __restrict__ perm,
                                                       const int* __restrict__ col,
@@ -784,20 +796,35 @@ __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int mainBloc
                                                       float* __restrict__ y) {
   constexpr int kRows = VEC ? 4 : 1;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  int s0, n;
-  bool atomic;
+  int r[4];
   if ((int)blockIdx.x < mainBlocks) {
     const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (q * kRows >= R) return;
-    s0 = (int)(q * kRows);
+    const int s0 = (int)(q * kRows);
     const int k = s0 / S;
     const int k0 = k * S;
     const int h = min(S, R - k0);
-    const int base = secPtr[k];
-    const int w = (secPtr[k + 1] - base) / h;
-    n = min(kRows, R - s0);
+    const int n = min(kRows, R - s0);
+    // issue the loads that do not depend on each other before the slot loop:
+    // section bounds, the rows' original indices, then their y values
+    const int base = __ldg(secPtr + k);
+    const int end = __ldg(secPtr + k + 1);
+    sell_perm<VEC>(perm, s0, n, r);
+    float y0[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) y0[u] = u < n ? y[r[u]] : 0.f;
+    const int w = end <= slots ? (end - base) / h : 0;  // never past the arrays
     sell_rows<VEC>(col, val, x, base, h, s0 - k0, n, 0, min(w, kSellMainSlots), acc);
-    atomic = w > kSellMainSlots;
+    const bool atomic = w > kSellMainSlots;  // tail items add to these rows too
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (u < n) {
+        if (atomic)
+          atomicAdd(y + r[u], acc[u]);
+        else
+          y[r[u]] = y0[u] + acc[u];
+      }
+    }
   } else {
     const long long id = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
                          (threadIdx.x >> 5);
@@ -807,31 +834,19 @@ __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int mainBloc
     const int h = min(S, R - k0);
     const int j = it.j0 + (threadIdx.x & 31) * kRows;
     if (j >= h) return;
-    n = min(kRows, h - j);
-    sell_rows<VEC>(col, val, x, secPtr[it.k], h, j, n, it.t0, it.t1, acc);
-    s0 = k0 + j;
-    atomic = true;
-  }
-  int r[4];
-  if (VEC && n == 4) {
-    const int4 p = *reinterpret_cast<const int4*>(perm + s0);
-    r[0] = p.x; r[1] = p.y; r[2] = p.z; r[3] = p.w;
-  } else {
+    const int n = min(kRows, h - j);
+    const int base = __ldg(secPtr + it.k);
+    const int end = __ldg(secPtr + it.k + 1);
+    if (end > slots || it.t1 > (end - base) / h) return;  // item beyond its section
+    sell_perm<VEC>(perm, k0 + j, n, r);
+    sell_rows<VEC>(col, val, x, base, h, j, n, it.t0, it.t1, acc);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) r[u] = u < n ? perm[s0 + u] : 0;
-  }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (u < n) {
-      if (atomic)
-        atomicAdd(y + r[u], acc[u]);
-      else
-        y[r[u]] += acc[u];
-    }
+    for (int u = 0; u < 4; ++u)
+      if (u < n) atomicAdd(y + r[u], acc[u]);
   }
 }
 
-cudaError_t launch_spmv_sell(int R, int S, const int* secPtr, const int* perm,
+cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
                              const int* sellCol, const float* sellVal, const SellItem* items,
                              int nItems, const float* x, float* y, cudaStream_t s) {
   if (R <= 0 || S <= 0) return cudaSuccess;
@@ -841,10 +856,10 @@ cudaError_t launch_spmv_sell(int R, int S, const int* secPtr, const int* perm,
   const long long tailBlocks = ((long long)nItems + 7) / 8;
   const unsigned grid = (unsigned)(mainBlocks + tailBlocks);
   if (vec)
-    k_spmv_sell<true><<<grid, 256, 0, s>>>(R, S, (int)mainBlocks, secPtr, perm, sellCol, sellVal,
-                                           items, nItems, x, y);
+    k_spmv_sell<true><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm, sellCol,
+                                           sellVal, items, nItems, x, y);
   else
-    k_spmv_sell<false><<<grid, 256, 0, s>>>(R, S, (int)mainBlocks, secPtr, perm, sellCol,
+    k_spmv_sell<false><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm, sellCol,
                                             sellVal, items, nItems, x, y);
   note_launches(1);
   return cudaGetLastError();
