@@ -10,6 +10,11 @@ fp64 in CSR order. Parity status per function:
 * validate, row stats, SpMV (every format), CSR<->COO/ELL/HYB/JDS: pinned by
   the worked examples of Fig. 14.1 and the ELL/JDS figures, dense brute force,
   closed forms, round trips and invariants (``tests/test_oracle_*.py``).
+* ``cg`` (conjugate gradient for A·X + Y = 0): pinned by closed-form
+  eigenpairs of the Dirichlet Laplacian (one-step convergence), finite
+  termination on matrices with few distinct eigenvalues, a dense direct
+  solve, and the monotone decrease of the A-norm error
+  (``tests/test_oracle_cg.py``).
 * ``select``: parity unpinned (the page's comparison operators are stripped);
   only its outcome on the cases the page describes in words is checked.
 """
@@ -46,6 +51,7 @@ _SIGS = {
     "or_csr_to_sell": (_i64, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_sell_to_csr": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_spmv_sell": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_cg_csr": (_i64, [_i64, _p, _p, _p, _p, _p, _i64, C.c_double, _p, _p, _p]),
     "or_select": (C.c_int, [_i64, _i64, _i64]),
     "or_hyb_auto_width": (_i64, [_i64, _p, _i64]),
 }
@@ -287,6 +293,21 @@ class Oracle:
                                 _ptr(sell["col_idx"]), _ptr(sell["value"]), _ptr(rp), _ptr(ci),
                                 _ptr(v))
         return rp, ci, v
+
+    def cg(self, row_ptrs, col_idx, value, Y, X0=None, max_iter=1000, tol=1e-6):
+        """Conjugate gradient for A·X + Y = 0 (A symmetric positive definite).
+        Returns {"x": fp64 X, "iterations", "status" (0 tolerance, 1 max_iter,
+        2 non-positive curvature), "gnorm": |A·X_k + Y| for k = 0..iterations}."""
+        rp, ci, v, y = _i32(row_ptrs), _i32(col_idx), _f32(value), _f32(Y)
+        R = rp.shape[0] - 1
+        x0 = None if X0 is None else _f32(X0)
+        x = np.zeros(max(R, 1), np.float64)
+        gn = np.zeros(int(max_iter) + 1, np.float64)
+        st = np.zeros(1, np.int32)
+        k = self.lib.or_cg_csr(R, _ptr(rp), _ptr(ci), _ptr(v), _ptr(y),
+                               None if x0 is None else _ptr(x0), int(max_iter), float(tol),
+                               _ptr(x), _ptr(gn), _ptr(st))
+        return {"x": x[:R], "iterations": int(k), "status": int(st[0]), "gnorm": gn[:k + 1]}
 
     def spmv_sell(self, sell, x, y0):
         R = sell["num_rows"]

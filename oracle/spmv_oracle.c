@@ -7,6 +7,9 @@
  * includes this file; only the tests, the smoke check and the bench's CPU
  * baseline do. It shares no code, header, table or helper with the CUDA path.
  *
+ * Also: the conjugate-gradient loop that the first page names as the main
+ * user of the SpMV (or_cg_csr, at the end of this file).
+ *
  * Sources (web pages, cited by title and section):
  *   [P1] PMPP notes, "Sparse Matrices and Basic Formats (COO and CSR)":
  *        "Background & SpMV", Fig. 14.1, "COO format and SpMV",
@@ -536,4 +539,89 @@ void or_spmv_sell(int64_t R, int64_t S, const int32_t *perm, const int64_t *secP
             y[perm[s0 + j]] += acc;
         }
     }
+}
+
+/* ---------------------------------------------------------------------------
+ * Conjugate gradient around the SpMV ([P1] "Background & SpMV": for a
+ * positive-definite A the system A·X + Y = 0 is solved iteratively -- take a
+ * guess X, form A·X + Y, stop when it is close to zero, otherwise correct X
+ * along a direction built from the gradient). A·X + Y is the gradient of
+ * f(X) = X'AX/2 + Y'X, so this is the textbook method of Hestenes and
+ * Stiefel (1952) for A X = -Y, written with the gradient g = A·X + Y:
+ *   g_0 = A·X_0 + Y,  d_0 = -g_0
+ *   iteration k:  q = A d_k,  alpha = (g_k'g_k) / (d_k'q)
+ *                 X_{k+1} = X_k + alpha d_k,  g_{k+1} = g_k + alpha q
+ *                 stop when |g_{k+1}| <= tol |Y|
+ *                 beta = (g_{k+1}'g_{k+1}) / (g_k'g_k),  d_{k+1} = -g_{k+1} + beta d_k
+ * fp64 throughout. X (R doubles) gets the last iterate. gnorm, when not NULL
+ * (maxIter + 1 doubles), gets |g_k| for k = 0 .. iterations. *status: 0 =
+ * stopped by the tolerance (or g = 0 exactly), 1 = maxIter reached, 2 = the
+ * curvature d'q was not positive (A not positive definite). Returns the
+ * number of iterations done.
+ * ------------------------------------------------------------------------- */
+static void csr_apply_f64(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
+                          const float *value, const double *v, double *out) {
+    for (int64_t r = 0; r < R; ++r) {
+        double s = 0.0;
+        for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k)
+            s += (double)value[k] * v[colIdx[k]];
+        out[r] = s;
+    }
+}
+
+static double dot_f64(int64_t n, const double *a, const double *b) {
+    double s = 0.0;
+    for (int64_t i = 0; i < n; ++i) s += a[i] * b[i];
+    return s;
+}
+
+int64_t or_cg_csr(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
+                  const float *value, const float *Y, const float *X0, int64_t maxIter,
+                  double tol, double *X, double *gnorm, int32_t *status) {
+    size_t n = (size_t)(R > 0 ? R : 1);
+    double *g = (double *)malloc(sizeof(double) * n);
+    double *d = (double *)malloc(sizeof(double) * n);
+    double *q = (double *)malloc(sizeof(double) * n);
+    for (int64_t i = 0; i < R; ++i) X[i] = X0 ? (double)X0[i] : 0.0;
+    /* g_0 = A·X_0 + Y */
+    csr_apply_f64(R, rowPtrs, colIdx, value, X, g);
+    double yy = 0.0;
+    for (int64_t i = 0; i < R; ++i) {
+        g[i] += (double)Y[i];
+        yy += (double)Y[i] * (double)Y[i];
+        d[i] = -g[i];
+    }
+    double gg = dot_f64(R, g, g);
+    const double stop = tol * sqrt(yy);
+    if (gnorm) gnorm[0] = sqrt(gg);
+    int64_t k = 0;
+    *status = 1;
+    if (sqrt(gg) <= stop || gg == 0.0) *status = 0;
+    while (*status == 1 && k < maxIter) {
+        csr_apply_f64(R, rowPtrs, colIdx, value, d, q);
+        double dq = dot_f64(R, d, q);
+        if (!(dq > 0.0)) {
+            *status = 2;
+            break;
+        }
+        double alpha = gg / dq;
+        for (int64_t i = 0; i < R; ++i) {
+            X[i] += alpha * d[i];
+            g[i] += alpha * q[i];
+        }
+        double ggNew = dot_f64(R, g, g);
+        ++k;
+        if (gnorm) gnorm[k] = sqrt(ggNew);
+        if (sqrt(ggNew) <= stop || ggNew == 0.0) {
+            *status = 0;
+            break;
+        }
+        double beta = ggNew / gg;
+        for (int64_t i = 0; i < R; ++i) d[i] = -g[i] + beta * d[i];
+        gg = ggNew;
+    }
+    free(g);
+    free(d);
+    free(q);
+    return k;
 }

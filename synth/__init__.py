@@ -231,6 +231,42 @@ def random_csr(seed: int, num_rows: int, num_cols: int, *, mean_len: float = 4.0
     return CSRInput(name, num_rows, num_cols, _row_ptrs_from_lengths(lens), col, val, x, y0)
 
 
+def spd_random(seed: int, n: int, pairs_per_row: float = 3.0, name: str = "spd_random"
+               ) -> CSRInput:
+    """Symmetric, strictly diagonally dominant n x n matrix (so symmetric
+    positive definite): about ``pairs_per_row`` random off-diagonal pairs
+    (i, j) / (j, i) per row, both with the same value uniform in [-1, -0.1);
+    a pair drawn twice holds the sum of its draws. Diagonal = 1 + the sum (in
+    float64, then rounded to float32) of the row's |off-diagonal| values.
+    Columns ascending within a row. Draw order: pair rows, pair columns,
+    pair values, x, y0."""
+    rng = np.random.default_rng(seed)
+    m = int(round(pairs_per_row * n))
+    i = rng.integers(0, n, m)
+    j = rng.integers(0, n, m)
+    v = rng.uniform(-1.0, -0.1, m).astype(np.float32)
+    keep = i != j
+    i, j, v = i[keep], j[keep], v[keep]
+    rows = np.concatenate([i, j])
+    cols = np.concatenate([j, i])
+    vals = np.concatenate([v, v]).astype(np.float64)
+    key = rows.astype(np.int64) * n + cols
+    uk, inv = np.unique(key, return_inverse=True)
+    acc = np.zeros(uk.shape[0], np.float64)
+    np.add.at(acc, inv, vals)
+    off_r, off_c = uk // n, uk % n
+    off_v = acc.astype(np.float32)
+    diag = 1.0 + np.bincount(off_r, weights=np.abs(off_v.astype(np.float64)), minlength=n)
+    r_all = np.concatenate([off_r, np.arange(n)])
+    c_all = np.concatenate([off_c, np.arange(n)])
+    v_all = np.concatenate([off_v, diag.astype(np.float32)])
+    order = np.lexsort((c_all, r_all))
+    lens = np.bincount(r_all, minlength=n).astype(np.int64)
+    x, y0 = vectors(rng, n, n)
+    return CSRInput(name, n, n, _row_ptrs_from_lengths(lens), c_all[order].astype(np.int32),
+                    v_all[order].astype(np.float32), x, y0)
+
+
 WORKLOADS = {
     "tiny_uniform": lambda seed=0: uniform_rows("tiny_uniform", 4096, 8, seed),
     "laplace2d": lambda seed=0: laplace2d(2048, seed),

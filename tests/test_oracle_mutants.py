@@ -50,6 +50,12 @@ MUTANTS = {
     "stats_sample_variance": ("*var = R > 0 ? ss / (double)R : 0.0;",
                               "*var = R > 1 ? ss / (double)(R - 1) : 0.0;"),
     "auto_width_strict": ("if (100 * cum >= 99 * R) break;", "if (100 * cum > 99 * R) break;"),
+    "cg_alpha_uses_dd": ("double alpha = gg / dq;", "double alpha = gg / dot_f64(R, d, d);"),
+    "cg_beta_inverted": ("double beta = ggNew / gg;", "double beta = gg / ggNew;"),
+    "cg_gradient_sign": ("            g[i] += alpha * q[i];", "            g[i] -= alpha * q[i];"),
+    "cg_direction_sign": ("d[i] = -g[i] + beta * d[i];", "d[i] = -g[i] - beta * d[i];"),
+    "cg_drops_y": ("        g[i] += (double)Y[i];", "        g[i] += 0.0 * (double)Y[i];"),
+    "cg_no_restart_from_x0": ("X[i] = X0 ? (double)X0[i] : 0.0;", "X[i] = 0.0;"),
     "sell_row_major": ("                    int64_t i = slots + t * h + j;",
                        "                    int64_t i = slots + j * w + t;"),
     "sell_width_from_last_row": ("        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];",
@@ -70,6 +76,13 @@ def _pin_calls():
     import test_oracle_sell as sell
     calls += [(sell.test_fig14_1_sections_of_two, {}), (sell.test_fig14_1_spmv, {})]
     calls += [(sell.test_round_trip_and_padding, {"idx": i, "S": 3}) for i in range(7)]
+    import test_oracle_cg as cg
+    calls += [(cg.test_laplacian_eigenvector_converges_in_one_step, {"m": 7, "p": 2, "q": 5}),
+              (cg.test_finite_termination_distinct_eigenvalues, {}),
+              (cg.test_three_laplacian_modes_three_steps, {}),
+              (cg.test_matches_dense_direct_solve, {"which": "spd"}),
+              (cg.test_a_norm_error_decreases_and_recurrence_matches, {}),
+              (cg.test_starting_guess, {}), (cg.test_degenerate_cases, {})]
     for i in range(7):
         calls += [(pins.test_round_trips_bit_exact, {"idx": i}),
                   (pins.test_layout_invariants, {"idx": i}),
