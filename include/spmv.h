@@ -188,6 +188,38 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void *stream);
  * several thousand entries. */
 int spmv_run(spmv_handle h, spmv_format format, const float *d_x, float *d_y, void *stream);
 
+/* Result of spmv_cg_solve. */
+typedef struct {
+  int32_t iterations;     /* iterations done */
+  int32_t status;         /* 0: |A·X + Y| <= tol*|Y| reached; 1: maxIter iterations done first;
+                             2: stopped because d'Ad <= 0 (A is not positive definite) */
+  double residual_norm;   /* |g| = |A·X + Y| after the last iteration (recurrence value) */
+  double y_norm;          /* |Y| */
+} spmv_cg_info;
+
+/* Solve A·X + Y = 0 for X by conjugate gradients ("Sparse Matrices and
+ * Basic Formats (COO and CSR)", section "Background & SpMV": the iterative
+ * method for positive-definite A that guesses X, forms A·X + Y -- this
+ * library's SpMV -- and corrects X along the gradient). Textbook CG
+ * (Hestenes-Stiefel) in gradient form: g = A·X + Y, d = -g; per iteration
+ * q = A d, alpha = g'g/d'q, X += alpha d, g += alpha q, stop when
+ * |g| <= tol*|Y|, beta = g'g(new)/g'g(old), d = -g + beta d.
+ *   A must be square (numRows == numCols) and symmetric positive definite
+ *   (symmetry is not checked; a non-positive curvature stops with status 2).
+ *   format: any converted format or SPMV_AUTO; SPMV_ELL runs a fused
+ *   q = A d + d'q kernel, the others their spmv_run kernel plus a dot.
+ *   d_y: numRows floats (Y, read only); d_x: numRows floats, the starting
+ *   guess on entry and the solution on return; x and y must not overlap.
+ *   maxIter >= 0, tol >= 0 (tol = 0: run maxIter iterations unless g
+ *   becomes exactly 0). fp32 vectors; inner products summed in fp32 within
+ *   a block and fp64 across blocks.
+ *   Allocates 3*numRows floats of work from the library pool for the call.
+ *   SYNCHRONISES `stream`: after 1, 2, 4, ..., 64 iterations, then every
+ *   64, and at the end, to read the device's stop decision into *info.
+ * Returns SPMV_ERR_NOT_CONVERTED for a format not converted yet. */
+int spmv_cg_solve(spmv_handle h, spmv_format format, const float *d_y, float *d_x,
+                  int32_t maxIter, double tol, spmv_cg_info *info, void *stream);
+
 /* Format choice from the row-length statistics ("[CUDA performance tuning]
  * SpMV storage format selection and performance comparison", section 4.3;
  * its comparison operators are lost in the page, the reading is):

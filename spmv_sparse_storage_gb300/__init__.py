@@ -59,6 +59,11 @@ class spmv_arrays(C.Structure):
                 ("section_rows", C.c_int32)]
 
 
+class spmv_cg_info(C.Structure):
+    _fields_ = [("iterations", C.c_int32), ("status", C.c_int32),
+                ("residual_norm", C.c_double), ("y_norm", C.c_double)]
+
+
 _H = C.c_void_p
 _P = C.c_void_p
 _SIGS = {
@@ -69,6 +74,8 @@ _SIGS = {
     "spmv_convert_jds": (C.c_int, [_H, _P]),
     "spmv_convert_sell": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_run": (C.c_int, [_H, C.c_int, _P, _P, _P]),
+    "spmv_cg_solve": (C.c_int, [_H, C.c_int, _P, _P, C.c_int32, C.c_double,
+                                C.POINTER(spmv_cg_info), _P]),
     "spmv_select": (C.c_int, [_H, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
     "spmv_get_stats": (C.c_int, [_H, C.POINTER(spmv_stats)]),
     "spmv_export": (C.c_int, [_H, C.c_int, C.POINTER(spmv_arrays)]),
@@ -158,6 +165,15 @@ def spmv_convert_sell(h, section_rows=0, stream=None):
 def spmv_run(h, fmt, x, y, stream=None):
     """y <- A x + y in the given format (name or code)."""
     _check(_lib.spmv_run(h, _fmt(fmt), _ptr(x), _ptr(y), _stream(stream)), "spmv_run")
+
+
+def spmv_cg_solve(h, fmt, y, x, max_iter, tol, stream=None):
+    """Solve A·X + Y = 0 by conjugate gradients; ``x`` holds the starting
+    guess and receives the solution. Returns the spmv_cg_info fields."""
+    info = spmv_cg_info()
+    _check(_lib.spmv_cg_solve(h, _fmt(fmt), _ptr(y), _ptr(x), int(max_iter), float(tol),
+                              C.byref(info), _stream(stream)), "spmv_cg_solve")
+    return {name: getattr(info, name) for name, _ in spmv_cg_info._fields_}
 
 
 def spmv_select(h):
@@ -300,6 +316,9 @@ class SparseMatrix:
 
     def run(self, fmt, x, y, stream=None):
         spmv_run(self.handle, fmt, x, y, stream)
+
+    def cg_solve(self, fmt, y, x, max_iter=1000, tol=1e-6, stream=None):
+        return spmv_cg_solve(self.handle, fmt, y, x, max_iter, tol, stream)
 
     def select(self):
         return spmv_select(self.handle)

@@ -673,6 +673,23 @@ int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
   return SPMV_OK;
 }
 
+namespace {
+int run_format(spmv_handle h, spmv_format format, const float* d_x, float* d_y,
+               cudaStream_t s);
+
+int converted(const spmv_handle_s* h, spmv_format format) {
+  switch (format) {
+    case SPMV_CSR: return SPMV_OK;
+    case SPMV_COO: return h->hasCoo ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    case SPMV_ELL: return h->hasEll ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    case SPMV_HYB: return h->hasHyb ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    case SPMV_JDS: return h->hasJds ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    case SPMV_SELL: return h->hasSell ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    default: return SPMV_ERR_INVALID_ARG;
+  }
+}
+}  // namespace
+
 int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
   SPMV_TRY(check_handle(h));
   if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
@@ -685,14 +702,7 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
     const char* yb = reinterpret_cast<const char*>(d_y);
     if (xb < yb + (size_t)h->R * 4 && yb < xb + (size_t)h->C * 4) return SPMV_ERR_INVALID_ARG;
   }
-  switch (format) {
-    case SPMV_COO: if (!h->hasCoo) return SPMV_ERR_NOT_CONVERTED; break;
-    case SPMV_ELL: if (!h->hasEll) return SPMV_ERR_NOT_CONVERTED; break;
-    case SPMV_HYB: if (!h->hasHyb) return SPMV_ERR_NOT_CONVERTED; break;
-    case SPMV_JDS: if (!h->hasJds) return SPMV_ERR_NOT_CONVERTED; break;
-    case SPMV_SELL: if (!h->hasSell) return SPMV_ERR_NOT_CONVERTED; break;
-    default: break;
-  }
+  SPMV_TRY(converted(h, format));
   if (h->R == 0) return SPMV_OK;
   DeviceGuard g;
   SPMV_TRY(g.set(h->device));
@@ -700,6 +710,13 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   if (h->C > 0) SPMV_TRY(check_device_ptr(d_x, h->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   h->lastStream = s;
+  return run_format(h, format, d_x, d_y, s);
+}
+
+namespace {
+// y <- A x + y in a converted format; arguments already checked.
+int run_format(spmv_handle h, spmv_format format, const float* d_x, float* d_y,
+               cudaStream_t s) {
   switch (format) {
     case SPMV_CSR:
       return record(spmv::launch_spmv_csr(
@@ -733,6 +750,107 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
     default:
       return SPMV_ERR_INVALID_ARG;
   }
+}
+}  // namespace
+
+namespace {
+// pinned host copy of the CG state, one per host thread
+spmv::CgState* pinned_cg_buffer() {
+  thread_local spmv::CgState* buf = nullptr;
+  if (!buf) {
+    void* p = nullptr;
+    if (cudaMallocHost(&p, sizeof(spmv::CgState)) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    buf = static_cast<spmv::CgState*>(p);
+  }
+  return buf;
+}
+}  // namespace
+
+int spmv_cg_solve(spmv_handle h, spmv_format format, const float* d_y, float* d_x,
+                  int32_t maxIter, double tol, spmv_cg_info* info, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (!info || maxIter < 0 || !(tol >= 0.0)) return SPMV_ERR_INVALID_ARG;
+  if (h->R != h->C) return SPMV_ERR_INVALID_ARG;
+  if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
+  SPMV_TRY(converted(h, format));
+  std::memset(info, 0, sizeof(*info));
+  const long long R = h->R;
+  if (R == 0) return SPMV_OK;
+  if (!d_y || !d_x) return SPMV_ERR_INVALID_ARG;
+  {
+    const char* xb = reinterpret_cast<const char*>(d_x);
+    const char* yb = reinterpret_cast<const char*>(d_y);
+    if (xb < yb + (size_t)R * 4 && yb < xb + (size_t)R * 4) return SPMV_ERR_INVALID_ARG;
+  }
+  DeviceGuard dg;
+  SPMV_TRY(dg.set(h->device));
+  SPMV_TRY(check_device_ptr(d_y, h->device));
+  SPMV_TRY(check_device_ptr(d_x, h->device));
+  spmv::CgState* host = pinned_cg_buffer();
+  if (!host) return SPMV_ERR_ALLOC;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  // work: g, d, q (each padded to 64 floats) and the state
+  const long long pitch = (R + 63) / 64 * 64;
+  std::vector<Buf> tmp;
+  void* work = nullptr;
+  int st = h->alloc(sizeof(float) * 3 * (size_t)pitch + sizeof(spmv::CgState), s, &work, tmp);
+  auto done = [&](int code) {
+    h->release(tmp, s);
+    return code;
+  };
+  if (st != SPMV_OK) return done(st);
+  float* g = static_cast<float*>(work);
+  float* d = g + pitch;
+  float* q = d + pitch;
+  auto* state = reinterpret_cast<spmv::CgState*>(q + pitch);
+  const bool fusedEll = format == SPMV_ELL;
+  st = record(cudaMemsetAsync(state, 0, sizeof(spmv::CgState), s));
+  // g_0 = A·X_0 + Y: the SpMV-and-accumulate itself
+  if (st == SPMV_OK)
+    st = record(cudaMemcpyAsync(g, d_y, sizeof(float) * (size_t)R, cudaMemcpyDeviceToDevice, s));
+  if (st == SPMV_OK) st = run_format(h, format, d_x, g, s);
+  if (st == SPMV_OK) st = record(spmv::launch_cg_start((int)R, g, d_y, d, tol, state, s));
+  auto read_state = [&]() {
+    int e = record(cudaMemcpyAsync(host, state, sizeof(spmv::CgState), cudaMemcpyDeviceToHost, s));
+    if (e == SPMV_OK) e = record(cudaStreamSynchronize(s));
+    return e;
+  };
+  // Iterations are enqueued in batches; the device stops itself at
+  // convergence, the host reads the state between batches (after 1, 2, 4, ...,
+  // 64 iterations, then every 64) so as not to enqueue far past the stop.
+  int enq = 0, nextCheck = 1;
+  if (st == SPMV_OK && maxIter > 0) {
+    st = read_state();
+    if (st == SPMV_OK && host->status != spmv::kCgRunning) nextCheck = -1;
+  }
+  while (st == SPMV_OK && nextCheck > 0 && enq < maxIter) {
+    if (fusedEll) {
+      st = record(spmv::launch_cg_ell_q((int)R, h->ellK, h->ellCol, h->ellVal, d, q, state, s));
+    } else {
+      st = record(cudaMemsetAsync(q, 0, sizeof(float) * (size_t)R, s));
+      if (st == SPMV_OK) st = run_format(h, format, d, q, s);
+      if (st == SPMV_OK) st = record(spmv::launch_cg_dot((int)R, d, q, state, s));
+    }
+    if (st == SPMV_OK) st = record(spmv::launch_cg_update((int)R, d_x, g, d, q, state, s));
+    if (st == SPMV_OK) st = record(spmv::launch_cg_direction((int)R, g, d, state, s));
+    ++enq;
+    if (st == SPMV_OK && (enq == nextCheck || enq == maxIter)) {
+      st = read_state();
+      if (st == SPMV_OK && host->status != spmv::kCgRunning) break;
+      nextCheck = nextCheck < 64 ? nextCheck * 2 : nextCheck + 64;
+    }
+  }
+  if (st == SPMV_OK) st = read_state();
+  if (st != SPMV_OK) return done(st);
+  info->iterations = host->iter;
+  info->status = host->status == spmv::kCgRunning ? spmv::kCgMaxIter : host->status;
+  info->residual_norm = host->gnorm;
+  info->y_norm = host->ynorm;
+  return done(SPMV_OK);
 }
 
 int spmv_get_stats(spmv_handle h, spmv_stats* out) {

@@ -145,6 +145,35 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
                             const float* x, float* y, cudaStream_t s);
+// Conjugate gradient for A·X + Y = 0: device state shared by the kernels of
+// one solve (zeroed before the first). status: kCgRunning until the stop test
+// passes (kCgConverged) or d'Ad <= 0 (kCgBreakdown).
+constexpr int kCgRunning = -1;
+constexpr int kCgConverged = 0;
+constexpr int kCgMaxIter = 1;
+constexpr int kCgBreakdown = 2;
+struct CgState {
+  double acc[2];  // cross-block fp64 sums (cleared by the last block)
+  double gg;      // g'g of the current gradient
+  double alpha, beta;
+  double stop;    // tol * |Y|
+  double gnorm;   // |g| after the last iteration
+  double ynorm;   // |Y|
+  int iter;       // iterations done
+  int status;
+  unsigned ticket;
+  unsigned pad;
+};
+cudaError_t launch_cg_start(int R, const float* g, const float* Y, float* d, double tol,
+                            CgState* st, cudaStream_t s);
+cudaError_t launch_cg_dot(int R, const float* d, const float* q, CgState* st, cudaStream_t s);
+cudaError_t launch_cg_ell_q(int R, int K, const int* ellCol, const float* ellVal, const float* d,
+                            float* q, CgState* st, cudaStream_t s);
+cudaError_t launch_cg_update(int R, float* X, float* g, const float* d, const float* q,
+                             CgState* st, cudaStream_t s);
+cudaError_t launch_cg_direction(int R, const float* g, float* d, const CgState* st,
+                                cudaStream_t s);
+
 // items: tail work of the sections wider than kSellMainSlots (nItems of them)
 cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
                              const int* sellCol, const float* sellVal, const SellItem* items,
