@@ -401,6 +401,83 @@ def run_kernels(args, device):
             "peak_kind": peak_kind, "auto": sel, "kernels": out}
 
 
+def cg_alg_bytes(R, slots):
+    """Algorithmic HBM bytes of one CG iteration on the ELL path: the fused
+    direction + SpMV kernel reads the slots (8 B each), g and d_old (4 B per
+    row each, once) and writes d_new and q (4 B each); the update reads X, g,
+    d_new, q and writes X, g (24 B per row)."""
+    return 8 * slots + (16 + 24) * R
+
+
+def run_cg(args, device):
+    """Conjugate gradient for A·X + Y = 0 on the workload (ELL, tol 0 so that
+    exactly --cg-iters iterations run): iterations per second from CUDA events
+    around spmv_cg_solve on the launching stream (its periodic stop checks
+    included), over --steps solves after --warmup."""
+    import torch
+    import spmv_sparse_storage_gb300 as sp
+    inp = synth.make_workload(args.workload, seed=0)
+    R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
+    stream = torch.cuda.current_stream(device)
+    rp = torch.from_numpy(inp.row_ptrs).to(device)
+    ci = torch.from_numpy(inp.col_idx).to(device)
+    va = torch.from_numpy(inp.value).to(device)
+    Y = torch.from_numpy(inp.y0).to(device)
+    X = torch.zeros(R, dtype=torch.float32, device=device)
+    iters = args.cg_iters
+    peak, peak_kind = load_peaks()
+    with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
+        m.convert("ELL", stream=stream)
+        slots = sp.spmv_export(m.handle, "ELL")["ell_slots"]
+        for _ in range(args.warmup):
+            X.zero_()
+            m.cg_solve("ELL", Y, X, max_iter=iters, tol=0.0, stream=stream)
+        torch.cuda.synchronize(device)
+        clocks = ClockSampler(device.index if device.index is not None else 0)
+        clocks.start()
+        time.sleep(0.3)
+        times = []
+        launches0 = sp.spmv_launch_count()
+        for _ in range(args.steps):
+            X.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            info = m.cg_solve("ELL", Y, X, max_iter=iters, tol=0.0, stream=stream)
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1))
+        launches = (sp.spmv_launch_count() - launches0) // max(1, args.steps)
+        clk = clocks.stop()
+    ms = float(np.median(times))
+    it_s = iters / (ms * 1e-3)
+    b = cg_alg_bytes(R, slots)
+    gbs = b * iters / (ms * 1e-3) / 1e9
+    # CPU oracle: the same solve, a bounded number of iterations on the full matrix
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        orc = oracle.get()
+        n_cpu = 5
+        t = time.perf_counter()
+        orc.cg(inp.row_ptrs, inp.col_idx, inp.value, inp.y0, None, max_iter=n_cpu, tol=0.0)
+        dt = time.perf_counter() - t
+        cpu = {"value": round(n_cpu / dt, 3), "unit": "iterations/s", "cores": 1,
+               "kind": "oracle", "sample": f"{n_cpu} CG iterations on the full {args.workload} "
+                                           "matrix (fp64, 1 thread), one run"}
+    return {"mode": "cg", "metric": "CG iterations/s (A·X + Y = 0, fp32 vectors, ELL)",
+            "value": round(it_s, 1), "unit": "iterations/s", "higher_is_better": True,
+            "workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
+            "iterations_per_solve": iters, "solves": args.steps, "ms_per_solve": round(ms, 4),
+            "us_per_iteration": round(ms * 1e3 / iters, 2), "residual_ratio":
+                round(info["residual_norm"] / max(info["y_norm"], 1e-300), 6),
+            "gpu_launches_per_solve": launches,
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "alg_bytes_per_iteration": b, "traffic": None},
+            "cpu_baseline": cpu, "clocks": clk}
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -507,8 +584,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
-    ap.add_argument("--mode", choices=["step", "kernels"], default="step",
-                    help="step: the whole path (default); kernels: per-format SpMV, cold L2")
+    ap.add_argument("--mode", choices=["step", "kernels", "cg"], default="step",
+                    help="step: the whole path (default); kernels: per-format SpMV, cold L2; "
+                         "cg: conjugate-gradient iterations/s")
+    ap.add_argument("--cg-iters", type=int, default=200)
     ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL")
     ap.add_argument("--reps", type=int, default=50)
     args = ap.parse_args()
@@ -540,9 +619,10 @@ def main():
         spec.loader.exec_module(mod)
         mod.build()
     barrier(world)
-    if args.mode == "kernels":
+    if args.mode in ("kernels", "cg"):
         if rank == 0:
-            print(json.dumps(run_kernels(args, device)), flush=True)
+            fn = run_kernels if args.mode == "kernels" else run_cg
+            print(json.dumps(fn(args, device)), flush=True)
         return
     line = run_ours(args, rank, world, device)
     if rank == 0:

@@ -793,27 +793,34 @@ int spmv_cg_solve(spmv_handle h, spmv_format format, const float* d_y, float* d_
   if (!host) return SPMV_ERR_ALLOC;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   h->lastStream = s;
-  // work: g, d, q (each padded to 64 floats) and the state
+  // work: g, two d buffers, q (each padded to 64 floats), the per-block
+  // partial sums and the state
   const long long pitch = (R + 63) / 64 * 64;
+  const size_t nPart = spmv::cg_partials_floats();
   std::vector<Buf> tmp;
   void* work = nullptr;
-  int st = h->alloc(sizeof(float) * 3 * (size_t)pitch + sizeof(spmv::CgState), s, &work, tmp);
+  int st = h->alloc(sizeof(float) * (4 * (size_t)pitch + nPart) + sizeof(spmv::CgState), s,
+                    &work, tmp);
   auto done = [&](int code) {
     h->release(tmp, s);
     return code;
   };
   if (st != SPMV_OK) return done(st);
   float* g = static_cast<float*>(work);
-  float* d = g + pitch;
-  float* q = d + pitch;
-  auto* state = reinterpret_cast<spmv::CgState*>(q + pitch);
+  float* dBuf[2] = {g + pitch, g + 2 * pitch};
+  float* q = g + 3 * pitch;
+  float* partials = g + 4 * pitch;
+  auto* state = reinterpret_cast<spmv::CgState*>(partials + nPart);
   const bool fusedEll = format == SPMV_ELL;
   st = record(cudaMemsetAsync(state, 0, sizeof(spmv::CgState), s));
+  // both d buffers start at 0: with beta = 0 the first direction is -g
+  if (st == SPMV_OK)
+    st = record(cudaMemsetAsync(dBuf[0], 0, sizeof(float) * 2 * (size_t)pitch, s));
   // g_0 = A·X_0 + Y: the SpMV-and-accumulate itself
   if (st == SPMV_OK)
     st = record(cudaMemcpyAsync(g, d_y, sizeof(float) * (size_t)R, cudaMemcpyDeviceToDevice, s));
   if (st == SPMV_OK) st = run_format(h, format, d_x, g, s);
-  if (st == SPMV_OK) st = record(spmv::launch_cg_start((int)R, g, d_y, d, tol, state, s));
+  if (st == SPMV_OK) st = record(spmv::launch_cg_start((int)R, g, d_y, tol, partials, state, s));
   auto read_state = [&]() {
     int e = record(cudaMemcpyAsync(host, state, sizeof(spmv::CgState), cudaMemcpyDeviceToHost, s));
     if (e == SPMV_OK) e = record(cudaStreamSynchronize(s));
@@ -828,15 +835,20 @@ int spmv_cg_solve(spmv_handle h, spmv_format format, const float* d_y, float* d_
     if (st == SPMV_OK && host->status != spmv::kCgRunning) nextCheck = -1;
   }
   while (st == SPMV_OK && nextCheck > 0 && enq < maxIter) {
+    float* d = dBuf[(enq + 1) & 1];
     if (fusedEll) {
-      st = record(spmv::launch_cg_ell_q((int)R, h->ellK, h->ellCol, h->ellVal, d, q, state, s));
+      // d = -g + beta d_old, q = A d, d'q in one kernel (d_old: the other buffer)
+      st = record(spmv::launch_cg_ell_q((int)R, h->ellK, h->ellCol, h->ellVal, g, dBuf[enq & 1],
+                                        d, q, partials, state, s));
     } else {
-      st = record(cudaMemsetAsync(q, 0, sizeof(float) * (size_t)R, s));
+      d = dBuf[0];
+      st = record(spmv::launch_cg_direction((int)R, g, d, state, s));
+      if (st == SPMV_OK) st = record(cudaMemsetAsync(q, 0, sizeof(float) * (size_t)R, s));
       if (st == SPMV_OK) st = run_format(h, format, d, q, s);
-      if (st == SPMV_OK) st = record(spmv::launch_cg_dot((int)R, d, q, state, s));
+      if (st == SPMV_OK) st = record(spmv::launch_cg_dot((int)R, d, q, partials, state, s));
     }
-    if (st == SPMV_OK) st = record(spmv::launch_cg_update((int)R, d_x, g, d, q, state, s));
-    if (st == SPMV_OK) st = record(spmv::launch_cg_direction((int)R, g, d, state, s));
+    if (st == SPMV_OK)
+      st = record(spmv::launch_cg_update((int)R, d_x, g, d, q, partials, state, s));
     ++enq;
     if (st == SPMV_OK && (enq == nextCheck || enq == maxIter)) {
       st = read_state();

@@ -153,7 +153,6 @@ constexpr int kCgConverged = 0;
 constexpr int kCgMaxIter = 1;
 constexpr int kCgBreakdown = 2;
 struct CgState {
-  double acc[2];  // cross-block fp64 sums (cleared by the last block)
   double gg;      // g'g of the current gradient
   double alpha, beta;
   double stop;    // tol * |Y|
@@ -164,15 +163,21 @@ struct CgState {
   unsigned ticket;
   unsigned pad;
 };
-cudaError_t launch_cg_start(int R, const float* g, const float* Y, float* d, double tol,
+// per-block partial sums of the CG kernels (floats, in the work buffer)
+size_t cg_partials_floats();
+cudaError_t launch_cg_start(int R, const float* g, const float* Y, double tol, float* partials,
                             CgState* st, cudaStream_t s);
-cudaError_t launch_cg_dot(int R, const float* d, const float* q, CgState* st, cudaStream_t s);
-cudaError_t launch_cg_ell_q(int R, int K, const int* ellCol, const float* ellVal, const float* d,
-                            float* q, CgState* st, cudaStream_t s);
-cudaError_t launch_cg_update(int R, float* X, float* g, const float* d, const float* q,
-                             CgState* st, cudaStream_t s);
+// generic format path: d = -g + beta d; (q = A d by spmv); d'q
 cudaError_t launch_cg_direction(int R, const float* g, float* d, const CgState* st,
                                 cudaStream_t s);
+cudaError_t launch_cg_dot(int R, const float* d, const float* q, float* partials, CgState* st,
+                          cudaStream_t s);
+// ELL path: dNew = -g + beta dOld, q = A dNew, dNew'q in one kernel
+cudaError_t launch_cg_ell_q(int R, int K, const int* ellCol, const float* ellVal, const float* g,
+                            const float* dOld, float* dNew, float* q, float* partials,
+                            CgState* st, cudaStream_t s);
+cudaError_t launch_cg_update(int R, float* X, float* g, const float* d, const float* q,
+                             float* partials, CgState* st, cudaStream_t s);
 
 // items: tail work of the sections wider than kSellMainSlots (nItems of them)
 cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
