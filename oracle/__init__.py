@@ -15,6 +15,10 @@ fp64 in CSR order. Parity status per function:
   termination on matrices with few distinct eigenvalues, a dense direct
   solve, and the monotone decrease of the A-norm error
   (``tests/test_oracle_cg.py``).
+* x-blocked list (CSR<->XBLOCK, its SpMV): pinned by hand-worked Fig. 14.1
+  chunkings, reduction to the oracle's COO when one chunk holds every
+  column, dense brute force, round trips and layout invariants
+  (``tests/test_oracle_xblock.py``).
 * ``select``: parity unpinned (the page's comparison operators are stripped);
   only its outcome on the cases the page describes in words is checked.
 """
@@ -51,6 +55,9 @@ _SIGS = {
     "or_csr_to_sell": (_i64, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_sell_to_csr": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_spmv_sell": (None, [_i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_csr_to_xblock": (_i64, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_xblock_to_csr": (None, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_spmv_xblock": (None, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_cg_csr": (_i64, [_i64, _p, _p, _p, _p, _p, _i64, C.c_double, _p, _p, _p]),
     "or_select": (C.c_int, [_i64, _i64, _i64]),
     "or_hyb_auto_width": (_i64, [_i64, _p, _i64]),
@@ -293,6 +300,43 @@ class Oracle:
                                 _ptr(sell["col_idx"]), _ptr(sell["value"]), _ptr(rp), _ptr(ci),
                                 _ptr(v))
         return rp, ci, v
+
+    def csr_to_xblock(self, row_ptrs, col_idx, value, num_cols, chunk_cols):
+        """x-blocked list: {num_rows, chunk_cols, num_chunks, chunk_ptr (int64),
+        row_idx (int32, -1 padding), col16 (uint16 local column), value}."""
+        rp, ci, v = _i32(row_ptrs), _i32(col_idx), _f32(value)
+        R, C, B = rp.shape[0] - 1, int(num_cols), int(chunk_cols)
+        Be = max(B, 1)
+        nch = (C + Be - 1) // Be
+        n = self.lib.or_csr_to_xblock(R, C, B, _ptr(rp), _ptr(ci), _ptr(v), None, None, None,
+                                      None)
+        cp = np.zeros(nch + 1, np.int64)
+        rows = np.zeros(n, np.int32)
+        cols = np.zeros(n, np.uint16)
+        vals = np.zeros(n, np.float32)
+        self.lib.or_csr_to_xblock(R, C, B, _ptr(rp), _ptr(ci), _ptr(v), _ptr(cp), _ptr(rows),
+                                  _ptr(cols), _ptr(vals))
+        return {"num_rows": R, "chunk_cols": Be, "num_chunks": nch, "chunk_ptr": cp,
+                "row_idx": rows, "col16": cols, "value": vals}
+
+    def xblock_to_csr(self, xb):
+        R = xb["num_rows"]
+        Z = int((xb["row_idx"] >= 0).sum())
+        rp = np.zeros(R + 1, np.int32)
+        ci = np.zeros(Z, np.int32)
+        v = np.zeros(Z, np.float32)
+        self.lib.or_xblock_to_csr(R, xb["chunk_cols"], xb["num_chunks"], _ptr(xb["chunk_ptr"]),
+                                  _ptr(xb["row_idx"]), _ptr(xb["col16"]), _ptr(xb["value"]),
+                                  _ptr(rp), _ptr(ci), _ptr(v))
+        return rp, ci, v
+
+    def spmv_xblock(self, xb, x, y0):
+        R = xb["num_rows"]
+        y = np.zeros(max(R, 1), np.float64)
+        self.lib.or_spmv_xblock(R, xb["chunk_cols"], xb["num_chunks"], _ptr(xb["chunk_ptr"]),
+                                _ptr(xb["row_idx"]), _ptr(xb["col16"]), _ptr(xb["value"]),
+                                _ptr(_f32(x)), _ptr(_f32(y0)), _ptr(y))
+        return y[:R]
 
     def cg(self, row_ptrs, col_idx, value, Y, X0=None, max_iter=1000, tol=1e-6):
         """Conjugate gradient for A·X + Y = 0 (A symmetric positive definite).

@@ -625,3 +625,87 @@ int64_t or_cg_csr(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
     free(q);
     return k;
 }
+
+/* ---------------------------------------------------------------------------
+ * x-blocked list ([P4] "Building the problem framework", memory efficiency:
+ * with random columns, split x into chunks and let a thread block handle
+ * only the nonzeros whose columns fall in one chunk, so that the gather stays
+ * local -- "blocking + reordering"). Chunk c covers the columns
+ * [c*B, min(C, (c+1)*B)); its entries are the nonzeros whose column falls in
+ * it, in CSR order (by row, then by position in the row), stored from
+ * chunkPtr[c]: row index, local column col - c*B (16 bits, B <= 65536) and
+ * value. Each chunk is padded to a multiple of 4 entries with (row -1, local
+ * column 0, value +0.0f). Returns the slot count chunkPtr[nChunks]; the
+ * arrays may be NULL to only count.
+ * ------------------------------------------------------------------------- */
+int64_t or_csr_to_xblock(int64_t R, int64_t C, int64_t B, const int32_t *rowPtrs,
+                         const int32_t *colIdx, const float *value, int64_t *chunkPtr,
+                         int32_t *xbRow, uint16_t *xbCol, float *xbVal) {
+    if (B < 1) B = 1;
+    int64_t nch = (C + B - 1) / B;
+    int64_t *cnt = (int64_t *)calloc((size_t)(nch > 0 ? nch : 1), sizeof(int64_t));
+    int64_t *cur = (int64_t *)calloc((size_t)(nch > 0 ? nch : 1), sizeof(int64_t));
+    int64_t Z = R > 0 ? rowPtrs[R] : 0;
+    for (int64_t k = 0; k < Z; ++k) cnt[colIdx[k] / B] += 1;
+    int64_t slots = 0;
+    for (int64_t c = 0; c < nch; ++c) {
+        if (chunkPtr) chunkPtr[c] = slots;
+        cur[c] = slots;
+        slots += (cnt[c] + 3) / 4 * 4;
+    }
+    if (chunkPtr) chunkPtr[nch] = slots;
+    if (xbRow) {
+        for (int64_t r = 0; r < R; ++r)
+            for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k) {
+                int64_t c = colIdx[k] / B, i = cur[c]++;
+                xbRow[i] = (int32_t)r;
+                xbCol[i] = (uint16_t)(colIdx[k] - c * B);
+                xbVal[i] = value[k];
+            }
+        for (int64_t c = 0; c < nch; ++c)
+            for (int64_t i = cur[c]; i < (cur[c] + 3) / 4 * 4; ++i) {  /* to the padded end */
+                xbRow[i] = -1;
+                xbCol[i] = 0;
+                xbVal[i] = 0.0f;
+            }
+    }
+    free(cnt);
+    free(cur);
+    return slots;
+}
+
+/* x-blocked list -> CSR: each row's entries in chunk order, then in stored
+ * order (the original order when every row's columns ascend). */
+void or_xblock_to_csr(int64_t R, int64_t B, int64_t nch, const int64_t *chunkPtr,
+                      const int32_t *xbRow, const uint16_t *xbCol, const float *xbVal,
+                      int32_t *rowPtrs, int32_t *colIdx, float *value) {
+    if (B < 1) B = 1;
+    int64_t slots = chunkPtr[nch];
+    for (int64_t r = 0; r <= R; ++r) rowPtrs[r] = 0;
+    for (int64_t i = 0; i < slots; ++i)
+        if (xbRow[i] >= 0) rowPtrs[xbRow[i] + 1] += 1;
+    for (int64_t r = 0; r < R; ++r) rowPtrs[r + 1] += rowPtrs[r];
+    int64_t *pos = (int64_t *)malloc(sizeof(int64_t) * (size_t)(R > 0 ? R : 1));
+    for (int64_t r = 0; r < R; ++r) pos[r] = rowPtrs[r];
+    for (int64_t c = 0; c < nch; ++c)
+        for (int64_t i = chunkPtr[c]; i < chunkPtr[c + 1]; ++i) {
+            if (xbRow[i] < 0) continue;
+            int64_t k = pos[xbRow[i]]++;
+            colIdx[k] = (int32_t)(c * B + xbCol[i]);
+            value[k] = xbVal[i];
+        }
+    free(pos);
+}
+
+/* SpMV over the x-blocked list: every non-padding entry adds val*x[c*B +
+ * local column] to its row, rows summed in fp64 in storage order. */
+void or_spmv_xblock(int64_t R, int64_t B, int64_t nch, const int64_t *chunkPtr,
+                    const int32_t *xbRow, const uint16_t *xbCol, const float *xbVal,
+                    const float *x, const float *y0, double *y) {
+    if (B < 1) B = 1;
+    for (int64_t r = 0; r < R; ++r) y[r] = (double)y0[r];
+    for (int64_t c = 0; c < nch; ++c)
+        for (int64_t i = chunkPtr[c]; i < chunkPtr[c + 1]; ++i)
+            if (xbRow[i] >= 0)
+                y[xbRow[i]] += (double)xbVal[i] * (double)x[c * B + xbCol[i]];
+}

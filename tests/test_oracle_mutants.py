@@ -56,6 +56,12 @@ MUTANTS = {
     "cg_direction_sign": ("d[i] = -g[i] + beta * d[i];", "d[i] = -g[i] - beta * d[i];"),
     "cg_drops_y": ("        g[i] += (double)Y[i];", "        g[i] += 0.0 * (double)Y[i];"),
     "cg_no_restart_from_x0": ("X[i] = X0 ? (double)X0[i] : 0.0;", "X[i] = 0.0;"),
+    "xblock_global_column": ("xbCol[i] = (uint16_t)(colIdx[k] - c * B);",
+                             "xbCol[i] = (uint16_t)(colIdx[k]);"),
+    "xblock_no_padding": ("slots += (cnt[c] + 3) / 4 * 4;", "slots += cnt[c];"),
+    "xblock_rows_reversed": ("    if (xbRow) {\n        for (int64_t r = 0; r < R; ++r)",
+                             "    if (xbRow) {\n        for (int64_t r = R - 1; r >= 0; --r)"),
+    "xblock_spmv_drops_chunk_base": ("(double)x[c * B + xbCol[i]]", "(double)x[xbCol[i]]"),
     "sell_row_major": ("                    int64_t i = slots + t * h + j;",
                        "                    int64_t i = slots + j * w + t;"),
     "sell_width_from_last_row": ("        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];",
@@ -76,6 +82,11 @@ def _pin_calls():
     import test_oracle_sell as sell
     calls += [(sell.test_fig14_1_sections_of_two, {}), (sell.test_fig14_1_spmv, {})]
     calls += [(sell.test_round_trip_and_padding, {"idx": i, "S": 3}) for i in range(7)]
+    import test_oracle_xblock as xbk
+    calls += [(xbk.test_fig14_1_chunkings, {"case": c}) for c in range(3)]
+    calls += [(xbk.test_single_chunk_is_coo, {"idx": i}) for i in (0, 5, 6)]
+    calls += [(xbk.test_spmv_matches_dense, {"case": c, "B": 7}) for c in (2, 3)]
+    calls += [(xbk.test_round_trip_and_invariants, {"idx": i, "B": 5}) for i in (0, 5, 6)]
     import test_oracle_cg as cg
     calls += [(cg.test_laplacian_eigenvector_converges_in_one_step, {"m": 7, "p": 2, "q": 5}),
               (cg.test_finite_termination_distinct_eigenvalues, {}),
