@@ -393,7 +393,7 @@ def run_kernels(args, device):
             out[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                       "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1),
                       "convert_us": conv_us.get(f)}
-            if f in ("ELL", "HYB", "SELL"):
+            if f in ("ELL", "HYB", "SELL", "XBLOCK"):
                 out[f]["slots"] = sp.spmv_export(m.handle, f)["ell_slots"]
         sel = m.select()
     return {"mode": "kernels", "workload": args.workload, "rows": R, "nnz": Z,
@@ -588,7 +588,7 @@ def main():
                     help="step: the whole path (default); kernels: per-format SpMV, cold L2; "
                          "cg: conjugate-gradient iterations/s")
     ap.add_argument("--cg-iters", type=int, default=200)
-    ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL")
+    ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL,XBLOCK")
     ap.add_argument("--reps", type=int, default=50)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)

@@ -23,6 +23,10 @@
  *   SELL -- same page, same section, the variant it describes: the sorted
  *           rows cut into sections of S rows, each section an ELL padded to
  *           its own longest row (sectioned / sliced ELL).
+ *   XBLOCK -- "Introduction to sparse computing and performance bottleneck
+ *           location", section "Building the problem framework": x split
+ *           into chunks of B columns, the nonzeros grouped by the chunk their
+ *           column falls in, so that one thread block gathers from one chunk.
  *
  * Conventions for every function:
  *   - Every function returns an int status (spmv_status); nothing throws or
@@ -60,7 +64,8 @@ typedef enum {
   SPMV_HYB = 3,
   SPMV_JDS = 4,
   SPMV_AUTO = 5, /* spmv_run: the format spmv_select would choose */
-  SPMV_SELL = 6  /* sectioned ELL over the JDS row order */
+  SPMV_SELL = 6,  /* sectioned ELL over the JDS row order */
+  SPMV_XBLOCK = 7 /* nonzeros grouped by column chunk of x */
 } spmv_format;
 
 typedef enum {
@@ -107,10 +112,10 @@ typedef struct {
   int64_t num_rows, num_cols, nnz;
   int32_t width;            /* ELL and HYB: K (slots per row); JDS: longest row;
                                SELL: width of the widest (first) section */
-  int64_t ell_slots;        /* ELL/HYB: num_rows * width; SELL: total slots */
+  int64_t ell_slots;        /* ELL/HYB: num_rows * width; SELL, XBLOCK: total slots */
   int64_t coo_nnz;          /* COO: nnz; HYB: entries of the COO part */
   const int32_t *row_ptrs;  /* CSR: numRows + 1 (the caller's array) */
-  const int32_t *row_idx;   /* COO: nnz;  HYB: coo_nnz */
+  const int32_t *row_idx;   /* COO: nnz;  HYB: coo_nnz;  XBLOCK: ell_slots (padding = -1) */
   const int32_t *col_idx;   /* CSR/COO: nnz; ELL/HYB/SELL: ell_slots (padding = -1); JDS: nnz */
   const float *value;       /* as col_idx (padding = +0.0f) */
   const int32_t *nnz_per_row;  /* ELL/HYB: entries of each row held in the ELL slots */
@@ -121,6 +126,11 @@ typedef struct {
   const int32_t *sec_ptr;   /* SELL: ceil(numRows/S) + 1 entries, first slot of each
                                section, sec_ptr[last] = ell_slots */
   int32_t section_rows;     /* SELL: S, rows per section (the last may be shorter) */
+  const int32_t *chunk_ptr; /* XBLOCK: num_chunks + 1 entries, first slot of each chunk
+                               (multiples of 4); chunk_ptr[num_chunks] = ell_slots */
+  const uint16_t *col16;    /* XBLOCK: ell_slots local columns (column - chunk * chunk_cols) */
+  int32_t chunk_cols;       /* XBLOCK: B, columns per chunk */
+  int32_t num_chunks;       /* XBLOCK: ceil(numCols / B) */
 } spmv_arrays;
 
 /* Create a handle over a CSR matrix that lives on the current device.
@@ -176,12 +186,27 @@ int spmv_convert_jds(spmv_handle h, void *stream);
  * more entries. */
 int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void *stream);
 
+/* CSR -> XBLOCK ("Introduction to sparse computing and performance bottleneck
+ * location", section "Building the problem framework": split x into chunks
+ * and let a thread block process only the nonzeros whose columns fall in one
+ * chunk, localising the random gather). Chunk c covers columns
+ * [c*B, min(numCols, (c+1)*B)); its entries are the nonzeros with a column
+ * there, in CSR order (by row, then position in the row), from chunk_ptr[c]:
+ * row_idx (int32), col16 = column - c*B (uint16), value; each chunk padded
+ * to a multiple of 4 entries with row -1, col16 0, value +0.0f.
+ *   chunkCols: B in [1, 49152] (the SpMV stages B floats of x in shared
+ *   memory), 0 picks 49152; else SPMV_ERR_INVALID_ARG. More than 65536
+ *   chunks, or nnz + 3*chunks above INT32_MAX: SPMV_ERR_TOO_LARGE.
+ *   Asynchronous. The slot count stays on the device; spmv_export of XBLOCK
+ *   reads it (one synchronisation, the first time). */
+int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void *stream);
+
 /* y <- A*x + y with the given format (SPMV_AUTO = spmv_select's choice).
  * d_x: numCols floats, d_y: numRows floats, both on the handle's device;
  * x and y must not overlap (SPMV_ERR_INVALID_ARG). The format must have been
  * converted (SPMV_CSR always is), else SPMV_ERR_NOT_CONVERTED; nothing is
  * converted implicitly. Asynchronous on `stream`; launches 1 kernel
- * (CSR, COO, ELL, JDS, SELL) or 2 (HYB: ELL part, then the COO part with a
+ * (CSR, COO, ELL, JDS, SELL, XBLOCK) or 2 (HYB: ELL part, then the COO part with a
  * programmatic dependent launch). Floating-point rounding differs from a
  * sequential sum (tree and atomic reductions); per row the result is within
  * 1e-5 * (sum_j |a_ij x_j| + |y_i|) of the exact value for rows up to

@@ -24,9 +24,9 @@ if not os.path.exists(LIB_PATH):
 _lib = C.CDLL(LIB_PATH)
 
 # --- enums -----------------------------------------------------------------
-SPMV_COO, SPMV_CSR, SPMV_ELL, SPMV_HYB, SPMV_JDS, SPMV_AUTO, SPMV_SELL = range(7)
+SPMV_COO, SPMV_CSR, SPMV_ELL, SPMV_HYB, SPMV_JDS, SPMV_AUTO, SPMV_SELL, SPMV_XBLOCK = range(8)
 FORMATS = {"COO": SPMV_COO, "CSR": SPMV_CSR, "ELL": SPMV_ELL, "HYB": SPMV_HYB,
-           "JDS": SPMV_JDS, "AUTO": SPMV_AUTO, "SELL": SPMV_SELL}
+           "JDS": SPMV_JDS, "AUTO": SPMV_AUTO, "SELL": SPMV_SELL, "XBLOCK": SPMV_XBLOCK}
 FORMAT_NAMES = {v: k for k, v in FORMATS.items()}
 
 SPMV_OK = 0
@@ -56,7 +56,8 @@ class spmv_arrays(C.Structure):
                 ("col_idx", C.c_void_p), ("value", C.c_void_p), ("nnz_per_row", C.c_void_p),
                 ("coo_col_idx", C.c_void_p), ("coo_value", C.c_void_p), ("perm", C.c_void_p),
                 ("iter_ptr", C.c_void_p), ("sec_ptr", C.c_void_p),
-                ("section_rows", C.c_int32)]
+                ("section_rows", C.c_int32), ("chunk_ptr", C.c_void_p), ("col16", C.c_void_p),
+                ("chunk_cols", C.c_int32), ("num_chunks", C.c_int32)]
 
 
 class spmv_cg_info(C.Structure):
@@ -73,6 +74,7 @@ _SIGS = {
     "spmv_convert_hyb": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_convert_jds": (C.c_int, [_H, _P]),
     "spmv_convert_sell": (C.c_int, [_H, C.c_int32, _P]),
+    "spmv_convert_xblock": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_run": (C.c_int, [_H, C.c_int, _P, _P, _P]),
     "spmv_cg_solve": (C.c_int, [_H, C.c_int, _P, _P, C.c_int32, C.c_double,
                                 C.POINTER(spmv_cg_info), _P]),
@@ -162,6 +164,10 @@ def spmv_convert_sell(h, section_rows=0, stream=None):
     _check(_lib.spmv_convert_sell(h, section_rows, _stream(stream)), "spmv_convert_sell")
 
 
+def spmv_convert_xblock(h, chunk_cols=0, stream=None):
+    _check(_lib.spmv_convert_xblock(h, chunk_cols, _stream(stream)), "spmv_convert_xblock")
+
+
 def spmv_run(h, fmt, x, y, stream=None):
     """y <- A x + y in the given format (name or code)."""
     _check(_lib.spmv_run(h, _fmt(fmt), _ptr(x), _ptr(y), _stream(stream)), "spmv_run")
@@ -248,7 +254,7 @@ def device_view(ptr, n, dtype):
     valid while the owning handle and format live)."""
     if n == 0 or not ptr:
         return torch.empty(0, dtype=dtype, device="cuda")
-    typestr = {torch.int32: "<i4", torch.float32: "<f4"}[dtype]
+    typestr = {torch.int32: "<i4", torch.float32: "<f4", torch.int16: "<i2"}[dtype]
     return torch.as_tensor(_DeviceView(ptr, n, typestr), device="cuda")
 
 
@@ -281,6 +287,13 @@ def export_tensors(h, fmt):
     elif f == "JDS":
         out.update(perm=get(a["perm"], R, i32), iter_ptr=get(a["iter_ptr"], a["width"] + 1, i32),
                    col_idx=get(a["col_idx"], Z, i32), value=get(a["value"], Z, f32))
+    elif f == "XBLOCK":
+        n, nch = a["ell_slots"], a["num_chunks"]
+        out.update(chunk_cols=a["chunk_cols"], num_chunks=nch,
+                   chunk_ptr=get(a["chunk_ptr"], nch + 1, i32),
+                   row_idx=get(a["row_idx"], n, i32),
+                   col16=get(a["col16"], n, torch.int16).view("u2"),
+                   value=get(a["value"], n, f32))
     elif f == "SELL":
         S, n = a["section_rows"], a["ell_slots"]
         out.update(section_rows=S, perm=get(a["perm"], R, i32),
@@ -299,7 +312,7 @@ class SparseMatrix:
         self.handle = spmv_create_csr(self.num_rows, self.num_cols, self.nnz, row_ptrs, col_idx,
                                       value, stream)
 
-    def convert(self, fmt, ell_width=0, stream=None, section_rows=0):
+    def convert(self, fmt, ell_width=0, stream=None, section_rows=0, chunk_cols=0):
         f = FORMAT_NAMES[_fmt(fmt)]
         if f == "COO":
             spmv_convert_coo(self.handle, stream)
@@ -311,6 +324,8 @@ class SparseMatrix:
             spmv_convert_jds(self.handle, stream)
         elif f == "SELL":
             spmv_convert_sell(self.handle, section_rows, stream)
+        elif f == "XBLOCK":
+            spmv_convert_xblock(self.handle, chunk_cols, stream)
         elif f != "CSR":
             raise ValueError(f"cannot convert to {f}")
 

@@ -208,6 +208,17 @@ struct spmv_handle_s {
   spmv::SellItem* sellItems = nullptr;
   std::vector<Buf> sellBufs;
 
+  // XBLOCK (nonzeros grouped by column chunk of x)
+  bool hasXb = false;
+  int xbB = 0;
+  int xbNch = 0;
+  long long xbSlots = -1;  // read from the device on first export
+  int* xbChunkPtr = nullptr;
+  int* xbRow = nullptr;
+  unsigned short* xbCol = nullptr;
+  float* xbVal = nullptr;
+  std::vector<Buf> xbBufs;
+
   int alloc(size_t bytes, cudaStream_t s, void** out, std::vector<Buf>& list) {
     *out = nullptr;
     if (bytes == 0) return SPMV_OK;
@@ -666,6 +677,53 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
   return SPMV_OK;
 }
 
+int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (chunkCols < 0 || chunkCols > spmv::kXbDefaultChunk) return SPMV_ERR_INVALID_ARG;
+  const int B = chunkCols > 0 ? chunkCols : spmv::kXbDefaultChunk;
+  const long long nch = ((long long)h->C + B - 1) / B;
+  if (nch > spmv::kXbMaxChunks) return SPMV_ERR_TOO_LARGE;
+  const long long bound = (long long)h->Z + 3 * nch;  // slots, padding included
+  if (bound > INT32_MAX) return SPMV_ERR_TOO_LARGE;
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  h->lastStream = s;
+  h->release(h->xbBufs, s);
+  h->hasXb = false;
+  std::vector<Buf> tmp;
+  auto fail = [&](int code) {
+    h->release(tmp, s);
+    h->release(h->xbBufs, s);
+    return code;
+  };
+  int st = alloc_typed(h, nch + 1, s, &h->xbChunkPtr, h->xbBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbRow, h->xbBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbCol, h->xbBufs);
+  if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbVal, h->xbBufs);
+  // row of every nonzero: the COO conversion's array when present
+  const int* rowIdx = h->hasCoo ? h->cooRow : nullptr;
+  if (st == SPMV_OK && !rowIdx && h->Z > 0) {
+    int* tmpRow = nullptr;
+    st = alloc_typed(h, h->Z, s, &tmpRow, tmp);
+    if (st == SPMV_OK)
+      st = record(spmv::launch_expand_rows(h->R, h->Z, h->rowPtrs, h->chunkDesc, tmpRow, s));
+    rowIdx = tmpRow;
+  }
+  void* scratch = nullptr;
+  if (st == SPMV_OK) st = h->alloc(spmv::xb_scratch_bytes(h->Z, (int)nch), s, &scratch, tmp);
+  if (st == SPMV_OK)
+    st = record(spmv::launch_xb_build(h->Z, B, (int)nch, h->colIdx, h->value, rowIdx,
+                                      h->xbChunkPtr, h->xbRow, h->xbCol, h->xbVal, scratch, s));
+  if (st != SPMV_OK) return fail(st);
+  h->release(tmp, s);
+  h->xbB = B;
+  h->xbNch = (int)nch;
+  h->xbSlots = -1;
+  h->hasXb = true;
+  return SPMV_OK;
+}
+
 int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
   SPMV_TRY(check_handle(h));
   if (format) *format = (spmv_format)h->stats.auto_format;
@@ -685,6 +743,7 @@ int converted(const spmv_handle_s* h, spmv_format format) {
     case SPMV_HYB: return h->hasHyb ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
     case SPMV_JDS: return h->hasJds ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
     case SPMV_SELL: return h->hasSell ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
+    case SPMV_XBLOCK: return h->hasXb ? SPMV_OK : SPMV_ERR_NOT_CONVERTED;
     default: return SPMV_ERR_INVALID_ARG;
   }
 }
@@ -693,7 +752,7 @@ int converted(const spmv_handle_s* h, spmv_format format) {
 int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
   SPMV_TRY(check_handle(h));
   if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
-  if (format < SPMV_COO || format > SPMV_SELL || format == SPMV_AUTO)
+  if (format < SPMV_COO || format > SPMV_XBLOCK || format == SPMV_AUTO)
     return SPMV_ERR_INVALID_ARG;
   if (h->R > 0 && !d_y) return SPMV_ERR_INVALID_ARG;
   if (h->C > 0 && !d_x) return SPMV_ERR_INVALID_ARG;
@@ -747,6 +806,9 @@ int run_format(spmv_handle h, spmv_format format, const float* d_x, float* d_y,
       return record(spmv::launch_spmv_sell(h->R, h->sellS, (int)h->sellSlots, h->sellSecPtr,
                                            h->sellPerm, h->sellCol, h->sellVal, h->sellItems,
                                            h->sellNItems, d_x, d_y, s));
+    case SPMV_XBLOCK:
+      return record(spmv::launch_spmv_xb(h->C, h->xbB, h->xbNch, h->xbChunkPtr, h->xbRow,
+                                         h->xbCol, h->xbVal, d_x, d_y, s));
     default:
       return SPMV_ERR_INVALID_ARG;
   }
@@ -931,6 +993,25 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       out->sec_ptr = h->sellSecPtr;
       out->section_rows = h->sellS;
       return SPMV_OK;
+    case SPMV_XBLOCK:
+      if (!h->hasXb) return SPMV_ERR_NOT_CONVERTED;
+      if (h->xbSlots < 0) {  // the slot count lives on the device
+        int n = 0;
+        DeviceGuard g;
+        SPMV_TRY(g.set(h->device));
+        SPMV_TRY(record(cudaMemcpyAsync(&n, h->xbChunkPtr + h->xbNch, sizeof(int),
+                                        cudaMemcpyDeviceToHost, h->lastStream)));
+        SPMV_TRY(record(cudaStreamSynchronize(h->lastStream)));
+        h->xbSlots = n;
+      }
+      out->ell_slots = h->xbSlots;
+      out->row_idx = h->xbRow;
+      out->value = h->xbVal;
+      out->chunk_ptr = h->xbChunkPtr;
+      out->col16 = h->xbCol;
+      out->chunk_cols = h->xbB;
+      out->num_chunks = h->xbNch;
+      return SPMV_OK;
     default:
       return SPMV_ERR_INVALID_ARG;
   }
@@ -947,6 +1028,7 @@ int spmv_destroy(spmv_handle h) {
   h->release(h->hybBufs, s);
   h->release(h->jdsBufs, s);
   h->release(h->sellBufs, s);
+  h->release(h->xbBufs, s);
   delete h;
   return st;
 }

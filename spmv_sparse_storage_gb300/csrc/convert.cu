@@ -229,6 +229,8 @@ constexpr int kSortTile = kSortThreads * kSortRounds;  // rows per tile
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
 
+// Key sources of the radix sort: pass 0 derives (key, item) from the input,
+// later passes read the previous pass's output (keysIn/valsIn).
 struct SortIn {
   // pass 0 reads keys from rowPtrs (items are the rows themselves)
   const int* rowPtrs;
@@ -246,10 +248,28 @@ struct SortIn {
   }
 };
 
+struct ChunkKeyIn {
+  // pass 0: key = column chunk of nonzero i (items are the nonzeros)
+  const int* colIdx;
+  int B;
+  const int* keysIn;
+  const int* valsIn;
+  __device__ void get(long long i, int& key, int& val) const {
+    if (keysIn) {
+      key = keysIn[i];
+      val = valsIn[i];
+    } else {
+      key = colIdx[i] / B;
+      val = (int)i;
+    }
+  }
+};
+
 // Per tile, count keys per digit; hist is digit-major: hist[d * nTiles + tile].
 // All of a thread's keys are loaded before any is counted; equal digits in a
 // warp are counted with one shared atomic (warp match).
-__global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, int shift, int nTiles,
+template <class In>
+__global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int shift, int nTiles,
                                                              int* __restrict__ hist) {
   __shared__ int sCount[kRadix];
   for (int d = threadIdx.x; d < kRadix; d += kSortThreads) sCount[d] = 0;
@@ -285,7 +305,8 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(SortIn in, int R, i
 // round. The last pass also writes the inverse permutation (invOut[row] =
 // sorted position) when invOut is given; keysOut may be null when the sorted
 // keys are not needed.
-__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(SortIn in, int R, int shift, int nTiles,
+template <class In>
+__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, int shift, int nTiles,
                                                                 const int* __restrict__ offs,
                                                                 int* __restrict__ keysOut,
                                                                 int* __restrict__ valsOut,
@@ -457,9 +478,10 @@ size_t jds_sort_scratch_bytes(int R, int maxLen) {
 // with 8-bit digits): perm[s] = row at sorted position s, inv[row] = s. The
 // sorted keys are left in keysB when needKeys (else they are not written).
 // Scratch (int32): keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles+1] scan.
-static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, int* scratch,
-                            bool needKeys, const int** sortedKeys, int** invOut,
-                            int** scanScratchOut, cudaStream_t s) {
+template <class In>
+static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scratch,
+                              bool needKeys, const int** sortedKeys, int** invOut,
+                              int** scanScratchOut, cudaStream_t s) {
   const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
   const long long nh = (long long)kRadix * nTiles;
   int* keysA = scratch;
@@ -481,7 +503,9 @@ static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, in
   const int* vIn = nullptr;
   cudaError_t err = cudaSuccess;
   for (int p = 0; p < passes; ++p) {
-    SortIn in{rowPtrs, maxLen, kIn, vIn};
+    In in = first;
+    in.keysIn = kIn;
+    in.valsIn = vIn;
     const int shift = p * kRadixBits;
     k_radix_hist<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, (int)nTiles, hist);
     note_launches(1);
@@ -498,6 +522,13 @@ static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, in
   }
   *sortedKeys = kIn;
   return cudaGetLastError();
+}
+
+static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, int* scratch,
+                            bool needKeys, const int** sortedKeys, int** invOut,
+                            int** scanScratchOut, cudaStream_t s) {
+  return radix_sort(SortIn{rowPtrs, maxLen, nullptr, nullptr}, R, maxLen, perm, scratch,
+                    needKeys, sortedKeys, invOut, scanScratchOut, s);
 }
 
 cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
@@ -659,6 +690,129 @@ cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* col
   k_sell_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
       R, S, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
   note_launches(1);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// x-blocked list ("Introduction to sparse computing and performance
+// bottleneck location", section "Building the problem framework": split x
+// into chunks, a thread block handles only the nonzeros whose columns fall in
+// one chunk). Chunk c (columns [cB, (c+1)B)) holds its nonzeros in CSR order
+// from chunkPtr[c]: row, 16-bit local column, value; padded to 4 entries.
+// Build: per-chunk counts, the unpadded and padded chunk starts (scans), a
+// stable radix sort of the nonzeros by chunk (rank of each nonzero), then a
+// scatter in CSR order and the padding.
+// ---------------------------------------------------------------------------
+constexpr int kXbCountThreads = 256;
+constexpr int kXbSmemBins = 8192;
+
+__global__ void __launch_bounds__(kXbCountThreads) k_xb_count(int Z, int B, int nch,
+                                                              const int* __restrict__ colIdx,
+                                                              int* __restrict__ cnt) {
+  __shared__ int sCnt[kXbSmemBins];
+  const bool local = nch <= kXbSmemBins;
+  if (local) {
+    for (int c = threadIdx.x; c < nch; c += blockDim.x) sCnt[c] = 0;
+    __syncthreads();
+  }
+  for (long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x; k < Z;
+       k += (long long)gridDim.x * blockDim.x) {
+    const int c = colIdx[k] / B;
+    if (local)
+      atomicAdd(&sCnt[c], 1);
+    else
+      atomicAdd(cnt + c, 1);
+  }
+  if (local) {
+    __syncthreads();
+    for (int c = threadIdx.x; c < nch; c += blockDim.x)
+      if (sCnt[c]) atomicAdd(cnt + c, sCnt[c]);
+  }
+}
+
+struct Pad4In {  // chunk sizes rounded up to 4 entries
+  const int* p;
+  __device__ int operator()(long long i) const { return (p[i] + 3) & ~3; }
+};
+
+__global__ void __launch_bounds__(256) k_xb_scatter(int Z, int B, const int* __restrict__ colIdx,
+                                                    const float* __restrict__ value,
+                                                    const int* __restrict__ rowIdx,
+                                                    const int* __restrict__ inv,
+                                                    const int* __restrict__ ustart,
+                                                    const int* __restrict__ chunkPtr,
+                                                    int* __restrict__ xbRow,
+                                                    unsigned short* __restrict__ xbCol,
+                                                    float* __restrict__ xbVal) {
+  const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (k >= Z) return;
+  const int col = colIdx[k];
+  const int c = col / B;
+  const long long p = (long long)chunkPtr[c] + (inv[k] - ustart[c]);
+  xbRow[p] = rowIdx[k];
+  xbCol[p] = (unsigned short)(col - c * B);
+  xbVal[p] = value[k];
+}
+
+__global__ void k_xb_pad(int nch, const int* __restrict__ cnt, const int* __restrict__ chunkPtr,
+                         int* __restrict__ xbRow, unsigned short* __restrict__ xbCol,
+                         float* __restrict__ xbVal) {
+  const long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= nch) return;
+  for (long long i = (long long)chunkPtr[c] + cnt[c]; i < chunkPtr[c + 1]; ++i) {
+    xbRow[i] = -1;
+    xbCol[i] = 0;
+    xbVal[i] = 0.0f;
+  }
+}
+
+size_t xb_scratch_bytes(int Z, int nch) {
+  // cnt[nch], ustart[nch + 1], scan scratch for nch, the sort's item order
+  // perm[Z], then the radix sort's own scratch for Z items
+  const size_t ints = 2 * (size_t)nch + 1 + (size_t)scan_scratch_ints(nch) + (size_t)Z;
+  return ints * sizeof(int) + jds_sort_scratch_bytes(Z, nch > 0 ? nch - 1 : 0);
+}
+
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const float* value,
+                            const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
+                            float* xbVal, void* scratch, cudaStream_t s) {
+  if (nch <= 0) return cudaMemsetAsync(chunkPtr, 0, sizeof(int), s);
+  int* cnt = static_cast<int*>(scratch);
+  int* ustart = cnt + nch;
+  int* scanScratch = ustart + nch + 1;
+  int* sortScratch = scanScratch + scan_scratch_ints(nch);
+  cudaError_t err = cudaMemsetAsync(cnt, 0, sizeof(int) * (size_t)nch, s);
+  if (err != cudaSuccess) return err;
+  if (Z > 0) {
+    long long blocks = ((long long)Z + kXbCountThreads * 16 - 1) / (kXbCountThreads * 16);
+    const long long cap = 8LL * num_sms();
+    k_xb_count<<<(unsigned)(blocks < cap ? blocks : cap), kXbCountThreads, 0, s>>>(Z, B, nch,
+                                                                                 colIdx, cnt);
+    note_launches(1);
+  }
+  err = exclusive_scan(ArrayIn{cnt}, nch, ustart, scanScratch, s);
+  if (err == cudaSuccess) err = exclusive_scan(Pad4In{cnt}, nch, chunkPtr, scanScratch, s);
+  if (err != cudaSuccess || Z <= 0) {
+    if (err == cudaSuccess) {
+      k_xb_pad<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol,
+                                                            xbVal);
+      note_launches(1);
+      err = cudaGetLastError();
+    }
+    return err;
+  }
+  // stable rank of every nonzero among the nonzeros of its chunk
+  int* perm = sortScratch;  // sorted item order (not used beyond the sort)
+  const int* sortedKeys = nullptr;
+  int* inv = nullptr;
+  int* unusedScan = nullptr;
+  err = radix_sort(ChunkKeyIn{colIdx, B, nullptr, nullptr}, Z, nch - 1, perm, sortScratch + Z,
+                   false, &sortedKeys, &inv, &unusedScan, s);
+  if (err != cudaSuccess) return err;
+  k_xb_scatter<<<(unsigned)(((long long)Z + 255) / 256), 256, 0, s>>>(
+      Z, B, colIdx, value, rowIdx, inv, ustart, chunkPtr, xbRow, xbCol, xbVal);
+  k_xb_pad<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol, xbVal);
+  note_launches(2);
   return cudaGetLastError();
 }
 

@@ -145,6 +145,18 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
                             const float* x, float* y, bool dependent, cudaStream_t s);
 cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
                             const float* x, float* y, cudaStream_t s);
+// x-blocked list: nonzeros grouped by column chunk of B columns (CSR order in
+// a chunk), 16-bit local columns, chunks padded to 4 entries (row -1).
+constexpr int kXbDefaultChunk = 49152;  // columns per chunk = floats of x staged per CTA
+constexpr int kXbMaxChunks = 65536;     // chunk ids sorted in at most two radix passes
+size_t xb_scratch_bytes(int Z, int nch);
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const float* value,
+                            const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
+                            float* xbVal, void* scratch, cudaStream_t s);
+cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int* xbRow,
+                           const unsigned short* xbCol, const float* xbVal, const float* x,
+                           float* y, cudaStream_t s);
+
 // Conjugate gradient for A·X + Y = 0: device state shared by the kernels of
 // one solve (zeroed before the first). status: kCgRunning until the stop test
 // passes (kCgConverged) or d'Ad <= 0 (kCgBreakdown).

@@ -865,4 +865,121 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// x-blocked list ("Introduction to sparse computing and performance
+// bottleneck location", section "Building the problem framework": a thread
+// block handles only the nonzeros whose columns fall in one chunk of x, so
+// the gather stays local). Persistent CTAs, one per SM: CTA b takes the b-th
+// nnz-balanced slice of the chunk-ordered list; for every chunk its slice
+// meets it stages that chunk of x (B floats) in shared memory, then its
+// warps walk the slice 128 entries at a time -- lane l holds entries 4l..4l+3
+// (16-byte loads of rows and values, 8 bytes of 16-bit local columns),
+// gathers from shared memory, and the warp adds runs of equal row with the
+// segmented shuffle scan (one atomicAdd per row run; rows ascend inside a
+// chunk, so a warp's reductions fall on a few neighbouring lines of y).
+// ---------------------------------------------------------------------------
+constexpr int kXbThreads = 512;
+
+__global__ void __launch_bounds__(kXbThreads, 1) k_spmv_xb(int C, int B, int nch,
+                                                           const int* __restrict__ chunkPtr,
+                                                           const int* __restrict__ xbRow,
+                                                           const unsigned short* __restrict__ xbCol,
+                                                           const float* __restrict__ xbVal,
+                                                           const float* __restrict__ x,
+                                                           float* __restrict__ y) {
+  extern __shared__ float4 sX4[];
+  float* sX = reinterpret_cast<float*>(sX4);
+  __shared__ int sFirst;
+  const long long groups = (long long)__ldg(chunkPtr + nch) >> 2;  // slots are 4-aligned
+  const long long lo = 4 * (groups * blockIdx.x / gridDim.x);
+  const long long hi = 4 * (groups * (blockIdx.x + 1) / gridDim.x);
+  if (lo >= hi) return;
+  if (threadIdx.x == 0) {  // first chunk that ends after lo
+    int a = 0, b = nch - 1;
+    while (a < b) {
+      const int m = (a + b) >> 1;
+      if (__ldg(chunkPtr + m + 1) > lo) b = m; else a = m + 1;
+    }
+    sFirst = a;
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nWarps = blockDim.x >> 5;
+  for (int c = sFirst; c < nch; ++c) {
+    const long long cs = __ldg(chunkPtr + c);
+    if (cs >= hi) break;
+    const long long s0 = cs > lo ? cs : lo;
+    const long long ce = __ldg(chunkPtr + c + 1);
+    const long long s1 = ce < hi ? ce : hi;
+    if (s0 >= s1) continue;
+    // stage x[cB, cB + n) (the previous chunk's readers are past the barrier)
+    const long long xb = (long long)c * B;
+    const int n = (int)(C - xb < B ? C - xb : B);
+    __syncthreads();
+    const float* xs = x + xb;
+    if ((reinterpret_cast<uintptr_t>(xs) & 15) == 0) {
+      const float4* x4 = reinterpret_cast<const float4*>(xs);
+      for (int i = threadIdx.x; i < (n >> 2); i += blockDim.x) sX4[i] = __ldg(x4 + i);
+      for (int i = (n & ~3) + threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
+    } else {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
+    }
+    __syncthreads();
+    for (long long e0 = s0 + (long long)warp * 128; e0 < s1; e0 += (long long)nWarps * 128) {
+      const long long base = e0 + 4 * lane;  // 4-aligned, so base < s1 means base + 4 <= s1
+      int row[4] = {-1, -1, -1, -1};
+      float p[4] = {0.f, 0.f, 0.f, 0.f};
+      if (base < s1) {
+        const int4 r4 = ld_stream(reinterpret_cast<const int4*>(xbRow + base));
+        const float4 v4 = ld_stream(reinterpret_cast<const float4*>(xbVal + base));
+        const uint2 c2 = __ldcs(reinterpret_cast<const uint2*>(xbCol + base));
+        row[0] = r4.x; row[1] = r4.y; row[2] = r4.z; row[3] = r4.w;
+        // padding (row -1) has local column 0 and value 0: never summed
+        p[0] = r4.x >= 0 ? v4.x * sX[c2.x & 0xffff] : 0.f;
+        p[1] = r4.y >= 0 ? v4.y * sX[c2.x >> 16] : 0.f;
+        p[2] = r4.z >= 0 ? v4.z * sX[c2.y & 0xffff] : 0.f;
+        p[3] = r4.w >= 0 ? v4.w * sX[c2.y >> 16] : 0.f;
+      }
+      warp_segmented_add(row, p, y, false);
+    }
+  }
+}
+
+cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int* xbRow,
+                           const unsigned short* xbCol, const float* xbVal, const float* x,
+                           float* y, cudaStream_t s) {
+  if (nch <= 0) return cudaSuccess;
+  const size_t smem = ((size_t)B * sizeof(float) + 15) / 16 * 16;
+  // per device: the dynamic shared-memory limit raised once, and the blocks
+  // per SM for the last chunk size seen
+  constexpr int kDevs = 64;
+  static bool raised[kDevs] = {};
+  static size_t lastSmem[kDevs] = {};
+  static int lastPerSm[kDevs] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool cache = dev >= 0 && dev < kDevs;
+  if (!cache || !raised[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(k_spmv_xb, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(kXbDefaultChunk * sizeof(float)));
+    if (e != cudaSuccess) return e;
+    if (cache) raised[dev] = true;
+  }
+  int perSm = cache && lastSmem[dev] == smem ? lastPerSm[dev] : 0;
+  if (perSm < 1) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&perSm, k_spmv_xb, kXbThreads, smem) !=
+            cudaSuccess || perSm < 1) {
+      cudaGetLastError();
+      perSm = 1;
+    }
+    if (cache) {
+      lastSmem[dev] = smem;
+      lastPerSm[dev] = perSm;
+    }
+  }
+  k_spmv_xb<<<(unsigned)(perSm * num_sms()), kXbThreads, smem, s>>>(C, B, nch, chunkPtr, xbRow,
+                                                                     xbCol, xbVal, x, y);
+  note_launches(1);
+  return cudaGetLastError();
+}
+
 }  // namespace spmv

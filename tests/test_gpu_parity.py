@@ -16,7 +16,14 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS", "SELL")
+FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK")
+
+
+def xb_fits(C, Z, B):
+    """The library's size rule for XBLOCK: at most 65536 chunks and
+    nnz + 3 * chunks within int32."""
+    nch = (C + B - 1) // B
+    return nch <= 65536 and Z + 3 * nch <= 2**31 - 1
 
 
 def sell_fits(row_ptrs, S):
@@ -57,7 +64,7 @@ def check_tol(y, yref, mag, what):
 
 
 def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, ell_ok=True,
-                 offset=0, sell_rows=(0,)):
+                 offset=0, sell_rows=(0,), xb_chunks=(0,)):
     """Convert `inp` to every format on the GPU, compare the arrays with the
     oracle's conversions and the SpMV results with the oracle's y."""
     rp_t = dev(inp.row_ptrs)
@@ -83,7 +90,8 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
         if R and ost["max_len"] < 4096:
             assert st["auto_hyb_width"] == orc.hyb_auto_width(inp.row_ptrs)
         for f in formats:
-            widths = hyb_widths if f == "HYB" else sell_rows if f == "SELL" else (None,)
+            widths = (hyb_widths if f == "HYB" else sell_rows if f == "SELL" else
+                      xb_chunks if f == "XBLOCK" else (None,))
             for w in widths:
                 if f == "ELL" and not ell_ok:
                     with pytest.raises(sp.SpmvError) as ei:
@@ -98,10 +106,17 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
                         m.run("SELL", x_t, dev(inp.y0))
                     assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
                     continue
+                if f == "XBLOCK" and not xb_fits(inp.num_cols, Z, w or 49152):
+                    with pytest.raises(sp.SpmvError) as ei:
+                        m.convert("XBLOCK", chunk_cols=w)
+                    assert ei.value.code == sp.SPMV_ERR_TOO_LARGE
+                    continue
                 if f == "HYB":
                     m.convert(f, ell_width=w)
                 elif f == "SELL":
                     m.convert(f, section_rows=w)
+                elif f == "XBLOCK":
+                    m.convert(f, chunk_cols=w)
                 else:
                     m.convert(f)
                 if arrays:
@@ -110,7 +125,7 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
                 y_t = dev(inp.y0)
                 m.run(f, x_t, y_t)
                 torch.cuda.synchronize()
-                key = f"{f}{w}" if f in ("HYB", "SELL") else f
+                key = f"{f}{w}" if f in ("HYB", "SELL", "XBLOCK") else f
                 results[key] = check_tol(y_t.cpu().numpy(), yref, mag, f"{inp.name}/{key}")
         if st["auto_format"] in formats and (st["auto_format"] != "ELL" or ell_ok):
             y_t = dev(inp.y0)
@@ -163,6 +178,14 @@ def compare_arrays(orc, inp, f, got, w, st):
         assert same_bits(got["value"], want["value"])
         lens = np.diff(rp)
         assert got["width"] == (int(lens.max()) if lens.size else 0)
+    elif f == "XBLOCK":
+        B = w or 49152
+        want = orc.csr_to_xblock(rp, ci, va, inp.num_cols, B)
+        assert got["chunk_cols"] == B and got["num_chunks"] == want["num_chunks"]
+        assert np.array_equal(got["chunk_ptr"].astype(np.int64), want["chunk_ptr"])
+        assert same_bits(got["row_idx"], want["row_idx"])
+        assert np.array_equal(got["col16"], want["col16"])
+        assert same_bits(got["value"], want["value"])
 
 
 # --- the worked example -------------------------------------------------------
@@ -171,10 +194,11 @@ def test_fig14_1_every_format(sp, orc):
     rp, ci, va = orc.dense_to_csr(synth.fig14_1_dense())
     inp = synth.CSRInput("fig14_1", 4, 4, rp, ci, va, np.array([1, 2, 3, 4], np.float32),
                          np.zeros(4, np.float32))
-    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 2, 3), sell_rows=(0, 1, 2, 3, 4, 100))
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 2, 3), sell_rows=(0, 1, 2, 3, 4, 100),
+                 xb_chunks=(0, 1, 2, 3))
     with sp.SparseMatrix(4, 4, dev(rp), dev(ci), dev(va)) as m:
-        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
-            m.convert(f, ell_width=2, section_rows=2)
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK"):
+            m.convert(f, ell_width=2, section_rows=2, chunk_cols=2)
         for f in FORMATS:
             y = torch.zeros(4, device="cuda")
             m.run(f, dev(inp.x), y)
@@ -190,6 +214,11 @@ def test_fig14_1_every_format(sp, orc):
         assert sell["sec_ptr"].tolist() == [0, 6, 10]
         assert sell["value"].tolist() == [5, 1, 3, 7, 9, 0, 2, 6, 8, 0]
         assert sell["col_idx"].tolist() == [0, 0, 2, 1, 3, -1, 1, 3, 2, -1]
+        xb = m.export("XBLOCK")  # chunks of columns {0, 1} and {2, 3}
+        assert xb["chunk_ptr"].tolist() == [0, 4, 8]
+        assert xb["row_idx"].tolist() == [0, 0, 1, 2, 1, 1, 2, 3]
+        assert xb["col16"].tolist() == [0, 1, 0, 1, 0, 1, 0, 1]
+        assert xb["value"].tolist() == [1, 7, 5, 2, 3, 9, 8, 6]
 
 
 # --- irregular and degenerate matrices -------------------------------------------
@@ -221,7 +250,8 @@ def test_edge_cases(sp, orc, name):
     mx = int(lens.max()) if lens.size else 0
     R, Z = inp.num_rows, inp.nnz
     ell_ok = R * mx <= min(2**31 - 1, 4 * Z + R)
-    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 5), ell_ok=ell_ok, sell_rows=(0, 1, 3, 32))
+    check_matrix(sp, orc, inp, hyb_widths=(0, 1, 5), ell_ok=ell_ok, sell_rows=(0, 1, 3, 32),
+                 xb_chunks=(0, 1, 7, 1000))
 
 
 @pytest.mark.parametrize("offset", [1, 2, 3])
@@ -237,7 +267,7 @@ def test_empty_matrix(sp):
     rp = torch.zeros(1, dtype=torch.int32, device="cuda")
     with sp.SparseMatrix(0, 0, rp, torch.empty(0, dtype=torch.int32, device="cuda"),
                          torch.empty(0, device="cuda")) as m:
-        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK"):
             m.convert(f)
         for f in FORMATS:
             m.run(f, None, None)
@@ -338,7 +368,7 @@ def test_not_converted_and_argument_errors(sp, orc):
     with _fig(sp, orc) as m:
         x = dev(np.array([1, 2, 3, 4], np.float32))
         y = torch.zeros(4, device="cuda")
-        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK"):
             with pytest.raises(sp.SpmvError) as ei:
                 m.run(f, x, y)
             assert ei.value.code == sp.SPMV_ERR_NOT_CONVERTED
@@ -377,6 +407,48 @@ def test_sell_section_heights_and_wide_sections(sp, orc):
     check_matrix(sp, orc, big, formats=("SELL",), sell_rows=(0, 4, 7, 128))
 
 
+def test_xblock_chunkings(sp, orc):
+    """Chunk widths that are and are not multiples of 4 (x staged with 16-byte
+    or scalar loads), numCols not a multiple of B, empty chunks, rows spread
+    over many chunks and CTAs; converted without a COO conversion first (rows
+    expanded on the fly) and after it (the COO row array reused)."""
+    inp = synth.random_csr(51, 20_011, 70_001, mean_len=9, empty_frac=0.05, long_rows=5,
+                           long_len=3000, name="xb_scatter")
+    check_matrix(sp, orc, inp, formats=("XBLOCK",), xb_chunks=(0, 1, 3, 16, 1001, 4096,
+                                                               49152, 49153))
+    check_matrix(sp, orc, inp, formats=("COO", "XBLOCK"), xb_chunks=(5, 777))
+    # columns only in a few chunks: the others are empty
+    band = synth.random_csr(52, 3000, 60_000, mean_len=4, name="xb_narrow")
+    band.col_idx[:] = (band.col_idx % 500) + 20_000
+    for r in range(band.num_rows):  # keep each row's columns distinct and ascending
+        a, b = band.row_ptrs[r], band.row_ptrs[r + 1]
+        band.col_idx[a:b] = np.sort(np.unique(band.col_idx[a:b]).tolist() +
+                                    list(range(30_000, 30_000 + (b - a) -
+                                               np.unique(band.col_idx[a:b]).size)))
+    check_matrix(sp, orc, band, formats=("XBLOCK",), xb_chunks=(0, 64, 4000))
+
+
+def test_xblock_misaligned_x(sp, orc):
+    inp = synth.random_csr(53, 5003, 9001, mean_len=7, name="xb_misaligned")
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
+                         dev(inp.value)) as m:
+        for B in (0, 1000, 1024):
+            m.convert("XBLOCK", chunk_cols=B)
+            for off in (1, 2, 3):
+                xb = dev(np.concatenate([np.zeros(off, np.float32), inp.x]))
+                y = dev(inp.y0)
+                m.run("XBLOCK", xb[off:], y)
+                torch.cuda.synchronize()
+                check_tol(y.cpu().numpy(), yref, mag, f"xblock B={B} x offset {off}")
+        with pytest.raises(sp.SpmvError) as ei:
+            m.convert("XBLOCK", chunk_cols=49153)
+        assert ei.value.code == sp.SPMV_ERR_INVALID_ARG
+        with pytest.raises(sp.SpmvError) as ei:
+            m.convert("XBLOCK", chunk_cols=-1)
+        assert ei.value.code == sp.SPMV_ERR_INVALID_ARG
+
+
 def test_sell_reconvert_and_too_large(sp, orc):
     inp = synth.random_csr(33, 2000, 50_000, mean_len=2, long_rows=1, long_len=40_000)
     yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
@@ -409,7 +481,7 @@ def test_accumulates_and_streams(sp, orc):
     with torch.cuda.stream(s):
         m = sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                             dev(inp.value))
-        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK"):
             m.convert(f)
         for f in FORMATS:
             y = dev(inp.y0)
@@ -428,7 +500,7 @@ def test_guard_bands_untouched(sp, orc):
     sentinel = np.float32(-7.25e33)
     with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                          dev(inp.value)) as m:
-        for f in ("COO", "ELL", "HYB", "JDS", "SELL"):
+        for f in ("COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK"):
             m.convert(f)
         for f in FORMATS:
             buf = torch.full((inp.num_rows + 2 * G,), float(sentinel), device="cuda")
