@@ -362,12 +362,12 @@ def run_kernels(args, device):
         conv_us = {}
         for f in fmts:
             try:
-                m.convert(f, stream=stream)  # warm (pool growth, first launches)
+                m.convert(f, stream=stream, chunk_cols=args.chunk_cols)  # warm (pool, launches)
                 flush.fill_(-1.0)
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                m.convert(f, stream=stream)
+                m.convert(f, stream=stream, chunk_cols=args.chunk_cols)
                 e1.record(stream)
                 e1.synchronize()
                 conv_us[f] = round(e0.elapsed_time(e1) * 1e3, 2)
@@ -588,6 +588,8 @@ def main():
                     help="step: the whole path (default); kernels: per-format SpMV, cold L2; "
                          "cg: conjugate-gradient iterations/s")
     ap.add_argument("--cg-iters", type=int, default=200)
+    ap.add_argument("--chunk-cols", type=int, default=0,
+                    help="XBLOCK chunk width B (0: the library default)")
     ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL,XBLOCK")
     ap.add_argument("--reps", type=int, default=50)
     args = ap.parse_args()

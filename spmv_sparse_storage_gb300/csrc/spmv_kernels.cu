@@ -871,16 +871,22 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
 // block handles only the nonzeros whose columns fall in one chunk of x, so
 // the gather stays local). Persistent CTAs, one per SM: CTA b takes the b-th
 // nnz-balanced slice of the chunk-ordered list; for every chunk its slice
-// meets it stages that chunk of x (B floats) in shared memory, then its
-// warps walk the slice 128 entries at a time -- lane l holds entries 4l..4l+3
-// (16-byte loads of rows and values, 8 bytes of 16-bit local columns),
-// gathers from shared memory, and the warp adds runs of equal row with the
-// segmented shuffle scan (one atomicAdd per row run; rows ascend inside a
-// chunk, so a warp's reductions fall on a few neighbouring lines of y).
+// meets it stages that chunk of x (B floats) in shared memory, then each warp
+// walks the slice kXbUnroll x 32 entries at a time, lane l taking entries l,
+// l + 32, ... (every load coalesced, all of them issued before the first
+// use), gathers from shared memory and adds each product into y with a
+// fire-and-forget atomic. Rows ascend inside a chunk, so the 32 atomics of
+// one instruction fall on a few neighbouring sectors of y, where the L2
+// combines them; summing runs of equal row first would cost more shuffles
+// than it saves.
 // ---------------------------------------------------------------------------
-constexpr int kXbThreads = 512;
+constexpr int kXbUnroll = 8;
 
-__global__ void __launch_bounds__(kXbThreads, 1) k_spmv_xb(int C, int B, int nch,
+// THREADS = 1024 for the widest chunks (one CTA per SM); 512 when the chunk
+// leaves shared memory for two or more CTAs per SM, so that one CTA stages
+// its chunk while the others stream entries.
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 1) k_spmv_xb(int C, int B, int nch,
                                                            const int* __restrict__ chunkPtr,
                                                            const int* __restrict__ xbRow,
                                                            const unsigned short* __restrict__ xbCol,
@@ -904,6 +910,7 @@ __global__ void __launch_bounds__(kXbThreads, 1) k_spmv_xb(int C, int B, int nch
   }
   __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nWarps = blockDim.x >> 5;
+  constexpr int kStep = 32 * kXbUnroll;
   for (int c = sFirst; c < nch; ++c) {
     const long long cs = __ldg(chunkPtr + c);
     if (cs >= hi) break;
@@ -924,22 +931,21 @@ __global__ void __launch_bounds__(kXbThreads, 1) k_spmv_xb(int C, int B, int nch
       for (int i = threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
     }
     __syncthreads();
-    for (long long e0 = s0 + (long long)warp * 128; e0 < s1; e0 += (long long)nWarps * 128) {
-      const long long base = e0 + 4 * lane;  // 4-aligned, so base < s1 means base + 4 <= s1
-      int row[4] = {-1, -1, -1, -1};
-      float p[4] = {0.f, 0.f, 0.f, 0.f};
-      if (base < s1) {
-        const int4 r4 = ld_stream(reinterpret_cast<const int4*>(xbRow + base));
-        const float4 v4 = ld_stream(reinterpret_cast<const float4*>(xbVal + base));
-        const uint2 c2 = __ldcs(reinterpret_cast<const uint2*>(xbCol + base));
-        row[0] = r4.x; row[1] = r4.y; row[2] = r4.z; row[3] = r4.w;
-        // padding (row -1) has local column 0 and value 0: never summed
-        p[0] = r4.x >= 0 ? v4.x * sX[c2.x & 0xffff] : 0.f;
-        p[1] = r4.y >= 0 ? v4.y * sX[c2.x >> 16] : 0.f;
-        p[2] = r4.z >= 0 ? v4.z * sX[c2.y & 0xffff] : 0.f;
-        p[3] = r4.w >= 0 ? v4.w * sX[c2.y >> 16] : 0.f;
+    for (long long e0 = s0 + (long long)warp * kStep; e0 < s1; e0 += (long long)nWarps * kStep) {
+      int row[kXbUnroll];
+      float val[kXbUnroll];
+      int col[kXbUnroll];
+#pragma unroll
+      for (int j = 0; j < kXbUnroll; ++j) {
+        const long long e = e0 + 32 * j + lane;
+        const bool in = e < s1;
+        row[j] = in ? __ldcs(xbRow + e) : -1;
+        val[j] = in ? __ldcs(xbVal + e) : 0.f;
+        col[j] = in ? (int)__ldcs(xbCol + e) : 0;
       }
-      warp_segmented_add(row, p, y, false);
+#pragma unroll
+      for (int j = 0; j < kXbUnroll; ++j)
+        if (row[j] >= 0) atomicAdd(y + row[j], val[j] * sX[col[j]]);  // padding: row -1
     }
   }
 }
@@ -949,35 +955,43 @@ cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int
                            float* y, cudaStream_t s) {
   if (nch <= 0) return cudaSuccess;
   const size_t smem = ((size_t)B * sizeof(float) + 15) / 16 * 16;
-  // per device: the dynamic shared-memory limit raised once, and the blocks
-  // per SM for the last chunk size seen
+  const bool wide = smem > 100 * 1024;  // one CTA per SM
+  // per device and variant: the dynamic shared-memory limit raised once,
+  // and the blocks per SM for the last chunk size seen
   constexpr int kDevs = 64;
-  static bool raised[kDevs] = {};
-  static size_t lastSmem[kDevs] = {};
-  static int lastPerSm[kDevs] = {};
+  static bool raised[2][kDevs] = {};
+  static size_t lastSmem[2][kDevs] = {};
+  static int lastPerSm[2][kDevs] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   const bool cache = dev >= 0 && dev < kDevs;
-  if (!cache || !raised[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(k_spmv_xb, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int v = wide ? 1 : 0;
+  const void* fn = wide ? reinterpret_cast<const void*>(k_spmv_xb<1024>)
+                        : reinterpret_cast<const void*>(k_spmv_xb<512>);
+  const int threads = wide ? 1024 : 512;
+  if (!cache || !raised[v][dev]) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(kXbDefaultChunk * sizeof(float)));
     if (e != cudaSuccess) return e;
-    if (cache) raised[dev] = true;
+    if (cache) raised[v][dev] = true;
   }
-  int perSm = cache && lastSmem[dev] == smem ? lastPerSm[dev] : 0;
+  int perSm = cache && lastSmem[v][dev] == smem ? lastPerSm[v][dev] : 0;
   if (perSm < 1) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&perSm, k_spmv_xb, kXbThreads, smem) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&perSm, fn, threads, smem) !=
             cudaSuccess || perSm < 1) {
       cudaGetLastError();
       perSm = 1;
     }
     if (cache) {
-      lastSmem[dev] = smem;
-      lastPerSm[dev] = perSm;
+      lastSmem[v][dev] = smem;
+      lastPerSm[v][dev] = perSm;
     }
   }
-  k_spmv_xb<<<(unsigned)(perSm * num_sms()), kXbThreads, smem, s>>>(C, B, nch, chunkPtr, xbRow,
-                                                                     xbCol, xbVal, x, y);
+  const unsigned grid = (unsigned)(perSm * num_sms());
+  if (wide)
+    k_spmv_xb<1024><<<grid, 1024, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
+  else
+    k_spmv_xb<512><<<grid, 512, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
