@@ -19,6 +19,10 @@ fp64 in CSR order. Parity status per function:
   chunkings, reduction to the oracle's COO when one chunk holds every
   column, dense brute force, round trips and layout invariants
   (``tests/test_oracle_xblock.py``).
+* ``spmv_csr_f64`` (8-byte values): pinned by exact rational arithmetic
+  (``fractions``), Fig. 14.1, sums that need 8-byte values, and a
+  cancellation that only compensated summation gets right
+  (``tests/test_oracle_f64.py``).
 * ``select``: parity unpinned (the page's comparison operators are stripped);
   only its outcome on the cases the page describes in words is checked.
 """
@@ -58,6 +62,7 @@ _SIGS = {
     "or_csr_to_xblock": (_i64, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_xblock_to_csr": (None, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_spmv_xblock": (None, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
+    "or_spmv_csr_f64": (None, [_i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_cg_csr": (_i64, [_i64, _p, _p, _p, _p, _p, _i64, C.c_double, _p, _p, _p]),
     "or_select": (C.c_int, [_i64, _i64, _i64]),
     "or_hyb_auto_width": (_i64, [_i64, _p, _i64]),
@@ -300,6 +305,20 @@ class Oracle:
                                 _ptr(sell["col_idx"]), _ptr(sell["value"]), _ptr(rp), _ptr(ci),
                                 _ptr(v))
         return rp, ci, v
+
+    def spmv_csr_f64(self, row_ptrs, col_idx, value, x, y0):
+        """y = A x + y0 with 8-byte values and vectors (compensated fp64 sums);
+        returns (y, mag) with mag = |y0| + sum |a x| per row."""
+        rp, ci = _i32(row_ptrs), _i32(col_idx)
+        v = np.ascontiguousarray(value, np.float64)
+        xx = np.ascontiguousarray(x, np.float64)
+        yy = np.ascontiguousarray(y0, np.float64)
+        R = rp.shape[0] - 1
+        y = np.zeros(max(R, 1), np.float64)
+        mag = np.zeros(max(R, 1), np.float64)
+        self.lib.or_spmv_csr_f64(R, _ptr(rp), _ptr(ci), _ptr(v), _ptr(xx), _ptr(yy), _ptr(y),
+                                 _ptr(mag))
+        return y[:R], mag[:R]
 
     def csr_to_xblock(self, row_ptrs, col_idx, value, num_cols, chunk_cols):
         """x-blocked list: {num_rows, chunk_cols, num_chunks, chunk_ptr (int64),

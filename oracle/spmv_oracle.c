@@ -709,3 +709,38 @@ void or_spmv_xblock(int64_t R, int64_t B, int64_t nch, const int64_t *chunkPtr,
             if (xbRow[i] >= 0)
                 y[xbRow[i]] += (double)xbVal[i] * (double)x[c * B + xbCol[i]];
 }
+
+/* ---------------------------------------------------------------------------
+ * SpMV with 8-byte values ([P4] "Building the problem framework": a
+ * nonzero's value and an x entry take 4 or 8 bytes; [P1] "Background &
+ * SpMV": y <- A*x + y). fp64 inputs; every product is split exactly into
+ * p + e (p = a*x rounded, e = fma(a, x, -p)), and the row is summed with
+ * Neumaier's compensated summation, so y_i is within about one rounding of
+ * the exact value whatever the order in which the code under test adds.
+ * mag_i = |y0_i| + sum_k |a_k x_col(k)|.
+ * ------------------------------------------------------------------------- */
+static void neumaier_add(double *s, double *c, double t) {
+    double u = *s + t;
+    if (fabs(*s) >= fabs(t))
+        *c += (*s - u) + t;
+    else
+        *c += (t - u) + *s;
+    *s = u;
+}
+
+void or_spmv_csr_f64(int64_t R, const int32_t *rowPtrs, const int32_t *colIdx,
+                     const double *value, const double *x, const double *y0, double *y,
+                     double *mag) {
+    for (int64_t r = 0; r < R; ++r) {
+        double s = y0[r], c = 0.0, a = fabs(y0[r]);
+        for (int64_t k = rowPtrs[r]; k < rowPtrs[r + 1]; ++k) {
+            double p = value[k] * x[colIdx[k]];
+            double e = fma(value[k], x[colIdx[k]], -p);
+            neumaier_add(&s, &c, p);
+            c += e;
+            a += fabs(p);
+        }
+        y[r] = s + c;
+        if (mag) mag[r] = a;
+    }
+}

@@ -62,6 +62,14 @@ MUTANTS = {
     "xblock_rows_reversed": ("    if (xbRow) {\n        for (int64_t r = 0; r < R; ++r)",
                              "    if (xbRow) {\n        for (int64_t r = R - 1; r >= 0; --r)"),
     "xblock_spmv_drops_chunk_base": ("(double)x[c * B + xbCol[i]]", "(double)x[xbCol[i]]"),
+    "f64_values_as_float": ("            double p = value[k] * x[colIdx[k]];\n"
+                            "            double e = fma(value[k], x[colIdx[k]], -p);",
+                            "            double p = (double)(float)value[k] * x[colIdx[k]];\n"
+                            "            double e = fma((double)(float)value[k], x[colIdx[k]], -p);"),
+    "f64_no_product_error": ("            c += e;", "            c += 0.0 * e;"),
+    "f64_plain_sum": ("            neumaier_add(&s, &c, p);", "            s += p;"),
+    "f64_drops_y0": ("double s = y0[r], c = 0.0, a = fabs(y0[r]);",
+                     "double s = 0.0, c = 0.0, a = fabs(y0[r]);"),
     "sell_row_major": ("                    int64_t i = slots + t * h + j;",
                        "                    int64_t i = slots + j * w + t;"),
     "sell_width_from_last_row": ("        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];",
@@ -87,6 +95,10 @@ def _pin_calls():
     calls += [(xbk.test_single_chunk_is_coo, {"idx": i}) for i in (0, 5, 6)]
     calls += [(xbk.test_spmv_matches_dense, {"case": c, "B": 7}) for c in (2, 3)]
     calls += [(xbk.test_round_trip_and_invariants, {"idx": i, "B": 5}) for i in (0, 5, 6)]
+    import test_oracle_f64 as f64
+    calls += [(f64.test_matches_exact_rationals, {"seed": 0}), (f64.test_fig14_1, {}),
+              (f64.test_needs_eight_byte_values, {}),
+              (f64.test_cancellation_needs_compensation, {})]
     import test_oracle_cg as cg
     calls += [(cg.test_laplacian_eigenvector_converges_in_one_step, {"m": 7, "p": 2, "q": 5}),
               (cg.test_finite_termination_distinct_eigenvalues, {}),
