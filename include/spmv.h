@@ -131,6 +131,9 @@ typedef struct {
   const uint16_t *col16;    /* XBLOCK: ell_slots local columns (column - chunk * chunk_cols) */
   int32_t chunk_cols;       /* XBLOCK: B, columns per chunk */
   int32_t num_chunks;       /* XBLOCK: ceil(numCols / B) */
+  int32_t value_bytes;      /* 4 (handle from spmv_create_csr) or 8 (spmv_create_csr_f64) */
+  const double *value_f64;     /* 8-byte handles: the value array (value is then NULL) */
+  const double *coo_value_f64; /* 8-byte handles: HYB's COO values (coo_value is then NULL) */
 } spmv_arrays;
 
 /* Create a handle over a CSR matrix that lives on the current device.
@@ -146,6 +149,16 @@ typedef struct {
 int spmv_create_csr(spmv_handle *out, int32_t numRows, int32_t numCols, int32_t nnz,
                     const int32_t *d_rowPtrs, const int32_t *d_colIdx,
                     const float *d_value, void *stream);
+
+/* As spmv_create_csr with 8-byte values ("Introduction to sparse computing
+ * and performance bottleneck location", section "Building the problem
+ * framework": a value and an x entry take 4 or 8 bytes). Every conversion
+ * keeps the values in 8 bytes; the handle is run with spmv_run_f64 on
+ * double x and y (spmv_run and spmv_cg_solve answer SPMV_ERR_INVALID_ARG).
+ * XBLOCK chunks hold at most 24576 columns (chunkCols 0 picks 24576). */
+int spmv_create_csr_f64(spmv_handle *out, int32_t numRows, int32_t numCols, int32_t nnz,
+                        const int32_t *d_rowPtrs, const int32_t *d_colIdx,
+                        const double *d_value, void *stream);
 
 /* CSR -> COO ("COO format and SpMV"): expands rowPtrs into rowIdx[nnz]
  * (rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]). colIdx and value are
@@ -194,8 +207,9 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void *stream);
  * there, in CSR order (by row, then position in the row), from chunk_ptr[c]:
  * row_idx (int32), col16 = column - c*B (uint16), value; each chunk padded
  * to a multiple of 4 entries with row -1, col16 0, value +0.0f.
- *   chunkCols: B in [1, 49152] (the SpMV stages B floats of x in shared
- *   memory), 0 picks 49152; else SPMV_ERR_INVALID_ARG. More than 65536
+ *   chunkCols: B in [1, 49152] (the SpMV stages B floats of x in 192 KiB of
+ *   shared memory; [1, 24576] for 8-byte values), 0 picks the largest;
+ *   else SPMV_ERR_INVALID_ARG. More than 65536
  *   chunks, or nnz + 3*chunks above INT32_MAX: SPMV_ERR_TOO_LARGE.
  *   Asynchronous. The slot count stays on the device; spmv_export of XBLOCK
  *   reads it (one synchronisation, the first time). */
@@ -212,6 +226,13 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void *stream);
  * 1e-5 * (sum_j |a_ij x_j| + |y_i|) of the exact value for rows up to
  * several thousand entries. */
 int spmv_run(spmv_handle h, spmv_format format, const float *d_x, float *d_y, void *stream);
+
+/* y <- A*x + y for a handle made by spmv_create_csr_f64: double x (numCols)
+ * and y (numRows), every product and sum in fp64; otherwise as spmv_run
+ * (SPMV_ERR_INVALID_ARG for a 4-byte handle). Per row the result is within
+ * (len + 2) * 2^-52 * (sum_j |a_ij x_j| + |y_i|) of the exact value. */
+int spmv_run_f64(spmv_handle h, spmv_format format, const double *d_x, double *d_y,
+                 void *stream);
 
 /* Result of spmv_cg_solve. */
 typedef struct {

@@ -57,7 +57,9 @@ class spmv_arrays(C.Structure):
                 ("coo_col_idx", C.c_void_p), ("coo_value", C.c_void_p), ("perm", C.c_void_p),
                 ("iter_ptr", C.c_void_p), ("sec_ptr", C.c_void_p),
                 ("section_rows", C.c_int32), ("chunk_ptr", C.c_void_p), ("col16", C.c_void_p),
-                ("chunk_cols", C.c_int32), ("num_chunks", C.c_int32)]
+                ("chunk_cols", C.c_int32), ("num_chunks", C.c_int32),
+                ("value_bytes", C.c_int32), ("value_f64", C.c_void_p),
+                ("coo_value_f64", C.c_void_p)]
 
 
 class spmv_cg_info(C.Structure):
@@ -69,6 +71,8 @@ _H = C.c_void_p
 _P = C.c_void_p
 _SIGS = {
     "spmv_create_csr": (C.c_int, [C.POINTER(_H), C.c_int32, C.c_int32, C.c_int32, _P, _P, _P, _P]),
+    "spmv_create_csr_f64": (C.c_int, [C.POINTER(_H), C.c_int32, C.c_int32, C.c_int32, _P, _P, _P,
+                                      _P]),
     "spmv_convert_coo": (C.c_int, [_H, _P]),
     "spmv_convert_ell": (C.c_int, [_H, _P]),
     "spmv_convert_hyb": (C.c_int, [_H, C.c_int32, _P]),
@@ -76,6 +80,7 @@ _SIGS = {
     "spmv_convert_sell": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_convert_xblock": (C.c_int, [_H, C.c_int32, _P]),
     "spmv_run": (C.c_int, [_H, C.c_int, _P, _P, _P]),
+    "spmv_run_f64": (C.c_int, [_H, C.c_int, _P, _P, _P]),
     "spmv_cg_solve": (C.c_int, [_H, C.c_int, _P, _P, C.c_int32, C.c_double,
                                 C.POINTER(spmv_cg_info), _P]),
     "spmv_select": (C.c_int, [_H, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
@@ -144,6 +149,15 @@ def spmv_create_csr(num_rows, num_cols, nnz, row_ptrs, col_idx, value, stream=No
     return h.value
 
 
+def spmv_create_csr_f64(num_rows, num_cols, nnz, row_ptrs, col_idx, value, stream=None):
+    """As spmv_create_csr with float64 values (a torch.float64 tensor)."""
+    h = _H()
+    _check(_lib.spmv_create_csr_f64(C.byref(h), num_rows, num_cols, nnz, _ptr(row_ptrs),
+                                    _ptr(col_idx), _ptr(value), _stream(stream)),
+           "spmv_create_csr_f64")
+    return h.value
+
+
 def spmv_convert_coo(h, stream=None):
     _check(_lib.spmv_convert_coo(h, _stream(stream)), "spmv_convert_coo")
 
@@ -162,6 +176,11 @@ def spmv_convert_jds(h, stream=None):
 
 def spmv_convert_sell(h, section_rows=0, stream=None):
     _check(_lib.spmv_convert_sell(h, section_rows, _stream(stream)), "spmv_convert_sell")
+
+
+def spmv_run_f64(h, fmt, x, y, stream=None):
+    """y <- A x + y for a float64 handle (x, y float64)."""
+    _check(_lib.spmv_run_f64(h, _fmt(fmt), _ptr(x), _ptr(y), _stream(stream)), "spmv_run_f64")
 
 
 def spmv_convert_xblock(h, chunk_cols=0, stream=None):
@@ -254,7 +273,8 @@ def device_view(ptr, n, dtype):
     valid while the owning handle and format live)."""
     if n == 0 or not ptr:
         return torch.empty(0, dtype=dtype, device="cuda")
-    typestr = {torch.int32: "<i4", torch.float32: "<f4", torch.int16: "<i2"}[dtype]
+    typestr = {torch.int32: "<i4", torch.float32: "<f4", torch.int16: "<i2",
+               torch.float64: "<f8"}[dtype]
     return torch.as_tensor(_DeviceView(ptr, n, typestr), device="cuda")
 
 
@@ -269,6 +289,9 @@ def export_tensors(h, fmt):
 
     f = FORMAT_NAMES[a["format"]]
     out = {"format": f, "num_rows": R, "nnz": Z, "width": a["width"]}
+    if a["value_bytes"] == 8:  # 8-byte values: read the f64 fields under the usual names
+        f32 = torch.float64
+        a["value"], a["coo_value"] = a["value_f64"], a["coo_value_f64"]
     if f == "CSR":
         out.update(row_ptrs=get(a["row_ptrs"], R + 1, i32), col_idx=get(a["col_idx"], Z, i32),
                    value=get(a["value"], Z, f32))
@@ -303,14 +326,17 @@ def export_tensors(h, fmt):
 
 
 class SparseMatrix:
-    """Owns a handle and keeps the borrowed CSR tensors alive until close()."""
+    """Owns a handle and keeps the borrowed CSR tensors alive until close().
+    A float64 ``value`` tensor makes an 8-byte handle (run on float64 x, y)."""
 
     def __init__(self, num_rows, num_cols, row_ptrs, col_idx, value, stream=None):
         self._keep = (row_ptrs, col_idx, value)
         self.num_rows, self.num_cols = int(num_rows), int(num_cols)
         self.nnz = int(col_idx.numel())
-        self.handle = spmv_create_csr(self.num_rows, self.num_cols, self.nnz, row_ptrs, col_idx,
-                                      value, stream)
+        self.f64 = isinstance(value, torch.Tensor) and value.dtype == torch.float64
+        create = spmv_create_csr_f64 if self.f64 else spmv_create_csr
+        self.handle = create(self.num_rows, self.num_cols, self.nnz, row_ptrs, col_idx, value,
+                             stream)
 
     def convert(self, fmt, ell_width=0, stream=None, section_rows=0, chunk_cols=0):
         f = FORMAT_NAMES[_fmt(fmt)]
@@ -330,7 +356,7 @@ class SparseMatrix:
             raise ValueError(f"cannot convert to {f}")
 
     def run(self, fmt, x, y, stream=None):
-        spmv_run(self.handle, fmt, x, y, stream)
+        (spmv_run_f64 if self.f64 else spmv_run)(self.handle, fmt, x, y, stream)
 
     def cg_solve(self, fmt, y, x, max_iter=1000, tol=1e-6, stream=None):
         return spmv_cg_solve(self.handle, fmt, y, x, max_iter, tol, stream)

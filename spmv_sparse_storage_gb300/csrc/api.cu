@@ -6,6 +6,7 @@
 #include <climits>
 #include <cstring>
 #include <mutex>
+#include <type_traits>
 #include <new>
 #include <vector>
 
@@ -149,7 +150,8 @@ struct spmv_handle_s {
   int R = 0, C = 0, Z = 0;
   const int* rowPtrs = nullptr;
   const int* colIdx = nullptr;
-  const float* value = nullptr;
+  const void* value = nullptr;  // float or double (f64)
+  bool f64 = false;             // 8-byte values and vectors
   spmv_stats stats;
   std::vector<unsigned> histExact;  // exact row-length counts for len < kExactLenBins
 
@@ -168,7 +170,7 @@ struct spmv_handle_s {
   bool hasEll = false;
   int ellK = 0;
   int* ellCol = nullptr;
-  float* ellVal = nullptr;
+  void* ellVal = nullptr;
   int* ellNnz = nullptr;
   std::vector<Buf> ellBufs;
 
@@ -177,11 +179,11 @@ struct spmv_handle_s {
   int hybK = 0;
   int hybCooN = 0;
   int* hybCol = nullptr;
-  float* hybVal = nullptr;
+  void* hybVal = nullptr;
   int* hybNnz = nullptr;
   int* hybCooRow = nullptr;
   int* hybCooCol = nullptr;
-  float* hybCooVal = nullptr;
+  void* hybCooVal = nullptr;
   std::vector<Buf> hybBufs;
 
   // JDS
@@ -192,7 +194,7 @@ struct spmv_handle_s {
   int* jdsPerm = nullptr;
   int* jdsIterPtr = nullptr;
   int* jdsCol = nullptr;
-  float* jdsVal = nullptr;
+  void* jdsVal = nullptr;
   std::vector<Buf> jdsBufs;
 
   // SELL (sectioned ELL, the JDS variant)
@@ -204,7 +206,7 @@ struct spmv_handle_s {
   int* sellPerm = nullptr;
   int* sellSecPtr = nullptr;
   int* sellCol = nullptr;
-  float* sellVal = nullptr;
+  void* sellVal = nullptr;
   spmv::SellItem* sellItems = nullptr;
   std::vector<Buf> sellBufs;
 
@@ -216,7 +218,7 @@ struct spmv_handle_s {
   int* xbChunkPtr = nullptr;
   int* xbRow = nullptr;
   unsigned short* xbCol = nullptr;
-  float* xbVal = nullptr;
+  void* xbVal = nullptr;
   std::vector<Buf> xbBufs;
 
   int alloc(size_t bytes, cudaStream_t s, void** out, std::vector<Buf>& list) {
@@ -256,6 +258,26 @@ struct spmv_handle_s {
 };
 
 namespace {
+
+// n values of the handle's value type (4 or 8 bytes)
+int alloc_values(spmv_handle h, long long n, cudaStream_t s, void** out, std::vector<Buf>& list) {
+  return h->alloc((size_t)n * (h->f64 ? sizeof(double) : sizeof(float)), s, out, list);
+}
+
+// Calls f(T{}) with T = the handle's value type; f returns a cudaError_t.
+template <class F>
+cudaError_t with_type(const spmv_handle_s* h, F&& f) {
+  return h->f64 ? f(double{}) : f(float{});
+}
+
+template <class T>
+const T* cval(const void* p) {
+  return static_cast<const T*>(p);
+}
+template <class T>
+T* val(void* p) {
+  return static_cast<T*>(p);
+}
 
 template <class T>
 int alloc_typed(spmv_handle h, long long n, cudaStream_t s, T** out, std::vector<Buf>& list) {
@@ -316,9 +338,10 @@ int check_handle(spmv_handle h) { return h ? SPMV_OK : SPMV_ERR_INVALID_ARG; }
 // ---------------------------------------------------------------------------
 extern "C" {
 
-int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
-                    const int32_t* d_rowPtrs, const int32_t* d_colIdx, const float* d_value,
-                    void* stream) {
+namespace {
+int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
+                const int32_t* d_rowPtrs, const int32_t* d_colIdx, const void* d_value, bool f64,
+                void* stream) {
   if (!out) return SPMV_ERR_INVALID_ARG;
   *out = nullptr;
   if (numRows < 0 || numCols < 0 || nnz < 0 || !d_rowPtrs) return SPMV_ERR_INVALID_ARG;
@@ -341,6 +364,7 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   h->rowPtrs = d_rowPtrs;
   h->colIdx = d_colIdx;
   h->value = d_value;
+  h->f64 = f64;
   h->lastStream = s;
   int st = get_pool(dev, &h->pool);
   std::vector<Buf> tmp;
@@ -416,6 +440,19 @@ int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t 
   *out = h;
   return SPMV_OK;
 }
+}  // namespace
+
+int spmv_create_csr(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
+                    const int32_t* d_rowPtrs, const int32_t* d_colIdx, const float* d_value,
+                    void* stream) {
+  return create_impl(out, numRows, numCols, nnz, d_rowPtrs, d_colIdx, d_value, false, stream);
+}
+
+int spmv_create_csr_f64(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
+                        const int32_t* d_rowPtrs, const int32_t* d_colIdx, const double* d_value,
+                        void* stream) {
+  return create_impl(out, numRows, numCols, nnz, d_rowPtrs, d_colIdx, d_value, true, stream);
+}
 
 int spmv_convert_coo(spmv_handle h, void* stream) {
   SPMV_TRY(check_handle(h));
@@ -443,10 +480,13 @@ int spmv_convert_ell(spmv_handle h, void* stream) {
   h->hasEll = false;
   const long long slots = (long long)h->R * K;
   SPMV_TRY(alloc_typed(h, slots, s, &h->ellCol, h->ellBufs));
-  SPMV_TRY(alloc_typed(h, slots, s, &h->ellVal, h->ellBufs));
+  SPMV_TRY(alloc_values(h, slots, s, &h->ellVal, h->ellBufs));
   SPMV_TRY(alloc_typed(h, h->R, s, &h->ellNnz, h->ellBufs));
-  SPMV_TRY(record(spmv::launch_csr_to_ell(h->R, (int)K, h->rowPtrs, h->colIdx, h->value,
-                                          h->ellCol, h->ellVal, h->ellNnz, s)));
+  SPMV_TRY(record(with_type(h, [&](auto tag) {
+    using T = decltype(tag);
+    return spmv::launch_csr_to_ell<T>(h->R, (int)K, h->rowPtrs, h->colIdx, cval<T>(h->value),
+                                      h->ellCol, val<T>(h->ellVal), h->ellNnz, s);
+  })));
   h->ellK = (int)K;
   h->hasEll = true;
   return SPMV_OK;
@@ -467,10 +507,13 @@ int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void* stream) {
   const long long R = h->R;
   const long long slots = R * K;
   SPMV_TRY(alloc_typed(h, slots, s, &h->hybCol, h->hybBufs));
-  SPMV_TRY(alloc_typed(h, slots, s, &h->hybVal, h->hybBufs));
+  SPMV_TRY(alloc_values(h, slots, s, &h->hybVal, h->hybBufs));
   SPMV_TRY(alloc_typed(h, R, s, &h->hybNnz, h->hybBufs));
-  SPMV_TRY(record(spmv::launch_csr_to_ell(h->R, (int)K, h->rowPtrs, h->colIdx, h->value,
-                                          h->hybCol, h->hybVal, h->hybNnz, s)));
+  SPMV_TRY(record(with_type(h, [&](auto tag) {
+    using T = decltype(tag);
+    return spmv::launch_csr_to_ell<T>(h->R, (int)K, h->rowPtrs, h->colIdx, cval<T>(h->value),
+                                      h->hybCol, val<T>(h->hybVal), h->hybNnz, s);
+  })));
   // COO part size: nnz - sum_r min(len_r, K), exact from the histogram when
   // K is below the exact range (longer rows then all keep K entries).
   long long tail = -1;
@@ -509,10 +552,14 @@ int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void* stream) {
   }
   st = alloc_typed(h, tail, s, &h->hybCooRow, h->hybBufs);
   if (st == SPMV_OK) st = alloc_typed(h, tail, s, &h->hybCooCol, h->hybBufs);
-  if (st == SPMV_OK) st = alloc_typed(h, tail, s, &h->hybCooVal, h->hybBufs);
+  if (st == SPMV_OK) st = alloc_values(h, tail, s, &h->hybCooVal, h->hybBufs);
   if (st == SPMV_OK && tail > 0)
-    st = record(spmv::launch_hyb_tail_copy(h->R, (int)K, h->rowPtrs, h->colIdx, h->value, tailPtr,
-                                           h->hybCooRow, h->hybCooCol, h->hybCooVal, s));
+    st = record(with_type(h, [&](auto tag) {
+      using T = decltype(tag);
+      return spmv::launch_hyb_tail_copy<T>(h->R, (int)K, h->rowPtrs, h->colIdx,
+                                           cval<T>(h->value), tailPtr, h->hybCooRow,
+                                           h->hybCooCol, val<T>(h->hybCooVal), s);
+    }));
   if (st != SPMV_OK) return done(st);
   h->hybK = (int)K;
   h->hybCooN = (int)tail;
@@ -533,7 +580,7 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   SPMV_TRY(alloc_typed(h, (long long)L + 1, s, &h->jdsIterPtr, h->jdsBufs));
   // padded so that the SpMV kernel's aligned 16-byte reads stay inside
   SPMV_TRY(alloc_typed(h, (long long)h->Z + spmv::kJdsPad, s, &h->jdsCol, h->jdsBufs));
-  SPMV_TRY(alloc_typed(h, (long long)h->Z + spmv::kJdsPad, s, &h->jdsVal, h->jdsBufs));
+  SPMV_TRY(alloc_values(h, (long long)h->Z + spmv::kJdsPad, s, &h->jdsVal, h->jdsBufs));
   // iterPtr from the exact length histogram when every row is shorter than
   // kExactLenBins: iterPtr[t+1] = iterPtr[t] + #{rows longer than t}
   std::vector<int> hostIp;
@@ -550,9 +597,12 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   void* scratch = nullptr;
   int st = h->alloc(spmv::jds_sort_scratch_bytes(h->R, L), s, &scratch, tmp);
   if (st == SPMV_OK)
-    st = record(spmv::launch_jds_build(h->R, L, h->rowPtrs, h->colIdx, h->value, h->jdsPerm,
-                                       h->jdsIterPtr, h->jdsCol, h->jdsVal, scratch,
-                                       hostIp.empty() ? nullptr : hostIp.data(), s));
+    st = record(with_type(h, [&](auto tag) {
+      using T = decltype(tag);
+      return spmv::launch_jds_build<T>(h->R, L, h->rowPtrs, h->colIdx, cval<T>(h->value),
+                                       h->jdsPerm, h->jdsIterPtr, h->jdsCol, val<T>(h->jdsVal),
+                                       scratch, hostIp.empty() ? nullptr : hostIp.data(), s);
+    }));
   h->release(tmp, s);
   if (st != SPMV_OK) return st;
   // Row-parallel part: the leading diagonals at least min(kJdsSplitMinWidth,
@@ -641,11 +691,14 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
                                 cudaMemcpyHostToDevice, s));
   }
   if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellCol, h->sellBufs);
-  if (st == SPMV_OK) st = alloc_typed(h, slots, s, &h->sellVal, h->sellBufs);
+  if (st == SPMV_OK) st = alloc_values(h, slots, s, &h->sellVal, h->sellBufs);
   if (st == SPMV_OK && slots > 0)
-    st = record(spmv::launch_sell_scatter(h->R, S, h->rowPtrs, h->colIdx, h->value, scratch,
-                                          h->sellSecPtr, (int)slots, h->sellCol, h->sellVal,
-                                          s));
+    st = record(with_type(h, [&](auto tag) {
+      using T = decltype(tag);
+      return spmv::launch_sell_scatter<T>(h->R, S, h->rowPtrs, h->colIdx, cval<T>(h->value),
+                                          scratch, h->sellSecPtr, (int)slots, h->sellCol,
+                                          val<T>(h->sellVal), s);
+    }));
   if (st != SPMV_OK) return fail(st);
   // tail work items of the sections wider than kSellMainSlots (a prefix)
   std::vector<spmv::SellItem> items;
@@ -679,8 +732,10 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
 
 int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
   SPMV_TRY(check_handle(h));
-  if (chunkCols < 0 || chunkCols > spmv::kXbDefaultChunk) return SPMV_ERR_INVALID_ARG;
-  const int B = chunkCols > 0 ? chunkCols : spmv::kXbDefaultChunk;
+  // the SpMV stages B values of x in kXbSmemBytes of shared memory
+  const int maxB = spmv::kXbSmemBytes / (h->f64 ? (int)sizeof(double) : (int)sizeof(float));
+  if (chunkCols < 0 || chunkCols > maxB) return SPMV_ERR_INVALID_ARG;
+  const int B = chunkCols > 0 ? chunkCols : maxB;
   const long long nch = ((long long)h->C + B - 1) / B;
   if (nch > spmv::kXbMaxChunks) return SPMV_ERR_TOO_LARGE;
   const long long bound = (long long)h->Z + 3 * nch;  // slots, padding included
@@ -700,7 +755,7 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
   int st = alloc_typed(h, nch + 1, s, &h->xbChunkPtr, h->xbBufs);
   if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbRow, h->xbBufs);
   if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbCol, h->xbBufs);
-  if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbVal, h->xbBufs);
+  if (st == SPMV_OK) st = alloc_values(h, bound, s, &h->xbVal, h->xbBufs);
   // row of every nonzero: the COO conversion's array when present
   const int* rowIdx = h->hasCoo ? h->cooRow : nullptr;
   if (st == SPMV_OK && !rowIdx && h->Z > 0) {
@@ -713,8 +768,12 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
   void* scratch = nullptr;
   if (st == SPMV_OK) st = h->alloc(spmv::xb_scratch_bytes(h->Z, (int)nch), s, &scratch, tmp);
   if (st == SPMV_OK)
-    st = record(spmv::launch_xb_build(h->Z, B, (int)nch, h->colIdx, h->value, rowIdx,
-                                      h->xbChunkPtr, h->xbRow, h->xbCol, h->xbVal, scratch, s));
+    st = record(with_type(h, [&](auto tag) {
+      using T = decltype(tag);
+      return spmv::launch_xb_build<T>(h->Z, B, (int)nch, h->colIdx, cval<T>(h->value), rowIdx,
+                                      h->xbChunkPtr, h->xbRow, h->xbCol, val<T>(h->xbVal),
+                                      scratch, s);
+    }));
   if (st != SPMV_OK) return fail(st);
   h->release(tmp, s);
   h->xbB = B;
@@ -731,9 +790,11 @@ int spmv_select(spmv_handle h, spmv_format* format, int32_t* ellWidth) {
   return SPMV_OK;
 }
 
+}  // extern "C"
+
 namespace {
-int run_format(spmv_handle h, spmv_format format, const float* d_x, float* d_y,
-               cudaStream_t s);
+template <class T>
+int run_format(spmv_handle h, spmv_format format, const T* d_x, T* d_y, cudaStream_t s);
 
 int converted(const spmv_handle_s* h, spmv_format format) {
   switch (format) {
@@ -749,8 +810,11 @@ int converted(const spmv_handle_s* h, spmv_format format) {
 }
 }  // namespace
 
-int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
+namespace {
+template <class T>
+int run_impl(spmv_handle h, spmv_format format, const T* d_x, T* d_y, void* stream) {
   SPMV_TRY(check_handle(h));
+  if (h->f64 != std::is_same<T, double>::value) return SPMV_ERR_INVALID_ARG;  // value type
   if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
   if (format < SPMV_COO || format > SPMV_XBLOCK || format == SPMV_AUTO)
     return SPMV_ERR_INVALID_ARG;
@@ -759,7 +823,8 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   if (h->R > 0 && h->C > 0) {
     const char* xb = reinterpret_cast<const char*>(d_x);
     const char* yb = reinterpret_cast<const char*>(d_y);
-    if (xb < yb + (size_t)h->R * 4 && yb < xb + (size_t)h->C * 4) return SPMV_ERR_INVALID_ARG;
+    if (xb < yb + (size_t)h->R * sizeof(T) && yb < xb + (size_t)h->C * sizeof(T))
+      return SPMV_ERR_INVALID_ARG;
   }
   SPMV_TRY(converted(h, format));
   if (h->R == 0) return SPMV_OK;
@@ -769,51 +834,71 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
   if (h->C > 0) SPMV_TRY(check_device_ptr(d_x, h->device));
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   h->lastStream = s;
-  return run_format(h, format, d_x, d_y, s);
+  return run_format<T>(h, format, d_x, d_y, s);
+}
+}  // namespace
+
+extern "C" {
+
+int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, void* stream) {
+  return run_impl<float>(h, format, d_x, d_y, stream);
 }
 
+int spmv_run_f64(spmv_handle h, spmv_format format, const double* d_x, double* d_y,
+                 void* stream) {
+  return run_impl<double>(h, format, d_x, d_y, stream);
+}
+
+}  // extern "C"
+
 namespace {
-// y <- A x + y in a converted format; arguments already checked.
-int run_format(spmv_handle h, spmv_format format, const float* d_x, float* d_y,
-               cudaStream_t s) {
+// y <- A x + y in a converted format; arguments already checked; T is the
+// handle's value type.
+template <class T>
+int run_format(spmv_handle h, spmv_format format, const T* d_x, T* d_y, cudaStream_t s) {
+  const T* value = cval<T>(h->value);
   switch (format) {
     case SPMV_CSR:
-      return record(spmv::launch_spmv_csr(
-          h->R, h->Z, h->rowPtrs, h->colIdx, h->value, h->chunkDesc, d_x, d_y, h->devStatus,
+      return record(spmv::launch_spmv_csr<T>(
+          h->R, h->Z, h->rowPtrs, h->colIdx, value, h->chunkDesc, d_x, d_y, h->devStatus,
           h->stats.gather_lines > 0.0 && h->stats.gather_lines <= spmv::kCsrPipelineMaxLines, s));
     case SPMV_COO:
-      return record(spmv::launch_spmv_coo(h->Z, h->cooRow, h->colIdx, h->value, d_x, d_y,
-                                          false, s));
+      return record(spmv::launch_spmv_coo<T>(h->Z, h->cooRow, h->colIdx, value, d_x, d_y, false,
+                                             s));
     case SPMV_ELL:
-      return record(spmv::launch_spmv_ell(h->R, h->ellK, h->ellCol, h->ellVal, d_x, d_y, s));
+      return record(spmv::launch_spmv_ell<T>(h->R, h->ellK, h->ellCol, cval<T>(h->ellVal), d_x,
+                                             d_y, s));
     case SPMV_HYB: {
       bool ellRan = false;
       if (h->hybK > 0) {
-        SPMV_TRY(record(spmv::launch_spmv_ell(h->R, h->hybK, h->hybCol, h->hybVal, d_x, d_y, s)));
+        SPMV_TRY(record(spmv::launch_spmv_ell<T>(h->R, h->hybK, h->hybCol, cval<T>(h->hybVal),
+                                                 d_x, d_y, s)));
         ellRan = true;
       }
       if (h->hybCooN > 0)
-        SPMV_TRY(record(spmv::launch_spmv_coo(h->hybCooN, h->hybCooRow, h->hybCooCol,
-                                              h->hybCooVal, d_x, d_y, ellRan, s)));
+        SPMV_TRY(record(spmv::launch_spmv_coo<T>(h->hybCooN, h->hybCooRow, h->hybCooCol,
+                                                 cval<T>(h->hybCooVal), d_x, d_y, ellRan, s)));
       return SPMV_OK;
     }
     case SPMV_JDS:
-      return record(spmv::launch_spmv_jds(h->R, h->jdsMaxLen, h->jdsTSplit, h->jdsWTail,
-                                          h->jdsIterPtr, h->jdsPerm, h->jdsCol, h->jdsVal, d_x,
-                                          d_y, s));
+      return record(spmv::launch_spmv_jds<T>(h->R, h->jdsMaxLen, h->jdsTSplit, h->jdsWTail,
+                                             h->jdsIterPtr, h->jdsPerm, h->jdsCol,
+                                             cval<T>(h->jdsVal), d_x, d_y, s));
     case SPMV_SELL:
       if (h->sellSlots == 0) return SPMV_OK;
-      return record(spmv::launch_spmv_sell(h->R, h->sellS, (int)h->sellSlots, h->sellSecPtr,
-                                           h->sellPerm, h->sellCol, h->sellVal, h->sellItems,
-                                           h->sellNItems, d_x, d_y, s));
+      return record(spmv::launch_spmv_sell<T>(h->R, h->sellS, (int)h->sellSlots, h->sellSecPtr,
+                                              h->sellPerm, h->sellCol, cval<T>(h->sellVal),
+                                              h->sellItems, h->sellNItems, d_x, d_y, s));
     case SPMV_XBLOCK:
-      return record(spmv::launch_spmv_xb(h->C, h->xbB, h->xbNch, h->xbChunkPtr, h->xbRow,
-                                         h->xbCol, h->xbVal, d_x, d_y, s));
+      return record(spmv::launch_spmv_xb<T>(h->C, h->xbB, h->xbNch, h->xbChunkPtr, h->xbRow,
+                                            h->xbCol, cval<T>(h->xbVal), d_x, d_y, s));
     default:
       return SPMV_ERR_INVALID_ARG;
   }
 }
 }  // namespace
+
+extern "C" {
 
 namespace {
 // pinned host copy of the CG state, one per host thread
@@ -835,6 +920,7 @@ int spmv_cg_solve(spmv_handle h, spmv_format format, const float* d_y, float* d_
                   int32_t maxIter, double tol, spmv_cg_info* info, void* stream) {
   SPMV_TRY(check_handle(h));
   if (!info || maxIter < 0 || !(tol >= 0.0)) return SPMV_ERR_INVALID_ARG;
+  if (h->f64) return SPMV_ERR_INVALID_ARG;  // the solver runs on 4-byte values
   if (h->R != h->C) return SPMV_ERR_INVALID_ARG;
   if (format == SPMV_AUTO) format = (spmv_format)h->stats.auto_format;
   SPMV_TRY(converted(h, format));
@@ -900,7 +986,8 @@ int spmv_cg_solve(spmv_handle h, spmv_format format, const float* d_y, float* d_
     float* d = dBuf[(enq + 1) & 1];
     if (fusedEll) {
       // d = -g + beta d_old, q = A d, d'q in one kernel (d_old: the other buffer)
-      st = record(spmv::launch_cg_ell_q((int)R, h->ellK, h->ellCol, h->ellVal, g, dBuf[enq & 1],
+      st = record(spmv::launch_cg_ell_q((int)R, h->ellK, h->ellCol, cval<float>(h->ellVal), g,
+                                        dBuf[enq & 1],
                                         d, q, partials, state, s));
     } else {
       d = dBuf[0];
@@ -942,17 +1029,31 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
   out->num_rows = h->R;
   out->num_cols = h->C;
   out->nnz = h->Z;
+  out->value_bytes = h->f64 ? (int32_t)sizeof(double) : (int32_t)sizeof(float);
+  // value arrays go to the field of the handle's value type
+  auto setv = [&](const void* v) {
+    if (h->f64)
+      out->value_f64 = static_cast<const double*>(v);
+    else
+      out->value = static_cast<const float*>(v);
+  };
+  auto setcv = [&](const void* v) {
+    if (h->f64)
+      out->coo_value_f64 = static_cast<const double*>(v);
+    else
+      out->coo_value = static_cast<const float*>(v);
+  };
   switch (format) {
     case SPMV_CSR:
       out->row_ptrs = h->rowPtrs;
       out->col_idx = h->colIdx;
-      out->value = h->value;
+      setv(h->value);
       return SPMV_OK;
     case SPMV_COO:
       if (!h->hasCoo) return SPMV_ERR_NOT_CONVERTED;
       out->row_idx = h->cooRow;
       out->col_idx = h->colIdx;
-      out->value = h->value;
+      setv(h->value);
       out->coo_nnz = h->Z;
       return SPMV_OK;
     case SPMV_ELL:
@@ -960,7 +1061,7 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       out->width = h->ellK;
       out->ell_slots = (int64_t)h->R * h->ellK;
       out->col_idx = h->ellCol;
-      out->value = h->ellVal;
+      setv(h->ellVal);
       out->nnz_per_row = h->ellNnz;
       return SPMV_OK;
     case SPMV_HYB:
@@ -968,18 +1069,18 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       out->width = h->hybK;
       out->ell_slots = (int64_t)h->R * h->hybK;
       out->col_idx = h->hybCol;
-      out->value = h->hybVal;
+      setv(h->hybVal);
       out->nnz_per_row = h->hybNnz;
       out->coo_nnz = h->hybCooN;
       out->row_idx = h->hybCooRow;
       out->coo_col_idx = h->hybCooCol;
-      out->coo_value = h->hybCooVal;
+      setcv(h->hybCooVal);
       return SPMV_OK;
     case SPMV_JDS:
       if (!h->hasJds) return SPMV_ERR_NOT_CONVERTED;
       out->width = h->jdsMaxLen;
       out->col_idx = h->jdsCol;
-      out->value = h->jdsVal;
+      setv(h->jdsVal);
       out->perm = h->jdsPerm;
       out->iter_ptr = h->jdsIterPtr;
       return SPMV_OK;
@@ -988,7 +1089,7 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       out->width = h->sellW0;
       out->ell_slots = h->sellSlots;
       out->col_idx = h->sellCol;
-      out->value = h->sellVal;
+      setv(h->sellVal);
       out->perm = h->sellPerm;
       out->sec_ptr = h->sellSecPtr;
       out->section_rows = h->sellS;
@@ -1006,7 +1107,7 @@ int spmv_export(spmv_handle h, spmv_format format, spmv_arrays* out) {
       }
       out->ell_slots = h->xbSlots;
       out->row_idx = h->xbRow;
-      out->value = h->xbVal;
+      setv(h->xbVal);
       out->chunk_ptr = h->xbChunkPtr;
       out->col16 = h->xbCol;
       out->chunk_cols = h->xbB;

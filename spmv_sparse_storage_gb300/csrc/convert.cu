@@ -39,11 +39,12 @@ __device__ __forceinline__ int find_segment(int start, int k) {
 
 // CSR -> ELL of width K (also the ELL part of HYB): thread per row, writes
 // coalesced across rows. Padding slots get column -1 and value +0.0f.
+template <class T>
 __global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __restrict__ rowPtrs,
                                                     const int* __restrict__ colIdx,
-                                                    const float* __restrict__ value,
+                                                    const T* __restrict__ value,
                                                     int* __restrict__ ellCol,
-                                                    float* __restrict__ ellVal,
+                                                    T* __restrict__ ellVal,
                                                     int* __restrict__ nnzPerRow) {
   const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= R) return;
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __r
   for (int t = 0; t < K; ++t) {
     const size_t i = (size_t)t * (size_t)R + (size_t)r;
     int c = -1;
-    float v = 0.0f;
+    T v = T(0);
     if (t < kept) {
       c = colIdx[a + t];
       v = value[a + t];
@@ -66,13 +67,14 @@ __global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __r
 
 // HYB COO part: row r's entries at in-row positions >= K, written at
 // tailPtr[r] ... in row order (warp-cooperative expansion as above).
+template <class T>
 __global__ void __launch_bounds__(256) k_hyb_tail_copy(int R, int K, const int* __restrict__ rowPtrs,
                                                        const int* __restrict__ colIdx,
-                                                       const float* __restrict__ value,
+                                                       const T* __restrict__ value,
                                                        const int* __restrict__ tailPtr,
                                                        int* __restrict__ cooRow,
                                                        int* __restrict__ cooCol,
-                                                       float* __restrict__ cooVal) {
+                                                       T* __restrict__ cooVal) {
   const int lane = threadIdx.x & 31;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long r0 = warp * 32;
@@ -390,14 +392,15 @@ __global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKe
 // staged in shared memory.
 constexpr int kCoop = 64;
 constexpr int kJdsScatterSmem = 1024;
+template <class T>
 __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
                                                      const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
-                                                     const float* __restrict__ value,
+                                                     const T* __restrict__ value,
                                                      const int* __restrict__ inv,
                                                      const int* __restrict__ iterPtr,
                                                      int* __restrict__ jdsCol,
-                                                     float* __restrict__ jdsVal) {
+                                                     T* __restrict__ jdsVal) {
   __shared__ int sIp[kJdsScatterSmem];
   const int nIp = maxLen < kJdsScatterSmem ? maxLen : kJdsScatterSmem;
   for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = iterPtr[t];
@@ -436,12 +439,13 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
 
 size_t scan_scratch_ints(long long n) { return (size_t)((n + kScanTile - 1) / kScanTile + 1); }
 
+template <class T>
 cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
-                              const float* value, int* ellCol, float* ellVal, int* nnzPerRow,
+                              const T* value, int* ellCol, T* ellVal, int* nnzPerRow,
                               cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const long long blocks = ((long long)R + 255) / 256;
-  k_csr_to_ell<<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, ellCol, ellVal,
+  k_csr_to_ell<T><<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, ellCol, ellVal,
                                                 nnzPerRow);
   note_launches(1);
   return cudaGetLastError();
@@ -452,13 +456,14 @@ cudaError_t launch_tail_scan(int R, int K, const int* rowPtrs, int* tailPtr, int
   return exclusive_scan(TailLenIn{rowPtrs, K}, (long long)R, tailPtr, scratch, s);
 }
 
+template <class T>
 cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* colIdx,
-                                 const float* value, const int* tailPtr, int* cooRow,
-                                 int* cooCol, float* cooVal, cudaStream_t s) {
+                                 const T* value, const int* tailPtr, int* cooRow,
+                                 int* cooCol, T* cooVal, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const long long warps = ((long long)R + 31) / 32;
   const long long blocks = (warps * 32 + 255) / 256;
-  k_hyb_tail_copy<<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, tailPtr, cooRow,
+  k_hyb_tail_copy<T><<<(unsigned)blocks, 256, 0, s>>>(R, K, rowPtrs, colIdx, value, tailPtr, cooRow,
                                                    cooCol, cooVal);
   note_launches(1);
   return cudaGetLastError();
@@ -531,9 +536,10 @@ static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, in
                     needKeys, sortedKeys, invOut, scanScratchOut, s);
 }
 
+template <class T>
 cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
-                             const float* value, int* perm, int* iterPtr, int* jdsCol,
-                             float* jdsVal, void* scratch, const int* hostIterPtr,
+                             const T* value, int* perm, int* iterPtr, int* jdsCol,
+                             T* jdsVal, void* scratch, const int* hostIterPtr,
                              cudaStream_t s) {
   if (R <= 0) {
     // iterPtr has maxLen + 1 = 1 entry
@@ -562,7 +568,7 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
       err = exclusive_scan(ArrayIn{width}, (long long)maxLen, iterPtr, scanScratch, s);
       if (err != cudaSuccess) return err;
     }
-    k_jds_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
+    k_jds_scatter<T><<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
         R, maxLen, rowPtrs, colIdx, value, inv, iterPtr, jdsCol, jdsVal);
     note_launches(1);
   } else {
@@ -635,13 +641,14 @@ cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const
 // of the section) writes its w_k slots, real entries then padding (column -1,
 // value +0.0f). A thread writes the first kCoop slots; the warp then writes
 // each wider section's remaining slots of its rows together, one per lane.
+template <class T>
 __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* __restrict__ rowPtrs,
                                                       const int* __restrict__ colIdx,
-                                                      const float* __restrict__ value,
+                                                      const T* __restrict__ value,
                                                       const int* __restrict__ inv,
                                                       const int* __restrict__ secPtr,
                                                       int cap, int* __restrict__ sellCol,
-                                                      float* __restrict__ sellVal) {
+                                                      T* __restrict__ sellVal) {
   const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
   int a = 0, len = 0, w = 0, h = 1, j = 0, base = 0;
@@ -660,7 +667,7 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
       const long long o = (long long)base + (long long)t * h + j;
       const bool real = t < len;
       sellCol[o] = real ? colIdx[a + t] : -1;
-      sellVal[o] = real ? value[a + t] : 0.0f;
+      sellVal[o] = real ? value[a + t] : T(0);
     }
   }
   unsigned wide = __ballot_sync(kFullMask, w > kCoop);
@@ -677,17 +684,18 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
       const long long o = (long long)lb + (long long)t * lh + lj;
       const bool real = t < ll;
       sellCol[o] = real ? colIdx[la + t] : -1;
-      sellVal[o] = real ? value[la + t] : 0.0f;
+      sellVal[o] = real ? value[la + t] : T(0);
     }
   }
 }
 
+template <class T>
 cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
-                                const float* value, const void* scratch, const int* secPtr,
-                                int slots, int* sellCol, float* sellVal, cudaStream_t s) {
+                                const T* value, const void* scratch, const int* secPtr,
+                                int slots, int* sellCol, T* sellVal, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const int* inv = static_cast<const int*>(scratch) + 3LL * R;  // row_sort's layout
-  k_sell_scatter<<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
+  k_sell_scatter<T><<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
       R, S, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
   note_launches(1);
   return cudaGetLastError();
@@ -735,15 +743,16 @@ struct Pad4In {  // chunk sizes rounded up to 4 entries
   __device__ int operator()(long long i) const { return (p[i] + 3) & ~3; }
 };
 
+template <class T>
 __global__ void __launch_bounds__(256) k_xb_scatter(int Z, int B, const int* __restrict__ colIdx,
-                                                    const float* __restrict__ value,
+                                                    const T* __restrict__ value,
                                                     const int* __restrict__ rowIdx,
                                                     const int* __restrict__ inv,
                                                     const int* __restrict__ ustart,
                                                     const int* __restrict__ chunkPtr,
                                                     int* __restrict__ xbRow,
                                                     unsigned short* __restrict__ xbCol,
-                                                    float* __restrict__ xbVal) {
+                                                    T* __restrict__ xbVal) {
   const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (k >= Z) return;
   const int col = colIdx[k];
@@ -754,15 +763,16 @@ __global__ void __launch_bounds__(256) k_xb_scatter(int Z, int B, const int* __r
   xbVal[p] = value[k];
 }
 
+template <class T>
 __global__ void k_xb_pad(int nch, const int* __restrict__ cnt, const int* __restrict__ chunkPtr,
                          int* __restrict__ xbRow, unsigned short* __restrict__ xbCol,
-                         float* __restrict__ xbVal) {
+                         T* __restrict__ xbVal) {
   const long long c = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (c >= nch) return;
   for (long long i = (long long)chunkPtr[c] + cnt[c]; i < chunkPtr[c + 1]; ++i) {
     xbRow[i] = -1;
     xbCol[i] = 0;
-    xbVal[i] = 0.0f;
+    xbVal[i] = T(0);
   }
 }
 
@@ -773,9 +783,10 @@ size_t xb_scratch_bytes(int Z, int nch) {
   return ints * sizeof(int) + jds_sort_scratch_bytes(Z, nch > 0 ? nch - 1 : 0);
 }
 
-cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const float* value,
+template <class T>
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* value,
                             const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
-                            float* xbVal, void* scratch, cudaStream_t s) {
+                            T* xbVal, void* scratch, cudaStream_t s) {
   if (nch <= 0) return cudaMemsetAsync(chunkPtr, 0, sizeof(int), s);
   int* cnt = static_cast<int*>(scratch);
   int* ustart = cnt + nch;
@@ -794,7 +805,7 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const floa
   if (err == cudaSuccess) err = exclusive_scan(Pad4In{cnt}, nch, chunkPtr, scanScratch, s);
   if (err != cudaSuccess || Z <= 0) {
     if (err == cudaSuccess) {
-      k_xb_pad<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol,
+      k_xb_pad<T><<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol,
                                                             xbVal);
       note_launches(1);
       err = cudaGetLastError();
@@ -809,11 +820,29 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const floa
   err = radix_sort(ChunkKeyIn{colIdx, B, nullptr, nullptr}, Z, nch - 1, perm, sortScratch + Z,
                    false, &sortedKeys, &inv, &unusedScan, s);
   if (err != cudaSuccess) return err;
-  k_xb_scatter<<<(unsigned)(((long long)Z + 255) / 256), 256, 0, s>>>(
+  k_xb_scatter<T><<<(unsigned)(((long long)Z + 255) / 256), 256, 0, s>>>(
       Z, B, colIdx, value, rowIdx, inv, ustart, chunkPtr, xbRow, xbCol, xbVal);
-  k_xb_pad<<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol, xbVal);
+  k_xb_pad<T><<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol,
+                                                           xbVal);
   note_launches(2);
   return cudaGetLastError();
 }
+
+// the two value types
+#define SPMV_INSTANTIATE(T)                                                                      \
+  template cudaError_t launch_csr_to_ell<T>(int, int, const int*, const int*, const T*, int*,   \
+                                            T*, int*, cudaStream_t);                             \
+  template cudaError_t launch_hyb_tail_copy<T>(int, int, const int*, const int*, const T*,      \
+                                               const int*, int*, int*, T*, cudaStream_t);        \
+  template cudaError_t launch_jds_build<T>(int, int, const int*, const int*, const T*, int*,    \
+                                           int*, int*, T*, void*, const int*, cudaStream_t);     \
+  template cudaError_t launch_sell_scatter<T>(int, int, const int*, const int*, const T*,       \
+                                              const void*, const int*, int, int*, T*,            \
+                                              cudaStream_t);                                     \
+  template cudaError_t launch_xb_build<T>(int, int, int, const int*, const T*, const int*, int*, \
+                                          int*, unsigned short*, T*, void*, cudaStream_t);
+SPMV_INSTANTIATE(float)
+SPMV_INSTANTIATE(double)
+#undef SPMV_INSTANTIATE
 
 }  // namespace spmv

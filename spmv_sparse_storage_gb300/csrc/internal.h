@@ -93,22 +93,25 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
 // CSR -> COO rowIdx from the CSR chunk records (spmv_kernels.cu)
 cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
                                int* rowIdx, cudaStream_t s);
+template <class T>
 cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
-                              const float* value, int* ellCol, float* ellVal, int* nnzPerRow,
+                              const T* value, int* ellCol, T* ellVal, int* nnzPerRow,
                               cudaStream_t s);
 // Exclusive scan of max(0, len(r) - K) over rows into tailPtr[0..R].
 cudaError_t launch_tail_scan(int R, int K, const int* rowPtrs, int* tailPtr, int* scratch,
                              cudaStream_t s);
 size_t scan_scratch_ints(long long n);
+template <class T>
 cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* colIdx,
-                                 const float* value, const int* tailPtr, int* cooRow,
-                                 int* cooCol, float* cooVal, cudaStream_t s);
+                                 const T* value, const int* tailPtr, int* cooRow,
+                                 int* cooCol, T* cooVal, cudaStream_t s);
 // JDS: stable sort of rows by length (longest first), iterPtr, jagged scatter.
 size_t jds_sort_scratch_bytes(int R, int maxLen);
 // hostIterPtr: iterPtr computed on the host (nullptr: computed on the device)
+template <class T>
 cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
-                             const float* value, int* perm, int* iterPtr, int* jdsCol,
-                             float* jdsVal, void* scratch, const int* hostIterPtr,
+                             const T* value, int* perm, int* iterPtr, int* jdsCol,
+                             T* jdsVal, void* scratch, const int* hostIterPtr,
                              cudaStream_t s);
 constexpr int kJdsPad = 8;  // extra elements after the JDS arrays (aligned vector reads)
 // Sectioned ELL (the JDS variant): sort, section widths (for a read-back when
@@ -130,32 +133,39 @@ cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, v
                              cudaStream_t s);
 cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const int* perm,
                                int* widths, cudaStream_t s);
+template <class T>
 cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
-                                const float* value, const void* scratch, const int* secPtr,
-                                int slots, int* sellCol, float* sellVal, cudaStream_t s);
+                                const T* value, const void* scratch, const int* secPtr,
+                                int slots, int* sellCol, T* sellVal, cudaStream_t s);
 
 // spmv_kernels.cu
 // fills hi, flags and mask of every chunk record; runs after the stats pass
 cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks,
                                    CsrChunkDesc* desc, cudaStream_t s);
+template <class T>
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const CsrChunkDesc* desc, const float* x,
-                            float* y, int* devStatus, bool pipelined, cudaStream_t s);
-cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
-                            const float* x, float* y, bool dependent, cudaStream_t s);
-cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
-                            const float* x, float* y, cudaStream_t s);
+                            const T* value, const CsrChunkDesc* desc, const T* x,
+                            T* y, int* devStatus, bool pipelined, cudaStream_t s);
+template <class T>
+cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const T* value,
+                            const T* x, T* y, bool dependent, cudaStream_t s);
+template <class T>
+cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
+                            const T* x, T* y, cudaStream_t s);
 // x-blocked list: nonzeros grouped by column chunk of B columns (CSR order in
 // a chunk), 16-bit local columns, chunks padded to 4 entries (row -1).
-constexpr int kXbDefaultChunk = 49152;  // columns per chunk = floats of x staged per CTA
+constexpr int kXbSmemBytes = 196608;    // x staged per CTA: 192 KiB
+constexpr int kXbDefaultChunk = 49152;  // columns per chunk with 4-byte values (24576 with 8)
 constexpr int kXbMaxChunks = 65536;     // chunk ids sorted in at most two radix passes
 size_t xb_scratch_bytes(int Z, int nch);
-cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const float* value,
+template <class T>
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* value,
                             const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
-                            float* xbVal, void* scratch, cudaStream_t s);
+                            T* xbVal, void* scratch, cudaStream_t s);
+template <class T>
 cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int* xbRow,
-                           const unsigned short* xbCol, const float* xbVal, const float* x,
-                           float* y, cudaStream_t s);
+                           const unsigned short* xbCol, const T* xbVal, const T* x,
+                           T* y, cudaStream_t s);
 
 // Conjugate gradient for A·X + Y = 0: device state shared by the kernels of
 // one solve (zeroed before the first). status: kCgRunning until the stop test
@@ -192,11 +202,13 @@ cudaError_t launch_cg_update(int R, float* X, float* g, const float* d, const fl
                              float* partials, CgState* st, cudaStream_t s);
 
 // items: tail work of the sections wider than kSellMainSlots (nItems of them)
+template <class T>
 cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
-                             const int* sellCol, const float* sellVal, const SellItem* items,
-                             int nItems, const float* x, float* y, cudaStream_t s);
+                             const int* sellCol, const T* sellVal, const SellItem* items,
+                             int nItems, const T* x, T* y, cudaStream_t s);
+template <class T>
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
-                            const int* perm, const int* jdsCol, const float* jdsVal,
-                            const float* x, float* y, cudaStream_t s);
+                            const int* perm, const int* jdsCol, const T* jdsVal,
+                            const T* x, T* y, cudaStream_t s);
 
 }  // namespace spmv

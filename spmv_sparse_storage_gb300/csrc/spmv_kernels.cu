@@ -8,6 +8,7 @@
 // so the designs below are about streaming those bytes at HBM speed, keeping
 // the gathered x resident in L2, and balancing the work.
 #include <climits>
+#include <type_traits>
 
 #include "device_util.cuh"
 #include "internal.h"
@@ -25,32 +26,33 @@ namespace {
 // atomic per row per chunk. `waitFirst`: wait for the preceding kernel of the
 // stream (programmatic dependent launch) before the first write to y.
 // ===========================================================================
-__device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const float (&p)[4],
-                                                   float* __restrict__ y, bool waitFirst) {
+template <class T>
+__device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T (&p)[4],
+                                                   T* __restrict__ y, bool waitFirst) {
   const int lane = threadIdx.x & 31;
   // in-lane run sums: s[e] = sum of the run that ends at e
-  float s[4];
+  T s[4];
   s[0] = p[0];
 #pragma unroll
   for (int e = 1; e < 4; ++e) s[e] = (row[e] == row[e - 1]) ? s[e - 1] + p[e] : p[e];
   const int hEnd = row[1] != row[0] ? 0 : row[2] != row[1] ? 1 : row[3] != row[2] ? 2 : 3;
   const bool single = (hEnd == 3);
   const int rh = row[0], rt = row[3];
-  const float sh = s[hEnd], st = s[3];
+  const T sh = s[hEnd], st = s[3];
 
   // across lanes: w = tail-run sum carried to the right while lanes continue one run
   const int prevRt = __shfl_up_sync(kFullMask, rt, 1);
   const bool connected = lane > 0 && prevRt == rh;
   const unsigned heads = __ballot_sync(kFullMask, !(single && connected));
   const int segStart = 31 - __clz(heads & (0xffffffffu >> (31 - lane)));
-  float w = st;
+  T w = st;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const float o = __shfl_up_sync(kFullMask, w, off);
+    const T o = __shfl_up_sync(kFullMask, w, off);
     if (lane - off >= segStart) w += o;
   }
-  const float wPrev = __shfl_up_sync(kFullMask, w, 1);
-  const float carryIn = connected ? wPrev : 0.0f;
+  const T wPrev = __shfl_up_sync(kFullMask, w, 1);
+  const T carryIn = connected ? wPrev : T(0);
   const int nextRh = __shfl_down_sync(kFullMask, rh, 1);
   const bool tailEnds = (lane == 31) || nextRh != rt;
 
@@ -230,24 +232,24 @@ __global__ void __launch_bounds__((kCsrConsumerWarps + 1) * 32, 3) k_spmv_csr_tm
 
 // Chunks [c0, c1) with plain loads: the partial last chunk, and every chunk
 // when colIdx/value are not 16-byte aligned. One warp per chunk.
-template <bool VEC>
+template <class T, bool VEC>
 __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, long long c1,
                                                         const int* __restrict__ rowPtrs,
                                                         const int* __restrict__ colIdx,
-                                                        const float* __restrict__ value,
+                                                        const T* __restrict__ value,
                                                         const CsrChunkDesc* __restrict__ desc,
-                                                        const float* __restrict__ x,
-                                                        float* __restrict__ y) {
+                                                        const T* __restrict__ x,
+                                                        T* __restrict__ y) {
   const int lane = threadIdx.x & 31;
   const long long c = c0 + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if (c >= c1) return;  // warp-uniform
   const long long cb = c * kCsrChunk;
   const long long base = cb + 4 * lane;
   const CsrChunkDesc d = desc[c];
-  float p[4];
+  T p[4];
   if (VEC && base + 4 <= Z) {
     const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+    const Vec4<T> v4 = ld4_stream(value + base);
     p[0] = v4.x * ld_x(x + c4.x);
     p[1] = v4.y * ld_x(x + c4.y);
     p[2] = v4.z * ld_x(x + c4.z);
@@ -256,7 +258,7 @@ __global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, lon
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const long long k = base + e;
-      p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : 0.0f;
+      p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : T(0);
     }
   }
   int row[4];
@@ -346,11 +348,11 @@ __global__ void k_csr_chunk_masks(int R, int Z, const int* __restrict__ rowPtrs,
 // is never read. VEC4: numRows % 4 == 0 and 16-byte aligned arrays, a thread
 // handles 4 consecutive rows with 16-byte loads.
 // ===========================================================================
-template <bool VEC4>
+template <class T, bool VEC4>
 __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __restrict__ ellCol,
-                                                     const float* __restrict__ ellVal,
-                                                     const float* __restrict__ x,
-                                                     float* __restrict__ y) {
+                                                     const T* __restrict__ ellVal,
+                                                     const T* __restrict__ x,
+                                                     T* __restrict__ y) {
   // let a programmatically dependent kernel (the COO part of HYB) start its
   // loads; it waits for this grid to finish before it writes y
   grid_dependency_trigger();
@@ -359,44 +361,42 @@ __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __
     const long long ld = R >> 2;
     if (q >= ld) return;
     const int4* c4 = reinterpret_cast<const int4*>(ellCol);
-    const float4* v4 = reinterpret_cast<const float4*>(ellVal);
-    float4* y4 = reinterpret_cast<float4*>(y);
-    const float4 y0 = y4[q];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    const Vec4<T> y0 = ld4(y + 4 * q);
+    Vec4<T> acc = {T(0), T(0), T(0), T(0)};
     int t = 0;
     for (; t + 4 <= K; t += 4) {
       int4 c[4];
-      float4 v[4];
+      Vec4<T> v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         c[u] = ld_stream(c4 + (size_t)(t + u) * ld + q);
-        v[u] = ld_stream(v4 + (size_t)(t + u) * ld + q);
+        v[u] = ld4_stream(ellVal + 4 * ((size_t)(t + u) * ld + q));
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (c[u].x >= 0) acc.x = fmaf(v[u].x, ld_x(x + c[u].x), acc.x);
-        if (c[u].y >= 0) acc.y = fmaf(v[u].y, ld_x(x + c[u].y), acc.y);
-        if (c[u].z >= 0) acc.z = fmaf(v[u].z, ld_x(x + c[u].z), acc.z);
-        if (c[u].w >= 0) acc.w = fmaf(v[u].w, ld_x(x + c[u].w), acc.w);
+        if (c[u].x >= 0) acc.x = fma_t(v[u].x, ld_x(x + c[u].x), acc.x);
+        if (c[u].y >= 0) acc.y = fma_t(v[u].y, ld_x(x + c[u].y), acc.y);
+        if (c[u].z >= 0) acc.z = fma_t(v[u].z, ld_x(x + c[u].z), acc.z);
+        if (c[u].w >= 0) acc.w = fma_t(v[u].w, ld_x(x + c[u].w), acc.w);
       }
     }
     for (; t < K; ++t) {
       const int4 c = ld_stream(c4 + (size_t)t * ld + q);
-      const float4 v = ld_stream(v4 + (size_t)t * ld + q);
-      if (c.x >= 0) acc.x = fmaf(v.x, ld_x(x + c.x), acc.x);
-      if (c.y >= 0) acc.y = fmaf(v.y, ld_x(x + c.y), acc.y);
-      if (c.z >= 0) acc.z = fmaf(v.z, ld_x(x + c.z), acc.z);
-      if (c.w >= 0) acc.w = fmaf(v.w, ld_x(x + c.w), acc.w);
+      const Vec4<T> v = ld4_stream(ellVal + 4 * ((size_t)t * ld + q));
+      if (c.x >= 0) acc.x = fma_t(v.x, ld_x(x + c.x), acc.x);
+      if (c.y >= 0) acc.y = fma_t(v.y, ld_x(x + c.y), acc.y);
+      if (c.z >= 0) acc.z = fma_t(v.z, ld_x(x + c.z), acc.z);
+      if (c.w >= 0) acc.w = fma_t(v.w, ld_x(x + c.w), acc.w);
     }
-    y4[q] = make_float4(y0.x + acc.x, y0.y + acc.y, y0.z + acc.z, y0.w + acc.w);
+    st4(y + 4 * q, Vec4<T>{y0.x + acc.x, y0.y + acc.y, y0.z + acc.z, y0.w + acc.w});
   } else {
     if (q >= R) return;
-    const float y0 = y[q];
-    float acc = 0.0f;
+    const T y0 = y[q];
+    T acc = T(0);
     int t = 0;
     for (; t + 4 <= K; t += 4) {
       int c[4];
-      float v[4];
+      T v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         c[u] = ld_stream(ellCol + (size_t)(t + u) * R + q);
@@ -404,12 +404,12 @@ __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
-        if (c[u] >= 0) acc = fmaf(v[u], ld_x(x + c[u]), acc);
+        if (c[u] >= 0) acc = fma_t(v[u], ld_x(x + c[u]), acc);
     }
     for (; t < K; ++t) {
       const int c = ld_stream(ellCol + (size_t)t * R + q);
-      const float v = ld_stream(ellVal + (size_t)t * R + q);
-      if (c >= 0) acc = fmaf(v, ld_x(x + c), acc);
+      const T v = ld_stream(ellVal + (size_t)t * R + q);
+      if (c >= 0) acc = fma_t(v, ld_x(x + c), acc);
     }
     y[q] = y0 + acc;
   }
@@ -424,22 +424,22 @@ __global__ void __launch_bounds__(256, 4) k_spmv_ell(int R, int K, const int* __
 // the ELL part of HYB, the kernel loads and reduces before waiting for that
 // kernel, and only then touches y.
 // ===========================================================================
-template <bool VEC>
+template <class T, bool VEC>
 __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__ rowIdx,
                                                   const int* __restrict__ colIdx,
-                                                  const float* __restrict__ value,
-                                                  const float* __restrict__ x,
-                                                  float* __restrict__ y, int dependent) {
+                                                  const T* __restrict__ value,
+                                                  const T* __restrict__ x,
+                                                  T* __restrict__ y, int dependent) {
   const int lane = threadIdx.x & 31;
   const long long warp = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long base = warp * 128 + 4 * lane;
 
   int row[4];
-  float p[4];
+  T p[4];
   if (VEC && base + 4 <= Z) {
     const int4 r4 = ld_stream(reinterpret_cast<const int4*>(rowIdx + base));
     const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-    const float4 v4 = ld_stream(reinterpret_cast<const float4*>(value + base));
+    const Vec4<T> v4 = ld4_stream(value + base);
     row[0] = r4.x; row[1] = r4.y; row[2] = r4.z; row[3] = r4.w;
     p[0] = v4.x * ld_x(x + c4.x);
     p[1] = v4.y * ld_x(x + c4.y);
@@ -454,7 +454,7 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
         p[e] = ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k));
       } else {
         row[e] = -1;  // sentinel: no entry
-        p[e] = 0.0f;
+        p[e] = T(0);
       }
     }
   }
@@ -478,14 +478,15 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // atomically. The result of sorted row s goes straight to y[perm[s]] (the
 // page permutes the result back with the row array).
 // ===========================================================================
+template <class T>
 __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
                                                      const int* __restrict__ perm,
                                                      const int* __restrict__ jdsCol,
-                                                     const float* __restrict__ jdsVal,
-                                                     const float* __restrict__ x,
-                                                     float* __restrict__ y) {
+                                                     const T* __restrict__ jdsVal,
+                                                     const T* __restrict__ x,
+                                                     T* __restrict__ y) {
   __shared__ int sIp[kJdsSplitMaxDiag + 1];
   if ((int)blockIdx.x < nMainBlocks) {
     for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
@@ -495,7 +496,6 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
     const long long s0 = 4 * q;                                 // first of this thread's 4 rows
     const long long warpFirst = 4 * (q - lane);                 // first row of the warp
     const int4* col4 = reinterpret_cast<const int4*>(jdsCol);  // padded by kJdsPad entries
-    const float4* val4 = reinterpret_cast<const float4*>(jdsVal);
     int r[4];
     if (s0 + 4 <= R) {
       const int4 p4 = __ldg(reinterpret_cast<const int4*>(perm) + q);
@@ -504,11 +504,11 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
 #pragma unroll
       for (int e = 0; e < 4; ++e) r[e] = s0 + e < R ? __ldg(perm + s0 + e) : -1;
     }
-    float y0[4], acc[4];
+    T y0[4], acc[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      y0[e] = (r[e] >= 0 && s0 + e >= wTail) ? y[r[e]] : 0.0f;
-      acc[e] = 0.0f;
+      y0[e] = (r[e] >= 0 && s0 + e >= wTail) ? y[r[e]] : T(0);
+      acc[e] = T(0);
     }
     for (int t = 0; t < tSplit; ++t) {
       const int a = sIp[t];
@@ -521,19 +521,19 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
       const int m = a & 3;
       const long long vi = ((long long)(a - m) >> 2) + q;
       int4 cv = make_int4(0, 0, 0, 0);
-      float4 vv = make_float4(0.f, 0.f, 0.f, 0.f);
+      Vec4<T> vv = {T(0), T(0), T(0), T(0)};
       if (s0 - m < wt) {
         cv = ld_stream(col4 + vi);
-        vv = ld_stream(val4 + vi);
+        vv = ld4_stream(jdsVal + 4 * vi);
       }
       int cw[4];
-      float fw[4];
+      T fw[4];
       if (m == 0) {
         cw[0] = cv.x; cw[1] = cv.y; cw[2] = cv.z; cw[3] = cv.w;
         fw[0] = vv.x; fw[1] = vv.y; fw[2] = vv.z; fw[3] = vv.w;
       } else {
         int4 cn;
-        float4 vn;
+        Vec4<T> vn;
         cn.x = __shfl_down_sync(kFullMask, cv.x, 1);
         cn.y = __shfl_down_sync(kFullMask, cv.y, 1);
         cn.z = __shfl_down_sync(kFullMask, cv.z, 1);
@@ -544,10 +544,10 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
         vn.w = __shfl_down_sync(kFullMask, vv.w, 1);
         if (lane == 31 && s0 + 4 - m < wt) {
           cn = ld_stream(col4 + vi + 1);
-          vn = ld_stream(val4 + vi + 1);
+          vn = ld4_stream(jdsVal + 4 * (vi + 1));
         }
         const int ca[8] = {cv.x, cv.y, cv.z, cv.w, cn.x, cn.y, cn.z, cn.w};
-        const float fa[8] = {vv.x, vv.y, vv.z, vv.w, vn.x, vn.y, vn.z, vn.w};
+        const T fa[8] = {vv.x, vv.y, vv.z, vv.w, vn.x, vn.y, vn.z, vn.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           cw[e] = m == 1 ? ca[e + 1] : m == 2 ? ca[e + 2] : ca[e + 3];
@@ -556,7 +556,7 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
       }
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (s0 + e < wt) acc[e] = fmaf(fw[e], ld_x(x + cw[e]), acc[e]);
+        if (s0 + e < wt) acc[e] = fma_t(fw[e], ld_x(x + cw[e]), acc[e]);
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -574,14 +574,14 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
     const int tBeg = tSplit + tb * kJdsTailDiags;
     const int tEnd = min(tBeg + kJdsTailDiags, maxLen);
     if (s >= wTail) return;
-    float acc = 0.0f;
+    T acc = T(0);
     bool any = false;
     for (int t = tBeg; t < tEnd; ++t) {
       const int a = __ldg(iterPtr + t);
       const int wdt = __ldg(iterPtr + t + 1) - a;
       if (s >= wdt) break;  // widths shrink: no later diagonal reaches s
       const long long i = (long long)a + s;
-      acc = fmaf(ld_stream(jdsVal + i), ld_x(x + ld_stream(jdsCol + i)), acc);
+      acc = fma_t(ld_stream(jdsVal + i), ld_x(x + ld_stream(jdsCol + i)), acc);
       any = true;
     }
     if (any) atomicAdd(y + perm[s], acc);
@@ -610,16 +610,20 @@ cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks
   return cudaGetLastError();
 }
 
+template <class T>
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
-                            const float* value, const CsrChunkDesc* desc, const float* x,
-                            float* y, int* devStatus, bool pipelined, cudaStream_t s) {
+                            const T* value, const CsrChunkDesc* desc, const T* x,
+                            T* y, int* devStatus, bool pipelined, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
   const long long nGroups = (long long)Z / ((long long)kCsrGroupChunks * kCsrChunk);
   const bool vec = aligned16(colIdx) && aligned16(value);
-  const bool tma = pipelined && vec && nGroups > 0;
+  // the shared-memory pipeline stages 4-byte values; 8-byte values take the
+  // direct-load kernel
+  const bool tma = std::is_same<T, float>::value && pipelined && vec && nGroups > 0;
   int n = 0;
-  if (tma) {
+  if constexpr (std::is_same<T, float>::value) {
+   if (tma) {
     static int perSm = 0;  // blocks per SM (same on every device of one architecture)
     if (perSm == 0) {
       int v = 0;
@@ -636,25 +640,27 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
     k_spmv_csr_tma<<<(unsigned)blocks, (kCsrConsumerWarps + 1) * 32, kCsrTmaSmemBytes, s>>>(
         Z, rowPtrs, colIdx, value, desc, (int)nGroups, x, y, devStatus);
     ++n;
+   }
   }
   const long long p0 = tma ? nGroups * kCsrGroupChunks : 0;
   if (p0 < nChunks) {
     const long long warps = nChunks - p0;
     const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
     if (vec)
-      k_spmv_csr_plain<true><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value, desc,
-                                                    x, y);
+      k_spmv_csr_plain<T, true><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
+                                                       desc, x, y);
     else
-      k_spmv_csr_plain<false><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
-                                                     desc, x, y);
+      k_spmv_csr_plain<T, false><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
+                                                        desc, x, y);
     ++n;
   }
   note_launches(n);
   return cudaGetLastError();
 }
 
-cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const float* value,
-                            const float* x, float* y, bool dependent, cudaStream_t s) {
+template <class T>
+cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const T* value,
+                            const T* x, T* y, bool dependent, cudaStream_t s) {
   if (Z <= 0) return cudaSuccess;
   const long long warps = ((long long)Z + 127) / 128;
   const long long blocks = (warps * 32 + 255) / 256;
@@ -672,30 +678,32 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const f
   const int dep = dependent ? 1 : 0;
   cudaError_t err;
   if (vec)
-    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<true>, Z, rowIdx, colIdx, value, x, y, dep);
+    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<T, true>, Z, rowIdx, colIdx, value, x, y, dep);
   else
-    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<false>, Z, rowIdx, colIdx, value, x, y, dep);
+    err = cudaLaunchKernelEx(&cfg, k_spmv_coo<T, false>, Z, rowIdx, colIdx, value, x, y, dep);
   note_launches(1);
   return err;
 }
 
-cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const float* ellVal,
-                            const float* x, float* y, cudaStream_t s) {
+template <class T>
+cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
+                            const T* x, T* y, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const bool vec4 = (R % 4 == 0) && aligned16(ellCol) && aligned16(ellVal) && aligned16(y);
   const long long threads = vec4 ? R / 4 : R;
   const long long blocks = (threads + 255) / 256;
   if (vec4)
-    k_spmv_ell<true><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
+    k_spmv_ell<T, true><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
   else
-    k_spmv_ell<false><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
+    k_spmv_ell<T, false><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
 
+template <class T>
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
-                            const int* perm, const int* jdsCol, const float* jdsVal,
-                            const float* x, float* y, cudaStream_t s) {
+                            const int* perm, const int* jdsCol, const T* jdsVal,
+                            const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
   const long long mainBlocks = ((long long)R + 1023) / 1024;  // 4 sorted rows per thread
   long long tailBlocks = 0;
@@ -705,7 +713,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
     const long long diagBlocks = ((long long)(maxLen - tSplit) + kJdsTailDiags - 1) / kJdsTailDiags;
     tailBlocks = (long long)tailRowBlocks * diagBlocks;
   }
-  k_spmv_jds<<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+  k_spmv_jds<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
       R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, perm, jdsCol, jdsVal, x,
       y);
   note_launches(1);
@@ -723,39 +731,39 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
 // the rows being sorted) are cut into SellItems handled by extra warps; the
 // rows of those sections add into y with atomics.
 // ---------------------------------------------------------------------------
-template <bool VEC>
+template <class T, bool VEC>
 __device__ __forceinline__ void sell_rows(const int* __restrict__ col,
-                                          const float* __restrict__ val,
-                                          const float* __restrict__ x, long long base, int h,
-                                          int j, int n, int t0, int t1, float acc[4]) {
+                                          const T* __restrict__ val,
+                                          const T* __restrict__ x, long long base, int h,
+                                          int j, int n, int t0, int t1, T acc[4]) {
   if (VEC && n == 4 && (h & 3) == 0) {
     const long long hq = h >> 2;
     const int4* c4 = reinterpret_cast<const int4*>(col + base + (long long)t0 * h + j);
-    const float4* v4 = reinterpret_cast<const float4*>(val + base + (long long)t0 * h + j);
+    const T* v4 = val + base + (long long)t0 * h + j;  // 4 values per step of h
     int t = t0;
-    for (; t + 4 <= t1; t += 4, c4 += 4 * hq, v4 += 4 * hq) {
+    for (; t + 4 <= t1; t += 4, c4 += 4 * hq, v4 += 4 * (size_t)h) {
       int4 c[4];
-      float4 v[4];
+      Vec4<T> v[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         c[u] = ld_stream(c4 + u * hq);
-        v[u] = ld_stream(v4 + u * hq);
+        v[u] = ld4_stream(v4 + u * (size_t)h);
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        if (c[u].x >= 0) acc[0] = fmaf(v[u].x, ld_x(x + c[u].x), acc[0]);
-        if (c[u].y >= 0) acc[1] = fmaf(v[u].y, ld_x(x + c[u].y), acc[1]);
-        if (c[u].z >= 0) acc[2] = fmaf(v[u].z, ld_x(x + c[u].z), acc[2]);
-        if (c[u].w >= 0) acc[3] = fmaf(v[u].w, ld_x(x + c[u].w), acc[3]);
+        if (c[u].x >= 0) acc[0] = fma_t(v[u].x, ld_x(x + c[u].x), acc[0]);
+        if (c[u].y >= 0) acc[1] = fma_t(v[u].y, ld_x(x + c[u].y), acc[1]);
+        if (c[u].z >= 0) acc[2] = fma_t(v[u].z, ld_x(x + c[u].z), acc[2]);
+        if (c[u].w >= 0) acc[3] = fma_t(v[u].w, ld_x(x + c[u].w), acc[3]);
       }
     }
-    for (; t < t1; ++t, c4 += hq, v4 += hq) {
+    for (; t < t1; ++t, c4 += hq, v4 += h) {
       const int4 c = ld_stream(c4);
-      const float4 v = ld_stream(v4);
-      if (c.x >= 0) acc[0] = fmaf(v.x, ld_x(x + c.x), acc[0]);
-      if (c.y >= 0) acc[1] = fmaf(v.y, ld_x(x + c.y), acc[1]);
-      if (c.z >= 0) acc[2] = fmaf(v.z, ld_x(x + c.z), acc[2]);
-      if (c.w >= 0) acc[3] = fmaf(v.w, ld_x(x + c.w), acc[3]);
+      const Vec4<T> v = ld4_stream(v4);
+      if (c.x >= 0) acc[0] = fma_t(v.x, ld_x(x + c.x), acc[0]);
+      if (c.y >= 0) acc[1] = fma_t(v.y, ld_x(x + c.y), acc[1]);
+      if (c.z >= 0) acc[2] = fma_t(v.z, ld_x(x + c.z), acc[2]);
+      if (c.w >= 0) acc[3] = fma_t(v.w, ld_x(x + c.w), acc[3]);
     }
   } else {
     // the last, partial section (h % 4 != 0), or S % 4 != 0
@@ -765,8 +773,8 @@ __device__ __forceinline__ void sell_rows(const int* __restrict__ col,
       for (int u = 0; u < 4; ++u) {
         if (u < n) {
           const int c = ld_stream(col + o + u);
-          const float v = ld_stream(val + o + u);
-          if (c >= 0) acc[u] = fmaf(v, ld_x(x + c), acc[u]);
+          const T v = ld_stream(val + o + u);
+          if (c >= 0) acc[u] = fma_t(v, ld_x(x + c), acc[u]);
         }
       }
     }
@@ -785,17 +793,17 @@ __device__ __forceinline__ void sell_perm(const int* __restrict__ perm, int s0, 
   }
 }
 
-template <bool VEC>
+template <class T, bool VEC>
 __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, int mainBlocks,
                                                       const int* __restrict__ secPtr,
                                                       const int* __restrict__ perm,
                                                       const int* __restrict__ col,
-                                                      const float* __restrict__ val,
+                                                      const T* __restrict__ val,
                                                       const SellItem* __restrict__ items,
-                                                      int nItems, const float* __restrict__ x,
-                                                      float* __restrict__ y) {
+                                                      int nItems, const T* __restrict__ x,
+                                                      T* __restrict__ y) {
   constexpr int kRows = VEC ? 4 : 1;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  T acc[4] = {T(0), T(0), T(0), T(0)};
   int r[4];
   if ((int)blockIdx.x < mainBlocks) {
     const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -810,11 +818,11 @@ __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, i
     const int base = __ldg(secPtr + k);
     const int end = __ldg(secPtr + k + 1);
     sell_perm<VEC>(perm, s0, n, r);
-    float y0[4];
+    T y0[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) y0[u] = u < n ? y[r[u]] : 0.f;
+    for (int u = 0; u < 4; ++u) y0[u] = u < n ? y[r[u]] : T(0);
     const int w = end <= slots ? (end - base) / h : 0;  // never past the arrays
-    sell_rows<VEC>(col, val, x, base, h, s0 - k0, n, 0, min(w, kSellMainSlots), acc);
+    sell_rows<T, VEC>(col, val, x, base, h, s0 - k0, n, 0, min(w, kSellMainSlots), acc);
     const bool atomic = w > kSellMainSlots;  // tail items add to these rows too
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -839,16 +847,17 @@ __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, i
     const int end = __ldg(secPtr + it.k + 1);
     if (end > slots || it.t1 > (end - base) / h) return;  // item beyond its section
     sell_perm<VEC>(perm, k0 + j, n, r);
-    sell_rows<VEC>(col, val, x, base, h, j, n, it.t0, it.t1, acc);
+    sell_rows<T, VEC>(col, val, x, base, h, j, n, it.t0, it.t1, acc);
 #pragma unroll
     for (int u = 0; u < 4; ++u)
       if (u < n) atomicAdd(y + r[u], acc[u]);
   }
 }
 
+template <class T>
 cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
-                             const int* sellCol, const float* sellVal, const SellItem* items,
-                             int nItems, const float* x, float* y, cudaStream_t s) {
+                             const int* sellCol, const T* sellVal, const SellItem* items,
+                             int nItems, const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || S <= 0) return cudaSuccess;
   const bool vec = (S & 3) == 0;
   const long long threads = vec ? ((long long)R + 3) / 4 : R;
@@ -856,11 +865,11 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
   const long long tailBlocks = ((long long)nItems + 7) / 8;
   const unsigned grid = (unsigned)(mainBlocks + tailBlocks);
   if (vec)
-    k_spmv_sell<true><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm, sellCol,
-                                           sellVal, items, nItems, x, y);
+    k_spmv_sell<T, true><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm,
+                                              sellCol, sellVal, items, nItems, x, y);
   else
-    k_spmv_sell<false><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm, sellCol,
-                                            sellVal, items, nItems, x, y);
+    k_spmv_sell<T, false><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm,
+                                               sellCol, sellVal, items, nItems, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -885,16 +894,16 @@ constexpr int kXbUnroll = 8;
 // THREADS = 1024 for the widest chunks (one CTA per SM); 512 when the chunk
 // leaves shared memory for two or more CTAs per SM, so that one CTA stages
 // its chunk while the others stream entries.
-template <int THREADS>
+template <class T, int THREADS>
 __global__ void __launch_bounds__(THREADS, 1) k_spmv_xb(int C, int B, int nch,
                                                            const int* __restrict__ chunkPtr,
                                                            const int* __restrict__ xbRow,
                                                            const unsigned short* __restrict__ xbCol,
-                                                           const float* __restrict__ xbVal,
-                                                           const float* __restrict__ x,
-                                                           float* __restrict__ y) {
-  extern __shared__ float4 sX4[];
-  float* sX = reinterpret_cast<float*>(sX4);
+                                                           const T* __restrict__ xbVal,
+                                                           const T* __restrict__ x,
+                                                           T* __restrict__ y) {
+  extern __shared__ int4 sXraw[];
+  T* sX = reinterpret_cast<T*>(sXraw);
   __shared__ int sFirst;
   const long long groups = (long long)__ldg(chunkPtr + nch) >> 2;  // slots are 4-aligned
   const long long lo = 4 * (groups * blockIdx.x / gridDim.x);
@@ -922,25 +931,27 @@ __global__ void __launch_bounds__(THREADS, 1) k_spmv_xb(int C, int B, int nch,
     const long long xb = (long long)c * B;
     const int n = (int)(C - xb < B ? C - xb : B);
     __syncthreads();
-    const float* xs = x + xb;
+    const T* xs = x + xb;
     if ((reinterpret_cast<uintptr_t>(xs) & 15) == 0) {
-      const float4* x4 = reinterpret_cast<const float4*>(xs);
-      for (int i = threadIdx.x; i < (n >> 2); i += blockDim.x) sX4[i] = __ldg(x4 + i);
-      for (int i = (n & ~3) + threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
+      // 16-byte copies of the chunk's bytes, then the remaining elements
+      constexpr int kPer16 = 16 / sizeof(T);
+      const int4* x16 = reinterpret_cast<const int4*>(xs);
+      for (int i = threadIdx.x; i < n / kPer16; i += blockDim.x) sXraw[i] = __ldg(x16 + i);
+      for (int i = n / kPer16 * kPer16 + threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
     } else {
       for (int i = threadIdx.x; i < n; i += blockDim.x) sX[i] = __ldg(xs + i);
     }
     __syncthreads();
     for (long long e0 = s0 + (long long)warp * kStep; e0 < s1; e0 += (long long)nWarps * kStep) {
       int row[kXbUnroll];
-      float val[kXbUnroll];
+      T val[kXbUnroll];
       int col[kXbUnroll];
 #pragma unroll
       for (int j = 0; j < kXbUnroll; ++j) {
         const long long e = e0 + 32 * j + lane;
         const bool in = e < s1;
         row[j] = in ? __ldcs(xbRow + e) : -1;
-        val[j] = in ? __ldcs(xbVal + e) : 0.f;
+        val[j] = in ? __ldcs(xbVal + e) : T(0);
         col[j] = in ? (int)__ldcs(xbCol + e) : 0;
       }
 #pragma unroll
@@ -950,11 +961,12 @@ __global__ void __launch_bounds__(THREADS, 1) k_spmv_xb(int C, int B, int nch,
   }
 }
 
+template <class T>
 cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int* xbRow,
-                           const unsigned short* xbCol, const float* xbVal, const float* x,
-                           float* y, cudaStream_t s) {
+                           const unsigned short* xbCol, const T* xbVal, const T* x,
+                           T* y, cudaStream_t s) {
   if (nch <= 0) return cudaSuccess;
-  const size_t smem = ((size_t)B * sizeof(float) + 15) / 16 * 16;
+  const size_t smem = ((size_t)B * sizeof(T) + 15) / 16 * 16;
   const bool wide = smem > 100 * 1024;  // one CTA per SM
   // per device and variant: the dynamic shared-memory limit raised once,
   // and the blocks per SM for the last chunk size seen
@@ -966,12 +978,12 @@ cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int
   cudaGetDevice(&dev);
   const bool cache = dev >= 0 && dev < kDevs;
   const int v = wide ? 1 : 0;
-  const void* fn = wide ? reinterpret_cast<const void*>(k_spmv_xb<1024>)
-                        : reinterpret_cast<const void*>(k_spmv_xb<512>);
+  const void* fn = wide ? reinterpret_cast<const void*>(k_spmv_xb<T, 1024>)
+                        : reinterpret_cast<const void*>(k_spmv_xb<T, 512>);
   const int threads = wide ? 1024 : 512;
   if (!cache || !raised[v][dev]) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kXbDefaultChunk * sizeof(float)));
+                                         (int)kXbSmemBytes);
     if (e != cudaSuccess) return e;
     if (cache) raised[v][dev] = true;
   }
@@ -989,11 +1001,32 @@ cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int
   }
   const unsigned grid = (unsigned)(perSm * num_sms());
   if (wide)
-    k_spmv_xb<1024><<<grid, 1024, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
+    k_spmv_xb<T, 1024><<<grid, 1024, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
   else
-    k_spmv_xb<512><<<grid, 512, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
+    k_spmv_xb<T, 512><<<grid, 512, smem, s>>>(C, B, nch, chunkPtr, xbRow, xbCol, xbVal, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
+
+// the two value types
+#define SPMV_INSTANTIATE(T)                                                                     \
+  template cudaError_t launch_spmv_csr<T>(int, int, const int*, const int*, const T*,          \
+                                          const CsrChunkDesc*, const T*, T*, int*, bool,       \
+                                          cudaStream_t);                                        \
+  template cudaError_t launch_spmv_coo<T>(int, const int*, const int*, const T*, const T*, T*, \
+                                          bool, cudaStream_t);                                  \
+  template cudaError_t launch_spmv_ell<T>(int, int, const int*, const T*, const T*, T*,        \
+                                          cudaStream_t);                                        \
+  template cudaError_t launch_spmv_jds<T>(int, int, int, int, const int*, const int*,          \
+                                          const int*, const T*, const T*, T*, cudaStream_t);    \
+  template cudaError_t launch_spmv_sell<T>(int, int, int, const int*, const int*, const int*,  \
+                                           const T*, const SellItem*, int, const T*, T*,        \
+                                           cudaStream_t);                                       \
+  template cudaError_t launch_spmv_xb<T>(int, int, int, const int*, const int*,                \
+                                         const unsigned short*, const T*, const T*, T*,         \
+                                         cudaStream_t);
+SPMV_INSTANTIATE(float)
+SPMV_INSTANTIATE(double)
+#undef SPMV_INSTANTIATE
 
 }  // namespace spmv
