@@ -62,6 +62,9 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
+# nominal fp64 rate of a GB300 (the vector unit; no tensor fp64 path)
+FP64_NOMINAL_GFLOPS = 1250.0
+
 # (call, kernel): the kernel with the largest share of the step's ncu launch list
 DOMINANT = ("convert_ell", "k_csr_to_ell")
 
@@ -85,8 +88,10 @@ def traffic_record(workload, kernel):
         return None
 
 
-def compulsory_bytes(R, C, Z):
-    return 8 * Z + 12 * R + 4 * C
+def compulsory_bytes(R, C, Z, vb=4):
+    """Bytes an SpMV must move with vb-byte values: value + column per
+    nonzero, rowPtrs and y read + write per row, x once."""
+    return (vb + 4) * Z + (4 + 2 * vb) * R + vb * C
 
 
 def call_bytes(name, R, C, Z, K_ell, K_hyb, hyb_tail):
@@ -348,11 +353,13 @@ def run_kernels(args, device):
     inp = synth.make_workload(args.workload, seed=0)
     R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
     stream = torch.cuda.current_stream(device)
+    vdt = np.float64 if args.dtype == "f64" else np.float32
+    vb = np.dtype(vdt).itemsize
     rp = torch.from_numpy(inp.row_ptrs).to(device)
     ci = torch.from_numpy(inp.col_idx).to(device)
-    va = torch.from_numpy(inp.value).to(device)
-    x = torch.from_numpy(inp.x).to(device)
-    y = torch.from_numpy(inp.y0).to(device)
+    va = torch.from_numpy(inp.value.astype(vdt)).to(device)
+    x = torch.from_numpy(inp.x.astype(vdt)).to(device)
+    y = torch.from_numpy(inp.y0.astype(vdt)).to(device)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
     peak, peak_kind = load_peaks()
@@ -389,14 +396,18 @@ def run_kernels(args, device):
                 if rep >= args.warmup:
                     times.append(e0.elapsed_time(e1))
             ms = float(np.median(times))
-            gbs = compulsory_bytes(R, C, Z) / (ms * 1e-3) / 1e9
+            gbs = compulsory_bytes(R, C, Z, vb) / (ms * 1e-3) / 1e9
+            gflops = 2 * Z / (ms * 1e-3) / 1e9
             out[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
-                      "frac": round(gbs / peak, 4), "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1),
+                      "frac": round(gbs / peak, 4), "GFLOP/s": round(gflops, 1),
                       "convert_us": conv_us.get(f)}
+            if vb == 8:  # fp64 multiply-adds against the nominal 1.25 TFLOP/s fp64 rate
+                out[f]["fp64_frac_nominal"] = round(gflops / FP64_NOMINAL_GFLOPS, 4)
             if f in ("ELL", "HYB", "SELL", "XBLOCK"):
                 out[f]["slots"] = sp.spmv_export(m.handle, f)["ell_slots"]
         sel = m.select()
-    return {"mode": "kernels", "workload": args.workload, "rows": R, "nnz": Z,
+    return {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
+            "nnz": Z,
             "l2_flush_bytes": int(flush.numel() * 4), "reps": args.reps, "peak": peak,
             "peak_kind": peak_kind, "auto": sel, "kernels": out}
 
@@ -588,6 +599,8 @@ def main():
                     help="step: the whole path (default); kernels: per-format SpMV, cold L2; "
                          "cg: conjugate-gradient iterations/s")
     ap.add_argument("--cg-iters", type=int, default=200)
+    ap.add_argument("--dtype", choices=["f32", "f64"], default="f32",
+                    help="--mode kernels: value and vector type")
     ap.add_argument("--chunk-cols", type=int, default=0,
                     help="XBLOCK chunk width B (0: the library default)")
     ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL,XBLOCK")
