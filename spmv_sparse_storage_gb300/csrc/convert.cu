@@ -298,15 +298,17 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int s
     hist[(long long)d * nTiles + blockIdx.x] = sCount[d];
 }
 
-// Stable scatter: rank of each item among equal digits = tile offset (from the
-// scanned histogram) + items of earlier rounds + earlier warps of this round +
-// earlier lanes of this warp (found with a warp match). Per round, the warp
-// leaders record their counts, then one thread per digit turns them into
-// per-warp starting positions (and advances the digit's running count), so
-// each item reads a single shared value. All keys are loaded before the first
-// round. The last pass also writes the inverse permutation (invOut[row] =
-// sorted position) when invOut is given; keysOut may be null when the sorted
-// keys are not needed.
+// Stable scatter. Warp w of a tile owns the tile's items [256w, 256w + 256)
+// (8 rounds of 32 consecutive items, all loaded before the first is used).
+// Rank of an item among equal digits = tile offset (from the scanned
+// histogram) + items of that digit in earlier warps + earlier rounds of this
+// warp + earlier lanes of this round (warp match). Each warp first counts its
+// own digits in a warp-private shared-memory row, one pass over the digits
+// turns the rows into starting positions, and each warp then walks its items
+// again, advancing its private cursors: two block barriers per tile. The
+// last pass also writes the inverse permutation (invOut[item] = sorted
+// position) when invOut is given; keysOut may be null when the sorted keys
+// are not needed.
 template <class In>
 __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, int shift, int nTiles,
                                                                 const int* __restrict__ offs,
@@ -314,58 +316,55 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, in
                                                                 int* __restrict__ valsOut,
                                                                 int* __restrict__ invOut) {
   constexpr int kWarps = kSortThreads / 32;
-  __shared__ int sRun[kRadix];              // running count per digit in this tile
-  __shared__ int sWarp[2][kWarps][kRadix];  // per round (alternating): counts, then starts
+  constexpr int kPerWarp = kSortTile / kWarps;  // = 32 * kSortRounds
+  __shared__ int sCur[kWarps][kRadix];          // counts, then running positions
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
-    sRun[d] = offs[(long long)d * nTiles + blockIdx.x];
-#pragma unroll
-    for (int q = 0; q < kWarps; ++q) {
-      sWarp[0][q][d] = 0;
-      sWarp[1][q][d] = 0;
-    }
-  }
-  const long long base = (long long)blockIdx.x * kSortTile;
-  int key[kSortRounds], val[kSortRounds];
+  for (int d = lane; d < kRadix; d += 32) sCur[w][d] = 0;
+  const long long wbase = (long long)blockIdx.x * kSortTile + (long long)w * kPerWarp;
+  int key[kSortRounds], val[kSortRounds], digit[kSortRounds];
 #pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
-    const long long i = base + rd * kSortThreads + threadIdx.x;
+    const long long i = wbase + rd * 32 + lane;
     key[rd] = 0;
     val[rd] = 0;
     if (i < R) in.get(i, key[rd], val[rd]);
+    digit[rd] = i < R ? (key[rd] >> shift) & (kRadix - 1) : kRadix;  // kRadix: no one shares
+  }
+  __syncwarp();
+  // this warp's count of every digit
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const unsigned peers = __match_any_sync(kFullMask, digit[rd]);
+    if (digit[rd] < kRadix && lane == __ffs(peers) - 1) sCur[w][digit[rd]] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // counts -> where each warp's items of each digit start
+  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
+    int run = offs[(long long)d * nTiles + blockIdx.x];
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+      const int cnt = sCur[q][d];
+      sCur[q][d] = run;
+      run += cnt;
+    }
   }
   __syncthreads();
 #pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
-    int(*cur)[kRadix] = sWarp[rd & 1];
-    int(*nxt)[kRadix] = sWarp[(rd + 1) & 1];
-    const long long i = base + rd * kSortThreads + threadIdx.x;
-    const bool valid = i < R;
-    const int digit = valid ? (key[rd] >> shift) & (kRadix - 1) : kRadix;  // kRadix: no one shares
-    const unsigned peers = __match_any_sync(kFullMask, digit);
-    const int rankInWarp = __popc(peers & lanemask_lt());
-    if (valid && lane == __ffs(peers) - 1) cur[w][digit] = __popc(peers);
-    __syncthreads();
-    // counts -> starting positions; clear the other buffer for the next round
-    // (its readers, the previous round, finished before the barrier above)
-    for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
-      int run = sRun[d];
-#pragma unroll
-      for (int q = 0; q < kWarps; ++q) {
-        const int cnt = cur[q][d];
-        cur[q][d] = run;  // where warp q's items of digit d start
-        run += cnt;
-        nxt[q][d] = 0;
-      }
-      sRun[d] = run;
-    }
-    __syncthreads();
+    const int dg = digit[rd];
+    const unsigned peers = __match_any_sync(kFullMask, dg);
+    const bool valid = dg < kRadix;
+    const int start = valid ? sCur[w][dg] : 0;
+    __syncwarp();
     if (valid) {
-      const int pos = cur[w][digit] + rankInWarp;
+      const int pos = start + __popc(peers & lanemask_lt());
       if (keysOut) keysOut[pos] = key[rd];
       valsOut[pos] = val[rd];
       if (invOut) invOut[val[rd]] = pos;
+      if (lane == __ffs(peers) - 1) sCur[w][dg] = start + __popc(peers);
     }
+    __syncwarp();
   }
 }
 
