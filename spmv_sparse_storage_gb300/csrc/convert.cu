@@ -186,6 +186,69 @@ __global__ void __launch_bounds__(kScanThreads) k_scan_block_sums(int* sums, lon
   }
 }
 
+// In-place exclusive scan of a small array (n <= kSmallScan) by one block of
+// 1024 threads, 8192 entries per pass: coalesced loads into shared memory, 8
+// consecutive entries per thread summed there, a block scan of the thread
+// totals, the exclusive prefixes written back to shared memory, coalesced
+// stores.
+constexpr int kSmallScanThreads = 1024;
+constexpr int kSmallScanItems = 8;
+constexpr int kSmallScanPass = kSmallScanThreads * kSmallScanItems;
+__global__ void __launch_bounds__(kSmallScanThreads) k_scan_small(int* __restrict__ a, int n) {
+  __shared__ int sVal[kSmallScanPass];
+  __shared__ int sWarp[kSmallScanThreads / 32];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int carry = 0;
+  for (int base0 = 0; base0 < n; base0 += kSmallScanPass) {
+#pragma unroll
+    for (int k = 0; k < kSmallScanItems; ++k) {
+      const int i = k * kSmallScanThreads + threadIdx.x;
+      sVal[i] = base0 + i < n ? a[base0 + i] : 0;
+    }
+    __syncthreads();
+    int v[kSmallScanItems];
+    int sum = 0;
+#pragma unroll
+    for (int i = 0; i < kSmallScanItems; ++i) {
+      v[i] = sVal[threadIdx.x * kSmallScanItems + i];
+      sum += v[i];
+    }
+    int inc = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFullMask, inc, off);
+      if (lane >= off) inc += o;
+    }
+    if (lane == 31) sWarp[w] = inc;
+    __syncthreads();
+    if (w == 0) {
+      int x = sWarp[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(kFullMask, x, off);
+        if (lane >= off) x += o;
+      }
+      sWarp[lane] = x;  // inclusive over warps
+    }
+    __syncthreads();
+    int ex = carry + (w > 0 ? sWarp[w - 1] : 0) + inc - sum;
+    const int total = sWarp[kSmallScanThreads / 32 - 1];
+#pragma unroll
+    for (int i = 0; i < kSmallScanItems; ++i) {
+      sVal[threadIdx.x * kSmallScanItems + i] = ex;
+      ex += v[i];
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kSmallScanItems; ++k) {
+      const int i = k * kSmallScanThreads + threadIdx.x;
+      if (base0 + i < n) a[base0 + i] = sVal[i];
+    }
+    carry += total;
+    __syncthreads();  // sVal and sWarp are reused by the next pass
+  }
+}
+
 template <class In>
 __global__ void __launch_bounds__(kScanThreads) k_scan_apply(In in, long long n, const int* blockOffs,
                                                              int* out) {
@@ -230,6 +293,7 @@ constexpr int kSortRounds = 8;
 constexpr int kSortTile = kSortThreads * kSortRounds;  // rows per tile
 constexpr int kRadixBits = 8;
 constexpr int kRadix = 1 << kRadixBits;
+constexpr long long kSmallScan = 32768;  // histograms up to this size: one-block scan
 
 // Key sources of the radix sort: pass 0 derives (key, item) from the input,
 // later passes read the previous pass's output (keysIn/valsIn).
@@ -271,10 +335,10 @@ struct ChunkKeyIn {
 // All of a thread's keys are loaded before any is counted; equal digits in a
 // warp are counted with one shared atomic (warp match).
 template <class In>
-__global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int shift, int nTiles,
-                                                             int* __restrict__ hist) {
+__global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int shift, int nBuckets,
+                                                             int nTiles, int* __restrict__ hist) {
   __shared__ int sCount[kRadix];
-  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) sCount[d] = 0;
+  for (int d = threadIdx.x; d < nBuckets; d += kSortThreads) sCount[d] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const long long base = (long long)blockIdx.x * kSortTile;
@@ -289,12 +353,12 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int s
 #pragma unroll
   for (int rd = 0; rd < kSortRounds; ++rd) {
     const long long i = base + rd * kSortThreads + threadIdx.x;
-    const int digit = i < R ? (key[rd] >> shift) & (kRadix - 1) : kRadix;
+    const int digit = i < R ? (key[rd] >> shift) & (nBuckets - 1) : kRadix;
     const unsigned peers = __match_any_sync(kFullMask, digit);
     if (digit < kRadix && lane == __ffs(peers) - 1) atomicAdd(&sCount[digit], __popc(peers));
   }
   __syncthreads();
-  for (int d = threadIdx.x; d < kRadix; d += kSortThreads)
+  for (int d = threadIdx.x; d < nBuckets; d += kSortThreads)
     hist[(long long)d * nTiles + blockIdx.x] = sCount[d];
 }
 
@@ -310,7 +374,8 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_hist(In in, int R, int s
 // position) when invOut is given; keysOut may be null when the sorted keys
 // are not needed.
 template <class In>
-__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, int shift, int nTiles,
+__global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, int shift,
+                                                                int nBuckets, int nTiles,
                                                                 const int* __restrict__ offs,
                                                                 int* __restrict__ keysOut,
                                                                 int* __restrict__ valsOut,
@@ -319,7 +384,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, in
   constexpr int kPerWarp = kSortTile / kWarps;  // = 32 * kSortRounds
   __shared__ int sCur[kWarps][kRadix];          // counts, then running positions
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  for (int d = lane; d < kRadix; d += 32) sCur[w][d] = 0;
+  for (int d = lane; d < nBuckets; d += 32) sCur[w][d] = 0;
   const long long wbase = (long long)blockIdx.x * kSortTile + (long long)w * kPerWarp;
   int key[kSortRounds], val[kSortRounds], digit[kSortRounds];
 #pragma unroll
@@ -328,7 +393,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, in
     key[rd] = 0;
     val[rd] = 0;
     if (i < R) in.get(i, key[rd], val[rd]);
-    digit[rd] = i < R ? (key[rd] >> shift) & (kRadix - 1) : kRadix;  // kRadix: no one shares
+    digit[rd] = i < R ? (key[rd] >> shift) & (nBuckets - 1) : kRadix;  // kRadix: no one shares
   }
   __syncwarp();
   // this warp's count of every digit
@@ -340,7 +405,7 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, in
   }
   __syncthreads();
   // counts -> where each warp's items of each digit start
-  for (int d = threadIdx.x; d < kRadix; d += kSortThreads) {
+  for (int d = threadIdx.x; d < nBuckets; d += kSortThreads) {
     int run = offs[(long long)d * nTiles + blockIdx.x];
 #pragma unroll
     for (int q = 0; q < kWarps; ++q) {
@@ -511,13 +576,24 @@ static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scrat
     in.keysIn = kIn;
     in.valsIn = vIn;
     const int shift = p * kRadixBits;
-    k_radix_hist<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, (int)nTiles, hist);
+    // only the buckets this pass's digit can take (the last digit may be narrower)
+    const int digitBits = bits - shift < kRadixBits ? (bits - shift > 0 ? bits - shift : 0)
+                                                     : kRadixBits;
+    const int nBuckets = 1 << digitBits;
+    const long long nhp = (long long)nBuckets * nTiles;
+    k_radix_hist<<<(unsigned)nTiles, kSortThreads, 0, s>>>(in, R, shift, nBuckets, (int)nTiles,
+                                                           hist);
     note_launches(1);
-    err = exclusive_scan(ArrayIn{hist}, nh, hist, scanScratch, s);
-    if (err != cudaSuccess) return err;
+    if (nhp <= kSmallScan) {  // one block scans the whole histogram in place
+      k_scan_small<<<1, kSmallScanThreads, 0, s>>>(hist, (int)nhp);
+      note_launches(1);
+    } else {
+      err = exclusive_scan(ArrayIn{hist}, nhp, hist, scanScratch, s);
+      if (err != cudaSuccess) return err;
+    }
     const bool last = p == passes - 1;
     k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(
-        in, R, shift, (int)nTiles, hist, (last && !needKeys) ? nullptr : kBuf[outSlot],
+        in, R, shift, nBuckets, (int)nTiles, hist, (last && !needKeys) ? nullptr : kBuf[outSlot],
         vBuf[outSlot], last ? inv : nullptr);
     note_launches(1);
     kIn = kBuf[outSlot];
