@@ -77,7 +77,7 @@ typedef enum {
   SPMV_ERR_NOT_CONVERTED = -5,    /* spmv_run/export of a format not converted yet */
   SPMV_ERR_CUDA = -6,             /* a CUDA runtime call failed (see spmv_last_cuda_error) */
   SPMV_ERR_ALLOC = -7,            /* device allocation failed or exceeded the set limit */
-  SPMV_ERR_TIMEOUT = -8           /* reserved: a bounded device wait gave up */
+  SPMV_ERR_TIMEOUT = -8           /* reserved (no kernel of this library waits on another) */
 } spmv_status;
 
 /* Row-length statistics computed on the device by spmv_create_csr
@@ -305,7 +305,7 @@ int spmv_destroy(spmv_handle h);
  *   Concurrency: every call reuses the same array, so calls that overlap on
  *   the GPU (different streams, no ordering between them) race and give
  *   wrong results; calls ordered on one stream are fine.
- *   Asynchronous on `stream`; launches 3 kernels and 1 memset. */
+ *   Asynchronous on `stream`; launches 3 kernels. */
 int spmv_run_csr_noalloc(int32_t numRows, int32_t numCols, int32_t nnz,
                          const int32_t *d_rowPtrs, const int32_t *d_colIdx,
                          const float *d_value, const float *d_x, float *d_y, void *stream);

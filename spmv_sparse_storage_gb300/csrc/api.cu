@@ -158,7 +158,6 @@ struct spmv_handle_s {
   // CSR: nnz-balanced split, one warp per kCsrChunk nonzeros (computed at creation)
   int nChunks = 0;
   spmv::CsrChunkDesc* chunkDesc = nullptr;  // one record per kCsrChunk nonzeros
-  int* devStatus = nullptr;                  // set by kernels whose bounded waits time out
   std::vector<Buf> csrBufs;
 
   // COO (shares colIdx/value with the caller's CSR arrays)
@@ -386,10 +385,6 @@ int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
   // (which checks bounds, so it stays in bounds even if validation fails)
   h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
   st = alloc_typed(h, (long long)h->nChunks, s, &h->chunkDesc, h->csrBufs);
-  if (st != SPMV_OK) return fail(st);
-  st = alloc_typed(h, 1, s, &h->devStatus, h->csrBufs);
-  if (st != SPMV_OK) return fail(st);
-  st = record(cudaMemsetAsync(h->devStatus, 0, sizeof(int), s));
   if (st != SPMV_OK) return fail(st);
   if (h->nChunks > 0) {  // masks and flags are OR-ed into zeroed records
     st = record(cudaMemsetAsync(h->chunkDesc, 0, sizeof(spmv::CsrChunkDesc) * h->nChunks, s));
@@ -859,9 +854,8 @@ int run_format(spmv_handle h, spmv_format format, const T* d_x, T* d_y, cudaStre
   const T* value = cval<T>(h->value);
   switch (format) {
     case SPMV_CSR:
-      return record(spmv::launch_spmv_csr<T>(
-          h->R, h->Z, h->rowPtrs, h->colIdx, value, h->chunkDesc, d_x, d_y, h->devStatus,
-          h->stats.gather_lines > 0.0 && h->stats.gather_lines <= spmv::kCsrPipelineMaxLines, s));
+      return record(spmv::launch_spmv_csr<T>(h->R, h->Z, h->rowPtrs, h->colIdx, value,
+                                             h->chunkDesc, d_x, d_y, s));
     case SPMV_COO:
       return record(spmv::launch_spmv_coo<T>(h->Z, h->cooRow, h->colIdx, value, d_x, d_y, false,
                                              s));

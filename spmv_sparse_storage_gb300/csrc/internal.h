@@ -62,13 +62,6 @@ struct __align__(16) CsrChunkDesc {
   uint4 mask;  // bit p: a row other than lo starts at position p of the chunk
 };
 constexpr int kCsrChunkHasEmptyRow = 1;
-constexpr int kCsrConsumerWarps = 16;              // per block, one chunk each per stage
-constexpr int kCsrGroupChunks = kCsrConsumerWarps;  // chunks moved by one stage
-constexpr int kCsrStages = 4;                       // stages in flight per block
-// Gathers of x touching at most this many distinct 128-byte lines per 32
-// lanes (banded matrices) use the shared-memory pipeline; more scattered
-// gathers are limited by the L1 and use one warp per chunk.
-constexpr double kCsrPipelineMaxLines = 12.0;
 constexpr int kGatherSampleBlocks = 64;  // blocks of the column check that sample gathers
 
 constexpr int kJdsSplitMinWidth = 8192;  // diagonals at least this wide run thread-per-row
@@ -145,7 +138,7 @@ cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks
 template <class T>
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const T* value, const CsrChunkDesc* desc, const T* x,
-                            T* y, int* devStatus, bool pipelined, cudaStream_t s);
+                            T* y, cudaStream_t s);
 template <class T>
 cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const T* value,
                             const T* x, T* y, bool dependent, cudaStream_t s);

@@ -17,34 +17,26 @@ namespace spmv {
 namespace {
 
 // Shared scratch: one record per kCsrChunk nonzeros, at most
-// kNoAllocMaxChunks of them (1 MiB per GPU that loads the library), plus a
-// status word. Every call overwrites what it uses; calls that overlap on the
-// GPU race on it.
+// kNoAllocMaxChunks of them (1 MiB per GPU that loads the library). Every
+// call overwrites what it uses; calls that overlap on the GPU race on it.
 constexpr int kNoAllocMaxChunks = 32768;  // nnz <= 4,194,304
 static __device__ __align__(256) CsrChunkDesc g_noallocDesc[kNoAllocMaxChunks];
-static __device__ __align__(256) int g_noallocStatus[64];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setupMu;
 CsrChunkDesc* g_descPtr[kMaxDevices] = {};
-int* g_statusPtr[kMaxDevices] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device (the host-side symbols are stand-ins, not device addresses).
-cudaError_t scratch_for_device(int dev, CsrChunkDesc** desc, int** status) {
+// device (the host-side symbol is a stand-in, not a device address).
+cudaError_t scratch_for_device(int dev, CsrChunkDesc** desc) {
   std::lock_guard<std::mutex> lk(g_setupMu);
   if (!g_descPtr[dev]) {
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_noallocDesc);
     if (e != cudaSuccess) return e;
-    void* q = nullptr;
-    e = cudaGetSymbolAddress(&q, g_noallocStatus);
-    if (e != cudaSuccess) return e;
     g_descPtr[dev] = static_cast<CsrChunkDesc*>(p);
-    g_statusPtr[dev] = static_cast<int*>(q);
   }
   *desc = g_descPtr[dev];
-  *status = g_statusPtr[dev];
   return cudaSuccess;
 }
 
@@ -80,12 +72,9 @@ extern "C" int spmv_run_csr_noalloc(int32_t numRows, int32_t numCols, int32_t nn
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPMV_ERR_CUDA;
   CsrChunkDesc* desc = nullptr;
-  int* status = nullptr;
-  e = scratch_for_device(dev, &desc, &status);
+  e = scratch_for_device(dev, &desc);
   if (e != cudaSuccess) return SPMV_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  e = cudaMemsetAsync(status, 0, sizeof(int), s);
-  if (e != cudaSuccess) return SPMV_ERR_CUDA;
   k_noalloc_chunk_lo<<<(unsigned)(((long long)numRows + 255) / 256), 256, 0, s>>>(
       numRows, nnz, d_rowPtrs, (int)nChunks, desc);
   note_launches(1);
@@ -93,7 +82,6 @@ extern "C" int spmv_run_csr_noalloc(int32_t numRows, int32_t numCols, int32_t nn
   if (e != cudaSuccess) return SPMV_ERR_CUDA;
   e = launch_csr_chunk_masks(numRows, nnz, d_rowPtrs, (int)nChunks, desc, s);
   if (e != cudaSuccess) return SPMV_ERR_CUDA;
-  e = launch_spmv_csr(numRows, nnz, d_rowPtrs, d_colIdx, d_value, desc, d_x, d_y, status,
-                      /*pipelined=*/false, s);
+  e = launch_spmv_csr(numRows, nnz, d_rowPtrs, d_colIdx, d_value, desc, d_x, d_y, s);
   return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
 }

@@ -16,31 +16,16 @@
 namespace spmv {
 namespace {
 
-// ===========================================================================
-// Warp-level segmented add. Each lane holds 4 consecutive entries of a
-// 128-entry chunk (entry 4*lane + e): their row `row[e]` (-1 = no entry) and
-// product `p[e]`. Runs of equal row are summed inside the lane, then across
-// lanes with a segmented shuffle scan, and each run is added into y with ONE
-// atomicAdd (a fire-and-forget reduction in L2). Only adjacent equal rows
-// merge, so any entry order is correct; rows grouped together give one
-// atomic per row per chunk. `waitFirst`: wait for the preceding kernel of the
-// stream (programmatic dependent launch) before the first write to y.
-// ===========================================================================
+// Across lanes: each lane holds a run of consecutive entries summarised as
+// its head run (row rh, sum sh), its tail run (row rt, sum st) and whether
+// the whole lane is one run (single); runs strictly inside a lane are the
+// caller's. Adds the head and tail runs into y, joining runs that continue
+// across lanes with a segmented shuffle scan, one atomicAdd per joined run.
 template <class T>
-__device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T (&p)[4],
-                                                   T* __restrict__ y, bool waitFirst) {
+__device__ __forceinline__ void warp_join_runs(int rh, int rt, T sh, T st, bool single,
+                                               T* __restrict__ y, bool waitFirst) {
   const int lane = threadIdx.x & 31;
-  // in-lane run sums: s[e] = sum of the run that ends at e
-  T s[4];
-  s[0] = p[0];
-#pragma unroll
-  for (int e = 1; e < 4; ++e) s[e] = (row[e] == row[e - 1]) ? s[e - 1] + p[e] : p[e];
-  const int hEnd = row[1] != row[0] ? 0 : row[2] != row[1] ? 1 : row[3] != row[2] ? 2 : 3;
-  const bool single = (hEnd == 3);
-  const int rh = row[0], rt = row[3];
-  const T sh = s[hEnd], st = s[3];
-
-  // across lanes: w = tail-run sum carried to the right while lanes continue one run
+  // w = tail-run sum carried to the right while lanes continue one run
   const int prevRt = __shfl_up_sync(kFullMask, rt, 1);
   const bool connected = lane > 0 && prevRt == rh;
   const unsigned heads = __ballot_sync(kFullMask, !(single && connected));
@@ -61,10 +46,35 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T 
     if (tailEnds && rt >= 0) atomicAdd(y + rt, st + carryIn);
   } else {
     if (rh >= 0) atomicAdd(y + rh, sh + carryIn);
+    if (tailEnds && rt >= 0) atomicAdd(y + rt, st);
+  }
+}
+
+// ===========================================================================
+// Warp-level segmented add. Each lane holds 4 consecutive entries of a
+// 128-entry chunk (entry 4*lane + e): their row `row[e]` (-1 = no entry) and
+// product `p[e]`. Runs of equal row are summed inside the lane, then across
+// lanes with a segmented shuffle scan, and each run is added into y with ONE
+// atomicAdd (a fire-and-forget reduction in L2). Only adjacent equal rows
+// merge, so any entry order is correct; rows grouped together give one
+// atomic per row per chunk. `waitFirst`: wait for the preceding kernel of the
+// stream (programmatic dependent launch) before the first write to y.
+// ===========================================================================
+template <class T>
+__device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T (&p)[4],
+                                                   T* __restrict__ y, bool waitFirst) {
+  // in-lane run sums: s[e] = sum of the run that ends at e
+  T s[4];
+  s[0] = p[0];
+#pragma unroll
+  for (int e = 1; e < 4; ++e) s[e] = (row[e] == row[e - 1]) ? s[e - 1] + p[e] : p[e];
+  const int hEnd = row[1] != row[0] ? 0 : row[2] != row[1] ? 1 : row[3] != row[2] ? 2 : 3;
+  const bool single = (hEnd == 3);
+  warp_join_runs(row[0], row[3], s[hEnd], s[3], single, y, waitFirst);
+  if (!single) {
 #pragma unroll
     for (int e = 1; e < 3; ++e)  // runs strictly inside the lane
       if (e > hEnd && row[e] != row[e + 1] && row[e] >= 0) atomicAdd(y + row[e], s[e]);
-    if (tailEnds && rt >= 0) atomicAdd(y + rt, st);
   }
 }
 
@@ -85,14 +95,6 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T 
 // the number of mask bits at positions <= p (popcounts), so the kernel reads
 // 0.25 byte of index per nonzero and never waits on rowPtrs; a chunk in
 // which an empty row sits (flagged) binary-searches rowPtrs instead.
-//
-// Streaming: a block keeps kCsrStages groups of kCsrGroupChunks chunks in
-// flight with bulk (TMA) copies into shared memory, so the bytes in flight
-// per SM are set by shared memory, not by registers, and each copy is large
-// (8 KiB) so that the copy engine's per-operation cost stays small.
-// Each chunk: lane l takes entries 4l..4l+3, gathers x, and the warp sums
-// runs of equal row with a segmented shuffle scan, one atomicAdd per row
-// per chunk (warp_segmented_add): no warp waits on a read of y.
 // ===========================================================================
 
 // Row of each of the lane's 4 entries (entries at or beyond Z get -1).
@@ -143,127 +145,116 @@ __device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long 
   }
 }
 
-// One stage: kCsrGroupChunks consecutive chunks (colIdx, value, records).
-struct __align__(128) CsrGroupStage {
-  int col[kCsrGroupChunks * kCsrChunk];
-  float val[kCsrGroupChunks * kCsrChunk];
-  CsrChunkDesc desc[kCsrGroupChunks];
-};
-constexpr unsigned kCsrStageBytes = sizeof(CsrGroupStage);
-constexpr size_t kCsrTmaSmemBytes = kCsrStages * sizeof(CsrGroupStage) + 2 * kCsrStages * 8;
+// The CSR kernel: kCsrLane = 8 consecutive entries per lane. A warp takes
+// 256 nonzeros (two chunks); lane l takes the entries at 8l, which sit in
+// chunk l/16 at position 8(l%16): one byte of one mask word. The lane's
+// first row is lo + the set bits up to that position, and the row advances
+// at every further set bit. Runs of equal row are summed in the lane
+// with one multiply-add per entry (a run that starts and ends inside the lane
+// goes to y directly), and the lane's head and tail runs are joined across
+// lanes once per 256 entries (warp_join_runs). The decode, the join and the
+// loop are paid once per 8 entries and the accumulation is one fused
+// multiply-add per entry, so the kernel is not bound by instruction issue
+// (with 4 entries per lane it was, in a shared-memory (bulk copy) pipeline as
+// well: 214 warp instructions per 128 entries). Loads are direct 16-byte
+// vectors. A chunk that holds an empty row is decoded by a binary search on
+// rowPtrs.
+constexpr int kCsrLane = 8;
+constexpr int kCsrSuper = 32 * kCsrLane;             // entries per warp
+constexpr int kCsrLanesPerChunk = kCsrChunk / kCsrLane;
 
-// TMA-fed kernel over groups of kCsrGroupChunks full chunks (g < nGroups);
-// needs 16-byte aligned colIdx and value. A producer warp fills kCsrStages
-// shared-memory stages with three bulk copies each (8 KiB + 8 KiB + 512 B)
-// and kCsrConsumerWarps consumer warps take one chunk each per stage; full
-// and empty mbarriers hand the stages back and forth. Blocks take groups
-// blockIdx.x, blockIdx.x + gridDim.x, ... (a persistent grid over all SMs).
-// Every wait is bounded: on timeout the block records it in devStatus and
-// stops.
-__global__ void __launch_bounds__((kCsrConsumerWarps + 1) * 32, 3) k_spmv_csr_tma(
-    int Z, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
-    const float* __restrict__ value, const CsrChunkDesc* __restrict__ desc, int nGroups,
-    const float* __restrict__ x, float* __restrict__ y, int* __restrict__ devStatus) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  CsrGroupStage* stage = reinterpret_cast<CsrGroupStage*>(smem);
-  uint64_t* fullBar = reinterpret_cast<uint64_t*>(smem + kCsrStages * sizeof(CsrGroupStage));
-  uint64_t* emptyBar = fullBar + kCsrStages;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const long long G = gridDim.x;
-  const long long nk = nGroups > blockIdx.x ? (nGroups - blockIdx.x + G - 1) / G : 0;
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kCsrStages; ++s) {
-      mbar_init(&fullBar[s], 1);
-      mbar_init(&emptyBar[s], kCsrConsumerWarps);
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (nk == 0) return;  // block-uniform
-
-  if (warp == kCsrConsumerWarps) {
-    // producer
-    if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
-      for (long long k = 0; k < nk; ++k) {
-        const int s = (int)(k % kCsrStages);
-        if (k >= kCsrStages &&
-            !mbar_wait_bounded(&emptyBar[s], (unsigned)(((k / kCsrStages) - 1) & 1))) {
-          atomicOr(devStatus, 1);
-          break;
-        }
-        const long long g = blockIdx.x + k * G;
-        const long long c0 = g * kCsrGroupChunks;
-        mbar_arrive_expect_tx(&fullBar[s], kCsrStageBytes);
-        bulk_g2s(stage[s].col, colIdx + c0 * kCsrChunk, kCsrGroupChunks * kCsrChunk * 4,
-                 &fullBar[s], pol);
-        bulk_g2s(stage[s].val, value + c0 * kCsrChunk, kCsrGroupChunks * kCsrChunk * 4,
-                 &fullBar[s], pol);
-        bulk_g2s(stage[s].desc, desc + c0, kCsrGroupChunks * sizeof(CsrChunkDesc), &fullBar[s],
-                 pol);
-      }
-    }
-    return;
-  }
-  // consumers: warp `warp` takes chunk `warp` of every stage
-  for (long long k = 0; k < nk; ++k) {
-    const int s = (int)(k % kCsrStages);
-    if (!mbar_wait_bounded(&fullBar[s], (unsigned)((k / kCsrStages) & 1))) {
-      if (lane == 0) atomicOr(devStatus, 1);
-      break;
-    }
-    const int4 c4 = reinterpret_cast<const int4*>(stage[s].col + warp * kCsrChunk)[lane];
-    const float4 v4 = reinterpret_cast<const float4*>(stage[s].val + warp * kCsrChunk)[lane];
-    const CsrChunkDesc d = stage[s].desc[warp];
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&emptyBar[s]);  // the stage may be refilled
-    const long long c = (blockIdx.x + k * G) * kCsrGroupChunks + warp;
-    float p[4];
-    p[0] = v4.x * ld_x(x + c4.x);
-    p[1] = v4.y * ld_x(x + c4.y);
-    p[2] = v4.z * ld_x(x + c4.z);
-    p[3] = v4.w * ld_x(x + c4.w);
-    int row[4];
-    csr_chunk_rows(d, c * kCsrChunk, lane, Z, rowPtrs, row);
-    warp_segmented_add(row, p, y, false);
-  }
-}
-
-// Chunks [c0, c1) with plain loads: the partial last chunk, and every chunk
-// when colIdx/value are not 16-byte aligned. One warp per chunk.
 template <class T, bool VEC>
-__global__ void __launch_bounds__(256) k_spmv_csr_plain(int Z, long long c0, long long c1,
-                                                        const int* __restrict__ rowPtrs,
-                                                        const int* __restrict__ colIdx,
-                                                        const T* __restrict__ value,
-                                                        const CsrChunkDesc* __restrict__ desc,
-                                                        const T* __restrict__ x,
-                                                        T* __restrict__ y) {
+__global__ void __launch_bounds__(256) k_spmv_csr_wide(int Z, const int* __restrict__ rowPtrs,
+                                                       const int* __restrict__ colIdx,
+                                                       const T* __restrict__ value,
+                                                       const CsrChunkDesc* __restrict__ desc,
+                                                       const T* __restrict__ x,
+                                                       T* __restrict__ y) {
   const int lane = threadIdx.x & 31;
-  const long long c = c0 + (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if (c >= c1) return;  // warp-uniform
-  const long long cb = c * kCsrChunk;
-  const long long base = cb + 4 * lane;
-  const CsrChunkDesc d = desc[c];
-  T p[4];
-  if (VEC && base + 4 <= Z) {
-    const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base));
-    const Vec4<T> v4 = ld4_stream(value + base);
-    p[0] = v4.x * ld_x(x + c4.x);
-    p[1] = v4.y * ld_x(x + c4.y);
-    p[2] = v4.z * ld_x(x + c4.z);
-    p[3] = v4.w * ld_x(x + c4.w);
+  const long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (g * kCsrSuper >= Z) return;  // warp-uniform
+  const long long base = g * kCsrSuper + (long long)lane * kCsrLane;
+  const bool any = base < Z;
+  const bool full = base + kCsrLane <= Z;
+  // the lane's chunk record (chunk index < nChunks whenever base < Z)
+  CsrChunkDesc d = {};
+  if (any) d = desc[(g * kCsrSuper + (long long)lane * kCsrLane) / kCsrChunk];
+  int col[kCsrLane];
+  T val[kCsrLane];
+  if (VEC && full) {
+#pragma unroll
+    for (int q = 0; q < kCsrLane / 4; ++q) {
+      const int4 c4 = ld_stream(reinterpret_cast<const int4*>(colIdx + base) + q);
+      col[4 * q] = c4.x; col[4 * q + 1] = c4.y; col[4 * q + 2] = c4.z; col[4 * q + 3] = c4.w;
+      const Vec4<T> v4 = ld4_stream(value + base + 4 * q);
+      val[4 * q] = v4.x; val[4 * q + 1] = v4.y; val[4 * q + 2] = v4.z; val[4 * q + 3] = v4.w;
+    }
   } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const long long k = base + e;
-      p[e] = k < Z ? ld_stream(value + k) * ld_x(x + ld_stream(colIdx + k)) : T(0);
+    for (int e = 0; e < kCsrLane; ++e) {
+      const bool in = base + e < Z;
+      col[e] = in ? ld_stream(colIdx + base + e) : 0;
+      val[e] = in ? ld_stream(value + base + e) : T(0);
     }
   }
-  int row[4];
-  csr_chunk_rows(d, cb, lane, Z, rowPtrs, row);
-  warp_segmented_add(row, p, y, false);
+  // rows of the 16 entries (-1 past nnz)
+  int row[kCsrLane];
+  if (!(d.flags & kCsrChunkHasEmptyRow)) {
+    const int q0 = kCsrLane * (lane % kCsrLanesPerChunk);  // position in the chunk
+    const int wd = q0 >> 5;
+    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
+    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
+                       (wd > 2 ? __popc(d.mask.z) : 0);
+    const int sh = q0 & 31;  // the lane's entries are bits sh .. sh + kCsrLane - 1 of mw
+    int r = d.lo + before + __popc(mw & ((2u << sh) - 1u));
+    const unsigned bits = mw >> sh;
+#pragma unroll
+    for (int e = 0; e < kCsrLane; ++e) {
+      if (e > 0) r += (bits >> e) & 1u;
+      row[e] = (full || base + e < Z) ? r : -1;
+    }
+  } else {
+    const int hi = d.hi;
+    int r = d.lo;
+    if (any) {
+      int b = hi;
+      while (r < b) {
+        const int m = (r + b + 1) >> 1;
+        if (__ldg(rowPtrs + m) <= (int)base) r = m; else b = m - 1;
+      }
+    }
+    int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+#pragma unroll
+    for (int e = 0; e < kCsrLane; ++e) {
+      const long long k = base + e;
+      while (k >= nextStart) {  // skips empty rows; bounded by hi
+        ++r;
+        nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+      }
+      row[e] = k < Z ? r : -1;
+    }
+  }
+  // gathers, all issued before the multiply-adds
+  T xg[kCsrLane];
+#pragma unroll
+  for (int e = 0; e < kCsrLane; ++e) xg[e] = row[e] >= 0 ? ld_x(x + col[e]) : T(0);
+  // runs inside the lane
+  T run = T(0), head = T(0);
+  bool boundary = false;
+#pragma unroll
+  for (int e = 0; e < kCsrLane; ++e) {
+    const bool cont = e == 0 || row[e] == row[e - 1];
+    if (!cont) {
+      if (boundary) {
+        if (row[e - 1] >= 0) atomicAdd(y + row[e - 1], run);  // a row that ended in the lane
+      } else {
+        head = run;
+        boundary = true;
+      }
+    }
+    run = fma_t(val[e], xg[e], cont ? run : T(0));
+  }
+  warp_join_runs(row[0], row[kCsrLane - 1], boundary ? head : run, run, !boundary, y, false);
 }
 
 // CSR -> COO ("Sparse Matrices and Basic Formats ...", section "COO format
@@ -613,48 +604,16 @@ cudaError_t launch_csr_chunk_masks(int R, int Z, const int* rowPtrs, int nChunks
 template <class T>
 cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
                             const T* value, const CsrChunkDesc* desc, const T* x,
-                            T* y, int* devStatus, bool pipelined, cudaStream_t s) {
+                            T* y, cudaStream_t s) {
   if (Z <= 0 || R <= 0) return cudaSuccess;
-  const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long nGroups = (long long)Z / ((long long)kCsrGroupChunks * kCsrChunk);
   const bool vec = aligned16(colIdx) && aligned16(value);
-  // the shared-memory pipeline stages 4-byte values; 8-byte values take the
-  // direct-load kernel
-  const bool tma = std::is_same<T, float>::value && pipelined && vec && nGroups > 0;
-  int n = 0;
-  if constexpr (std::is_same<T, float>::value) {
-   if (tma) {
-    static int perSm = 0;  // blocks per SM (same on every device of one architecture)
-    if (perSm == 0) {
-      int v = 0;
-      if (cudaFuncSetAttribute(k_spmv_csr_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kCsrTmaSmemBytes) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_spmv_csr_tma,
-                                                        (kCsrConsumerWarps + 1) * 32,
-                                                        kCsrTmaSmemBytes) != cudaSuccess)
-        v = 1;
-      perSm = v < 1 ? 1 : v;
-    }
-    long long blocks = (long long)perSm * num_sms();
-    if (blocks > nGroups) blocks = nGroups;
-    k_spmv_csr_tma<<<(unsigned)blocks, (kCsrConsumerWarps + 1) * 32, kCsrTmaSmemBytes, s>>>(
-        Z, rowPtrs, colIdx, value, desc, (int)nGroups, x, y, devStatus);
-    ++n;
-   }
-  }
-  const long long p0 = tma ? nGroups * kCsrGroupChunks : 0;
-  if (p0 < nChunks) {
-    const long long warps = nChunks - p0;
-    const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
-    if (vec)
-      k_spmv_csr_plain<T, true><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
-                                                       desc, x, y);
-    else
-      k_spmv_csr_plain<T, false><<<blocks, 256, 0, s>>>(Z, p0, nChunks, rowPtrs, colIdx, value,
-                                                        desc, x, y);
-    ++n;
-  }
-  note_launches(n);
+  const long long warps = ((long long)Z + kCsrSuper - 1) / kCsrSuper;
+  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  if (vec)
+    k_spmv_csr_wide<T, true><<<blocks, 256, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
+  else
+    k_spmv_csr_wide<T, false><<<blocks, 256, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
+  note_launches(1);
   return cudaGetLastError();
 }
 
@@ -1011,8 +970,7 @@ cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int
 // the two value types
 #define SPMV_INSTANTIATE(T)                                                                     \
   template cudaError_t launch_spmv_csr<T>(int, int, const int*, const int*, const T*,          \
-                                          const CsrChunkDesc*, const T*, T*, int*, bool,       \
-                                          cudaStream_t);                                        \
+                                          const CsrChunkDesc*, const T*, T*, cudaStream_t);    \
   template cudaError_t launch_spmv_coo<T>(int, const int*, const int*, const T*, const T*, T*, \
                                           bool, cudaStream_t);                                  \
   template cudaError_t launch_spmv_ell<T>(int, int, const int*, const T*, const T*, T*,        \
