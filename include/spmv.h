@@ -219,7 +219,10 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void *stream);
  * d_x: numCols floats, d_y: numRows floats, both on the handle's device;
  * x and y must not overlap (SPMV_ERR_INVALID_ARG). The format must have been
  * converted (SPMV_CSR always is), else SPMV_ERR_NOT_CONVERTED; nothing is
- * converted implicitly. Asynchronous on `stream`; launches 1 kernel
+ * converted implicitly. Allocates nothing and never synchronises, so it can
+ * be captured into a CUDA graph (after one call outside capture for each
+ * format on each device, which sets kernel attributes once) and replayed.
+ * Asynchronous on `stream`; launches 1 kernel
  * (CSR, COO, ELL, JDS, SELL, XBLOCK) or 2 (HYB: ELL part, then the COO part with a
  * programmatic dependent launch). Floating-point rounding differs from a
  * sequential sum (tree and atomic reductions); per row the result is within

@@ -62,6 +62,29 @@ def test_noalloc_matches_handle_path(sp, orc, name):
         assert ok, (name, call, worst)
 
 
+def test_noalloc_replays_from_a_cuda_graph(sp, orc):
+    """The reason the entry point allocates nothing: it can be captured into
+    a CUDA graph (after one call outside capture has looked up its scratch
+    array) and replayed; three replays add 3 A x."""
+    inp = CASES["irregular"]()
+    rp, ci, va, x = dev(inp.row_ptrs), dev(inp.col_idx), dev(inp.value), dev(inp.x)
+    yref, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    ax = yref - inp.y0.astype(np.float64)
+    y = dev(inp.y0)
+    sp.spmv_run_csr_noalloc(inp.num_rows, inp.num_cols, inp.nnz, rp, ci, va, x, y)
+    torch.cuda.synchronize()
+    y.copy_(dev(inp.y0))
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sp.spmv_run_csr_noalloc(inp.num_rows, inp.num_cols, inp.nnz, rp, ci, va, x, y)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    ok, worst = oracle.within_tolerance(y.cpu().numpy(), inp.y0 + 3 * ax, 3 * mag)
+    assert ok, worst
+
+
 def test_noalloc_rejects_too_large(sp):
     lib = sp._lib
     st = lib.spmv_run_csr_noalloc(1, 1, MAX_NNZ + 1, ctypes.c_void_p(8), ctypes.c_void_p(8),
