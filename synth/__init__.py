@@ -267,6 +267,23 @@ def spd_random(seed: int, n: int, pairs_per_row: float = 3.0, name: str = "spd_r
                     v_all[order].astype(np.float32), x, y0)
 
 
+def hashed_entries(k0: int, k1: int, num_cols: int):
+    """Columns and values of nonzeros k0 .. k1-1 of a large matrix defined by
+    closed forms (no stored randomness, so any slice can be made on demand):
+    column = (k * 40503 + 17) mod numCols, value = ((k * 2246822519) mod 65521)
+    / 65521 - 0.5 in float32."""
+    k = np.arange(k0, k1, dtype=np.int64)
+    col = ((k * 40503 + 17) % num_cols).astype(np.int32)
+    val = (((k * 2246822519) % 65521).astype(np.float64) / 65521.0 - 0.5).astype(np.float32)
+    return col, val
+
+
+def hashed_vector(n: int, salt: int) -> np.ndarray:
+    """x or y0 of the large matrix: ((i * 1103515245 + salt) mod 4093) / 4093 - 0.5."""
+    i = np.arange(n, dtype=np.int64)
+    return (((i * 1103515245 + salt) % 4093).astype(np.float64) / 4093.0 - 0.5).astype(np.float32)
+
+
 WORKLOADS = {
     "tiny_uniform": lambda seed=0: uniform_rows("tiny_uniform", 4096, 8, seed),
     "laplace2d": lambda seed=0: laplace2d(2048, seed),
