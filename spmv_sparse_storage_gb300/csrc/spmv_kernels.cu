@@ -97,54 +97,6 @@ __device__ __forceinline__ void warp_segmented_add(const int (&row)[4], const T 
 // which an empty row sits (flagged) binary-searches rowPtrs instead.
 // ===========================================================================
 
-// Row of each of the lane's 4 entries (entries at or beyond Z get -1).
-__device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long cb, int lane,
-                                               int Z, const int* __restrict__ rowPtrs,
-                                               int (&row)[4]) {
-  const long long base = cb + 4 * lane;
-  if (!(d.flags & kCsrChunkHasEmptyRow)) {
-    // entries 4*lane .. 4*lane+3 sit in mask word lane/8, bits 4*(lane%8)+e:
-    // row of entry 0 = lo + set bits up to it, then +1 at every later set bit
-    const int wd = lane >> 3;
-    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
-    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
-                       (wd > 2 ? __popc(d.mask.z) : 0);
-    const int b0 = 4 * (lane & 7);
-    const unsigned nib = mw >> b0;  // this lane's 4 bits at the bottom
-    int r = d.lo + before + __popc(mw & ((2u << b0) - 1u));
-    row[0] = base < Z ? r : -1;
-#pragma unroll
-    for (int e = 1; e < 4; ++e) {
-      r += (nib >> e) & 1u;
-      row[e] = base + e < Z ? r : -1;
-    }
-  } else {
-    // a chunk holding empty rows: binary search on rowPtrs, then walk
-    const int hi = d.hi;
-    int r = d.lo;
-    if (base < Z) {
-      int b = hi;
-      while (r < b) {
-        const int m = (r + b + 1) >> 1;
-        if (__ldg(rowPtrs + m) <= (int)base)
-          r = m;
-        else
-          b = m - 1;
-      }
-    }
-    int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const long long k = base + e;
-      while (k >= nextStart) {  // skips empty rows; bounded by hi
-        ++r;
-        nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-      }
-      row[e] = k < Z ? r : -1;
-    }
-  }
-}
-
 // The CSR kernel: kCsrLane = 8 consecutive entries per lane. A warp takes
 // 256 nonzeros (two chunks); lane l takes the entries at 8l, which sit in
 // chunk l/16 at position 8(l%16): one byte of one mask word. The lane's
@@ -162,6 +114,51 @@ __device__ __forceinline__ void csr_chunk_rows(const CsrChunkDesc& d, long long 
 constexpr int kCsrLane = 8;
 constexpr int kCsrSuper = 32 * kCsrLane;             // entries per warp
 constexpr int kCsrLanesPerChunk = kCsrChunk / kCsrLane;
+
+// Rows of a lane's kCsrLane consecutive entries starting at `base`, which
+// sit in chunk base / kCsrChunk at position kCsrLane * (lane % 16): one byte
+// of one mask word (the row advances at every set bit after lo + the set
+// bits up to that position). Entries at or past Z get -1. A chunk holding an
+// empty row is decoded by a binary search on rowPtrs instead.
+__device__ __forceinline__ void lane_rows(const CsrChunkDesc& d, long long base, int lane, int Z,
+                                          const int* __restrict__ rowPtrs, int (&row)[kCsrLane]) {
+  const bool full = base + kCsrLane <= Z;
+  if (!(d.flags & kCsrChunkHasEmptyRow)) {
+    const int q0 = kCsrLane * (lane % kCsrLanesPerChunk);  // position in the chunk
+    const int wd = q0 >> 5;
+    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
+    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
+                       (wd > 2 ? __popc(d.mask.z) : 0);
+    const int sh = q0 & 31;  // the lane's entries are bits sh .. sh + kCsrLane - 1 of mw
+    int r = d.lo + before + __popc(mw & ((2u << sh) - 1u));
+    const unsigned bits = mw >> sh;
+#pragma unroll
+    for (int e = 0; e < kCsrLane; ++e) {
+      if (e > 0) r += (bits >> e) & 1u;
+      row[e] = (full || base + e < Z) ? r : -1;
+    }
+  } else {
+    const int hi = d.hi;
+    int r = d.lo;
+    if (base < Z) {
+      int b = hi;
+      while (r < b) {
+        const int m = (r + b + 1) >> 1;
+        if (__ldg(rowPtrs + m) <= (int)base) r = m; else b = m - 1;
+      }
+    }
+    int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+#pragma unroll
+    for (int e = 0; e < kCsrLane; ++e) {
+      const long long k = base + e;
+      while (k >= nextStart) {  // skips empty rows; bounded by hi
+        ++r;
+        nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
+      }
+      row[e] = k < Z ? r : -1;
+    }
+  }
+}
 
 template <class T, bool VEC>
 __global__ void __launch_bounds__(256) k_spmv_csr_wide(int Z, const int* __restrict__ rowPtrs,
@@ -197,43 +194,9 @@ __global__ void __launch_bounds__(256) k_spmv_csr_wide(int Z, const int* __restr
       val[e] = in ? ld_stream(value + base + e) : T(0);
     }
   }
-  // rows of the 16 entries (-1 past nnz)
+  // rows of the lane's entries (-1 past nnz)
   int row[kCsrLane];
-  if (!(d.flags & kCsrChunkHasEmptyRow)) {
-    const int q0 = kCsrLane * (lane % kCsrLanesPerChunk);  // position in the chunk
-    const int wd = q0 >> 5;
-    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
-    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
-                       (wd > 2 ? __popc(d.mask.z) : 0);
-    const int sh = q0 & 31;  // the lane's entries are bits sh .. sh + kCsrLane - 1 of mw
-    int r = d.lo + before + __popc(mw & ((2u << sh) - 1u));
-    const unsigned bits = mw >> sh;
-#pragma unroll
-    for (int e = 0; e < kCsrLane; ++e) {
-      if (e > 0) r += (bits >> e) & 1u;
-      row[e] = (full || base + e < Z) ? r : -1;
-    }
-  } else {
-    const int hi = d.hi;
-    int r = d.lo;
-    if (any) {
-      int b = hi;
-      while (r < b) {
-        const int m = (r + b + 1) >> 1;
-        if (__ldg(rowPtrs + m) <= (int)base) r = m; else b = m - 1;
-      }
-    }
-    int nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-#pragma unroll
-    for (int e = 0; e < kCsrLane; ++e) {
-      const long long k = base + e;
-      while (k >= nextStart) {  // skips empty rows; bounded by hi
-        ++r;
-        nextStart = r < hi ? __ldg(rowPtrs + r + 1) : INT_MAX;
-      }
-      row[e] = k < Z ? r : -1;
-    }
-  }
+  lane_rows(d, base, lane, Z, rowPtrs, row);
   // gathers, all issued before the multiply-adds
   T xg[kCsrLane];
 #pragma unroll
@@ -258,37 +221,30 @@ __global__ void __launch_bounds__(256) k_spmv_csr_wide(int Z, const int* __restr
 }
 
 // CSR -> COO ("Sparse Matrices and Basic Formats ...", section "COO format
-// and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. A warp takes
-// kExpandChunks consecutive 128-entry chunks and loads all their records
-// before using any; the rows come from each record exactly as in the CSR
-// kernel, and each lane stores its 4 row ids with one 16-byte store.
-constexpr int kExpandChunks = 4;
-__global__ void __launch_bounds__(256) k_expand_rows(int Z, long long nChunks,
-                                                     const int* __restrict__ rowPtrs,
+// and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. The layout of
+// the CSR kernel: a warp takes 256 nonzeros, each lane 8 consecutive ones,
+// decodes their rows from its chunk record (lane_rows) and stores them with
+// two 16-byte stores (VEC: rowIdx is 16-byte aligned).
+template <bool VEC>
+__global__ void __launch_bounds__(256) k_expand_rows(int Z, const int* __restrict__ rowPtrs,
                                                      const CsrChunkDesc* __restrict__ desc,
                                                      int* __restrict__ rowIdx) {
   const int lane = threadIdx.x & 31;
-  const long long c0 = (((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5) * kExpandChunks;
-  if (c0 >= nChunks) return;  // warp-uniform
-  CsrChunkDesc d[kExpandChunks];
+  const long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (g * kCsrSuper >= Z) return;  // warp-uniform
+  const long long base = g * kCsrSuper + (long long)lane * kCsrLane;
+  if (base >= Z) return;  // no shuffles below: lanes may leave
+  const CsrChunkDesc d = desc[base / kCsrChunk];
+  int row[kCsrLane];
+  lane_rows(d, base, lane, Z, rowPtrs, row);
+  if (VEC && base + kCsrLane <= Z) {
+    int4* out = reinterpret_cast<int4*>(rowIdx + base);
+    __stcs(out, make_int4(row[0], row[1], row[2], row[3]));
+    __stcs(out + 1, make_int4(row[4], row[5], row[6], row[7]));
+  } else {
 #pragma unroll
-  for (int u = 0; u < kExpandChunks; ++u)
-    d[u] = desc[c0 + u < nChunks ? c0 + u : nChunks - 1];
-#pragma unroll
-  for (int u = 0; u < kExpandChunks; ++u) {
-    const long long c = c0 + u;
-    if (c >= nChunks) break;  // warp-uniform
-    const long long cb = c * kCsrChunk;
-    const long long base = cb + 4 * lane;
-    int row[4];
-    csr_chunk_rows(d[u], cb, lane, Z, rowPtrs, row);
-    if (base + 4 <= Z) {
-      __stcs(reinterpret_cast<int4*>(rowIdx + base), make_int4(row[0], row[1], row[2], row[3]));
-    } else {
-#pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (base + e < Z) rowIdx[base + e] = row[e];
-    }
+    for (int e = 0; e < kCsrLane; ++e)
+      if (base + e < Z) rowIdx[base + e] = row[e];
   }
 }
 
@@ -584,10 +540,12 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
 cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
                                int* rowIdx, cudaStream_t s) {
   if (R <= 0 || Z <= 0) return cudaSuccess;
-  const long long nChunks = ((long long)Z + kCsrChunk - 1) / kCsrChunk;
-  const long long warps = (nChunks + kExpandChunks - 1) / kExpandChunks;
-  k_expand_rows<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(Z, nChunks, rowPtrs, desc,
-                                                                      rowIdx);
+  const long long warps = ((long long)Z + kCsrSuper - 1) / kCsrSuper;
+  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  if (aligned16(rowIdx))
+    k_expand_rows<true><<<grid, 256, 0, s>>>(Z, rowPtrs, desc, rowIdx);
+  else
+    k_expand_rows<false><<<grid, 256, 0, s>>>(Z, rowPtrs, desc, rowIdx);
   note_launches(1);
   return cudaGetLastError();
 }

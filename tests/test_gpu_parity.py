@@ -407,6 +407,19 @@ def test_sell_section_heights_and_wide_sections(sp, orc):
     check_matrix(sp, orc, big, formats=("SELL",), sell_rows=(0, 4, 7, 128))
 
 
+@pytest.mark.parametrize("max_len", [1, 63, 64, 65, 200, 255, 256])
+def test_length_sort_pass_boundary(sp, orc, max_len):
+    """Longest row on both sides of 256 (the row sort by length takes one
+    8-bit radix pass below it, two from it) and of 64 (rows longer than that
+    are copied by the whole warp), over several 2048-row sort tiles with a
+    ragged last tile: JDS and SELL arrays bit-exact, perm included."""
+    inp = synth.random_csr(70 + max_len, 7001, 9000, mean_len=0 if max_len < 8 else 4,
+                           empty_frac=0.1, long_rows=37, long_len=max_len,
+                           name=f"sort_boundary_{max_len}")
+    assert int(np.diff(inp.row_ptrs).max()) == max_len
+    check_matrix(sp, orc, inp, formats=("JDS", "SELL"), sell_rows=(0, 3, 128))
+
+
 def test_xblock_chunkings(sp, orc):
     """Chunk widths that are and are not multiples of 4 (x staged with 16-byte
     or scalar loads), numCols not a multiple of B, empty chunks, rows spread
