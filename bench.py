@@ -386,9 +386,10 @@ def run_ours(args, rank, world, device):
 
 
 def run_kernels(args, device):
-    """Per-format SpMV timing on one workload: each rep flushes L2 (writes a
-    buffer of twice its size) outside the timed events, then times one
-    spmv_run with CUDA events on the launching stream; median over reps."""
+    """Per-format SpMV timing on one workload: each rep resets y to y0 and
+    flushes L2 (writes a buffer of twice its size, then reads another, so that
+    L2 is left clean) outside the timed events, then times one spmv_run with
+    CUDA events on the launching stream; median over reps."""
     import torch
     import spmv_sparse_storage_gb300 as sp
     inp = synth.make_workload(args.workload, seed=0)
@@ -400,9 +401,16 @@ def run_kernels(args, device):
     ci = torch.from_numpy(inp.col_idx).to(device)
     va = torch.from_numpy(inp.value.astype(vdt)).to(device)
     x = torch.from_numpy(inp.x.astype(vdt)).to(device)
-    y = torch.from_numpy(inp.y0.astype(vdt)).to(device)
+    y0 = torch.from_numpy(inp.y0.astype(vdt)).to(device)
+    y = y0.clone()
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    # cold L2 before every run: write a buffer of twice the L2 size, then read
+    # another one, so that L2 holds clean lines of neither the matrix nor the
+    # vectors (after the write alone, up to the whole L2 is dirty and the timed
+    # kernel pays its write-back: 34-40 MB more DRAM writes, ELL on stencil27
+    # 143 -> 158 us)
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+    flush_clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
     peak, peak_kind = load_peaks()
     out = {}
     with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
@@ -412,6 +420,7 @@ def run_kernels(args, device):
             try:
                 m.convert(f, stream=stream, chunk_cols=args.chunk_cols)  # warm (pool, launches)
                 flush.fill_(-1.0)
+                flush_clean.sum()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -427,7 +436,9 @@ def run_kernels(args, device):
                 continue
             times = []
             for rep in range(args.warmup + args.reps):
+                y.copy_(y0)  # y = y0 before every run, outside the events
                 flush.fill_(float(rep))
+                flush_clean.sum()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -447,10 +458,16 @@ def run_kernels(args, device):
             if f in ("ELL", "HYB", "SELL", "XBLOCK"):
                 out[f]["slots"] = sp.spmv_export(m.handle, f)["ell_slots"]
         sel = m.select()
-    return {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
+    line = {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
             "nnz": Z,
-            "l2_flush_bytes": int(flush.numel() * 4), "reps": args.reps, "peak": peak,
+            "l2_flush": f"write {flush.numel() * 4} B, then read another {flush.numel() * 4} B "
+                        "(clean L2), before every run, outside the events",
+            "reps": args.reps, "peak": peak,
             "peak_kind": peak_kind, "auto": sel, "kernels": out}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = time_oracle_spmv(inp, inp.value.astype(vdt), inp.x.astype(vdt),
+                                                inp.y0.astype(vdt))
+    return line
 
 
 def cg_alg_bytes(R, slots):
@@ -578,6 +595,48 @@ def row_sample(inp, rows):
                           inp.value[:end].copy(), inp.x, inp.y0[:rows].copy())
 
 
+def host_cpu():
+    """The host's core count and CPU model (lscpu's "Model name", else the
+    platform's processor string), for labelling single-core oracle timings."""
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        import platform
+        model = platform.processor() or platform.machine()
+    return {"host_cores": os.cpu_count(), "cpu_model": model}
+
+
+def time_oracle_spmv(inp, value, x, y0, reps=3):
+    """The fp64 CSR SpMV oracle (plain C, one thread) on the whole matrix:
+    median of `reps` runs, as effective GB/s of the same compulsory bytes."""
+    import oracle
+    orc = oracle.get()
+    f64 = value.dtype == np.float64
+    times = []
+    for _ in range(reps):
+        t = time.perf_counter()
+        if f64:
+            orc.spmv_csr_f64(inp.row_ptrs, inp.col_idx, value, x, y0)
+        else:
+            orc.spmv_csr(inp.row_ptrs, inp.col_idx, value, x, y0)
+        times.append(time.perf_counter() - t)
+    s_med = float(np.median(times))
+    vb = 8 if f64 else 4
+    gbs = compulsory_bytes(inp.num_rows, inp.num_cols, inp.nnz, vb) / s_med / 1e9
+    host = host_cpu()
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"the whole matrix, CSR SpMV only, median of {reps} runs "
+                      f"(1 core of {host['host_cores']})",
+            "us": round(s_med * 1e6, 1), "GFLOP/s": round(2 * inp.nnz / s_med / 1e9, 4), **host}
+
+
 def time_oracle(inp, budget_s, max_steps=None):
     import oracle
     orc = oracle.get()
@@ -601,7 +660,7 @@ def time_oracle(inp, budget_s, max_steps=None):
     return {"value": round(b / step_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"rows [0, {sample.num_rows}) of {inp.name} ({sample.nnz} nnz), "
                       f"whole path per step, median of {len(times)} steps",
-            "ms_per_step": round(step_s * 1e3, 3), "steps": len(times)}
+            "ms_per_step": round(step_s * 1e3, 3), "steps": len(times), **host_cpu()}
 
 
 def run_reference(args, rank, world):
