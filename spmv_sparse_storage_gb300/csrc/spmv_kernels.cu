@@ -481,18 +481,25 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // s < width(t), contiguous in s, so a warp's loads are coalesced. Widths only
 // shrink with t; the first tSplit diagonals (those at least
 // kJdsSplitMinWidth wide, at most kJdsSplitMaxDiag of them) run one thread
-// per sorted row, 4 consecutive rows per thread read with one aligned
-// 16-byte load per diagonal and array (diagonals start anywhere, so lanes
-// realign with one shuffle from the next lane; the arrays are padded so the
-// last vector stays inside). The remaining diagonals belong to the few
+// per sorted row: a warp's 32 rows of a diagonal are 32 consecutive entries,
+// so 4-byte loads are coalesced wherever the diagonal starts, and a thread
+// loads kJdsGroup<T> diagonals before it gathers any x. (4 rows per thread with
+// 16-byte loads needed a shuffle realignment per diagonal and 64 registers.)
+// The remaining diagonals belong to the few
 // longest rows (s < wTail) and would serialise one thread over thousands of
 // entries, so they are split into blocks of kJdsTailRows rows x
 // kJdsTailDiags diagonals that run in parallel and add their partial sums
 // atomically. The result of sorted row s goes straight to y[perm[s]] (the
 // page permutes the result back with the row array).
 // ===========================================================================
+// diagonals whose loads a thread issues together: 8 with 4-byte values (32
+// registers; laplace2d 45.1 us, 27-point stencil 148 us, against 53.3 and
+// 152 with 4), 5 with 8-byte values (8 needs 48 registers: 27-point stencil
+// 251 us against 227)
 template <class T>
-__global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
+constexpr int kJdsGroup = sizeof(T) == 4 ? 8 : 5;
+template <class T>
+__global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
                                                      const int* __restrict__ perm,
@@ -505,79 +512,41 @@ __global__ void __launch_bounds__(256, 4) k_spmv_jds(int R, int maxLen, int tSpl
     for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
     __syncthreads();
     const int lane = threadIdx.x & 31;
-    const long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const long long s0 = 4 * q;                                 // first of this thread's 4 rows
-    const long long warpFirst = 4 * (q - lane);                 // first row of the warp
-    const int4* col4 = reinterpret_cast<const int4*>(jdsCol);  // padded by kJdsPad entries
-    int r[4];
-    if (s0 + 4 <= R) {
-      const int4 p4 = __ldg(reinterpret_cast<const int4*>(perm) + q);
-      r[0] = p4.x; r[1] = p4.y; r[2] = p4.z; r[3] = p4.w;
-    } else {
+    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
+    const long long warpFirst = s - lane;
+    const int r = s < R ? __ldg(perm + s) : -1;
+    const T y0 = (r >= 0 && s >= wTail) ? y[r] : T(0);
+    T acc = T(0);
+    // kJdsGroup<T> diagonals at a time: all their column and value loads are
+    // issued before the gathers, and all gathers before the multiply-adds
+    for (int t0 = 0; t0 < tSplit; t0 += kJdsGroup<T>) {
+      if (warpFirst >= sIp[t0 + 1] - sIp[t0]) break;  // widths shrink
+      int c[kJdsGroup<T>];
+      T v[kJdsGroup<T>];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) r[e] = s0 + e < R ? __ldg(perm + s0 + e) : -1;
-    }
-    T y0[4], acc[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      y0[e] = (r[e] >= 0 && s0 + e >= wTail) ? y[r[e]] : T(0);
-      acc[e] = T(0);
-    }
-    for (int t = 0; t < tSplit; ++t) {
-      const int a = sIp[t];
-      const int wt = sIp[t + 1] - a;
-      if (warpFirst >= wt) break;  // widths shrink: no later diagonal reaches this warp
-      // rows s0..s0+3 of diagonal t sit at a+s0 .. a+s0+3, m entries past a
-      // 16-byte boundary (m is the same in every lane): lane q reads the
-      // aligned vector holding rows s0-m .. s0-m+3 and takes the rest from
-      // lane q+1's vector (the last lane reads that one itself)
-      const int m = a & 3;
-      const long long vi = ((long long)(a - m) >> 2) + q;
-      int4 cv = make_int4(0, 0, 0, 0);
-      Vec4<T> vv = {T(0), T(0), T(0), T(0)};
-      if (s0 - m < wt) {
-        cv = ld_stream(col4 + vi);
-        vv = ld4_stream(jdsVal + 4 * vi);
-      }
-      int cw[4];
-      T fw[4];
-      if (m == 0) {
-        cw[0] = cv.x; cw[1] = cv.y; cw[2] = cv.z; cw[3] = cv.w;
-        fw[0] = vv.x; fw[1] = vv.y; fw[2] = vv.z; fw[3] = vv.w;
-      } else {
-        int4 cn;
-        Vec4<T> vn;
-        cn.x = __shfl_down_sync(kFullMask, cv.x, 1);
-        cn.y = __shfl_down_sync(kFullMask, cv.y, 1);
-        cn.z = __shfl_down_sync(kFullMask, cv.z, 1);
-        cn.w = __shfl_down_sync(kFullMask, cv.w, 1);
-        vn.x = __shfl_down_sync(kFullMask, vv.x, 1);
-        vn.y = __shfl_down_sync(kFullMask, vv.y, 1);
-        vn.z = __shfl_down_sync(kFullMask, vv.z, 1);
-        vn.w = __shfl_down_sync(kFullMask, vv.w, 1);
-        if (lane == 31 && s0 + 4 - m < wt) {
-          cn = ld_stream(col4 + vi + 1);
-          vn = ld4_stream(jdsVal + 4 * (vi + 1));
-        }
-        const int ca[8] = {cv.x, cv.y, cv.z, cv.w, cn.x, cn.y, cn.z, cn.w};
-        const T fa[8] = {vv.x, vv.y, vv.z, vv.w, vn.x, vn.y, vn.z, vn.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          cw[e] = m == 1 ? ca[e + 1] : m == 2 ? ca[e + 2] : ca[e + 3];
-          fw[e] = m == 1 ? fa[e + 1] : m == 2 ? fa[e + 2] : fa[e + 3];
+      for (int g = 0; g < kJdsGroup<T>; ++g) {
+        const int t = t0 + g;
+        c[g] = -1;
+        v[g] = T(0);
+        if (t < tSplit) {
+          const int a = sIp[t];
+          if (s < sIp[t + 1] - a) {
+            c[g] = ld_stream(jdsCol + a + s);
+            v[g] = ld_stream(jdsVal + a + s);
+          }
         }
       }
+      T xg[kJdsGroup<T>];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (s0 + e < wt) acc[e] = fma_t(fw[e], ld_x(x + cw[e]), acc[e]);
+      for (int g = 0; g < kJdsGroup<T>; ++g) xg[g] = c[g] >= 0 ? ld_x(x + c[g]) : T(0);
+#pragma unroll
+      for (int g = 0; g < kJdsGroup<T>; ++g) acc = fma_t(v[g], xg[g], acc);
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (r[e] < 0) continue;
-      if (s0 + e < wTail)
-        atomicAdd(y + r[e], acc[e]);  // the tail blocks add to this row too
+    if (r >= 0) {
+      if (s < wTail)
+        atomicAdd(y + r, acc);  // the tail blocks add to this row too
       else
-        y[r[e]] = y0[e] + acc[e];
+        y[r] = y0 + acc;
     }
   } else {
     const int b = blockIdx.x - nMainBlocks;
@@ -688,7 +657,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
                             const int* perm, const int* jdsCol, const T* jdsVal,
                             const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
-  const long long mainBlocks = ((long long)R + 1023) / 1024;  // 4 sorted rows per thread
+  const long long mainBlocks = ((long long)R + 255) / 256;  // a sorted row per thread
   long long tailBlocks = 0;
   int tailRowBlocks = 1;
   if (tSplit < maxLen && wTail > 0) {
