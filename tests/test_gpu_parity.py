@@ -420,6 +420,15 @@ def test_length_sort_pass_boundary(sp, orc, max_len):
     check_matrix(sp, orc, inp, formats=("JDS", "SELL"), sell_rows=(0, 3, 128))
 
 
+def test_length_sort_two_scan_passes(sp, orc):
+    """5,120,077 rows of at most 7 entries: the row sort's per-tile counts
+    (8 digits x 2,501 tiles of 2048 rows = 20,008) take two passes of the
+    one-block scan, the second ragged; JDS and SELL arrays bit-exact."""
+    inp = synth.random_csr(91, 5_120_077, 7, mean_len=2, name="two_scan_passes")
+    assert int(np.diff(inp.row_ptrs).max()) == 7
+    check_matrix(sp, orc, inp, formats=("JDS", "SELL"))
+
+
 def test_xblock_chunkings(sp, orc):
     """Chunk widths that are and are not multiples of 4 (x staged with 16-byte
     or scalar loads), numCols not a multiple of B, empty chunks, rows spread
