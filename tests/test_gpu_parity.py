@@ -429,6 +429,17 @@ def test_length_sort_two_scan_passes(sp, orc):
     check_matrix(sp, orc, inp, formats=("JDS", "SELL"))
 
 
+def test_csr_large_ragged(sp, orc):
+    """CSR on 621K nonzeros (2426 full 256-entry warp blocks) with empty rows
+    (chunks decoded by search), rows spanning many blocks and nnz not a
+    multiple of 256; aligned (16-byte loads) and misaligned (scalar loads)."""
+    inp = synth.random_csr(61, 100_003, 50_000, mean_len=7, empty_frac=0.2, long_rows=3,
+                           long_len=20_000, name="csr_pipelined")
+    assert inp.nnz // 256 >= 8 * 152 and inp.nnz % 256 != 0
+    check_matrix(sp, orc, inp, formats=("CSR",))
+    check_matrix(sp, orc, inp, formats=("CSR",), offset=1)
+
+
 def test_xblock_chunkings(sp, orc):
     """Chunk widths that are and are not multiples of 4 (x staged with 16-byte
     or scalar loads), numCols not a multiple of B, empty chunks, rows spread
