@@ -697,7 +697,7 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
   if (st != SPMV_OK) return fail(st);
   // tail work items of the sections wider than kSellMainSlots (a prefix)
   std::vector<spmv::SellItem> items;
-  const int rowsPerItem = (S & 3) == 0 ? 128 : 32;
+  const int rowsPerItem = 32;  // one row per lane
   for (long long k = 0; k < nsec && width[(size_t)k] > spmv::kSellMainSlots; ++k) {
     const int wk = width[(size_t)k];
     for (int t0 = spmv::kSellMainSlots; t0 < wk; t0 += spmv::kSellTailSlots) {

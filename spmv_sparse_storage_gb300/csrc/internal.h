@@ -113,7 +113,7 @@ constexpr int kSellDefaultRows = 128;  // default section height
 constexpr int kSellMainSlots = 64;     // slots per row done by the row-parallel part
 constexpr int kSellTailSlots = 64;     // slots per row of one tail work item
 // One tail work item of a section wider than kSellMainSlots: slots [t0, t1) of
-// rows j0 .. j0 + 127 (4 per lane; 32 rows, one per lane, when S % 4 != 0).
+// rows j0 .. j0 + 31 of section k (one row per lane).
 struct SellItem {
   int k, t0, t1, j0;
 };

@@ -675,14 +675,117 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
 // ---------------------------------------------------------------------------
 // Sectioned ELL ("Regularized Formats (ELL, Hybrid ELL-COO and JDS)", section
 // "JDS format", variant paragraph). Sorted rows in sections of S; slot t of
-// row j of section k at secPtr[k] + t*h_k + j. A thread owns 4 consecutive
-// sorted rows (one when S % 4 != 0): with S % 4 == 0 every section starts on
-// a multiple of 4 slots, so a full section's 4 rows are one aligned 16-byte
-// load of columns and one of values per slot, a warp reads 512 contiguous
-// bytes per slot. Slots past kSellMainSlots of the wide sections (a prefix,
-// the rows being sorted) are cut into SellItems handled by extra warps; the
+// row j of section k at secPtr[k] + t*h_k + j. The main part takes the first
+// kSellMainSlots slots of every row, either 4 consecutive sorted rows per
+// thread with 16-byte loads (k_spmv_sell4: with S % 4 == 0 every section
+// starts on a multiple of 4 slots, so a full section's 4 rows are one aligned
+// load of columns and one of values per slot) or one row per thread
+// (k_spmv_sell1), chosen by the mean slots per row. Slots past
+// kSellMainSlots of the wide sections (a prefix, the rows being sorted) are
+// cut into SellItems of 32 rows handled by extra warps, one row per lane; the
 // rows of those sections add into y with atomics.
 // ---------------------------------------------------------------------------
+// slots whose loads a thread issues together (as kJdsGroup)
+template <class T>
+constexpr int kSellGroup = sizeof(T) == 4 ? 8 : 5;
+// mean slots per row above which the main part takes a row per thread (with
+// 4-byte values)
+constexpr int kSellRowsWide = 8;
+
+// Sum over slots [t0, t1) of the row at position j of the section starting at
+// base (height h): kSellGroup<T> slots' loads issued before their gathers;
+// padding slots (column -1) add nothing.
+template <class T>
+__device__ __forceinline__ T sell_row_slots(const int* __restrict__ col, const T* __restrict__ val,
+                                            const T* __restrict__ x, int base, int h, int j,
+                                            int t0, int t1) {
+  T acc = T(0);
+  // offsets of loaded slots stay below the slot count (< 2^31); unsigned, as
+  // the offset is advanced past the last slot and may then wrap
+  unsigned o = (unsigned)base + (unsigned)t0 * (unsigned)h + (unsigned)j;
+  for (int tg = t0; tg < t1; tg += kSellGroup<T>) {
+    int c[kSellGroup<T>];
+    T v[kSellGroup<T>];
+#pragma unroll
+    for (int g = 0; g < kSellGroup<T>; ++g) {
+      c[g] = -1;
+      v[g] = T(0);
+      if (tg + g < t1) {
+        c[g] = ld_stream(col + o);
+        v[g] = ld_stream(val + o);
+      }
+      o += (unsigned)h;
+    }
+    T xg[kSellGroup<T>];
+#pragma unroll
+    for (int g = 0; g < kSellGroup<T>; ++g) xg[g] = c[g] >= 0 ? ld_x(x + c[g]) : T(0);
+#pragma unroll
+    for (int g = 0; g < kSellGroup<T>; ++g) acc = fma_t(v[g], xg[g], acc);
+  }
+  return acc;
+}
+
+// Tail item id (slots [t0, t1) of 32 rows of a wide section, one per lane),
+// added into y atomically.
+template <class T>
+__device__ __forceinline__ void sell_tail_item(int R, int S, int slots, long long id,
+                                               const int* __restrict__ secPtr,
+                                               const int* __restrict__ perm,
+                                               const int* __restrict__ col,
+                                               const T* __restrict__ val,
+                                               const SellItem* __restrict__ items,
+                                               const T* __restrict__ x, T* __restrict__ y) {
+  const SellItem it = items[id];
+  const int k0 = it.k * S;
+  const int h = min(S, R - k0);
+  const int j = it.j0 + (threadIdx.x & 31);
+  if (j >= h) return;
+  const int base = __ldg(secPtr + it.k);
+  const int end = __ldg(secPtr + it.k + 1);
+  if (end > slots || it.t1 > (end - base) / h) return;  // item beyond its section
+  const int r = __ldg(perm + k0 + j);
+  atomicAdd(y + r, sell_row_slots(col, val, x, base, h, j, it.t0, it.t1));
+}
+
+// Main part, one sorted row per thread: a warp's rows are consecutive slots
+// of a section, so every 4-byte load is coalesced and kSellGroup<T> slots'
+// loads go out together. Chosen for more than kSellRowsWide slots per row on
+// average (27-point stencil: 153.6 us against 160.4 with 4 rows per thread;
+// the random-length workload 138 against 160).
+template <class T>
+__global__ void __launch_bounds__(256) k_spmv_sell1(int R, int S, int slots, int mainBlocks,
+                                                   const int* __restrict__ secPtr,
+                                                   const int* __restrict__ perm,
+                                                   const int* __restrict__ col,
+                                                   const T* __restrict__ val,
+                                                   const SellItem* __restrict__ items,
+                                                   int nItems, const T* __restrict__ x,
+                                                   T* __restrict__ y) {
+  if ((int)blockIdx.x < mainBlocks) {
+    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (s >= R) return;
+    const int k = (int)(s / S);
+    const int k0 = k * S;
+    const int h = min(S, R - k0);
+    // the loads that do not depend on each other first: section bounds, the
+    // row's original index, then its y value
+    const int base = __ldg(secPtr + k);
+    const int end = __ldg(secPtr + k + 1);
+    const int r = __ldg(perm + s);
+    const T y0 = y[r];
+    const int w = end <= slots ? (end - base) / h : 0;  // never past the arrays
+    const T acc = sell_row_slots(col, val, x, base, h, (int)(s - k0), 0, min(w, kSellMainSlots));
+    if (w > kSellMainSlots)
+      atomicAdd(y + r, acc);  // tail items add to this row too
+    else
+      y[r] = y0 + acc;
+  } else {
+    const long long id = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
+                         (threadIdx.x >> 5);
+    if (id < nItems) sell_tail_item(R, S, slots, id, secPtr, perm, col, val, items, x, y);
+  }
+}
+
 template <class T, bool VEC>
 __device__ __forceinline__ void sell_rows(const int* __restrict__ col,
                                           const T* __restrict__ val,
@@ -745,15 +848,19 @@ __device__ __forceinline__ void sell_perm(const int* __restrict__ perm, int s0, 
   }
 }
 
+// Main part, 4 consecutive sorted rows per thread (1 when S % 4 != 0) with
+// 16-byte loads: the section bounds, perm and y are loaded once per 4 rows.
+// Chosen for at most kSellRowsWide slots per row on average, where those
+// loads weigh most (laplace2d: 48.3 us against 61.5 with a row per thread).
 template <class T, bool VEC>
-__global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, int mainBlocks,
-                                                      const int* __restrict__ secPtr,
-                                                      const int* __restrict__ perm,
-                                                      const int* __restrict__ col,
-                                                      const T* __restrict__ val,
-                                                      const SellItem* __restrict__ items,
-                                                      int nItems, const T* __restrict__ x,
-                                                      T* __restrict__ y) {
+__global__ void __launch_bounds__(256, 4) k_spmv_sell4(int R, int S, int slots, int mainBlocks,
+                                                       const int* __restrict__ secPtr,
+                                                       const int* __restrict__ perm,
+                                                       const int* __restrict__ col,
+                                                       const T* __restrict__ val,
+                                                       const SellItem* __restrict__ items,
+                                                       int nItems, const T* __restrict__ x,
+                                                       T* __restrict__ y) {
   constexpr int kRows = VEC ? 4 : 1;
   T acc[4] = {T(0), T(0), T(0), T(0)};
   int r[4];
@@ -788,21 +895,7 @@ __global__ void __launch_bounds__(256, 4) k_spmv_sell(int R, int S, int slots, i
   } else {
     const long long id = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
                          (threadIdx.x >> 5);
-    if (id >= nItems) return;
-    const SellItem it = items[id];
-    const int k0 = it.k * S;
-    const int h = min(S, R - k0);
-    const int j = it.j0 + (threadIdx.x & 31) * kRows;
-    if (j >= h) return;
-    const int n = min(kRows, h - j);
-    const int base = __ldg(secPtr + it.k);
-    const int end = __ldg(secPtr + it.k + 1);
-    if (end > slots || it.t1 > (end - base) / h) return;  // item beyond its section
-    sell_perm<VEC>(perm, k0 + j, n, r);
-    sell_rows<T, VEC>(col, val, x, base, h, j, n, it.t0, it.t1, acc);
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      if (u < n) atomicAdd(y + r[u], acc[u]);
+    if (id < nItems) sell_tail_item(R, S, slots, id, secPtr, perm, col, val, items, x, y);
   }
 }
 
@@ -811,17 +904,24 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
                              const int* sellCol, const T* sellVal, const SellItem* items,
                              int nItems, const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || S <= 0) return cudaSuccess;
-  const bool vec = (S & 3) == 0;
-  const long long threads = vec ? ((long long)R + 3) / 4 : R;
-  const long long mainBlocks = (threads + 255) / 256;
-  const long long tailBlocks = ((long long)nItems + 7) / 8;
-  const unsigned grid = (unsigned)(mainBlocks + tailBlocks);
-  if (vec)
-    k_spmv_sell<T, true><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm,
-                                              sellCol, sellVal, items, nItems, x, y);
-  else
-    k_spmv_sell<T, false><<<grid, 256, 0, s>>>(R, S, slots, (int)mainBlocks, secPtr, perm,
-                                               sellCol, sellVal, items, nItems, x, y);
+  const long long tailBlocks = ((long long)nItems + 7) / 8;  // an item per warp
+  // 8-byte values keep 4 rows per thread (a row per thread measured 229 us
+  // against 223 on the 27-point stencil)
+  if (sizeof(T) == 4 && (long long)slots > (long long)kSellRowsWide * R) {
+    const long long mainBlocks = ((long long)R + 255) / 256;  // a sorted row per thread
+    k_spmv_sell1<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+        R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
+  } else {
+    const bool vec = (S & 3) == 0;
+    const long long threads = vec ? ((long long)R + 3) / 4 : R;
+    const long long mainBlocks = (threads + 255) / 256;
+    if (vec)
+      k_spmv_sell4<T, true><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+          R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
+    else
+      k_spmv_sell4<T, false><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+          R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
+  }
   note_launches(1);
   return cudaGetLastError();
 }

@@ -405,6 +405,14 @@ def test_sell_section_heights_and_wide_sections(sp, orc):
     big = synth.random_csr(32, 3000, 40_000, mean_len=20, long_rows=130, long_len=1500,
                            name="sell_readback")
     check_matrix(sp, orc, big, formats=("SELL",), sell_rows=(0, 4, 7, 128))
+    # few slots per row on average (the main part takes 4 rows per thread)
+    # with wide sections all the same (tail items)
+    narrow = synth.random_csr(34, 100_003, 50_000, mean_len=3, long_rows=5, long_len=1000,
+                              name="sell_narrow_wide")
+    lens = np.sort(np.diff(narrow.row_ptrs))[::-1]
+    slots = sum(min(128, lens.size - k) * int(lens[k]) for k in range(0, lens.size, 128))
+    assert slots <= 8 * narrow.num_rows
+    check_matrix(sp, orc, narrow, formats=("SELL",), sell_rows=(0, 6, 128))
 
 
 @pytest.mark.parametrize("max_len", [1, 63, 64, 65, 200, 255, 256])
