@@ -50,9 +50,19 @@ __host__ __device__ inline WorkLayout work_layout(int nbRow, int nbCol) {
   return L;
 }
 
+// Row blocks: at most kRowBlocksPerSm per SM, each walking several
+// kStatsRows-row tiles, so that a block's fixed tail (shared-memory
+// histogram, reductions, fence, ticket) is paid once per block rather than
+// once per tile.
+constexpr int kRowBlocksPerSm = 2;
+long long row_tiles(int R) {
+  const long long t = ((long long)R + kStatsRows - 1) / kStatsRows;
+  return t < 1 ? 1 : t;
+}
 int row_blocks(int R) {
-  const long long rb = ((long long)R + kStatsRows - 1) / kStatsRows;
-  return (int)(rb < 1 ? 1 : rb);
+  const long long t = row_tiles(R);
+  const long long cap = (long long)kRowBlocksPerSm * num_sms();
+  return (int)(t < cap ? t : cap);
 }
 
 int col_blocks(int Z, bool vec) {
@@ -63,16 +73,17 @@ int col_blocks(int Z, bool vec) {
   return (int)(cb < 1 ? 1 : (cb > cap ? cap : cb));
 }
 
-// Row part. A block takes kStatsRows consecutive rows, kStatsRowsPerThread
-// per thread, 256 apart so that each load is coalesced, and issues all its
-// loads before it uses any: monotonicity, lengths, min/max/sum of squares,
+// Row part. A block walks tiles blk, blk + nbRow, ... of kStatsRows
+// consecutive rows, kStatsRowsPerThread per thread, 256 apart so that each
+// load is coalesced, and issues all of a tile's loads before it uses any:
+// monotonicity, lengths, min/max/sum of squares,
 // the max nonzeros of any 32 consecutive rows, an exact length histogram
 // (lengths < kExactLenBins; longer rows go to the log2 bins), and the CSR
 // chunk records (bounds-checked: they are written before validation is
 // known). A nonempty row is `lo` of every chunk whose first nonzero it holds
 // (and `hi` of the chunk before) and sets the bit of its start position in
 // the chunk where it starts; an empty row inside a chunk flags that chunk.
-__device__ void row_part(int blk, int R, int Z, const int* __restrict__ rowPtrs,
+__device__ void row_part(int blk, int nbRow, int R, int Z, const int* __restrict__ rowPtrs,
                          DevStats* __restrict__ st, StatsPartial* __restrict__ partials,
                          unsigned* __restrict__ histRep, int nChunks,
                          CsrChunkDesc* __restrict__ desc) {
@@ -88,62 +99,65 @@ __device__ void row_part(int blk, int R, int Z, const int* __restrict__ rowPtrs,
     if (nChunks > 0) desc[nChunks - 1].hi = R > 0 ? R - 1 : 0;
   }
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const long long base = (long long)blk * kStatsRows + threadIdx.x;
-  int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
-#pragma unroll
-  for (int i = 0; i < kStatsRowsPerThread; ++i) {
-    const long long r = base + i * 256;
-    a[i] = r < R ? rowPtrs[r] : 0;
-    b[i] = r < R ? rowPtrs[r + 1] : 0;
-    // 32 consecutive rows handled by one warp of a row-per-thread kernel
-    g[i] = (r < R && lane == 0) ? rowPtrs[min(r + 32, (long long)R)] : 0;
-  }
   int lmax = 0, lmin = INT_MAX, empties = 0, gmax = 0;
   unsigned long long sq = 0ull;
   int firstBad = INT_MAX;
+  const long long nTiles = ((long long)R + kStatsRows - 1) / kStatsRows;
+  for (long long tile = blk; tile < (nTiles > 0 ? nTiles : 1); tile += nbRow) {
+    const long long base = tile * kStatsRows + threadIdx.x;
+    int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
 #pragma unroll
-  for (int i = 0; i < kStatsRowsPerThread; ++i) {
-    const long long r = base + i * 256;
-    const bool live = r < R;
-    int len = 0;
-    if (live) {
-      if (b[i] < a[i])
-        firstBad = min(firstBad, (int)r);
-      else
-        len = b[i] - a[i];
-      lmax = max(lmax, len);
-      lmin = min(lmin, len);
-      empties += (len == 0);
-      sq += (unsigned long long)len * (unsigned long long)len;
-      if (lane == 0) gmax = max(gmax, g[i] - a[i]);
-      if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
-      if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
-        const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
-        const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
-        for (int c = c0; c <= c1; ++c) {
-          desc[c].lo = (int)r;
-          if (c > 0) desc[c - 1].hi = (int)r;
-        }
-        const int pos = a[i] % kCsrChunk;
-        if (pos != 0) {
-          unsigned* m = reinterpret_cast<unsigned*>(&desc[a[i] / kCsrChunk].mask);
-          atomicOr(m + (pos >> 5), 1u << (pos & 31));
-        }
-      } else if (a[i] == b[i] && a[i] > 0 && a[i] < Z && a[i] % kCsrChunk != 0) {
-        atomicOr(&desc[a[i] / kCsrChunk].flags, kCsrChunkHasEmptyRow);
-      }
+    for (int i = 0; i < kStatsRowsPerThread; ++i) {
+      const long long r = base + i * 256;
+      a[i] = r < R ? rowPtrs[r] : 0;
+      b[i] = r < R ? rowPtrs[r + 1] : 0;
+      // 32 consecutive rows handled by one warp of a row-per-thread kernel
+      g[i] = (r < R && lane == 0) ? rowPtrs[min(r + 32, (long long)R)] : 0;
     }
-    // warp-aggregated exact histogram: when all 32 rows share one length
-    // (stencils, uniform rows) one shared atomic; otherwise one per distinct
-    // length found with a warp match
-    const int key = (live && len < kExactLenBins) ? len : -1;
-    const int kmin = __reduce_min_sync(kFullMask, key);
-    const int kmax = __reduce_max_sync(kFullMask, key);
-    if (kmin == kmax) {
-      if (lane == 0 && key >= 0) atomicAdd(&sExact[key], 32u);
-    } else {
-      const unsigned peers = __match_any_sync(kFullMask, key);
-      if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
+#pragma unroll
+    for (int i = 0; i < kStatsRowsPerThread; ++i) {
+      const long long r = base + i * 256;
+      const bool live = r < R;
+      int len = 0;
+      if (live) {
+        if (b[i] < a[i])
+          firstBad = min(firstBad, (int)r);
+        else
+          len = b[i] - a[i];
+        lmax = max(lmax, len);
+        lmin = min(lmin, len);
+        empties += (len == 0);
+        sq += (unsigned long long)len * (unsigned long long)len;
+        if (lane == 0) gmax = max(gmax, g[i] - a[i]);
+        if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
+        if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
+          const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
+          const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
+          for (int c = c0; c <= c1; ++c) {
+            desc[c].lo = (int)r;
+            if (c > 0) desc[c - 1].hi = (int)r;
+          }
+          const int pos = a[i] % kCsrChunk;
+          if (pos != 0) {
+            unsigned* m = reinterpret_cast<unsigned*>(&desc[a[i] / kCsrChunk].mask);
+            atomicOr(m + (pos >> 5), 1u << (pos & 31));
+          }
+        } else if (a[i] == b[i] && a[i] > 0 && a[i] < Z && a[i] % kCsrChunk != 0) {
+          atomicOr(&desc[a[i] / kCsrChunk].flags, kCsrChunkHasEmptyRow);
+        }
+      }
+      // warp-aggregated exact histogram: when all 32 rows share one length
+      // (stencils, uniform rows) one shared atomic; otherwise one per distinct
+      // length found with a warp match
+      const int key = (live && len < kExactLenBins) ? len : -1;
+      const int kmin = __reduce_min_sync(kFullMask, key);
+      const int kmax = __reduce_max_sync(kFullMask, key);
+      if (kmin == kmax) {
+        if (lane == 0 && key >= 0) atomicAdd(&sExact[key], 32u);
+      } else {
+        const unsigned peers = __match_any_sync(kFullMask, key);
+        if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
+      }
     }
   }
   lmax = warp_max(lmax);
@@ -350,7 +364,7 @@ __global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
   StatsPartial* partials = reinterpret_cast<StatsPartial*>(work + L.rowPart);
   ColPartial* colPart = reinterpret_cast<ColPartial*>(work + L.colPart);
   if ((int)blockIdx.x < nbRow)
-    row_part(blockIdx.x, R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
+    row_part(blockIdx.x, nbRow, R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
   else
     col_part<VEC>(blockIdx.x - nbRow, nbCol, Z, C, colIdx, colPart);
   // publish this block's results, then take a ticket; the last block folds
