@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_ell_q(
     int R, int K, const int* __restrict__ ellCol, const float* __restrict__ ellVal,
     const float* __restrict__ g, const float* __restrict__ dOld, float* __restrict__ dNew,
     float* __restrict__ q, float* partials, CgState* st) {
+  grid_dependency_wait();     // the previous update's g, d and state
+  grid_dependency_trigger();  // the next kernel may be scheduled as blocks exit
   if (!running(st)) return;
   const float b = (float)st->beta;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -254,6 +256,8 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_update(int R, float* __res
                                                              const float* __restrict__ d,
                                                              const float* __restrict__ q,
                                                              float* partials, CgState* st) {
+  grid_dependency_wait();     // the direction, q and alpha of this iteration
+  grid_dependency_trigger();
   if (!running(st)) return;
   const float a = (float)st->alpha;
   float part[1] = {0.f};
@@ -385,29 +389,50 @@ cudaError_t launch_cg_dot(int R, const float* d, const float* q, float* partials
   return cudaGetLastError();
 }
 
+// The ELL path's two kernels per iteration go out as programmatic dependent
+// launches: each waits (griddepcontrol.wait) for the kernel before it to
+// complete, so the launch and the scheduling of its blocks overlap the end
+// of that kernel instead of following it.
+template <class Kernel, class... Args>
+cudaError_t launch_dependent(Kernel kernel, unsigned grid, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kCgThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_cg_ell_q(int R, int K, const int* ellCol, const float* ellVal, const float* g,
                             const float* dOld, float* dNew, float* q, float* partials,
                             CgState* st, cudaStream_t s) {
+  cudaError_t e;
   if ((R & 3) == 0 && aligned16(ellCol) && aligned16(ellVal))
-    k_cg_ell_q<true><<<resident_grid(k_cg_ell_q<true>, kSlotEll4, R / 4), kCgThreads, 0, s>>>(
-        R, K, ellCol, ellVal, g, dOld, dNew, q, partials, st);
+    e = launch_dependent(k_cg_ell_q<true>, resident_grid(k_cg_ell_q<true>, kSlotEll4, R / 4), s,
+                         R, K, ellCol, ellVal, g, dOld, dNew, q, partials, st);
   else
-    k_cg_ell_q<false><<<resident_grid(k_cg_ell_q<false>, kSlotEll1, R), kCgThreads, 0, s>>>(
-        R, K, ellCol, ellVal, g, dOld, dNew, q, partials, st);
+    e = launch_dependent(k_cg_ell_q<false>, resident_grid(k_cg_ell_q<false>, kSlotEll1, R), s,
+                         R, K, ellCol, ellVal, g, dOld, dNew, q, partials, st);
   note_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_cg_update(int R, float* X, float* g, const float* d, const float* q,
                              float* partials, CgState* st, cudaStream_t s) {
+  cudaError_t e;
   if ((R & 3) == 0 && aligned16(X))
-    k_cg_update<true><<<resident_grid(k_cg_update<true>, kSlotUpd4, R / 4), kCgThreads, 0, s>>>(
-        R, X, g, d, q, partials, st);
+    e = launch_dependent(k_cg_update<true>, resident_grid(k_cg_update<true>, kSlotUpd4, R / 4), s,
+                         R, X, g, d, q, partials, st);
   else
-    k_cg_update<false><<<resident_grid(k_cg_update<false>, kSlotUpd1, R), kCgThreads, 0, s>>>(
-        R, X, g, d, q, partials, st);
+    e = launch_dependent(k_cg_update<false>, resident_grid(k_cg_update<false>, kSlotUpd1, R), s,
+                         R, X, g, d, q, partials, st);
   note_launches(1);
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace spmv
