@@ -65,28 +65,32 @@ int row_blocks(int R) {
   return (int)(t < cap ? t : cap);
 }
 
-int col_blocks(int Z, bool vec) {
-  if (Z <= 0) return 0;
-  const long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
-  const long long cb = (work + 255) / 256;
-  const long long cap = 8LL * num_sms();
-  return (int)(cb < 1 ? 1 : (cb > cap ? cap : cb));
+// Word W of the flat bit array of chunk masks: bit p (nonzero position p)
+// is bit p % 32 of word p / 32, kept in the mask of chunk p / kCsrChunk.
+__device__ __forceinline__ unsigned* mask_word(CsrChunkDesc* desc, long long W) {
+  return reinterpret_cast<unsigned*>(&desc[W >> 2].mask) + (W & 3);
 }
 
 // Row part. A block walks tiles blk, blk + nbRow, ... of kStatsRows
-// consecutive rows, kStatsRowsPerThread per thread, 256 apart so that each
-// load is coalesced, and issues all of a tile's loads before it uses any:
-// monotonicity, lengths, min/max/sum of squares,
-// the max nonzeros of any 32 consecutive rows, an exact length histogram
-// (lengths < kExactLenBins; longer rows go to the log2 bins), and the CSR
-// chunk records (bounds-checked: they are written before validation is
-// known). A nonempty row is `lo` of every chunk whose first nonzero it holds
-// (and `hi` of the chunk before) and sets the bit of its start position in
-// the chunk where it starts; an empty row inside a chunk flags that chunk.
-__device__ void row_part(int blk, int nbRow, int R, int Z, const int* __restrict__ rowPtrs,
+// consecutive rows; a lane takes kStatsRowsPerThread consecutive rows, whose
+// kStatsRowsPerThread + 1 row pointers come from two 16-byte loads and one
+// shuffle (rowVec: rowPtrs 16-byte aligned; and the tile whole; scalar loads
+// otherwise). From them, in registers: monotonicity, lengths, min/max/sum of
+// squares, the nonzeros of each 32 consecutive rows (4 lanes), an exact
+// length histogram (lengths < kExactLenBins; one shared add per warp when its
+// 256 rows share a length, else one per run of equal lengths; longer rows go
+// to the log2 bins), and the CSR chunk records (bounds-checked: they are
+// written before validation is known). A nonempty row is `lo` of every chunk
+// whose first nonzero it holds (and `hi` of the chunk before) and sets the
+// bit of its start position in the chunk where it starts; a lane gathers its
+// rows' bits in a 64-bit window and ORs at most two words into the records.
+// An empty row inside a chunk flags that chunk.
+__device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
+                         const int* __restrict__ rowPtrs,
                          DevStats* __restrict__ st, StatsPartial* __restrict__ partials,
                          unsigned* __restrict__ histRep, int nChunks,
                          CsrChunkDesc* __restrict__ desc) {
+  constexpr int E = kStatsRowsPerThread;
   __shared__ unsigned int sExact[kExactLenBins];
   __shared__ int sRed[5][8];
   __shared__ unsigned long long sSq[8];
@@ -103,60 +107,116 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, const int* __restrict
   unsigned long long sq = 0ull;
   int firstBad = INT_MAX;
   const long long nTiles = ((long long)R + kStatsRows - 1) / kStatsRows;
-  for (long long tile = blk; tile < (nTiles > 0 ? nTiles : 1); tile += nbRow) {
-    const long long base = tile * kStatsRows + threadIdx.x;
-    int a[kStatsRowsPerThread], b[kStatsRowsPerThread], g[kStatsRowsPerThread];
+  for (long long tile = blk; tile < nTiles; tile += nbRow) {
+    const long long r0 = tile * kStatsRows + (long long)threadIdx.x * E;
+    const bool wholeTile = (tile + 1) * kStatsRows <= (long long)R;  // block-uniform
+    // p[e] = rowPtrs[r0 + e]; past rowPtrs[R] it is INT_MAX (never a start)
+    int p[E + 1];
+    int nLive;  // rows r0 .. r0 + nLive - 1 exist
+    if (rowVec && wholeTile) {
+      const int4 u = *reinterpret_cast<const int4*>(rowPtrs + r0);
+      const int4 v = *reinterpret_cast<const int4*>(rowPtrs + r0 + 4);
+      const int last = lane == 31 ? __ldg(rowPtrs + r0 + E) : 0;
+      p[0] = u.x; p[1] = u.y; p[2] = u.z; p[3] = u.w;
+      p[4] = v.x; p[5] = v.y; p[6] = v.z; p[7] = v.w;
+      const int next = __shfl_down_sync(kFullMask, p[0], 1);
+      p[E] = lane == 31 ? last : next;
+      nLive = E;
+    } else {
 #pragma unroll
-    for (int i = 0; i < kStatsRowsPerThread; ++i) {
-      const long long r = base + i * 256;
-      a[i] = r < R ? rowPtrs[r] : 0;
-      b[i] = r < R ? rowPtrs[r + 1] : 0;
-      // 32 consecutive rows handled by one warp of a row-per-thread kernel
-      g[i] = (r < R && lane == 0) ? rowPtrs[min(r + 32, (long long)R)] : 0;
+      for (int e = 0; e <= E; ++e) p[e] = r0 + e <= R ? rowPtrs[r0 + e] : INT_MAX;
+      const long long left = (long long)R - r0;
+      nLive = left <= 0 ? 0 : (left >= E ? E : (int)left);
     }
+    // per-row statistics (lengths are recomputed from p where needed)
+    int kmn = INT_MAX, kmx = -1;
 #pragma unroll
-    for (int i = 0; i < kStatsRowsPerThread; ++i) {
-      const long long r = base + i * 256;
-      const bool live = r < R;
-      int len = 0;
+    for (int e = 0; e < E; ++e) {
+      const bool live = e < nLive;
+      int l = p[e + 1] - p[e];
+      if (live && l < 0) firstBad = min(firstBad, (int)(r0 + e));
+      l = l > 0 ? l : 0;
       if (live) {
-        if (b[i] < a[i])
-          firstBad = min(firstBad, (int)r);
-        else
-          len = b[i] - a[i];
-        lmax = max(lmax, len);
-        lmin = min(lmin, len);
-        empties += (len == 0);
-        sq += (unsigned long long)len * (unsigned long long)len;
-        if (lane == 0) gmax = max(gmax, g[i] - a[i]);
-        if (len >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(len)], 1ull);
-        if (a[i] >= 0 && b[i] <= Z && b[i] > a[i]) {
-          const int c0 = (a[i] + kCsrChunk - 1) / kCsrChunk;
-          const int c1 = min((b[i] - 1) / kCsrChunk, nChunks - 1);
-          for (int c = c0; c <= c1; ++c) {
-            desc[c].lo = (int)r;
-            if (c > 0) desc[c - 1].hi = (int)r;
-          }
-          const int pos = a[i] % kCsrChunk;
-          if (pos != 0) {
-            unsigned* m = reinterpret_cast<unsigned*>(&desc[a[i] / kCsrChunk].mask);
-            atomicOr(m + (pos >> 5), 1u << (pos & 31));
-          }
-        } else if (a[i] == b[i] && a[i] > 0 && a[i] < Z && a[i] % kCsrChunk != 0) {
-          atomicOr(&desc[a[i] / kCsrChunk].flags, kCsrChunkHasEmptyRow);
+        lmax = max(lmax, l);
+        lmin = min(lmin, l);
+        empties += l == 0;
+        sq += (unsigned long long)(unsigned)l * (unsigned)l;
+        kmn = min(kmn, l);
+        kmx = max(kmx, l);
+      }
+    }
+    // nonzeros of each aligned group of 32 rows (4 lanes)
+    const int pBeg = p[0];
+    int pEnd = pBeg;  // p[nLive], by selects (no dynamic register index)
+#pragma unroll
+    for (int e = 1; e <= E; ++e) pEnd = e <= nLive ? p[e] : pEnd;
+    int groupNnz = nLive > 0 ? pEnd - pBeg : 0;
+    groupNnz += __shfl_xor_sync(kFullMask, groupNnz, 1);
+    groupNnz += __shfl_xor_sync(kFullMask, groupNnz, 2);
+    gmax = max(gmax, groupNnz);
+    // exact histogram
+    const int wmn = __reduce_min_sync(kFullMask, kmn);
+    const int wmx = __reduce_max_sync(kFullMask, kmx);
+    if (wmn == wmx && wmx < kExactLenBins) {  // one length (wmx >= 0: some row lives)
+      const int rows = __reduce_add_sync(kFullMask, (unsigned)nLive);
+      if (lane == 0) atomicAdd(&sExact[wmx], (unsigned)rows);
+    } else {
+      int cur = -1;
+      unsigned cnt = 0u;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int l = e < nLive ? max(p[e + 1] - p[e], 0) : -1;
+        if (l >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(l)], 1ull);
+        const int key = l < kExactLenBins ? l : -1;
+        if (key != cur) {
+          if (cur >= 0) atomicAdd(&sExact[cur], cnt);
+          cur = key;
+          cnt = 0u;
+        }
+        ++cnt;
+      }
+      if (cur >= 0) atomicAdd(&sExact[cur], cnt);
+    }
+    // chunk records; only on a consistent lane range (always, for valid input)
+    if (nLive > 0 && 0 <= pBeg && pBeg < pEnd && pEnd <= Z) {
+      // lo/hi of the chunks whose first position q lies in [pBeg, pEnd): the
+      // row holding q is the last of the lane's rows starting at or before q
+      const int cLast = min((pEnd - 1) / kCsrChunk, nChunks - 1);
+      for (int c = (pBeg + kCsrChunk - 1) / kCsrChunk; c <= cLast; ++c) {
+        const int q = c * kCsrChunk;
+        int e = 0;
+#pragma unroll
+        for (int k = 1; k < E; ++k) e += (k < nLive && p[k] <= q);
+        const int r = (int)(r0 + e);
+        desc[c].lo = r;
+        if (c > 0) desc[c - 1].hi = r;
+      }
+      // start bits of nonempty rows, in a 64-bit window from word pBeg / 32
+      const long long W0 = pBeg >> 5;
+      unsigned long long win = 0ull;
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int a = p[e];
+        const bool live = e < nLive;
+        if (live && p[e + 1] > a && (a & (kCsrChunk - 1)) != 0 && a >= 0 && p[e + 1] <= Z) {
+          const long long off = (long long)a - (W0 << 5);
+          if (off >= 0 && off < 64)  // (off < 0 only on invalid input)
+            win |= 1ull << off;
+          else
+            atomicOr(mask_word(desc, a >> 5), 1u << (a & 31));
+        } else if (live && p[e + 1] <= a && a > 0 && a < Z && (a & (kCsrChunk - 1)) != 0) {
+          atomicOr(&desc[a / kCsrChunk].flags, kCsrChunkHasEmptyRow);
         }
       }
-      // warp-aggregated exact histogram: when all 32 rows share one length
-      // (stencils, uniform rows) one shared atomic; otherwise one per distinct
-      // length found with a warp match
-      const int key = (live && len < kExactLenBins) ? len : -1;
-      const int kmin = __reduce_min_sync(kFullMask, key);
-      const int kmax = __reduce_max_sync(kFullMask, key);
-      if (kmin == kmax) {
-        if (lane == 0 && key >= 0) atomicAdd(&sExact[key], 32u);
-      } else {
-        const unsigned peers = __match_any_sync(kFullMask, key);
-        if (key >= 0 && lane == __ffs(peers) - 1) atomicAdd(&sExact[key], (unsigned)__popc(peers));
+      if ((unsigned)win) atomicOr(mask_word(desc, W0), (unsigned)win);
+      if ((unsigned)(win >> 32)) atomicOr(mask_word(desc, W0 + 1), (unsigned)(win >> 32));
+    } else if (nLive > 0) {
+      // empty lane range: every live row is empty (or the input is invalid)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const int a = p[e];
+        if (e < nLive && p[e + 1] <= a && a > 0 && a < Z && (a & (kCsrChunk - 1)) != 0)
+          atomicOr(&desc[a / kCsrChunk].flags, kCsrChunkHasEmptyRow);
       }
     }
   }
@@ -204,30 +264,39 @@ __device__ void col_part(int cblk, int nbCol, int Z, int C, const int* __restric
                          ColPartial* __restrict__ colPart) {
   const unsigned uc = (unsigned)C;
   int firstBad = INT_MAX;
-  const long long stride = (long long)nbCol * blockDim.x;
-  long long i = (long long)cblk * blockDim.x + threadIdx.x;
   const bool sample = cblk < kGatherSampleBlocks;
-  unsigned long long lines = 0ull, sets = 0ull;
+  unsigned nLines = 0u, nSets = 0u;
   if (VEC) {
-    const long long nv = Z / 4;
+    // 32-bit indices: nv < 2^29 and the grid stride is small
+    const int nv = Z / 4;
+    const int stride = nbCol * (int)blockDim.x;
     const int4* c4 = reinterpret_cast<const int4*>(colIdx);
+    int i = cblk * (int)blockDim.x + (int)threadIdx.x;
     // all lanes of a warp run the same number of iterations (the bound only
     // depends on the warp's first index), so the warp match below is uniform
-    long long i0 = i - (threadIdx.x & 31);
+    int i0 = i - (int)(threadIdx.x & 31);
     for (; i0 < nv; i += kColUnroll * stride, i0 += kColUnroll * stride) {
       int4 c[kColUnroll];
 #pragma unroll
       for (int u = 0; u < kColUnroll; ++u)
         c[u] = i + u * stride < nv ? ld_stream(c4 + i + u * stride) : make_int4(0, 0, 0, 0);
+      // any entry out of range? (the zero fill is in range: C > 0 when Z > 0)
+      bool bad = false;
 #pragma unroll
-      for (int u = 0; u < kColUnroll; ++u) {
-        const long long iu = i + u * stride;
-        if (iu < nv) {
-          const int k = (int)(4 * iu);
-          if ((unsigned)c[u].x >= uc) firstBad = min(firstBad, k);
-          if ((unsigned)c[u].y >= uc) firstBad = min(firstBad, k + 1);
-          if ((unsigned)c[u].z >= uc) firstBad = min(firstBad, k + 2);
-          if ((unsigned)c[u].w >= uc) firstBad = min(firstBad, k + 3);
+      for (int u = 0; u < kColUnroll; ++u)
+        bad |= ((unsigned)c[u].x >= uc) | ((unsigned)c[u].y >= uc) | ((unsigned)c[u].z >= uc) |
+               ((unsigned)c[u].w >= uc);
+      if (bad) {  // the first bad position (only on invalid input)
+#pragma unroll
+        for (int u = 0; u < kColUnroll; ++u) {
+          const int iu = i + u * stride;
+          if (iu < nv) {
+            const int k = 4 * iu;
+            if ((unsigned)c[u].x >= uc) firstBad = min(firstBad, k);
+            if ((unsigned)c[u].y >= uc) firstBad = min(firstBad, k + 1);
+            if ((unsigned)c[u].z >= uc) firstBad = min(firstBad, k + 2);
+            if ((unsigned)c[u].w >= uc) firstBad = min(firstBad, k + 3);
+          }
         }
       }
       if (sample) {
@@ -236,18 +305,20 @@ __device__ void col_part(int cblk, int nbCol, int Z, int C, const int* __restric
         const unsigned peers = __match_any_sync(kFullMask, ln);
         const bool leader = (threadIdx.x & 31) == __ffs(peers) - 1;
         if (i0 + 32 <= nv) {  // full sets only
-          if (leader) ++lines;
-          if ((threadIdx.x & 31) == 0) ++sets;
+          if (leader) ++nLines;
+          if ((threadIdx.x & 31) == 0) ++nSets;
         }
       }
     }
     const long long t = (long long)cblk * blockDim.x + threadIdx.x;
-    const long long k = 4 * nv + t;
+    const long long k = 4LL * nv + t;
     if (k < Z && (unsigned)colIdx[k] >= uc) firstBad = min(firstBad, (int)k);
   } else {
-    for (; i < Z; i += stride)
+    const long long stride = (long long)nbCol * blockDim.x;
+    for (long long i = (long long)cblk * blockDim.x + threadIdx.x; i < Z; i += stride)
       if ((unsigned)ld_stream(colIdx + i) >= uc) firstBad = min(firstBad, (int)i);
   }
+  unsigned long long lines = nLines, sets = nSets;
   __shared__ unsigned long long sL[8], sS[8];
   __shared__ int sB[8];
   firstBad = warp_min(firstBad);
@@ -356,7 +427,8 @@ __global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
                                                         const int* __restrict__ colIdx,
                                                         unsigned char* __restrict__ work,
                                                         int nbRow, int nbCol, int nChunks,
-                                                        CsrChunkDesc* __restrict__ desc) {
+                                                        CsrChunkDesc* __restrict__ desc,
+                                                        bool rowVec) {
   const WorkLayout L = work_layout(nbRow, nbCol);
   DevStats* st = reinterpret_cast<DevStats*>(work);
   unsigned* ticket = reinterpret_cast<unsigned*>(work + L.ticket);
@@ -364,7 +436,7 @@ __global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
   StatsPartial* partials = reinterpret_cast<StatsPartial*>(work + L.rowPart);
   ColPartial* colPart = reinterpret_cast<ColPartial*>(work + L.colPart);
   if ((int)blockIdx.x < nbRow)
-    row_part(blockIdx.x, nbRow, R, Z, rowPtrs, st, partials, histRep, nChunks, desc);
+    row_part(blockIdx.x, nbRow, R, Z, rowVec, rowPtrs, st, partials, histRep, nChunks, desc);
   else
     col_part<VEC>(blockIdx.x - nbRow, nbCol, Z, C, colIdx, colPart);
   // publish this block's results, then take a ticket; the last block folds
@@ -379,6 +451,16 @@ __global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
   }
 }
 
+// Column blocks: up to 8 per SM, each walking the column array grid-stride;
+// blocks beyond those resident start as row blocks finish.
+int col_blocks(int Z, bool vec) {
+  if (Z <= 0) return 0;
+  const long long work = vec ? ((long long)Z / 4 + 1) : (long long)Z;
+  const long long cb = (work + 255) / 256;
+  const long long cap = 8LL * num_sms();
+  return (int)(cb < 1 ? 1 : (cb > cap ? cap : cb));
+}
+
 }  // namespace
 
 size_t stats_work_bytes(int R, int Z, const int* colIdx) {
@@ -390,15 +472,16 @@ size_t stats_zero_bytes() { return work_layout(1, 1).zero; }
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx, void* work,
                          int nChunks, CsrChunkDesc* desc, cudaStream_t s) {
   const bool vec = aligned16(colIdx);
+  const bool rowVec = aligned16(rowPtrs);
   const int nbRow = row_blocks(R);
   const int nbCol = col_blocks(Z, vec);
   unsigned char* w = static_cast<unsigned char*>(work);
   if (vec)
     k_validate_stats<true><<<nbRow + nbCol, 256, 0, s>>>(R, C, Z, rowPtrs, colIdx, w, nbRow,
-                                                         nbCol, nChunks, desc);
+                                                         nbCol, nChunks, desc, rowVec);
   else
     k_validate_stats<false><<<nbRow + nbCol, 256, 0, s>>>(R, C, Z, rowPtrs, colIdx, w, nbRow,
-                                                          nbCol, nChunks, desc);
+                                                          nbCol, nChunks, desc, rowVec);
   note_launches(1);
   return cudaGetLastError();
 }

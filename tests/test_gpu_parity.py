@@ -69,7 +69,9 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
     oracle's conversions and the SpMV results with the oracle's y."""
     rp_t = dev(inp.row_ptrs)
     if offset:
-        # misaligned views of colIdx/value/y to exercise the scalar paths
+        # misaligned views of rowPtrs/colIdx/value/y to exercise the scalar paths
+        rp_buf = dev(np.concatenate([np.zeros(offset, np.int32), inp.row_ptrs]))
+        rp_t = rp_buf[offset:]
         ci_buf = dev(np.concatenate([np.zeros(offset, np.int32), inp.col_idx]))
         va_buf = dev(np.concatenate([np.zeros(offset, np.float32), inp.value]))
         ci_t, va_t = ci_buf[offset:], va_buf[offset:]
@@ -87,6 +89,16 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
         assert st["mean_len"] == pytest.approx(ost["mean"], rel=1e-12, abs=1e-12)
         assert st["var_len"] == pytest.approx(ost["var"], rel=1e-9, abs=1e-9)
         assert st["auto_format"] == orc.select(R, Z, ost["max_len"])
+        # the other row statistics, by their definitions over the row lengths
+        lens = np.diff(inp.row_ptrs.astype(np.int64))
+        if R:
+            assert st["min_len"] == int(lens.min())
+            assert st["empty_rows"] == int((lens == 0).sum())
+            assert st["sum_sq_len"] == int((lens * lens).sum())
+            if Z:
+                groups = np.add.reduceat(lens, np.arange(0, R, 32))  # 32 consecutive rows
+                want = float(groups.max()) / (Z / ((R + 31) // 32))
+                assert st["imbalance_warp"] == pytest.approx(want, rel=1e-12)
         if R and ost["max_len"] < 4096:
             assert st["auto_hyb_width"] == orc.hyb_auto_width(inp.row_ptrs)
         for f in formats:
