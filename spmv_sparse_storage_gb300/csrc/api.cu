@@ -397,9 +397,10 @@ int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
   if (st != SPMV_OK) return fail(st);
   st = record(cudaStreamSynchronize(s));
   if (st != SPMV_OK) return fail(st);
-  if (hst->err & (spmv::kErrRowPtrStart | spmv::kErrRowPtrDecrease | spmv::kErrRowPtrEnd))
+  const unsigned errs = spmv::stats_errors(*hst);
+  if (errs & (spmv::kErrRowPtrStart | spmv::kErrRowPtrDecrease | spmv::kErrRowPtrEnd))
     return fail(SPMV_ERR_BAD_ROWPTRS);
-  if (hst->err & spmv::kErrColRange) return fail(SPMV_ERR_COL_OUT_OF_RANGE);
+  if (errs & spmv::kErrColRange) return fail(SPMV_ERR_COL_OUT_OF_RANGE);
 
   spmv_stats& S = h->stats;
   std::memset(&S, 0, sizeof(S));
@@ -407,7 +408,7 @@ int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
   S.num_cols = numCols;
   S.nnz = nnz;
   S.max_len = hst->maxLen;
-  S.min_len = numRows > 0 ? hst->minLen : 0;
+  S.min_len = numRows > 0 ? spmv::stats_min_len(*hst) : 0;
   S.empty_rows = hst->emptyRows;
   S.sum_sq_len = (int64_t)hst->sumSq;
   S.mean_len = numRows > 0 ? (double)nnz / (double)numRows : 0.0;

@@ -22,12 +22,15 @@ enum : unsigned {
   kErrColRange = 8u,        // colIdx outside [0, numCols)
 };
 
+// Results of the statistics pass, accumulated by every block with atomics
+// into a zeroed record (no fold at the end). Minima are kept as maxima of
+// INT_MAX - v, so that 0 means "none".
 struct DevStats {
-  unsigned int err;
-  int firstBadRow;
-  int firstBadNnz;
+  unsigned int err;      // kErrRowPtrStart | kErrRowPtrEnd (the others: stats_errors)
+  int badRowKey;         // max over decreasing rows r of INT_MAX - r
+  int badNnzKey;         // max over out-of-range positions k of INT_MAX - k
   int maxLen;
-  int minLen;
+  int minLenKey;         // max over rows of INT_MAX - len
   int emptyRows;
   int maxWarpNnz;
   int pad0;
@@ -38,14 +41,15 @@ struct DevStats {
   unsigned int histExact[kExactLenBins];
 };
 
-// Per-block partial record of the statistics pass (stats.cu).
-struct StatsPartial {
-  int maxLen, minLen, emptyRows, maxWarpNnz, firstBadRow, pad0;
-  unsigned long long sumSq;
-};
-// Work area of the statistics pass: DevStats first (read back by the host),
-// then counters and per-block records; its first stats_zero_bytes() bytes
-// must be zeroed before launch_stats.
+// Every validation error bit of a finished record.
+inline unsigned stats_errors(const DevStats& d) {
+  return d.err | (d.badRowKey ? kErrRowPtrDecrease : 0u) | (d.badNnzKey ? kErrColRange : 0u);
+}
+// Shortest row (INT_MAX when there is no row).
+inline int stats_min_len(const DevStats& d) { return 2147483647 - d.minLenKey; }
+
+// Work area of the statistics pass: the DevStats record (read back by the
+// host); its first stats_zero_bytes() bytes must be zeroed before launch_stats.
 size_t stats_work_bytes(int R, int Z, const int* colIdx);
 size_t stats_zero_bytes();
 

@@ -11,9 +11,9 @@
 // bottleneck location", section "Building the problem framework".
 //
 // One grid does everything: its first blocks walk rowPtrs, the others walk
-// colIdx (both streams at once), each block writes a partial record, and the
-// last block to finish folds the records into DevStats (no inter-block wait:
-// a block learns it is last from an atomic ticket).
+// colIdx (both streams at once), and each block adds its results into the
+// zeroed DevStats record with atomics (maxima, sums, histogram bins) as it
+// finishes, so that nothing is left to fold after the last block.
 #include <climits>
 
 #include "device_util.cuh"
@@ -25,34 +25,13 @@ namespace {
 constexpr int kStatsRowsPerThread = 8;
 constexpr int kStatsRows = 256 * kStatsRowsPerThread;  // rows per row block
 constexpr int kColUnroll = 4;                           // column check: vectors in flight
-constexpr int kStatsReplicaCount = 8;                   // copies of the exact histogram
 
-struct ColPartial {
-  int firstBad;
-  int pad0;
-  unsigned long long lines, sets;
-};
-
-// Work area layout (one allocation, zeroed up to `zero_bytes`):
-//   DevStats | ticket (16 B) | histogram replicas | row partials | column partials
-struct WorkLayout {
-  size_t ticket, rep, rowPart, colPart, zero, total;
-};
-
-__host__ __device__ inline WorkLayout work_layout(int nbRow, int nbCol) {
-  WorkLayout L;
-  L.ticket = (sizeof(DevStats) + 15) / 16 * 16;
-  L.rep = L.ticket + 16;
-  L.rowPart = L.rep + (size_t)kStatsReplicaCount * kExactLenBins * sizeof(unsigned);
-  L.zero = L.rowPart;
-  L.colPart = L.rowPart + (size_t)nbRow * sizeof(StatsPartial);
-  L.total = L.colPart + (size_t)(nbCol > 0 ? nbCol : 1) * sizeof(ColPartial);
-  return L;
-}
+// Work area: the DevStats record alone (zeroed before the launch).
+constexpr size_t kWorkBytes = (sizeof(DevStats) + 255) / 256 * 256;
 
 // Row blocks: at most kRowBlocksPerSm per SM, each walking several
 // kStatsRows-row tiles, so that a block's fixed tail (shared-memory
-// histogram, reductions, fence, ticket) is paid once per block rather than
+// histogram flush, reductions, atomics) is paid once per block rather than
 // once per tile.
 constexpr int kRowBlocksPerSm = 2;
 long long row_tiles(int R) {
@@ -87,8 +66,7 @@ __device__ __forceinline__ unsigned* mask_word(CsrChunkDesc* desc, long long W) 
 // An empty row inside a chunk flags that chunk.
 __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
                          const int* __restrict__ rowPtrs,
-                         DevStats* __restrict__ st, StatsPartial* __restrict__ partials,
-                         unsigned* __restrict__ histRep, int nChunks,
+                         DevStats* __restrict__ st, int nChunks,
                          CsrChunkDesc* __restrict__ desc) {
   constexpr int E = kStatsRowsPerThread;
   __shared__ unsigned int sExact[kExactLenBins];
@@ -236,22 +214,25 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    StatsPartial p;
-    p.maxLen = 0; p.minLen = INT_MAX; p.emptyRows = 0; p.maxWarpNnz = 0;
-    p.firstBadRow = INT_MAX; p.pad0 = 0; p.sumSq = 0ull;
+    int mx = 0, mn = INT_MAX, emp = 0, gm = 0, fb = INT_MAX;
+    unsigned long long sqs = 0ull;
     for (int w = 0; w < 8; ++w) {
-      p.maxLen = max(p.maxLen, sRed[0][w]);
-      p.minLen = min(p.minLen, sRed[1][w]);
-      p.emptyRows += sRed[2][w];
-      p.maxWarpNnz = max(p.maxWarpNnz, sRed[3][w]);
-      p.firstBadRow = min(p.firstBadRow, sRed[4][w]);
-      p.sumSq += sSq[w];
+      mx = max(mx, sRed[0][w]);
+      mn = min(mn, sRed[1][w]);
+      emp += sRed[2][w];
+      gm = max(gm, sRed[3][w]);
+      fb = min(fb, sRed[4][w]);
+      sqs += sSq[w];
     }
-    partials[blk] = p;
+    if (mx) atomicMax(&st->maxLen, mx);
+    if (mn != INT_MAX) atomicMax(&st->minLenKey, INT_MAX - mn);
+    if (emp) atomicAdd(&st->emptyRows, emp);
+    if (gm) atomicMax(&st->maxWarpNnz, gm);
+    if (fb != INT_MAX) atomicMax(&st->badRowKey, INT_MAX - fb);
+    if (sqs) atomicAdd(&st->sumSq, sqs);
   }
-  unsigned* rep = histRep + (size_t)(blk % kStatsReplicaCount) * kExactLenBins;
   for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x)
-    if (sExact[i]) atomicAdd(rep + i, sExact[i]);
+    if (sExact[i]) atomicAdd(&st->histExact[i], sExact[i]);
 }
 
 // Column part: every column index must satisfy 0 <= c < numCols (unsigned
@@ -261,7 +242,7 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
 // among the 32 gathers of one warp load.
 template <bool VEC>
 __device__ void col_part(int cblk, int nbCol, int Z, int C, const int* __restrict__ colIdx,
-                         ColPartial* __restrict__ colPart) {
+                         DevStats* __restrict__ st) {
   const unsigned uc = (unsigned)C;
   int firstBad = INT_MAX;
   const bool sample = cblk < kGatherSampleBlocks;
@@ -331,93 +312,16 @@ __device__ void col_part(int cblk, int nbCol, int Z, int C, const int* __restric
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    ColPartial p;
-    p.firstBad = INT_MAX;
-    p.pad0 = 0;
-    p.lines = 0ull;
-    p.sets = 0ull;
+    int fb = INT_MAX;
+    unsigned long long ln = 0ull, ss = 0ull;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-      p.firstBad = min(p.firstBad, sB[w]);
-      p.lines += sL[w];
-      p.sets += sS[w];
+      fb = min(fb, sB[w]);
+      ln += sL[w];
+      ss += sS[w];
     }
-    colPart[cblk] = p;
-  }
-}
-
-// The last block: fold row partials, column partials and histogram replicas.
-__device__ void finalize(int nbRow, int nbCol, DevStats* __restrict__ st,
-                         const StatsPartial* __restrict__ partials,
-                         const ColPartial* __restrict__ colPart,
-                         const unsigned* __restrict__ histRep) {
-  __shared__ int sRed[6][8];
-  __shared__ unsigned long long sU[3][8];
-  for (int i = threadIdx.x; i < kExactLenBins; i += blockDim.x) {
-    unsigned v = 0u;
-#pragma unroll
-    for (int r = 0; r < kStatsReplicaCount; ++r) v += histRep[(size_t)r * kExactLenBins + i];
-    st->histExact[i] = v;
-  }
-  int mx = 0, mn = INT_MAX, emp = 0, gm = 0, fb = INT_MAX, fc = INT_MAX;
-  unsigned long long sq = 0ull, ln = 0ull, ss = 0ull;
-  for (int i = threadIdx.x; i < nbRow; i += blockDim.x) {
-    const StatsPartial p = partials[i];
-    mx = max(mx, p.maxLen);
-    mn = min(mn, p.minLen);
-    emp += p.emptyRows;
-    gm = max(gm, p.maxWarpNnz);
-    fb = min(fb, p.firstBadRow);
-    sq += p.sumSq;
-  }
-  for (int i = threadIdx.x; i < nbCol; i += blockDim.x) {
-    const ColPartial p = colPart[i];
-    fc = min(fc, p.firstBad);
-    ln += p.lines;
-    ss += p.sets;
-  }
-  mx = warp_max(mx);
-  mn = warp_min(mn);
-  emp = warp_sum(emp);
-  gm = warp_max(gm);
-  fb = warp_min(fb);
-  fc = warp_min(fc);
-  sq = warp_sum(sq);
-  ln = warp_sum(ln);
-  ss = warp_sum(ss);
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  if (lane == 0) {
-    sRed[0][wid] = mx; sRed[1][wid] = mn; sRed[2][wid] = emp;
-    sRed[3][wid] = gm; sRed[4][wid] = fb; sRed[5][wid] = fc;
-    sU[0][wid] = sq; sU[1][wid] = ln; sU[2][wid] = ss;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    mx = 0; mn = INT_MAX; emp = 0; gm = 0; fb = INT_MAX; fc = INT_MAX;
-    sq = ln = ss = 0ull;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) {
-      mx = max(mx, sRed[0][w]);
-      mn = min(mn, sRed[1][w]);
-      emp += sRed[2][w];
-      gm = max(gm, sRed[3][w]);
-      fb = min(fb, sRed[4][w]);
-      fc = min(fc, sRed[5][w]);
-      sq += sU[0][w];
-      ln += sU[1][w];
-      ss += sU[2][w];
-    }
-    st->maxLen = mx;
-    st->minLen = mn;
-    st->emptyRows = emp;
-    st->maxWarpNnz = gm;
-    st->sumSq = sq;
-    st->gatherLines = ln;
-    st->gatherSets = ss;
-    st->firstBadRow = fb;
-    st->firstBadNnz = fc;
-    unsigned err = st->err;
-    if (fb != INT_MAX) err |= kErrRowPtrDecrease;
-    if (fc != INT_MAX) err |= kErrColRange;
-    st->err = err;
+    if (fb != INT_MAX) atomicMax(&st->badNnzKey, INT_MAX - fb);
+    if (ln) atomicAdd(&st->gatherLines, ln);
+    if (ss) atomicAdd(&st->gatherSets, ss);
   }
 }
 
@@ -425,30 +329,14 @@ template <bool VEC>
 __global__ void __launch_bounds__(256) k_validate_stats(int R, int C, int Z,
                                                         const int* __restrict__ rowPtrs,
                                                         const int* __restrict__ colIdx,
-                                                        unsigned char* __restrict__ work,
-                                                        int nbRow, int nbCol, int nChunks,
+                                                        DevStats* __restrict__ st, int nbRow,
+                                                        int nbCol, int nChunks,
                                                         CsrChunkDesc* __restrict__ desc,
                                                         bool rowVec) {
-  const WorkLayout L = work_layout(nbRow, nbCol);
-  DevStats* st = reinterpret_cast<DevStats*>(work);
-  unsigned* ticket = reinterpret_cast<unsigned*>(work + L.ticket);
-  unsigned* histRep = reinterpret_cast<unsigned*>(work + L.rep);
-  StatsPartial* partials = reinterpret_cast<StatsPartial*>(work + L.rowPart);
-  ColPartial* colPart = reinterpret_cast<ColPartial*>(work + L.colPart);
   if ((int)blockIdx.x < nbRow)
-    row_part(blockIdx.x, nbRow, R, Z, rowVec, rowPtrs, st, partials, histRep, nChunks, desc);
+    row_part(blockIdx.x, nbRow, R, Z, rowVec, rowPtrs, st, nChunks, desc);
   else
-    col_part<VEC>(blockIdx.x - nbRow, nbCol, Z, C, colIdx, colPart);
-  // publish this block's results, then take a ticket; the last block folds
-  __shared__ bool sLast;
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) sLast = atomicAdd(ticket, 1u) == (unsigned)(nbRow + nbCol - 1);
-  __syncthreads();
-  if (sLast) {
-    __threadfence();
-    finalize(nbRow, nbCol, st, partials, colPart, histRep);
-  }
+    col_part<VEC>(blockIdx.x - nbRow, nbCol, Z, C, colIdx, st);
 }
 
 // Column blocks: up to 8 per SM, each walking the column array grid-stride;
@@ -463,11 +351,9 @@ int col_blocks(int Z, bool vec) {
 
 }  // namespace
 
-size_t stats_work_bytes(int R, int Z, const int* colIdx) {
-  return work_layout(row_blocks(R), col_blocks(Z, aligned16(colIdx))).total;
-}
+size_t stats_work_bytes(int, int, const int*) { return kWorkBytes; }
 
-size_t stats_zero_bytes() { return work_layout(1, 1).zero; }
+size_t stats_zero_bytes() { return sizeof(DevStats); }
 
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx, void* work,
                          int nChunks, CsrChunkDesc* desc, cudaStream_t s) {
@@ -475,7 +361,7 @@ cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* col
   const bool rowVec = aligned16(rowPtrs);
   const int nbRow = row_blocks(R);
   const int nbCol = col_blocks(Z, vec);
-  unsigned char* w = static_cast<unsigned char*>(work);
+  DevStats* w = static_cast<DevStats*>(work);
   if (vec)
     k_validate_stats<true><<<nbRow + nbCol, 256, 0, s>>>(R, C, Z, rowPtrs, colIdx, w, nbRow,
                                                          nbCol, nChunks, desc, rowVec);
