@@ -258,29 +258,42 @@ __global__ void __launch_bounds__(256) k_spmv_csr_wide(int Z, const int* __restr
 
 // CSR -> COO ("Sparse Matrices and Basic Formats ...", section "COO format
 // and SpMV"): rowIdx[k] = r for rowPtrs[r] <= k < rowPtrs[r+1]. The layout of
-// the CSR kernel: a warp takes 256 nonzeros, each lane 8 consecutive ones,
+// the CSR kernel: per 256 nonzeros, each lane takes 8 consecutive ones,
 // decodes their rows from its chunk record (lane_rows) and stores them with
-// two 16-byte stores (VEC: rowIdx is 16-byte aligned).
+// two 16-byte stores (VEC: rowIdx is 16-byte aligned). A warp takes
+// kExpandSupers consecutive blocks of 256 and loads all their chunk records
+// before decoding any, so that one load round trip serves them all (the
+// kernel has nothing else to wait on).
+constexpr int kExpandSupers = 4;
 template <bool VEC>
 __global__ void __launch_bounds__(256) k_expand_rows(int Z, const int* __restrict__ rowPtrs,
                                                      const CsrChunkDesc* __restrict__ desc,
                                                      int* __restrict__ rowIdx) {
   const int lane = threadIdx.x & 31;
   const long long g = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (g * kCsrSuper >= Z) return;  // warp-uniform
-  const long long base = g * kCsrSuper + (long long)lane * kCsrLane;
-  if (base >= Z) return;  // no shuffles below: lanes may leave
-  const CsrChunkDesc d = desc[base / kCsrChunk];
-  int row[kCsrLane];
-  lane_rows(d, base, lane, Z, rowPtrs, row);
-  if (VEC && base + kCsrLane <= Z) {
-    int4* out = reinterpret_cast<int4*>(rowIdx + base);
-    __stcs(out, make_int4(row[0], row[1], row[2], row[3]));
-    __stcs(out + 1, make_int4(row[4], row[5], row[6], row[7]));
-  } else {
+  const long long first = g * kExpandSupers * kCsrSuper + (long long)lane * kCsrLane;
+  if (first >= Z) return;  // no shuffles below: lanes may leave
+  CsrChunkDesc d[kExpandSupers];
 #pragma unroll
-    for (int e = 0; e < kCsrLane; ++e)
-      if (base + e < Z) rowIdx[base + e] = row[e];
+  for (int k = 0; k < kExpandSupers; ++k) {
+    const long long base = first + (long long)k * kCsrSuper;
+    if (base < Z) d[k] = desc[base / kCsrChunk];
+  }
+#pragma unroll
+  for (int k = 0; k < kExpandSupers; ++k) {
+    const long long base = first + (long long)k * kCsrSuper;
+    if (base >= Z) break;
+    int row[kCsrLane];
+    lane_rows(d[k], base, lane, Z, rowPtrs, row);
+    if (VEC && base + kCsrLane <= Z) {
+      int4* out = reinterpret_cast<int4*>(rowIdx + base);
+      __stcs(out, make_int4(row[0], row[1], row[2], row[3]));
+      __stcs(out + 1, make_int4(row[4], row[5], row[6], row[7]));
+    } else {
+#pragma unroll
+      for (int e = 0; e < kCsrLane; ++e)
+        if (base + e < Z) rowIdx[base + e] = row[e];
+    }
   }
 }
 
@@ -575,7 +588,8 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
 cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
                                int* rowIdx, cudaStream_t s) {
   if (R <= 0 || Z <= 0) return cudaSuccess;
-  const long long warps = ((long long)Z + kCsrSuper - 1) / kCsrSuper;
+  const long long perWarp = (long long)kExpandSupers * kCsrSuper;
+  const long long warps = ((long long)Z + perWarp - 1) / perWarp;
   const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
   if (aligned16(rowIdx))
     k_expand_rows<true><<<grid, 256, 0, s>>>(Z, rowPtrs, desc, rowIdx);
