@@ -389,7 +389,8 @@ def run_kernels(args, device):
     """Per-format SpMV timing on one workload: each rep resets y to y0 and
     flushes L2 (writes a buffer of twice its size, then reads another, so that
     L2 is left clean) outside the timed events, then times one spmv_run with
-    CUDA events on the launching stream; median over reps."""
+    CUDA events on the launching stream; median over reps. Warm-L2 times
+    (the same runs back to back without the flush) are reported apart."""
     import torch
     import spmv_sparse_storage_gb300 as sp
     inp = synth.make_workload(args.workload, seed=0)
@@ -447,12 +448,27 @@ def run_kernels(args, device):
                 e1.synchronize()
                 if rep >= args.warmup:
                     times.append(e0.elapsed_time(e1))
+            # warm L2, reported apart: the same runs back to back, y reset, no flush
+            warm = []
+            for rep in range(args.warmup + args.reps):
+                y.copy_(y0)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                m.run(f, x, y, stream=stream)
+                e1.record(stream)
+                e1.synchronize()
+                if rep >= args.warmup:
+                    warm.append(e0.elapsed_time(e1))
             ms = float(np.median(times))
+            ms_warm = float(np.median(warm))
             gbs = compulsory_bytes(R, C, Z, vb) / (ms * 1e-3) / 1e9
             gflops = 2 * Z / (ms * 1e-3) / 1e9
+            gbs_warm = compulsory_bytes(R, C, Z, vb) / (ms_warm * 1e-3) / 1e9
             out[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                       "frac": round(gbs / peak, 4), "GFLOP/s": round(gflops, 1),
-                      "convert_us": conv_us.get(f)}
+                      "convert_us": conv_us.get(f), "warm_l2_us": round(ms_warm * 1e3, 2),
+                      "warm_l2_frac": round(gbs_warm / peak, 4)}
             if vb == 8:  # fp64 multiply-adds against the nominal 1.25 TFLOP/s fp64 rate
                 out[f]["fp64_frac_nominal"] = round(gflops / FP64_NOMINAL_GFLOPS, 4)
             if f in ("ELL", "HYB", "SELL", "XBLOCK"):
@@ -461,7 +477,8 @@ def run_kernels(args, device):
     line = {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
             "nnz": Z,
             "l2_flush": f"write {flush.numel() * 4} B, then read another {flush.numel() * 4} B "
-                        "(clean L2), before every run, outside the events",
+                        "(clean L2), before every run, outside the events; warm_l2_*: the "
+                        "same runs back to back without the flush",
             "reps": args.reps, "peak": peak,
             "peak_kind": peak_kind, "auto": sel, "kernels": out}
     if not args.no_cpu_baseline:
