@@ -291,9 +291,9 @@ int spmv_destroy(spmv_handle h);
 
 /* y <- A*x + y straight from CSR arrays, with no handle and no allocation.
  * (The pages have no counterpart: this entry point exists for callers that
- * cannot allocate device memory -- code running while a stream is captured
- * into a CUDA graph, processes whose device memory is fully reserved by
- * another allocator or pool, real-time loops that forbid allocation.)
+ * cannot allocate device memory -- processes whose device memory is fully
+ * reserved by another allocator or pool, real-time loops that forbid
+ * allocation and the synchronisation it may bring.)
  *   Arguments as spmv_create_csr plus d_x (numCols floats) and d_y (numRows
  *   floats); all device pointers on the current device, x and y not
  *   overlapping. The CSR input is NOT validated: pass arrays that

@@ -1,10 +1,9 @@
 // noalloc.cu -- a one-shot CSR SpMV that allocates nothing.
 //
-// Some callers cannot call cudaMalloc: code that runs while a stream is
-// being captured into a CUDA graph (allocation is not a capturable
-// operation), processes whose device memory is fully reserved by another
-// allocator or a fixed pool, and real-time loops whose rules forbid
-// allocation after start-up. spmv_run_csr_noalloc serves them: it runs
+// Some callers cannot call cudaMalloc: processes whose device memory is
+// fully reserved by another allocator or a fixed pool, and real-time loops
+// whose rules forbid allocation (and the device synchronisation that
+// cudaMalloc and cudaFree may bring) after start-up. spmv_run_csr_noalloc serves them: it runs
 // y <- A*x + y from the caller's CSR arrays without a handle, keeping the
 // per-chunk row index the CSR kernel needs in a fixed array in device global
 // memory that the library reserves for the life of the process.

@@ -53,7 +53,7 @@ __device__ __forceinline__ unsigned* mask_word(CsrChunkDesc* desc, long long W) 
 // Row part. A block walks tiles blk, blk + nbRow, ... of kStatsRows
 // consecutive rows; a lane takes kStatsRowsPerThread consecutive rows, whose
 // kStatsRowsPerThread + 1 row pointers come from two 16-byte loads and one
-// shuffle (rowVec: rowPtrs 16-byte aligned; and the tile whole; scalar loads
+// shuffle (when rowPtrs is 16-byte aligned and the tile whole; scalar loads
 // otherwise). From them, in registers: monotonicity, lengths, min/max/sum of
 // squares, the nonzeros of each 32 consecutive rows (4 lanes), an exact
 // length histogram (lengths < kExactLenBins; one shared add per warp when its
