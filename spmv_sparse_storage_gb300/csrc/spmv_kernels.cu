@@ -585,16 +585,29 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
 
 }  // namespace
 
+// Threads per block of the short-lived kernels (each thread or warp streams
+// its share once and exits). A block's slot on an SM frees only when its
+// last warp ends, so smaller blocks keep more warps resident. Measured with
+// 256 / 128 / 64 threads (cold L2): CSR on the 27-point stencil 191.6 /
+// 178.8 / 172.1 us; ELL on the 5-point Laplacian 38.9 / 36.9 / 36.9 us and
+// on the 27-point stencil 144.0 / 139.0 / 137.9 us; COO on the 27-point
+// stencil 209.5 / 205.1 / 221.8 us; the COO row expansion on the Laplacian
+// 24.2 / 23.3 / 22.4 us.
+constexpr int kCsrBlock = 64;
+constexpr int kCooBlock = 128;
+constexpr int kEllBlock = 64;
+constexpr int kExpandBlock = 64;
+
 cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
                                int* rowIdx, cudaStream_t s) {
   if (R <= 0 || Z <= 0) return cudaSuccess;
   const long long perWarp = (long long)kExpandSupers * kCsrSuper;
   const long long warps = ((long long)Z + perWarp - 1) / perWarp;
-  const unsigned grid = (unsigned)((warps * 32 + 255) / 256);
+  const unsigned grid = (unsigned)((warps * 32 + kExpandBlock - 1) / kExpandBlock);
   if (aligned16(rowIdx))
-    k_expand_rows<true><<<grid, 256, 0, s>>>(Z, rowPtrs, desc, rowIdx);
+    k_expand_rows<true><<<grid, kExpandBlock, 0, s>>>(Z, rowPtrs, desc, rowIdx);
   else
-    k_expand_rows<false><<<grid, 256, 0, s>>>(Z, rowPtrs, desc, rowIdx);
+    k_expand_rows<false><<<grid, kExpandBlock, 0, s>>>(Z, rowPtrs, desc, rowIdx);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -615,11 +628,11 @@ cudaError_t launch_spmv_csr(int R, int Z, const int* rowPtrs, const int* colIdx,
   if (Z <= 0 || R <= 0) return cudaSuccess;
   const bool vec = aligned16(colIdx) && aligned16(value);
   const long long warps = ((long long)Z + kCsrSuper - 1) / kCsrSuper;
-  const unsigned blocks = (unsigned)((warps * 32 + 255) / 256);
+  const unsigned blocks = (unsigned)((warps * 32 + kCsrBlock - 1) / kCsrBlock);
   if (vec)
-    k_spmv_csr_wide<T, true><<<blocks, 256, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
+    k_spmv_csr_wide<T, true><<<blocks, kCsrBlock, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
   else
-    k_spmv_csr_wide<T, false><<<blocks, 256, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
+    k_spmv_csr_wide<T, false><<<blocks, kCsrBlock, 0, s>>>(Z, rowPtrs, colIdx, value, desc, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -629,11 +642,11 @@ cudaError_t launch_spmv_coo(int Z, const int* rowIdx, const int* colIdx, const T
                             const T* x, T* y, bool dependent, cudaStream_t s) {
   if (Z <= 0) return cudaSuccess;
   const long long warps = ((long long)Z + 127) / 128;
-  const long long blocks = (warps * 32 + 255) / 256;
+  const long long blocks = (warps * 32 + kCooBlock - 1) / kCooBlock;
   const bool vec = aligned16(rowIdx) && aligned16(colIdx) && aligned16(value);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)blocks);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kCooBlock);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -657,11 +670,11 @@ cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
   if (R <= 0) return cudaSuccess;
   const bool vec4 = (R % 4 == 0) && aligned16(ellCol) && aligned16(ellVal) && aligned16(y);
   const long long threads = vec4 ? R / 4 : R;
-  const long long blocks = (threads + 255) / 256;
+  const long long blocks = (threads + kEllBlock - 1) / kEllBlock;
   if (vec4)
-    k_spmv_ell<T, true><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
+    k_spmv_ell<T, true><<<(unsigned)blocks, kEllBlock, 0, s>>>(R, K, ellCol, ellVal, x, y);
   else
-    k_spmv_ell<T, false><<<(unsigned)blocks, 256, 0, s>>>(R, K, ellCol, ellVal, x, y);
+    k_spmv_ell<T, false><<<(unsigned)blocks, kEllBlock, 0, s>>>(R, K, ellCol, ellVal, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
