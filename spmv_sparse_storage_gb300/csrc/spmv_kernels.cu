@@ -562,24 +562,27 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
         y[r] = y0 + acc;
     }
   } else {
+    // a tile of kJdsTailRows rows x kJdsTailDiags diagonals, walked by the
+    // block's threads (a row per thread per pass, whatever the block size)
     const int b = blockIdx.x - nMainBlocks;
     const int rb = b % tailRowBlocks;
     const int tb = b / tailRowBlocks;
-    const long long s = (long long)rb * kJdsTailRows + threadIdx.x;
     const int tBeg = tSplit + tb * kJdsTailDiags;
     const int tEnd = min(tBeg + kJdsTailDiags, maxLen);
-    if (s >= wTail) return;
-    T acc = T(0);
-    bool any = false;
-    for (int t = tBeg; t < tEnd; ++t) {
-      const int a = __ldg(iterPtr + t);
-      const int wdt = __ldg(iterPtr + t + 1) - a;
-      if (s >= wdt) break;  // widths shrink: no later diagonal reaches s
-      const long long i = (long long)a + s;
-      acc = fma_t(ld_stream(jdsVal + i), ld_x(x + ld_stream(jdsCol + i)), acc);
-      any = true;
+    const long long sEnd = min((long long)(rb + 1) * kJdsTailRows, (long long)wTail);
+    for (long long s = (long long)rb * kJdsTailRows + threadIdx.x; s < sEnd; s += blockDim.x) {
+      T acc = T(0);
+      bool any = false;
+      for (int t = tBeg; t < tEnd; ++t) {
+        const int a = __ldg(iterPtr + t);
+        const int wdt = __ldg(iterPtr + t + 1) - a;
+        if (s >= wdt) break;  // widths shrink: no later diagonal reaches s
+        const long long i = (long long)a + s;
+        acc = fma_t(ld_stream(jdsVal + i), ld_x(x + ld_stream(jdsCol + i)), acc);
+        any = true;
+      }
+      if (any) atomicAdd(y + perm[s], acc);
     }
-    if (any) atomicAdd(y + perm[s], acc);
   }
 }
 
@@ -592,11 +595,16 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
 // 178.8 / 172.1 us; ELL on the 5-point Laplacian 38.9 / 36.9 / 36.9 us and
 // on the 27-point stencil 144.0 / 139.0 / 137.9 us; COO on the 27-point
 // stencil 209.5 / 205.1 / 221.8 us; the COO row expansion on the Laplacian
-// 24.2 / 23.3 / 22.4 us.
+// 24.2 / 23.3 / 22.4 us; SELL on the Laplacian 47.1 / 44.6 / 43.7 us and on
+// the skewed matrix 138.9 / 133.0 / 131.7 us. JDS stays at 256: no gain on
+// the stencils, and its long-row tail tiles of kJdsTailRows rows lose
+// threads (skewed matrix 169.6 / 217.1 / 309.2 us).
 constexpr int kCsrBlock = 64;
 constexpr int kCooBlock = 128;
 constexpr int kEllBlock = 64;
 constexpr int kExpandBlock = 64;
+constexpr int kJdsBlock = 256;
+constexpr int kSellBlock = 64;
 
 cudaError_t launch_expand_rows(int R, int Z, const int* rowPtrs, const CsrChunkDesc* desc,
                                int* rowIdx, cudaStream_t s) {
@@ -684,7 +692,8 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
                             const int* perm, const int* jdsCol, const T* jdsVal,
                             const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
-  const long long mainBlocks = ((long long)R + 255) / 256;  // a sorted row per thread
+  // a sorted row per thread
+  const long long mainBlocks = ((long long)R + kJdsBlock - 1) / kJdsBlock;
   long long tailBlocks = 0;
   int tailRowBlocks = 1;
   if (tSplit < maxLen && wTail > 0) {
@@ -692,7 +701,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
     const long long diagBlocks = ((long long)(maxLen - tSplit) + kJdsTailDiags - 1) / kJdsTailDiags;
     tailBlocks = (long long)tailRowBlocks * diagBlocks;
   }
-  k_spmv_jds<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+  k_spmv_jds<T><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
       R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, perm, jdsCol, jdsVal, x,
       y);
   note_launches(1);
@@ -931,22 +940,25 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
                              const int* sellCol, const T* sellVal, const SellItem* items,
                              int nItems, const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || S <= 0) return cudaSuccess;
-  const long long tailBlocks = ((long long)nItems + 7) / 8;  // an item per warp
+  constexpr int kSellWarps = kSellBlock / 32;
+  // an item per warp
+  const long long tailBlocks = ((long long)nItems + kSellWarps - 1) / kSellWarps;
   // 8-byte values keep 4 rows per thread (a row per thread measured 229 us
   // against 223 on the 27-point stencil)
   if (sizeof(T) == 4 && (long long)slots > (long long)kSellRowsWide * R) {
-    const long long mainBlocks = ((long long)R + 255) / 256;  // a sorted row per thread
-    k_spmv_sell1<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+    // a sorted row per thread
+    const long long mainBlocks = ((long long)R + kSellBlock - 1) / kSellBlock;
+    k_spmv_sell1<T><<<(unsigned)(mainBlocks + tailBlocks), kSellBlock, 0, s>>>(
         R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
   } else {
     const bool vec = (S & 3) == 0;
     const long long threads = vec ? ((long long)R + 3) / 4 : R;
-    const long long mainBlocks = (threads + 255) / 256;
+    const long long mainBlocks = (threads + kSellBlock - 1) / kSellBlock;
     if (vec)
-      k_spmv_sell4<T, true><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+      k_spmv_sell4<T, true><<<(unsigned)(mainBlocks + tailBlocks), kSellBlock, 0, s>>>(
           R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
     else
-      k_spmv_sell4<T, false><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+      k_spmv_sell4<T, false><<<(unsigned)(mainBlocks + tailBlocks), kSellBlock, 0, s>>>(
           R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
   }
   note_launches(1);
