@@ -111,8 +111,12 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const bool live = e < nLive;
-      int l = p[e + 1] - p[e];
-      if (live && l < 0) firstBad = min(firstBad, (int)(r0 + e));
+      // monotonicity by comparison, not by the sign of a 32-bit difference
+      // (which wraps for far-apart values); with rowPtrs[0] = 0 and
+      // rowPtrs[R] = nnz it confines every row pointer to [0, nnz]
+      const bool dec = p[e + 1] < p[e];
+      if (live && dec) firstBad = min(firstBad, (int)(r0 + e));
+      int l = dec ? 0 : (int)((unsigned)p[e + 1] - (unsigned)p[e]);
       l = l > 0 ? l : 0;
       if (live) {
         lmax = max(lmax, l);
@@ -128,7 +132,7 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
     int pEnd = pBeg;  // p[nLive], by selects (no dynamic register index)
 #pragma unroll
     for (int e = 1; e <= E; ++e) pEnd = e <= nLive ? p[e] : pEnd;
-    int groupNnz = nLive > 0 ? pEnd - pBeg : 0;
+    int groupNnz = nLive > 0 ? (int)((unsigned)pEnd - (unsigned)pBeg) : 0;
     groupNnz += __shfl_xor_sync(kFullMask, groupNnz, 1);
     groupNnz += __shfl_xor_sync(kFullMask, groupNnz, 2);
     gmax = max(gmax, groupNnz);
@@ -143,7 +147,9 @@ __device__ void row_part(int blk, int nbRow, int R, int Z, bool rowVec,
       unsigned cnt = 0u;
 #pragma unroll
       for (int e = 0; e < E; ++e) {
-        const int l = e < nLive ? max(p[e + 1] - p[e], 0) : -1;
+        int l = -1;  // as in the statistics loop above
+        if (e < nLive && p[e + 1] >= p[e]) l = max((int)((unsigned)p[e + 1] - (unsigned)p[e]), 0);
+        else if (e < nLive) l = 0;
         if (l >= kExactLenBins) atomicAdd(&st->histLog2[32 - __clz(l)], 1ull);
         const int key = l < kExactLenBins ? l : -1;
         if (key != cur) {

@@ -355,6 +355,17 @@ def test_validation_errors(sp, orc):
         sp.SPMV_ERR_BAD_ROWPTRS  # row pointers are reported first
     # the same checks the oracle makes
     assert orc.validate(4, 4, np.array([0, 3, 2, 7, 8], np.int32), ci) == oracle.BAD_ROWPTRS
+    # a decrease whose 32-bit difference wraps to a positive value (2e9 -> -2e9),
+    # inside a lane's 8 rows, at a lane boundary and at a 2048-row tile boundary
+    Z = 10
+    ci10, va10 = np.zeros(Z, np.int32), np.ones(Z, np.float32)
+    for at in (1005, 1008, 2048):
+        rp_w = np.zeros(4097, np.int32)
+        rp_w[at] = 2_000_000_000
+        rp_w[at + 1] = -2_000_000_000
+        rp_w[at + 2:] = Z
+        assert orc.validate(4096, 4, rp_w, ci10) == oracle.BAD_ROWPTRS
+        assert _create_status(sp, 4096, 4, rp_w, ci10, va10) == sp.SPMV_ERR_BAD_ROWPTRS, at
 
 
 def test_large_validation_error_position(sp):
