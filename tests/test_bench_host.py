@@ -5,7 +5,6 @@ column), the algorithmic bytes of the conversions, and the rule that a
 committed DRAM-traffic record is dropped once its kernel's source changes."""
 import hashlib
 import json
-import os
 
 import pytest
 
@@ -54,4 +53,3 @@ def test_traffic_record_follows_its_source(tmp_path, monkeypatch):
     assert bench.traffic_record("absent", "k_demo") is None     # no capture
     src.write_text("// kernel source, changed\n")
     assert bench.traffic_record("demo", "k_demo") is None       # stale capture
-
