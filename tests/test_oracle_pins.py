@@ -295,6 +295,16 @@ def test_validate(orc):
     assert orc.validate(4, 4, both, badc) == oracle.BAD_ROWPTRS  # rowPtrs first
 
 
+def test_validate_decrease_that_wraps(orc):
+    # 0, 2e9, -2e9, 10: every 32-bit difference of neighbours is non-negative
+    # after wrapping, yet the sequence decreases; "never decreases" (section
+    # 5.3 of the SpGEMM page) is a comparison of neighbours
+    rp = np.array([0, 2_000_000_000, -2_000_000_000, 10], np.int32)
+    wrapped = rp[1:] - rp[:-1]  # int32 arithmetic wraps
+    assert (wrapped >= 0).all() and not (rp[1:] >= rp[:-1]).all()
+    assert orc.validate(3, 4, rp, np.zeros(10, np.int32)) == oracle.BAD_ROWPTRS
+
+
 # --- row statistics -----------------------------------------------------------
 
 @pytest.mark.parametrize("idx", range(7))
