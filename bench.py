@@ -654,29 +654,43 @@ def time_oracle_spmv(inp, value, x, y0, reps=3):
             "us": round(s_med * 1e6, 1), "GFLOP/s": round(2 * inp.nnz / s_med / 1e9, 4), **host}
 
 
-def time_oracle(inp, budget_s, max_steps=None):
+def time_oracle(inp, budget_s, steps=None, warmup=0):
+    """The oracle doing the step on a row sample of `inp`, sized so that the
+    whole run takes about budget_s. With `steps`, `warmup` untimed steps and
+    then exactly `steps` timed ones; without, timed steps until budget_s has
+    passed (at least one)."""
     import oracle
     orc = oracle.get()
-    # calibrate: size the row sample so one step takes about budget_s / 5
+    # calibrate: the time per row of one step on a small sample
     probe = row_sample(inp, max(1, inp.num_rows // 64))
     t = time.perf_counter()
     oracle_step(orc, probe)
     per_row = (time.perf_counter() - t) / probe.num_rows
-    rows = int(min(inp.num_rows, max(1, (budget_s / 5) / max(per_row, 1e-12))))
+    n_steps = (steps + warmup) if steps else 5
+    rows = int(min(inp.num_rows, max(1, (budget_s / n_steps) / max(per_row, 1e-12))))
     sample = row_sample(inp, rows)
     times = []
-    t_end = time.perf_counter() + budget_s
-    while time.perf_counter() < t_end and (max_steps is None or len(times) < max_steps):
-        t = time.perf_counter()
-        oracle_step(orc, sample)
-        times.append(time.perf_counter() - t)
+    if steps:
+        for _ in range(warmup):
+            oracle_step(orc, sample)
+        for _ in range(steps):
+            t = time.perf_counter()
+            oracle_step(orc, sample)
+            times.append(time.perf_counter() - t)
+    else:
+        t_end = time.perf_counter() + budget_s
+        while not times or time.perf_counter() < t_end:
+            t = time.perf_counter()
+            oracle_step(orc, sample)
+            times.append(time.perf_counter() - t)
     step_s = float(np.median(times))
     b = len(FORMATS) * compulsory_bytes(sample.num_rows, sample.num_rows if
                                         sample.num_rows < inp.num_cols else inp.num_cols,
                                         sample.nnz)
     return {"value": round(b / step_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"rows [0, {sample.num_rows}) of {inp.name} ({sample.nnz} nnz), "
-                      f"whole path per step, median of {len(times)} steps",
+                      f"whole path per step, median of {len(times)} timed steps"
+                      + (f" after {warmup} untimed" if steps and warmup else ""),
             "ms_per_step": round(step_s * 1e3, 3), "steps": len(times), **host_cpu()}
 
 
@@ -685,10 +699,11 @@ def run_reference(args, rank, world):
         return None
     inp = synth.make_workload(args.workload, seed=0)
     budget = max(5.0, min(120.0, 0.5 * (args.steps + args.warmup)))
-    cb = time_oracle(inp, budget_s=budget, max_steps=args.steps + args.warmup)
+    cb = time_oracle(inp, budget_s=budget, steps=args.steps, warmup=args.warmup)
     line = {
         "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s",
-        "n_gpus": world, "steps": cb["steps"], "warmup": 0, "ms_per_step": cb["ms_per_step"],
+        "n_gpus": world, "steps": cb["steps"], "warmup": args.warmup,
+        "ms_per_step": cb["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded generator, seed 0)",
         "config": {"workload": f"{args.workload}: {WORKLOAD_DESC[args.workload]}",
