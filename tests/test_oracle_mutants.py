@@ -70,6 +70,12 @@ MUTANTS = {
     "f64_plain_sum": ("            neumaier_add(&s, &c, p);", "            s += p;"),
     "f64_drops_y0": ("double s = y0[r], c = 0.0, a = fabs(y0[r]);",
                      "double s = 0.0, c = 0.0, a = fabs(y0[r]);"),
+    "csr_rows_y0_by_position": ("y[i] = (double)y0[r] + s;\n        mag[i] = a + fabs((double)y0[r]);",
+                                "y[i] = (double)y0[i] + s;\n        mag[i] = a + fabs((double)y0[i]);"),
+    "csr_rows_skips_first_entry": ("int64_t r = rows[i];\n        double s = 0.0, a = 0.0;\n"
+                                   "        for (int64_t k = rowPtrs[r]; k",
+                                   "int64_t r = rows[i];\n        double s = 0.0, a = 0.0;\n"
+                                   "        for (int64_t k = rowPtrs[r] + 1; k"),
     "sell_row_major": ("                    int64_t i = slots + t * h + j;",
                        "                    int64_t i = slots + j * w + t;"),
     "sell_width_from_last_row": ("        int64_t w = rowPtrs[order[s0] + 1] - rowPtrs[order[s0]];",
@@ -85,6 +91,8 @@ def _pin_calls():
              (pins.test_validate, {}), (pins.test_hyb_auto_width_quantile, {}),
              (pins.test_select_outcomes_described_by_page, {})]
     calls += [(pins.test_spmv_matches_dense_brute_force, {"seed": 0, "case": c})
+              for c in range(len(pins.CASES))]
+    calls += [(pins.test_spmv_rows_matches_dense_brute_force, {"case": c})
               for c in range(len(pins.CASES))]
     calls += [(pins.test_laplace2d_closed_form, {"side": 5})]
     import test_oracle_sell as sell

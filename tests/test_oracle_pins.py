@@ -144,6 +144,36 @@ def test_spmv_matches_dense_brute_force(orc, seed, case):
     assert np.all(mag >= np.abs(inp.y0))
 
 
+def entry_magnitudes(inp):
+    """Per row: sum over its stored entries of |a_k x_col(k)|, plus |y0|."""
+    rows = np.repeat(np.arange(inp.num_rows), np.diff(inp.row_ptrs))
+    mag = np.zeros(inp.num_rows, np.float64)
+    np.add.at(mag, rows, np.abs(inp.value.astype(np.float64) *
+                                inp.x.astype(np.float64)[inp.col_idx]))
+    return mag + np.abs(inp.y0.astype(np.float64))
+
+
+@pytest.mark.parametrize("case", range(len(CASES)))
+def test_spmv_rows_matches_dense_brute_force(orc, case):
+    """The same definition over a chosen list of rows (the form used to check
+    sampled rows of very large matrices): entry i of the result is row
+    rows[i] of A x + y0. The list has repeats, is in no particular order and
+    is shorter than the row count where it can be, so that a result indexed by
+    list position instead of row number fails."""
+    inp = synth.random_csr(3, **CASES[case])
+    R = inp.num_rows
+    rng = np.random.default_rng(100 + case)
+    n = max(1, (2 * R) // 3)
+    rows = rng.integers(0, R, size=n)
+    if n > 2:
+        rows[1] = rows[0]  # a repeat
+        rows[-1] = R - 1   # the last row
+    full = inp.y0.astype(np.float64) + dense_of(inp) @ inp.x.astype(np.float64)
+    y, mag = orc.spmv_csr_rows(rows, inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+    np.testing.assert_allclose(y, full[rows], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(mag, entry_magnitudes(inp)[rows], rtol=1e-12, atol=1e-12)
+
+
 def test_spmv_unit_vectors_give_columns(orc):
     """x = e_j gives y - y0 = column j of A (exactly: one product per entry)."""
     inp = synth.random_csr(5, 17, 13, mean_len=4)
