@@ -17,11 +17,18 @@ y0 and the device-to-host read of its five results are inside the timed
 region; the copies of neighbouring steps overlap the compute on their own
 streams (two device buffer sets).
 
+The default workload is the largest of the five (the 27-point stencil on
+160^3, 109.2M nonzeros). After the timed steps, `per_config` times every
+format's SpMV alone on each of the five workloads with L2 flushed before every
+run (the per-format protocol of --mode kernels, fewer reps), with the
+selector's choice and the fastest format of each.
+
 --impl reference times the CPU oracle (plain single-threaded C, fp64) on the
 same workload and metric, on a bounded row sample per step.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload laplace2d] [--no-e2e] [--no-cpu-baseline]
+                       [--workload stencil27] [--no-e2e] [--no-cpu-baseline]
+                       [--no-per-config]
 """
 from __future__ import annotations
 
@@ -44,7 +51,9 @@ import synth  # noqa: E402
 
 METRIC = ("SpMV fp32 GFLOP/s & effective HBM GB/s (fraction of ~8 TB/s) per format, 1 GB300")
 FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS")
-DEFAULT_WORKLOAD = "laplace2d"
+ALL_FORMATS = ("CSR", "COO", "ELL", "HYB", "JDS", "SELL", "XBLOCK")
+DEFAULT_WORKLOAD = "stencil27"
+CONFIG_ORDER = ("tiny_uniform", "laplace2d", "uniform_random", "skewed", "stencil27")
 WORKLOAD_DESC = {
     "tiny_uniform": "uniform 4096x4096, 8 nnz/row (32,768 nnz)",
     "laplace2d": "2D 5-point Laplacian on 2048x2048, Dirichlet (4,194,304 rows, 20,963,328 nnz)",
@@ -67,8 +76,16 @@ def load_peaks():
 # nominal fp64 rate of a GB300 (the vector unit; no tensor fp64 path)
 FP64_NOMINAL_GFLOPS = 1250.0
 
-# (call, kernel): the kernel with the largest share of the step's ncu launch list
-DOMINANT = ("convert_ell", "k_csr_to_ell")
+# Per workload, (call, kernel): the kernel with the largest share of the
+# step's ncu launch list, and the library call whose CUDA-event time is that
+# kernel's duration (the call launches that kernel alone). Workloads without
+# a launch list take the single-kernel call with the longest event time.
+DOMINANT = {"laplace2d": ("convert_ell", "k_csr_to_ell"),
+            "stencil27": ("convert_ell", "k_csr_to_ell")}
+# calls that launch exactly one kernel of the library (on every workload)
+SINGLE_KERNEL_CALLS = {"convert_ell": "k_csr_to_ell", "convert_coo": "k_expand_rows",
+                       "spmv_CSR": "k_spmv_csr_wide", "spmv_COO": "k_spmv_coo",
+                       "spmv_ELL": "k_spmv_ell"}
 
 
 def traffic_record(workload, kernel):
@@ -168,11 +185,10 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, rank, world, device):
+def run_ours(args, rank, world, device, inp):
     import torch
     import spmv_sparse_storage_gb300 as sp
 
-    inp = synth.make_workload(args.workload, seed=0)
     R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
     stream = torch.cuda.current_stream(device)
     def make_bufs():
@@ -348,12 +364,18 @@ def run_ours(args, rank, world, device):
             calls[nm]["GFLOP/s"] = round(2 * Z / (ms * 1e-3) / 1e9, 1)
     top = max(calls, key=lambda n: calls[n]["ms"])
     best_spmv = min((n for n in calls if n.startswith("spmv_")), key=lambda n: calls[n]["ms"])
-    # The dominant kernel is the one with the largest share of the ncu launch
-    # list (profiles/launches_laplace2d_step.md): k_csr_to_ell, the only
-    # kernel of spmv_convert_ell, so that call's event time is its duration.
-    dom_call, dom_kernel = DOMINANT
+    # The dominant kernel: from the workload's ncu launch list where one is
+    # committed, else the single-kernel call with the longest event time.
+    if args.workload in DOMINANT:
+        dom_call, dom_kernel = DOMINANT[args.workload]
+        dom_source = "largest share of the ncu launch list of this workload's step"
+    else:
+        dom_call = max(SINGLE_KERNEL_CALLS, key=lambda n: calls[n]["ms"])
+        dom_kernel = SINGLE_KERNEL_CALLS[dom_call]
+        dom_source = "longest single-kernel call by CUDA events (no launch list committed)"
     dom_traffic = traffic_record(args.workload, dom_kernel)
     roof = {"bound": "hbm", "kernel": dom_kernel, "kernel_call": dom_call,
+            "kernel_source": dom_source,
             "achieved": calls[dom_call]["GB/s"], "peak": peak, "peak_kind": peak_kind,
             "unit": "GB/s", "frac": calls[dom_call]["frac"],
             "alg_bytes_per_launch": calls[dom_call]["alg_bytes"],
@@ -385,11 +407,51 @@ def run_ours(args, rank, world, device):
     return line
 
 
+class L2Flush:
+    """Leaves L2 cold and clean: writes a buffer of twice the L2 size, then
+    reads another one, so that L2 holds clean lines of neither the matrix nor
+    the vectors (after the write alone, up to the whole L2 is dirty and the
+    timed kernel pays its write-back: 34-40 MB more DRAM writes, ELL on
+    stencil27 143 -> 158 us)."""
+
+    def __init__(self, torch, device):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.dirty = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+        self.clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+
+    def __call__(self, tag=0.0):
+        self.dirty.fill_(float(tag))
+        self.clean.sum()
+
+    def describe(self):
+        n = self.dirty.numel() * 4
+        return f"write {n} B, then read another {n} B (clean L2), before every run"
+
+
+def cold_spmv_times(torch, m, f, x, y, y0, stream, flush, reps, warmup, warm=False):
+    """Median ms of `reps` runs of one format's SpMV after `warmup` untimed
+    ones: y reset to y0 and L2 flushed before every run, outside the CUDA
+    events on the launching stream. warm=True: the same without the flush."""
+    times = []
+    for rep in range(warmup + reps):
+        y.copy_(y0)  # y = y0 before every run, outside the events
+        if not warm:
+            flush(rep)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        m.run(f, x, y, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        if rep >= warmup:
+            times.append(e0.elapsed_time(e1))
+    return float(np.median(times))
+
+
 def run_kernels(args, device):
     """Per-format SpMV timing on one workload: each rep resets y to y0 and
-    flushes L2 (writes a buffer of twice its size, then reads another, so that
-    L2 is left clean) outside the timed events, then times one spmv_run with
-    CUDA events on the launching stream; median over reps. Warm-L2 times
+    flushes L2 (L2Flush) outside the timed events, then times one spmv_run
+    with CUDA events on the launching stream; median over reps. Warm-L2 times
     (the same runs back to back without the flush) are reported apart."""
     import torch
     import spmv_sparse_storage_gb300 as sp
@@ -404,14 +466,7 @@ def run_kernels(args, device):
     x = torch.from_numpy(inp.x.astype(vdt)).to(device)
     y0 = torch.from_numpy(inp.y0.astype(vdt)).to(device)
     y = y0.clone()
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    # cold L2 before every run: write a buffer of twice the L2 size, then read
-    # another one, so that L2 holds clean lines of neither the matrix nor the
-    # vectors (after the write alone, up to the whole L2 is dirty and the timed
-    # kernel pays its write-back: 34-40 MB more DRAM writes, ELL on stencil27
-    # 143 -> 158 us)
-    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
-    flush_clean = torch.ones(2 * l2 // 4 + 1024, dtype=torch.float32, device=device)
+    flush = L2Flush(torch, device)
     peak, peak_kind = load_peaks()
     out = {}
     with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
@@ -420,8 +475,7 @@ def run_kernels(args, device):
         for f in fmts:
             try:
                 m.convert(f, stream=stream, chunk_cols=args.chunk_cols)  # warm (pool, launches)
-                flush.fill_(-1.0)
-                flush_clean.sum()
+                flush()
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -435,33 +489,9 @@ def run_kernels(args, device):
         for f in fmts:
             if f in out:
                 continue
-            times = []
-            for rep in range(args.warmup + args.reps):
-                y.copy_(y0)  # y = y0 before every run, outside the events
-                flush.fill_(float(rep))
-                flush_clean.sum()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                m.run(f, x, y, stream=stream)
-                e1.record(stream)
-                e1.synchronize()
-                if rep >= args.warmup:
-                    times.append(e0.elapsed_time(e1))
-            # warm L2, reported apart: the same runs back to back, y reset, no flush
-            warm = []
-            for rep in range(args.warmup + args.reps):
-                y.copy_(y0)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                m.run(f, x, y, stream=stream)
-                e1.record(stream)
-                e1.synchronize()
-                if rep >= args.warmup:
-                    warm.append(e0.elapsed_time(e1))
-            ms = float(np.median(times))
-            ms_warm = float(np.median(warm))
+            ms = cold_spmv_times(torch, m, f, x, y, y0, stream, flush, args.reps, args.warmup)
+            ms_warm = cold_spmv_times(torch, m, f, x, y, y0, stream, flush, args.reps,
+                                      args.warmup, warm=True)
             gbs = compulsory_bytes(R, C, Z, vb) / (ms * 1e-3) / 1e9
             gflops = 2 * Z / (ms * 1e-3) / 1e9
             gbs_warm = compulsory_bytes(R, C, Z, vb) / (ms_warm * 1e-3) / 1e9
@@ -476,8 +506,7 @@ def run_kernels(args, device):
         sel = m.select()
     line = {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
             "nnz": Z,
-            "l2_flush": f"write {flush.numel() * 4} B, then read another {flush.numel() * 4} B "
-                        "(clean L2), before every run, outside the events; warm_l2_*: the "
+            "l2_flush": flush.describe() + ", outside the events; warm_l2_*: the "
                         "same runs back to back without the flush",
             "reps": args.reps, "peak": peak,
             "peak_kind": peak_kind, "auto": sel, "kernels": out}
@@ -485,6 +514,59 @@ def run_kernels(args, device):
         line["cpu_baseline"] = time_oracle_spmv(inp, inp.value.astype(vdt), inp.x.astype(vdt),
                                                 inp.y0.astype(vdt))
     return line
+
+
+def per_config_table(args, device, inputs):
+    """Every format's SpMV alone on each of the five workloads, cold L2
+    (cold_spmv_times: y reset, L2 flushed before every run), with the
+    selector's choice and the fastest format. `inputs` maps workload names to
+    already generated inputs (others are generated here)."""
+    import torch
+    import spmv_sparse_storage_gb300 as sp
+    stream = torch.cuda.current_stream(device)
+    flush = L2Flush(torch, device)
+    peak, _ = load_peaks()
+    table = {}
+    for w in CONFIG_ORDER:
+        inp = inputs.get(w) or synth.make_workload(w, seed=0)
+        R, C, Z = inp.num_rows, inp.num_cols, inp.nnz
+        cb = compulsory_bytes(R, C, Z)
+        rp = torch.from_numpy(inp.row_ptrs).to(device)
+        ci = torch.from_numpy(inp.col_idx).to(device)
+        va = torch.from_numpy(inp.value).to(device)
+        x = torch.from_numpy(inp.x).to(device)
+        y0 = torch.from_numpy(inp.y0).to(device)
+        y = y0.clone()
+        fm = {}
+        with sp.SparseMatrix(R, C, rp, ci, va, stream) as m:
+            for f in ALL_FORMATS:
+                try:
+                    if f != "CSR":
+                        m.convert(f, stream=stream)
+                except sp.SpmvError as e:
+                    fm[f] = {"error": str(e)}
+                    continue
+                ms = cold_spmv_times(torch, m, f, x, y, y0, stream, flush, args.config_reps,
+                                     args.config_warmup)
+                gbs = cb / (ms * 1e-3) / 1e9
+                fm[f] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                         "frac": round(gbs / peak, 4),
+                         "GFLOP/s": round(2 * Z / (ms * 1e-3) / 1e9, 1)}
+            auto, width = m.select()
+        timed = {f: v["us"] for f, v in fm.items() if "us" in v}
+        best = min(timed, key=timed.get)
+        table[w] = {"rows": R, "cols": C, "nnz": Z, "compulsory_bytes": cb, "formats": fm,
+                    "auto": auto, "auto_hyb_width": width, "auto_us": timed.get(auto),
+                    "best": best, "best_us": timed[best], "best_frac": fm[best]["frac"],
+                    "auto_over_best": round(timed[auto] / timed[best], 4)
+                    if auto in timed else None}
+        del rp, ci, va, x, y0, y
+        torch.cuda.empty_cache()
+    return {"protocol": f"each format's spmv_run alone, median of {args.config_reps} runs after "
+                        f"{args.config_warmup}; y reset and L2 flushed ({flush.describe()}) "
+                        "before every run, outside the CUDA events; fraction of the measured "
+                        "copy peak",
+            "configs": table}
 
 
 def cg_alg_bytes(R, slots):
@@ -595,7 +677,7 @@ def oracle_step(orc, inp):
     K = orc.hyb_auto_width(rp)
     hyb = orc.csr_to_hyb(rp, ci, va, K)
     jds = orc.csr_to_jds(rp, ci, va)
-    orc.select(R, inp.nnz, st["max_len"])
+    orc.select(R, inp.num_cols, inp.nnz, st["max_len"], 0.0)
     orc.spmv_csr(rp, ci, va, x, y0)
     orc.spmv_coo(R, coo["row_idx"], coo["col_idx"], coo["value"], x, y0)
     orc.spmv_ell(ell, x, y0)
@@ -654,6 +736,15 @@ def time_oracle_spmv(inp, value, x, y0, reps=3):
             "us": round(s_med * 1e6, 1), "GFLOP/s": round(2 * inp.nnz / s_med / 1e9, 4), **host}
 
 
+def sample_bytes(sample):
+    """Compulsory SpMV bytes of a row sample: value and column per nonzero,
+    rowPtrs and y per row, and the x entries it reads once (the distinct
+    columns its nonzeros reference; a row sample of a banded matrix reads only
+    part of x)."""
+    cols = int(np.unique(sample.col_idx).size) if sample.nnz else 0
+    return 8 * sample.nnz + 12 * sample.num_rows + 4 * cols
+
+
 def time_oracle(inp, budget_s, steps=None, warmup=0):
     """The oracle doing the step on a row sample of `inp`, sized so that the
     whole run takes about budget_s. With `steps`, `warmup` untimed steps and
@@ -684,13 +775,13 @@ def time_oracle(inp, budget_s, steps=None, warmup=0):
             oracle_step(orc, sample)
             times.append(time.perf_counter() - t)
     step_s = float(np.median(times))
-    b = len(FORMATS) * compulsory_bytes(sample.num_rows, sample.num_rows if
-                                        sample.num_rows < inp.num_cols else inp.num_cols,
-                                        sample.nnz)
+    b = len(FORMATS) * sample_bytes(sample)
     return {"value": round(b / step_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
             "sample": f"rows [0, {sample.num_rows}) of {inp.name} ({sample.nnz} nnz), "
                       f"whole path per step, median of {len(times)} timed steps"
-                      + (f" after {warmup} untimed" if steps and warmup else ""),
+                      + (f" after {warmup} untimed" if steps and warmup else "")
+                      + "; bytes: 8 per nonzero, 12 per row, 4 per distinct column "
+                        "the sample references (its share of x)",
             "ms_per_step": round(step_s * 1e3, 3), "steps": len(times), **host_cpu()}
 
 
@@ -737,6 +828,10 @@ def main():
                     help="XBLOCK chunk width B (0: the library default)")
     ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL,XBLOCK")
     ap.add_argument("--reps", type=int, default=50)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="step mode: skip the per-format table of the five workloads")
+    ap.add_argument("--config-reps", type=int, default=10)
+    ap.add_argument("--config-warmup", type=int, default=3)
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -771,10 +866,12 @@ def main():
             fn = run_kernels if args.mode == "kernels" else run_cg
             print(json.dumps(fn(args, device)), flush=True)
         return
-    line = run_ours(args, rank, world, device)
+    inp = synth.make_workload(args.workload, seed=0)
+    line = run_ours(args, rank, world, device, inp)
     if rank == 0:
+        if not args.no_per_config:
+            line["per_config"] = per_config_table(args, device, {args.workload: inp})
         if not args.no_cpu_baseline:
-            inp = synth.make_workload(args.workload, seed=0)
             line["cpu_baseline"] = time_oracle(inp, budget_s=args.cpu_seconds)
         print(json.dumps(line), flush=True)
     if world > 1:

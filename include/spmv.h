@@ -176,8 +176,11 @@ int spmv_convert_ell(spmv_handle h, void *stream);
  * min(len, K) entries of each row, and a COO part with every row's remaining
  * entries in row order, then in-row order. ellWidth = 0 picks K as the
  * smallest L such that 99% of the rows have length <= L; ellWidth > 0 is used
- * as given (capped at the longest row). Same size limits as ELL. Async
- * except for one small device-to-host read of the COO part's size. */
+ * as given (capped at the longest row). Same size limits as ELL.
+ * Asynchronous when K < 1024: the COO part's size then follows from the
+ * exact row-length histogram taken by spmv_create_csr. With K >= 1024 the
+ * size is computed on the device and read back, which SYNCHRONISES `stream`
+ * once. */
 int spmv_convert_hyb(spmv_handle h, int32_t ellWidth, void *stream);
 
 /* CSR -> JDS ("JDS format", steps 1-4): perm sorts the rows by length,
@@ -194,9 +197,10 @@ int spmv_convert_jds(spmv_handle h, void *stream);
  * sec_ptr[k] + t*h_k + j (column-major inside the section), padding as ELL
  * (column -1, value +0.0f). sectionRows = 0 picks S = 128; sectionRows < 0 is
  * SPMV_ERR_INVALID_ARG. Returns SPMV_ERR_TOO_LARGE (nothing kept) when the
- * slot count exceeds INT32_MAX or 4*nnz + numRows. Asynchronous, except for
- * one device-to-host read of the section widths when some row has 1024 or
- * more entries. */
+ * slot count exceeds INT32_MAX or 4*nnz + numRows. Asynchronous when every
+ * row has fewer than 1024 entries (the section widths then follow from the
+ * exact row-length histogram). Otherwise the widths are computed on the
+ * device after the sort and read back, which SYNCHRONISES `stream` once. */
 int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void *stream);
 
 /* CSR -> XBLOCK ("Introduction to sparse computing and performance bottleneck
@@ -269,12 +273,17 @@ typedef struct {
 int spmv_cg_solve(spmv_handle h, spmv_format format, const float *d_y, float *d_x,
                   int32_t maxIter, double tol, spmv_cg_info *info, void *stream);
 
-/* Format choice from the row-length statistics ("[CUDA performance tuning]
- * SpMV storage format selection and performance comparison", section 4.3;
- * its comparison operators are lost in the page, the reading is):
+/* Format choice from the statistics of spmv_create_csr ("[CUDA performance
+ * tuning] SpMV storage format selection and performance comparison", section
+ * 4.3; its comparison operators are lost in the page, the reading is):
  * longest <= 2*mean -> ELL; else mean < 10 -> COO; else HYB when
- * longest > 5*mean, otherwise CSR. *ellWidth gets the automatic HYB width.
- * Host-only; either output pointer may be NULL. */
+ * longest > 5*mean, otherwise CSR. Two rules of this library come around it:
+ * compulsory SpMV bytes (8 per nonzero + 12 per row + 4 per column) below
+ * 4 MiB -> CSR, checked first (a matrix that small is bound by memory round
+ * trips, not bandwidth); and in the HYB case, scattered columns
+ * (stats.gather_lines >= 16) -> XBLOCK, the x-blocked list. The chosen format
+ * must be converted before spmv_run(SPMV_AUTO). *ellWidth gets the automatic
+ * HYB width. Host-only; either output pointer may be NULL. */
 int spmv_select(spmv_handle h, spmv_format *format, int32_t *ellWidth);
 
 /* Copy the statistics computed at creation into *out (host). */
@@ -302,9 +311,15 @@ int spmv_destroy(spmv_handle h);
  *   memory reserved by the library (1 MiB on every GPU that loads it, held
  *   until the process exits), so nnz is limited to 4,194,304 (32768 chunks of
  *   128); a larger nnz returns SPMV_ERR_TOO_LARGE and does nothing.
- *   Set-up: the first call on a device (with that device current) looks up
- *   the array's device address; make that first call before any stream
- *   capture. Calls neither allocate nor free memory.
+ *   Set-up: the first call with nnz > 0 on a device (with that device
+ *   current) looks up the array's device address. That is also when the
+ *   array and the kernels this call launches take their device memory (CUDA
+ *   loads a module on its first use), so a caller whose other allocator
+ *   reserves the device should make one such call at start-up, before that
+ *   reservation (any small valid matrix will do), and before any stream
+ *   capture. Later calls neither allocate nor free memory. A CUDA failure
+ *   returns SPMV_ERR_CUDA (SPMV_ERR_ALLOC when it is an out-of-memory error),
+ *   with the cudaError_t in spmv_last_cuda_error().
  *   Concurrency: every call reuses the same array, so calls that overlap on
  *   the GPU (different streams, no ordering between them) race and give
  *   wrong results; calls ordered on one stream are fine.

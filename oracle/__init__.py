@@ -64,12 +64,12 @@ _SIGS = {
     "or_spmv_xblock": (None, [_i64, _i64, _i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_spmv_csr_f64": (None, [_i64, _p, _p, _p, _p, _p, _p, _p]),
     "or_cg_csr": (_i64, [_i64, _p, _p, _p, _p, _p, _i64, C.c_double, _p, _p, _p]),
-    "or_select": (C.c_int, [_i64, _i64, _i64]),
+    "or_select": (C.c_int, [_i64, _i64, _i64, _i64, C.c_double]),
     "or_hyb_auto_width": (_i64, [_i64, _p, _i64]),
 }
 
 OK, BAD_ARG, BAD_ROWPTRS, COL_RANGE, NO_MEMORY = 0, 1, 2, 3, 4
-FORMAT_NAMES = {0: "COO", 1: "CSR", 2: "ELL", 3: "HYB"}
+FORMAT_NAMES = {0: "COO", 1: "CSR", 2: "ELL", 3: "HYB", 7: "XBLOCK"}
 
 _lib = None
 
@@ -381,8 +381,9 @@ class Oracle:
         return y
 
     # --- selection -----------------------------------------------------------
-    def select(self, num_rows, nnz, max_len):
-        return FORMAT_NAMES[self.lib.or_select(num_rows, nnz, max_len)]
+    def select(self, num_rows, num_cols, nnz, max_len, gather_lines):
+        return FORMAT_NAMES[self.lib.or_select(num_rows, num_cols, nnz, max_len,
+                                               float(gather_lines))]
 
     def hyb_auto_width(self, row_ptrs):
         rp = _i32(row_ptrs)

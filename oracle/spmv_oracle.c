@@ -403,13 +403,22 @@ void or_spmv_jds(int64_t R, int64_t maxLen, const int32_t *perm,
 /* Format selection, [P3] section 4.3. The page's comparison operators are
  * lost in extraction; the reading used here is: longest row <= 2 x mean ->
  * ELL; else mean < 10 -> COO; else HYB when longest > 5 x mean, otherwise
- * CSR. (parity unpinned: the thresholds' directions are a reading.)
- * Format codes: 0 COO, 1 CSR, 2 ELL, 3 HYB. */
-int or_select(int64_t R, int64_t Z, int64_t maxLen) {
+ * CSR. Two rules of ours come around it: a matrix whose compulsory SpMV
+ * bytes (8 per nonzero, 12 per row, 4 per column) are below 4 MiB -> CSR
+ * (too small to be bound by bandwidth: the format with the fewest dependent
+ * memory round trips), checked first; and in the HYB case, columns that are
+ * scattered (gatherLines, the sampled number of distinct 128-byte lines of x
+ * among 32 consecutive nonzeros, at least 16) -> the x-blocked list of
+ * "Introduction to sparse computing and performance bottleneck location".
+ * (parity unpinned: the thresholds and their directions are a reading.)
+ * Format codes as the library's: 0 COO, 1 CSR, 2 ELL, 3 HYB, 7 XBLOCK. */
+int or_select(int64_t R, int64_t C, int64_t Z, int64_t maxLen, double gatherLines) {
     double mean = R > 0 ? (double)Z / (double)R : 0.0;
+    if (8.0 * (double)Z + 12.0 * (double)R + 4.0 * (double)C < 4194304.0) return 1;
     if ((double)maxLen <= 2.0 * mean) return 2;
     if (mean < 10.0) return 0;
-    return (double)maxLen > 5.0 * mean ? 3 : 1;
+    if ((double)maxLen > 5.0 * mean) return gatherLines >= 16.0 ? 7 : 3;
+    return 1;
 }
 
 /* Automatic HYB width: the smallest L such that at least 99% of the rows

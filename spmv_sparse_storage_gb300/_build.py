@@ -19,7 +19,8 @@ LIB_DIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIB_DIR, "libspmv_gb300.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "stats.cu", "convert.cu", "spmv_kernels.cu", "noalloc.cu", "cg.cu"]
+SOURCES = ["api.cu", "stats.cu", "convert.cu", "ell_convert.cu", "spmv_kernels.cu", "noalloc.cu",
+           "cg.cu"]
 
 
 def nvcc() -> str:

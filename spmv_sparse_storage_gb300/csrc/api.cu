@@ -126,6 +126,8 @@ int check_device_ptr(const void* p, int dev) {
 namespace spmv {
 void note_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
+int record_cuda(cudaError_t e) { return record(e); }
+
 int num_sms() {
   int dev = 0;
   cudaGetDevice(&dev);
@@ -289,12 +291,27 @@ int alloc_typed(spmv_handle h, long long n, cudaStream_t s, T** out, std::vector
 // Format choice ("[CUDA performance tuning] SpMV storage format selection and
 // performance comparison", section 4.3). The page's comparison operators are
 // lost; the reading: longest <= 2*mean -> ELL, else mean < 10 -> COO, else
-// HYB when longest > 5*mean, otherwise CSR.
-int select_format(long long R, long long Z, long long maxLen) {
+// HYB when longest > 5*mean, otherwise CSR. Two rules of ours around it,
+// from measurements on GB300 (the fastest format of each workload type):
+//  - compulsory SpMV bytes below kSmallMatrixBytes -> CSR, first: such a
+//    matrix is bound by dependent memory round trips, not bandwidth, and the
+//    nnz-balanced CSR kernel has the fewest (4096 x 4096 with 8 per row:
+//    CSR 6.8 us, ELL 10.9 us);
+//  - in the HYB case, scattered columns (gatherLines >= kScatteredLines: the
+//    sampled distinct 128-byte lines of x among 32 consecutive nonzeros) ->
+//    XBLOCK, whose gathers come from shared memory ("Introduction to sparse
+//    computing and performance bottleneck location", x-blocking): 2M rows of
+//    10-20 random columns plus 200 rows of 1000-5000, XBLOCK 113 us against
+//    HYB 120 us.
+constexpr double kSmallMatrixBytes = 4194304.0;
+constexpr double kScatteredLines = 16.0;
+int select_format(long long R, long long C, long long Z, long long maxLen, double gatherLines) {
   const double mean = R > 0 ? (double)Z / (double)R : 0.0;
+  if (8.0 * (double)Z + 12.0 * (double)R + 4.0 * (double)C < kSmallMatrixBytes) return SPMV_CSR;
   if ((double)maxLen <= 2.0 * mean) return SPMV_ELL;
   if (mean < 10.0) return SPMV_COO;
-  return (double)maxLen > 5.0 * mean ? SPMV_HYB : SPMV_CSR;
+  if ((double)maxLen > 5.0 * mean) return gatherLines >= kScatteredLines ? SPMV_XBLOCK : SPMV_HYB;
+  return SPMV_CSR;
 }
 
 // Automatic HYB width: smallest L with 100 * #{len <= L} >= 99 * R (section
@@ -376,20 +393,22 @@ int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
   if (st != SPMV_OK) return fail(st);
   DevStats* hst = pinned_stats_buffer();
   if (!hst) return fail(SPMV_ERR_ALLOC);
-  void* work = nullptr;
-  st = h->alloc(spmv::stats_work_bytes(numRows, nnz, d_colIdx), s, &work, tmp);
-  if (st != SPMV_OK) return fail(st);
-  st = record(cudaMemsetAsync(work, 0, spmv::stats_zero_bytes(), s));
-  if (st != SPMV_OK) return fail(st);
-  // nnz-balanced split for the CSR kernel, written by the statistics pass
-  // (which checks bounds, so it stays in bounds even if validation fails)
+  // One allocation, zeroed by one memset: the statistics record (its work
+  // area, a multiple of 256 bytes) followed by the nnz-balanced split for the
+  // CSR kernel, whose masks and flags the statistics pass ORs into zeroed
+  // records (it checks bounds, so it stays in bounds even if validation
+  // fails). Both stay with the handle.
   h->nChunks = (int)(((long long)nnz + spmv::kCsrChunk - 1) / spmv::kCsrChunk);
-  st = alloc_typed(h, (long long)h->nChunks, s, &h->chunkDesc, h->csrBufs);
+  const size_t statsBytes = spmv::stats_work_bytes(numRows, nnz, d_colIdx);
+  const size_t zeroBytes = statsBytes + sizeof(spmv::CsrChunkDesc) * (size_t)h->nChunks;
+  void* work = nullptr;
+  st = h->alloc(zeroBytes, s, &work, h->csrBufs);
   if (st != SPMV_OK) return fail(st);
-  if (h->nChunks > 0) {  // masks and flags are OR-ed into zeroed records
-    st = record(cudaMemsetAsync(h->chunkDesc, 0, sizeof(spmv::CsrChunkDesc) * h->nChunks, s));
-    if (st != SPMV_OK) return fail(st);
-  }
+  st = record(cudaMemsetAsync(work, 0, zeroBytes, s));
+  if (st != SPMV_OK) return fail(st);
+  h->chunkDesc = h->nChunks > 0 ? reinterpret_cast<spmv::CsrChunkDesc*>(
+                                      static_cast<char*>(work) + statsBytes)
+                                : nullptr;
   st = record(spmv::launch_stats(numRows, numCols, nnz, d_rowPtrs, d_colIdx, work, h->nChunks,
                                  h->chunkDesc, s));
   if (st != SPMV_OK) return fail(st);
@@ -430,7 +449,7 @@ int create_impl(spmv_handle* out, int32_t numRows, int32_t numCols, int32_t nnz,
   }
   h->histExact.assign(hst->histExact, hst->histExact + spmv::kExactLenBins);
   S.gather_lines = hst->gatherSets ? (double)hst->gatherLines / (double)hst->gatherSets : 0.0;
-  S.auto_format = select_format(numRows, nnz, S.max_len);
+  S.auto_format = select_format(numRows, numCols, nnz, S.max_len, S.gather_lines);
   S.auto_hyb_width = auto_hyb_width(h);
   h->release(tmp, s);
   *out = h;

@@ -37,34 +37,6 @@ __device__ __forceinline__ int find_segment(int start, int k) {
   return j;
 }
 
-// CSR -> ELL of width K (also the ELL part of HYB): thread per row, writes
-// coalesced across rows. Padding slots get column -1 and value +0.0f.
-template <class T>
-__global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __restrict__ rowPtrs,
-                                                    const int* __restrict__ colIdx,
-                                                    const T* __restrict__ value,
-                                                    int* __restrict__ ellCol,
-                                                    T* __restrict__ ellVal,
-                                                    int* __restrict__ nnzPerRow) {
-  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= R) return;
-  const int a = rowPtrs[r];
-  const int len = rowPtrs[r + 1] - a;
-  const int kept = len < K ? len : K;
-  nnzPerRow[r] = kept;
-  for (int t = 0; t < K; ++t) {
-    const size_t i = (size_t)t * (size_t)R + (size_t)r;
-    int c = -1;
-    T v = T(0);
-    if (t < kept) {
-      c = colIdx[a + t];
-      v = value[a + t];
-    }
-    __stcs(ellCol + i, c);
-    __stcs(ellVal + i, v);
-  }
-}
-
 // HYB COO part: row r's entries at in-row positions >= K, written at
 // tailPtr[r] ... in row order (warp-cooperative expansion as above).
 template <class T>
@@ -84,8 +56,9 @@ __global__ void __launch_bounds__(256) k_hyb_tail_copy(int R, int K, const int* 
   const int src = r < R ? rowPtrs[r] + K : 0;
   const int A = __shfl_sync(kFullMask, start, 0);
   const int B = tailPtr[min(r0 + 32, (long long)R)];
-  for (int base = A; base < B; base += 32) {
-    const int o = base + lane;
+  // 64-bit counter: B may lie within one step of INT32_MAX
+  for (long long base = A; base < B; base += 32) {
+    const int o = (int)min(base + lane, (long long)B);  // o == B: no entry
     const int j = find_segment(start, o);
     const int sj = __shfl_sync(kFullMask, start, j);
     const int srcj = __shfl_sync(kFullMask, src, j);
@@ -462,22 +435,38 @@ __global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKe
 // length have consecutive sorted positions, so the writes of a warp are
 // contiguous per diagonal. A thread copies the first kCoop entries of its
 // row; the warp then copies each longer row's remaining entries together,
-// one entry per lane. The first kJdsScatterSmem entries of iterPtr are
-// staged in shared memory.
+// one entry per lane. The first kJdsScatterSmem entries of iterPtr are staged
+// in shared memory. (Loads issued 8 at a time before their stores, and the
+// block's entries staged in shared memory, measured no faster.)
 constexpr int kCoop = 64;
 constexpr int kJdsScatterSmem = 1024;
+// iterPtr passed by value when the host knows it and it is short (longest
+// row below kIpArg): block 0 writes it to memory, every block reads it from
+// its arguments. n = 0: iterPtr is already in memory.
+constexpr int kIpArg = 256;
+struct IterPtrArg {
+  int n;
+  int v[kIpArg];
+};
 template <class T>
 __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
                                                      const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
                                                      const T* __restrict__ value,
                                                      const int* __restrict__ inv,
-                                                     const int* __restrict__ iterPtr,
+                                                     int* __restrict__ iterPtr,
+                                                     const __grid_constant__ IterPtrArg ipArg,
                                                      int* __restrict__ jdsCol,
                                                      T* __restrict__ jdsVal) {
   __shared__ int sIp[kJdsScatterSmem];
   const int nIp = maxLen < kJdsScatterSmem ? maxLen : kJdsScatterSmem;
-  for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = iterPtr[t];
+  if (ipArg.n > 0) {  // n = maxLen + 1 <= kIpArg
+    for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = ipArg.v[t];
+    if (blockIdx.x == 0)
+      for (int t = threadIdx.x; t < ipArg.n; t += blockDim.x) iterPtr[t] = ipArg.v[t];
+  } else {
+    for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = iterPtr[t];
+  }
   __syncthreads();
   const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   const int lane = threadIdx.x & 31;
@@ -500,7 +489,7 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
     const int la = __shfl_sync(kFullMask, a, src);
     const int ll = __shfl_sync(kFullMask, len, src);
     const int ls = __shfl_sync(kFullMask, srow, src);
-    for (int t = kCoop + lane; t < ll; t += 32) {
+    for (long long t = kCoop + lane; t < ll; t += 32) {  // 64-bit: ll may be near INT32_MAX
       const int ip = t < kJdsScatterSmem ? sIp[t] : __ldg(iterPtr + t);
       const long long o = (long long)ip + ls;
       jdsCol[o] = colIdx[la + t];
@@ -511,26 +500,12 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
 
 }  // namespace
 
-// Threads per block of the CSR -> ELL scatter and the HYB tail copy (128 and
-// 64 measured slower: CSR -> ELL on the 27-point stencil 325 / 338 / 332 us
-// with 256 / 128 / 64 threads, the HYB conversion of the skewed matrix 197 /
-// 218 / 209 us).
-constexpr int kCsrToEllBlock = 256;
+// Threads per block of the HYB tail copy (128 and 64 measured slower: the
+// HYB conversion of the skewed matrix 197 / 218 / 209 us with 256 / 128 / 64
+// threads).
 constexpr int kTailBlock = 256;
 
 size_t scan_scratch_ints(long long n) { return (size_t)((n + kScanTile - 1) / kScanTile + 1); }
-
-template <class T>
-cudaError_t launch_csr_to_ell(int R, int K, const int* rowPtrs, const int* colIdx,
-                              const T* value, int* ellCol, T* ellVal, int* nnzPerRow,
-                              cudaStream_t s) {
-  if (R <= 0) return cudaSuccess;
-  const long long blocks = ((long long)R + kCsrToEllBlock - 1) / kCsrToEllBlock;
-  k_csr_to_ell<T><<<(unsigned)blocks, kCsrToEllBlock, 0, s>>>(R, K, rowPtrs, colIdx, value,
-                                                              ellCol, ellVal, nnzPerRow);
-  note_launches(1);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_tail_scan(int R, int K, const int* rowPtrs, int* tailPtr, int* scratch,
                              cudaStream_t s) {
@@ -648,8 +623,13 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
   if (err != cudaSuccess) return err;
   int* width = scanScratch + scan_scratch_ints(scanN);
   if (maxLen > 0) {
-    if (hostIterPtr) {
-      // widths known exactly on the host from the length histogram
+    IterPtrArg ipArg;
+    ipArg.n = 0;
+    if (hostIterPtr && maxLen + 1 <= kIpArg) {
+      // known exactly on the host from the length histogram: kernel argument
+      ipArg.n = maxLen + 1;
+      for (int t = 0; t <= maxLen; ++t) ipArg.v[t] = hostIterPtr[t];
+    } else if (hostIterPtr) {
       err = cudaMemcpyAsync(iterPtr, hostIterPtr, sizeof(int) * ((size_t)maxLen + 1),
                             cudaMemcpyHostToDevice, s);
       if (err != cudaSuccess) return err;
@@ -661,7 +641,7 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
       if (err != cudaSuccess) return err;
     }
     k_jds_scatter<T><<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
-        R, maxLen, rowPtrs, colIdx, value, inv, iterPtr, jdsCol, jdsVal);
+        R, maxLen, rowPtrs, colIdx, value, inv, iterPtr, ipArg, jdsCol, jdsVal);
     note_launches(1);
   } else {
     err = cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
@@ -772,8 +752,8 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
     const int lh = __shfl_sync(kFullMask, h, src);
     const int lj = __shfl_sync(kFullMask, j, src);
     const int lb = __shfl_sync(kFullMask, base, src);
-    for (int t = kCoop + lane; t < lw; t += 32) {
-      const long long o = (long long)lb + (long long)t * lh + lj;
+    for (long long t = kCoop + lane; t < lw; t += 32) {  // 64-bit: lw may be near INT32_MAX
+      const long long o = (long long)lb + t * lh + lj;
       const bool real = t < ll;
       sellCol[o] = real ? colIdx[la + t] : -1;
       sellVal[o] = real ? value[la + t] : T(0);
@@ -922,8 +902,6 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* v
 
 // the two value types
 #define SPMV_INSTANTIATE(T)                                                                      \
-  template cudaError_t launch_csr_to_ell<T>(int, int, const int*, const int*, const T*, int*,   \
-                                            T*, int*, cudaStream_t);                             \
   template cudaError_t launch_hyb_tail_copy<T>(int, int, const int*, const int*, const T*,      \
                                                const int*, int*, int*, T*, cudaStream_t);        \
   template cudaError_t launch_jds_build<T>(int, int, const int*, const int*, const T*, int*,    \

@@ -97,3 +97,4 @@ __device__ __forceinline__ int warp_min(int v) {
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace spmv
+

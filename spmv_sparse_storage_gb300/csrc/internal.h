@@ -49,9 +49,8 @@ inline unsigned stats_errors(const DevStats& d) {
 inline int stats_min_len(const DevStats& d) { return 2147483647 - d.minLenKey; }
 
 // Work area of the statistics pass: the DevStats record (read back by the
-// host); its first stats_zero_bytes() bytes must be zeroed before launch_stats.
+// host), a multiple of 256 bytes, zeroed before launch_stats.
 size_t stats_work_bytes(int R, int Z, const int* colIdx);
-size_t stats_zero_bytes();
 
 // ---------------------------------------------------------------------------
 // CSR work split: the nonzeros in chunks of kCsrChunk, each described by a
@@ -78,6 +77,10 @@ constexpr int kJdsTailDiags = 64;        // tail blocks: diagonals per block
 // ---------------------------------------------------------------------------
 void note_launches(int n);
 int num_sms();
+// A CUDA result as a library status: cudaSuccess -> SPMV_OK; otherwise the
+// error is kept for spmv_last_cuda_error() on this thread and mapped to
+// SPMV_ERR_ALLOC (out of memory) or SPMV_ERR_CUDA.
+int record_cuda(cudaError_t e);
 
 // ---------------------------------------------------------------------------
 // Launchers. Each returns the cudaError_t of its launches.

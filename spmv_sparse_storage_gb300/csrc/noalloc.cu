@@ -18,6 +18,10 @@ namespace {
 // Shared scratch: one record per kCsrChunk nonzeros, at most
 // kNoAllocMaxChunks of them (1 MiB per GPU that loads the library). Every
 // call overwrites what it uses; calls that overlap on the GPU race on it.
+// Under CUDA's lazy module loading the array (and the kernels) take their
+// device memory when this module is first loaded on a device, i.e. at the
+// first call with nnz > 0 there (cudaGetSymbolAddress below), not when the
+// library is loaded.
 constexpr int kNoAllocMaxChunks = 32768;  // nnz <= 4,194,304
 static __device__ __align__(256) CsrChunkDesc g_noallocDesc[kNoAllocMaxChunks];
 
@@ -67,20 +71,23 @@ extern "C" int spmv_run_csr_noalloc(int32_t numRows, int32_t numCols, int32_t nn
   const long long nChunks = ((long long)nnz + kCsrChunk - 1) / kCsrChunk;
   if (nChunks > kNoAllocMaxChunks) return SPMV_ERR_TOO_LARGE;
   if (numRows == 0 || nnz == 0) return SPMV_OK;
+  // every CUDA failure goes through record_cuda, so that spmv_last_cuda_error()
+  // names it
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPMV_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return SPMV_ERR_INVALID_ARG;
   CsrChunkDesc* desc = nullptr;
   e = scratch_for_device(dev, &desc);
-  if (e != cudaSuccess) return SPMV_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda(e);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   k_noalloc_chunk_lo<<<(unsigned)(((long long)numRows + 255) / 256), 256, 0, s>>>(
       numRows, nnz, d_rowPtrs, (int)nChunks, desc);
   note_launches(1);
   e = cudaGetLastError();
-  if (e != cudaSuccess) return SPMV_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda(e);
   e = launch_csr_chunk_masks(numRows, nnz, d_rowPtrs, (int)nChunks, desc, s);
-  if (e != cudaSuccess) return SPMV_ERR_CUDA;
-  e = launch_spmv_csr(numRows, nnz, d_rowPtrs, d_colIdx, d_value, desc, d_x, d_y, s);
-  return e == cudaSuccess ? SPMV_OK : SPMV_ERR_CUDA;
+  if (e != cudaSuccess) return record_cuda(e);
+  return record_cuda(
+      launch_spmv_csr(numRows, nnz, d_rowPtrs, d_colIdx, d_value, desc, d_x, d_y, s));
 }

@@ -359,7 +359,6 @@ int col_blocks(int Z, bool vec) {
 
 size_t stats_work_bytes(int, int, const int*) { return kWorkBytes; }
 
-size_t stats_zero_bytes() { return sizeof(DevStats); }
 
 cudaError_t launch_stats(int R, int C, int Z, const int* rowPtrs, const int* colIdx, void* work,
                          int nChunks, CsrChunkDesc* desc, cudaStream_t s) {

@@ -53,3 +53,25 @@ def test_traffic_record_follows_its_source(tmp_path, monkeypatch):
     assert bench.traffic_record("absent", "k_demo") is None     # no capture
     src.write_text("// kernel source, changed\n")
     assert bench.traffic_record("demo", "k_demo") is None       # stale capture
+
+
+def test_sample_bytes_count_only_referenced_columns():
+    """A row sample reads x only at the columns its nonzeros reference."""
+    import numpy as np
+    import synth
+    rp = np.array([0, 2, 3, 3], np.int32)           # rows of 2, 1 and 0 entries
+    ci = np.array([5, 9, 5], np.int32)              # columns 5 and 9, 5 twice
+    va = np.ones(3, np.float32)
+    s = synth.CSRInput("t", 3, 100, rp, ci, va, np.zeros(100, np.float32),
+                       np.zeros(3, np.float32))
+    assert bench.sample_bytes(s) == 8 * 3 + 12 * 3 + 4 * 2
+
+
+def test_dominant_kernels_name_single_kernel_calls():
+    """The roofline's kernel is timed by the CUDA events of a call that
+    launches that kernel alone."""
+    for call, kernel in bench.DOMINANT.values():
+        assert bench.SINGLE_KERNEL_CALLS[call] == kernel
+    assert bench.DEFAULT_WORKLOAD == "stencil27"
+    assert bench.DEFAULT_WORKLOAD in bench.DOMINANT
+    assert set(bench.CONFIG_ORDER) == set(bench.WORKLOAD_DESC)

@@ -88,7 +88,8 @@ def check_matrix(sp, orc, inp, formats=FORMATS, hyb_widths=(0,), arrays=True, el
         assert st["hist_log2"] == ost["hist_log2"].tolist()
         assert st["mean_len"] == pytest.approx(ost["mean"], rel=1e-12, abs=1e-12)
         assert st["var_len"] == pytest.approx(ost["var"], rel=1e-9, abs=1e-9)
-        assert st["auto_format"] == orc.select(R, Z, ost["max_len"])
+        assert st["auto_format"] == orc.select(R, inp.num_cols, Z, ost["max_len"],
+                                               st["gather_lines"])
         # the other row statistics, by their definitions over the row lengths
         lens = np.diff(inp.row_ptrs.astype(np.int64))
         if R:
@@ -314,11 +315,15 @@ def test_workload_full_size(sp, orc, name):
     print(name, {k: round(v, 4) for k, v in res.items()})
 
 
-def test_skewed_selects_hyb_width_20(sp):
+def test_skewed_selects_xblock_and_hyb_width_20(sp):
+    """Rows of 10-20 random columns plus a few of 1000-5000: the HYB width is
+    20, as the format-selection page says; the columns are scattered, so the
+    x-blocked list is chosen."""
     inp = workload("skewed")
     with sp.SparseMatrix(inp.num_rows, inp.num_cols, dev(inp.row_ptrs), dev(inp.col_idx),
                          dev(inp.value)) as m:
-        assert m.select() == ("HYB", 20)
+        assert m.stats()["gather_lines"] > 30
+        assert m.select() == ("XBLOCK", 20)
 
 
 # --- validation errors (input sanity rules) --------------------------------------

@@ -356,13 +356,35 @@ def test_row_stats(orc, idx):
 
 def test_select_outcomes_described_by_page(orc):
     # regular stencil-like rows (scientific computing) -> ELL
-    assert orc.select(4_194_304, 20_963_328, 5) == "ELL"
-    assert orc.select(4_096_000, 109_215_352, 27) == "ELL"
+    assert orc.select(4_194_304, 4_194_304, 20_963_328, 5, 3.5) == "ELL"
+    assert orc.select(4_096_000, 4_096_000, 109_215_352, 27, 9.0) == "ELL"
     # 99% of rows of length 10-20 plus rows longer than 1000 -> HYB of width 20
+    # (with columns close together; scattered columns take the x-blocked list)
     inp = synth.skewed(n=20_000, n_long=2, seed=3)
     lens = np.diff(inp.row_ptrs)
-    assert orc.select(inp.num_rows, inp.nnz, int(lens.max())) == "HYB"
+    big = 2_000_000  # the same row mix at a size bound by bandwidth
+    assert orc.select(big, big, int(big * inp.nnz / inp.num_rows), int(lens.max()), 4.0) == "HYB"
+    assert orc.select(big, big, int(big * inp.nnz / inp.num_rows), int(lens.max()),
+                      32.0) == "XBLOCK"
     assert orc.hyb_auto_width(inp.row_ptrs) == 20
+    # short irregular rows -> COO; moderate spread with long rows -> CSR
+    assert orc.select(1_000_000, 1_000_000, 5_000_000, 40, 32.0) == "COO"
+    assert orc.select(1_000_000, 1_000_000, 30_000_000, 100, 4.0) == "CSR"
+
+
+def test_select_small_matrices_take_csr(orc):
+    """Below 4 MiB of compulsory bytes (8 per nonzero, 12 per row, 4 per
+    column) the choice is CSR whatever the row mix; at the boundary the
+    other rules apply."""
+    assert orc.select(4096, 4096, 32_768, 8, 32.0) == "CSR"  # 327,680 bytes
+    assert orc.select(4, 4, 8, 3, 0.0) == "CSR"
+    assert orc.select(0, 0, 0, 0, 0.0) == "CSR"
+    # 8*Z + 12*R + 4*C = 4 MiB exactly: not below, so ELL for equal rows
+    R = 65_536
+    Z = (4_194_304 - 16 * R) // 8
+    assert 8 * Z + 12 * R + 4 * R == 4_194_304
+    assert orc.select(R, R, Z, Z // R, 1.0) == "ELL"
+    assert orc.select(R - 1, R - 1, Z, Z // R + 1, 1.0) == "CSR"
 
 
 def test_hyb_auto_width_quantile(orc):

@@ -69,3 +69,48 @@ def test_noalloc_rejects_too_large(sp):
                                   ctypes.c_void_p(8), ctypes.c_void_p(8), ctypes.c_void_p(8),
                                   None)
     assert st == sp.SPMV_ERR_TOO_LARGE
+
+
+def chunk_edge_matrix():
+    """A matrix whose empty rows sit exactly at 128-entry chunk starts and
+    inside chunks, with rows that end on a chunk boundary and rows longer
+    than a chunk."""
+    rng = np.random.default_rng(21)
+    lens = [128, 0, 0, 127, 1, 0, 128, 0, 300, 0, 0, 0, 5, 123, 0, 0]
+    lens += list(rng.choice([0, 0, 1, 3, 64, 127, 128, 129], size=4000))
+    lens = np.array(lens, np.int64)
+    R, C = lens.size, 3000
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    Z = int(rp[-1])
+    ci = rng.integers(0, C, size=Z).astype(np.int32)
+    va = rng.uniform(-1, 1, size=Z).astype(np.float32)
+    x = rng.uniform(-1, 1, size=C).astype(np.float32)
+    y0 = rng.uniform(-1, 1, size=R).astype(np.float32)
+    return synth.CSRInput("chunk_edges", R, C, rp, ci, va, x, y0)
+
+
+def test_noalloc_smaller_matrix_after_larger(sp, orc):
+    """A call on a smaller, irregular matrix issued right after one on the
+    largest matrix, on the same stream with no synchronisation between them,
+    must not see the first call's records; each call launches 3 kernels."""
+    big = CASES["at_limit"]()
+    small = chunk_edge_matrix()
+    assert small.nnz < big.nnz
+    rows_at_chunk_start = np.isin(small.row_ptrs[:-1], np.arange(0, small.nnz, 128)) & (
+        np.diff(small.row_ptrs) == 0)
+    assert rows_at_chunk_start.any()  # the case this test is about
+    db = [dev(a) for a in (big.row_ptrs, big.col_idx, big.value, big.x)]
+    ds = [dev(a) for a in (small.row_ptrs, small.col_idx, small.value, small.x)]
+    yb, ys = dev(big.y0), dev(small.y0)
+    torch.cuda.synchronize()
+    n0 = sp.spmv_launch_count()
+    sp.spmv_run_csr_noalloc(big.num_rows, big.num_cols, big.nnz, *db, yb)
+    n1 = sp.spmv_launch_count()
+    sp.spmv_run_csr_noalloc(small.num_rows, small.num_cols, small.nnz, *ds, ys)
+    n2 = sp.spmv_launch_count()
+    torch.cuda.synchronize()
+    assert n1 - n0 == 3 and n2 - n1 == 3
+    for inp, y in ((big, yb), (small, ys)):
+        want, mag = orc.spmv_csr(inp.row_ptrs, inp.col_idx, inp.value, inp.x, inp.y0)
+        ok, worst = oracle.within_tolerance(y.cpu().numpy(), want, mag)
+        assert ok, (inp.name, worst)
