@@ -11,11 +11,16 @@ namespace {
 
 // Thread per row, writes coalesced across rows (slot t of consecutive rows
 // is one store per warp for every t). Padding slots get column -1 and value
-// +0.0f; nnzPerRow[r] = min(len(r), K). (Measured alternatives, both slower:
-// a row's loads issued 8 at a time before their stores, laplace2d 60.4 ->
-// 68.4 us and 27-point stencil 334 -> 344 us in the bench step; the block's
-// CSR entries staged in shared memory with coalesced 16-byte loads, 128 rows
-// per block, 60.4 -> 117.8 and 334 -> 350 us.)
+// +0.0f; nnzPerRow[r] = min(len(r), K). A warp's load of the rows' t-th
+// entries touches a sector per lane (the rows are one row length apart), and
+// ncu shows the L1 pipeline as the bound on a 27-point stencil (lg_throttle
+// stalls; L2-to-L1 reads 2.6 times the entries), while DRAM moves exactly
+// the algorithmic bytes. Measured alternatives, all slower in the bench step
+// (5-point Laplacian / 27-point stencil, against 60.4 / 334 us): a row's
+// loads issued 8 at a time before its stores, 68.4 / 344 us; the block's CSR
+// entries staged in shared memory with coalesced 16-byte loads, 128 rows per
+// block, 117.8 / 350 us; each warp's entries staged in its own shared memory
+// sized to the width, 89.1 / 359 us.
 template <class T>
 __global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __restrict__ rowPtrs,
                                                     const int* __restrict__ colIdx,
