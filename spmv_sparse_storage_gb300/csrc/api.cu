@@ -614,7 +614,9 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   if (st == SPMV_OK)
     st = record(with_type(h, [&](auto tag) {
       using T = decltype(tag);
-      return spmv::launch_jds_build<T>(h->R, L, h->rowPtrs, h->colIdx, cval<T>(h->value),
+      // rows longer than kJdsCoop: exact from the length histogram (kJdsCoop < kExactLenBins)
+      const int wLong = (int)h->width_at(spmv::kJdsCoop);
+      return spmv::launch_jds_build<T>(h->R, L, wLong, h->rowPtrs, h->colIdx, cval<T>(h->value),
                                        h->jdsPerm, h->jdsIterPtr, h->jdsCol, val<T>(h->jdsVal),
                                        scratch, hostIp.empty() ? nullptr : hostIp.data(), s);
     }));

@@ -429,17 +429,19 @@ __global__ void k_jds_widths(int R, int maxLen, const int* __restrict__ sortedKe
   for (int t = next; t < len; ++t) width[t] = (int)(s + 1);
 }
 
-// Jagged scatter, row side: entry t of original row r goes to
-// iterPtr[t] + inv[r] (inv = sorted position). Rows are read in CSR order
-// (coalesced row pointers, row-contiguous entries); consecutive rows of one
-// length have consecutive sorted positions, so the writes of a warp are
-// contiguous per diagonal. A thread copies the first kCoop entries of its
-// row; the warp then copies each longer row's remaining entries together,
-// one entry per lane. The first kJdsScatterSmem entries of iterPtr are staged
-// in shared memory. (Loads issued 8 at a time before their stores, and the
-// block's entries staged in shared memory, measured no faster.)
-constexpr int kCoop = 64;
+// Jagged scatter, in sorted order: thread s takes sorted row s (original row
+// perm[s]) and writes its entry t to iterPtr[t] + s. Rows are sorted longest
+// first, so for every t the lanes of a warp that still have an entry are a
+// prefix of the warp and their stores are contiguous (walking rows in their
+// original order instead split a warp's stores wherever the length changed:
+// 392 us per launch on the 27-point stencil). A thread copies the first
+// kJdsCoop entries of its row. The longer rows are the first wLong sorted
+// rows; their entries from kJdsCoop on are cut into segments of kJdsSeg,
+// one segment per warp of the blocks after the first mainBlocks (a warp per
+// long row would serialise the longest rows, which sit together). The first
+// kJdsScatterSmem entries of iterPtr are staged in shared memory.
 constexpr int kJdsScatterSmem = 1024;
+constexpr int kJdsSeg = 1024;
 // iterPtr passed by value when the host knows it and it is short (longest
 // row below kIpArg): block 0 writes it to memory, every block reads it from
 // its arguments. n = 0: iterPtr is already in memory.
@@ -449,11 +451,12 @@ struct IterPtrArg {
   int v[kIpArg];
 };
 template <class T>
-__global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
+__global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen, int mainBlocks,
+                                                     int wLong, int nSegs,
                                                      const int* __restrict__ rowPtrs,
                                                      const int* __restrict__ colIdx,
                                                      const T* __restrict__ value,
-                                                     const int* __restrict__ inv,
+                                                     const int* __restrict__ perm,
                                                      int* __restrict__ iterPtr,
                                                      const __grid_constant__ IterPtrArg ipArg,
                                                      int* __restrict__ jdsCol,
@@ -468,32 +471,34 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen,
     for (int t = threadIdx.x; t < nIp; t += blockDim.x) sIp[t] = iterPtr[t];
   }
   __syncthreads();
-  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const int lane = threadIdx.x & 31;
-  int a = 0, len = 0, srow = 0;
-  if (r < R) {
-    a = rowPtrs[r];
-    len = rowPtrs[r + 1] - a;
-    srow = inv[r];
-    const int lim = len < kCoop ? len : kCoop;
+  if ((int)blockIdx.x < mainBlocks) {
+    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
+    if (s >= R) return;
+    const int r = perm[s];
+    const int a = rowPtrs[r];
+    const int len = rowPtrs[r + 1] - a;
+    const int lim = len < kJdsCoop ? len : kJdsCoop;
     for (int t = 0; t < lim; ++t) {
-      const long long o = (long long)sIp[t] + srow;
+      const long long o = (long long)sIp[t] + s;
       jdsCol[o] = colIdx[a + t];
       jdsVal[o] = value[a + t];
     }
-  }
-  unsigned longRows = __ballot_sync(kFullMask, len > kCoop);
-  while (longRows) {
-    const int src = __ffs(longRows) - 1;
-    longRows &= longRows - 1;
-    const int la = __shfl_sync(kFullMask, a, src);
-    const int ll = __shfl_sync(kFullMask, len, src);
-    const int ls = __shfl_sync(kFullMask, srow, src);
-    for (long long t = kCoop + lane; t < ll; t += 32) {  // 64-bit: ll may be near INT32_MAX
+  } else {
+    // one segment of one long row per warp, one entry per lane
+    const long long item = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
+                           (threadIdx.x >> 5);
+    const long long s = item / nSegs;
+    if (s >= wLong) return;
+    const int r = perm[s];
+    const int a = rowPtrs[r];
+    const int len = rowPtrs[r + 1] - a;
+    const long long t0 = kJdsCoop + (item % nSegs) * (long long)kJdsSeg;
+    const long long t1 = min(t0 + kJdsSeg, (long long)len);
+    for (long long t = t0 + (threadIdx.x & 31); t < t1; t += 32) {
       const int ip = t < kJdsScatterSmem ? sIp[t] : __ldg(iterPtr + t);
-      const long long o = (long long)ip + ls;
-      jdsCol[o] = colIdx[la + t];
-      jdsVal[o] = value[la + t];
+      const long long o = (long long)ip + s;
+      jdsCol[o] = colIdx[a + t];
+      jdsVal[o] = value[a + t];
     }
   }
 }
@@ -536,8 +541,9 @@ size_t jds_sort_scratch_bytes(int R, int maxLen) {
 }
 
 // Stable sort of the rows by length, longest first (LSD radix on maxLen - len
-// with 8-bit digits): perm[s] = row at sorted position s, inv[row] = s. The
-// sorted keys are left in keysB when needKeys (else they are not written).
+// with 8-bit digits): perm[s] = row at sorted position s, and, when invOut is
+// given, inv[row] = s. The sorted keys are left in keysB when needKeys (else
+// they are not written).
 // Scratch (int32): keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles+1] scan.
 template <class In>
 static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scratch,
@@ -551,7 +557,7 @@ static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scrat
   int* inv = keysB + R;
   int* hist = inv + R;
   int* scanScratch = hist + nh + 1;
-  *invOut = inv;
+  if (invOut) *invOut = inv;
   *scanScratchOut = scanScratch;
   int bits = 0;
   while (bits < 31 && (1LL << bits) <= maxLen) ++bits;
@@ -586,7 +592,7 @@ static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scrat
     const bool last = p == passes - 1;
     k_radix_scatter<<<(unsigned)nTiles, kSortThreads, 0, s>>>(
         in, R, shift, nBuckets, (int)nTiles, hist, (last && !needKeys) ? nullptr : kBuf[outSlot],
-        vBuf[outSlot], last ? inv : nullptr);
+        vBuf[outSlot], (last && invOut) ? inv : nullptr);
     note_launches(1);
     kIn = kBuf[outSlot];
     vIn = vBuf[outSlot];
@@ -604,9 +610,9 @@ static cudaError_t row_sort(int R, int maxLen, const int* rowPtrs, int* perm, in
 }
 
 template <class T>
-cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
-                             const T* value, int* perm, int* iterPtr, int* jdsCol,
-                             T* jdsVal, void* scratch, const int* hostIterPtr,
+cudaError_t launch_jds_build(int R, int maxLen, int wLong, const int* rowPtrs,
+                             const int* colIdx, const T* value, int* perm, int* iterPtr,
+                             int* jdsCol, T* jdsVal, void* scratch, const int* hostIterPtr,
                              cudaStream_t s) {
   if (R <= 0) {
     // iterPtr has maxLen + 1 = 1 entry
@@ -616,10 +622,10 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
   const long long nh = (long long)kRadix * nTiles;
   const long long scanN = nh > maxLen ? nh : maxLen;
   const int* sortedKeys = nullptr;
-  int* inv = nullptr;
   int* scanScratch = nullptr;
+  // the scatter walks rows in sorted order (perm): no inverse permutation
   cudaError_t err = row_sort(R, maxLen, rowPtrs, perm, static_cast<int*>(scratch),
-                             hostIterPtr == nullptr, &sortedKeys, &inv, &scanScratch, s);
+                             hostIterPtr == nullptr, &sortedKeys, nullptr, &scanScratch, s);
   if (err != cudaSuccess) return err;
   int* width = scanScratch + scan_scratch_ints(scanN);
   if (maxLen > 0) {
@@ -640,8 +646,14 @@ cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* c
       err = exclusive_scan(ArrayIn{width}, (long long)maxLen, iterPtr, scanScratch, s);
       if (err != cudaSuccess) return err;
     }
-    k_jds_scatter<T><<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
-        R, maxLen, rowPtrs, colIdx, value, inv, iterPtr, ipArg, jdsCol, jdsVal);
+    // a thread per sorted row, then a warp per kJdsSeg-entry segment of the
+    // wLong rows longer than kJdsCoop
+    const long long mainBlocks = ((long long)R + 255) / 256;
+    const int nSegs = maxLen > kJdsCoop ? (maxLen - kJdsCoop + kJdsSeg - 1) / kJdsSeg : 1;
+    const long long tailBlocks = ((long long)wLong * nSegs + 7) / 8;
+    k_jds_scatter<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
+        R, maxLen, (int)mainBlocks, wLong, nSegs, rowPtrs, colIdx, value, perm, iterPtr, ipArg,
+        jdsCol, jdsVal);
     note_launches(1);
   } else {
     err = cudaMemsetAsync(iterPtr, 0, sizeof(int), s);
@@ -711,7 +723,7 @@ cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const
 
 // Row-side scatter: original row r (sorted position inv[r], section k, row j
 // of the section) writes its w_k slots, real entries then padding (column -1,
-// value +0.0f). A thread writes the first kCoop slots; the warp then writes
+// value +0.0f). A thread writes the first kJdsCoop slots; the warp then writes
 // each wider section's remaining slots of its rows together, one per lane.
 template <class T>
 __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* __restrict__ rowPtrs,
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
     base = secPtr[k];
     const int end = secPtr[k + 1];
     w = end <= cap ? (end - base) / h : 0;  // offsets past the arrays: write nothing
-    const int lim = w < kCoop ? w : kCoop;
+    const int lim = w < kJdsCoop ? w : kJdsCoop;
     for (int t = 0; t < lim; ++t) {
       const long long o = (long long)base + (long long)t * h + j;
       const bool real = t < len;
@@ -742,7 +754,7 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
       sellVal[o] = real ? value[a + t] : T(0);
     }
   }
-  unsigned wide = __ballot_sync(kFullMask, w > kCoop);
+  unsigned wide = __ballot_sync(kFullMask, w > kJdsCoop);
   while (wide) {
     const int src = __ffs(wide) - 1;
     wide &= wide - 1;
@@ -752,7 +764,7 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
     const int lh = __shfl_sync(kFullMask, h, src);
     const int lj = __shfl_sync(kFullMask, j, src);
     const int lb = __shfl_sync(kFullMask, base, src);
-    for (long long t = kCoop + lane; t < lw; t += 32) {  // 64-bit: lw may be near INT32_MAX
+    for (long long t = kJdsCoop + lane; t < lw; t += 32) {  // 64-bit: lw may be near INT32_MAX
       const long long o = (long long)lb + t * lh + lj;
       const bool real = t < ll;
       sellCol[o] = real ? colIdx[la + t] : -1;
@@ -904,8 +916,9 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* v
 #define SPMV_INSTANTIATE(T)                                                                      \
   template cudaError_t launch_hyb_tail_copy<T>(int, int, const int*, const int*, const T*,      \
                                                const int*, int*, int*, T*, cudaStream_t);        \
-  template cudaError_t launch_jds_build<T>(int, int, const int*, const int*, const T*, int*,    \
-                                           int*, int*, T*, void*, const int*, cudaStream_t);     \
+  template cudaError_t launch_jds_build<T>(int, int, int, const int*, const int*, const T*,     \
+                                           int*, int*, int*, T*, void*, const int*,              \
+                                           cudaStream_t);                                        \
   template cudaError_t launch_sell_scatter<T>(int, int, const int*, const int*, const T*,       \
                                               const void*, const int*, int, int*, T*,            \
                                               cudaStream_t);                                     \

@@ -107,11 +107,14 @@ cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* co
                                  int* cooCol, T* cooVal, cudaStream_t s);
 // JDS: stable sort of rows by length (longest first), iterPtr, jagged scatter.
 size_t jds_sort_scratch_bytes(int R, int maxLen);
-// hostIterPtr: iterPtr computed on the host (nullptr: computed on the device)
+// hostIterPtr: iterPtr computed on the host (nullptr: computed on the device);
+// wLong: the number of rows longer than kJdsCoop (their entries past kJdsCoop
+// are copied by extra warps)
+constexpr int kJdsCoop = 64;
 template <class T>
-cudaError_t launch_jds_build(int R, int maxLen, const int* rowPtrs, const int* colIdx,
-                             const T* value, int* perm, int* iterPtr, int* jdsCol,
-                             T* jdsVal, void* scratch, const int* hostIterPtr,
+cudaError_t launch_jds_build(int R, int maxLen, int wLong, const int* rowPtrs,
+                             const int* colIdx, const T* value, int* perm, int* iterPtr,
+                             int* jdsCol, T* jdsVal, void* scratch, const int* hostIterPtr,
                              cudaStream_t s);
 constexpr int kJdsPad = 8;  // extra elements after the JDS arrays (aligned vector reads)
 // Sectioned ELL (the JDS variant): sort, section widths (for a read-back when
