@@ -10,7 +10,10 @@ The metric counts the compulsory SpMV bytes of the five products:
   effective GB/s = 5 * (8*nnz + 12*rows + 4*cols) / step time,
   GFLOP/s        = 5 * 2*nnz / step time.
 Per-call CUDA-event times inside the timed steps give each stage's own
-GB/s; `roofline` reports the call that takes the largest share of the step.
+GB/s. `roofline` reports the kernel with the largest share of the workload's
+ncu launch list, timed by the events of the call that launches it alone,
+with its per-launch DRAM traffic from the committed capture; it also names
+the call with the largest share of the step and the fastest SpMV.
 The e2e figure repeats the step through the same C ABI with the inputs in
 pinned host memory: every step's host-to-device copy of the CSR arrays, x and
 y0 and the device-to-host read of its five results are inside the timed
