@@ -286,6 +286,25 @@ int spmv_cg_solve(spmv_handle h, spmv_format format, const float *d_y, float *d_
  * HYB width. Host-only; either output pointer may be NULL. */
 int spmv_select(spmv_handle h, spmv_format *format, int32_t *ellWidth);
 
+/* Format choice by timing ("[CUDA performance tuning] SpMV storage format
+ * selection and performance comparison", end of section 4.3: run every
+ * format on the matrix and keep the fastest). Runs y <- A*x + y in every
+ * format converted so far (CSR always; COO, ELL, HYB, JDS, SELL, XBLOCK
+ * when converted): one untimed run, then `reps` runs each timed with CUDA
+ * events on `stream` (back to back, L2 as the previous run left it), and
+ * takes each format's median.
+ *   d_x: numCols floats; d_y: numRows floats of SCRATCH, overwritten (it
+ *   accumulates every run). reps in [1, 1000]. 4-byte handles only
+ *   (SPMV_ERR_INVALID_ARG for a handle from spmv_create_csr_f64).
+ *   *best: the fastest format. From then on spmv_select, spmv_get_stats'
+ *   auto_format and spmv_run(SPMV_AUTO) use it (it is converted by
+ *   construction). times_ms (optional, NULL allowed): 8 floats indexed by
+ *   spmv_format, the median ms of each timed format, -1 for formats not
+ *   timed (not converted, and SPMV_AUTO).
+ *   SYNCHRONISES `stream` after every timed run. */
+int spmv_autotune(spmv_handle h, const float *d_x, float *d_y, int32_t reps,
+                  spmv_format *best, float *times_ms, void *stream);
+
 /* Copy the statistics computed at creation into *out (host). */
 int spmv_get_stats(spmv_handle h, spmv_stats *out);
 

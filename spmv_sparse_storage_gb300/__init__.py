@@ -84,6 +84,8 @@ _SIGS = {
     "spmv_cg_solve": (C.c_int, [_H, C.c_int, _P, _P, C.c_int32, C.c_double,
                                 C.POINTER(spmv_cg_info), _P]),
     "spmv_select": (C.c_int, [_H, C.POINTER(C.c_int), C.POINTER(C.c_int32)]),
+    "spmv_autotune": (C.c_int, [_H, _P, _P, C.c_int32, C.POINTER(C.c_int),
+                                C.POINTER(C.c_float), _P]),
     "spmv_get_stats": (C.c_int, [_H, C.POINTER(spmv_stats)]),
     "spmv_export": (C.c_int, [_H, C.c_int, C.POINTER(spmv_arrays)]),
     "spmv_destroy": (C.c_int, [_H]),
@@ -206,6 +208,19 @@ def spmv_select(h):
     w = C.c_int32()
     _check(_lib.spmv_select(h, C.byref(f), C.byref(w)), "spmv_select")
     return FORMAT_NAMES[f.value], w.value
+
+
+def spmv_autotune(h, x, y, reps=5, stream=None):
+    """Time every converted format's SpMV (``y`` is scratch, overwritten) and
+    make the fastest the handle's automatic choice. Returns (format name,
+    {format name: median ms} for the timed formats)."""
+    best = C.c_int()
+    times = (C.c_float * 8)()
+    _check(_lib.spmv_autotune(h, _ptr(x), _ptr(y), int(reps), C.byref(best), times,
+                              _stream(stream)), "spmv_autotune")
+    timed = {FORMAT_NAMES[f]: float(times[f]) for f in range(8)
+             if f in FORMAT_NAMES and times[f] >= 0.0}
+    return FORMAT_NAMES[best.value], timed
 
 
 def spmv_get_stats(h):
@@ -363,6 +378,9 @@ class SparseMatrix:
 
     def select(self):
         return spmv_select(self.handle)
+
+    def autotune(self, x, y, reps=5, stream=None):
+        return spmv_autotune(self.handle, x, y, reps, stream)
 
     def stats(self):
         return spmv_get_stats(self.handle)

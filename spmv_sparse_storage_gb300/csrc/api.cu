@@ -2,6 +2,7 @@
 // device-memory pool, validation read-back, format selection, conversion and
 // SpMV dispatch. All arithmetic on the matrix runs in the CUDA kernels of
 // stats.cu, convert.cu and spmv_kernels.cu.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cstring>
@@ -864,6 +865,55 @@ int spmv_run(spmv_handle h, spmv_format format, const float* d_x, float* d_y, vo
 int spmv_run_f64(spmv_handle h, spmv_format format, const double* d_x, double* d_y,
                  void* stream) {
   return run_impl<double>(h, format, d_x, d_y, stream);
+}
+
+int spmv_autotune(spmv_handle h, const float* d_x, float* d_y, int32_t reps, spmv_format* best,
+                  float* times_ms, void* stream) {
+  SPMV_TRY(check_handle(h));
+  if (h->f64 || !best || reps < 1 || reps > 1000) return SPMV_ERR_INVALID_ARG;
+  if (times_ms)
+    for (int f = 0; f < 8; ++f) times_ms[f] = -1.0f;
+  DeviceGuard g;
+  SPMV_TRY(g.set(h->device));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaEvent_t ev[2] = {nullptr, nullptr};
+  int st = record(cudaEventCreate(&ev[0]));
+  if (st == SPMV_OK) st = record(cudaEventCreate(&ev[1]));
+  const spmv_format order[] = {SPMV_CSR, SPMV_COO, SPMV_ELL, SPMV_HYB,
+                               SPMV_JDS, SPMV_SELL, SPMV_XBLOCK};
+  spmv_format fastest = SPMV_CSR;
+  float fastestMs = -1.0f;
+  std::vector<float> t;
+  for (const spmv_format f : order) {
+    if (st != SPMV_OK) break;
+    if (converted(h, f) != SPMV_OK) continue;
+    st = run_impl<float>(h, f, d_x, d_y, stream);  // untimed (checks the arguments too)
+    t.clear();
+    for (int r = 0; r < reps && st == SPMV_OK; ++r) {
+      st = record(cudaEventRecord(ev[0], s));
+      if (st == SPMV_OK) st = run_impl<float>(h, f, d_x, d_y, stream);
+      if (st == SPMV_OK) st = record(cudaEventRecord(ev[1], s));
+      if (st == SPMV_OK) st = record(cudaEventSynchronize(ev[1]));
+      float ms = 0.0f;
+      if (st == SPMV_OK) st = record(cudaEventElapsedTime(&ms, ev[0], ev[1]));
+      if (st == SPMV_OK) t.push_back(ms);
+    }
+    if (st != SPMV_OK) break;
+    std::sort(t.begin(), t.end());
+    const float med = t.size() % 2 ? t[t.size() / 2]
+                                   : 0.5f * (t[t.size() / 2 - 1] + t[t.size() / 2]);
+    if (times_ms) times_ms[f] = med;
+    if (fastestMs < 0.0f || med < fastestMs) {
+      fastestMs = med;
+      fastest = f;
+    }
+  }
+  for (cudaEvent_t e : ev)
+    if (e) cudaEventDestroy(e);
+  if (st != SPMV_OK) return st;
+  h->stats.auto_format = fastest;
+  *best = fastest;
+  return SPMV_OK;
 }
 
 }  // extern "C"
