@@ -83,9 +83,13 @@ FP64_NOMINAL_GFLOPS = 1250.0
 # step's ncu launch list, and the library call whose CUDA-event time is that
 # kernel's duration (the call launches that kernel alone). Workloads without
 # a launch list take the single-kernel call with the longest event time.
+# (The CSR -> ELL scatter stages rows of 24 to 32 entries through shared
+# memory, k_csr_to_ell_staged, and reads narrower or wider ones directly,
+# k_csr_to_ell.)
 DOMINANT = {"laplace2d": ("convert_ell", "k_csr_to_ell"),
-            "stencil27": ("convert_ell", "k_csr_to_ell")}
-# calls that launch exactly one kernel of the library (on every workload)
+            "stencil27": ("convert_ell", "k_csr_to_ell_staged")}
+# calls that launch exactly one kernel of the library (on every workload): the
+# kernel's name, or the prefix of the names of its forms
 SINGLE_KERNEL_CALLS = {"convert_ell": "k_csr_to_ell", "convert_coo": "k_expand_rows",
                        "spmv_CSR": "k_spmv_csr_wide", "spmv_COO": "k_spmv_coo",
                        "spmv_ELL": "k_spmv_ell"}

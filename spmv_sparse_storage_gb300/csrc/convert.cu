@@ -503,6 +503,62 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen, int main
   }
 }
 
+// Warp-staged jagged scatter for a longest row in [kStageMinK, kStageMaxK<T>]
+// (the 27-point stencil): warp w takes sorted rows s0 .. s0 + 31. Their entries are not
+// contiguous in CSR (rows of other lengths lie between them), so the warp
+// copies them row by row into its shared buffers, lane t taking entry t of
+// the row (asynchronous copies, coalesced within the row, all in flight
+// before one wait); each lane then writes its own row's entries to
+// iterPtr[t] + s from there. Reading them straight from global memory, a
+// warp's load of the rows' t-th entries touches a sector per lane. Buffer
+// rows are maxLen rounded up to an odd number of entries apart, so that
+// the lanes' reads fall in different banks.
+template <class T>
+__global__ void __launch_bounds__(32 * kStageWarps) k_jds_scatter_staged(
+    int R, int maxLen, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
+    const T* __restrict__ value, const int* __restrict__ perm, int* __restrict__ iterPtr,
+    const __grid_constant__ IterPtrArg ipArg, int* __restrict__ jdsCol, T* __restrict__ jdsVal) {
+  __shared__ int sIp[kStageMaxK<float>];
+  extern __shared__ int4 sRaw[];
+  if (ipArg.n > 0) {  // n = maxLen + 1
+    for (int t = threadIdx.x; t < maxLen; t += blockDim.x) sIp[t] = ipArg.v[t];
+    if (blockIdx.x == 0)
+      for (int t = threadIdx.x; t < ipArg.n; t += blockDim.x) iterPtr[t] = ipArg.v[t];
+  } else {
+    for (int t = threadIdx.x; t < maxLen; t += blockDim.x) sIp[t] = iterPtr[t];
+  }
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int stride = maxLen | 1;
+  const int cap = 32 * stride;
+  int* sCol = reinterpret_cast<int*>(sRaw) + warp * cap;
+  T* sVal = reinterpret_cast<T*>(reinterpret_cast<int*>(sRaw) + kStageWarps * cap) + warp * cap;
+  const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
+  if (s - lane >= R) return;                                            // warp-uniform
+  int a = 0, len = 0;
+  if (s < R) {
+    const int r = perm[s];
+    a = rowPtrs[r];
+    len = min(rowPtrs[r + 1] - a, maxLen);
+  }
+  for (int j = 0; j < 32; ++j) {
+    const int aj = __shfl_sync(kFullMask, a, j);
+    const int lj = __shfl_sync(kFullMask, len, j);
+    if (lane < lj) {
+      cp_async_small<4>(sCol + j * stride + lane, colIdx + aj + lane);
+      cp_async_small<(int)sizeof(T)>(sVal + j * stride + lane, value + aj + lane);
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+  if (s >= R) return;
+  for (int t = 0; t < len; ++t) {
+    const long long o = (long long)sIp[t] + s;
+    jdsCol[o] = sCol[lane * stride + t];
+    jdsVal[o] = sVal[lane * stride + t];
+  }
+}
+
 }  // namespace
 
 // Threads per block of the HYB tail copy (128 and 64 measured slower: the
@@ -651,6 +707,16 @@ cudaError_t launch_jds_build(int R, int maxLen, int wLong, const int* rowPtrs,
     const long long mainBlocks = ((long long)R + 255) / 256;
     const int nSegs = maxLen > kJdsCoop ? (maxLen - kJdsCoop + kJdsSeg - 1) / kJdsSeg : 1;
     const long long tailBlocks = ((long long)wLong * nSegs + 7) / 8;
+    if (maxLen >= kStageMinK && maxLen <= kStageMaxK<T>) {  // wLong = 0: no row past kJdsCoop
+      constexpr int threads = 32 * kStageWarps;
+      const unsigned blocks = (unsigned)(((long long)R + threads - 1) / threads);
+      const size_t smem =
+          (size_t)kStageWarps * 32 * (size_t)(maxLen | 1) * (sizeof(int) + sizeof(T));
+      k_jds_scatter_staged<T><<<blocks, threads, smem, s>>>(R, maxLen, rowPtrs, colIdx, value,
+                                                            perm, iterPtr, ipArg, jdsCol, jdsVal);
+      note_launches(1);
+      return cudaGetLastError();
+    }
     k_jds_scatter<T><<<(unsigned)(mainBlocks + tailBlocks), 256, 0, s>>>(
         R, maxLen, (int)mainBlocks, wLong, nSegs, rowPtrs, colIdx, value, perm, iterPtr, ipArg,
         jdsCol, jdsVal);

@@ -71,7 +71,7 @@ def test_dominant_kernels_name_single_kernel_calls():
     """The roofline's kernel is timed by the CUDA events of a call that
     launches that kernel alone."""
     for call, kernel in bench.DOMINANT.values():
-        assert bench.SINGLE_KERNEL_CALLS[call] == kernel
+        assert kernel.startswith(bench.SINGLE_KERNEL_CALLS[call])
     assert bench.DEFAULT_WORKLOAD == "stencil27"
     assert bench.DEFAULT_WORKLOAD in bench.DOMINANT
     assert set(bench.CONFIG_ORDER) == set(bench.WORKLOAD_DESC)

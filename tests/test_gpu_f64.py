@@ -209,3 +209,19 @@ def test_type_errors(sp, orc):
             sp.spmv_run_f64(m.handle, "CSR", dev(inp.x.astype(np.float64)),
                             dev(inp.y0.astype(np.float64)))
         assert ei.value.code == sp.SPMV_ERR_INVALID_ARG
+
+
+def test_warp_staged_width_24(sp, orc):
+    """8-byte values with rows of 12-24 entries: the ELL, HYB (automatic
+    width) and JDS conversions take the warp-staged scatters (two 16-byte
+    copies per 4 values)."""
+    rng = np.random.default_rng(77)
+    R, C = 3001, 2500
+    lens = rng.integers(12, 25, R).astype(np.int64)
+    lens[0] = 24
+    cols = synth._distinct_sorted_columns(rng, lens, C)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
+    inp = synth.CSRInput("wide24", R, C, rp, cols, val, np.zeros(C, np.float32),
+                         np.zeros(R, np.float32))
+    check_f64(sp, orc, inp, formats=("ELL", "HYB", "JDS"))

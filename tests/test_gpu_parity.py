@@ -639,3 +639,28 @@ def test_gather_locality_statistic(sp):
             got[inp.name] = m.stats()["gather_lines"]
     assert 0 < got["laplace2d"] <= 8, got
     assert got["rand"] >= 24, got
+
+
+def wide_rows(seed, num_rows, num_cols, lo, hi, name):
+    """Rows of lo..hi distinct sorted columns, the first row exactly hi long;
+    values, x and y0 U(-1, 1)."""
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(lo, hi + 1, num_rows).astype(np.int64)
+    lens[0] = hi
+    cols = synth._distinct_sorted_columns(rng, lens, num_cols)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
+    x = rng.uniform(-1.0, 1.0, num_cols).astype(np.float32)
+    y0 = rng.uniform(-1.0, 1.0, num_rows).astype(np.float32)
+    return synth.CSRInput(name, num_rows, num_cols, rp, cols, val, x, y0)
+
+
+@pytest.mark.parametrize("offset", [0, 1, 3])
+def test_warp_staged_row_scatters(sp, orc, offset):
+    """Rows of 17-32 entries take the warp-staged scatters: ELL (width 32),
+    JDS (longest row 32), and HYB at widths 24 and 28, where the warps whose
+    rows hold more entries than their buffer read directly. Aligned arrays
+    stage by 16-byte asynchronous copies, misaligned views entry by entry; the
+    last warp is ragged (5003 rows)."""
+    inp = wide_rows(31 + offset, 5003, 4000, 17, 32, f"wide{offset}")
+    check_matrix(sp, orc, inp, formats=("ELL", "HYB", "JDS"), hyb_widths=(24, 28), offset=offset)
