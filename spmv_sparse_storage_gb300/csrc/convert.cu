@@ -504,16 +504,19 @@ __global__ void __launch_bounds__(256) k_jds_scatter(int R, int maxLen, int main
 }
 
 // Warp-staged jagged scatter for a longest row in [kStageMinK, kStageMaxK<T>]
-// (the 27-point stencil): warp w takes sorted rows s0 .. s0 + 31. Their entries are not
-// contiguous in CSR (rows of other lengths lie between them), so the warp
-// copies them row by row into its shared buffers, lane t taking entry t of
-// the row (asynchronous copies, coalesced within the row, all in flight
-// before one wait); each lane then writes its own row's entries to
-// iterPtr[t] + s from there. Reading them straight from global memory, a
-// warp's load of the rows' t-th entries touches a sector per lane. Buffer
-// rows are maxLen rounded up to an odd number of entries apart, so that
-// the lanes' reads fall in different banks.
-template <class T>
+// (the 27-point stencil): warp w takes sorted rows s0 .. s0 + 31 and copies
+// their entries into its shared buffers, then each lane writes its own row's
+// entries to iterPtr[t] + s from there (reading them straight from global
+// memory, a warp's load of the rows' t-th entries touches a sector per lane).
+// When the 32 rows are consecutive original rows (the sort is stable, so a
+// run of rows of one length stays together), their entries are one
+// contiguous range, staged as for the ELL scatter (warp_stage_entries:
+// 16-byte asynchronous copies). Otherwise the warp copies row by row, lane t
+// taking entry t of the row (asynchronous 4- or 8-byte copies, coalesced
+// within the row), rows maxLen rounded up to an odd count apart so that the
+// lanes' reads fall in different banks. Either way all copies are in flight
+// before one wait.
+template <class T, bool VEC>
 __global__ void __launch_bounds__(32 * kStageWarps) k_jds_scatter_staged(
     int R, int maxLen, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
     const T* __restrict__ value, const int* __restrict__ perm, int* __restrict__ iterPtr,
@@ -530,32 +533,46 @@ __global__ void __launch_bounds__(32 * kStageWarps) k_jds_scatter_staged(
   __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int stride = maxLen | 1;
-  const int cap = 32 * stride;
+  const int cap = 32 * stride + 8;  // a multiple of 4 when stride is odd plus 8: see below
   int* sCol = reinterpret_cast<int*>(sRaw) + warp * cap;
   T* sVal = reinterpret_cast<T*>(reinterpret_cast<int*>(sRaw) + kStageWarps * cap) + warp * cap;
   const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
-  if (s - lane >= R) return;                                            // warp-uniform
-  int a = 0, len = 0;
+  const long long s0 = s - lane;
+  if (s0 >= R) return;  // warp-uniform
+  int r = -1, a = 0, len = 0;
   if (s < R) {
-    const int r = perm[s];
+    r = perm[s];
     a = rowPtrs[r];
     len = min(rowPtrs[r + 1] - a, maxLen);
   }
-  for (int j = 0; j < 32; ++j) {
-    const int aj = __shfl_sync(kFullMask, a, j);
-    const int lj = __shfl_sync(kFullMask, len, j);
-    if (lane < lj) {
-      cp_async_small<4>(sCol + j * stride + lane, colIdx + aj + lane);
-      cp_async_small<(int)sizeof(T)>(sVal + j * stride + lane, value + aj + lane);
+  const int r0 = __shfl_sync(kFullMask, r, 0);
+  const int nRows = (int)min(32LL, (long long)R - s0);
+  // consecutive original rows: one contiguous range [a0, a1)
+  const bool run = __all_sync(kFullMask, lane >= nRows || r == r0 + lane) && VEC;
+  int off;
+  if (run) {
+    const int a0 = __shfl_sync(kFullMask, a, 0);
+    const int a1 = __ldg(rowPtrs + r0 + nRows);  // a1 - a0 <= 32 * maxLen
+    warp_stage_entries<T, true>(colIdx, value, a0, a1, lane, sCol, sVal);
+    off = (int)(a - (a0 & ~3LL));
+  } else {
+    for (int j = 0; j < 32; ++j) {
+      const int aj = __shfl_sync(kFullMask, a, j);
+      const int lj = __shfl_sync(kFullMask, len, j);
+      if (lane < lj) {
+        cp_async_small<4>(sCol + j * stride + lane, colIdx + aj + lane);
+        cp_async_small<(int)sizeof(T)>(sVal + j * stride + lane, value + aj + lane);
+      }
     }
+    cp_async_wait_all();
+    off = lane * stride;
   }
-  cp_async_wait_all();
   __syncwarp();
   if (s >= R) return;
   for (int t = 0; t < len; ++t) {
     const long long o = (long long)sIp[t] + s;
-    jdsCol[o] = sCol[lane * stride + t];
-    jdsVal[o] = sVal[lane * stride + t];
+    jdsCol[o] = sCol[off + t];
+    jdsVal[o] = sVal[off + t];
   }
 }
 
@@ -711,9 +728,13 @@ cudaError_t launch_jds_build(int R, int maxLen, int wLong, const int* rowPtrs,
       constexpr int threads = 32 * kStageWarps;
       const unsigned blocks = (unsigned)(((long long)R + threads - 1) / threads);
       const size_t smem =
-          (size_t)kStageWarps * 32 * (size_t)(maxLen | 1) * (sizeof(int) + sizeof(T));
-      k_jds_scatter_staged<T><<<blocks, threads, smem, s>>>(R, maxLen, rowPtrs, colIdx, value,
-                                                            perm, iterPtr, ipArg, jdsCol, jdsVal);
+          (size_t)kStageWarps * (32 * (size_t)(maxLen | 1) + 8) * (sizeof(int) + sizeof(T));
+      if (aligned16(colIdx) && aligned16(value))
+        k_jds_scatter_staged<T, true><<<blocks, threads, smem, s>>>(
+            R, maxLen, rowPtrs, colIdx, value, perm, iterPtr, ipArg, jdsCol, jdsVal);
+      else
+        k_jds_scatter_staged<T, false><<<blocks, threads, smem, s>>>(
+            R, maxLen, rowPtrs, colIdx, value, perm, iterPtr, ipArg, jdsCol, jdsVal);
       note_launches(1);
       return cudaGetLastError();
     }

@@ -48,8 +48,9 @@ __global__ void __launch_bounds__(256) k_csr_to_ell(int R, int K, const int* __r
 // its own part of shared memory (warp_stage_entries: asynchronous 16-byte
 // copies, all in flight before one wait), then each lane writes its row's K
 // slots from there (one coalesced store per warp for every t). ncu on a
-// 27-point stencil: 266 us against 333 for the direct form, DRAM at 83 % with
-// exactly the algorithmic bytes, L2-to-L1 reads near the entries' bytes.
+// 27-point stencil: 267 us against 333 for the direct form, DRAM at 82 % with
+// exactly the algorithmic bytes, no lg_throttle stalls (the 16-byte copies
+// bypass L1, so L2 serves each 32-byte sector as two requests).
 // Measured alternatives, slower than the direct form in the bench step
 // (5-point Laplacian / 27-point stencil, against 60.4 / 334 us): staging
 // with plain loads, whose stores to shared memory waited on each load in

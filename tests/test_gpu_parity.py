@@ -656,11 +656,25 @@ def wide_rows(seed, num_rows, num_cols, lo, hi, name):
 
 
 @pytest.mark.parametrize("offset", [0, 1, 3])
-def test_warp_staged_row_scatters(sp, orc, offset):
+@pytest.mark.parametrize("kind", ["random", "runs"])
+def test_warp_staged_row_scatters(sp, orc, offset, kind):
     """Rows of 17-32 entries take the warp-staged scatters: ELL (width 32),
     JDS (longest row 32), and HYB at widths 24 and 28, where the warps whose
     rows hold more entries than their buffer read directly. Aligned arrays
     stage by 16-byte asynchronous copies, misaligned views entry by entry; the
-    last warp is ragged (5003 rows)."""
+    last warp is ragged (5003 rows). "runs": rows of 27 entries with one of
+    24 every 50 rows, so that after the length sort most warps of the JDS
+    scatter hold consecutive original rows (one contiguous range) and some do
+    not; "random": lengths at random, so that no warp does."""
     inp = wide_rows(31 + offset, 5003, 4000, 17, 32, f"wide{offset}")
+    if kind == "runs":
+        lens = np.full(inp.num_rows, 27, np.int64)
+        lens[::50] = 24
+        lens[1] = 32
+        rng = np.random.default_rng(7 + offset)
+        cols = synth._distinct_sorted_columns(rng, lens, inp.num_cols)
+        rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
+        inp = synth.CSRInput(f"runs{offset}", inp.num_rows, inp.num_cols, rp, cols, val,
+                             inp.x, inp.y0)
     check_matrix(sp, orc, inp, formats=("ELL", "HYB", "JDS"), hyb_widths=(24, 28), offset=offset)
