@@ -193,6 +193,7 @@ struct spmv_handle_s {
   int jdsMaxLen = 0;
   int jdsTSplit = 0;
   int jdsWTail = 0;
+  std::vector<int> jdsIpHost;  // iterPtr[0 .. jdsTSplit], from the length histogram
   int* jdsPerm = nullptr;
   int* jdsIterPtr = nullptr;
   int* jdsCol = nullptr;
@@ -633,6 +634,9 @@ int spmv_convert_jds(spmv_handle h, void* stream) {
   while (tSplit < cap && thr > 0 && h->width_at(tSplit) >= thr) ++tSplit;
   h->jdsTSplit = tSplit;
   h->jdsWTail = tSplit < L ? (int)h->width_at(tSplit) : 0;
+  h->jdsIpHost.assign((size_t)tSplit + 1, 0);
+  for (int t = 0; t < tSplit; ++t)
+    h->jdsIpHost[(size_t)t + 1] = h->jdsIpHost[(size_t)t] + (int)h->width_at(t);
   h->jdsMaxLen = L;
   h->hasJds = true;
   return SPMV_OK;
@@ -948,8 +952,8 @@ int run_format(spmv_handle h, spmv_format format, const T* d_x, T* d_y, cudaStre
     }
     case SPMV_JDS:
       return record(spmv::launch_spmv_jds<T>(h->R, h->jdsMaxLen, h->jdsTSplit, h->jdsWTail,
-                                             h->jdsIterPtr, h->jdsPerm, h->jdsCol,
-                                             cval<T>(h->jdsVal), d_x, d_y, s));
+                                             h->jdsIterPtr, h->jdsIpHost.data(), h->jdsPerm,
+                                             h->jdsCol, cval<T>(h->jdsVal), d_x, d_y, s));
     case SPMV_SELL:
       if (h->sellSlots == 0) return SPMV_OK;
       return record(spmv::launch_spmv_sell<T>(h->R, h->sellS, (int)h->sellSlots, h->sellSecPtr,

@@ -209,9 +209,12 @@ template <class T>
 cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const int* perm,
                              const int* sellCol, const T* sellVal, const SellItem* items,
                              int nItems, const T* x, T* y, cudaStream_t s);
+// hostIterPtr: iterPtr[0 .. tSplit] on the host (or nullptr); with tSplit <=
+// kJdsParamDiags the kernel takes them as a launch parameter
+constexpr int kJdsParamDiags = 64;
 template <class T>
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
-                            const int* perm, const int* jdsCol, const T* jdsVal,
-                            const T* x, T* y, cudaStream_t s);
+                            const int* hostIterPtr, const int* perm, const int* jdsCol,
+                            const T* jdsVal, const T* x, T* y, cudaStream_t s);
 
 }  // namespace spmv

@@ -503,7 +503,13 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // entries, so they are split into blocks of kJdsTailRows rows x
 // kJdsTailDiags diagonals that run in parallel and add their partial sums
 // atomically. The result of sorted row s goes straight to y[perm[s]] (the
-// page permutes the result back with the row array).
+// page permutes the result back with the row array). With at most
+// kJdsParamDiags row-parallel diagonals their iterPtr entries come with the
+// launch (from the host's length histogram): a block then starts its loads at
+// once instead of first copying them into shared memory behind a barrier
+// (cold L2: 5-point Laplacian 45.0 -> 43.0 us, uniform random rows 29.7 ->
+// 26.6 us, skewed rows 168.6 -> 163.8 us; 64-thread blocks gained nothing
+// more).
 // ===========================================================================
 // diagonals whose loads a thread issues together: 8 with 4-byte values (32
 // registers; laplace2d 45.1 us, 27-point stencil 148 us, against 53.3 and
@@ -511,19 +517,30 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // 251 us against 227)
 template <class T>
 constexpr int kJdsGroup = sizeof(T) == 4 ? 8 : 5;
-template <class T>
+// iterPtr[0 .. tSplit] as a launch parameter (PARAM kernels): read through the
+// constant cache, so that a block starts its row loads at once. Otherwise
+// the block first copies them into shared memory and synchronises, one more
+// round trip on the path of a short-lived block.
+struct JdsIterPtrs {
+  int v[kJdsParamDiags + 1];
+};
+template <class T, bool PARAM>
 __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
+                                                     const __grid_constant__ JdsIterPtrs ipArg,
                                                      const int* __restrict__ perm,
                                                      const int* __restrict__ jdsCol,
                                                      const T* __restrict__ jdsVal,
                                                      const T* __restrict__ x,
                                                      T* __restrict__ y) {
-  __shared__ int sIp[kJdsSplitMaxDiag + 1];
+  __shared__ int sIpBuf[PARAM ? 1 : kJdsSplitMaxDiag + 1];
+  const int* sIp = PARAM ? ipArg.v : sIpBuf;
   if ((int)blockIdx.x < nMainBlocks) {
-    for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIp[t] = iterPtr[t];
-    __syncthreads();
+    if (!PARAM) {
+      for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIpBuf[t] = iterPtr[t];
+      __syncthreads();
+    }
     const int lane = threadIdx.x & 31;
     const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
     const long long warpFirst = s - lane;
@@ -689,8 +706,8 @@ cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
 
 template <class T>
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
-                            const int* perm, const int* jdsCol, const T* jdsVal,
-                            const T* x, T* y, cudaStream_t s) {
+                            const int* hostIterPtr, const int* perm, const int* jdsCol,
+                            const T* jdsVal, const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
   // a sorted row per thread
   const long long mainBlocks = ((long long)R + kJdsBlock - 1) / kJdsBlock;
@@ -701,9 +718,17 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
     const long long diagBlocks = ((long long)(maxLen - tSplit) + kJdsTailDiags - 1) / kJdsTailDiags;
     tailBlocks = (long long)tailRowBlocks * diagBlocks;
   }
-  k_spmv_jds<T><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
-      R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, perm, jdsCol, jdsVal, x,
-      y);
+  JdsIterPtrs ip;
+  const bool param = hostIterPtr != nullptr && tSplit <= kJdsParamDiags;
+  for (int t = 0; t <= kJdsParamDiags; ++t) ip.v[t] = param && t <= tSplit ? hostIterPtr[t] : 0;
+  if (param)
+    k_spmv_jds<T, true><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
+        R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, ip, perm, jdsCol,
+        jdsVal, x, y);
+  else
+    k_spmv_jds<T, false><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
+        R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, ip, perm, jdsCol,
+        jdsVal, x, y);
   note_launches(1);
   return cudaGetLastError();
 }
@@ -1108,7 +1133,8 @@ cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int
   template cudaError_t launch_spmv_ell<T>(int, int, const int*, const T*, const T*, T*,        \
                                           cudaStream_t);                                        \
   template cudaError_t launch_spmv_jds<T>(int, int, int, int, const int*, const int*,          \
-                                          const int*, const T*, const T*, T*, cudaStream_t);    \
+                                          const int*, const int*, const T*, const T*, T*,      \
+                                          cudaStream_t);                                       \
   template cudaError_t launch_spmv_sell<T>(int, int, int, const int*, const int*, const int*,  \
                                            const T*, const SellItem*, int, const T*, T*,        \
                                            cudaStream_t);                                       \

@@ -456,6 +456,25 @@ def test_length_sort_pass_boundary(sp, orc, max_len):
     check_matrix(sp, orc, inp, formats=("JDS", "SELL"), sell_rows=(0, 3, 128))
 
 
+@pytest.mark.parametrize("width", [63, 64, 65])
+def test_jds_diagonal_parameter_boundary(sp, orc, width):
+    """9000 rows of `width` entries and 40 rows of 100: the first `width`
+    diagonals are row-parallel (at least 8192 wide). Up to 64 of them the
+    SpMV takes their iterPtr entries as a launch parameter, past 64 from
+    shared memory; the 35-36 diagonals of the long rows run as tail tiles."""
+    rng = np.random.default_rng(500 + width)
+    R, C = 9040, 3000
+    lens = np.full(R, width, np.int64)
+    lens[rng.choice(R, 40, replace=False)] = 100
+    cols = synth._distinct_sorted_columns(rng, lens, C)
+    rp = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
+    x = rng.uniform(-1.0, 1.0, C).astype(np.float32)
+    y0 = rng.uniform(-1.0, 1.0, R).astype(np.float32)
+    check_matrix(sp, orc, synth.CSRInput(f"jds_param{width}", R, C, rp, cols, val, x, y0),
+                 formats=("JDS",))
+
+
 def test_length_sort_two_scan_passes(sp, orc):
     """5,120,077 rows of at most 7 entries: the row sort's per-tile counts
     (8 digits x 2,501 tiles of 2048 rows = 20,008) take two passes of the
