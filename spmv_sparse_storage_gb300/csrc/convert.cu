@@ -416,6 +416,185 @@ __global__ void __launch_bounds__(kSortThreads) k_radix_scatter(In in, int R, in
   }
 }
 
+// Single-pass form (every key below kSortMaxBuckets, at most kSortMaxGroups
+// groups of tiles):
+// two kernels instead of five (the histogram, three scan kernels for a large
+// histogram, the scatter), and no block waits on another. k_radix_count1
+// writes each tile's digit counts (tile-major) and adds them into the sums of
+// its group of kSortGroup tiles (zeroed before the launch). k_radix_scatter1,
+// a programmatic dependent launch, loads its keys and counts its warps' digits
+// while the counts finish, then finds its tile's start for every digit by
+// itself: the digit's start (an exclusive scan over the digits of the group
+// sums' totals) plus the groups before its group plus the tiles before it in
+// its group, read by all 256 threads (256 / nBuckets per digit). It then
+// scatters as k_radix_scatter does.
+constexpr int kSortGroup = 32;
+// bounds of the single-pass form: at most kSortMaxGroups groups (2048 tiles,
+// 4,194,304 items) and kSortMaxBuckets digits, so that each thread's share of
+// the prefix reads is a few loads issued together; larger sorts (the
+// x-blocked list's chunk sort, with thousands of tiles) take the general form
+constexpr int kSortMaxGroups = 64;
+constexpr int kSortMaxBuckets = 32;
+__host__ __device__ inline long long sort_groups(long long nTiles) {
+  return (nTiles + kSortGroup - 1) / kSortGroup;
+}
+
+template <class In>
+__global__ void __launch_bounds__(kSortThreads) k_radix_count1(In in, int R, int nBuckets,
+                                                               int* __restrict__ tileHist,
+                                                               int* __restrict__ groupSum) {
+  grid_dependency_trigger();  // the scatter may load its keys meanwhile
+  __shared__ int sCount[kRadix];
+  for (int d = threadIdx.x; d < nBuckets; d += kSortThreads) sCount[d] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long base = (long long)blockIdx.x * kSortTile;
+  int key[kSortRounds];
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    int val;
+    key[rd] = 0;
+    if (i < R) in.get(i, key[rd], val);
+  }
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = base + rd * kSortThreads + threadIdx.x;
+    const int digit = i < R ? key[rd] & (nBuckets - 1) : kRadix;
+    const unsigned peers = __match_any_sync(kFullMask, digit);
+    if (digit < kRadix && lane == __ffs(peers) - 1) atomicAdd(&sCount[digit], __popc(peers));
+  }
+  __syncthreads();
+  int* grp = groupSum + (long long)(blockIdx.x / kSortGroup) * nBuckets;
+  for (int d = threadIdx.x; d < nBuckets; d += kSortThreads) {
+    const int c = sCount[d];
+    tileHist[(long long)blockIdx.x * nBuckets + d] = c;
+    if (c) atomicAdd(grp + d, c);
+  }
+}
+
+template <class In>
+__global__ void __launch_bounds__(kSortThreads) k_radix_scatter1(
+    In in, int R, int nBuckets, int nTiles, const int* __restrict__ tileHist,
+    const int* __restrict__ groupSum, int* __restrict__ keysOut, int* __restrict__ valsOut,
+    int* __restrict__ invOut) {
+  constexpr int kWarps = kSortThreads / 32;
+  constexpr int kPerWarp = kSortTile / kWarps;  // = 32 * kSortRounds
+  __shared__ int sCur[kWarps][kRadix];          // counts, then running positions
+  __shared__ int sBefore[kSortThreads], sTotal[kSortThreads];
+  __shared__ int sStart[kRadix];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int d = lane; d < nBuckets; d += 32) sCur[w][d] = 0;
+  const long long wbase = (long long)blockIdx.x * kSortTile + (long long)w * kPerWarp;
+  int key[kSortRounds], val[kSortRounds], digit[kSortRounds];
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const long long i = wbase + rd * 32 + lane;
+    key[rd] = 0;
+    val[rd] = 0;
+    if (i < R) in.get(i, key[rd], val[rd]);
+    digit[rd] = i < R ? key[rd] & (nBuckets - 1) : kRadix;  // kRadix: no one shares
+  }
+  __syncwarp();
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const unsigned peers = __match_any_sync(kFullMask, digit[rd]);
+    if (digit[rd] < kRadix && lane == __ffs(peers) - 1) sCur[w][digit[rd]] += __popc(peers);
+    __syncwarp();
+  }
+  grid_dependency_wait();  // the counts are complete and visible
+  // partial sums: thread (digit d, part p) takes the groups g = p mod P and the
+  // tiles of its group before this one, t = p mod P
+  const int P = kSortThreads / nBuckets;  // nBuckets: a power of two <= kRadix
+  const int d = threadIdx.x % nBuckets, p = threadIdx.x / nBuckets;
+  const int tile = blockIdx.x, myGroup = tile / kSortGroup;
+  const int nGroups = (int)sort_groups(nTiles);
+  // at most kSortMaxGroups / P group sums and kSortGroup / P tile counts per
+  // thread (P >= kSortThreads / kSortMaxBuckets), all loaded together
+  constexpr int kG = kSortMaxGroups / (kSortThreads / kSortMaxBuckets);
+  constexpr int kT = kSortGroup / (kSortThreads / kSortMaxBuckets);
+  int gv[kG], tv[kT];
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    const int g = p + k * P;
+    gv[k] = g < nGroups ? __ldcg(groupSum + (long long)g * nBuckets + d) : 0;
+  }
+#pragma unroll
+  for (int k = 0; k < kT; ++k) {
+    const int t = myGroup * kSortGroup + p + k * P;
+    tv[k] = t < tile ? __ldcg(tileHist + (long long)t * nBuckets + d) : 0;
+  }
+  int before = 0, total = 0;
+#pragma unroll
+  for (int k = 0; k < kG; ++k) {
+    total += gv[k];
+    if (p + k * P < myGroup) before += gv[k];
+  }
+#pragma unroll
+  for (int k = 0; k < kT; ++k) before += tv[k];
+  sBefore[threadIdx.x] = before;
+  sTotal[threadIdx.x] = total;
+  __syncthreads();
+  if (threadIdx.x < nBuckets) {
+    int b = 0, t = 0;
+    for (int q = 1; q < P; ++q) {
+      b += sBefore[q * nBuckets + threadIdx.x];
+      t += sTotal[q * nBuckets + threadIdx.x];
+    }
+    sBefore[threadIdx.x] += b;
+    sTotal[threadIdx.x] += t;
+  }
+  __syncthreads();
+  // digit starts: exclusive scan of the totals (lane l takes nBuckets / 32
+  // consecutive digits, or one)
+  if (w == 0) {
+    const int per = (nBuckets + 31) / 32;
+    const int lo = lane * per;
+    int own = 0;
+    for (int k = 0; k < per && lo + k < nBuckets; ++k) own += sTotal[lo + k];
+    int incl = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(kFullMask, incl, off);
+      if (lane >= off) incl += o;
+    }
+    int run = incl - own;
+    for (int k = 0; k < per && lo + k < nBuckets; ++k) {
+      const int v = sTotal[lo + k];
+      sStart[lo + k] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  // counts -> where each warp's items of each digit start
+  for (int dd = threadIdx.x; dd < nBuckets; dd += kSortThreads) {
+    int run = sStart[dd] + sBefore[dd];
+#pragma unroll
+    for (int q = 0; q < kWarps; ++q) {
+      const int cnt = sCur[q][dd];
+      sCur[q][dd] = run;
+      run += cnt;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int rd = 0; rd < kSortRounds; ++rd) {
+    const int dg = digit[rd];
+    const unsigned peers = __match_any_sync(kFullMask, dg);
+    const bool valid = dg < kRadix;
+    const int start = valid ? sCur[w][dg] : 0;
+    __syncwarp();
+    if (valid) {
+      const int pos = start + __popc(peers & lanemask_lt());
+      if (keysOut) keysOut[pos] = key[rd];
+      valsOut[pos] = val[rd];
+      if (invOut) invOut[val[rd]] = pos;
+      if (lane == __ffs(peers) - 1) sCur[w][dg] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
 // Diagonal widths from the sorted lengths: width(t) = #{s : len(s) > t}. With
 // lengths non-increasing over s, width(t) = s+1 for t in [len(s+1), len(s)).
 // (Used when some row is at least kExactLenBins long; otherwise iterPtr comes
@@ -604,12 +783,18 @@ cudaError_t launch_hyb_tail_copy(int R, int K, const int* rowPtrs, const int* co
 }
 
 // Scratch layout for the JDS build (all int32):
-//   keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles + 1] scanScratch[...] width[maxLen]
+//   keysA[R] valsA[R] keysB[R] inv[R] hist[sort_hist_ints(nTiles)] scanScratch[...] width[maxLen]
+// (hist: the tiles' digit counts, then the single-pass form's group sums)
+long long sort_hist_ints(long long nTiles) {
+  if (nTiles < 1) nTiles = 1;
+  return (long long)kRadix * (nTiles + sort_groups(nTiles)) + 1;
+}
 size_t jds_sort_scratch_bytes(int R, int maxLen) {
   const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
   const long long nh = (long long)kRadix * (nTiles > 0 ? nTiles : 1);
   const long long scanN = nh > maxLen ? nh : maxLen;
-  const long long ints = 4LL * R + (nh + 1) + (long long)scan_scratch_ints(scanN) + maxLen + 16;
+  const long long ints = 4LL * R + sort_hist_ints(nTiles) + (long long)scan_scratch_ints(scanN) +
+                         maxLen + 16;
   return (size_t)ints * sizeof(int);
 }
 
@@ -617,24 +802,53 @@ size_t jds_sort_scratch_bytes(int R, int maxLen) {
 // with 8-bit digits): perm[s] = row at sorted position s, and, when invOut is
 // given, inv[row] = s. The sorted keys are left in keysB when needKeys (else
 // they are not written).
-// Scratch (int32): keysA[R] valsA[R] keysB[R] inv[R] hist[kRadix*nTiles+1] scan.
+// Scratch (int32): keysA[R] valsA[R] keysB[R] inv[R] hist[sort_hist_ints(nTiles)] scan.
 template <class In>
 static cudaError_t radix_sort(In first, int R, int maxLen, int* perm, int* scratch,
                               bool needKeys, const int** sortedKeys, int** invOut,
                               int** scanScratchOut, cudaStream_t s) {
   const long long nTiles = ((long long)R + kSortTile - 1) / kSortTile;
-  const long long nh = (long long)kRadix * nTiles;
   int* keysA = scratch;
   int* valsA = keysA + R;
   int* keysB = valsA + R;
   int* inv = keysB + R;
   int* hist = inv + R;
-  int* scanScratch = hist + nh + 1;
+  int* scanScratch = hist + sort_hist_ints(nTiles);
   if (invOut) *invOut = inv;
   *scanScratchOut = scanScratch;
   int bits = 0;
   while (bits < 31 && (1LL << bits) <= maxLen) ++bits;
   const int passes = bits == 0 ? 1 : (bits + kRadixBits - 1) / kRadixBits;
+  if (passes == 1 && (1 << bits) <= kSortMaxBuckets && sort_groups(nTiles) <= kSortMaxGroups) {
+    const int nBuckets = 1 << bits;
+    int* tileHist = hist;
+    int* groupSum = hist + (long long)kRadix * nTiles;
+    cudaError_t err = cudaMemsetAsync(groupSum, 0,
+                                      sizeof(int) * (size_t)(sort_groups(nTiles) * nBuckets), s);
+    if (err != cudaSuccess) return err;
+    k_radix_count1<<<(unsigned)nTiles, kSortThreads, 0, s>>>(first, R, nBuckets, tileHist,
+                                                             groupSum);
+    note_launches(1);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nTiles);
+    cfg.blockDim = dim3(kSortThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, k_radix_scatter1<In>, first, R, nBuckets, (int)nTiles,
+                             (const int*)tileHist, (const int*)groupSum,
+                             needKeys ? keysB : nullptr, perm, invOut ? inv : nullptr);
+    note_launches(1);
+    if (err != cudaSuccess) return err;
+    *sortedKeys = keysB;
+    return cudaGetLastError();
+  }
   // Ping-pong so that the last pass writes perm (values) and keysB (keys).
   int* kBuf[2] = {keysA, keysB};
   int* vBuf[2] = {valsA, perm};

@@ -443,9 +443,10 @@ def test_sell_section_heights_and_wide_sections(sp, orc):
     check_matrix(sp, orc, narrow, formats=("SELL",), sell_rows=(0, 6, 128))
 
 
-@pytest.mark.parametrize("max_len", [1, 63, 64, 65, 200, 255, 256])
+@pytest.mark.parametrize("max_len", [1, 31, 32, 63, 64, 65, 200, 255, 256])
 def test_length_sort_pass_boundary(sp, orc, max_len):
-    """Longest row on both sides of 256 (the row sort by length takes one
+    """Longest row on both sides of 32 (the row sort's single-pass form, two
+    kernels, takes at most 32 digits), of 256 (the general form takes one
     8-bit radix pass below it, two from it) and of 64 (rows longer than that
     are copied by the whole warp), over several 2048-row sort tiles with a
     ragged last tile: JDS and SELL arrays bit-exact, perm included."""
