@@ -999,11 +999,21 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
 // meets it stages that chunk of x (B floats) in shared memory, then each warp
 // walks the slice kXbUnroll x 32 entries at a time, lane l taking entries l,
 // l + 32, ... (every load coalesced, all of them issued before the first
-// use), gathers from shared memory and adds each product into y with a
-// fire-and-forget atomic. Rows ascend inside a chunk, so the 32 atomics of
-// one instruction fall on a few neighbouring sectors of y, where the L2
-// combines them; summing runs of equal row first would cost more shuffles
-// than it saves.
+// use), gathers from shared memory and adds into y with fire-and-forget
+// atomics. Rows ascend inside a chunk, so equal rows of one instruction's 32
+// entries sit in adjacent lanes: where any lane continues its neighbour's
+// row (a 27-point stencil row keeps up to 27 entries in one chunk, the skewed
+// matrix's long rows many more) the runs are summed by a segmented shuffle
+// scan first, one reduction per run; where none does (scattered columns,
+// about one entry per row in a chunk) each product goes to y by itself. The
+// test costs one shuffle and one ballot per 32 entries. Cold L2: 27-point
+// stencil 554.6 -> 262.1 us, skewed rows 115.3 -> 95.2 us (its long rows'
+// reductions all fall on a few addresses), 5-point Laplacian (runs of 5)
+// 65.5 -> 69.6 us. Taking the scan only where at least 28 of the 32 lanes
+// continue a run kept the Laplacian at 67.6 us but left the skewed matrix
+// at 108.6 us; a scan of only as many steps as the longest run needs (a
+// runtime bound) measured 75.8 and 326 us. With 8-byte values every product
+// goes to y by itself: the scan's fp64 adds cost more than the reductions.
 // ---------------------------------------------------------------------------
 constexpr int kXbUnroll = 8;
 
@@ -1071,8 +1081,35 @@ __global__ void __launch_bounds__(THREADS, 1) k_spmv_xb(int C, int B, int nch,
         col[j] = in ? (int)__ldcs(xbCol + e) : 0;
       }
 #pragma unroll
-      for (int j = 0; j < kXbUnroll; ++j)
-        if (row[j] >= 0) atomicAdd(y + row[j], val[j] * sX[col[j]]);  // padding: row -1
+      for (int j = 0; j < kXbUnroll; ++j) {
+        // 32 consecutive entries, rows ascending: equal rows sit in adjacent
+        // lanes. With no lane continuing its left neighbour's row (scattered
+        // columns) each product goes to y by itself; otherwise each run of
+        // equal row is summed by a segmented shuffle scan and its last lane
+        // adds the sum, one reduction per run (padding: row -1, product 0)
+        const T prod = row[j] >= 0 ? val[j] * sX[col[j]] : T(0);
+        if constexpr (sizeof(T) == 8) {
+          // 8-byte values: the fp64 adds of a scan would cost more than the
+          // reductions they save (27-point stencil 432 -> 1292 us)
+          if (row[j] >= 0) atomicAdd(y + row[j], prod);
+          continue;
+        }
+        const int left = __shfl_up_sync(kFullMask, row[j], 1);
+        const unsigned cont = __ballot_sync(kFullMask, lane > 0 && left == row[j]);
+        if (cont == 0u) {  // warp-uniform
+          if (row[j] >= 0) atomicAdd(y + row[j], prod);
+        } else {
+          const int segStart = 31 - __clz(~cont & (0xffffffffu >> (31 - lane)));
+          T v = prod;
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const T o = __shfl_up_sync(kFullMask, v, off);
+            if (lane - off >= segStart) v += o;
+          }
+          const bool last = lane == 31 || ((cont >> (lane + 1)) & 1u) == 0u;
+          if (last && row[j] >= 0) atomicAdd(y + row[j], v);
+        }
+      }
     }
   }
 }
