@@ -778,9 +778,10 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
   if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbRow, h->xbBufs);
   if (st == SPMV_OK) st = alloc_typed(h, bound, s, &h->xbCol, h->xbBufs);
   if (st == SPMV_OK) st = alloc_values(h, bound, s, &h->xbVal, h->xbBufs);
-  // row of every nonzero: the COO conversion's array when present
+  // row of every nonzero, for more than kXbTileChunks chunks: the COO
+  // conversion's array when present (fewer chunks decode rows on the fly)
   const int* rowIdx = h->hasCoo ? h->cooRow : nullptr;
-  if (st == SPMV_OK && !rowIdx && h->Z > 0) {
+  if (st == SPMV_OK && !rowIdx && h->Z > 0 && nch > spmv::kXbTileChunks) {
     int* tmpRow = nullptr;
     st = alloc_typed(h, h->Z, s, &tmpRow, tmp);
     if (st == SPMV_OK)
@@ -792,9 +793,10 @@ int spmv_convert_xblock(spmv_handle h, int32_t chunkCols, void* stream) {
   if (st == SPMV_OK)
     st = record(with_type(h, [&](auto tag) {
       using T = decltype(tag);
-      return spmv::launch_xb_build<T>(h->Z, B, (int)nch, h->colIdx, cval<T>(h->value), rowIdx,
-                                      h->xbChunkPtr, h->xbRow, h->xbCol, val<T>(h->xbVal),
-                                      scratch, s);
+      return spmv::launch_xb_build<T>(h->Z, B, (int)nch, h->rowPtrs, h->chunkDesc, h->colIdx,
+                                      cval<T>(h->value), rowIdx,
+                                      h->stats.gather_lines >= kScatteredLines, h->xbChunkPtr,
+                                      h->xbRow, h->xbCol, val<T>(h->xbVal), scratch, s);
     }));
   if (st != SPMV_OK) return fail(st);
   h->release(tmp, s);

@@ -1161,7 +1161,260 @@ __global__ void k_xb_pad(int nch, const int* __restrict__ cnt, const int* __rest
   }
 }
 
+// Tiled build, for at most kXbTileChunks chunks: tiles of kXbTile consecutive
+// nonzeros. (1) k_xb_tile_count: each tile's nonzeros per chunk, chunk-major
+// (tileCnt[c * nTiles + t]); a thread counts its 8 consecutive entries in runs
+// of equal chunk (a row's columns ascend) and adds each run with one shared
+// atomic. (2) An exclusive scan of tileCnt: tile t's first position among
+// chunk c's nonzeros, unpadded. (3) k_xb_chunk_ptr: chunk sizes and their
+// padded starts. (4) k_xb_tile_scatter: each tile ranks its entries by chunk
+// (stable: peer masks per 32 entries, warps in order), sorts them by chunk in
+// shared memory, and writes every chunk's run of entries contiguously. The
+// rows come from the CSR chunk records (no expanded row array). The earlier
+// build sorted every nonzero by chunk with the general radix sort and then
+// scattered each one by itself (a store instruction's 32 lanes on up to 32
+// chunks): 1.09 ms on the skewed rows' 30.6M nonzeros and 1.63 ms on the
+// 27-point stencil.
+constexpr int kXbTile = 2048;
+constexpr int kXbTileThreads = 256;
+
+// col / B without a division: with M = ceil(2^64 / B), the high 64 bits of
+// col * M are col / B + col * e / 2^64 for some e in [0, 1), and col < 2^31
+// keeps that excess below 2^-33, under the 1/B gap to the next integer
+// (B < 2^17). B = 1 is passed as M = 0.
+struct ChunkDiv {
+  unsigned long long m;
+  int b;
+  __device__ int operator()(int col) const {
+    return m ? (int)__umul64hi((unsigned long long)(unsigned)col, m) : col;
+  }
+};
+inline ChunkDiv chunk_div(int B) {
+  ChunkDiv d;
+  d.b = B;
+  d.m = B <= 1 ? 0ull : (~0ull) / (unsigned long long)B + 1ull;  // ceil(2^64 / B), B > 1
+  return d;
+}
+constexpr int kXbTileRounds = kXbTile / kXbTileThreads;  // 8
+static_assert(kXbTileChunks <= 256, "chunk ids are kept in one byte");
+
+template <bool VEC>
+__global__ void __launch_bounds__(kXbTileThreads) k_xb_tile_count(int Z, ChunkDiv div, int nch,
+                                                                  int nTiles,
+                                                                  const int* __restrict__ colIdx,
+                                                                  int* __restrict__ tileCnt) {
+  __shared__ int sCnt[kXbTileChunks];
+  for (int c = threadIdx.x; c < nch; c += kXbTileThreads) sCnt[c] = 0;
+  const long long k0 = (long long)blockIdx.x * kXbTile + (long long)threadIdx.x * kXbTileRounds;
+  int cols[kXbTileRounds];
+  if (VEC && k0 + kXbTileRounds <= Z) {  // 16-byte aligned: tiles start on multiples of 2048
+    const int4 a = ld_stream(reinterpret_cast<const int4*>(colIdx + k0));
+    const int4 b = ld_stream(reinterpret_cast<const int4*>(colIdx + k0) + 1);
+    cols[0] = a.x; cols[1] = a.y; cols[2] = a.z; cols[3] = a.w;
+    cols[4] = b.x; cols[5] = b.y; cols[6] = b.z; cols[7] = b.w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < kXbTileRounds; ++e)
+      cols[e] = k0 + e < Z ? ld_stream(colIdx + k0 + e) : 0;
+  }
+  __syncthreads();
+  int cur = -1, run = 0;
+#pragma unroll
+  for (int e = 0; e < kXbTileRounds; ++e) {
+    const long long k = k0 + e;
+    if (k < Z) {
+      const int c = div(cols[e]);
+      if (c != cur) {
+        if (run) atomicAdd(&sCnt[cur], run);
+        cur = c;
+        run = 0;
+      }
+      ++run;
+    }
+  }
+  if (run) atomicAdd(&sCnt[cur], run);
+  __syncthreads();
+  for (int c = threadIdx.x; c < nch; c += kXbTileThreads)
+    tileCnt[(long long)c * nTiles + blockIdx.x] = sCnt[c];
+}
+
+// One block: cnt[c] from the scanned tile counts (start of chunk c's first
+// tile to the next chunk's), chunkPtr = exclusive scan of cnt rounded up to 4.
+__global__ void __launch_bounds__(kScanThreads) k_xb_chunk_ptr(int Z, int nch, int nTiles,
+                                                               const int* __restrict__ tileOff,
+                                                               int* __restrict__ cnt,
+                                                               int* __restrict__ chunkPtr) {
+  __shared__ int sWarp[kScanThreads / 32 + 1];
+  const int c = threadIdx.x;  // nch <= kXbTileChunks <= kScanThreads
+  int padded = 0;
+  if (c < nch) {
+    const int a = tileOff[(long long)c * nTiles];
+    const int b = c + 1 < nch ? tileOff[(long long)(c + 1) * nTiles] : Z;
+    cnt[c] = b - a;
+    padded = (b - a + 3) & ~3;
+  }
+  int total = 0;
+  const int ex = block_exclusive_scan(padded, &total, sWarp);
+  if (c < nch) chunkPtr[c] = ex;
+  if (c == 0) chunkPtr[nch] = total;
+}
+
+// Row of nonzero k from its chunk record: lo plus the row starts at or
+// before k's position (a binary search on rowPtrs in a chunk that holds an
+// empty row).
+__device__ __forceinline__ int xb_row_of(const CsrChunkDesc& d, long long k,
+                                         const int* __restrict__ rowPtrs) {
+  if (!(d.flags & kCsrChunkHasEmptyRow)) {
+    const int pos = (int)(k & (kCsrChunk - 1));
+    const int wd = pos >> 5;
+    const unsigned mw = wd == 0 ? d.mask.x : wd == 1 ? d.mask.y : wd == 2 ? d.mask.z : d.mask.w;
+    const int before = (wd > 0 ? __popc(d.mask.x) : 0) + (wd > 1 ? __popc(d.mask.y) : 0) +
+                       (wd > 2 ? __popc(d.mask.z) : 0);
+    return d.lo + before + __popc(mw & ((2u << (pos & 31)) - 1u));
+  }
+  int r = d.lo, b = d.hi;
+  while (r < b) {
+    const int m = (r + b + 1) >> 1;
+    if (__ldg(rowPtrs + m) <= k) r = m; else b = m - 1;
+  }
+  return r;
+}
+
+// Lanes of the warp holding the same value v < 2^nbits (nbits warp-uniform).
+// BALLOTS: one ballot per bit of v; otherwise __match_any_sync. The launch
+// takes ballots for scattered columns (many chunks among 32 consecutive
+// entries), the match otherwise. Measured on the tile scatter: skewed rows
+// 459 us with the match (ncu: its pipe at 75 % of peak, DRAM at 17 %) and
+// 393 us with ballots; 27-point stencil (one or two chunks per 32 entries)
+// 952 us with the match and 1291 us with ballots. Choosing per 32 entries
+// (by the number of value changes between neighbouring lanes) cost more than
+// it saved: 420 and 1030 us.
+template <bool BALLOTS>
+__device__ __forceinline__ unsigned warp_peers(unsigned v, int nbits) {
+  if (!BALLOTS) return __match_any_sync(kFullMask, v);
+  unsigned peers = kFullMask;
+  for (int b = 0; b < nbits; ++b) {
+    const unsigned bit = (v >> b) & 1u;
+    const unsigned bal = __ballot_sync(kFullMask, bit);
+    peers &= bit ? bal : ~bal;
+  }
+  return peers;
+}
+
+template <class T, bool BALLOTS>
+__global__ void __launch_bounds__(kXbTileThreads, 6) k_xb_tile_scatter(
+    int Z, ChunkDiv div, int nch, int nTiles, const int* __restrict__ rowPtrs,
+    const CsrChunkDesc* __restrict__ desc, const int* __restrict__ colIdx,
+    const T* __restrict__ value, const int* __restrict__ tileOff,
+    const int* __restrict__ chunkPtr, int* __restrict__ xbRow, unsigned short* __restrict__ xbCol,
+    T* __restrict__ xbVal) {
+  constexpr int kWarps = kXbTileThreads / 32;
+  constexpr int kPerWarp = kXbTile / kWarps;  // 32 * kXbTileRounds
+  __shared__ int sCur[kWarps][kXbTileChunks];  // counts, then running positions in the tile
+  __shared__ int sBase[kXbTileChunks];         // output position of the tile's first entry of c
+  __shared__ int sRow[kXbTile];
+  __shared__ T sVal[kXbTile];
+  __shared__ unsigned short sLoc[kXbTile];
+  __shared__ unsigned char sChk[kXbTile];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  for (int c = lane; c < nch; c += 32) sCur[w][c] = 0;
+  // output start of this tile's entries of chunk threadIdx.x, loaded while
+  // the entries load
+  int outBase = 0;
+  if ((int)threadIdx.x < nch) {
+    const long long row0 = (long long)threadIdx.x * nTiles;
+    outBase = __ldg(chunkPtr + threadIdx.x) + (__ldg(tileOff + row0 + blockIdx.x) -
+                                               __ldg(tileOff + row0));
+  }
+  const long long tileBase = (long long)blockIdx.x * kXbTile;
+  const long long wbase = tileBase + (long long)w * kPerWarp;
+  int chk[kXbTileRounds], row[kXbTileRounds], loc[kXbTileRounds];
+  T val[kXbTileRounds];
+#pragma unroll
+  for (int rd = 0; rd < kXbTileRounds; ++rd) {
+    const long long k = wbase + rd * 32 + lane;
+    chk[rd] = nch;  // no entry: a value no chunk takes
+    row[rd] = 0;
+    loc[rd] = 0;
+    val[rd] = T(0);
+    if (k < Z) {
+      const int col = __ldcs(colIdx + k);
+      val[rd] = __ldcs(value + k);
+      const int c = div(col);
+      chk[rd] = c;
+      loc[rd] = col - c * div.b;
+      row[rd] = xb_row_of(desc[k >> 7], k, rowPtrs);  // 32 lanes, one record
+    }
+  }
+  __syncwarp();
+  const int nbits = 32 - __clz(nch);  // bits of the values 0 .. nch
+#pragma unroll
+  for (int rd = 0; rd < kXbTileRounds; ++rd) {
+    const unsigned peers = warp_peers<BALLOTS>((unsigned)chk[rd], nbits);
+    if (chk[rd] < nch && lane == __ffs(peers) - 1) sCur[w][chk[rd]] += __popc(peers);
+    __syncwarp();
+  }
+  __syncthreads();
+  // tile-local starts of the chunks (scan over the chunks of the tile's
+  // counts), each warp's start inside its chunk, and the output position of
+  // the tile's first entry of each chunk
+  __shared__ int sWarp[kScanThreads / 32 + 1];
+  {
+    const int c = threadIdx.x;  // nch <= kXbTileChunks <= kXbTileThreads
+    int tot = 0;
+    if (c < nch)
+#pragma unroll
+      for (int q = 0; q < kWarps; ++q) tot += sCur[q][c];
+    int all = 0;
+    const int lstart = block_exclusive_scan(tot, &all, sWarp);
+    if (c < nch) {
+      int run = lstart;
+#pragma unroll
+      for (int q = 0; q < kWarps; ++q) {
+        const int cntq = sCur[q][c];
+        sCur[q][c] = run;
+        run += cntq;
+      }
+      sBase[c] = outBase - lstart;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int rd = 0; rd < kXbTileRounds; ++rd) {
+    const int c = chk[rd];
+    const unsigned peers = warp_peers<BALLOTS>((unsigned)c, nbits);
+    const bool valid = c < nch;
+    const int start = valid ? sCur[w][c] : 0;
+    __syncwarp();
+    if (valid) {
+      const int q = start + __popc(peers & lanemask_lt());
+      sRow[q] = row[rd];
+      sVal[q] = val[rd];
+      sLoc[q] = (unsigned short)loc[rd];
+      sChk[q] = (unsigned char)c;
+      if (lane == __ffs(peers) - 1) sCur[w][c] = start + __popc(peers);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  // out: the tile's entries in chunk order; a chunk's entries are
+  // consecutive here and in the output
+  const int n = (int)(Z - tileBase < kXbTile ? Z - tileBase : kXbTile);
+  for (int q = threadIdx.x; q < n; q += kXbTileThreads) {
+    const long long p = (long long)sBase[sChk[q]] + q;
+    __stcs(xbRow + p, sRow[q]);
+    __stcs(xbCol + p, sLoc[q]);
+    __stcs(xbVal + p, sVal[q]);
+  }
+}
+
 size_t xb_scratch_bytes(int Z, int nch) {
+  if (nch <= kXbTileChunks) {
+    // cnt[nch], tileCnt[nch * nTiles + 1], scan scratch for it
+    const long long nTiles = ((long long)Z + kXbTile - 1) / kXbTile;
+    const long long n = (long long)nch * (nTiles > 0 ? nTiles : 1);
+    return sizeof(int) * (size_t)(nch + n + 1 + (long long)scan_scratch_ints(n) + 16);
+  }
   // cnt[nch], ustart[nch + 1], scan scratch for nch, the sort's item order
   // perm[Z], then the radix sort's own scratch for Z items
   const size_t ints = 2 * (size_t)nch + 1 + (size_t)scan_scratch_ints(nch) + (size_t)Z;
@@ -1169,10 +1422,42 @@ size_t xb_scratch_bytes(int Z, int nch) {
 }
 
 template <class T>
-cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* value,
-                            const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
-                            T* xbVal, void* scratch, cudaStream_t s) {
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* rowPtrs, const CsrChunkDesc* desc,
+                            const int* colIdx, const T* value, const int* rowIdx, bool scattered,
+                            int* chunkPtr, int* xbRow, unsigned short* xbCol, T* xbVal,
+                            void* scratch, cudaStream_t s) {
   if (nch <= 0) return cudaMemsetAsync(chunkPtr, 0, sizeof(int), s);
+  if (nch <= kXbTileChunks && Z > 0) {
+    const long long nTiles = ((long long)Z + kXbTile - 1) / kXbTile;
+    const long long n = (long long)nch * nTiles;
+    int* cnt = static_cast<int*>(scratch);
+    int* tileCnt = cnt + nch;
+    int* scanScratch = tileCnt + n + 1;
+    const ChunkDiv div = chunk_div(B);
+    if (aligned16(colIdx))
+      k_xb_tile_count<true><<<(unsigned)nTiles, kXbTileThreads, 0, s>>>(Z, div, nch, (int)nTiles,
+                                                                        colIdx, tileCnt);
+    else
+      k_xb_tile_count<false><<<(unsigned)nTiles, kXbTileThreads, 0, s>>>(Z, div, nch,
+                                                                         (int)nTiles, colIdx,
+                                                                         tileCnt);
+    note_launches(1);
+    cudaError_t err = exclusive_scan(ArrayIn{tileCnt}, n, tileCnt, scanScratch, s);
+    if (err != cudaSuccess) return err;
+    k_xb_chunk_ptr<<<1, kScanThreads, 0, s>>>(Z, nch, (int)nTiles, tileCnt, cnt, chunkPtr);
+    if (scattered)
+      k_xb_tile_scatter<T, true><<<(unsigned)nTiles, kXbTileThreads, 0, s>>>(
+          Z, div, nch, (int)nTiles, rowPtrs, desc, colIdx, value, tileCnt, chunkPtr, xbRow,
+          xbCol, xbVal);
+    else
+      k_xb_tile_scatter<T, false><<<(unsigned)nTiles, kXbTileThreads, 0, s>>>(
+          Z, div, nch, (int)nTiles, rowPtrs, desc, colIdx, value, tileCnt, chunkPtr, xbRow,
+          xbCol, xbVal);
+    k_xb_pad<T><<<(unsigned)((nch + 255) / 256), 256, 0, s>>>(nch, cnt, chunkPtr, xbRow, xbCol,
+                                                             xbVal);
+    note_launches(3);
+    return cudaGetLastError();
+  }
   int* cnt = static_cast<int*>(scratch);
   int* ustart = cnt + nch;
   int* scanScratch = ustart + nch + 1;
@@ -1223,8 +1508,9 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* v
   template cudaError_t launch_sell_scatter<T>(int, int, const int*, const int*, const T*,       \
                                               const void*, const int*, int, int*, T*,            \
                                               cudaStream_t);                                     \
-  template cudaError_t launch_xb_build<T>(int, int, int, const int*, const T*, const int*, int*, \
-                                          int*, unsigned short*, T*, void*, cudaStream_t);
+  template cudaError_t launch_xb_build<T>(int, int, int, const int*, const CsrChunkDesc*,       \
+                                          const int*, const T*, const int*, bool, int*, int*,   \
+                                          unsigned short*, T*, void*, cudaStream_t);
 SPMV_INSTANTIATE(float)
 SPMV_INSTANTIATE(double)
 #undef SPMV_INSTANTIATE

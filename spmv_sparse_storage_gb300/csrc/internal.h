@@ -160,11 +160,17 @@ cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
 constexpr int kXbSmemBytes = 196608;    // x staged per CTA: 192 KiB
 constexpr int kXbDefaultChunk = 49152;  // columns per chunk with 4-byte values (24576 with 8)
 constexpr int kXbMaxChunks = 65536;     // chunk ids sorted in at most two radix passes
+// up to this many chunks the build sorts tiles of nonzeros by chunk in shared
+// memory and decodes rows from the CSR chunk records (rowIdx unused;
+// scattered: the columns are scattered, many chunks among 32 consecutive
+// nonzeros); more chunks take a radix sort of all nonzeros and need rowIdx
+constexpr int kXbTileChunks = 256;
 size_t xb_scratch_bytes(int Z, int nch);
 template <class T>
-cudaError_t launch_xb_build(int Z, int B, int nch, const int* colIdx, const T* value,
-                            const int* rowIdx, int* chunkPtr, int* xbRow, unsigned short* xbCol,
-                            T* xbVal, void* scratch, cudaStream_t s);
+cudaError_t launch_xb_build(int Z, int B, int nch, const int* rowPtrs, const CsrChunkDesc* desc,
+                            const int* colIdx, const T* value, const int* rowIdx, bool scattered,
+                            int* chunkPtr, int* xbRow, unsigned short* xbCol, T* xbVal,
+                            void* scratch, cudaStream_t s);
 template <class T>
 cudaError_t launch_spmv_xb(int C, int B, int nch, const int* chunkPtr, const int* xbRow,
                            const unsigned short* xbCol, const T* xbVal, const T* x,

@@ -499,12 +499,15 @@ def test_csr_large_ragged(sp, orc):
 def test_xblock_chunkings(sp, orc):
     """Chunk widths that are and are not multiples of 4 (x staged with 16-byte
     or scalar loads), numCols not a multiple of B, empty chunks, rows spread
-    over many chunks and CTAs; converted without a COO conversion first (rows
-    expanded on the fly) and after it (the COO row array reused)."""
+    over many chunks and CTAs. Up to 256 chunks the build sorts tiles of
+    nonzeros in shared memory and decodes rows from the CSR chunk records (B
+    = 274: 256 chunks); more chunks take the radix sort of all nonzeros (B =
+    273: 257 chunks), converted without a COO conversion first (rows
+    expanded) and after it (the COO row array reused)."""
     inp = synth.random_csr(51, 20_011, 70_001, mean_len=9, empty_frac=0.05, long_rows=5,
                            long_len=3000, name="xb_scatter")
-    check_matrix(sp, orc, inp, formats=("XBLOCK",), xb_chunks=(0, 1, 3, 16, 1001, 4096,
-                                                               49152))
+    check_matrix(sp, orc, inp, formats=("XBLOCK",), xb_chunks=(0, 1, 3, 16, 273, 274, 1001,
+                                                               4096, 49152))
     check_matrix(sp, orc, inp, formats=("COO", "XBLOCK"), xb_chunks=(5, 777))
     # columns only in a few chunks: the others are empty
     band = synth.random_csr(52, 3000, 60_000, mean_len=4, name="xb_narrow")
