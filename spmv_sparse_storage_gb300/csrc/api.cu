@@ -717,7 +717,8 @@ int spmv_convert_sell(spmv_handle h, int32_t sectionRows, void* stream) {
   if (st == SPMV_OK && slots > 0)
     st = record(with_type(h, [&](auto tag) {
       using T = decltype(tag);
-      return spmv::launch_sell_scatter<T>(h->R, S, h->rowPtrs, h->colIdx, cval<T>(h->value),
+      return spmv::launch_sell_scatter<T>(h->R, S, (int)h->stats.max_len, h->rowPtrs,
+                                          h->colIdx, cval<T>(h->value),
                                           scratch, h->sellSecPtr, (int)slots, h->sellCol,
                                           val<T>(h->sellVal), s);
     }));

@@ -1074,12 +1074,79 @@ __global__ void __launch_bounds__(256) k_sell_scatter(int R, int S, const int* _
   }
 }
 
+// Warp-staged form for a longest row of kStageMinK to kStageMaxK entries
+// (every section at most that wide, below kJdsCoop: no cooperative part): a
+// warp's 32 consecutive original rows are one contiguous CSR range, copied
+// into its shared memory with asynchronous 16-byte copies
+// (warp_stage_entries), then each lane writes its row's slots from there, as
+// k_csr_to_ell_staged does. A warp whose rows hold more than 32 * K entries
+// reads directly.
+template <class T, bool VEC>
+__global__ void __launch_bounds__(32 * kStageWarps) k_sell_scatter_staged(
+    int R, int S, int K, const int* __restrict__ rowPtrs, const int* __restrict__ colIdx,
+    const T* __restrict__ value, const int* __restrict__ inv, const int* __restrict__ secPtr,
+    int cap, int* __restrict__ sellCol, T* __restrict__ sellVal) {
+  extern __shared__ int4 sRaw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bufCap = 32 * K + 8;  // a multiple of 4: every warp's buffers start 16-byte aligned
+  int* sCol = reinterpret_cast<int*>(sRaw) + warp * bufCap;
+  T* sVal = reinterpret_cast<T*>(reinterpret_cast<int*>(sRaw) + kStageWarps * bufCap) +
+            warp * bufCap;
+  const long long r = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long w0 = r - lane;  // the warp's first row
+  if (w0 >= R) return;            // warp-uniform
+  const long long wEnd = w0 + 32 < R ? w0 + 32 : R;
+  const int a0 = __ldg(rowPtrs + w0);
+  const int a1 = __ldg(rowPtrs + wEnd);
+  int a = 0, len = 0, w = 0, h = 1, j = 0, base = 0;
+  if (r < R) {
+    a = __ldg(rowPtrs + r);
+    len = __ldg(rowPtrs + r + 1) - a;
+    const int sidx = inv[r];
+    const int k = sidx / S;
+    j = sidx - k * S;
+    h = min(S, R - k * S);
+    base = secPtr[k];
+    const int end = secPtr[k + 1];
+    w = end <= cap ? (end - base) / h : 0;  // offsets past the arrays: write nothing
+  }
+  const bool staged = (long long)a1 - a0 <= 32LL * K;  // warp-uniform
+  if (staged) warp_stage_entries<T, VEC>(colIdx, value, a0, a1, lane, sCol, sVal);
+  __syncwarp();
+  if (r >= R) return;
+  const int off = (int)(a - (a0 & ~3LL));
+  for (int t = 0; t < w; ++t) {
+    const long long o = (long long)base + (long long)t * h + j;
+    int c = -1;
+    T v = T(0);
+    if (t < len) {
+      c = staged ? sCol[off + t] : colIdx[a + t];
+      v = staged ? sVal[off + t] : value[a + t];
+    }
+    sellCol[o] = c;
+    sellVal[o] = v;
+  }
+}
+
 template <class T>
-cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
+cudaError_t launch_sell_scatter(int R, int S, int maxLen, const int* rowPtrs, const int* colIdx,
                                 const T* value, const void* scratch, const int* secPtr,
                                 int slots, int* sellCol, T* sellVal, cudaStream_t s) {
   if (R <= 0) return cudaSuccess;
   const int* inv = static_cast<const int*>(scratch) + 3LL * R;  // row_sort's layout
+  if (maxLen >= kStageMinK && maxLen <= kStageMaxK<T>) {
+    constexpr int threads = 32 * kStageWarps;
+    const unsigned blocks = (unsigned)(((long long)R + threads - 1) / threads);
+    const size_t smem = warp_stage_smem<T>(maxLen);
+    if (aligned16(colIdx) && aligned16(value))
+      k_sell_scatter_staged<T, true><<<blocks, threads, smem, s>>>(
+          R, S, maxLen, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
+    else
+      k_sell_scatter_staged<T, false><<<blocks, threads, smem, s>>>(
+          R, S, maxLen, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
+    note_launches(1);
+    return cudaGetLastError();
+  }
   k_sell_scatter<T><<<(unsigned)(((long long)R + 255) / 256), 256, 0, s>>>(
       R, S, rowPtrs, colIdx, value, inv, secPtr, slots, sellCol, sellVal);
   note_launches(1);
@@ -1505,7 +1572,7 @@ cudaError_t launch_xb_build(int Z, int B, int nch, const int* rowPtrs, const Csr
   template cudaError_t launch_jds_build<T>(int, int, int, const int*, const int*, const T*,     \
                                            int*, int*, int*, T*, void*, const int*,              \
                                            cudaStream_t);                                        \
-  template cudaError_t launch_sell_scatter<T>(int, int, const int*, const int*, const T*,       \
+  template cudaError_t launch_sell_scatter<T>(int, int, int, const int*, const int*, const T*,  \
                                               const void*, const int*, int, int*, T*,            \
                                               cudaStream_t);                                     \
   template cudaError_t launch_xb_build<T>(int, int, int, const int*, const CsrChunkDesc*,       \

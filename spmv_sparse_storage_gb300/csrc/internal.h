@@ -136,8 +136,9 @@ cudaError_t launch_sell_sort(int R, int maxLen, const int* rowPtrs, int* perm, v
                              cudaStream_t s);
 cudaError_t launch_sell_widths(int R, int S, int nsec, const int* rowPtrs, const int* perm,
                                int* widths, cudaStream_t s);
+// maxLen: the longest row (rows of kStageMinK to kStageMaxK entries are staged)
 template <class T>
-cudaError_t launch_sell_scatter(int R, int S, const int* rowPtrs, const int* colIdx,
+cudaError_t launch_sell_scatter(int R, int S, int maxLen, const int* rowPtrs, const int* colIdx,
                                 const T* value, const void* scratch, const int* secPtr,
                                 int slots, int* sellCol, T* sellVal, cudaStream_t s);
 

@@ -213,8 +213,8 @@ def test_type_errors(sp, orc):
 
 def test_warp_staged_width_24(sp, orc):
     """8-byte values with rows of 12-24 entries: the ELL, HYB (automatic
-    width) and JDS conversions take the warp-staged scatters (two 16-byte
-    copies per 4 values)."""
+    width), JDS and SELL conversions take the warp-staged scatters (two
+    16-byte copies per 4 values)."""
     rng = np.random.default_rng(77)
     R, C = 3001, 2500
     lens = rng.integers(12, 25, R).astype(np.int64)
@@ -224,4 +224,4 @@ def test_warp_staged_width_24(sp, orc):
     val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
     inp = synth.CSRInput("wide24", R, C, rp, cols, val, np.zeros(C, np.float32),
                          np.zeros(R, np.float32))
-    check_f64(sp, orc, inp, formats=("ELL", "HYB", "JDS"))
+    check_f64(sp, orc, inp, formats=("ELL", "HYB", "JDS", "SELL"))

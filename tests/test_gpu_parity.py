@@ -682,8 +682,9 @@ def wide_rows(seed, num_rows, num_cols, lo, hi, name):
 @pytest.mark.parametrize("kind", ["random", "runs"])
 def test_warp_staged_row_scatters(sp, orc, offset, kind):
     """Rows of 17-32 entries take the warp-staged scatters: ELL (width 32),
-    JDS (longest row 32), and HYB at widths 24 and 28, where the warps whose
-    rows hold more entries than their buffer read directly. Aligned arrays
+    JDS and SELL (longest row 32; SELL with sections of 1, 7 and 128 rows),
+    and HYB at widths 24 and 28, where the warps whose rows hold more entries
+    than their buffer read directly. Aligned arrays
     stage by 16-byte asynchronous copies, misaligned views entry by entry; the
     last warp is ragged (5003 rows). "runs": rows of 27 entries with one of
     24 every 50 rows, so that after the length sort most warps of the JDS
@@ -700,4 +701,5 @@ def test_warp_staged_row_scatters(sp, orc, offset, kind):
         val = rng.uniform(-1.0, 1.0, cols.size).astype(np.float32)
         inp = synth.CSRInput(f"runs{offset}", inp.num_rows, inp.num_cols, rp, cols, val,
                              inp.x, inp.y0)
-    check_matrix(sp, orc, inp, formats=("ELL", "HYB", "JDS"), hyb_widths=(24, 28), offset=offset)
+    check_matrix(sp, orc, inp, formats=("ELL", "HYB", "JDS", "SELL"), hyb_widths=(24, 28),
+                 sell_rows=(1, 7, 128), offset=offset)
