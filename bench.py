@@ -134,6 +134,24 @@ def call_bytes(name, R, C, Z, K_ell, K_hyb, hyb_tail):
     }[name]
 
 
+def convert_bytes(fmt, R, C, Z, vb=4, width=0, tail=0, slots=0):
+    """Algorithmic bytes of converting CSR to `fmt` with vb-byte values: what
+    the conversion must read from CSR and write (width: ELL/HYB slots per
+    row; tail: HYB's COO entries; slots: SELL/XBLOCK stored entries, padding
+    included)."""
+    rp = 4 * (R + 1)
+    return {
+        "COO": rp + 4 * Z,                                       # rowIdx written
+        "ELL": rp + (4 + vb) * Z + (4 + vb) * R * width + 4 * R,  # + nnzPerRow
+        "HYB": rp + (4 + vb) * Z + (4 + vb) * R * width + 4 * R + (8 + vb) * tail,
+        "JDS": rp + 4 * R + 2 * (4 + vb) * Z,                     # perm, entries moved
+        "SELL": rp + 4 * R + (4 + vb) * Z + (4 + vb) * slots,
+        # columns read twice (count, scatter), values once; row, 16-bit
+        # column and value written per slot
+        "XBLOCK": 4 * Z + (4 + vb) * Z + (6 + vb) * slots,
+    }[fmt]
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 100 ms while running."""
 
@@ -459,7 +477,10 @@ def run_kernels(args, device):
     """Per-format SpMV timing on one workload: each rep resets y to y0 and
     flushes L2 (L2Flush) outside the timed events, then times one spmv_run
     with CUDA events on the launching stream; median over reps. Warm-L2 times
-    (the same runs back to back without the flush) are reported apart."""
+    (the same runs back to back without the flush) are reported apart. Each
+    format's conversion from CSR: after one untimed conversion, the median of
+    --convert-reps conversions, each after an L2 flush, against the
+    conversion's algorithmic bytes (convert_bytes)."""
     import torch
     import spmv_sparse_storage_gb300 as sp
     inp = synth.make_workload(args.workload, seed=0)
@@ -480,16 +501,21 @@ def run_kernels(args, device):
         fmts = [f for f in args.formats.split(",") if f]
         conv_us = {}
         for f in fmts:
+            if f == "CSR":
+                continue
             try:
                 m.convert(f, stream=stream, chunk_cols=args.chunk_cols)  # warm (pool, launches)
-                flush()
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                m.convert(f, stream=stream, chunk_cols=args.chunk_cols)
-                e1.record(stream)
-                e1.synchronize()
-                conv_us[f] = round(e0.elapsed_time(e1) * 1e3, 2)
+                ts = []
+                for _ in range(args.convert_reps):
+                    flush()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    m.convert(f, stream=stream, chunk_cols=args.chunk_cols)
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+                conv_us[f] = round(statistics.median(ts), 2)
             except sp.SpmvError as e:
                 out[f] = {"error": str(e)}
         torch.cuda.synchronize(device)
@@ -510,6 +536,13 @@ def run_kernels(args, device):
                 out[f]["fp64_frac_nominal"] = round(gflops / FP64_NOMINAL_GFLOPS, 4)
             if f in ("ELL", "HYB", "SELL", "XBLOCK"):
                 out[f]["slots"] = sp.spmv_export(m.handle, f)["ell_slots"]
+            if f in conv_us:
+                ex = sp.spmv_export(m.handle, f)
+                cb = convert_bytes(f, R, C, Z, vb, width=ex.get("width", 0),
+                                   tail=ex.get("coo_nnz", 0), slots=ex.get("ell_slots", 0))
+                cgbs = cb / (conv_us[f] * 1e-6) / 1e9
+                out[f].update({"convert_alg_bytes": cb, "convert_GB/s": round(cgbs, 1),
+                               "convert_frac": round(cgbs / peak, 4)})
         sel = m.select()
     line = {"mode": "kernels", "workload": args.workload, "dtype": args.dtype, "rows": R,
             "nnz": Z,
@@ -835,6 +868,9 @@ def main():
                     help="XBLOCK chunk width B (0: the library default)")
     ap.add_argument("--formats", default="CSR,COO,ELL,HYB,JDS,SELL,XBLOCK")
     ap.add_argument("--reps", type=int, default=50)
+    ap.add_argument("--convert-reps", type=int, default=5,
+                    help="--mode kernels: conversions timed per format (median; L2 flushed "
+                         "before each)")
     ap.add_argument("--no-per-config", action="store_true",
                     help="step mode: skip the per-format table of the five workloads")
     ap.add_argument("--config-reps", type=int, default=10)

@@ -39,6 +39,24 @@ def test_call_bytes_laplace2d():
         assert cb("spmv_" + f) == 234_815_488
 
 
+def test_convert_bytes_agree_with_the_step_calls():
+    """The per-format conversion bytes of --mode kernels: the step's own
+    figures for COO, ELL, HYB and JDS with 4-byte values, and the arrays
+    each format reads and writes by hand for SELL and XBLOCK."""
+    R, C, Z, K, tail = 1000, 900, 7000, 9, 55
+    for f, name in (("COO", "convert_coo"), ("ELL", "convert_ell"), ("JDS", "convert_jds")):
+        assert bench.convert_bytes(f, R, C, Z, 4, width=K) == \
+            bench.call_bytes(name, R, C, Z, K, K, 0)
+    assert bench.convert_bytes("HYB", R, C, Z, 4, width=K, tail=tail) == \
+        bench.call_bytes("convert_hyb", R, C, Z, K, K, tail)
+    slots = 7300
+    # SELL: rowPtrs, perm, CSR entries read, column + value per slot written
+    assert bench.convert_bytes("SELL", R, C, Z, 8, slots=slots) == \
+        4 * (R + 1) + 4 * R + 12 * Z + 12 * slots
+    # XBLOCK: columns twice, values once; row + 16-bit column + value per slot
+    assert bench.convert_bytes("XBLOCK", R, C, Z, 4, slots=slots) == 4 * Z + 8 * Z + 10 * slots
+
+
 def test_traffic_record_follows_its_source(tmp_path, monkeypatch):
     src = tmp_path / "kernel.cu"
     src.write_text("// kernel source\n")
