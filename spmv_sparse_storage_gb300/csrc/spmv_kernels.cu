@@ -494,10 +494,11 @@ __global__ void __launch_bounds__(256) k_spmv_coo(int Z, const int* __restrict__
 // s < width(t), contiguous in s, so a warp's loads are coalesced. Widths only
 // shrink with t; the first tSplit diagonals (those at least
 // kJdsSplitMinWidth wide, at most kJdsSplitMaxDiag of them) run one thread
-// per sorted row: a warp's 32 rows of a diagonal are 32 consecutive entries,
-// so 4-byte loads are coalesced wherever the diagonal starts, and a thread
-// loads kJdsGroup<T> diagonals before it gathers any x. (4 rows per thread with
-// 16-byte loads needed a shuffle realignment per diagonal and 64 registers.)
+// per sorted row (two with 4-byte values: rows 32 apart): a warp's 32 rows of
+// a diagonal are 32 consecutive entries, so 4-byte loads are coalesced
+// wherever the diagonal starts, and a thread loads a group of diagonals
+// before it gathers any x. (4 consecutive rows per thread with 16-byte loads
+// needed a shuffle realignment per diagonal and 64 registers.)
 // The remaining diagonals belong to the few
 // longest rows (s < wTail) and would serialise one thread over thousands of
 // entries, so they are split into blocks of kJdsTailRows rows x
@@ -524,7 +525,13 @@ constexpr int kJdsGroup = sizeof(T) == 4 ? 8 : 5;
 struct JdsIterPtrs {
   int v[kJdsParamDiags + 1];
 };
-template <class T, bool PARAM>
+// RPT sorted rows per thread: rows warpBase + 32 j + lane, j < RPT, so that
+// every load of a warp is still 32 consecutive entries of a diagonal and a
+// thread keeps RPT rows' loads in flight. Diagonals are loaded
+// kJdsRowGroup<T, RPT> at a time.
+template <class T, int RPT>
+constexpr int kJdsRowGroup = RPT == 1 ? kJdsGroup<T> : 4;
+template <class T, bool PARAM, int RPT>
 __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit, int wTail,
                                                      int nMainBlocks, int tailRowBlocks,
                                                      const int* __restrict__ iterPtr,
@@ -541,42 +548,60 @@ __global__ void __launch_bounds__(256) k_spmv_jds(int R, int maxLen, int tSplit,
       for (int t = threadIdx.x; t <= tSplit; t += blockDim.x) sIpBuf[t] = iterPtr[t];
       __syncthreads();
     }
-    const int lane = threadIdx.x & 31;
-    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;  // sorted row
-    const long long warpFirst = s - lane;
-    const int r = s < R ? __ldg(perm + s) : -1;
-    const T y0 = (r >= 0 && s >= wTail) ? y[r] : T(0);
-    T acc = T(0);
-    // kJdsGroup<T> diagonals at a time: all their column and value loads are
-    // issued before the gathers, and all gathers before the multiply-adds
-    for (int t0 = 0; t0 < tSplit; t0 += kJdsGroup<T>) {
-      if (warpFirst >= sIp[t0 + 1] - sIp[t0]) break;  // widths shrink
-      int c[kJdsGroup<T>];
-      T v[kJdsGroup<T>];
+    constexpr int G = kJdsRowGroup<T, RPT>;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long warpFirst =
+        ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * (32LL * RPT);  // sorted row
+    long long s[RPT];
+    int r[RPT];
+    T y0[RPT], acc[RPT];
 #pragma unroll
-      for (int g = 0; g < kJdsGroup<T>; ++g) {
+    for (int j = 0; j < RPT; ++j) {
+      s[j] = warpFirst + 32 * j + lane;
+      r[j] = s[j] < R ? __ldg(perm + s[j]) : -1;
+      acc[j] = T(0);
+    }
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) y0[j] = (r[j] >= 0 && s[j] >= wTail) ? y[r[j]] : T(0);
+    // G diagonals at a time: all their column and value loads are issued
+    // before the gathers, and all gathers before the multiply-adds
+    for (int t0 = 0; t0 < tSplit; t0 += G) {
+      if (warpFirst >= sIp[t0 + 1] - sIp[t0]) break;  // widths shrink
+      int c[RPT][G];
+      T v[RPT][G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
         const int t = t0 + g;
-        c[g] = -1;
-        v[g] = T(0);
-        if (t < tSplit) {
-          const int a = sIp[t];
-          if (s < sIp[t + 1] - a) {
-            c[g] = ld_stream(jdsCol + a + s);
-            v[g] = ld_stream(jdsVal + a + s);
+        const int a = t < tSplit ? sIp[t] : 0;
+        const int wd = t < tSplit ? sIp[t + 1] - a : 0;
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+          c[j][g] = -1;
+          v[j][g] = T(0);
+          if (s[j] < wd) {
+            c[j][g] = ld_stream(jdsCol + a + s[j]);
+            v[j][g] = ld_stream(jdsVal + a + s[j]);
           }
         }
       }
-      T xg[kJdsGroup<T>];
+      T xg[RPT][G];
 #pragma unroll
-      for (int g = 0; g < kJdsGroup<T>; ++g) xg[g] = c[g] >= 0 ? ld_x(x + c[g]) : T(0);
+      for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int g = 0; g < kJdsGroup<T>; ++g) acc = fma_t(v[g], xg[g], acc);
+        for (int j = 0; j < RPT; ++j) xg[j][g] = c[j][g] >= 0 ? ld_x(x + c[j][g]) : T(0);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) acc[j] = fma_t(v[j][g], xg[j][g], acc[j]);
     }
-    if (r >= 0) {
-      if (s < wTail)
-        atomicAdd(y + r, acc);  // the tail blocks add to this row too
-      else
-        y[r] = y0 + acc;
+#pragma unroll
+    for (int j = 0; j < RPT; ++j) {
+      if (r[j] >= 0) {
+        if (s[j] < wTail)
+          atomicAdd(y + r[j], acc[j]);  // the tail blocks add to this row too
+        else
+          y[r[j]] = y0[j] + acc[j];
+      }
     }
   } else {
     // a tile of kJdsTailRows rows x kJdsTailDiags diagonals, walked by the
@@ -704,13 +729,22 @@ cudaError_t launch_spmv_ell(int R, int K, const int* ellCol, const T* ellVal,
   return cudaGetLastError();
 }
 
+// sorted rows per thread of the JDS kernel's main part: 2 with 4-byte values
+// (cold L2: 27-point stencil 147.1 -> 143.4 us against 1, the 5-point
+// Laplacian unchanged at 43.0 us; 4 rows took 64 registers and measured
+// 148.1 and 49.2 us), 1 with 8-byte values (bound by the fp64 adds)
+template <class T>
+constexpr int kJdsRowsPerThread = sizeof(T) == 4 ? 2 : 1;
+
 template <class T>
 cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int* iterPtr,
                             const int* hostIterPtr, const int* perm, const int* jdsCol,
                             const T* jdsVal, const T* x, T* y, cudaStream_t s) {
   if (R <= 0 || maxLen <= 0) return cudaSuccess;
-  // a sorted row per thread
-  const long long mainBlocks = ((long long)R + kJdsBlock - 1) / kJdsBlock;
+  // kJdsRowsPerThread<T> sorted rows per thread
+  constexpr int rpt = kJdsRowsPerThread<T>;
+  const long long mainBlocks = ((long long)R + (long long)kJdsBlock * rpt - 1) /
+                               ((long long)kJdsBlock * rpt);
   long long tailBlocks = 0;
   int tailRowBlocks = 1;
   if (tSplit < maxLen && wTail > 0) {
@@ -724,11 +758,11 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
   const bool param = sizeof(T) == 4 && hostIterPtr != nullptr && tSplit <= kJdsParamDiags;
   for (int t = 0; t <= kJdsParamDiags; ++t) ip.v[t] = param && t <= tSplit ? hostIterPtr[t] : 0;
   if (param)
-    k_spmv_jds<T, true><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
+    k_spmv_jds<T, true, rpt><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
         R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, ip, perm, jdsCol,
         jdsVal, x, y);
   else
-    k_spmv_jds<T, false><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
+    k_spmv_jds<T, false, rpt><<<(unsigned)(mainBlocks + tailBlocks), kJdsBlock, 0, s>>>(
         R, maxLen, tSplit, wTail, (int)mainBlocks, tailRowBlocks, iterPtr, ip, perm, jdsCol,
         jdsVal, x, y);
   note_launches(1);
