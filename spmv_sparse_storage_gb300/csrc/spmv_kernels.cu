@@ -776,7 +776,7 @@ cudaError_t launch_spmv_jds(int R, int maxLen, int tSplit, int wTail, const int*
 // kSellMainSlots slots of every row, either 4 consecutive sorted rows per
 // thread with 16-byte loads (k_spmv_sell4: with S % 4 == 0 every section
 // starts on a multiple of 4 slots, so a full section's 4 rows are one aligned
-// load of columns and one of values per slot) or one row per thread
+// load of columns and one of values per slot) or two rows per thread
 // (k_spmv_sell1), chosen by the mean slots per row. Slots past
 // kSellMainSlots of the wide sections (a prefix, the rows being sorted) are
 // cut into SellItems of 32 rows handled by extra warps, one row per lane; the
@@ -822,6 +822,54 @@ __device__ __forceinline__ T sell_row_slots(const int* __restrict__ col, const T
   return acc;
 }
 
+// Sorted rows per thread of k_spmv_sell1 (two, 32 apart; cold L2 against
+// one: 27-point stencil 152.3 -> 143.4 us, skewed rows 131.7 -> 127.0 us)
+// and their slot groups.
+constexpr int kSell1Rows = 2;
+constexpr int kSell1Group = 4;
+// Slots [0, n[q]) of Q rows (row q: section base[q], height h[q], row j[q]),
+// kSell1Group slots of every row loaded before their gathers.
+template <class T, int Q>
+__device__ __forceinline__ void sell_rows_slots(const int* __restrict__ col,
+                                                const T* __restrict__ val,
+                                                const T* __restrict__ x, const int (&base)[Q],
+                                                const int (&h)[Q], const int (&j)[Q],
+                                                const int (&n)[Q], T (&acc)[Q]) {
+  unsigned o[Q];
+  int nmax = 0;
+#pragma unroll
+  for (int q = 0; q < Q; ++q) {
+    acc[q] = T(0);
+    o[q] = (unsigned)base[q] + (unsigned)j[q];  // unsigned: may wrap past the last slot
+    nmax = max(nmax, n[q]);
+  }
+  for (int tg = 0; tg < nmax; tg += kSell1Group) {
+    int c[Q][kSell1Group];
+    T v[Q][kSell1Group];
+#pragma unroll
+    for (int g = 0; g < kSell1Group; ++g)
+#pragma unroll
+      for (int q = 0; q < Q; ++q) {
+        c[q][g] = -1;
+        v[q][g] = T(0);
+        if (tg + g < n[q]) {
+          c[q][g] = ld_stream(col + o[q]);
+          v[q][g] = ld_stream(val + o[q]);
+        }
+        o[q] += (unsigned)h[q];
+      }
+    T xg[Q][kSell1Group];
+#pragma unroll
+    for (int g = 0; g < kSell1Group; ++g)
+#pragma unroll
+      for (int q = 0; q < Q; ++q) xg[q][g] = c[q][g] >= 0 ? ld_x(x + c[q][g]) : T(0);
+#pragma unroll
+    for (int g = 0; g < kSell1Group; ++g)
+#pragma unroll
+      for (int q = 0; q < Q; ++q) acc[q] = fma_t(v[q][g], xg[q][g], acc[q]);
+  }
+}
+
 // Tail item id (slots [t0, t1) of 32 rows of a wide section, one per lane),
 // added into y atomically.
 template <class T>
@@ -859,23 +907,49 @@ __global__ void __launch_bounds__(256) k_spmv_sell1(int R, int S, int slots, int
                                                    int nItems, const T* __restrict__ x,
                                                    T* __restrict__ y) {
   if ((int)blockIdx.x < mainBlocks) {
-    const long long s = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (s >= R) return;
-    const int k = (int)(s / S);
-    const int k0 = k * S;
-    const int h = min(S, R - k0);
-    // the loads that do not depend on each other first: section bounds, the
-    // row's original index, then its y value
-    const int base = __ldg(secPtr + k);
-    const int end = __ldg(secPtr + k + 1);
-    const int r = __ldg(perm + s);
-    const T y0 = y[r];
-    const int w = end <= slots ? (end - base) / h : 0;  // never past the arrays
-    const T acc = sell_row_slots(col, val, x, base, h, (int)(s - k0), 0, min(w, kSellMainSlots));
-    if (w > kSellMainSlots)
-      atomicAdd(y + r, acc);  // tail items add to this row too
-    else
-      y[r] = y0 + acc;
+    // kSell1Rows sorted rows per thread, 32 apart (a warp's loads stay 32
+    // consecutive slots of one section row)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const long long first =
+        ((long long)blockIdx.x * (blockDim.x >> 5) + warp) * (32LL * kSell1Rows) + lane;
+    int base[kSell1Rows], h[kSell1Rows], j[kSell1Rows], n[kSell1Rows], r[kSell1Rows],
+        w[kSell1Rows];
+    T y0[kSell1Rows];
+#pragma unroll
+    for (int q = 0; q < kSell1Rows; ++q) {
+      const long long s = first + 32LL * q;
+      r[q] = -1;
+      n[q] = 0;
+      w[q] = 0;
+      base[q] = 0;
+      h[q] = 1;
+      j[q] = 0;
+      if (s < R) {
+        const int k = (int)(s / S);
+        const int k0 = k * S;
+        h[q] = min(S, R - k0);
+        j[q] = (int)(s - k0);
+        // the loads that do not depend on each other first: section bounds,
+        // the row's original index, then its y value
+        base[q] = __ldg(secPtr + k);
+        const int end = __ldg(secPtr + k + 1);
+        r[q] = __ldg(perm + s);
+        w[q] = end <= slots ? (end - base[q]) / h[q] : 0;  // never past the arrays
+        n[q] = min(w[q], kSellMainSlots);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kSell1Rows; ++q) y0[q] = r[q] >= 0 ? y[r[q]] : T(0);
+    T acc[kSell1Rows];
+    sell_rows_slots<T, kSell1Rows>(col, val, x, base, h, j, n, acc);
+#pragma unroll
+    for (int q = 0; q < kSell1Rows; ++q) {
+      if (r[q] < 0) continue;
+      if (w[q] > kSellMainSlots)
+        atomicAdd(y + r[q], acc[q]);  // tail items add to this row too
+      else
+        y[r[q]] = y0[q] + acc[q];
+    }
   } else {
     const long long id = (long long)(blockIdx.x - mainBlocks) * (blockDim.x >> 5) +
                          (threadIdx.x >> 5);
@@ -1007,8 +1081,9 @@ cudaError_t launch_spmv_sell(int R, int S, int slots, const int* secPtr, const i
   // 8-byte values keep 4 rows per thread (a row per thread measured 229 us
   // against 223 on the 27-point stencil)
   if (sizeof(T) == 4 && (long long)slots > (long long)kSellRowsWide * R) {
-    // a sorted row per thread
-    const long long mainBlocks = ((long long)R + kSellBlock - 1) / kSellBlock;
+    // kSell1Rows sorted rows per thread
+    constexpr long long rowsPerBlock = (long long)kSellBlock * kSell1Rows;
+    const long long mainBlocks = ((long long)R + rowsPerBlock - 1) / rowsPerBlock;
     k_spmv_sell1<T><<<(unsigned)(mainBlocks + tailBlocks), kSellBlock, 0, s>>>(
         R, S, slots, (int)mainBlocks, secPtr, perm, sellCol, sellVal, items, nItems, x, y);
   } else {
