@@ -256,12 +256,8 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_update(int R, float* __res
                                                              const float* __restrict__ d,
                                                              const float* __restrict__ q,
                                                              float* partials, CgState* st) {
-  grid_dependency_wait();     // the direction, q and alpha of this iteration
-  grid_dependency_trigger();
-  if (!running(st)) return;
-  const float a = (float)st->alpha;
-  float part[1] = {0.f};
   const long long stride = (long long)gridDim.x * blockDim.x;
+  float part[1] = {0.f};
   if (VEC) {
     float4* X4 = reinterpret_cast<float4*>(X);
     float4* g4 = reinterpret_cast<float4*>(g);
@@ -269,13 +265,35 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_update(int R, float* __res
     const float4* q4 = reinterpret_cast<const float4*>(q);
     const long long n4 = R >> 2;
     long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    // two elements per trip so that 8 independent 16-byte loads are in flight
-    for (; i + stride < n4; i += 2 * stride) {
-      float4 x[2], gi[2], di[2], qi[2];
+    // X and g of the first trip load before the wait: the SpMV kernel this
+    // waits for writes only d and q (and reads g), and the update before it
+    // has finished (that kernel waits for it before it lets this one start)
+    float4 x[2], gi[2];
+    bool have = i + stride < n4;
+    if (have) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         x[u] = X4[i + u * stride];
         gi[u] = g4[i + u * stride];
+      }
+    }
+    grid_dependency_wait();  // the direction, q and alpha of this iteration
+    grid_dependency_trigger();
+    if (!running(st)) return;
+    const float a = (float)st->alpha;
+    // two elements per trip so that 8 independent 16-byte loads are in flight
+    for (; i + stride < n4; i += 2 * stride) {
+      float4 di[2], qi[2];
+      if (!have) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          x[u] = X4[i + u * stride];
+          gi[u] = g4[i + u * stride];
+        }
+      }
+      have = false;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
         di[u] = d4[i + u * stride];
         qi[u] = q4[i + u * stride];
       }
@@ -303,6 +321,10 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_update(int R, float* __res
       part[0] = fmaf(gi.x, gi.x, fmaf(gi.y, gi.y, fmaf(gi.z, gi.z, fmaf(gi.w, gi.w, part[0]))));
     }
   } else {
+    grid_dependency_wait();  // the direction, q and alpha of this iteration
+    grid_dependency_trigger();
+    if (!running(st)) return;
+    const float a = (float)st->alpha;
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < R; i += stride) {
       X[i] = fmaf(a, d[i], X[i]);
       const float gi = fmaf(a, q[i], g[i]);
