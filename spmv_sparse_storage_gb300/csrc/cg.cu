@@ -178,6 +178,11 @@ __device__ __forceinline__ float gather_dir(const float* __restrict__ g,
   return dir(b, ld_x(dOld + c), ld_x(g + c));
 }
 
+// Asks L2 to fetch the line holding p (no register, no wait).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ELL path: d_new = -g + beta d_old (own rows, stored), q = A d_new (stored),
 // d_new'q; alpha = g'g / d_new'q. Grid-stride over groups of 4 rows when
 // numRows % 4 == 0 (aligned 16-byte slot loads), else over single rows.
@@ -186,6 +191,18 @@ __global__ void __launch_bounds__(kCgThreads, 4) k_cg_ell_q(
     int R, int K, const int* __restrict__ ellCol, const float* __restrict__ ellVal,
     const float* __restrict__ g, const float* __restrict__ dOld, float* __restrict__ dNew,
     float* __restrict__ q, float* partials, CgState* st) {
+  if (VEC4) {
+    // the first four slot rows of this thread's first rows into L2 before the
+    // wait (the matrix is never written during the solve; no registers held)
+    const long long first = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long ld = R >> 2;
+    if (first < ld) {
+      for (int u = 0; u < 4 && u < K; ++u) {
+        prefetch_l2(reinterpret_cast<const int4*>(ellCol) + (size_t)u * ld + first);
+        prefetch_l2(reinterpret_cast<const float4*>(ellVal) + (size_t)u * ld + first);
+      }
+    }
+  }
   grid_dependency_wait();     // the previous update's g, d and state
   grid_dependency_trigger();  // the next kernel may be scheduled as blocks exit
   if (!running(st)) return;
